@@ -1,0 +1,312 @@
+/*
+ * echo.h -- C ABI of the GB300 (sm_103a) ECHO decode step.
+ *
+ * One layer of a DeepSeek-V3.2-style sparse-attention decode step, as the ECHO
+ * review describes it (marsggbo.github.io, "OSDI'26 | ECHO: sparse attention saves
+ * compute but blows up HBM", section 4 step list):
+ *   indexer score (with the fused lossless prefetch) -> exact top-k ->
+ *   guaranteed recall through the graph-friendly cache manager -> EMA of the k-th
+ *   score, optionally preceded by the write-through append of the new token.
+ *
+ * Conventions for every call:
+ *   - Returns ECHO_OK (0) or a negative-free error code below.  Argument errors are
+ *     detected on the host before anything is enqueued (ECHO_EINVAL); a failing
+ *     CUDA launch gives ECHO_ECUDA.  echo_last_error_string() describes the last
+ *     error of the calling thread.
+ *   - Work is enqueued on the caller's stream (`stream` is a cudaStream_t, NULL =
+ *     the legacy default stream).  No call synchronises, allocates device or host
+ *     memory, or reads device memory on the host, so every call can be captured
+ *     into a CUDA graph (the first call of a process also sets kernel attributes;
+ *     make one call outside capture first).
+ *   - The caller owns all memory.  Device pointers come from cudaMalloc or
+ *     PyTorch; the host KV pool must be pinned and mapped (cudaHostAlloc with
+ *     cudaHostAllocMapped, or any pinned allocation under unified addressing) and is
+ *     passed as its device-accessible pointer; kernels read and write it directly.
+ *   - Outcomes found on the device are OR-ed into the caller's `dev_status` int32
+ *     (device memory) as ECHO_DEV_* bits; the caller clears it and reads it after
+ *     synchronising.
+ *   - "INF" in the residency maps is ECHO_INF (INT32_MAX).
+ */
+#ifndef ECHO_GB300_H
+#define ECHO_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes -------------------------------------------------------- */
+#define ECHO_OK 0
+#define ECHO_EINVAL 1     /* bad argument (size, alignment, pointer kind)     */
+#define ECHO_ECUDA 2      /* a CUDA runtime/driver call failed                */
+#define ECHO_ENOTSUP 3    /* shape outside what the kernels support           */
+
+/* ---- device status bits (OR-ed into *dev_status) ------------------------- */
+#define ECHO_DEV_POOL_EXHAUSTED 1   /* too few evictable slots: rows left out   */
+#define ECHO_DEV_BAD_INDEX 2        /* an index outside its array was skipped   */
+#define ECHO_DEV_WAIT_TIMEOUT 4     /* a pipeline wait gave up (kernel aborted) */
+#define ECHO_DEV_PREFETCH_CAP_HIT 8 /* info: prefetch candidates exceeded the cap */
+
+#define ECHO_INF 0x7fffffff
+#define ECHO_H_INDEX 64      /* indexer heads            */
+#define ECHO_D_INDEX 128     /* indexer head dim (e4m3)  */
+#define ECHO_KV_ELEMS 576    /* latent KV per token: 512 + 64 rope, bf16 */
+#define ECHO_KV_BYTES 1152
+
+/*
+ * One layer's GPU pool and its view of the host pool (section 5.1 metadata table;
+ * GPU pool per layer, host pool per model).  All metadata arrays are device
+ * memory; together they take 4*n_h + 13*n_g bytes (section 5.1 storage law).
+ *   gpu_token_free      [n_g] uint8  GPUTokenFree: 1 = slot free
+ *   gpu_token_priority  [n_g] int32  GPUTokenPriority: eviction clock, -1 when free
+ *   gpu_indices_buffer  [n_g] int32  GPUIndicesBuffer: slots produced by the last
+ *                                    allocate (or evict) call, -1 beyond
+ *   gpu_token_to_host   [n_g] int32  GPUTokenToHost: INF when empty
+ *   host_token_to_gpu   [n_h] int32  HostTokenToGPU: INF when not resident
+ *   gpu_kv              [n_g][576] bf16  device latent-KV pool
+ *   host_kv             [n_h][576] bf16  pinned, mapped host pool (device pointer)
+ *   counters            [4] int32 device: [0] free slots, [1] entries in use in
+ *                       gpu_indices_buffer, [2..3] reserved
+ * Slots and host rows are plain indices; the pool is consistent when
+ * host_token_to_gpu[gpu_token_to_host[s]] == s for every occupied slot s.
+ */
+typedef struct echo_pool {
+    int32_t n_g;
+    int32_t n_h;
+    uint8_t *gpu_token_free;
+    int32_t *gpu_token_priority;
+    int32_t *gpu_indices_buffer;
+    int32_t *gpu_token_to_host;
+    int32_t *host_token_to_gpu;
+    uint16_t *gpu_kv;
+    uint16_t *host_kv;
+    int32_t *counters;
+} echo_pool;
+
+/*
+ * Device scratch of the cache-manager calls, sized by echo_workspace_bytes() for
+ * a pool of n_g slots and at most max_rows selected rows per call
+ * (B * n_q * k for recall; B for append; n for allocate).  Initialise once with
+ * echo_workspace_init(); every call leaves it initialised again.  One workspace
+ * serves calls that run one after another on one stream.
+ */
+typedef struct echo_workspace {
+    void *base;       /* device memory, 256-byte aligned */
+    size_t bytes;
+    int32_t n_g;
+    int32_t max_rows;
+} echo_workspace;
+
+/*
+ * Cumulative counters (device memory, int64 each; the caller zeroes them).
+ * selected/unique_rows/hits/misses count the selected rows of a recall (hits and
+ * misses after de-duplication, residency at step start); recalled = misses that
+ * got a slot; unrecalled = misses left out (pool exhausted); evicted = slots freed;
+ * staged = rows the prefetch copied; staged_used = recalled rows taken from the
+ * staging area; appended = tokens written through by append.
+ */
+typedef struct echo_stats {
+    int64_t steps, selected, unique_rows, hits, misses, recalled, unrecalled, evicted,
+        staged, staged_used, appended;
+} echo_stats;
+
+/*
+ * Prefetch staging area (section 6.1 intra-query prefetch; the page leaves the
+ * landing place of prefetched rows open, this library stages them in HBM):
+ *   rows        [B][stride][576] bf16 device
+ *   host_row    [B][stride] int32 device  host row held by each staged row
+ *   count       [B] int32 device          prefetch counter of each request; must
+ *                                         be 0 before the indexer runs; the recall
+ *                                         resets it to 0
+ *   stride      rows reserved per request
+ *   cap_div     request b stages at most min(stride, ceil(ctx_len[b] / cap_div))
+ *               rows (cap proportional to the context length)
+ */
+typedef struct echo_stage {
+    uint16_t *rows;
+    int32_t *host_row;
+    int32_t *count;
+    int32_t stride;
+    int32_t cap_div;
+} echo_stage;
+
+/*
+ * Lightning-indexer score (section 2 "DSA indexer"; section 6.3 fused kernel):
+ *   scores[b][j][p] = sum_{h<64} w[b][j][h] * ReLU( sum_{d<128} q[b][j][h][d] * k_index[b][p][d] )
+ * for p < ctx_len[b] - (n_q - 1 - j) (query j of a request scoring n_q new
+ * tokens sees that many keys); other entries of `scores` are left untouched.
+ *   q        [B][n_q][64][128] e4m3 device, 16-byte aligned
+ *   w        [B][n_q][64] fp32 device
+ *   k_index  [B][L_max][128] e4m3 device, 16-byte aligned (the indexer K cache)
+ *   ctx_len  [B] int32 device, 0 <= ctx_len[b] <= L_max
+ *   scores   [B][n_q][L_max] fp32 device
+ * FP8 products accumulate in the tensor cores' fp32 accumulator; the ReLU and the
+ * weighted head sum run in fp32.
+ * Fused prefetch (enabled when s_hat != NULL; section 6.1): a token whose score
+ * exceeds s_hat[b][j] for some j and whose host row req_to_host[b][p] is not
+ * resident takes a ticket from stage->count[b]; tickets below the cap copy the
+ * host row into stage->rows[b][ticket] and record it in stage->host_row.  The
+ * prefetch never changes what is selected.  Needs pool (read-only here),
+ * req_to_host [B][L_max] int32 device, stage.
+ */
+typedef struct echo_indexer_args {
+    const uint8_t *q;
+    const float *w;
+    const uint8_t *k_index;
+    const int32_t *ctx_len;
+    int32_t B, n_q, L_max;
+    float *scores;
+    /* fused prefetch, all optional */
+    const float *s_hat;
+    const int32_t *req_to_host;
+    const echo_pool *pool;
+    const echo_stage *stage;
+    int32_t *dev_status;
+} echo_indexer_args;
+
+int echo_indexer_score(const echo_indexer_args *args, void *stream);
+
+/*
+ * Exact top-k per (b, j) row of `scores` over its first
+ * ctx_len[b] - (n_q - 1 - j) entries (section 2: top-k with k = 2048).  Ties at the
+ * k-th value go to the lower token index.  sel[b][j][0..k) lists the selected
+ * token indices in ascending order, -1 padded when fewer than k tokens exist;
+ * kth[b][j] is the min(k, L)-th largest score (-inf for an empty row).
+ *   scores [B][n_q][L_max] fp32 device (no NaN); sel [B][n_q][k] int32; kth [B][n_q] fp32
+ * Limits: 1 <= k <= 8192, L_max <= 393216.
+ */
+int echo_select_topk(const float *scores, const int32_t *ctx_len, int32_t B, int32_t n_q,
+                     int32_t L_max, int32_t k, int32_t *sel, float *kth, void *stream);
+
+/* Sizes and initialisation of the cache-manager scratch. */
+int echo_workspace_bytes(int32_t n_g, int32_t max_rows, size_t *bytes);
+int echo_workspace_init(const echo_workspace *ws, void *stream);
+
+/* Empty pool: free = 1, priority = -1, indices buffer = -1, both maps = INF,
+   counters = {n_g, 0}.  Does not touch gpu_kv or host_kv. */
+int echo_pool_init(const echo_pool *pool, void *stream);
+
+/*
+ * Allocate (section 5.2): give host_idx[0..n) GPU slots, n = *n_dev (device),
+ * n <= max_n.  The i-th valid row takes the i-th lowest free slot (the atomic
+ * tickets of the page taken in slot order); the slot's priority becomes `clock`
+ * (or *clock_dev when clock_dev != NULL), both maps are set, out_slots[i] = slot
+ * and gpu_indices_buffer[0..granted) lists the slots.  Rows already resident,
+ * repeated or out of range get -1 and ECHO_DEV_BAD_INDEX; rows beyond the free
+ * slots get -1 and ECHO_DEV_POOL_EXHAUSTED.  No KV bytes move.
+ */
+int echo_pool_alloc(const echo_pool *pool, const echo_workspace *ws, const int32_t *host_idx,
+                    const int32_t *n_dev, int32_t max_n, int32_t clock, const int32_t *clock_dev,
+                    int32_t *out_slots, int32_t *dev_status, void *stream);
+
+/*
+ * Free (section 5.2): evict n = *n_needed_dev slots with the smallest
+ * (priority, slot) among occupied slots whose priority is below the clock
+ * (selected tokens carry priority == clock, which protects them).  Sets free = 1,
+ * priority = -1, HostTokenToGPU = INF, GPUTokenToHost = INF; gpu_indices_buffer
+ * lists the evicted slots in ascending order.  No KV bytes move.  Fewer evictable
+ * slots than asked: all of them go and ECHO_DEV_POOL_EXHAUSTED is set.
+ */
+int echo_pool_evict(const echo_pool *pool, const echo_workspace *ws, const int32_t *n_needed_dev,
+                    int32_t clock, const int32_t *clock_dev, int32_t *dev_status, void *stream);
+
+/*
+ * Guaranteed recall (section 4 step list; section 5.2 "Recall"):
+ *   (i) map sel[b][j][i] to host rows req_to_host[b][p], first occurrence in
+ *   (b, j, i) order; (ii) resident rows: priority = clock; (iii) evict
+ *   max(0, misses - free) slots; (iv) allocate the misses in order; (v) copy each
+ *   recalled row from the staging area when the prefetch staged it this step,
+ *   else from host_kv, into gpu_kv; (vi) out_slot[b][j][i] = slot of sel[b][j][i],
+ *   -1 for padding and for rows left out when the pool is exhausted.
+ *   sel [B][n_q][k] int32 device; req_to_host [B][L_max] int32 device;
+ *   stage optional (NULL: nothing staged); stats optional (device echo_stats).
+ * B * n_q * k must not exceed ws->max_rows.
+ */
+int echo_prefetch_recall(const echo_pool *pool, const echo_workspace *ws, const int32_t *sel,
+                         const int32_t *req_to_host, const int32_t *ctx_len, int32_t B, int32_t n_q,
+                         int32_t k, int32_t L_max, const echo_stage *stage, int32_t clock,
+                         const int32_t *clock_dev, int32_t *out_slot, echo_stats *stats,
+                         int32_t *dev_status, void *stream);
+
+/*
+ * Write-through append of the token each request generated (section 2 "offload";
+ * section 5.2 "Free" notes the host copy is made at generation): for request b,
+ * p = ctx_len[b]; new_kv[b] is written to host row req_to_host[b][p] and to a newly
+ * allocated GPU slot (priority = clock, evicting first if the pool is short),
+ * new_k_index[b] to k_index[b][p]; then ctx_len[b] = p + 1.
+ *   new_kv [B][576] bf16 device; new_k_index [B][128] e4m3 device.
+ */
+int echo_append(const echo_pool *pool, const echo_workspace *ws, uint8_t *k_index, int32_t *ctx_len,
+                const int32_t *req_to_host, int32_t B, int32_t L_max, const uint16_t *new_kv,
+                const uint8_t *new_k_index, int32_t clock, const int32_t *clock_dev,
+                echo_stats *stats, int32_t *dev_status, void *stream);
+
+/*
+ * EMA of the k-th score (section 6.1): s_hat = alpha*s_hat + (1-alpha)*kth in fp32
+ * (multiply, multiply, add, each rounded); s_hat = +inf (the start value, no
+ * prefetch) takes kth directly; a non-finite kth (empty row) leaves s_hat as is.
+ */
+int echo_ema_update(float *s_hat, const float *kth, int32_t n, float alpha, void *stream);
+
+/* Stages of echo_decode_step, in order (timing events are recorded before each
+   stage and after the last). */
+#define ECHO_STAGE_APPEND 0
+#define ECHO_STAGE_INDEXER 1
+#define ECHO_STAGE_TOPK 2
+#define ECHO_STAGE_RECALL 3
+#define ECHO_STAGE_EMA 4
+#define ECHO_NUM_STAGES 5
+
+/*
+ * One layer's decode step, every stage on the device (section 4 step list):
+ *   [append] -> indexer score + fused prefetch -> top-k -> guaranteed recall -> EMA.
+ * Fields as in the single calls.  new_kv == NULL skips the append.  s_hat may be
+ * NULL (no prefetch, no EMA).  When clock_dev != NULL the kernels read the clock
+ * there and, if advance_clock != 0, the last kernel increments it, so one captured
+ * graph can be replayed step after step.  stage_events: optional array of
+ * ECHO_NUM_STAGES + 1 cudaEvent_t (timing-enabled) recorded around the stages
+ * (as external event nodes under capture).
+ */
+typedef struct echo_step_args {
+    const echo_pool *pool;
+    const echo_workspace *ws;
+    const echo_stage *stage;
+    const uint8_t *q;
+    const float *w;
+    uint8_t *k_index;
+    int32_t *ctx_len;
+    const int32_t *req_to_host;
+    int32_t B, n_q, L_max, k;
+    float *scores;
+    int32_t *sel;
+    float *kth;
+    int32_t *out_slot;
+    float *s_hat;
+    float alpha;
+    const uint16_t *new_kv;
+    const uint8_t *new_k_index;
+    int32_t clock;
+    int32_t *clock_dev;
+    int32_t advance_clock;
+    echo_stats *stats;
+    int32_t *dev_status;
+    void **stage_events;
+} echo_step_args;
+
+int echo_decode_step(const echo_step_args *args, void *stream);
+
+/* Description of the calling thread's last error ("" if none). */
+const char *echo_last_error_string(void);
+
+/* Library version, (major << 16) | minor. */
+int32_t echo_version(void);
+
+/* Storage law of the metadata arrays of one pool (section 5.1): 4*n_h + 13*n_g. */
+int64_t echo_metadata_bytes(int64_t n_h, int64_t n_g);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ECHO_GB300_H */

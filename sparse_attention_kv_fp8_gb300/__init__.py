@@ -1,0 +1,331 @@
+"""GB300 (sm_103a) ECHO decode step: thin ctypes binding over libecho_gb300.
+
+Every function here marshals arguments (torch tensors -> raw pointers, the
+current CUDA stream) and calls the C ABI of include/echo.h with the same name;
+all work runs in the library's CUDA kernels.  There is no CPU or PyTorch
+fallback: importing the binding without the built library raises.
+
+Buffers are plain torch tensors: device tensors for the GPU side, a pinned
+(page-locked, mapped) CPU tensor for the host KV pool.  `Pool`, `Workspace`,
+`Stage` and `Stats` are small holders that allocate those tensors and build the
+C structs.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import platform
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, f"libecho_gb300_{platform.machine()}.so")
+
+ECHO_OK, ECHO_EINVAL, ECHO_ECUDA, ECHO_ENOTSUP = 0, 1, 2, 3
+DEV_POOL_EXHAUSTED, DEV_BAD_INDEX, DEV_WAIT_TIMEOUT, DEV_PREFETCH_CAP_HIT = 1, 2, 4, 8
+INF = 0x7FFFFFFF
+H_INDEX, D_INDEX, KV_ELEMS, KV_BYTES = 64, 128, 576, 1152
+STAGE_APPEND, STAGE_INDEXER, STAGE_TOPK, STAGE_RECALL, STAGE_EMA, NUM_STAGES = range(6)
+STAT_FIELDS = ("steps", "selected", "unique_rows", "hits", "misses", "recalled", "unrecalled",
+               "evicted", "staged", "staged_used", "appended")
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+
+
+class EchoError(RuntimeError):
+    pass
+
+
+class c_pool(ctypes.Structure):
+    _fields_ = [("n_g", _I32), ("n_h", _I32), ("gpu_token_free", _P), ("gpu_token_priority", _P),
+                ("gpu_indices_buffer", _P), ("gpu_token_to_host", _P), ("host_token_to_gpu", _P),
+                ("gpu_kv", _P), ("host_kv", _P), ("counters", _P)]
+
+
+class c_workspace(ctypes.Structure):
+    _fields_ = [("base", _P), ("bytes", ctypes.c_size_t), ("n_g", _I32), ("max_rows", _I32)]
+
+
+class c_stage(ctypes.Structure):
+    _fields_ = [("rows", _P), ("host_row", _P), ("count", _P), ("stride", _I32), ("cap_div", _I32)]
+
+
+class c_indexer_args(ctypes.Structure):
+    _fields_ = [("q", _P), ("w", _P), ("k_index", _P), ("ctx_len", _P), ("B", _I32), ("n_q", _I32),
+                ("L_max", _I32), ("scores", _P), ("s_hat", _P), ("req_to_host", _P),
+                ("pool", ctypes.POINTER(c_pool)), ("stage", ctypes.POINTER(c_stage)), ("dev_status", _P)]
+
+
+class c_step_args(ctypes.Structure):
+    _fields_ = [("pool", ctypes.POINTER(c_pool)), ("ws", ctypes.POINTER(c_workspace)),
+                ("stage", ctypes.POINTER(c_stage)), ("q", _P), ("w", _P), ("k_index", _P), ("ctx_len", _P),
+                ("req_to_host", _P), ("B", _I32), ("n_q", _I32), ("L_max", _I32), ("k", _I32),
+                ("scores", _P), ("sel", _P), ("kth", _P), ("out_slot", _P), ("s_hat", _P),
+                ("alpha", ctypes.c_float), ("new_kv", _P), ("new_k_index", _P), ("clock", _I32),
+                ("clock_dev", _P), ("advance_clock", _I32), ("stats", _P), ("dev_status", _P),
+                ("stage_events", ctypes.POINTER(_P))]
+
+
+_lib = None
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load the built library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise EchoError(f"libecho_gb300 is not built ({path}); run __graft_entry__.build()")
+    L = ctypes.CDLL(path)
+    S = ctypes.c_int
+    sig = {
+        "echo_indexer_score": ([ctypes.POINTER(c_indexer_args), _P], S),
+        "echo_select_topk": ([_P, _P, _I32, _I32, _I32, _I32, _P, _P, _P], S),
+        "echo_workspace_bytes": ([_I32, _I32, ctypes.POINTER(ctypes.c_size_t)], S),
+        "echo_workspace_init": ([ctypes.POINTER(c_workspace), _P], S),
+        "echo_pool_init": ([ctypes.POINTER(c_pool), _P], S),
+        "echo_pool_alloc": ([ctypes.POINTER(c_pool), ctypes.POINTER(c_workspace), _P, _P, _I32, _I32, _P, _P, _P, _P], S),
+        "echo_pool_evict": ([ctypes.POINTER(c_pool), ctypes.POINTER(c_workspace), _P, _I32, _P, _P, _P], S),
+        "echo_prefetch_recall": ([ctypes.POINTER(c_pool), ctypes.POINTER(c_workspace), _P, _P, _P, _I32, _I32, _I32,
+                                  _I32, ctypes.POINTER(c_stage), _I32, _P, _P, _P, _P, _P], S),
+        "echo_append": ([ctypes.POINTER(c_pool), ctypes.POINTER(c_workspace), _P, _P, _P, _I32, _I32, _P, _P, _I32,
+                         _P, _P, _P, _P], S),
+        "echo_ema_update": ([_P, _P, _I32, ctypes.c_float, _P], S),
+        "echo_decode_step": ([ctypes.POINTER(c_step_args), _P], S),
+        "echo_last_error_string": ([], ctypes.c_char_p),
+        "echo_version": ([], _I32),
+        "echo_metadata_bytes": ([ctypes.c_int64, ctypes.c_int64], ctypes.c_int64),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = L
+    return L
+
+
+def _check(rc: int, what: str):
+    if rc != ECHO_OK:
+        msg = load_library().echo_last_error_string().decode()
+        raise EchoError(f"{what} failed (code {rc}): {msg}")
+
+
+def _ptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise EchoError("tensors passed to libecho_gb300 must be contiguous")
+    return t.data_ptr()
+
+
+def _dev(t: torch.Tensor | None, name: str):
+    if t is not None and not t.is_cuda:
+        raise EchoError(f"{name} must be a CUDA tensor")
+    return _ptr(t)
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+# ---------------------------------------------------------------------------
+# holders
+# ---------------------------------------------------------------------------
+
+class Pool:
+    """One layer's GPU pool plus a view of the (per-model) pinned host pool."""
+
+    def __init__(self, n_g: int, host_kv: torch.Tensor, device="cuda"):
+        if host_kv.device.type != "cpu" or not host_kv.is_pinned():
+            raise EchoError("host_kv must be a pinned CPU tensor")
+        if host_kv.dtype not in (torch.int16, torch.uint16, torch.bfloat16) or host_kv.shape[-1] != KV_ELEMS:
+            raise EchoError("host_kv must be [n_h][576] 16-bit")
+        self.n_g = int(n_g)
+        self.n_h = int(host_kv.shape[0])
+        self.host_kv = host_kv
+        self.free = torch.empty(n_g, dtype=torch.uint8, device=device)
+        self.prio = torch.empty(n_g, dtype=torch.int32, device=device)
+        self.idxbuf = torch.empty(n_g, dtype=torch.int32, device=device)
+        self.to_host = torch.empty(n_g, dtype=torch.int32, device=device)
+        self.host_to_gpu = torch.empty(self.n_h, dtype=torch.int32, device=device)
+        self.gpu_kv = torch.zeros((n_g, KV_ELEMS), dtype=torch.int16, device=device)
+        self.counters = torch.zeros(4, dtype=torch.int32, device=device)
+        self.c = c_pool(self.n_g, self.n_h, _ptr(self.free), _ptr(self.prio), _ptr(self.idxbuf),
+                        _ptr(self.to_host), _ptr(self.host_to_gpu), _ptr(self.gpu_kv), _ptr(host_kv),
+                        _ptr(self.counters))
+
+    def load_state(self, st, gpu_kv=None):
+        """Install a workload.PoolState (metadata arrays + counters); gpu_kv defaults
+        to the host rows of the occupied slots."""
+        import numpy as np
+        self.free.copy_(torch.from_numpy(st.gpu_token_free))
+        self.prio.copy_(torch.from_numpy(st.gpu_token_priority))
+        self.idxbuf.copy_(torch.from_numpy(st.gpu_indices_buffer))
+        self.to_host.copy_(torch.from_numpy(st.gpu_token_to_host))
+        self.host_to_gpu.copy_(torch.from_numpy(st.host_token_to_gpu))
+        self.counters.copy_(torch.tensor([st.n_free, st.idx_count, 0, 0], dtype=torch.int32))
+        if gpu_kv is None:
+            occ = np.nonzero(st.gpu_token_free == 0)[0]
+            kv = torch.zeros((self.n_g, KV_ELEMS), dtype=torch.int16)
+            if occ.size:
+                hk = self.host_kv.view(torch.int16)
+                kv[torch.from_numpy(occ)] = hk[torch.from_numpy(st.gpu_token_to_host[occ].astype(np.int64))]
+            self.gpu_kv.copy_(kv)
+        else:
+            self.gpu_kv.copy_(gpu_kv)
+
+    def metadata(self):
+        return dict(free=self.free.cpu().numpy(), prio=self.prio.cpu().numpy(), idxbuf=self.idxbuf.cpu().numpy(),
+                    to_host=self.to_host.cpu().numpy(), host_to_gpu=self.host_to_gpu.cpu().numpy(),
+                    n_free=int(self.counters[0]), idx_count=int(self.counters[1]))
+
+
+class Workspace:
+    def __init__(self, n_g: int, max_rows: int, device="cuda", stream=None):
+        n = ctypes.c_size_t()
+        _check(load_library().echo_workspace_bytes(n_g, max_rows, ctypes.byref(n)), "echo_workspace_bytes")
+        self.buf = torch.empty(n.value + 256, dtype=torch.uint8, device=device)
+        base = (self.buf.data_ptr() + 255) & ~255
+        self.c = c_workspace(base, n.value, n_g, max_rows)
+        _check(load_library().echo_workspace_init(ctypes.byref(self.c), _stream(stream)), "echo_workspace_init")
+
+
+class Stage:
+    def __init__(self, B: int, stride: int, cap_div: int = 16, device="cuda"):
+        self.rows = torch.zeros((B, stride, KV_ELEMS), dtype=torch.int16, device=device)
+        self.host_row = torch.full((B, stride), -1, dtype=torch.int32, device=device)
+        self.count = torch.zeros(B, dtype=torch.int32, device=device)
+        self.stride, self.cap_div = int(stride), int(cap_div)
+        self.c = c_stage(_ptr(self.rows), _ptr(self.host_row), _ptr(self.count), self.stride, self.cap_div)
+
+
+class Stats:
+    def __init__(self, device="cuda"):
+        self.t = torch.zeros(len(STAT_FIELDS), dtype=torch.int64, device=device)
+
+    def as_dict(self):
+        v = self.t.cpu().tolist()
+        return dict(zip(STAT_FIELDS, v))
+
+
+# ---------------------------------------------------------------------------
+# C-ABI calls
+# ---------------------------------------------------------------------------
+
+def echo_indexer_score(q, w, k_index, ctx_len, scores, s_hat=None, req_to_host=None, pool: Pool | None = None,
+                       stage: Stage | None = None, dev_status=None, stream=None):
+    B, n_q = q.shape[0], q.shape[1]
+    a = c_indexer_args(_dev(q, "q"), _dev(w, "w"), _dev(k_index, "k_index"), _dev(ctx_len, "ctx_len"), B, n_q,
+                       k_index.shape[1], _dev(scores, "scores"), _dev(s_hat, "s_hat"),
+                       _dev(req_to_host, "req_to_host"),
+                       ctypes.pointer(pool.c) if pool is not None else None,
+                       ctypes.pointer(stage.c) if stage is not None else None, _dev(dev_status, "dev_status"))
+    _check(load_library().echo_indexer_score(ctypes.byref(a), _stream(stream)), "echo_indexer_score")
+
+
+def echo_select_topk(scores, ctx_len, k: int, sel, kth, stream=None):
+    B, n_q, L_max = scores.shape
+    _check(load_library().echo_select_topk(_dev(scores, "scores"), _dev(ctx_len, "ctx_len"), B, n_q, L_max, k,
+                                           _dev(sel, "sel"), _dev(kth, "kth"), _stream(stream)), "echo_select_topk")
+
+
+def echo_pool_init(pool: Pool, stream=None):
+    _check(load_library().echo_pool_init(ctypes.byref(pool.c), _stream(stream)), "echo_pool_init")
+
+
+def echo_pool_alloc(pool: Pool, ws: Workspace, host_idx, n_dev, clock: int, out_slots, dev_status=None,
+                    clock_dev=None, stream=None):
+    _check(load_library().echo_pool_alloc(ctypes.byref(pool.c), ctypes.byref(ws.c), _dev(host_idx, "host_idx"),
+                                          _dev(n_dev, "n_dev"), int(host_idx.numel()), int(clock),
+                                          _dev(clock_dev, "clock_dev"), _dev(out_slots, "out_slots"),
+                                          _dev(dev_status, "dev_status"), _stream(stream)), "echo_pool_alloc")
+
+
+def echo_pool_evict(pool: Pool, ws: Workspace, n_needed_dev, clock: int, dev_status=None, clock_dev=None,
+                    stream=None):
+    _check(load_library().echo_pool_evict(ctypes.byref(pool.c), ctypes.byref(ws.c), _dev(n_needed_dev, "n_needed"),
+                                          int(clock), _dev(clock_dev, "clock_dev"), _dev(dev_status, "dev_status"),
+                                          _stream(stream)), "echo_pool_evict")
+
+
+def echo_prefetch_recall(pool: Pool, ws: Workspace, sel, req_to_host, ctx_len, clock: int, out_slot,
+                         stage: Stage | None = None, stats: Stats | None = None, dev_status=None, clock_dev=None,
+                         stream=None):
+    B, n_q, k = sel.shape
+    _check(load_library().echo_prefetch_recall(
+        ctypes.byref(pool.c), ctypes.byref(ws.c), _dev(sel, "sel"), _dev(req_to_host, "req_to_host"),
+        _dev(ctx_len, "ctx_len"), B, n_q, k, req_to_host.shape[1],
+        ctypes.pointer(stage.c) if stage is not None else None, int(clock), _dev(clock_dev, "clock_dev"),
+        _dev(out_slot, "out_slot"), _dev(stats.t, "stats") if stats is not None else None,
+        _dev(dev_status, "dev_status"), _stream(stream)), "echo_prefetch_recall")
+
+
+def echo_append(pool: Pool, ws: Workspace, k_index, ctx_len, req_to_host, new_kv, new_k_index, clock: int,
+                stats: Stats | None = None, dev_status=None, clock_dev=None, stream=None):
+    B, L_max = k_index.shape[0], k_index.shape[1]
+    _check(load_library().echo_append(
+        ctypes.byref(pool.c), ctypes.byref(ws.c), _dev(k_index, "k_index"), _dev(ctx_len, "ctx_len"),
+        _dev(req_to_host, "req_to_host"), B, L_max, _dev(new_kv, "new_kv"), _dev(new_k_index, "new_k_index"),
+        int(clock), _dev(clock_dev, "clock_dev"), _dev(stats.t, "stats") if stats is not None else None,
+        _dev(dev_status, "dev_status"), _stream(stream)), "echo_append")
+
+
+def echo_ema_update(s_hat, kth, alpha: float = 0.5, stream=None):
+    _check(load_library().echo_ema_update(_dev(s_hat, "s_hat"), _dev(kth, "kth"), int(s_hat.numel()),
+                                          float(alpha), _stream(stream)), "echo_ema_update")
+
+
+class StepBuffers:
+    """Device outputs of one decode step for B requests, n_q queries, k."""
+
+    def __init__(self, B: int, n_q: int, L_max: int, k: int, device="cuda"):
+        self.scores = torch.empty((B, n_q, L_max), dtype=torch.float32, device=device)
+        self.sel = torch.empty((B, n_q, k), dtype=torch.int32, device=device)
+        self.kth = torch.empty((B, n_q), dtype=torch.float32, device=device)
+        self.out_slot = torch.empty((B, n_q, k), dtype=torch.int32, device=device)
+        self.dev_status = torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def make_step_args(pool: Pool, ws: Workspace, q, w, k_index, ctx_len, req_to_host, k: int, out: StepBuffers,
+                   stage: Stage | None = None, s_hat=None, alpha: float = 0.5, new_kv=None, new_k_index=None,
+                   clock: int = 0, clock_dev=None, advance_clock: bool = False, stats: Stats | None = None,
+                   events=None) -> c_step_args:
+    """Build the C struct once (e.g. before graph capture); keep the returned object
+    alive while it is in use."""
+    B, n_q = q.shape[0], q.shape[1]
+    a = c_step_args()
+    a.pool = ctypes.pointer(pool.c)
+    a.ws = ctypes.pointer(ws.c)
+    a.stage = ctypes.pointer(stage.c) if stage is not None else None
+    a.q, a.w, a.k_index = _dev(q, "q"), _dev(w, "w"), _dev(k_index, "k_index")
+    a.ctx_len, a.req_to_host = _dev(ctx_len, "ctx_len"), _dev(req_to_host, "req_to_host")
+    a.B, a.n_q, a.L_max, a.k = B, n_q, k_index.shape[1], int(k)
+    a.scores, a.sel, a.kth, a.out_slot = _ptr(out.scores), _ptr(out.sel), _ptr(out.kth), _ptr(out.out_slot)
+    a.s_hat = _dev(s_hat, "s_hat")
+    a.alpha = float(alpha)
+    a.new_kv, a.new_k_index = _dev(new_kv, "new_kv"), _dev(new_k_index, "new_k_index")
+    a.clock = int(clock)
+    a.clock_dev = _dev(clock_dev, "clock_dev")
+    a.advance_clock = 1 if advance_clock else 0
+    a.stats = _dev(stats.t, "stats") if stats is not None else None
+    a.dev_status = _ptr(out.dev_status)
+    if events is not None:
+        arr = (_P * (NUM_STAGES + 1))(*[e.cuda_event for e in events])
+        a._events_keepalive = arr
+        a.stage_events = arr
+    # keep the referenced holders alive with the struct
+    a._keep = (pool, ws, stage, q, w, k_index, ctx_len, req_to_host, out, s_hat, new_kv, new_k_index, clock_dev,
+               stats)
+    return a
+
+
+def echo_decode_step(args: c_step_args, stream=None):
+    _check(load_library().echo_decode_step(ctypes.byref(args), _stream(stream)), "echo_decode_step")
+
+
+def version() -> int:
+    return int(load_library().echo_version())

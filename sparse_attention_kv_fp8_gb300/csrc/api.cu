@@ -1,0 +1,309 @@
+// api.cu -- the extern "C" entry points declared in include/echo.h: argument
+// validation on the host, then kernel launches on the caller's stream.  Nothing
+// here allocates, synchronises or reads device memory.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "echo_common.cuh"
+
+namespace echo_host {
+
+static thread_local char g_err[512] = "";
+
+void set_error(const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+}
+
+int cuda_fail(cudaError_t e, const char *what) {
+  set_error("%s: %s", what, cudaGetErrorString(e));
+  return ECHO_ECUDA;
+}
+
+// launchers (indexer.cu, topk.cu, cache_mgr.cu)
+int launch_indexer(const echo_indexer_args *a, cudaStream_t stream);
+int launch_topk(const float *scores, const int32_t *ctx_len, int B, int n_q, int L_max, int k, int32_t *sel,
+                float *kth, cudaStream_t stream);
+size_t workspace_bytes(int32_t n_g, int32_t max_rows);
+int launch_workspace_init(const echo_workspace *w, cudaStream_t s);
+int launch_pool_init(const echo_pool *p, cudaStream_t s);
+int launch_pool_alloc(const echo_pool *pool, const echo_workspace *ws, const int32_t *host_idx, const int32_t *n_dev,
+                      int32_t max_n, int32_t clock, const int32_t *clock_dev, int32_t *out_slots, int32_t *status,
+                      cudaStream_t s);
+int launch_pool_evict(const echo_pool *pool, const echo_workspace *ws, const int32_t *n_needed_dev, int32_t clock,
+                      const int32_t *clock_dev, int32_t *status, cudaStream_t s);
+int launch_recall(const echo_pool *pool, const echo_workspace *ws, const int32_t *sel, const int32_t *req_to_host,
+                  const int32_t *ctx_len, int B, int n_q, int k, int L_max, const echo_stage *stage, int32_t clock,
+                  const int32_t *clock_dev, int32_t *out_slot, echo_stats *stats, int32_t *status, cudaStream_t s);
+int launch_append(const echo_pool *pool, const echo_workspace *ws, uint8_t *k_index, int32_t *ctx_len,
+                  const int32_t *req_to_host, int B, int L_max, const uint16_t *new_kv, const uint8_t *new_k_index,
+                  int32_t clock, const int32_t *clock_dev, echo_stats *stats, int32_t *status, cudaStream_t s);
+int launch_ema(float *s_hat, const float *kth, int n, float alpha, int32_t *clock_dev, int advance, cudaStream_t s);
+
+}  // namespace echo_host
+
+using namespace echo_host;
+
+#define REQUIRE(cond, ...)             \
+  do {                                 \
+    if (!(cond)) {                     \
+      set_error(__VA_ARGS__);          \
+      return ECHO_EINVAL;              \
+    }                                  \
+  } while (0)
+
+#define TRY(x)                  \
+  do {                          \
+    int _r = (x);               \
+    if (_r != ECHO_OK) return _r; \
+  } while (0)
+
+static bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// A pointer the kernels may dereference: device memory, managed memory, or
+// pinned host memory mapped at the same address.  Checked once per pointer (the
+// answer is cached) so that later calls stay capturable.
+static int check_device_accessible(const void *p, const char *name) {
+  static std::mutex mu;
+  static const void *seen[64];
+  static int n_seen = 0;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < n_seen; ++i)
+      if (seen[i] == p) return ECHO_OK;
+  }
+  cudaPointerAttributes at;
+  cudaError_t e = cudaPointerGetAttributes(&at, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    set_error("%s: not a CUDA-visible pointer (%s)", name, cudaGetErrorString(e));
+    return ECHO_EINVAL;
+  }
+  bool ok = at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged ||
+            (at.type == cudaMemoryTypeHost && at.devicePointer == p);
+  if (!ok) {
+    set_error("%s: must be device memory or pinned host memory mapped at the same address", name);
+    return ECHO_EINVAL;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  if (n_seen < 64) seen[n_seen++] = p;
+  return ECHO_OK;
+}
+
+static int check_pool(const echo_pool *p) {
+  REQUIRE(p, "pool is NULL");
+  REQUIRE(p->n_g > 0 && p->n_h > 0, "pool sizes must be positive (n_g=%d, n_h=%d)", p->n_g, p->n_h);
+  REQUIRE(p->gpu_token_free && p->gpu_token_priority && p->gpu_indices_buffer && p->gpu_token_to_host &&
+              p->host_token_to_gpu && p->counters,
+          "pool metadata pointer is NULL");
+  REQUIRE(p->gpu_kv && p->host_kv, "pool KV pointer is NULL");
+  REQUIRE(aligned(p->gpu_kv, 16) && aligned(p->host_kv, 16), "pool KV pools must be 16-byte aligned");
+  return check_device_accessible(p->host_kv, "pool.host_kv");
+}
+
+static int check_ws(const echo_workspace *w, const echo_pool *p, long long rows) {
+  REQUIRE(w && w->base, "workspace is NULL");
+  REQUIRE(aligned(w->base, 256), "workspace base must be 256-byte aligned");
+  REQUIRE(w->n_g == p->n_g, "workspace was sized for n_g=%d, pool has %d", w->n_g, p->n_g);
+  REQUIRE(rows <= w->max_rows, "call needs %lld workspace rows, workspace has %d", rows, w->max_rows);
+  REQUIRE(w->bytes >= workspace_bytes(w->n_g, w->max_rows), "workspace smaller than echo_workspace_bytes()");
+  return ECHO_OK;
+}
+
+static int check_stage(const echo_stage *st) {
+  REQUIRE(st->rows && st->host_row && st->count, "stage pointer is NULL");
+  REQUIRE(aligned(st->rows, 16), "stage rows must be 16-byte aligned");
+  REQUIRE(st->stride > 0 && st->cap_div > 0, "stage stride and cap_div must be positive");
+  return ECHO_OK;
+}
+
+extern "C" {
+
+const char *echo_last_error_string(void) { return g_err; }
+
+int32_t echo_version(void) { return (1 << 16) | 0; }
+
+int64_t echo_metadata_bytes(int64_t n_h, int64_t n_g) {
+  return static_cast<int64_t>(sizeof(int32_t)) * n_h +
+         static_cast<int64_t>(sizeof(uint8_t) + 3 * sizeof(int32_t)) * n_g;
+}
+
+int echo_indexer_score(const echo_indexer_args *a, void *stream) {
+  g_err[0] = 0;
+  REQUIRE(a, "args is NULL");
+  REQUIRE(a->q && a->w && a->k_index && a->ctx_len && a->scores, "indexer pointer is NULL");
+  REQUIRE(a->B >= 0 && a->L_max >= 0, "negative size");
+  REQUIRE(a->n_q == 1 || a->n_q == 2, "n_q must be 1 or 2 (got %d)", a->n_q);
+  REQUIRE(aligned(a->q, 16) && aligned(a->k_index, 16), "q and k_index must be 16-byte aligned");
+  REQUIRE(static_cast<long long>(a->B) * a->L_max <= (1ll << 31) - 1, "B * L_max too large");
+  REQUIRE(static_cast<long long>(a->B) * a->n_q * echo::kHeads <= (1ll << 31) - 1, "B too large");
+  if (a->s_hat) {
+    REQUIRE(a->req_to_host && a->pool && a->stage, "prefetch needs req_to_host, pool and stage");
+    TRY(check_pool(a->pool));
+    TRY(check_stage(a->stage));
+    REQUIRE(static_cast<long long>(a->B) * a->stage->stride <= (1ll << 31) - 1, "stage too large");
+  }
+  if (a->B == 0 || a->L_max == 0) return ECHO_OK;
+  return launch_indexer(a, static_cast<cudaStream_t>(stream));
+}
+
+int echo_select_topk(const float *scores, const int32_t *ctx_len, int32_t B, int32_t n_q, int32_t L_max, int32_t k,
+                     int32_t *sel, float *kth, void *stream) {
+  g_err[0] = 0;
+  REQUIRE(scores && ctx_len && sel && kth, "top-k pointer is NULL");
+  REQUIRE(B >= 0 && L_max >= 0, "negative size");
+  REQUIRE(n_q == 1 || n_q == 2, "n_q must be 1 or 2 (got %d)", n_q);
+  REQUIRE(k >= 1 && k <= 8192, "k must be in [1, 8192] (got %d)", k);
+  REQUIRE(static_cast<long long>(B) * n_q * 8 <= (1ll << 31) - 1, "B too large");
+  if (B == 0) return ECHO_OK;
+  return launch_topk(scores, ctx_len, B, n_q, L_max, k, sel, kth, static_cast<cudaStream_t>(stream));
+}
+
+int echo_workspace_bytes(int32_t n_g, int32_t max_rows, size_t *bytes) {
+  g_err[0] = 0;
+  REQUIRE(bytes, "bytes is NULL");
+  REQUIRE(n_g > 0 && max_rows >= 0, "bad workspace sizes");
+  *bytes = workspace_bytes(n_g, max_rows);
+  return ECHO_OK;
+}
+
+int echo_workspace_init(const echo_workspace *ws, void *stream) {
+  g_err[0] = 0;
+  REQUIRE(ws && ws->base, "workspace is NULL");
+  REQUIRE(aligned(ws->base, 256), "workspace base must be 256-byte aligned");
+  REQUIRE(ws->n_g > 0 && ws->max_rows >= 0, "bad workspace sizes");
+  REQUIRE(ws->bytes >= workspace_bytes(ws->n_g, ws->max_rows), "workspace smaller than echo_workspace_bytes()");
+  return launch_workspace_init(ws, static_cast<cudaStream_t>(stream));
+}
+
+int echo_pool_init(const echo_pool *pool, void *stream) {
+  g_err[0] = 0;
+  TRY(check_pool(pool));
+  return launch_pool_init(pool, static_cast<cudaStream_t>(stream));
+}
+
+int echo_pool_alloc(const echo_pool *pool, const echo_workspace *ws, const int32_t *host_idx, const int32_t *n_dev,
+                    int32_t max_n, int32_t clock, const int32_t *clock_dev, int32_t *out_slots, int32_t *dev_status,
+                    void *stream) {
+  g_err[0] = 0;
+  TRY(check_pool(pool));
+  REQUIRE(max_n >= 0, "max_n must be >= 0");
+  REQUIRE(n_dev && (max_n == 0 || (host_idx && out_slots)), "allocate pointer is NULL");
+  REQUIRE(clock >= 0 || clock_dev, "clock must be >= 0");
+  TRY(check_ws(ws, pool, max_n));
+  return launch_pool_alloc(pool, ws, host_idx, n_dev, max_n, clock, clock_dev, out_slots, dev_status,
+                           static_cast<cudaStream_t>(stream));
+}
+
+int echo_pool_evict(const echo_pool *pool, const echo_workspace *ws, const int32_t *n_needed_dev, int32_t clock,
+                    const int32_t *clock_dev, int32_t *dev_status, void *stream) {
+  g_err[0] = 0;
+  TRY(check_pool(pool));
+  REQUIRE(n_needed_dev, "n_needed_dev is NULL");
+  REQUIRE(clock >= 0 || clock_dev, "clock must be >= 0");
+  TRY(check_ws(ws, pool, 0));
+  return launch_pool_evict(pool, ws, n_needed_dev, clock, clock_dev, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+int echo_prefetch_recall(const echo_pool *pool, const echo_workspace *ws, const int32_t *sel,
+                         const int32_t *req_to_host, const int32_t *ctx_len, int32_t B, int32_t n_q, int32_t k,
+                         int32_t L_max, const echo_stage *stage, int32_t clock, const int32_t *clock_dev,
+                         int32_t *out_slot, echo_stats *stats, int32_t *dev_status, void *stream) {
+  g_err[0] = 0;
+  TRY(check_pool(pool));
+  REQUIRE(B >= 0 && L_max >= 0 && k >= 1, "bad sizes");
+  REQUIRE(n_q == 1 || n_q == 2, "n_q must be 1 or 2");
+  REQUIRE(B == 0 || (sel && req_to_host && out_slot && ctx_len), "recall pointer is NULL");
+  REQUIRE(clock >= 0 || clock_dev, "clock must be >= 0");
+  const long long F = static_cast<long long>(B) * n_q * k;
+  REQUIRE(F <= (1ll << 30), "B * n_q * k too large");
+  TRY(check_ws(ws, pool, F));
+  if (stage) TRY(check_stage(stage));
+  return launch_recall(pool, ws, sel, req_to_host, ctx_len, B, n_q, k, L_max, stage, clock, clock_dev, out_slot, stats,
+                       dev_status, static_cast<cudaStream_t>(stream));
+}
+
+int echo_append(const echo_pool *pool, const echo_workspace *ws, uint8_t *k_index, int32_t *ctx_len,
+                const int32_t *req_to_host, int32_t B, int32_t L_max, const uint16_t *new_kv,
+                const uint8_t *new_k_index, int32_t clock, const int32_t *clock_dev, echo_stats *stats,
+                int32_t *dev_status, void *stream) {
+  g_err[0] = 0;
+  TRY(check_pool(pool));
+  REQUIRE(B >= 0 && L_max >= 0, "bad sizes");
+  REQUIRE(B == 0 || (k_index && ctx_len && req_to_host && new_kv && new_k_index), "append pointer is NULL");
+  REQUIRE(aligned(new_kv, 16) && aligned(new_k_index, 16) && aligned(k_index, 16), "append buffers must be 16-byte aligned");
+  REQUIRE(clock >= 0 || clock_dev, "clock must be >= 0");
+  TRY(check_ws(ws, pool, B));
+  return launch_append(pool, ws, k_index, ctx_len, req_to_host, B, L_max, new_kv, new_k_index, clock, clock_dev, stats,
+                       dev_status, static_cast<cudaStream_t>(stream));
+}
+
+int echo_ema_update(float *s_hat, const float *kth, int32_t n, float alpha, void *stream) {
+  g_err[0] = 0;
+  REQUIRE(n >= 0, "n must be >= 0");
+  REQUIRE(n == 0 || (s_hat && kth), "EMA pointer is NULL");
+  REQUIRE(alpha >= 0.f && alpha <= 1.f, "alpha must be in [0, 1]");
+  if (n == 0) return ECHO_OK;
+  return launch_ema(s_hat, kth, n, alpha, nullptr, 0, static_cast<cudaStream_t>(stream));
+}
+
+int echo_decode_step(const echo_step_args *a, void *stream) {
+  g_err[0] = 0;
+  REQUIRE(a, "args is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  REQUIRE(a->pool && a->ws, "step needs pool and workspace");
+  REQUIRE(a->q && a->w && a->k_index && a->ctx_len && a->req_to_host && a->scores && a->sel && a->kth &&
+              a->out_slot,
+          "step pointer is NULL");
+  REQUIRE(a->clock >= 0 || a->clock_dev, "clock must be >= 0");
+  const bool prefetch = a->s_hat && a->stage;
+  cudaEvent_t *ev = reinterpret_cast<cudaEvent_t *>(a->stage_events);
+  auto mark = [&](int i) -> int {
+    if (!ev || !ev[i]) return ECHO_OK;
+    cudaError_t e = cudaEventRecordWithFlags(ev[i], s, cudaEventRecordExternal);
+    return e == cudaSuccess ? ECHO_OK : cuda_fail(e, "stage event");
+  };
+  TRY(mark(ECHO_STAGE_APPEND));
+  if (a->new_kv) {
+    TRY(echo_append(a->pool, a->ws, a->k_index, a->ctx_len, a->req_to_host, a->B, a->L_max, a->new_kv,
+                    a->new_k_index, a->clock, a->clock_dev, a->stats, a->dev_status, stream));
+  }
+  TRY(mark(ECHO_STAGE_INDEXER));
+  echo_indexer_args ia{};
+  ia.q = a->q;
+  ia.w = a->w;
+  ia.k_index = a->k_index;
+  ia.ctx_len = a->ctx_len;
+  ia.B = a->B;
+  ia.n_q = a->n_q;
+  ia.L_max = a->L_max;
+  ia.scores = a->scores;
+  ia.dev_status = a->dev_status;
+  if (prefetch) {
+    ia.s_hat = a->s_hat;
+    ia.req_to_host = a->req_to_host;
+    ia.pool = a->pool;
+    ia.stage = a->stage;
+  }
+  TRY(echo_indexer_score(&ia, stream));
+  TRY(mark(ECHO_STAGE_TOPK));
+  TRY(echo_select_topk(a->scores, a->ctx_len, a->B, a->n_q, a->L_max, a->k, a->sel, a->kth, stream));
+  TRY(mark(ECHO_STAGE_RECALL));
+  TRY(echo_prefetch_recall(a->pool, a->ws, a->sel, a->req_to_host, a->ctx_len, a->B, a->n_q, a->k, a->L_max,
+                           prefetch ? a->stage : nullptr, a->clock, a->clock_dev, a->out_slot, a->stats,
+                           a->dev_status, stream));
+  TRY(mark(ECHO_STAGE_EMA));
+  if (a->s_hat || (a->clock_dev && a->advance_clock)) {
+    const int n = a->s_hat ? a->B * a->n_q : 0;
+    TRY(launch_ema(a->s_hat, a->kth, n, a->alpha, a->clock_dev, a->advance_clock, s));
+  }
+  TRY(mark(ECHO_NUM_STAGES));
+  return ECHO_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,523 @@
+// indexer.cu -- DSA lightning-indexer score with the fused lossless prefetch.
+//
+// ECHO review (marsggbo.github.io, "OSDI'26 | ECHO"): section 2 "DSA indexer"
+// gives s(t,s) = sum_h w_{h,t} ReLU(q_{h,t} . k_s) with H_index = 64, d_index = 128
+// and FP8 q/k; section 6.3 describes the decode kernel as a warp-specialised
+// pipeline (TMA warps load K blocks, GEMM warps write scores, prefetch warps
+// compare scores with the predicted k-th score and load rows from host memory),
+// one SM per query vector and a slice of the K cache.
+//
+// sm_103a design (one persistent CTA per SM, 10 warps):
+//   warp 0      TMA producer: 128-token K tiles (16 KB, 128B-swizzled) into a
+//               6-stage shared-memory ring; the request's q (64*n_q x 128 e4m3)
+//               into one of two q buffers.
+//   warp 1      tensor-core issuer: per tile, 4 x tcgen05.mma kind::f8f6f4
+//               (M = 128 tokens, N = 64*n_q heads, K = 32) into one of two TMEM
+//               accumulators, so the next tile's MMA overlaps this tile's epilogue.
+//   warps 2-5   epilogue: tcgen05.ld one token row per thread, ReLU, weight, sum
+//               over heads in fp32, store the score; threshold test against the
+//               predicted k-th score; candidates take tickets and go to a queue.
+//   warps 6-9   prefetch: copy queued host rows (1152 B, 16-byte loads of the
+//               pinned, mapped host pool) into the HBM staging area.
+// The kernel is HBM-bound: 128 + 4*n_q bytes per token against 2*64*128*n_q
+// FLOP, far below the FP8 ridge point.
+#include <cstdio>
+
+#include "echo_common.cuh"
+
+namespace echo {
+
+constexpr int kTileTokens = 128;
+constexpr int kTileBytes = kTileTokens * kDim;  // 16 KB
+constexpr int kStages = 6;
+constexpr int kEpiWarps = 4;
+constexpr int kPfWarps = 4;
+constexpr int kIndexerThreads = 32 * (2 + kEpiWarps + kPfWarps);
+constexpr int kQueueCap = 64;      // entries per epilogue -> prefetch queue
+constexpr int kPfRowsPerBatch = 4; // rows one prefetch warp keeps in flight
+
+struct IndexerParams {
+  const float *w;
+  const int32_t *ctx_len;
+  float *scores;
+  int32_t B, L_max;
+  // fused prefetch (enabled when s_hat != nullptr)
+  const float *s_hat;
+  const int32_t *req_to_host;
+  const int32_t *host_to_gpu;
+  int32_t n_h;
+  const uint16_t *host_kv;
+  uint16_t *stage_rows;
+  int32_t *stage_host;
+  int32_t *stage_count;
+  int32_t stage_stride;
+  int32_t cap_div;
+  int32_t *status;
+};
+
+struct alignas(16) IndexerCtl {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
+  uint64_t q_full[2];
+  uint64_t q_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int first_b, first_t, n_tiles;
+  int queue_tail[kEpiWarps];
+  int queue_head[kEpiWarps];
+  int queue_done[kEpiWarps];
+  int2 queue[kEpiWarps][kQueueCap];
+  float wsm[kEpiWarps][2 * kHeads];  // head weights of the current request, per epilogue warp
+};
+
+__device__ __forceinline__ int clamp_ctx(int32_t L, int L_max) { return L < 0 ? 0 : (L > L_max ? L_max : L); }
+
+__device__ __forceinline__ int tiles_of(int L) { return (L + kTileTokens - 1) / kTileTokens; }
+
+// next (request, tile) in the flattened sequence of non-empty tiles
+__device__ __forceinline__ void next_tile(const IndexerParams &P, int &b, int &t) {
+  ++t;
+  while (b < P.B && t >= tiles_of(clamp_ctx(__ldg(P.ctx_len + b), P.L_max))) {
+    ++b;
+    t = 0;
+  }
+}
+
+// Bounded wait used while unwinding: ignores the abort flag.
+__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer() - t0 > kWaitLimitNs) return;
+}
+
+template <int NQ>
+__global__ void __launch_bounds__(kIndexerThreads, 1)
+    indexer_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                   const __grid_constant__ CUtensorMap tmap_q, const IndexerParams P) {
+  constexpr int N = kHeads * NQ;               // MMA N: all heads of all queries
+  constexpr uint32_t kQBytes = N * kDim;       // q of one request
+  constexpr uint32_t kTmemCols = 2 * N;        // two accumulators
+  constexpr uint32_t kIdesc = idesc_e4m3_f32(kTileTokens, N);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *k_smem = smem;                                  // kStages x 16 KB
+  uint8_t *q_smem = smem + kStages * kTileBytes;           // 2 x kQBytes
+  IndexerCtl *ctl = reinterpret_cast<IndexerCtl *>(q_smem + 2 * kQBytes);
+  volatile int *abort = &ctl->abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const bool prefetch = P.s_hat != nullptr;
+
+  // ---- work split: the non-empty tiles of all requests, evenly over the grid
+  if (threadIdx.x == 0) {
+    int total = 0;
+    for (int b = 0; b < P.B; ++b) {
+      int32_t L = __ldg(P.ctx_len + b);
+      if (L < 0 || L > P.L_max) set_status(P.status, ECHO_DEV_BAD_INDEX);
+      total += tiles_of(clamp_ctx(L, P.L_max));
+    }
+    const int v0 = static_cast<int>((static_cast<long long>(total) * blockIdx.x) / gridDim.x);
+    const int v1 = static_cast<int>((static_cast<long long>(total) * (blockIdx.x + 1)) / gridDim.x);
+    int b = 0, acc = 0;
+    while (b < P.B) {
+      int nt = tiles_of(clamp_ctx(__ldg(P.ctx_len + b), P.L_max));
+      if (v0 < acc + nt) break;
+      acc += nt;
+      ++b;
+    }
+    ctl->first_b = b;
+    ctl->first_t = v0 - acc;
+    ctl->n_tiles = v1 - v0;
+    ctl->abort = 0;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ctl->tmem_full[i], 1);
+      mbar_init(&ctl->tmem_empty[i], kEpiWarps);
+      mbar_init(&ctl->q_full[i], 1);
+      mbar_init(&ctl->q_empty[i], 1);
+    }
+    mbar_init(&ctl->drain, 1);
+    for (int e = 0; e < kEpiWarps; ++e) {
+      ctl->queue_tail[e] = 0;
+      ctl->queue_head[e] = 0;
+      ctl->queue_done[e] = 0;
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const int n_tiles = ctl->n_tiles;
+  const uint32_t tmem_base = ctl->tmem_base;
+
+  if (warp == 0) {
+    // ===================== TMA producer =====================
+    if (elect_one()) {
+      tma_prefetch_desc(&tmap_k);
+      tma_prefetch_desc(&tmap_q);
+      const uint64_t policy = l2_policy_evict_first();
+      int b = ctl->first_b, t = ctl->first_t, cur_b = -1, qcount = 0, issued = 0;
+      for (int i = 0; i < n_tiles; ++i) {
+        if (b != cur_b) {
+          const int qb = qcount & 1;
+          if (qcount >= 2 && !mbar_wait(&ctl->q_empty[qb], ((qcount >> 1) - 1) & 1, abort, P.status)) break;
+          mbar_arrive_expect_tx(&ctl->q_full[qb], kQBytes);
+          tma_load_2d(q_smem + qb * kQBytes, &tmap_q, &ctl->q_full[qb], 0, b * N);
+          cur_b = b;
+          ++qcount;
+        }
+        const int s = i % kStages;
+        if (i >= kStages && !mbar_wait(&ctl->empty[s], ((i / kStages) & 1) ^ 1, abort, P.status)) break;
+        mbar_arrive_expect_tx(&ctl->full[s], kTileBytes);
+        tma_load_3d_evict_first(k_smem + s * kTileBytes, &tmap_k, &ctl->full[s], 0, t * kTileTokens, b, policy);
+        ++issued;
+        next_tile(P, b, t);
+      }
+      if (*abort) {
+        // let every copy this thread started land before the CTA exits
+        for (int i = issued - kStages < 0 ? 0 : issued - kStages; i < issued; ++i)
+          mbar_drain(&ctl->full[i % kStages], (i / kStages) & 1);
+        for (int c = qcount - 2 < 0 ? 0 : qcount - 2; c < qcount; ++c) mbar_drain(&ctl->q_full[c & 1], (c >> 1) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ===================== tensor-core issuer =====================
+    if (elect_one()) {
+      int b = ctl->first_b, t = ctl->first_t, cur_b = -1, qcount = 0, qb = 0;
+      for (int i = 0; i < n_tiles; ++i) {
+        if (b != cur_b) {
+          if (cur_b >= 0) mma_commit(&ctl->q_empty[qb]);  // previous q no longer read
+          qb = qcount & 1;
+          if (!mbar_wait(&ctl->q_full[qb], (qcount >> 1) & 1, abort, P.status)) break;
+          cur_b = b;
+          ++qcount;
+        }
+        const int s = i % kStages;
+        if (!mbar_wait(&ctl->full[s], (i / kStages) & 1, abort, P.status)) break;
+        const int ab = i & 1;
+        if (i >= 2 && !mbar_wait(&ctl->tmem_empty[ab], ((i >> 1) & 1) ^ 1, abort, P.status)) break;
+        tc_fence_after();
+        const uint32_t a_addr = smem_u32(k_smem + s * kTileBytes);
+        const uint32_t b_addr = smem_u32(q_smem + qb * kQBytes);
+#pragma unroll
+        for (int kk = 0; kk < kDim / 32; ++kk)
+          mma_f8f6f4(tmem_base + ab * N, kmajor_sw128_desc(a_addr + kk * 32),
+                     kmajor_sw128_desc(b_addr + kk * 32), kIdesc, kk > 0);
+        mma_commit(&ctl->empty[s]);
+        mma_commit(&ctl->tmem_full[ab]);
+        next_tile(P, b, t);
+      }
+      // every MMA issued above completes before the accumulators are freed
+      mma_commit(&ctl->drain);
+      mbar_drain(&ctl->drain, 0);
+    }
+  } else if (warp < 2 + kEpiWarps) {
+    // ===================== epilogue =====================
+    const int e = warp - 2;
+    const int quad = warp & 3;  // TMEM lanes this warp may read
+    const int row = quad * 32 + lane;
+    float *wsm = ctl->wsm[e];
+    int b = ctl->first_b, t = ctl->first_t, cur_b = -1;
+    float shat[NQ];
+    int valid[NQ];
+    int cap = 0;
+    int tail = 0;  // queue tail, kept by every lane (lane 0 publishes it)
+    for (int i = 0; i < n_tiles; ++i) {
+      if (b != cur_b) {
+        __syncwarp();
+        for (int x = lane; x < N; x += 32) wsm[x] = __ldg(P.w + static_cast<size_t>(b) * N + x);
+        __syncwarp();
+        const int L = clamp_ctx(__ldg(P.ctx_len + b), P.L_max);
+#pragma unroll
+        for (int j = 0; j < NQ; ++j) {
+          valid[j] = query_valid_len(L, NQ, j);
+          shat[j] = prefetch ? __ldg(P.s_hat + b * NQ + j) : 0.f;
+        }
+        if (prefetch) {
+          int c = (L + P.cap_div - 1) / P.cap_div;
+          cap = c < P.stage_stride ? c : P.stage_stride;
+        }
+        cur_b = b;
+      }
+      const int ab = i & 1;
+      if (!mbar_wait(&ctl->tmem_full[ab], (i >> 1) & 1, abort, P.status)) break;
+      tc_fence_after();
+      float sc[NQ];
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + ab * N;
+#pragma unroll
+      for (int j = 0; j < NQ; ++j) {
+        float v0[32], v1[32];
+        tmem_ld_32x32b_x32(taddr + j * kHeads, v0);
+        tmem_ld_32x32b_x32(taddr + j * kHeads + 32, v1);
+        tmem_wait_ld();
+        float s = 0.f;
+#pragma unroll
+        for (int h = 0; h < 32; ++h) s = fmaf(wsm[j * kHeads + h], fmaxf(v0[h], 0.f), s);
+#pragma unroll
+        for (int h = 0; h < 32; ++h) s = fmaf(wsm[j * kHeads + 32 + h], fmaxf(v1[h], 0.f), s);
+        sc[j] = s;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->tmem_empty[ab]);
+
+      const int p = t * kTileTokens + row;
+#pragma unroll
+      for (int j = 0; j < NQ; ++j)
+        if (p < valid[j]) P.scores[(static_cast<size_t>(b) * NQ + j) * P.L_max + p] = sc[j];
+
+      if (prefetch) {
+        bool pass = false;
+#pragma unroll
+        for (int j = 0; j < NQ; ++j) pass |= (p < valid[j]) && (sc[j] > shat[j]);
+        int32_t h = -1;
+        bool cand = false;
+        if (pass) {
+          h = __ldg(P.req_to_host + static_cast<size_t>(b) * P.L_max + p);
+          if (h >= 0 && h < P.n_h) {
+            cand = P.host_to_gpu[h] == kInf;
+          } else {
+            set_status(P.status, ECHO_DEV_BAD_INDEX);
+          }
+        }
+        const uint32_t mask = __ballot_sync(0xffffffffu, cand);
+        if (mask) {
+          int n = 0, base = 0;
+          if (lane == 0) {
+            const int head = *reinterpret_cast<volatile int *>(&ctl->queue_head[e]);
+            const int room = kQueueCap - (tail - head);
+            n = __popc(mask);
+            n = n < room ? n : room;  // a full queue drops candidates: prefetch is best effort
+            if (n > 0) base = atomicAdd(P.stage_count + b, n);
+          }
+          n = __shfl_sync(0xffffffffu, n, 0);
+          base = __shfl_sync(0xffffffffu, base, 0);
+          int m = cap - base;  // tickets below the cap stage a row
+          m = m < 0 ? 0 : (m > n ? n : m);
+          const int rank = __popc(mask & ((1u << lane) - 1));
+          if (cand && rank < m)
+            ctl->queue[e][(tail + rank) % kQueueCap] = make_int2(h, b * P.stage_stride + base + rank);
+          if (lane == 0 && base + n > cap && n > 0) set_status(P.status, ECHO_DEV_PREFETCH_CAP_HIT);
+          __syncwarp();
+          tail += m;
+          if (lane == 0 && m > 0) {
+            __threadfence_block();
+            *reinterpret_cast<volatile int *>(&ctl->queue_tail[e]) = tail;
+          }
+        }
+      }
+      next_tile(P, b, t);
+    }
+    if (lane == 0) {
+      __threadfence_block();
+      *reinterpret_cast<volatile int *>(&ctl->queue_done[e]) = 1;
+    }
+  } else if (prefetch) {
+    // ===================== prefetch copies =====================
+    const int e = warp - 2 - kEpiWarps;
+    volatile int *vtail = &ctl->queue_tail[e];
+    volatile int *vhead = &ctl->queue_head[e];
+    volatile int *vdone = &ctl->queue_done[e];
+    const int4 *host = reinterpret_cast<const int4 *>(P.host_kv);
+    int4 *stage = reinterpret_cast<int4 *>(P.stage_rows);
+    int head = 0;
+    uint64_t idle_since = 0;
+    while (true) {
+      int tl = *vtail;
+      if (tl == head) {
+        if (*vdone) {
+          tl = *vtail;
+          if (tl == head) break;
+        } else {
+          const uint64_t now = globaltimer();
+          if (idle_since == 0) idle_since = now;
+          if (now - idle_since > kWaitLimitNs) {
+            set_status(P.status, ECHO_DEV_WAIT_TIMEOUT);
+            *abort = 1;
+            break;
+          }
+          __nanosleep(200);
+          continue;
+        }
+      }
+      idle_since = 0;
+      const int n = (tl - head) < kPfRowsPerBatch ? (tl - head) : kPfRowsPerBatch;
+      int32_t hr[kPfRowsPerBatch], dr[kPfRowsPerBatch];
+#pragma unroll
+      for (int r = 0; r < kPfRowsPerBatch; ++r) {
+        const volatile int2 *qe = reinterpret_cast<const volatile int2 *>(&ctl->queue[e][(head + r) % kQueueCap]);
+        hr[r] = r < n ? qe->x : 0;
+        dr[r] = r < n ? qe->y : 0;
+      }
+      constexpr int kPer = (kPfRowsPerBatch * kKvChunks + 31) / 32;  // 9 vectors per lane
+      int4 buf[kPer];
+#pragma unroll
+      for (int m = 0; m < kPer; ++m) {
+        const int idx = m * 32 + lane;
+        const int r = idx / kKvChunks, c = idx % kKvChunks;
+        if (r < n) buf[m] = __ldcs(host + static_cast<size_t>(hr[r]) * kKvChunks + c);
+      }
+#pragma unroll
+      for (int m = 0; m < kPer; ++m) {
+        const int idx = m * 32 + lane;
+        const int r = idx / kKvChunks, c = idx % kKvChunks;
+        if (r < n) stage[static_cast<size_t>(dr[r]) * kKvChunks + c] = buf[m];
+      }
+      if (lane < n) P.stage_host[dr[lane]] = hr[lane];
+      head += n;
+      __syncwarp();
+      if (lane == 0) *vhead = head;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace echo
+
+// ---------------------------------------------------------------------------
+// host launcher
+// ---------------------------------------------------------------------------
+namespace echo_host {
+
+using echo::IndexerCtl;
+
+typedef CUresult (*PFN_encodeTiled)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                    const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static PFN_encodeTiled encode_fn() {
+  static PFN_encodeTiled fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_encodeTiled>(p);
+  }
+  return fn;
+}
+
+// SM count of the current device (queried once per device, so that launches
+// made during stream capture issue no attribute queries)
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 1;
+  }
+  return cached[dev];
+}
+
+static size_t indexer_smem_bytes(int nq) {
+  return 1024 + echo::kStages * echo::kTileBytes + 2 * (echo::kHeads * nq * echo::kDim) + sizeof(IndexerCtl);
+}
+
+int launch_indexer(const echo_indexer_args *a, cudaStream_t stream) {
+  PFN_encodeTiled enc = encode_fn();
+  if (!enc) {
+    set_error("cuTensorMapEncodeTiled unavailable from the driver");
+    return ECHO_ECUDA;
+  }
+  const int nq = a->n_q;
+  CUtensorMap tk, tq;
+  {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(echo::kDim), static_cast<cuuint64_t>(a->L_max),
+                          static_cast<cuuint64_t>(a->B)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(echo::kDim),
+                             static_cast<cuuint64_t>(a->L_max) * echo::kDim};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(echo::kDim), static_cast<cuuint32_t>(echo::kTileTokens), 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = enc(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(a->k_index), dims, strides,
+                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+      set_error("tensor map for k_index failed (CUresult %d)", static_cast<int>(r));
+      return ECHO_ECUDA;
+    }
+  }
+  {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(echo::kDim),
+                          static_cast<cuuint64_t>(a->B) * nq * echo::kHeads};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(echo::kDim)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(echo::kDim), static_cast<cuuint32_t>(nq * echo::kHeads)};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = enc(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(a->q), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+      set_error("tensor map for q failed (CUresult %d)", static_cast<int>(r));
+      return ECHO_ECUDA;
+    }
+  }
+  echo::IndexerParams P{};
+  P.w = a->w;
+  P.ctx_len = a->ctx_len;
+  P.scores = a->scores;
+  P.B = a->B;
+  P.L_max = a->L_max;
+  P.status = a->dev_status;
+  if (a->s_hat) {
+    P.s_hat = a->s_hat;
+    P.req_to_host = a->req_to_host;
+    P.host_to_gpu = a->pool->host_token_to_gpu;
+    P.n_h = a->pool->n_h;
+    P.host_kv = a->pool->host_kv;
+    P.stage_rows = a->stage->rows;
+    P.stage_host = a->stage->host_row;
+    P.stage_count = a->stage->count;
+    P.stage_stride = a->stage->stride;
+    P.cap_div = a->stage->cap_div;
+  }
+  const long long tiles = static_cast<long long>(a->B) * ((a->L_max + echo::kTileTokens - 1) / echo::kTileTokens);
+  if (tiles == 0) return ECHO_OK;
+  const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
+  const size_t smem = indexer_smem_bytes(nq);
+  cudaError_t e;
+  if (nq == 1) {
+    static bool attr1 = false;
+    if (!attr1) {
+      e = cudaFuncSetAttribute(echo::indexer_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      if (e != cudaSuccess) return cuda_fail(e, "indexer smem attribute");
+      attr1 = true;
+    }
+    echo::indexer_kernel<1><<<grid, echo::kIndexerThreads, smem, stream>>>(tk, tq, P);
+  } else {
+    static bool attr2 = false;
+    if (!attr2) {
+      e = cudaFuncSetAttribute(echo::indexer_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      if (e != cudaSuccess) return cuda_fail(e, "indexer smem attribute");
+      attr2 = true;
+    }
+    echo::indexer_kernel<2><<<grid, echo::kIndexerThreads, smem, stream>>>(tk, tq, P);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "indexer launch");
+  return ECHO_OK;
+}
+
+}  // namespace echo_host

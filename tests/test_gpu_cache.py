@@ -1,0 +1,124 @@
+"""Cache manager and guaranteed recall on the GPU against the oracle: metadata,
+out_slot, statistics and GPU-pool bytes bit-exact on the same inputs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_attention_kv_fp8_gb300 as echo
+from sparse_attention_kv_fp8_gb300 import workload as wl
+from helpers import Case, dev, pinned_host_pool
+
+pytestmark = pytest.mark.gpu
+
+
+def test_pool_init_and_alloc_match_oracle():
+    n_g, n_h = 1000, 5000
+    host = wl.host_kv_pool(n_h, 1)
+    ht = pinned_host_pool(host)
+    P = echo.Pool(n_g, ht)
+    echo.echo_pool_init(P)
+    ws = echo.Workspace(n_g, 512)
+    O = oracle.Pool.empty(n_g, n_h, host.copy())
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    g = np.random.default_rng(1)
+    for it, n in enumerate((300, 0, 512, 400)):
+        rows = g.integers(0, n_h, size=512).astype(np.int32)
+        rows[5] = rows[3]          # a repeat
+        rows[7] = -4               # out of range
+        out = torch.empty(512, dtype=torch.int32, device="cuda")
+        echo.echo_pool_alloc(P, ws, dev(rows), dev(np.array([n], np.int32)), 10 + it, out, dev_status=st)
+        ref, rstatus = O.alloc(rows[:n], 10 + it)
+        torch.cuda.synchronize()
+        assert np.array_equal(out.cpu().numpy()[:n], ref)
+        m, o = P.metadata(), O.metadata()
+        for key in o:
+            assert np.array_equal(m[key], o[key]), (it, key)
+        assert (int(st.item()) & rstatus) == rstatus
+
+
+def test_evict_matches_oracle_and_moves_no_bytes():
+    c = Case(B=2, n_q=1, L_max=3000, ctx=3000, n_g=2000, n_resident=1900, clock=50, seed=3, k=64)
+    O = c.orc_pool
+    kv0 = c.pool.gpu_kv.clone()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for n, clock in ((0, 50), (37, 50), (600, 51), (5000, 52)):
+        echo.echo_pool_evict(c.pool, c.ws, dev(np.array([n], np.int32)), clock, dev_status=st)
+        ne, rs = O.evict(n, clock)
+        torch.cuda.synchronize()
+        c.assert_pool_equal(O, f"evict {n}")
+    assert int(st.item()) & echo.DEV_POOL_EXHAUSTED
+    assert torch.equal(c.pool.gpu_kv, kv0)
+
+
+def recall_and_compare(c: Case, sel: np.ndarray, clock: int, stage_rows=None):
+    out = torch.empty(sel.shape, dtype=torch.int32, device="cuda")
+    stats = echo.Stats()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    echo.echo_prefetch_recall(c.pool, c.ws, dev(sel), c.r2h_t, c.ctx, clock, out,
+                              stage=c.stage if stage_rows is not None else None, stats=stats, dev_status=st)
+    ost = oracle.Stats()
+    ref, rstatus = c.orc_pool.prefetch_recall(sel, c.r2h, clock, staged=stage_rows, stats=ost)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy(), ref)
+    c.assert_pool_equal(c.orc_pool, "recall")
+    assert int(st.item()) == rstatus
+    g, o = stats.as_dict(), ost.as_dict()
+    assert g == o, (g, o)
+    return out
+
+
+@pytest.mark.parametrize("B,n_q,L,k,n_g,res,seed", [
+    (1, 1, 4096, 256, 1024, 512, 1),       # the tiny workload: pool half full
+    (4, 1, 3000, 200, 1000, 1000, 2),      # full pool: eviction every step
+    (3, 2, 2000, 300, 1500, 1400, 3),      # two query tokens: de-duplicated union
+    (2, 1, 5000, 700, 900, 880, 4),        # misses exceed the pool: exhaustion
+])
+def test_recall_matches_oracle(B, n_q, L, k, n_g, res, seed):
+    c = Case(B, n_q, L, L, n_g, res, clock=100, seed=seed, k=k)
+    g = np.random.default_rng(seed)
+    for step in range(3):
+        scores = g.standard_normal((B, n_q, L)).astype(np.float32)
+        sel, _ = oracle.select_topk(scores, c.inp.ctx_len, k)
+        recall_and_compare(c, sel, clock=100 + step)
+
+
+def test_recall_uses_staged_rows_bytes_exact():
+    """Rows the prefetch staged are copied from the staging area; bytes still equal the host rows."""
+    c = Case(2, 1, 2000, 2000, 600, 500, clock=20, seed=6, k=150)
+    sel, _ = oracle.select_topk(np.random.default_rng(6).standard_normal((2, 1, 2000)).astype(np.float32),
+                                c.inp.ctx_len, 150)
+    staged = []
+    for b in range(2):
+        rows = [int(c.r2h[b, p]) for p in sel[b, 0][:60] if c.state.host_token_to_gpu[c.r2h[b, p]] == echo.INF]
+        rows += [int(c.r2h[b, 1999 - i]) for i in range(10)]      # staged but not selected
+        rows = [r for r in dict.fromkeys(rows) if c.state.host_token_to_gpu[r] == echo.INF][:c.stage_stride]
+        staged.append(rows)
+        c.stage.host_row[b, :len(rows)] = torch.tensor(rows, dtype=torch.int32)
+        c.stage.rows[b, :len(rows)] = torch.from_numpy(c.host_np[rows].view(np.int16)).cuda()
+        c.stage.count[b] = len(rows)
+    recall_and_compare(c, sel, 20, stage_rows=staged)
+    assert int(c.stage.count.sum()) == 0   # reset for the next step
+
+
+def test_append_matches_oracle():
+    B, L = 3, 500
+    c = Case(B, 1, L, [200, 499, 10], 300, 300, clock=9, seed=7, k=32)
+    kI = c.inp.k_index.copy()
+    ctx = c.inp.ctx_len.copy()
+    for step in range(3):
+        kv, kn = wl.new_tokens(B, 7, step)
+        stats = echo.Stats()
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        echo.echo_append(c.pool, c.ws, c.k_index, c.ctx, c.r2h_t, dev(kv.view(np.int16)), dev(kn), 9 + step,
+                         stats=stats, dev_status=st)
+        ost = oracle.Stats()
+        rs = c.orc_pool.append(kI, ctx, c.r2h, kv, kn, 9 + step, ost)
+        torch.cuda.synchronize()
+        assert int(st.item()) == rs
+        assert np.array_equal(c.ctx.cpu().numpy(), ctx)
+        assert np.array_equal(c.k_index.cpu().numpy(), kI)
+        assert np.array_equal(c.host_t.numpy().view(np.uint16), c.orc_pool.host_kv)
+        c.assert_pool_equal(c.orc_pool, f"append {step}")
+        assert stats.as_dict()["appended"] == ost.as_dict()["appended"]
+        assert stats.as_dict()["evicted"] == ost.as_dict()["evicted"]
