@@ -1,0 +1,420 @@
+"""Benchmark of the ECHO decode step on one GB300 (or N replicas).
+
+One step = one layer's decode step for a batch: FP8 lightning-indexer score with
+the fused prefetch -> exact top-k -> guaranteed recall (cache manager + host->HBM
+copies) -> EMA, on the DeepSeek-V3.2 decode shape: B = 8 requests, context
+L = 65536, k = 2048, latent KV 576 bf16 per token, host pool 1.8M rows pinned,
+GPU pool 200K slots (full at the start), consecutive-step top-k overlap 0.9.
+
+Each step replays a CUDA graph of the whole step (inputs resident in HBM); L2 is
+flushed between steps (a 256 MB write outside the timed events).  Prints one JSON
+line (rank 0).  `--impl reference` times the CPU oracle instead.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+B, L, K_TOP, N_H, N_G = 8, 65536, 2048, 1_800_000, 200_000
+CAP_DIV = 16
+T0 = 1000                  # step clock at the start (pre-resident rows carry older clocks)
+TARGET_OVERLAP = 0.9
+WORKLOAD = ("DeepSeek-V3.2 decode shape: 1 layer, B=8, L=65536, H_index=64, d_index=128 e4m3, k=2048, "
+            "latent KV 576 bf16, host pool 1.8M rows pinned, GPU pool 200K slots full at start, "
+            "consecutive top-k overlap 0.9")
+METRIC = "decode steps/s (indexer+select+recall, one layer)"
+L2_NOTE = "L2 flushed between steps (256 MB write outside the timed events)"
+
+
+def rho_for(L_: int, target: float) -> float:
+    path = os.path.join(ROOT, "tests", "golden", "rho_calibration.json")
+    try:
+        pts = json.load(open(path))["points"]
+        best = min(pts, key=lambda p: (abs(p["L"] - L_), abs(p["target_overlap"] - target)))
+        if best["L"] == L_ and abs(best["target_overlap"] - target) < 1e-9:
+            return float(best["rho"])
+    except (OSError, KeyError, ValueError):
+        pass
+    return 0.995
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.p = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.p is not None:
+            time.sleep(0.25)
+            self.p.terminate()
+            try:
+                self.out, _ = self.p.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.p.kill()
+                self.out = ""
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# workload
+# ---------------------------------------------------------------------------
+def build_inputs(n_steps: int, seed: int, host_out=None):
+    from sparse_attention_kv_fp8_gb300 import workload as wl
+    inp = wl.indexer_inputs(B, 1, L, L, seed=seed)
+    rho = rho_for(L, TARGET_OVERLAP)
+    qs = [inp.q]
+    qf = inp.q_float
+    for t in range(1, n_steps):
+        qf, q = wl.next_query(qf, rho, seed, t)
+        qs.append(q)
+    host = wl.host_kv_pool(N_H, seed, n_random=B * L, out=host_out)
+    r2h = wl.req_to_host(B, L)
+    rows = wl.random_resident_rows(B * L, N_G, seed)
+    st = wl.resident_pool(N_G, N_H, rows, wl.random_clocks(N_G, T0, seed), seed)
+    return inp, qs, host, r2h, st, rho
+
+
+def cpu_baseline_sample(inp, q, host, r2h, st, requests=1):
+    """Time the oracle's decode step for `requests` of the B requests (same state)."""
+    import oracle
+    b_sl = slice(0, requests)
+    P = oracle.Pool.from_state(st, host)
+    s_hat = np.full((requests, 1), np.inf, np.float32)
+    t = time.perf_counter()
+    oracle.decode_step(P, q[b_sl], inp.w[b_sl], inp.k_index[b_sl], inp.ctx_len[b_sl].copy(), r2h[b_sl], s_hat,
+                       K_TOP, clock=T0, stage_stride=L // CAP_DIV, cap_div=CAP_DIV)
+    return time.perf_counter() - t
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    steps = args.warmup + args.steps
+    host = np.zeros((N_H, 576), np.uint16)
+    inp, qs, host, r2h, st, rho = build_inputs(steps, seed=1, host_out=host)
+    times = []
+    for t in range(steps):
+        dt = cpu_baseline_sample(inp, qs[t], host, r2h, st, requests=1)
+        if t >= args.warmup:
+            times.append(dt)
+    per_step = float(np.mean(times)) * B     # one request sampled per step: scale to the batch
+    v = 1.0 / per_step
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "rho": rho},
+            "cpu_baseline": {"value": v, "unit": "steps/s", "cores": 1, "kind": "oracle",
+                             "sample": f"1 of the {B} requests per step (L={L}), scaled x{B}"},
+            "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import sparse_attention_kv_fp8_gb300 as echo
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        pg = dist
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        pass
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+
+    steps = args.warmup + args.steps
+    n_e2e = max(3, min(args.steps, 10))
+    seed = 1 + rank
+    host_t = torch.empty((N_H, echo.KV_ELEMS), dtype=torch.int16, pin_memory=True)
+    inp, qs, host_np, r2h, st, rho = build_inputs(steps + n_e2e + 1, seed, host_out=host_t.numpy().view(np.uint16))
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        dt = cpu_baseline_sample(inp, qs[0], host_np, r2h, st, requests=args.cpu_requests)
+        per_step = dt * B / args.cpu_requests
+        cpu = {"value": 1.0 / per_step, "unit": "steps/s", "cores": 1, "kind": "oracle",
+               "sample": f"{args.cpu_requests} of the {B} requests of one step (L={L}), {dt:.1f} s, scaled x{B / args.cpu_requests:g}"}
+
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    pool = echo.Pool(N_G, host_t)
+    pool.load_state(st)
+    ws = echo.Workspace(N_G, B * K_TOP)
+    stage = echo.Stage(B, L // CAP_DIV, CAP_DIV)
+    out = echo.StepBuffers(B, 1, L, K_TOP)
+    stats = echo.Stats()
+    q_ring = dev(np.stack(qs))                       # [steps][B][1][64][128]
+    w = dev(inp.w)
+    k_index = dev(inp.k_index)
+    ctx = dev(inp.ctx_len)
+    r2h_t = dev(r2h)
+    s_hat = torch.full((B, 1), float("inf"), dtype=torch.float32, device="cuda")
+    clock = torch.tensor([T0], dtype=torch.int32, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def new_events():
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(echo.NUM_STAGES + 1)]
+        for e in evs:
+            e.record()
+        return evs
+
+    def args_for(t, events=None, q=None):
+        return echo.make_step_args(pool, ws, q if q is not None else q_ring[t], w, k_index, ctx, r2h_t, K_TOP, out,
+                                   stage=stage, s_hat=s_hat, clock_dev=clock, advance_clock=True, stats=stats,
+                                   events=events)
+
+    # step 0 eagerly (first calls set kernel attributes), then one graph per step
+    echo.echo_decode_step(args_for(0))
+    torch.cuda.synchronize()
+    graphs, stage_ev, keep = [None], [None], []
+    cap_stream = torch.cuda.Stream()
+    for t in range(1, steps):
+        evs = new_events()
+        a = args_for(t, events=evs)
+        g = torch.cuda.CUDAGraph()
+        cap_stream.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(cap_stream):
+            with torch.cuda.graph(g, stream=cap_stream):
+                echo.echo_decode_step(a)
+        torch.cuda.current_stream().wait_stream(cap_stream)
+        graphs.append(g)
+        stage_ev.append(evs)
+        keep.append(a)
+    torch.cuda.synchronize()
+    for t in range(1, args.warmup):
+        flush.zero_()
+        graphs[t].replay()
+    torch.cuda.synchronize()
+    stats.t.zero_()
+    out.dev_status.zero_()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i, t in enumerate(range(max(1, args.warmup), max(1, args.warmup) + args.steps)):
+            flush.zero_()
+            starts[i].record()
+            graphs[t].replay()
+            ends[i].record()
+        torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    timed = list(range(max(1, args.warmup), max(1, args.warmup) + args.steps))
+    stage_ms = {name: [stage_ev[t][i].elapsed_time(stage_ev[t][i + 1]) for t in timed]
+                for i, name in enumerate(("append", "indexer", "topk", "recall", "ema"))}
+    st_vals = stats.as_dict()
+    status = int(out.dev_status.item())
+    total_ms = float(np.sum(step_ms))
+    if pg:
+        tt = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
+        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / args.steps
+    value = world * args.steps / (total_ms / 1e3)
+
+    # ---- e2e: the C-ABI call with host buffers (q, w in; out_slot, status out) ----
+    q_host = torch.empty((B, 1, 64, 128), dtype=torch.uint8, pin_memory=True)
+    w_host = torch.from_numpy(inp.w.copy()).pin_memory()
+    slot_host = torch.empty((B, 1, K_TOP), dtype=torch.int32, pin_memory=True)
+    stat_host = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    q_dev = torch.empty_like(q_ring[0])
+    ea = args_for(0, q=q_dev)
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
+    for i in range(n_e2e):
+        q_host.numpy()[...] = qs[steps + i]
+        flush.zero_()
+        e_s[i].record()
+        q_dev.copy_(q_host, non_blocking=True)
+        w.copy_(w_host, non_blocking=True)
+        echo.echo_decode_step(ea)
+        slot_host.copy_(out.out_slot, non_blocking=True)
+        stat_host.copy_(out.dev_status, non_blocking=True)
+        e_e[i].record()
+        torch.cuda.synchronize()
+    e2e_ms = float(np.mean([s.elapsed_time(e) for s, e in zip(e_s, e_e)]))
+    h2d = q_host.numel() + w_host.numel() * 4
+    d2h = slot_host.numel() * 4 + 4
+
+    # ---- host-link denominators: pinned H2D copy (copy engine), best of 10 ----
+    src = torch.empty(256 << 20, dtype=torch.uint8, pin_memory=True)
+    dst = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    best = 1e9
+    for _ in range(10):
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record()
+        dst.copy_(src, non_blocking=True)
+        a1.record()
+        torch.cuda.synchronize()
+        best = min(best, a0.elapsed_time(a1))
+    h2d_gbs = (256 << 20) / (best * 1e-3) / 1e9
+    recall_probe = recall_bandwidth_probe(echo, torch, host_t, flush)
+
+    # ---- roofline of the dominant kernel (the indexer) ----
+    idx_ms = float(np.mean(stage_ms["indexer"]))
+    idx_bytes = B * L * 128 + B * L * 4 + B * (64 * 128 + 64 * 4)       # k_index + scores + q/w per launch
+    achieved = idx_bytes / (idx_ms * 1e-3) / 1e9
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "indexer_traffic.json")
+    if os.path.exists(prof):
+        try:
+            traffic = json.load(open(prof)).get("bytes_per_launch_full_shape")
+        except (OSError, ValueError):
+            traffic = None
+    recalled_rows = st_vals["recalled"]
+    recall_ms = float(np.mean(stage_ms["recall"]))
+    hits, uniq = st_vals["hits"], max(1, st_vals["unique_rows"])
+    line = {
+        "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 (indexer); int32 metadata; bf16 bytes",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "l2": L2_NOTE, "rho": rho, "graph": "one CUDA graph per step",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "scored_tokens_per_s": value * B * L,
+        "hit_rate": hits / uniq,
+        "recalled_rows_per_step": recalled_rows / args.steps,
+        "staged_rows_per_step": st_vals["staged"] / args.steps,
+        "staged_used_per_step": st_vals["staged_used"] / args.steps,
+        "stage_ms": {k: float(np.mean(v)) for k, v in stage_ms.items()},
+        "recall": {"bytes_per_step": recalled_rows / args.steps * 1152, "ms": recall_ms,
+                   "probe": recall_probe, "h2d_gbs_copy_engine": h2d_gbs},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": traffic, "kernel": "indexer_kernel<1>",
+                     "peak_source": peak_src, "bytes_per_launch": idx_bytes},
+        "cpu_baseline": cpu,
+        "e2e": {"value": 1e3 / e2e_ms, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "how": "echo_decode_step (C ABI, eager) with q/w copied in from pinned host and out_slot/status "
+                       "copied back, per step"},
+        "gpu_launches": 6 * args.steps,
+        "clocks": clk.summary(),
+        "dev_status": status,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+def recall_bandwidth_probe(echo, torch, host_t, flush, rows=65536, n_g=65536):
+    """Recall of `rows` distinct non-resident host rows into an empty pool, prefetch
+    off: host-link bytes over the copy time (the recall call's three kernels)."""
+    pool = echo.Pool(n_g, host_t)
+    echo.echo_pool_init(pool)
+    ws = echo.Workspace(n_g, rows)
+    g = np.random.default_rng(5)
+    pick = np.sort(g.choice(B * L, size=rows, replace=False)).astype(np.int32)
+    r2h = torch.from_numpy(pick.reshape(1, rows)).cuda()
+    sel = torch.arange(rows, dtype=torch.int32, device="cuda").view(1, 1, rows)
+    ctx = torch.tensor([rows], dtype=torch.int32, device="cuda")
+    out = torch.empty_like(sel)
+    best = 1e9
+    for it in range(4):
+        echo.echo_pool_init(pool)
+        flush.zero_()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record()
+        echo.echo_prefetch_recall(pool, ws, sel, r2h, ctx, 10 + it, out)
+        a1.record()
+        torch.cuda.synchronize()
+        best = min(best, a0.elapsed_time(a1))
+    ok = bool((out >= 0).all().item())
+    return {"rows": rows, "bytes": rows * 1152, "ms": best, "gbs": rows * 1152 / (best * 1e-3) / 1e9, "all_recalled": ok}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-requests", type=int, default=1)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

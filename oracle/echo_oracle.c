@@ -83,12 +83,11 @@ static int valid_len(int L, int n_q, int j)
     return v < 0 ? 0 : v;
 }
 
-float orc_indexer_score_one(const uint8_t *q, const float *w, const uint8_t *k_index,
-                            int n_q, int L_max, int H, int D, int b, int j, int p)
+/* score of token p for query (b, j), given the query already decoded to qd[H][D] */
+static float score_token(const double *qd, const float *wb, const uint8_t *kp, int H, int D, double *kd)
 {
-    const uint8_t *qb = q + ((size_t)b * n_q + j) * H * D;
-    const float *wb = w + ((size_t)b * n_q + j) * H;
-    const uint8_t *kp = k_index + ((size_t)b * L_max + p) * D;
+    for (int d = 0; d < D; ++d)
+        kd[d] = orc_e4m3_value(kp[d]);
     double s = 0.0;
     for (int h = 0; h < H; ++h) {
         /* e4m3 values are multiples of 2^-9 with |x| <= 448; with |x| <= 8 the
@@ -96,11 +95,29 @@ float orc_indexer_score_one(const uint8_t *q, const float *w, const uint8_t *k_i
            inside 53 bits, so this fp64 dot product is exact */
         double dot = 0.0;
         for (int d = 0; d < D; ++d)
-            dot += orc_e4m3_value(qb[(size_t)h * D + d]) * orc_e4m3_value(kp[d]);
+            dot += qd[(size_t)h * D + d] * kd[d];
         double relu = dot > 0.0 ? dot : 0.0;
         s += (double)wb[h] * relu;
     }
     return (float)s;
+}
+
+static void decode_query(const uint8_t *q, int H, int D, double *qd)
+{
+    for (int i = 0; i < H * D; ++i)
+        qd[i] = orc_e4m3_value(q[i]);
+}
+
+float orc_indexer_score_one(const uint8_t *q, const float *w, const uint8_t *k_index,
+                            int n_q, int L_max, int H, int D, int b, int j, int p)
+{
+    double *qd = (double *)malloc(sizeof(double) * (size_t)H * D);
+    double *kd = (double *)malloc(sizeof(double) * (size_t)D);
+    decode_query(q + ((size_t)b * n_q + j) * H * D, H, D, qd);
+    float s = score_token(qd, w + ((size_t)b * n_q + j) * H, k_index + ((size_t)b * L_max + p) * D, H, D, kd);
+    free(qd);
+    free(kd);
+    return s;
 }
 
 /* scores[b][j][p] for p < valid_len(ctx_len[b], n_q, j); other entries untouched */
@@ -108,13 +125,19 @@ void orc_indexer_score(const uint8_t *q, const float *w, const uint8_t *k_index,
                        const int32_t *ctx_len, int B, int n_q, int L_max, int H, int D,
                        float *scores)
 {
+    double *qd = (double *)malloc(sizeof(double) * (size_t)H * D);
+    double *kd = (double *)malloc(sizeof(double) * (size_t)D);
     for (int b = 0; b < B; ++b)
         for (int j = 0; j < n_q; ++j) {
             int v = valid_len(ctx_len[b], n_q, j);
+            decode_query(q + ((size_t)b * n_q + j) * H * D, H, D, qd);
+            const float *wb = w + ((size_t)b * n_q + j) * H;
             for (int p = 0; p < v; ++p)
                 scores[((size_t)b * n_q + j) * L_max + p] =
-                    orc_indexer_score_one(q, w, k_index, n_q, L_max, H, D, b, j, p);
+                    score_token(qd, wb, k_index + ((size_t)b * L_max + p) * D, H, D, kd);
         }
+    free(qd);
+    free(kd);
 }
 
 /* ------------------------------------------------------------------------- */

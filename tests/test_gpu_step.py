@@ -156,9 +156,11 @@ def test_lossless_selection_and_pool_independent_of_the_prediction():
     """Section 6.1's lossless claim on the GPU: threshold -inf (prefetch up to the cap),
     +inf (no prefetch) and the EMA give identical selections, slots, metadata and bytes."""
     results = []
-    for s0 in (float("-inf"), float("inf"), 150.0):
+    # prediction -inf (stays -inf under the EMA: prefetch up to the cap every step),
+    # no prefetch at all, and the EMA started from +inf
+    for s0, prefetch in ((float("-inf"), True), (float("inf"), False), (float("inf"), True)):
         c = Case(2, 1, 6000, 6000, 3000, 3000, clock=500, seed=21, k=400)
-        R = StepRunner(c, s_hat0=s0, append=True)   # -inf stays -inf under the EMA
+        R = StepRunner(c, s_hat0=s0, append=True, prefetch=prefetch)
         qf = c.inp.q_float
         outs = []
         for step in range(4):
@@ -174,7 +176,7 @@ def test_lossless_selection_and_pool_independent_of_the_prediction():
         for key in meta:
             assert np.array_equal(results[0][1][key], meta[key]), key
         assert np.array_equal(results[0][2], kv)
-    assert results[0][3]["staged"] > 0 and results[1][3]["staged"] == 0
+    assert results[0][3]["staged"] > 0 and results[1][3]["staged"] == 0 and results[2][3]["staged"] > 0
 
 
 def test_graph_replay_equals_eager():
