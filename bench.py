@@ -7,7 +7,8 @@ L = 65536, k = 2048, latent KV 576 bf16 per token, host pool 1.8M rows pinned,
 GPU pool 200K slots (full at the start), consecutive-step top-k overlap 0.9.
 
 Each step replays a CUDA graph of the whole step (inputs resident in HBM); L2 is
-flushed between steps (a 256 MB write outside the timed events).  Prints one JSON
+flushed between steps (a 256 MB write, then a 256 MB read, outside the timed
+events).  Prints one JSON
 line (rank 0).  `--impl reference` times the CPU oracle instead.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -35,7 +36,7 @@ WORKLOAD = ("DeepSeek-V3.2 decode shape: 1 layer, B=8, L=65536, H_index=64, d_in
             "latent KV 576 bf16, host pool 1.8M rows pinned, GPU pool 200K slots full at start, "
             "consecutive top-k overlap 0.9")
 METRIC = "decode steps/s (indexer+select+recall, one layer)"
-L2_NOTE = "L2 flushed between steps (256 MB write outside the timed events)"
+L2_NOTE = "L2 flushed between steps outside the timed events (256 MB write, then 256 MB read)"
 
 
 def rho_for(L_: int, target: float) -> float:
@@ -199,7 +200,8 @@ def run_ours(args):
     n_e2e = max(3, min(args.steps, 10))
     seed = 1 + rank
     host_t = torch.empty((N_H, echo.KV_ELEMS), dtype=torch.int16, pin_memory=True)
-    inp, qs, host_np, r2h, st, rho = build_inputs(steps + n_e2e + 1, seed, host_out=host_t.numpy().view(np.uint16))
+    inp, qs, host_np, r2h, st, rho = build_inputs(steps + min(args.steps, 10) + n_e2e + 1, seed,
+                                                  host_out=host_t.numpy().view(np.uint16))
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -225,6 +227,13 @@ def run_ours(args):
     s_hat = torch.full((B, 1), float("inf"), dtype=torch.float32, device="cuda")
     clock = torch.tensor([T0], dtype=torch.int32, device="cuda")
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    flush_rd = torch.ones(64 << 20, dtype=torch.int32, device="cuda")
+
+    def flush_l2():
+        # write a buffer larger than L2, then read another one, so each step starts
+        # with an L2 that holds none of the step's data and no dirty lines
+        flush.zero_()
+        torch.amax(flush_rd)
 
     def new_events():
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(echo.NUM_STAGES + 1)]
@@ -237,13 +246,16 @@ def run_ours(args):
                                    stage=stage, s_hat=s_hat, clock_dev=clock, advance_clock=True, stats=stats,
                                    events=events)
 
-    # step 0 eagerly (first calls set kernel attributes), then one graph per step
+    # step 0 eagerly (first calls set kernel attributes), then one graph per step:
+    # plain graphs for the headline loop, graphs with stage events (external event
+    # nodes, about 2 us each) for the per-stage breakdown loop that follows it
+    n_stage = min(args.steps, 10)
     echo.echo_decode_step(args_for(0))
     torch.cuda.synchronize()
-    graphs, stage_ev, keep = [None], [None], []
+    graphs, stage_ev, keep = {}, {}, []
     cap_stream = torch.cuda.Stream()
-    for t in range(1, steps):
-        evs = new_events()
+    for t in range(1, steps + n_stage):
+        evs = new_events() if t >= steps else None
         a = args_for(t, events=evs)
         g = torch.cuda.CUDAGraph()
         cap_stream.wait_stream(torch.cuda.current_stream())
@@ -251,37 +263,43 @@ def run_ours(args):
             with torch.cuda.graph(g, stream=cap_stream):
                 echo.echo_decode_step(a)
         torch.cuda.current_stream().wait_stream(cap_stream)
-        graphs.append(g)
-        stage_ev.append(evs)
+        graphs[t] = g
+        stage_ev[t] = evs
         keep.append(a)
     torch.cuda.synchronize()
     for t in range(1, args.warmup):
-        flush.zero_()
+        flush_l2()
         graphs[t].replay()
     torch.cuda.synchronize()
     stats.t.zero_()
     out.dev_status.zero_()
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    def timed_loop(ts):
+        st = [torch.cuda.Event(enable_timing=True) for _ in ts]
+        en = [torch.cuda.Event(enable_timing=True) for _ in ts]
+        for i, t in enumerate(ts):
+            flush_l2()
+            st[i].record()
+            graphs[t].replay()
+            en[i].record()
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in zip(st, en)]
+
+    timed = list(range(args.warmup, args.warmup + args.steps))
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        for i, t in enumerate(range(max(1, args.warmup), max(1, args.warmup) + args.steps)):
-            flush.zero_()
-            starts[i].record()
-            graphs[t].replay()
-            ends[i].record()
-        torch.cuda.synchronize()
+        step_ms = timed_loop(timed)
     if pg:
         pg.barrier()
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    timed = list(range(max(1, args.warmup), max(1, args.warmup) + args.steps))
-    stage_ms = {name: [stage_ev[t][i].elapsed_time(stage_ev[t][i + 1]) for t in timed]
-                for i, name in enumerate(("append", "indexer", "topk", "recall", "ema"))}
     st_vals = stats.as_dict()
     status = int(out.dev_status.item())
+    staged_steps = list(range(steps, steps + n_stage))
+    staged_total_ms = timed_loop(staged_steps)
+    stage_ms = {name: [stage_ev[t][i].elapsed_time(stage_ev[t][i + 1]) for t in staged_steps]
+                for i, name in enumerate(("append", "indexer", "topk", "recall", "ema"))}
+    status |= int(out.dev_status.item())
     total_ms = float(np.sum(step_ms))
     if pg:
         tt = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
@@ -300,8 +318,8 @@ def run_ours(args):
     e_s = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
     e_e = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
     for i in range(n_e2e):
-        q_host.numpy()[...] = qs[steps + i]
-        flush.zero_()
+        q_host.numpy()[...] = qs[steps + n_stage + i]
+        flush_l2()
         e_s[i].record()
         q_dev.copy_(q_host, non_blocking=True)
         w.copy_(w_host, non_blocking=True)
@@ -326,7 +344,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         best = min(best, a0.elapsed_time(a1))
     h2d_gbs = (256 << 20) / (best * 1e-3) / 1e9
-    recall_probe = recall_bandwidth_probe(echo, torch, host_t, flush)
+    recall_probe = recall_bandwidth_probe(echo, torch, host_t, flush_l2)
 
     # ---- roofline of the dominant kernel (the indexer) ----
     idx_ms = float(np.mean(stage_ms["indexer"]))
@@ -355,6 +373,7 @@ def run_ours(args):
         "staged_rows_per_step": st_vals["staged"] / args.steps,
         "staged_used_per_step": st_vals["staged_used"] / args.steps,
         "stage_ms": {k: float(np.mean(v)) for k, v in stage_ms.items()},
+        "stage_ms_note": f"from {n_stage} further steps replayed with stage events ({float(np.mean(staged_total_ms)):.4f} ms/step with the events)",
         "recall": {"bytes_per_step": recalled_rows / args.steps * 1152, "ms": recall_ms,
                    "probe": recall_probe, "h2d_gbs_copy_engine": h2d_gbs},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
@@ -375,7 +394,7 @@ def run_ours(args):
     return 0
 
 
-def recall_bandwidth_probe(echo, torch, host_t, flush, rows=65536, n_g=65536):
+def recall_bandwidth_probe(echo, torch, host_t, flush_l2, rows=65536, n_g=65536):
     """Recall of `rows` distinct non-resident host rows into an empty pool, prefetch
     off: host-link bytes over the copy time (the recall call's three kernels)."""
     pool = echo.Pool(n_g, host_t)
@@ -390,7 +409,7 @@ def recall_bandwidth_probe(echo, torch, host_t, flush, rows=65536, n_g=65536):
     best = 1e9
     for it in range(4):
         echo.echo_pool_init(pool)
-        flush.zero_()
+        flush_l2()
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a0.record()
         echo.echo_prefetch_recall(pool, ws, sel, r2h, ctx, 10 + it, out)
@@ -401,6 +420,38 @@ def recall_bandwidth_probe(echo, torch, host_t, flush, rows=65536, n_g=65536):
     return {"rows": rows, "bytes": rows * 1152, "ms": best, "gbs": rows * 1152 / (best * 1e-3) / 1e9, "all_recalled": ok}
 
 
+def run_kernel_case(args):
+    """Small single-kernel case for profilers: the indexer (with the fused prefetch,
+    threshold = each row's k-th score) on B x L tokens, `--reps` launches."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import sparse_attention_kv_fp8_gb300 as echo
+    from sparse_attention_kv_fp8_gb300 import workload as wl
+    Bk, Lk = args.B, args.L
+    inp = wl.indexer_inputs(Bk, 1, Lk, Lk, seed=3)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    n_h = Bk * Lk
+    host_t = torch.zeros((n_h, echo.KV_ELEMS), dtype=torch.int16, pin_memory=True)
+    pool = echo.Pool(min(n_h, 200_000), host_t)
+    echo.echo_pool_init(pool)
+    stage = echo.Stage(Bk, Lk // CAP_DIV, CAP_DIV)
+    q, w, k_index, ctx, r2h = dev(inp.q), dev(inp.w), dev(inp.k_index), dev(inp.ctx_len), dev(wl.req_to_host(Bk, Lk))
+    scores = torch.empty((Bk, 1, Lk), dtype=torch.float32, device="cuda")
+    sel = torch.empty((Bk, 1, K_TOP), dtype=torch.int32, device="cuda")
+    kth = torch.empty((Bk, 1), dtype=torch.float32, device="cuda")
+    echo.echo_indexer_score(q, w, k_index, ctx, scores)
+    echo.echo_select_topk(scores, ctx, K_TOP, sel, kth)
+    for _ in range(args.reps):
+        stage.count.zero_()
+        echo.echo_indexer_score(q, w, k_index, ctx, scores, s_hat=kth, req_to_host=r2h, pool=pool, stage=stage)
+    torch.cuda.synchronize()
+    print(json.dumps({"kernel_case": "indexer", "B": Bk, "L": Lk, "reps": args.reps,
+                      "staged": int(stage.count.clamp(max=Lk // CAP_DIV).sum().item())}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -409,8 +460,15 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-requests", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", default=None, choices=[None, "indexer"],
+                    help="run one kernel on a small case (for profilers) instead of the benchmark")
+    ap.add_argument("--B", type=int, default=24)
+    ap.add_argument("--L", type=int, default=65536)
+    ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.kernel:
+        return run_kernel_case(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -47,26 +47,31 @@ def _headers():
         [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), lib_path: str | None = None,
+          build_dir: str | None = None) -> str:
+    """Compile csrc/*.cu and link the shared library (default: the product build).
+    `extra_flags`, `lib_path` and `build_dir` give a separate development build."""
+    lib_out = lib_path or LIB_PATH
+    bdir = build_dir or BUILD_DIR
+    os.makedirs(bdir, exist_ok=True)
     hdrs = _headers()
     objs = []
     jobs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        o = os.path.join(bdir, src.replace(".cu", ".o"))
         objs.append(o)
         if force or _stale(o, [s] + hdrs):
             jobs.append((s, o))
 
     def compile_one(so):
         s, o = so
-        cmd = [nvcc()] + _flags() + ["-c", s, "-o", o + ".tmp"]
+        cmd = [nvcc()] + _flags() + list(extra_flags) + ["-c", s, "-o", o + ".tmp"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {os.path.basename(s)}:\n{r.stderr}")
         os.replace(o + ".tmp", o)
-        log = os.path.join(BUILD_DIR, os.path.basename(s) + ".ptxas.txt")
+        log = os.path.join(bdir, os.path.basename(s) + ".ptxas.txt")
         with open(log, "w") as f:
             f.write(r.stderr)
         return r.stderr
@@ -76,14 +81,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
             for out in ex.map(compile_one, jobs):
                 if verbose:
                     print(out)
-    if force or jobs or _stale(LIB_PATH, objs):
-        tmp = LIB_PATH + f".tmp{os.getpid()}"
+    if force or jobs or _stale(lib_out, objs):
+        tmp = lib_out + f".tmp{os.getpid()}"
         cmd = [nvcc()] + ARCH + ["-shared", "-Xcompiler", "-fPIC", "-o", tmp] + objs + ["-lcudart_static", "-lrt", "-ldl", "-lpthread"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stderr}")
-        os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+        os.replace(tmp, lib_out)
+    return lib_out
 
 
 if __name__ == "__main__":

@@ -27,17 +27,11 @@
 //   copy   (grid-wide)  moves each recalled row (1152 B, 16-byte vectors, several
 //                       rows in flight per warp) from the staging area or the
 //                       pinned host pool into its slot and writes out_slot.
-#include <cooperative_groups.h>
+#include "cluster_select.cuh"
 
-#include "echo_common.cuh"
-
-namespace cg = cooperative_groups;
+ECHO_TRACE_UNIT(cache_mgr)
 
 namespace echo {
-
-constexpr int kPlanCluster = 8;
-constexpr int kPlanThreads = 1024;
-constexpr int kPlanWarps = kPlanThreads / 32;
 
 enum PlanMode { kModeRecall = 0, kModeAlloc = 1, kModeAppend = 2, kModeEvict = 3 };
 
@@ -177,97 +171,55 @@ __global__ void claim_kernel(const PlanParams P) {
 }
 
 // ---------------------------------------------------------------------------
-// plan: one cluster of kPlanCluster CTAs
+// plan: one thread-block cluster; every CTA stages its slice of the slots in
+// shared memory as one key per slot:
+//   kFreeKey          free slot
+//   kProtKey          occupied and not evictable (priority >= clock: protected)
+//   priority          occupied and evictable
 // ---------------------------------------------------------------------------
-struct PlanSmem {
-  uint32_t hist[2048];
-  uint32_t tot[2048];
-  uint32_t wa[kPlanWarps], wb[kPlanWarps];
-  uint32_t cta_a, cta_b;
-  uint32_t digit, below;
-};
+constexpr uint32_t kFreeKey = 0xFFFFFFFFu;
+constexpr uint32_t kProtKey = 0xFFFFFFFEu;
+constexpr int kPlanMaxChunk = 48 * 1024;  // slots per CTA (shared memory)
 
-// exclusive block scan of two counters; totals in ta/tb
-__device__ __forceinline__ void plan_scan2(uint32_t a, uint32_t b, uint32_t &ea, uint32_t &eb, uint32_t &ta,
-                                           uint32_t &tb, PlanSmem *S) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t ia = a, ib = b;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    uint32_t xa = __shfl_up_sync(0xffffffffu, ia, o), xb = __shfl_up_sync(0xffffffffu, ib, o);
-    if (lane >= o) {
-      ia += xa;
-      ib += xb;
-    }
-  }
-  if (lane == 31) {
-    S->wa[warp] = ia;
-    S->wb[warp] = ib;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    uint32_t x = S->wa[lane], y = S->wb[lane];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      uint32_t xa = __shfl_up_sync(0xffffffffu, x, o), xb = __shfl_up_sync(0xffffffffu, y, o);
-      if (lane >= o) {
-        x += xa;
-        y += xb;
-      }
-    }
-    S->wa[lane] = x;
-    S->wb[lane] = y;
-  }
-  __syncthreads();
-  ea = (warp ? S->wa[warp - 1] : 0) + ia - a;
-  eb = (warp ? S->wb[warp - 1] : 0) + ib - b;
-  ta = S->wa[kPlanWarps - 1];
-  tb = S->wb[kPlanWarps - 1];
-  __syncthreads();
-}
-
-// cluster-wide exclusive prefix of this CTA's totals (a, b) over lower ranks, and the grand totals
-__device__ __forceinline__ void cluster_prefix2(cg::cluster_group &cluster, PlanSmem *S, uint32_t ta, uint32_t tb,
-                                                uint32_t &pa, uint32_t &pb, uint32_t &ga, uint32_t &gb) {
-  if (threadIdx.x == 0) {
-    S->cta_a = ta;
-    S->cta_b = tb;
-  }
-  cluster.sync();
-  const int rank = static_cast<int>(cluster.block_rank());
-  pa = pb = ga = gb = 0;
-  for (int r = 0; r < kPlanCluster; ++r) {
-    PlanSmem *R = cluster.map_shared_rank(S, r);
-    const uint32_t x = R->cta_a, y = R->cta_b;
-    if (r < rank) {
-      pa += x;
-      pb += y;
-    }
-    ga += x;
-    gb += y;
-  }
-  cluster.sync();  // the per-CTA totals may be overwritten after this
-}
-
-__global__ void __cluster_dims__(kPlanCluster, 1, 1) __launch_bounds__(kPlanThreads, 1)
-    plan_kernel(const PlanParams P) {
-  cg::cluster_group cluster = cg::this_cluster();
-  const int rank = static_cast<int>(cluster.block_rank());
-  __shared__ PlanSmem S_;
-  PlanSmem *S = &S_;
+__global__ void __launch_bounds__(kSelThreads, 1) plan_kernel(const PlanParams P) {
+  cg::cluster_group cl = cg::this_cluster();
+  const int rank = static_cast<int>(cl.block_rank());
+  const int C = static_cast<int>(cl.num_blocks());
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  SelSmem *S = reinterpret_cast<SelSmem *>(smem_raw);
+  uint32_t *keys = reinterpret_cast<uint32_t *>(smem_raw + sizeof(SelSmem));
   const int32_t clock = read_clock(P);
   const int n_g = P.pool.n_g;
   const int32_t n_free0 = P.pool.counters[0];
   const int32_t prev_idx = P.pool.counters[1];
+  ECHO_TRACE_MARK(0);
+
+  // ===== this CTA's slots, staged =====
+  const int sc = (n_g + C - 1) / C;
+  const int lo = rank * sc < n_g ? rank * sc : n_g;
+  const int hi = lo + sc < n_g ? lo + sc : n_g;
+  const int nloc = hi - lo;
+  for (int i = threadIdx.x; i < nloc; i += kSelThreads) {
+    const int32_t pr = P.pool.prio[lo + i];
+    keys[i] = P.pool.free_[lo + i] ? kFreeKey
+                                   : ((pr >= 0 && pr < clock) ? static_cast<uint32_t>(pr) : kProtKey);
+  }
+  __syncthreads();
+  // contiguous per-thread segments of the slice, odd length (conflict-free reads)
+  int seg = (nloc + kSelThreads - 1) / kSelThreads;
+  seg |= 1;
+  const int t0 = threadIdx.x * seg < nloc ? threadIdx.x * seg : nloc;
+  const int t1 = t0 + seg < nloc ? t0 + seg : nloc;
+  ECHO_TRACE_MARK(1);
 
   // ===== phase A: owned misses in entry order (and unique hits) =====
   uint32_t M = 0, n_sel = 0, n_hit = 0;
   if (P.mode != kModeEvict) {
     const int n = entries_count(P);
-    const int c0 = static_cast<int>((static_cast<long long>(n) * rank) / kPlanCluster);
-    const int c1 = static_cast<int>((static_cast<long long>(n) * (rank + 1)) / kPlanCluster);
-    const int per = (c1 - c0 + kPlanThreads - 1) / kPlanThreads;
-    const int s0 = c0 + threadIdx.x * per;
+    const int c0 = static_cast<int>((static_cast<long long>(n) * rank) / C);
+    const int c1 = static_cast<int>((static_cast<long long>(n) * (rank + 1)) / C);
+    const int per = (c1 - c0 + kSelThreads - 1) / kSelThreads;
+    const int s0 = c0 + threadIdx.x * per < c1 ? c0 + threadIdx.x * per : c1;
     const int s1 = s0 + per < c1 ? s0 + per : c1;
     uint32_t own = 0, hits = 0, valid = 0;
     for (int f = s0; f < s1; ++f) {
@@ -287,12 +239,12 @@ __global__ void __cluster_dims__(kPlanCluster, 1, 1) __launch_bounds__(kPlanThre
         set_status(P.status, ECHO_DEV_BAD_INDEX);
       }
     }
-    uint32_t ex_own, ex_hit, t_own, t_hit;
-    plan_scan2(own, hits, ex_own, ex_hit, t_own, t_hit, S);
-    uint32_t pre_own, pre_hit, g_own, g_hit;
-    cluster_prefix2(cluster, S, t_own, t_hit, pre_own, pre_hit, g_own, g_hit);
+    uint32_t ex_own, ex_val, t_own, t_val;
+    sel_block_scan2(own, valid, ex_own, ex_val, t_own, t_val, S);
+    uint32_t pre_own, pre_val, g_own, g_val;
+    sel_cluster_prefix2(cl, S, t_own, t_val, pre_own, pre_val, g_own, g_val);
     M = g_own;
-    n_hit = g_hit;
+    n_sel = g_val;
     uint32_t r = pre_own + ex_own;
     for (int f = s0; f < s1; ++f) {
       const int32_t h = entry_row(P, f, n, false);
@@ -303,20 +255,22 @@ __global__ void __cluster_dims__(kPlanCluster, 1, 1) __launch_bounds__(kPlanThre
         ++r;
       }
     }
-    // selected-entry count for the statistics
-    uint32_t ev, dv, tv, td;
-    plan_scan2(valid, 0, ev, dv, tv, td, S);
-    uint32_t pv, pd, gv, gd;
-    cluster_prefix2(cluster, S, tv, 0, pv, pd, gv, gd);
-    n_sel = gv;
+    if (P.mode == kModeRecall) {
+      uint32_t eh, dz, th, tz;
+      sel_block_scan2(hits, 0, eh, dz, th, tz, S);
+      uint32_t ph, pz, gh, gz;
+      sel_cluster_prefix2(cl, S, th, 0, ph, pz, gh, gz);
+      n_hit = gh;
+    }
   }
 
+  ECHO_TRACE_MARK(2);
   // ===== phase A2: which claimed misses the prefetch staged this step =====
   uint32_t staged_total = 0;
   if (P.mode == kModeRecall && P.stage_count != nullptr) {
-    const int gw = rank * kPlanWarps + (threadIdx.x >> 5);
+    const int gw = rank * kSelWarps + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    for (int b = gw; b < P.B; b += kPlanCluster * kPlanWarps) {
+    for (int b = gw; b < P.B; b += C * kSelWarps) {
       int L = P.ctx_len[b];
       L = L < 0 ? 0 : (L > P.L_max ? P.L_max : L);
       int cap = (L + P.cap_div - 1) / P.cap_div;
@@ -336,7 +290,8 @@ __global__ void __cluster_dims__(kPlanCluster, 1, 1) __launch_bounds__(kPlanThre
     }
   }
 
-  // ===== phase B: evict max(0, M - free) slots with the smallest (priority, slot) =====
+  ECHO_TRACE_MARK(3);
+  // ===== phase B: evict E slots, the smallest (priority, slot) among evictable ones =====
   int32_t E = 0;
   if (P.mode == kModeEvict) {
     E = *P.evict_n_dev;
@@ -345,96 +300,67 @@ __global__ void __cluster_dims__(kPlanCluster, 1, 1) __launch_bounds__(kPlanThre
     E = static_cast<int32_t>(M) - n_free0;
     E = E < 0 ? 0 : E;
   }
-  const int sc = (n_g + kPlanCluster - 1) / kPlanCluster;
-  const int lo = rank * sc;
-  const int hi = lo + sc < n_g ? lo + sc : n_g;
-  const int nloc = hi > lo ? hi - lo : 0;
-  const int per_s = (nloc + kPlanThreads - 1) / kPlanThreads;
-  const int t0 = lo + threadIdx.x * per_s;
-  const int t1 = t0 + per_s < hi ? t0 + per_s : hi;
-  uint32_t T = 0, needT = 0;
   if (E > 0) {
-    uint32_t prefix = 0, pmask = 0, need = static_cast<uint32_t>(E);
-    const int shifts[3] = {21, 10, 0};
-    const int bins_of[3] = {2048, 2048, 1024};
-    for (int pass = 0; pass < 3; ++pass) {
-      const int shift = shifts[pass], nb = bins_of[pass];
-      const uint32_t dm = static_cast<uint32_t>(nb - 1);
-      for (int i = threadIdx.x; i < nb; i += kPlanThreads) S->hist[i] = 0;
-      __syncthreads();
-      for (int s = lo + threadIdx.x; s < hi; s += kPlanThreads) {
-        if (P.pool.free_[s]) continue;
-        const int32_t pr = P.pool.prio[s];
-        if (pr >= clock || pr < 0) continue;
-        const uint32_t key = static_cast<uint32_t>(pr);
-        if ((key & pmask) == prefix) atomicAdd(&S->hist[(key >> shift) & dm], 1u);
+    uint32_t cnt = 0, mn = 0xFFFFFFFFu, mx = 0;
+    for (int i = t0; i < t1; ++i) {
+      const uint32_t key = keys[i];
+      if (key < kProtKey) {
+        ++cnt;
+        mn = min(mn, key);
+        mx = max(mx, key);
       }
-      __syncthreads();
-      cluster.sync();
-      for (int i = threadIdx.x; i < nb; i += kPlanThreads) {
-        uint32_t s = 0;
-#pragma unroll
-        for (int r = 0; r < kPlanCluster; ++r) s += cluster.map_shared_rank(S->hist, r)[i];
-        S->tot[i] = s;
-      }
-      __syncthreads();
-      // prefix counts from the smallest digit up; thread t owns digits 2t, 2t+1
-      const int d0 = 2 * threadIdx.x, d1 = d0 + 1;
-      const uint32_t c0 = d0 < nb ? S->tot[d0] : 0, c1 = d1 < nb ? S->tot[d1] : 0;
-      uint32_t ex, dz, tt, tz;
-      plan_scan2(c0 + c1, 0, ex, dz, tt, tz, S);
-      if (pass == 0 && tt < need) need = tt;  // fewer evictable slots than asked
-      if (pass == 0) {
-        if (static_cast<uint32_t>(E) > tt) {
-          if (rank == 0 && threadIdx.x == 0) set_status(P.status, ECHO_DEV_POOL_EXHAUSTED);
-          E = static_cast<int32_t>(tt);
-        }
-      }
-      if (need == 0) break;
-      const uint32_t in0 = ex + c0, in1 = ex + c0 + c1;  // counts of digits <= d
-      if (d0 < nb && in0 >= need && ex < need) {
-        S->digit = static_cast<uint32_t>(d0);
-        S->below = ex;
-      }
-      if (d1 < nb && in1 >= need && in0 < need) {
-        S->digit = static_cast<uint32_t>(d1);
-        S->below = in0;
-      }
-      __syncthreads();
-      prefix |= S->digit << shift;
-      pmask |= dm << shift;
-      need -= S->below;
-      cluster.sync();
     }
-    T = prefix;
-    needT = need;
+    uint32_t ec, dz, tc, tz;
+    sel_block_scan2(cnt, 0, ec, dz, tc, tz, S);
+    uint32_t pc, pz, eligible, gz;
+    sel_cluster_prefix2(cl, S, tc, 0, pc, pz, eligible, gz);
+    if (static_cast<uint32_t>(E) > eligible) {
+      if (rank == 0 && threadIdx.x == 0) set_status(P.status, ECHO_DEV_POOL_EXHAUSTED);
+      E = static_cast<int32_t>(eligible);
+    }
   }
-  // victims: eligible with priority < T, or == T among the first needT in slot order
   if (E > 0) {
+    uint32_t mn = 0xFFFFFFFFu, mx = 0;
+    for (int i = t0; i < t1; ++i) {
+      const uint32_t key = keys[i];
+      if (key < kProtKey) {
+        mn = min(mn, key);
+        mx = max(mx, key);
+      }
+    }
+    ECHO_TRACE_MARK(4);
+    uint32_t pmin, pmax;
+    sel_cluster_minmax(cl, S, mn, mx, pmin, pmax);
+    ECHO_TRACE_MARK(5);
+    uint32_t T, needT;
+    sel_radix_select(cl, S, nloc, pmin, pmax, static_cast<uint32_t>(E), false,
+                     [&](int i, uint32_t &key) {
+                       key = keys[i];
+                       return key < kProtKey;
+                     },
+                     T, needT);
+    ECHO_TRACE_MARK(6);
+    // victims: priority < T, or == T among the first needT in slot order
     uint32_t lt = 0, eq = 0;
-    for (int s = t0; s < t1; ++s) {
-      if (P.pool.free_[s]) continue;
-      const int32_t pr = P.pool.prio[s];
-      if (pr >= clock || pr < 0) continue;
-      lt += static_cast<uint32_t>(pr) < T;
-      eq += static_cast<uint32_t>(pr) == T;
+    for (int i = t0; i < t1; ++i) {
+      const uint32_t key = keys[i];
+      lt += key < T;
+      eq += key == T;
     }
     uint32_t elt, eeq, tlt, teq;
-    plan_scan2(lt, eq, elt, eeq, tlt, teq, S);
+    sel_block_scan2(lt, eq, elt, eeq, tlt, teq, S);
     uint32_t plt, peq, glt, geq;
-    cluster_prefix2(cluster, S, tlt, teq, plt, peq, glt, geq);
-    uint32_t ob = plt + elt, eb = peq + eeq;  // victims before this segment: ob + min(eb, needT)
-    for (int s = t0; s < t1; ++s) {
-      if (P.pool.free_[s]) continue;
-      const int32_t pr = P.pool.prio[s];
-      if (pr >= clock || pr < 0) continue;
+    sel_cluster_prefix2(cl, S, tlt, teq, plt, peq, glt, geq);
+    uint32_t ob = plt + elt, eb = peq + eeq;
+    for (int i = t0; i < t1; ++i) {
+      const uint32_t key = keys[i];
       bool victim = false;
       uint32_t pos = 0;
-      if (static_cast<uint32_t>(pr) < T) {
+      if (key < T) {
         victim = true;
         pos = ob + (eb < needT ? eb : needT);
         ++ob;
-      } else if (static_cast<uint32_t>(pr) == T) {
+      } else if (key == T) {
         if (eb < needT) {
           victim = true;
           pos = ob + eb;
@@ -442,7 +368,9 @@ __global__ void __cluster_dims__(kPlanCluster, 1, 1) __launch_bounds__(kPlanThre
         ++eb;
       }
       if (!victim) continue;
+      const int s = lo + i;
       const int32_t h = P.pool.to_host[s];
+      keys[i] = kFreeKey;
       P.pool.free_[s] = 1;
       P.pool.prio[s] = -1;
       if (h >= 0 && h < P.pool.n_h) P.pool.h2g[h] = kInf;
@@ -450,24 +378,28 @@ __global__ void __cluster_dims__(kPlanCluster, 1, 1) __launch_bounds__(kPlanThre
       if (P.mode == kModeEvict) P.pool.idxbuf[pos] = s;
     }
   }
+  ECHO_TRACE_MARK(7);
   __syncthreads();
-  cluster.sync();
+  cl.sync();  // miss lists of every CTA written, evictions done
+  ECHO_TRACE_MARK(8);
 
   // ===== phase C: the r-th miss takes the r-th lowest free slot =====
   int32_t A = 0;
   if (P.mode != kModeEvict) {
     uint32_t nf = 0;
-    for (int s = t0; s < t1; ++s) nf += P.pool.free_[s] != 0;
+    for (int i = t0; i < t1; ++i) nf += keys[i] == kFreeKey;
     uint32_t enf, dz, tnf, tz;
-    plan_scan2(nf, 0, enf, dz, tnf, tz, S);
+    sel_block_scan2(nf, 0, enf, dz, tnf, tz, S);
     uint32_t pnf, pz, gnf, gz;
-    cluster_prefix2(cluster, S, tnf, 0, pnf, pz, gnf, gz);
+    sel_cluster_prefix2(cl, S, tnf, 0, pnf, pz, gnf, gz);
     A = static_cast<int32_t>(M < gnf ? M : gnf);
     uint32_t r = pnf + enf;
-    for (int s = t0; s < t1 && r < static_cast<uint32_t>(A); ++s) {
-      if (!P.pool.free_[s]) continue;
+    for (int i = t0; i < t1 && r < static_cast<uint32_t>(A); ++i) {
+      if (keys[i] != kFreeKey) continue;
+      const int s = lo + i;
       const int32_t f = P.ws.miss_f[r];
       const int32_t h = P.ws.miss_h[r];
+      keys[i] = kProtKey;
       P.pool.free_[s] = 0;
       P.pool.prio[s] = clock;
       P.pool.to_host[s] = h;
@@ -478,8 +410,8 @@ __global__ void __cluster_dims__(kPlanCluster, 1, 1) __launch_bounds__(kPlanThre
       ++r;
     }
     // misses beyond the free slots stay out of the pool
-    const int gt = rank * kPlanThreads + threadIdx.x;
-    for (int rr = A + gt; rr < static_cast<int>(M); rr += kPlanCluster * kPlanThreads) {
+    const int gt = rank * kSelThreads + threadIdx.x;
+    for (int rr = A + gt; rr < static_cast<int>(M); rr += C * kSelThreads) {
       const int32_t f = P.ws.miss_f[rr];
       P.pool.h2g[P.ws.miss_h[rr]] = kInf;
       if (P.mode == kModeRecall) P.ws.miss_stage[f] = -1;
@@ -487,35 +419,39 @@ __global__ void __cluster_dims__(kPlanCluster, 1, 1) __launch_bounds__(kPlanThre
     }
     if (static_cast<int32_t>(M) > A && rank == 0 && threadIdx.x == 0) set_status(P.status, ECHO_DEV_POOL_EXHAUSTED);
   }
+  ECHO_TRACE_MARK(9);
   // -1 over the rest of the previous index list
   const int32_t list_len = P.mode == kModeEvict ? E : A;
   {
-    const int gt = rank * kPlanThreads + threadIdx.x;
-    for (int i = list_len + gt; i < prev_idx && i < n_g; i += kPlanCluster * kPlanThreads) P.pool.idxbuf[i] = -1;
+    const int gt = rank * kSelThreads + threadIdx.x;
+    for (int i = list_len + gt; i < prev_idx && i < n_g; i += C * kSelThreads) P.pool.idxbuf[i] = -1;
   }
-  cluster.sync();
+  cl.sync();
   if (rank == 0 && threadIdx.x == 0) {
     P.pool.counters[0] = n_free0 + E - A;
     P.pool.counters[1] = list_len;
     P.ws.ctr[kCtrMisses] = static_cast<int32_t>(M);
     P.ws.ctr[kCtrGranted] = A;
     if (P.stats) {
+      auto add = [](int64_t *dst, unsigned long long v) {
+        atomicAdd(reinterpret_cast<unsigned long long *>(dst), v);
+      };
       if (P.mode == kModeRecall) {
-        atomicAdd(reinterpret_cast<unsigned long long *>(&P.stats->steps), 1ull);
-        atomicAdd(reinterpret_cast<unsigned long long *>(&P.stats->selected), static_cast<unsigned long long>(n_sel));
-        atomicAdd(reinterpret_cast<unsigned long long *>(&P.stats->unique_rows), static_cast<unsigned long long>(M + n_hit));
-        atomicAdd(reinterpret_cast<unsigned long long *>(&P.stats->hits), static_cast<unsigned long long>(n_hit));
-        atomicAdd(reinterpret_cast<unsigned long long *>(&P.stats->misses), static_cast<unsigned long long>(M));
-        atomicAdd(reinterpret_cast<unsigned long long *>(&P.stats->recalled), static_cast<unsigned long long>(A));
-        atomicAdd(reinterpret_cast<unsigned long long *>(&P.stats->unrecalled), static_cast<unsigned long long>(M - A));
+        add(&P.stats->steps, 1ull);
+        add(&P.stats->selected, n_sel);
+        add(&P.stats->unique_rows, M + n_hit);
+        add(&P.stats->hits, n_hit);
+        add(&P.stats->misses, M);
+        add(&P.stats->recalled, static_cast<unsigned long long>(A));
+        add(&P.stats->unrecalled, static_cast<unsigned long long>(M - A));
       }
-      if (P.mode == kModeAppend)
-        atomicAdd(reinterpret_cast<unsigned long long *>(&P.stats->appended), static_cast<unsigned long long>(M));
-      atomicAdd(reinterpret_cast<unsigned long long *>(&P.stats->evicted), static_cast<unsigned long long>(E));
+      if (P.mode == kModeAppend) add(&P.stats->appended, M);
+      add(&P.stats->evicted, static_cast<unsigned long long>(E));
     }
   }
   if (P.stats && P.mode == kModeRecall && staged_total)
     atomicAdd(reinterpret_cast<unsigned long long *>(&P.stats->staged), static_cast<unsigned long long>(staged_total));
+  ECHO_TRACE_MARK(10);
 }
 
 // ---------------------------------------------------------------------------
@@ -773,9 +709,35 @@ static echo::PlanParams base_params(const echo_pool *pool, const echo_workspace 
   return P;
 }
 
+// one cluster of 8 CTAs (16 for pools above 8 x kPlanMaxChunk slots)
 static int run_plan(const echo::PlanParams &P, cudaStream_t s) {
-  echo::plan_kernel<<<echo::kPlanCluster, echo::kPlanThreads, 0, s>>>(P);
-  return check("cache-manager plan");
+  const int C = P.pool.n_g <= 8 * echo::kPlanMaxChunk ? 8 : 16;
+  const int chunk = (P.pool.n_g + C - 1) / C;
+  if (chunk > echo::kPlanMaxChunk) {
+    set_error("pool of %d slots exceeds the supported %d", P.pool.n_g, 16 * echo::kPlanMaxChunk);
+    return ECHO_ENOTSUP;
+  }
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(echo::plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(echo::plan_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return cuda_fail(e, "plan kernel attributes");
+    attr = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C);
+  cfg.blockDim = dim3(echo::kSelThreads);
+  cfg.dynamicSmemBytes = sizeof(echo::SelSmem) + static_cast<size_t>(chunk) * sizeof(uint32_t);
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = C;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, echo::plan_kernel, P);
+  return e == cudaSuccess ? ECHO_OK : cuda_fail(e, "cache-manager plan");
 }
 
 int launch_pool_alloc(const echo_pool *pool, const echo_workspace *ws, const int32_t *host_idx, const int32_t *n_dev,

@@ -34,6 +34,28 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
+// Phase tracing for development builds (-DECHO_TRACE): each translation unit keeps
+// a small array of %globaltimer stamps written by block 0, thread 0, readable
+// through echo_debug_trace_<unit>().  Product builds compile the marks away.
+#ifdef ECHO_TRACE
+static __device__ unsigned long long g_echo_trace[32];
+#define ECHO_TRACE_UNIT(name)                                                          \
+  extern "C" int echo_debug_trace_##name(unsigned long long *out) {                    \
+    return cudaMemcpyFromSymbol(out, echo::g_echo_trace, sizeof(echo::g_echo_trace)) == cudaSuccess \
+               ? 0                                                                     \
+               : 2;                                                                    \
+  }
+#define ECHO_TRACE_MARK(slot)                                                          \
+  do {                                                                                 \
+    if (blockIdx.x == 0 && threadIdx.x == 0) g_echo_trace[slot] = echo::globaltimer(); \
+  } while (0)
+#else
+#define ECHO_TRACE_UNIT(name)
+#define ECHO_TRACE_MARK(slot) \
+  do {                        \
+  } while (0)
+#endif
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -33,6 +33,7 @@ constexpr int kStages = 6;
 constexpr int kEpiWarps = 4;
 constexpr int kPfWarps = 4;
 constexpr int kIndexerThreads = 32 * (2 + kEpiWarps + kPfWarps);
+constexpr int kAcc = 4;            // TMEM accumulators (MMA runs up to 3 tiles ahead of the epilogue)
 constexpr int kQueueCap = 64;      // entries per epilogue -> prefetch queue
 constexpr int kPfRowsPerBatch = 4; // rows one prefetch warp keeps in flight
 
@@ -58,8 +59,8 @@ struct IndexerParams {
 struct alignas(16) IndexerCtl {
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint64_t tmem_full[2];
-  uint64_t tmem_empty[2];
+  uint64_t tmem_full[kAcc];
+  uint64_t tmem_empty[kAcc];
   uint64_t q_full[2];
   uint64_t q_empty[2];
   uint64_t drain;
@@ -69,7 +70,7 @@ struct alignas(16) IndexerCtl {
   int queue_tail[kEpiWarps];
   int queue_head[kEpiWarps];
   int queue_done[kEpiWarps];
-  int2 queue[kEpiWarps][kQueueCap];
+  int queue[kEpiWarps][kQueueCap];  // token ids b * L_max + p that passed the threshold
   float wsm[kEpiWarps][2 * kHeads];  // head weights of the current request, per epilogue warp
 };
 
@@ -99,7 +100,7 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
                    const __grid_constant__ CUtensorMap tmap_q, const IndexerParams P) {
   constexpr int N = kHeads * NQ;               // MMA N: all heads of all queries
   constexpr uint32_t kQBytes = N * kDim;       // q of one request
-  constexpr uint32_t kTmemCols = 2 * N;        // two accumulators
+  constexpr uint32_t kTmemCols = kAcc * N;     // 256 (NQ = 1) or 512 (NQ = 2) columns
   constexpr uint32_t kIdesc = idesc_e4m3_f32(kTileTokens, N);
 
   extern __shared__ uint8_t smem_raw[];
@@ -138,9 +139,11 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
       mbar_init(&ctl->full[s], 1);
       mbar_init(&ctl->empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kAcc; ++i) {
       mbar_init(&ctl->tmem_full[i], 1);
       mbar_init(&ctl->tmem_empty[i], kEpiWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl->q_full[i], 1);
       mbar_init(&ctl->q_empty[i], 1);
     }
@@ -207,8 +210,8 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
         }
         const int s = i % kStages;
         if (!mbar_wait(&ctl->full[s], (i / kStages) & 1, abort, P.status)) break;
-        const int ab = i & 1;
-        if (i >= 2 && !mbar_wait(&ctl->tmem_empty[ab], ((i >> 1) & 1) ^ 1, abort, P.status)) break;
+        const int ab = i % kAcc;
+        if (i >= kAcc && !mbar_wait(&ctl->tmem_empty[ab], ((i / kAcc) & 1) ^ 1, abort, P.status)) break;
         tc_fence_after();
         const uint32_t a_addr = smem_u32(k_smem + s * kTileBytes);
         const uint32_t b_addr = smem_u32(q_smem + qb * kQBytes);
@@ -233,7 +236,6 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
     int b = ctl->first_b, t = ctl->first_t, cur_b = -1;
     float shat[NQ];
     int valid[NQ];
-    int cap = 0;
     int tail = 0;  // queue tail, kept by every lane (lane 0 publishes it)
     for (int i = 0; i < n_tiles; ++i) {
       if (b != cur_b) {
@@ -246,14 +248,10 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
           valid[j] = query_valid_len(L, NQ, j);
           shat[j] = prefetch ? __ldg(P.s_hat + b * NQ + j) : 0.f;
         }
-        if (prefetch) {
-          int c = (L + P.cap_div - 1) / P.cap_div;
-          cap = c < P.stage_stride ? c : P.stage_stride;
-        }
         cur_b = b;
       }
-      const int ab = i & 1;
-      if (!mbar_wait(&ctl->tmem_full[ab], (i >> 1) & 1, abort, P.status)) break;
+      const int ab = i % kAcc;
+      if (!mbar_wait(&ctl->tmem_full[ab], (i / kAcc) & 1, abort, P.status)) break;
       tc_fence_after();
       float sc[NQ];
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + ab * N;
@@ -263,12 +261,16 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
         tmem_ld_32x32b_x32(taddr + j * kHeads, v0);
         tmem_ld_32x32b_x32(taddr + j * kHeads + 32, v1);
         tmem_wait_ld();
-        float s = 0.f;
+        // four independent partial sums (heads 0-15, 16-31, 32-47, 48-63) shorten the FMA chain
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
-        for (int h = 0; h < 32; ++h) s = fmaf(wsm[j * kHeads + h], fmaxf(v0[h], 0.f), s);
-#pragma unroll
-        for (int h = 0; h < 32; ++h) s = fmaf(wsm[j * kHeads + 32 + h], fmaxf(v1[h], 0.f), s);
-        sc[j] = s;
+        for (int h = 0; h < 16; ++h) {
+          s0 = fmaf(wsm[j * kHeads + h], fmaxf(v0[h], 0.f), s0);
+          s1 = fmaf(wsm[j * kHeads + 16 + h], fmaxf(v0[16 + h], 0.f), s1);
+          s2 = fmaf(wsm[j * kHeads + 32 + h], fmaxf(v1[h], 0.f), s2);
+          s3 = fmaf(wsm[j * kHeads + 48 + h], fmaxf(v1[16 + h], 0.f), s3);
+        }
+        sc[j] = (s0 + s1) + (s2 + s3);
       }
       tc_fence_before();
       __syncwarp();
@@ -280,40 +282,26 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
         if (p < valid[j]) P.scores[(static_cast<size_t>(b) * NQ + j) * P.L_max + p] = sc[j];
 
       if (prefetch) {
+        // threshold test only; the host-row lookup, residency test, ticket and copy
+        // happen in the prefetch warps so that no global load sits on this path
         bool pass = false;
 #pragma unroll
         for (int j = 0; j < NQ; ++j) pass |= (p < valid[j]) && (sc[j] > shat[j]);
-        int32_t h = -1;
-        bool cand = false;
-        if (pass) {
-          h = __ldg(P.req_to_host + static_cast<size_t>(b) * P.L_max + p);
-          if (h >= 0 && h < P.n_h) {
-            cand = P.host_to_gpu[h] == kInf;
-          } else {
-            set_status(P.status, ECHO_DEV_BAD_INDEX);
-          }
-        }
-        const uint32_t mask = __ballot_sync(0xffffffffu, cand);
+        const uint32_t mask = __ballot_sync(0xffffffffu, pass);
         if (mask) {
-          int n = 0, base = 0;
+          int n = 0;
           if (lane == 0) {
             const int head = *reinterpret_cast<volatile int *>(&ctl->queue_head[e]);
             const int room = kQueueCap - (tail - head);
             n = __popc(mask);
             n = n < room ? n : room;  // a full queue drops candidates: prefetch is best effort
-            if (n > 0) base = atomicAdd(P.stage_count + b, n);
           }
           n = __shfl_sync(0xffffffffu, n, 0);
-          base = __shfl_sync(0xffffffffu, base, 0);
-          int m = cap - base;  // tickets below the cap stage a row
-          m = m < 0 ? 0 : (m > n ? n : m);
           const int rank = __popc(mask & ((1u << lane) - 1));
-          if (cand && rank < m)
-            ctl->queue[e][(tail + rank) % kQueueCap] = make_int2(h, b * P.stage_stride + base + rank);
-          if (lane == 0 && base + n > cap && n > 0) set_status(P.status, ECHO_DEV_PREFETCH_CAP_HIT);
+          if (pass && rank < n) ctl->queue[e][(tail + rank) % kQueueCap] = b * P.L_max + p;
           __syncwarp();
-          tail += m;
-          if (lane == 0 && m > 0) {
+          tail += n;
+          if (lane == 0 && n > 0) {
             __threadfence_block();
             *reinterpret_cast<volatile int *>(&ctl->queue_tail[e]) = tail;
           }
@@ -354,32 +342,72 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
         }
       }
       idle_since = 0;
-      const int n = (tl - head) < kPfRowsPerBatch ? (tl - head) : kPfRowsPerBatch;
-      int32_t hr[kPfRowsPerBatch], dr[kPfRowsPerBatch];
-#pragma unroll
-      for (int r = 0; r < kPfRowsPerBatch; ++r) {
-        const volatile int2 *qe = reinterpret_cast<const volatile int2 *>(&ctl->queue[e][(head + r) % kQueueCap]);
-        hr[r] = r < n ? qe->x : 0;
-        dr[r] = r < n ? qe->y : 0;
+      // ---- up to 32 queued tokens: host row, residency, ticket (one lane each)
+      const int n = (tl - head) < 32 ? (tl - head) : 32;
+      int32_t h = -1, b = 0, dst = -1;
+      bool cand = false;
+      if (lane < n) {
+        const int tok = *reinterpret_cast<volatile int *>(&ctl->queue[e][(head + lane) % kQueueCap]);
+        b = tok / P.L_max;
+        h = __ldg(P.req_to_host + tok);  // req_to_host is [B][L_max]: index b * L_max + p
+        if (h >= 0 && h < P.n_h) {
+          cand = P.host_to_gpu[h] == kInf;
+        } else {
+          set_status(P.status, ECHO_DEV_BAD_INDEX);
+        }
       }
-      constexpr int kPer = (kPfRowsPerBatch * kKvChunks + 31) / 32;  // 9 vectors per lane
-      int4 buf[kPer];
-#pragma unroll
-      for (int m = 0; m < kPer; ++m) {
-        const int idx = m * 32 + lane;
-        const int r = idx / kKvChunks, c = idx % kKvChunks;
-        if (r < n) buf[m] = __ldcs(host + static_cast<size_t>(hr[r]) * kKvChunks + c);
-      }
-#pragma unroll
-      for (int m = 0; m < kPer; ++m) {
-        const int idx = m * 32 + lane;
-        const int r = idx / kKvChunks, c = idx % kKvChunks;
-        if (r < n) stage[static_cast<size_t>(dr[r]) * kKvChunks + c] = buf[m];
-      }
-      if (lane < n) P.stage_host[dr[lane]] = hr[lane];
-      head += n;
+      head += n;  // entries are in registers: hand the slots back to the epilogue
       __syncwarp();
       if (lane == 0) *vhead = head;
+      const uint32_t cmask = __ballot_sync(0xffffffffu, cand);
+      if (cand) {
+        const uint32_t grp = __match_any_sync(cmask, b);  // candidates of the same request
+        const int leader = __ffs(grp) - 1;
+        int base = 0;
+        if (lane == leader) base = atomicAdd(P.stage_count + b, __popc(grp));
+        base = __shfl_sync(grp, base, leader);
+        const int ticket = base + __popc(grp & ((1u << lane) - 1));
+        const int L = clamp_ctx(__ldg(P.ctx_len + b), P.L_max);
+        int cap = (L + P.cap_div - 1) / P.cap_div;
+        cap = cap < P.stage_stride ? cap : P.stage_stride;
+        if (ticket < cap) {
+          dst = b * P.stage_stride + ticket;
+        } else if (ticket == cap) {
+          set_status(P.status, ECHO_DEV_PREFETCH_CAP_HIT);
+        }
+      }
+      // ---- copy the staged rows, kPfRowsPerBatch at a time (9 16-byte loads in flight per lane)
+      uint32_t rem = __ballot_sync(0xffffffffu, dst >= 0);
+      while (rem) {
+        int32_t hr[kPfRowsPerBatch], dr[kPfRowsPerBatch];
+        int cnt = 0;
+#pragma unroll
+        for (int r = 0; r < kPfRowsPerBatch; ++r) {
+          int src_lane = 0;
+          if (rem) {
+            src_lane = __ffs(rem) - 1;
+            rem &= rem - 1;
+            ++cnt;
+          }
+          hr[r] = __shfl_sync(0xffffffffu, h, src_lane);
+          dr[r] = __shfl_sync(0xffffffffu, dst, src_lane);
+        }
+        constexpr int kPer = (kPfRowsPerBatch * kKvChunks + 31) / 32;
+        int4 buf[kPer];
+#pragma unroll
+        for (int m = 0; m < kPer; ++m) {
+          const int idx = m * 32 + lane;
+          const int r = idx / kKvChunks, c = idx % kKvChunks;
+          if (r < cnt) buf[m] = __ldcs(host + static_cast<size_t>(hr[r]) * kKvChunks + c);
+        }
+#pragma unroll
+        for (int m = 0; m < kPer; ++m) {
+          const int idx = m * 32 + lane;
+          const int r = idx / kKvChunks, c = idx % kKvChunks;
+          if (r < cnt) stage[static_cast<size_t>(dr[r]) * kKvChunks + c] = buf[m];
+        }
+      }
+      if (dst >= 0) P.stage_host[dst] = h;
     }
   }
 
