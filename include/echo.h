@@ -175,7 +175,7 @@ int echo_indexer_score(const echo_indexer_args *args, void *stream);
  * token indices in ascending order, -1 padded when fewer than k tokens exist;
  * kth[b][j] is the min(k, L)-th largest score (-inf for an empty row).
  *   scores [B][n_q][L_max] fp32 device (no NaN); sel [B][n_q][k] int32; kth [B][n_q] fp32
- * Limits: 1 <= k <= 8192, L_max <= 393216.
+ * Limits: 1 <= k <= 8192, L_max <= 360448.
  */
 int echo_select_topk(const float *scores, const int32_t *ctx_len, int32_t B, int32_t n_q,
                      int32_t L_max, int32_t k, int32_t *sel, float *kth, void *stream);
@@ -251,7 +251,8 @@ int echo_append(const echo_pool *pool, const echo_workspace *ws, uint8_t *k_inde
 int echo_ema_update(float *s_hat, const float *kth, int32_t n, float alpha, void *stream);
 
 /* Stages of echo_decode_step, in order (timing events are recorded before each
-   stage and after the last). */
+   stage and after the last).  The EMA is computed by the recall's last kernel, so
+   the ECHO_STAGE_EMA interval is empty; the constant is kept for the event layout. */
 #define ECHO_STAGE_APPEND 0
 #define ECHO_STAGE_INDEXER 1
 #define ECHO_STAGE_TOPK 2
@@ -263,9 +264,12 @@ int echo_ema_update(float *s_hat, const float *kth, int32_t n, float alpha, void
  * One layer's decode step, every stage on the device (section 4 step list):
  *   [append] -> indexer score + fused prefetch -> top-k -> guaranteed recall -> EMA.
  * Fields as in the single calls.  new_kv == NULL skips the append.  s_hat may be
- * NULL (no prefetch, no EMA).  When clock_dev != NULL the kernels read the clock
- * there and, if advance_clock != 0, the last kernel increments it, so one captured
- * graph can be replayed step after step.  stage_events: optional array of
+ * NULL (no prefetch, no EMA); prefetch also needs stage.  When clock_dev != NULL
+ * the kernels read the clock there and, if advance_clock != 0, the recall advances
+ * it by one, so one captured graph can be replayed step after step.  All arguments
+ * are checked before the first launch: a rejected step enqueues nothing.
+ * Launches: 4 kernels (indexer, top-k, recall plan, recall copy), plus 3 for the
+ * append.  stage_events: optional array of
  * ECHO_NUM_STAGES + 1 cudaEvent_t (timing-enabled) recorded around the stages
  * (as external event nodes under capture).
  */

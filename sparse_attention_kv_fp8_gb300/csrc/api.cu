@@ -39,11 +39,12 @@ int launch_pool_evict(const echo_pool *pool, const echo_workspace *ws, const int
                       const int32_t *clock_dev, int32_t *status, cudaStream_t s);
 int launch_recall(const echo_pool *pool, const echo_workspace *ws, const int32_t *sel, const int32_t *req_to_host,
                   const int32_t *ctx_len, int B, int n_q, int k, int L_max, const echo_stage *stage, int32_t clock,
-                  const int32_t *clock_dev, int32_t *out_slot, echo_stats *stats, int32_t *status, cudaStream_t s);
+                  const int32_t *clock_dev, int32_t *out_slot, echo_stats *stats, int32_t *status, cudaStream_t s,
+                  float *ema_s_hat, const float *ema_kth, int ema_n, float ema_alpha, int32_t *clock_advance);
 int launch_append(const echo_pool *pool, const echo_workspace *ws, uint8_t *k_index, int32_t *ctx_len,
                   const int32_t *req_to_host, int B, int L_max, const uint16_t *new_kv, const uint8_t *new_k_index,
                   int32_t clock, const int32_t *clock_dev, echo_stats *stats, int32_t *status, cudaStream_t s);
-int launch_ema(float *s_hat, const float *kth, int n, float alpha, int32_t *clock_dev, int advance, cudaStream_t s);
+int launch_ema(float *s_hat, const float *kth, int n, float alpha, cudaStream_t s);
 
 }  // namespace echo_host
 
@@ -225,7 +226,7 @@ int echo_prefetch_recall(const echo_pool *pool, const echo_workspace *ws, const 
   TRY(check_ws(ws, pool, F));
   if (stage) TRY(check_stage(stage));
   return launch_recall(pool, ws, sel, req_to_host, ctx_len, B, n_q, k, L_max, stage, clock, clock_dev, out_slot, stats,
-                       dev_status, static_cast<cudaStream_t>(stream));
+                       dev_status, static_cast<cudaStream_t>(stream), nullptr, nullptr, 0, 0.f, nullptr);
 }
 
 int echo_append(const echo_pool *pool, const echo_workspace *ws, uint8_t *k_index, int32_t *ctx_len,
@@ -249,7 +250,7 @@ int echo_ema_update(float *s_hat, const float *kth, int32_t n, float alpha, void
   REQUIRE(n == 0 || (s_hat && kth), "EMA pointer is NULL");
   REQUIRE(alpha >= 0.f && alpha <= 1.f, "alpha must be in [0, 1]");
   if (n == 0) return ECHO_OK;
-  return launch_ema(s_hat, kth, n, alpha, nullptr, 0, static_cast<cudaStream_t>(stream));
+  return launch_ema(s_hat, kth, n, alpha, static_cast<cudaStream_t>(stream));
 }
 
 int echo_decode_step(const echo_step_args *a, void *stream) {
@@ -262,6 +263,22 @@ int echo_decode_step(const echo_step_args *a, void *stream) {
           "step pointer is NULL");
   REQUIRE(a->clock >= 0 || a->clock_dev, "clock must be >= 0");
   const bool prefetch = a->s_hat && a->stage;
+  // everything is checked before the first launch, so a rejected step enqueues nothing
+  TRY(check_pool(a->pool));
+  REQUIRE(a->B >= 0 && a->L_max >= 0, "negative size");
+  REQUIRE(a->n_q == 1 || a->n_q == 2, "n_q must be 1 or 2 (got %d)", a->n_q);
+  REQUIRE(a->k >= 1 && a->k <= 8192, "k must be in [1, 8192] (got %d)", a->k);
+  REQUIRE(aligned(a->q, 16) && aligned(a->k_index, 16), "q and k_index must be 16-byte aligned");
+  REQUIRE(static_cast<long long>(a->B) * a->L_max <= (1ll << 31) - 1, "B * L_max too large");
+  const long long F = static_cast<long long>(a->B) * a->n_q * a->k;
+  REQUIRE(F <= (1ll << 30), "B * n_q * k too large");
+  TRY(check_ws(a->ws, a->pool, F > a->B ? F : a->B));
+  REQUIRE(a->alpha >= 0.f && a->alpha <= 1.f, "alpha must be in [0, 1]");
+  if (prefetch) TRY(check_stage(a->stage));
+  if (a->new_kv) {
+    REQUIRE(a->new_k_index, "new_kv given without new_k_index");
+    REQUIRE(aligned(a->new_kv, 16) && aligned(a->new_k_index, 16), "append buffers must be 16-byte aligned");
+  }
   cudaEvent_t *ev = reinterpret_cast<cudaEvent_t *>(a->stage_events);
   auto mark = [&](int i) -> int {
     if (!ev || !ev[i]) return ECHO_OK;
@@ -294,14 +311,14 @@ int echo_decode_step(const echo_step_args *a, void *stream) {
   TRY(mark(ECHO_STAGE_TOPK));
   TRY(echo_select_topk(a->scores, a->ctx_len, a->B, a->n_q, a->L_max, a->k, a->sel, a->kth, stream));
   TRY(mark(ECHO_STAGE_RECALL));
-  TRY(echo_prefetch_recall(a->pool, a->ws, a->sel, a->req_to_host, a->ctx_len, a->B, a->n_q, a->k, a->L_max,
-                           prefetch ? a->stage : nullptr, a->clock, a->clock_dev, a->out_slot, a->stats,
-                           a->dev_status, stream));
-  TRY(mark(ECHO_STAGE_EMA));
-  if (a->s_hat || (a->clock_dev && a->advance_clock)) {
-    const int n = a->s_hat ? a->B * a->n_q : 0;
-    TRY(launch_ema(a->s_hat, a->kth, n, a->alpha, a->clock_dev, a->advance_clock, s));
+  {
+    // the recall's plan kernel also updates the EMA and advances the device clock
+    TRY(launch_recall(a->pool, a->ws, a->sel, a->req_to_host, a->ctx_len, a->B, a->n_q, a->k, a->L_max,
+                      prefetch ? a->stage : nullptr, a->clock, a->clock_dev, a->out_slot, a->stats, a->dev_status, s,
+                      a->s_hat, a->kth, a->B * a->n_q, a->alpha,
+                      (a->clock_dev && a->advance_clock) ? a->clock_dev : nullptr));
   }
+  TRY(mark(ECHO_STAGE_EMA));  // the EMA ran inside the recall: this stage is empty
   TRY(mark(ECHO_NUM_STAGES));
   return ECHO_OK;
 }

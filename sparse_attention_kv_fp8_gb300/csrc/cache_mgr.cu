@@ -12,39 +12,60 @@
 //               free + allocate, set the maps, copy the KV host -> GPU from kernels
 //               reading the mapped host memory.
 //
-// sm_103a design.  Three kernels per operation, all fixed-shape:
-//   claim  (grid-wide)  maps each selected entry to its host row; resident rows
-//                       are hits (priority = clock, protecting them); missing rows
-//                       are claimed in HostTokenToGPU with atomicMin(kClaim + f),
-//                       so the first entry in (b, j, i) order owns each row.
-//   plan   (one 8-CTA thread-block cluster) compacts the owned misses in entry
-//                       order, selects the victims -- the smallest (priority, slot)
-//                       by a 3-pass radix select with distributed-shared-memory
-//                       histograms -- and hands the lowest free slots to the
-//                       misses in order.  Block and cluster prefix scans replace
-//                       the page's atomic ticket race with its slot-ordered
-//                       interleaving, so the metadata is deterministic.
-//   copy   (grid-wide)  moves each recalled row (1152 B, 16-byte vectors, several
-//                       rows in flight per warp) from the staging area or the
-//                       pinned host pool into its slot and writes out_slot.
-#include "cluster_select.cuh"
+// sm_103a design: every operation (recall, allocate, evict, the append's
+// allocation) is ONE cooperative kernel over all SMs, its phases separated by
+// bounded grid barriers:
+//   P1  claims: each selected entry maps to its host row (kept for the later
+//       phases); resident rows are hits (priority = clock: protected); missing rows
+//       are claimed in HostTokenToGPU with atomicMin(kClaim + f) so the first entry
+//       in (b, j, i) order owns each row.  Slot pass: bounds of the evictable
+//       priorities.
+//   P2  histogram of evictable priorities (4096 bins over the bits in which they
+//       differ); per-CTA counts of owned misses; staged-row lookup.
+//   P3  misses M = sum of the owned counts; every CTA finds the same threshold
+//       priority T (the E-th smallest, E = max(0, M - free)) from the histogram
+//       (refined while a bin is wider than one value); per-CTA counts of slots
+//       below / at T and free.
+//   P4  prefix sums over the per-CTA counts give each owned miss its rank and each
+//       slot its eviction and free-slot rank: victims are scattered (free = 1,
+//       priority = -1, maps to INF), the r-th free slot is recorded for miss r.
+//       This is the page's ticket order taken in slot order, so it is deterministic.
+//   P5  the r-th miss takes the r-th free slot (maps, priority = clock, indices
+//       buffer) and its KV row is copied (16-byte vectors, 4 rows in flight per
+//       warp) from the staging area or the pinned host pool.
+//   P6  (recall) out_slot of every entry; each hit counted and cleared by its owner.
+#include "echo_common.cuh"
 
 ECHO_TRACE_UNIT(cache_mgr)
 
 namespace echo {
 
-enum PlanMode { kModeRecall = 0, kModeAlloc = 1, kModeAppend = 2, kModeEvict = 3 };
+enum Mode { kModeRecall = 0, kModeAlloc = 1, kModeAppend = 2, kModeEvict = 3 };
 
-// workspace counters
+constexpr int kCoopThreads = 512;
+constexpr int kCoopWarps = kCoopThreads / 32;
+constexpr int kMaxGrid = 1024;
+constexpr int kHistBins = 4096;
+constexpr int kHistLevels = 3;  // 12 + 12 + 8 bits cover any int32 priority range
+
+// global scratch counters (zero between calls, except kGMin = UINT32_MAX)
+enum { kGValid = 0, kGMin, kGMax, kGBar, kGCount = 16 };
+// per-CTA counts
+enum { kCOwn = 0, kCLt, kCEq, kCFree, kCVals };
+// ws.ctr: results readable after a call
 enum { kCtrMisses = 0, kCtrGranted = 1, kCtrCount = 16 };
 
 struct Workspace {
-  int32_t *slot_claim;  // [n_g]  min entry index protecting the slot (INT32_MAX = none)
+  int32_t *slot_claim;  // [n_g]  min entry index of this step's hits (INT32_MAX = none)
   int32_t *entry_rows;  // [max_rows] host row per entry (append)
+  int32_t *entry_h;     // [max_rows] host row of every entry, -1 if none (filled in P1)
   int32_t *miss_f;      // [max_rows] entry index of the r-th owned miss
   int32_t *miss_h;      // [max_rows] host row of the r-th owned miss
   int32_t *miss_stage;  // [max_rows] by entry: staging row index, -1 = not staged
-  int32_t *alloc_slot;  // [max_rows] slot granted to the r-th miss
+  int32_t *alloc_slot;  // [max_rows] the r-th free slot (taken by the r-th miss)
+  uint32_t *hist;       // [kHistLevels][kHistBins]
+  uint32_t *cta;        // [kMaxGrid][kCVals]
+  uint32_t *glob;       // [kGCount]
   int32_t *ctr;         // [kCtrCount]
 };
 
@@ -55,16 +76,20 @@ __host__ __device__ inline size_t ws_layout(int32_t n_g, int32_t max_rows, uintp
   auto take = [&](size_t n) {
     size_t o = off;
     off += ws_align(n * sizeof(int32_t));
-    return reinterpret_cast<int32_t *>(base + o);
+    return base + o;
   };
   Workspace x;
-  x.slot_claim = take(static_cast<size_t>(n_g));
-  x.entry_rows = take(static_cast<size_t>(max_rows));
-  x.miss_f = take(static_cast<size_t>(max_rows));
-  x.miss_h = take(static_cast<size_t>(max_rows));
-  x.miss_stage = take(static_cast<size_t>(max_rows));
-  x.alloc_slot = take(static_cast<size_t>(max_rows));
-  x.ctr = take(kCtrCount);
+  x.slot_claim = reinterpret_cast<int32_t *>(take(static_cast<size_t>(n_g)));
+  x.entry_rows = reinterpret_cast<int32_t *>(take(static_cast<size_t>(max_rows)));
+  x.entry_h = reinterpret_cast<int32_t *>(take(static_cast<size_t>(max_rows)));
+  x.miss_f = reinterpret_cast<int32_t *>(take(static_cast<size_t>(max_rows)));
+  x.miss_h = reinterpret_cast<int32_t *>(take(static_cast<size_t>(max_rows)));
+  x.miss_stage = reinterpret_cast<int32_t *>(take(static_cast<size_t>(max_rows)));
+  x.alloc_slot = reinterpret_cast<int32_t *>(take(static_cast<size_t>(max_rows)));
+  x.hist = reinterpret_cast<uint32_t *>(take(static_cast<size_t>(kHistLevels) * kHistBins));
+  x.cta = reinterpret_cast<uint32_t *>(take(static_cast<size_t>(kMaxGrid) * kCVals));
+  x.glob = reinterpret_cast<uint32_t *>(take(kGCount));
+  x.ctr = reinterpret_cast<int32_t *>(take(kCtrCount));
   if (w) *w = x;
   return off;
 }
@@ -77,16 +102,16 @@ struct PoolView {
   int32_t n_g, n_h;
 };
 
-struct PlanParams {
+struct OpParams {
   PoolView pool;
   Workspace ws;
   int mode;
-  int F;  // entries
+  int F;  // entries (recall: B * n_q * k; allocate: max_n; append: B)
   // recall entries
   const int32_t *sel;
   const int32_t *req_to_host;
   int n_q, k, L_max;
-  // alloc / append entries
+  // allocate / append entries
   const int32_t *rows;
   const int32_t *n_dev;
   int32_t *out_slots;
@@ -94,19 +119,30 @@ struct PlanParams {
   const int32_t *evict_n_dev;
   // staging (recall)
   const int32_t *stage_host;
-  const int32_t *stage_count;
+  int32_t *stage_count;
+  const uint16_t *stage_rows;
   const int32_t *ctx_len;
   int B, stage_stride, cap_div;
+  // append: source rows
+  const uint16_t *new_kv;
+  // recall output
+  int32_t *out_slot;
   int32_t clock;
   const int32_t *clock_dev;
   echo_stats *stats;
   int32_t *status;
+  // decode step only: EMA of the k-th score and the device clock's advance
+  float *s_hat;
+  const float *kth;
+  int n_ema;
+  float alpha;
+  int32_t *clock_advance;
 };
 
-__device__ __forceinline__ int32_t read_clock(const PlanParams &P) { return P.clock_dev ? *P.clock_dev : P.clock; }
+__device__ __forceinline__ int32_t read_clock(const OpParams &P) { return P.clock_dev ? *P.clock_dev : P.clock; }
 
 // host row of entry f, or -1 (with BAD_INDEX flagged for out-of-range indices)
-__device__ __forceinline__ int32_t entry_row(const PlanParams &P, int f, int n_entries, bool flag) {
+__device__ __forceinline__ int32_t entry_row(const OpParams &P, int f, int n_entries, bool flag) {
   if (f >= n_entries) return -1;
   int32_t h;
   if (P.mode == kModeRecall) {
@@ -128,149 +164,236 @@ __device__ __forceinline__ int32_t entry_row(const PlanParams &P, int f, int n_e
   return h;
 }
 
-__device__ __forceinline__ int entries_count(const PlanParams &P) {
+__device__ __forceinline__ int entries_count(const OpParams &P) {
+  if (P.mode == kModeEvict) return 0;
   if (P.mode == kModeAlloc) {
-    int n = *P.n_dev;
+    const int n = *P.n_dev;
     return n < 0 ? 0 : (n > P.F ? P.F : n);
   }
   return P.F;
 }
 
-// ---------------------------------------------------------------------------
-// claim: hits are protected, misses claim their host row (first entry wins)
-// ---------------------------------------------------------------------------
-__global__ void claim_kernel(const PlanParams P) {
-  const int n = entries_count(P);
-  const int32_t clock = read_clock(P);
-  for (int f = blockIdx.x * blockDim.x + threadIdx.x; f < n; f += gridDim.x * blockDim.x) {
-    const int32_t h = entry_row(P, f, n, true);
-    if (h < 0) {
-      if (P.mode == kModeAlloc) P.out_slots[f] = -1;
-      continue;
-    }
-    const int32_t v = P.pool.h2g[h];
-    const bool resident = v >= 0 && v < P.pool.n_g;
-    if (P.mode == kModeRecall) {
-      if (resident) {
-        P.pool.prio[v] = clock;  // protect + LRU clock
-        atomicMin(P.ws.slot_claim + v, f);
-      } else if (v == kInf || v < 0) {
-        atomicMin(P.pool.h2g + h, kClaim + f);
-      } else {
-        set_status(P.status, ECHO_DEV_BAD_INDEX);
-      }
-    } else {
-      if (v != kInf && v >= 0) {  // already resident (or corrupt): cannot allocate again
-        set_status(P.status, ECHO_DEV_BAD_INDEX);
-        if (P.mode == kModeAlloc) P.out_slots[f] = -1;
-      } else {
-        atomicMin(P.pool.h2g + h, kClaim + f);
-      }
-    }
+// EMA of the k-th score (fp32, each operation rounded; +inf start takes kth)
+__device__ __forceinline__ void ema_one(float *s_hat, const float *kth, int i, float alpha) {
+  const float x = kth[i];
+  if (!isfinite(x)) return;
+  const float s = s_hat[i];
+  if (isinf(s) && s > 0.f) {
+    s_hat[i] = x;
+  } else {
+    s_hat[i] = __fadd_rn(__fmul_rn(alpha, s), __fmul_rn(__fsub_rn(1.0f, alpha), x));
   }
 }
 
-// ---------------------------------------------------------------------------
-// plan: one thread-block cluster; every CTA stages its slice of the slots in
-// shared memory as one key per slot:
-//   kFreeKey          free slot
-//   kProtKey          occupied and not evictable (priority >= clock: protected)
-//   priority          occupied and evictable
-// ---------------------------------------------------------------------------
-constexpr uint32_t kFreeKey = 0xFFFFFFFFu;
-constexpr uint32_t kProtKey = 0xFFFFFFFEu;
-constexpr int kPlanMaxChunk = 48 * 1024;  // slots per CTA (shared memory)
+__device__ __forceinline__ bool evictable(uint8_t fr, int32_t pr, int32_t clock) {
+  return !fr && pr >= 0 && pr < clock;
+}
 
-__global__ void __launch_bounds__(kSelThreads, 1) plan_kernel(const PlanParams P) {
-  cg::cluster_group cl = cg::this_cluster();
-  const int rank = static_cast<int>(cl.block_rank());
-  const int C = static_cast<int>(cl.num_blocks());
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  SelSmem *S = reinterpret_cast<SelSmem *>(smem_raw);
-  uint32_t *keys = reinterpret_cast<uint32_t *>(smem_raw + sizeof(SelSmem));
+// ---------------------------------------------------------------------------
+// block-level helpers (kCoopThreads threads)
+// ---------------------------------------------------------------------------
+struct CoopSmem {
+  uint32_t hist[kHistBins];
+  uint32_t ws[4][kCoopWarps];
+  uint32_t red[8];
+  uint32_t pre[kCVals], tot[kCVals];
+};
+
+// exclusive block scan of NV counters; block totals in tot
+template <int NV>
+__device__ __forceinline__ void coop_scan(const uint32_t (&v)[NV], uint32_t (&ex)[NV], uint32_t (&tot)[NV],
+                                          CoopSmem *S) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t inc[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) inc[k] = v[k];
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1)
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const uint32_t u = __shfl_up_sync(0xffffffffu, inc[k], o);
+      if (lane >= o) inc[k] += u;
+    }
+  if (lane == 31)
+#pragma unroll
+    for (int k = 0; k < NV; ++k) S->ws[k][warp] = inc[k];
+  __syncthreads();
+  if (warp == 0)
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      uint32_t x = lane < kCoopWarps ? S->ws[k][lane] : 0u;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t u = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += u;
+      }
+      if (lane < kCoopWarps) S->ws[k][lane] = x;
+    }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    ex[k] = (warp ? S->ws[k][warp - 1] : 0) + inc[k] - v[k];
+    tot[k] = S->ws[k][kCoopWarps - 1];
+  }
+  __syncthreads();
+}
+
+// Bounded grid barrier of a cooperative launch (every CTA is resident).  One
+// monotone arrival counter that is never reset: a CTA arriving with old value v
+// waits until the counter reaches the next multiple of the grid size.  A CTA that
+// waits longer than kWaitLimitNs sets WAIT_TIMEOUT and reports failure; the caller
+// then skips the remaining phases (the workspace must be re-initialised).
+__device__ __forceinline__ bool grid_barrier(uint32_t *glob, int32_t *status, CoopSmem *S) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t ok = 1;
+    const uint32_t G = gridDim.x;
+    uint32_t old;
+    asm volatile("atom.add.release.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(glob + kGBar) : "memory");
+    const uint32_t target = (old / G + 1) * G;  // counts stay multiples of G between barriers
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+      uint32_t cur;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(cur) : "l"(glob + kGBar) : "memory");
+      if (static_cast<int32_t>(cur - target) >= 0) break;
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        set_status(status, ECHO_DEV_WAIT_TIMEOUT);
+        ok = 0;
+        break;
+      }
+    }
+    S->red[7] = ok;
+  }
+  __syncthreads();
+  return S->red[7] != 0;
+}
+
+__device__ __forceinline__ void add_stat(echo_stats *st, int64_t echo_stats::*field, unsigned long long v) {
+  if (st && v) atomicAdd(reinterpret_cast<unsigned long long *>(&(st->*field)), v);
+}
+
+// ---------------------------------------------------------------------------
+// the cooperative kernel
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParams P) {
+  __shared__ CoopSmem S_;
+  CoopSmem *S = &S_;
+  const int G = gridDim.x, c = blockIdx.x;
+  const int gtid = c * kCoopThreads + threadIdx.x, gthreads = G * kCoopThreads;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int32_t clock = read_clock(P);
   const int n_g = P.pool.n_g;
   const int32_t n_free0 = P.pool.counters[0];
   const int32_t prev_idx = P.pool.counters[1];
+  const int n = entries_count(P);
+  uint32_t *glob = P.ws.glob;
   ECHO_TRACE_MARK(0);
 
-  // ===== this CTA's slots, staged =====
-  const int sc = (n_g + C - 1) / C;
-  const int lo = rank * sc < n_g ? rank * sc : n_g;
-  const int hi = lo + sc < n_g ? lo + sc : n_g;
-  const int nloc = hi - lo;
-  for (int i = threadIdx.x; i < nloc; i += kSelThreads) {
-    const int32_t pr = P.pool.prio[lo + i];
-    keys[i] = P.pool.free_[lo + i] ? kFreeKey
-                                   : ((pr >= 0 && pr < clock) ? static_cast<uint32_t>(pr) : kProtKey);
-  }
-  __syncthreads();
-  // contiguous per-thread segments of the slice, odd length (conflict-free reads)
-  int seg = (nloc + kSelThreads - 1) / kSelThreads;
-  seg |= 1;
-  const int t0 = threadIdx.x * seg < nloc ? threadIdx.x * seg : nloc;
-  const int t1 = t0 + seg < nloc ? t0 + seg : nloc;
-  ECHO_TRACE_MARK(1);
+  // this CTA's slots and entries (contiguous ranges, for the ordered phases)
+  const int s_lo = static_cast<int>((static_cast<long long>(n_g) * c) / G);
+  const int s_hi = static_cast<int>((static_cast<long long>(n_g) * (c + 1)) / G);
+  const int e_lo = static_cast<int>((static_cast<long long>(n) * c) / G);
+  const int e_hi = static_cast<int>((static_cast<long long>(n) * (c + 1)) / G);
 
-  // ===== phase A: owned misses in entry order (and unique hits) =====
-  uint32_t M = 0, n_sel = 0, n_hit = 0;
+  // ===== P1: claims (no atomic result waited on); bounds of the evictable priorities =====
   if (P.mode != kModeEvict) {
-    const int n = entries_count(P);
-    const int c0 = static_cast<int>((static_cast<long long>(n) * rank) / C);
-    const int c1 = static_cast<int>((static_cast<long long>(n) * (rank + 1)) / C);
-    const int per = (c1 - c0 + kSelThreads - 1) / kSelThreads;
-    const int s0 = c0 + threadIdx.x * per < c1 ? c0 + threadIdx.x * per : c1;
-    const int s1 = s0 + per < c1 ? s0 + per : c1;
-    uint32_t own = 0, hits = 0, valid = 0;
-    for (int f = s0; f < s1; ++f) {
-      const int32_t h = entry_row(P, f, n, false);
-      if (h < 0) continue;
+    uint32_t valid = 0;
+    for (int f = gtid; f < n; f += gthreads) {
+      const int32_t h = entry_row(P, f, n, true);
+      P.ws.entry_h[f] = h;
+      if (h < 0) {
+        if (P.mode == kModeAlloc) P.out_slots[f] = -1;
+        continue;
+      }
       ++valid;
+      if (P.mode == kModeAppend) continue;  // claimed when the token was written
+      const int32_t v = P.pool.h2g[h];
+      if (v >= 0 && v < n_g) {
+        if (P.mode == kModeRecall) {
+          P.pool.prio[v] = clock;              // protect + LRU clock
+          atomicMin(P.ws.slot_claim + v, f);   // first entry of the row owns the hit
+        } else {                               // allocate: already resident
+          set_status(P.status, ECHO_DEV_BAD_INDEX);
+          P.out_slots[f] = -1;
+          P.ws.entry_h[f] = -1;
+        }
+      } else if (v == kInf || v < 0) {
+        atomicMin(P.pool.h2g + h, kClaim + f);  // first entry of the row owns the miss
+      } else {
+        set_status(P.status, ECHO_DEV_BAD_INDEX);
+        P.ws.entry_h[f] = -1;
+      }
+    }
+    for (int o = 16; o > 0; o >>= 1) valid += __shfl_xor_sync(0xffffffffu, valid, o);
+    if (lane == 0 && valid) atomicAdd(glob + kGValid, valid);
+  }
+  if (P.mode != kModeAlloc) {
+    uint32_t mn = 0xFFFFFFFFu, mx = 0;
+    for (int s = s_lo + threadIdx.x; s < s_hi; s += kCoopThreads) {
+      const int32_t pr = P.pool.prio[s];
+      if (evictable(P.pool.free_[s], pr, clock)) {
+        mn = min(mn, static_cast<uint32_t>(pr));
+        mx = max(mx, static_cast<uint32_t>(pr));
+      }
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+      mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    if (lane == 0 && mn <= mx) {
+      atomicMin(glob + kGMin, mn);
+      atomicMax(glob + kGMax, mx);
+    }
+  }
+  ECHO_TRACE_MARK(1);
+  if (!grid_barrier(glob, P.status, S)) return;
+  ECHO_TRACE_MARK(2);
+
+  // ===== P2: priority histogram; owned misses per CTA; staged rows =====
+  const uint32_t pmin = *reinterpret_cast<volatile uint32_t *>(glob + kGMin);
+  const uint32_t pmax = *reinterpret_cast<volatile uint32_t *>(glob + kGMax);
+  const bool any_evictable = P.mode != kModeAlloc && pmin <= pmax;
+  const uint32_t range = any_evictable ? pmax - pmin : 0u;
+  const int rbits = range == 0 ? 0 : 32 - __clz(range);
+  int shift = rbits > 12 ? rbits - 12 : 0;
+  if (any_evictable) {
+    for (int i = threadIdx.x; i < kHistBins; i += kCoopThreads) S->hist[i] = 0;
+    __syncthreads();
+    for (int s = s_lo + threadIdx.x; s < s_hi; s += kCoopThreads) {
+      const int32_t pr = P.pool.prio[s];
+      if (evictable(P.pool.free_[s], pr, clock))
+        atomicAdd(&S->hist[(static_cast<uint32_t>(pr) - pmin) >> shift], 1u);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < kHistBins; i += kCoopThreads)
+      if (S->hist[i]) atomicAdd(P.ws.hist + i, S->hist[i]);
+  }
+  if (P.mode != kModeEvict) {
+    uint32_t own = 0;
+    for (int f = e_lo + threadIdx.x; f < e_hi; f += kCoopThreads) {
+      const int32_t h = P.ws.entry_h[f];
+      if (h < 0) continue;
       const int32_t v = P.pool.h2g[h];
       if (v == kClaim + f) {
         ++own;
-      } else if (P.mode == kModeRecall && v >= 0 && v < n_g && P.ws.slot_claim[v] == f) {
-        ++hits;
-        P.ws.slot_claim[v] = INT32_MAX;  // leave the workspace initialised
       } else if (P.mode != kModeRecall && v < 0) {
-        // a repeat of a row an earlier entry claimed: rejected (resident rows were
-        // rejected by the claim kernel)
+        // a repeat of a row an earlier entry claimed: rejected
         if (P.mode == kModeAlloc) P.out_slots[f] = -1;
         set_status(P.status, ECHO_DEV_BAD_INDEX);
       }
     }
-    uint32_t ex_own, ex_val, t_own, t_val;
-    sel_block_scan2(own, valid, ex_own, ex_val, t_own, t_val, S);
-    uint32_t pre_own, pre_val, g_own, g_val;
-    sel_cluster_prefix2(cl, S, t_own, t_val, pre_own, pre_val, g_own, g_val);
-    M = g_own;
-    n_sel = g_val;
-    uint32_t r = pre_own + ex_own;
-    for (int f = s0; f < s1; ++f) {
-      const int32_t h = entry_row(P, f, n, false);
-      if (h < 0) continue;
-      if (P.pool.h2g[h] == kClaim + f) {
-        P.ws.miss_f[r] = f;
-        P.ws.miss_h[r] = h;
-        ++r;
-      }
-    }
-    if (P.mode == kModeRecall) {
-      uint32_t eh, dz, th, tz;
-      sel_block_scan2(hits, 0, eh, dz, th, tz, S);
-      uint32_t ph, pz, gh, gz;
-      sel_cluster_prefix2(cl, S, th, 0, ph, pz, gh, gz);
-      n_hit = gh;
+    for (int o = 16; o > 0; o >>= 1) own += __shfl_xor_sync(0xffffffffu, own, o);
+    if (lane == 0) S->ws[0][warp] = own;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      uint32_t t = 0;
+      for (int w = 0; w < kCoopWarps; ++w) t += S->ws[0][w];
+      P.ws.cta[c * kCVals + kCOwn] = t;
     }
   }
-
-  ECHO_TRACE_MARK(2);
-  // ===== phase A2: which claimed misses the prefetch staged this step =====
-  uint32_t staged_total = 0;
   if (P.mode == kModeRecall && P.stage_count != nullptr) {
-    const int gw = rank * kSelWarps + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    for (int b = gw; b < P.B; b += C * kSelWarps) {
+    // which claimed misses the prefetch staged this step (one warp per request)
+    for (int b = c * kCoopWarps + warp; b < P.B; b += G * kCoopWarps) {
       int L = P.ctx_len[b];
       L = L < 0 ? 0 : (L > P.L_max ? P.L_max : L);
       int cap = (L + P.cap_div - 1) / P.cap_div;
@@ -286,12 +409,25 @@ __global__ void __launch_bounds__(kSelThreads, 1) plan_kernel(const PlanParams P
           if (f < static_cast<uint32_t>(P.F)) P.ws.miss_stage[f] = b * P.stage_stride + i;
         }
       }
-      if (lane == 0) staged_total += static_cast<uint32_t>(nb);
+      if (lane == 0) add_stat(P.stats, &echo_stats::staged, static_cast<unsigned long long>(nb));
     }
   }
-
   ECHO_TRACE_MARK(3);
-  // ===== phase B: evict E slots, the smallest (priority, slot) among evictable ones =====
+  if (!grid_barrier(glob, P.status, S)) return;
+  ECHO_TRACE_MARK(4);
+
+  // ===== P3: misses M and evictions E; threshold T (the E-th smallest evictable
+  // priority); per-CTA counts =====
+  uint32_t M = 0;
+  if (P.mode != kModeEvict) {
+    uint32_t m = 0;
+    for (int r = threadIdx.x; r < G; r += kCoopThreads) m += __ldcg(P.ws.cta + r * kCVals + kCOwn);
+    for (int o = 16; o > 0; o >>= 1) m += __shfl_xor_sync(0xffffffffu, m, o);
+    if (lane == 0) S->ws[0][warp] = m;
+    __syncthreads();
+    for (int w = 0; w < kCoopWarps; ++w) M += S->ws[0][w];
+    __syncthreads();
+  }
   int32_t E = 0;
   if (P.mode == kModeEvict) {
     E = *P.evict_n_dev;
@@ -300,249 +436,344 @@ __global__ void __launch_bounds__(kSelThreads, 1) plan_kernel(const PlanParams P
     E = static_cast<int32_t>(M) - n_free0;
     E = E < 0 ? 0 : E;
   }
+  if (E > 0 && !any_evictable) {
+    if (c == 0 && threadIdx.x == 0) set_status(P.status, ECHO_DEV_POOL_EXHAUSTED);
+    E = 0;
+  }
+  uint32_t T = 0, needT = 0;
   if (E > 0) {
-    uint32_t cnt = 0, mn = 0xFFFFFFFFu, mx = 0;
-    for (int i = t0; i < t1; ++i) {
-      const uint32_t key = keys[i];
-      if (key < kProtKey) {
-        ++cnt;
-        mn = min(mn, key);
-        mx = max(mx, key);
+    uint32_t prefix = 0;  // priority - pmin, the digits above `shift` fixed so far
+    uint32_t need = static_cast<uint32_t>(E);
+    for (int lvl = 0;; ++lvl) {
+      const uint32_t *gh = P.ws.hist + lvl * kHistBins;
+      constexpr int per = kHistBins / kCoopThreads;  // 8 consecutive bins per thread
+      uint32_t cnt[per];
+      uint32_t mine = 0;
+#pragma unroll
+      for (int u = 0; u < per; ++u) {
+        cnt[u] = __ldcg(gh + threadIdx.x * per + u);
+        mine += cnt[u];
+      }
+      uint32_t v1[1] = {mine}, ex1[1], tot1[1];
+      coop_scan<1>(v1, ex1, tot1, S);
+      if (lvl == 0 && tot1[0] < need) {  // fewer evictable slots than asked
+        if (c == 0 && threadIdx.x == 0) set_status(P.status, ECHO_DEV_POOL_EXHAUSTED);
+        need = tot1[0];
+        E = static_cast<int32_t>(tot1[0]);
+      }
+      if (need == 0) break;  // nothing evictable after all (same answer in every CTA)
+      uint32_t run = ex1[0];
+#pragma unroll
+      for (int u = 0; u < per; ++u) {
+        if (run < need && run + cnt[u] >= need) {
+          S->red[0] = static_cast<uint32_t>(threadIdx.x * per + u);
+          S->red[1] = run;
+        }
+        run += cnt[u];
+      }
+      __syncthreads();
+      const uint32_t d = S->red[0];
+      need -= S->red[1];
+      prefix |= d << shift;
+      __syncthreads();
+      if (shift == 0) break;
+      // refine: the slots in bin d, by the next (up to 12) bits
+      const int nshift = shift > 12 ? shift - 12 : 0;
+      const uint32_t mask = (1u << (shift - nshift)) - 1u;
+      for (int i = threadIdx.x; i < kHistBins; i += kCoopThreads) S->hist[i] = 0;
+      __syncthreads();
+      for (int s = s_lo + threadIdx.x; s < s_hi; s += kCoopThreads) {
+        const int32_t pr = P.pool.prio[s];
+        if (!evictable(P.pool.free_[s], pr, clock)) continue;
+        const uint32_t x = static_cast<uint32_t>(pr) - pmin;
+        if ((x >> shift) == (prefix >> shift)) atomicAdd(&S->hist[(x >> nshift) & mask], 1u);
+      }
+      __syncthreads();
+      for (int i = threadIdx.x; i < kHistBins; i += kCoopThreads)
+        if (S->hist[i]) atomicAdd(P.ws.hist + (lvl + 1) * kHistBins + i, S->hist[i]);
+      shift = nshift;
+      if (!grid_barrier(glob, P.status, S)) return;
+    }
+    T = pmin + prefix;
+    needT = need;
+  }
+  {
+    uint32_t lt = 0, eq = 0, fr = 0;
+    for (int s = s_lo + threadIdx.x; s < s_hi; s += kCoopThreads) {
+      const uint8_t f8 = P.pool.free_[s];
+      if (f8) {
+        ++fr;
+      } else if (E > 0) {
+        const int32_t pr = P.pool.prio[s];
+        if (evictable(0, pr, clock)) {
+          lt += static_cast<uint32_t>(pr) < T;
+          eq += static_cast<uint32_t>(pr) == T;
+        }
       }
     }
-    uint32_t ec, dz, tc, tz;
-    sel_block_scan2(cnt, 0, ec, dz, tc, tz, S);
-    uint32_t pc, pz, eligible, gz;
-    sel_cluster_prefix2(cl, S, tc, 0, pc, pz, eligible, gz);
-    if (static_cast<uint32_t>(E) > eligible) {
-      if (rank == 0 && threadIdx.x == 0) set_status(P.status, ECHO_DEV_POOL_EXHAUSTED);
-      E = static_cast<int32_t>(eligible);
+    uint32_t v3[3] = {lt, eq, fr}, ex3[3], tot3[3];
+    coop_scan<3>(v3, ex3, tot3, S);
+    if (threadIdx.x == 0) {
+      P.ws.cta[c * kCVals + kCLt] = tot3[0];
+      P.ws.cta[c * kCVals + kCEq] = tot3[1];
+      P.ws.cta[c * kCVals + kCFree] = tot3[2];
     }
   }
-  if (E > 0) {
-    uint32_t mn = 0xFFFFFFFFu, mx = 0;
-    for (int i = t0; i < t1; ++i) {
-      const uint32_t key = keys[i];
-      if (key < kProtKey) {
-        mn = min(mn, key);
-        mx = max(mx, key);
+  ECHO_TRACE_MARK(5);
+  if (!grid_barrier(glob, P.status, S)) return;
+  ECHO_TRACE_MARK(6);
+
+  // ===== P4: ranks; owned misses listed in entry order; victims evicted; free-slot list =====
+  {
+    // sums over lower CTAs (pre) and over all CTAs (tot) of the per-CTA counts
+    uint32_t a[kCVals] = {0, 0, 0, 0}, t4[kCVals] = {0, 0, 0, 0};
+    for (int r = threadIdx.x; r < G; r += kCoopThreads) {
+#pragma unroll
+      for (int k = 0; k < kCVals; ++k) {
+        const uint32_t x = __ldcg(P.ws.cta + r * kCVals + k);
+        if (r < c) a[k] += x;
+        t4[k] += x;
       }
     }
-    ECHO_TRACE_MARK(4);
-    uint32_t pmin, pmax;
-    sel_cluster_minmax(cl, S, mn, mx, pmin, pmax);
-    ECHO_TRACE_MARK(5);
-    uint32_t T, needT;
-    sel_radix_select(cl, S, nloc, pmin, pmax, static_cast<uint32_t>(E), false,
-                     [&](int i, uint32_t &key) {
-                       key = keys[i];
-                       return key < kProtKey;
-                     },
-                     T, needT);
-    ECHO_TRACE_MARK(6);
-    // victims: priority < T, or == T among the first needT in slot order
-    uint32_t lt = 0, eq = 0;
-    for (int i = t0; i < t1; ++i) {
-      const uint32_t key = keys[i];
-      lt += key < T;
-      eq += key == T;
+#pragma unroll
+    for (int k = 0; k < kCVals; ++k)
+      for (int o = 16; o > 0; o >>= 1) {
+        a[k] += __shfl_xor_sync(0xffffffffu, a[k], o);
+        t4[k] += __shfl_xor_sync(0xffffffffu, t4[k], o);
+      }
+    if (lane == 0)
+#pragma unroll
+      for (int k = 0; k < kCVals; ++k) {
+        S->ws[k][warp] = a[k];
+      }
+    __syncthreads();
+    if (threadIdx.x < kCVals) {
+      uint32_t x = 0;
+      for (int w = 0; w < kCoopWarps; ++w) x += S->ws[threadIdx.x][w];
+      S->pre[threadIdx.x] = x;
     }
-    uint32_t elt, eeq, tlt, teq;
-    sel_block_scan2(lt, eq, elt, eeq, tlt, teq, S);
-    uint32_t plt, peq, glt, geq;
-    sel_cluster_prefix2(cl, S, tlt, teq, plt, peq, glt, geq);
-    uint32_t ob = plt + elt, eb = peq + eeq;
-    for (int i = t0; i < t1; ++i) {
-      const uint32_t key = keys[i];
-      bool victim = false;
-      uint32_t pos = 0;
-      if (key < T) {
-        victim = true;
-        pos = ob + (eb < needT ? eb : needT);
-        ++ob;
-      } else if (key == T) {
-        if (eb < needT) {
-          victim = true;
-          pos = ob + eb;
+    __syncthreads();
+    if (lane == 0)
+#pragma unroll
+      for (int k = 0; k < kCVals; ++k) S->ws[k][warp] = t4[k];
+    __syncthreads();
+    if (threadIdx.x < kCVals) {
+      uint32_t x = 0;
+      for (int w = 0; w < kCoopWarps; ++w) x += S->ws[threadIdx.x][w];
+      S->tot[threadIdx.x] = x;
+    }
+    __syncthreads();
+  }
+  const uint32_t pre_own = S->pre[kCOwn], pre_lt = S->pre[kCLt], pre_eq = S->pre[kCEq], pre_fr = S->pre[kCFree];
+  const uint32_t free_total = S->tot[kCFree];
+  const int32_t A = (P.mode == kModeEvict) ? 0 : static_cast<int32_t>(min(M, free_total + static_cast<uint32_t>(E)));
+  __syncthreads();
+  // owned misses, in entry order (contiguous per-thread segments)
+  if (P.mode != kModeEvict) {
+    const int cnt = e_hi - e_lo;
+    const int per = (cnt + kCoopThreads - 1) / kCoopThreads;
+    const int f0 = e_lo + min(cnt, static_cast<int>(threadIdx.x) * per);
+    const int f1 = e_lo + min(cnt, static_cast<int>(threadIdx.x + 1) * per);
+    uint32_t own = 0;
+    for (int f = f0; f < f1; ++f) {
+      const int32_t h = P.ws.entry_h[f];
+      if (h >= 0 && P.pool.h2g[h] == kClaim + f) ++own;
+    }
+    uint32_t v1[1] = {own}, ex1[1], tot1[1];
+    coop_scan<1>(v1, ex1, tot1, S);
+    uint32_t r = pre_own + ex1[0];
+    for (int f = f0; f < f1; ++f) {
+      const int32_t h = P.ws.entry_h[f];
+      if (h >= 0 && P.pool.h2g[h] == kClaim + f) {
+        P.ws.miss_f[r] = f;
+        P.ws.miss_h[r] = h;
+        ++r;
+      }
+    }
+  }
+  // slots: victims (priority < T, or == T among the first needT in slot order) and
+  // free-slot ranks, in slot order (contiguous per-thread segments)
+  {
+    const int cnt = s_hi - s_lo;
+    const int per = (cnt + kCoopThreads - 1) / kCoopThreads;
+    const int q0 = s_lo + min(cnt, static_cast<int>(threadIdx.x) * per);
+    const int q1 = s_lo + min(cnt, static_cast<int>(threadIdx.x + 1) * per);
+    uint32_t lt = 0, eq = 0, fr = 0;
+    for (int s = q0; s < q1; ++s) {
+      const uint8_t f8 = P.pool.free_[s];
+      if (f8) {
+        ++fr;
+      } else if (E > 0) {
+        const int32_t pr = P.pool.prio[s];
+        if (evictable(0, pr, clock)) {
+          lt += static_cast<uint32_t>(pr) < T;
+          eq += static_cast<uint32_t>(pr) == T;
         }
-        ++eb;
+      }
+    }
+    uint32_t v3[3] = {lt, eq, fr}, ex3[3], tot3[3];
+    coop_scan<3>(v3, ex3, tot3, S);
+    uint32_t lt_b = pre_lt + ex3[0], eq_b = pre_eq + ex3[1], fr_b = pre_fr + ex3[2];
+    for (int s = q0; s < q1; ++s) {
+      const uint8_t f8 = P.pool.free_[s];
+      // victims before s (all evictable slots below T, the first needT at T), and
+      // the slots before s that are free after the eviction (free ones and victims)
+      const uint32_t vb = lt_b + min(eq_b, needT);
+      const uint32_t before = fr_b + vb;
+      if (f8) {
+        if (before < static_cast<uint32_t>(A)) P.ws.alloc_slot[before] = s;
+        ++fr_b;
+        continue;
+      }
+      if (E == 0) continue;
+      const int32_t pr = P.pool.prio[s];
+      if (!evictable(0, pr, clock)) continue;
+      bool victim = false;
+      if (static_cast<uint32_t>(pr) < T) {
+        victim = true;
+        ++lt_b;
+      } else if (static_cast<uint32_t>(pr) == T) {
+        victim = eq_b < needT;
+        ++eq_b;
       }
       if (!victim) continue;
-      const int s = lo + i;
       const int32_t h = P.pool.to_host[s];
-      keys[i] = kFreeKey;
       P.pool.free_[s] = 1;
       P.pool.prio[s] = -1;
       if (h >= 0 && h < P.pool.n_h) P.pool.h2g[h] = kInf;
       P.pool.to_host[s] = kInf;
-      if (P.mode == kModeEvict) P.pool.idxbuf[pos] = s;
+      if (P.mode == kModeEvict) P.pool.idxbuf[vb] = s;  // evicted slots in ascending order
+      if (before < static_cast<uint32_t>(A)) P.ws.alloc_slot[before] = s;
     }
   }
   ECHO_TRACE_MARK(7);
-  __syncthreads();
-  cl.sync();  // miss lists of every CTA written, evictions done
+  if (!grid_barrier(glob, P.status, S)) return;
   ECHO_TRACE_MARK(8);
 
-  // ===== phase C: the r-th miss takes the r-th lowest free slot =====
-  int32_t A = 0;
-  if (P.mode != kModeEvict) {
-    uint32_t nf = 0;
-    for (int i = t0; i < t1; ++i) nf += keys[i] == kFreeKey;
-    uint32_t enf, dz, tnf, tz;
-    sel_block_scan2(nf, 0, enf, dz, tnf, tz, S);
-    uint32_t pnf, pz, gnf, gz;
-    sel_cluster_prefix2(cl, S, tnf, 0, pnf, pz, gnf, gz);
-    A = static_cast<int32_t>(M < gnf ? M : gnf);
-    uint32_t r = pnf + enf;
-    for (int i = t0; i < t1 && r < static_cast<uint32_t>(A); ++i) {
-      if (keys[i] != kFreeKey) continue;
-      const int s = lo + i;
-      const int32_t f = P.ws.miss_f[r];
-      const int32_t h = P.ws.miss_h[r];
-      keys[i] = kProtKey;
+  // ===== P5: the r-th miss takes the r-th free slot; KV rows copied =====
+  for (int r = gtid; r < static_cast<int>(M); r += gthreads) {
+    const int32_t f = P.ws.miss_f[r], h = P.ws.miss_h[r];
+    if (r < A) {
+      const int32_t s = P.ws.alloc_slot[r];
       P.pool.free_[s] = 0;
       P.pool.prio[s] = clock;
       P.pool.to_host[s] = h;
       P.pool.h2g[h] = s;
       P.pool.idxbuf[r] = s;
-      P.ws.alloc_slot[r] = s;
       if (P.mode == kModeAlloc) P.out_slots[f] = s;
-      ++r;
-    }
-    // misses beyond the free slots stay out of the pool
-    const int gt = rank * kSelThreads + threadIdx.x;
-    for (int rr = A + gt; rr < static_cast<int>(M); rr += C * kSelThreads) {
-      const int32_t f = P.ws.miss_f[rr];
-      P.pool.h2g[P.ws.miss_h[rr]] = kInf;
+    } else {  // no slot left: the row stays out of the pool
+      P.pool.h2g[h] = kInf;
       if (P.mode == kModeRecall) P.ws.miss_stage[f] = -1;
       if (P.mode == kModeAlloc) P.out_slots[f] = -1;
     }
-    if (static_cast<int32_t>(M) > A && rank == 0 && threadIdx.x == 0) set_status(P.status, ECHO_DEV_POOL_EXHAUSTED);
   }
-  ECHO_TRACE_MARK(9);
-  // -1 over the rest of the previous index list
+  if (static_cast<int32_t>(M) > A && c == 0 && threadIdx.x == 0) set_status(P.status, ECHO_DEV_POOL_EXHAUSTED);
   const int32_t list_len = P.mode == kModeEvict ? E : A;
-  {
-    const int gt = rank * kSelThreads + threadIdx.x;
-    for (int i = list_len + gt; i < prev_idx && i < n_g; i += C * kSelThreads) P.pool.idxbuf[i] = -1;
+  for (int i = list_len + gtid; i < prev_idx && i < n_g; i += gthreads) P.pool.idxbuf[i] = -1;
+  if (P.mode == kModeRecall || P.mode == kModeAppend) {
+    constexpr int kRows = 4;  // rows a warp moves at once (9 16-byte vectors in flight per lane)
+    const int4 *host = reinterpret_cast<const int4 *>(P.pool.host_kv);
+    const int4 *stg = reinterpret_cast<const int4 *>(P.stage_rows);
+    const int4 *nkv = reinterpret_cast<const int4 *>(P.new_kv);
+    int4 *dst = reinterpret_cast<int4 *>(P.pool.gpu_kv);
+    unsigned long long used = 0;
+    const int gw = gtid >> 5, nw = gthreads >> 5;
+    for (int r0 = gw * kRows; r0 < A; r0 += nw * kRows) {
+      const int nr = A - r0 < kRows ? A - r0 : kRows;
+      const int4 *src[kRows];
+      int32_t slot[kRows];
+#pragma unroll
+      for (int u = 0; u < kRows; ++u) {
+        src[u] = nullptr;
+        slot[u] = 0;
+        if (u < nr) {
+          const int32_t f = P.ws.miss_f[r0 + u];
+          slot[u] = P.ws.alloc_slot[r0 + u];
+          if (P.mode == kModeAppend) {
+            src[u] = nkv + static_cast<size_t>(f) * kKvChunks;
+          } else {
+            const int32_t st = P.ws.miss_stage[f];
+            if (st >= 0) {
+              src[u] = stg + static_cast<size_t>(st) * kKvChunks;
+              used += lane == 0;
+            } else {
+              src[u] = host + static_cast<size_t>(P.ws.miss_h[r0 + u]) * kKvChunks;
+            }
+          }
+        }
+      }
+      constexpr int kPer = (kRows * kKvChunks + 31) / 32;
+      int4 buf[kPer];
+#pragma unroll
+      for (int m = 0; m < kPer; ++m) {
+        const int idx = m * 32 + lane;
+        const int u = idx / kKvChunks, ch = idx % kKvChunks;
+        if (u < nr) buf[m] = __ldcs(src[u] + ch);
+      }
+#pragma unroll
+      for (int m = 0; m < kPer; ++m) {
+        const int idx = m * 32 + lane;
+        const int u = idx / kKvChunks, ch = idx % kKvChunks;
+        if (u < nr) dst[static_cast<size_t>(slot[u]) * kKvChunks + ch] = buf[m];
+      }
+      if (P.mode == kModeRecall && lane < nr) P.ws.miss_stage[P.ws.miss_f[r0 + lane]] = -1;
+    }
+    add_stat(P.stats, &echo_stats::staged_used, used);
   }
-  cl.sync();
-  if (rank == 0 && threadIdx.x == 0) {
+  // scratch back to its resting state (nothing reads it any more)
+  for (int i = gtid; i < kHistLevels * kHistBins; i += gthreads) P.ws.hist[i] = 0;
+  if (c == 0 && threadIdx.x == 0) {
     P.pool.counters[0] = n_free0 + E - A;
     P.pool.counters[1] = list_len;
     P.ws.ctr[kCtrMisses] = static_cast<int32_t>(M);
     P.ws.ctr[kCtrGranted] = A;
-    if (P.stats) {
-      auto add = [](int64_t *dst, unsigned long long v) {
-        atomicAdd(reinterpret_cast<unsigned long long *>(dst), v);
-      };
-      if (P.mode == kModeRecall) {
-        add(&P.stats->steps, 1ull);
-        add(&P.stats->selected, n_sel);
-        add(&P.stats->unique_rows, M + n_hit);
-        add(&P.stats->hits, n_hit);
-        add(&P.stats->misses, M);
-        add(&P.stats->recalled, static_cast<unsigned long long>(A));
-        add(&P.stats->unrecalled, static_cast<unsigned long long>(M - A));
-      }
-      if (P.mode == kModeAppend) add(&P.stats->appended, M);
-      add(&P.stats->evicted, static_cast<unsigned long long>(E));
+    const uint32_t valid = glob[kGValid];
+    glob[kGValid] = 0;
+    glob[kGMin] = 0xFFFFFFFFu;
+    glob[kGMax] = 0;
+    if (P.mode == kModeRecall) {
+      add_stat(P.stats, &echo_stats::steps, 1ull);
+      add_stat(P.stats, &echo_stats::selected, valid);
+      add_stat(P.stats, &echo_stats::unique_rows, static_cast<unsigned long long>(M));  // + hits, in P6
+      add_stat(P.stats, &echo_stats::misses, M);
+      add_stat(P.stats, &echo_stats::recalled, static_cast<unsigned long long>(A));
+      add_stat(P.stats, &echo_stats::unrecalled, static_cast<unsigned long long>(M - A));
     }
+    if (P.mode == kModeAppend) add_stat(P.stats, &echo_stats::appended, M);
+    add_stat(P.stats, &echo_stats::evicted, static_cast<unsigned long long>(E));
+    if (P.clock_advance) *P.clock_advance = clock + 1;  // every CTA read the clock at its start
   }
-  if (P.stats && P.mode == kModeRecall && staged_total)
-    atomicAdd(reinterpret_cast<unsigned long long *>(&P.stats->staged), static_cast<unsigned long long>(staged_total));
+  if (c == 0)
+    for (int i = threadIdx.x; i < P.n_ema; i += kCoopThreads) ema_one(P.s_hat, P.kth, i, P.alpha);
+  ECHO_TRACE_MARK(9);
+  if (P.mode != kModeRecall) return;
+  if (!grid_barrier(glob, P.status, S)) return;
+
+  // ===== P6 (recall): out_slot of every entry; each hit counted and cleared by its owner =====
+  uint32_t hits = 0;
+  for (int f = gtid; f < n; f += gthreads) {
+    const int32_t h = P.ws.entry_h[f];
+    int32_t o = -1;
+    if (h >= 0) {
+      const int32_t v = P.pool.h2g[h];
+      if (v >= 0 && v < n_g) {
+        o = v;
+        if (P.ws.slot_claim[v] == f) {
+          ++hits;
+          P.ws.slot_claim[v] = INT32_MAX;
+        }
+      }
+    }
+    P.out_slot[f] = o;
+  }
+  for (int o = 16; o > 0; o >>= 1) hits += __shfl_xor_sync(0xffffffffu, hits, o);
+  if (lane == 0 && hits) {
+    add_stat(P.stats, &echo_stats::hits, hits);
+    add_stat(P.stats, &echo_stats::unique_rows, hits);
+  }
+  if (P.stage_count && c == 0)
+    for (int b = threadIdx.x; b < P.B; b += kCoopThreads) P.stage_count[b] = 0;
   ECHO_TRACE_MARK(10);
-}
-
-// ---------------------------------------------------------------------------
-// copy: recalled / appended rows into their slots; out_slot of every entry
-// ---------------------------------------------------------------------------
-struct CopyParams {
-  PoolView pool;
-  Workspace ws;
-  int mode;
-  const uint16_t *stage_rows;  // recall: staged rows
-  const uint16_t *new_kv;      // append: source rows by request
-  // out_slot (recall)
-  const int32_t *sel;
-  const int32_t *req_to_host;
-  int F, n_q, k, L_max;
-  int32_t *out_slot;
-  int32_t *stage_count;
-  int B;
-  echo_stats *stats;
-};
-
-constexpr int kCopyRows = 4;  // rows a warp moves at once (9 vectors in flight per lane)
-
-__global__ void __launch_bounds__(256) copy_kernel(const CopyParams P) {
-  const int lane = threadIdx.x & 31;
-  const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int nwarps = (gridDim.x * blockDim.x) >> 5;
-  const int A = P.ws.ctr[kCtrGranted];
-  const int4 *host = reinterpret_cast<const int4 *>(P.pool.host_kv);
-  const int4 *stg = reinterpret_cast<const int4 *>(P.stage_rows);
-  const int4 *newkv = reinterpret_cast<const int4 *>(P.new_kv);
-  int4 *dst = reinterpret_cast<int4 *>(P.pool.gpu_kv);
-  unsigned long long used = 0;
-  for (int r0 = gwarp * kCopyRows; r0 < A; r0 += nwarps * kCopyRows) {
-    const int n = A - r0 < kCopyRows ? A - r0 : kCopyRows;
-    const int4 *src[kCopyRows];
-    int32_t slot[kCopyRows];
-#pragma unroll
-    for (int r = 0; r < kCopyRows; ++r) {
-      src[r] = nullptr;
-      slot[r] = 0;
-      if (r < n) {
-        const int32_t f = P.ws.miss_f[r0 + r];
-        slot[r] = P.ws.alloc_slot[r0 + r];
-        if (P.mode == kModeAppend) {
-          src[r] = newkv + static_cast<size_t>(f) * kKvChunks;
-        } else {
-          const int32_t st = P.ws.miss_stage[f];
-          if (st >= 0) {
-            src[r] = stg + static_cast<size_t>(st) * kKvChunks;
-            used += lane == 0;
-          } else {
-            src[r] = host + static_cast<size_t>(P.ws.miss_h[r0 + r]) * kKvChunks;
-          }
-        }
-      }
-    }
-    constexpr int kPer = (kCopyRows * kKvChunks + 31) / 32;
-    int4 buf[kPer];
-#pragma unroll
-    for (int m = 0; m < kPer; ++m) {
-      const int idx = m * 32 + lane;
-      const int r = idx / kKvChunks, c = idx % kKvChunks;
-      if (r < n) buf[m] = __ldcs(src[r] + c);
-    }
-#pragma unroll
-    for (int m = 0; m < kPer; ++m) {
-      const int idx = m * 32 + lane;
-      const int r = idx / kKvChunks, c = idx % kKvChunks;
-      if (r < n) dst[static_cast<size_t>(slot[r]) * kKvChunks + c] = buf[m];
-    }
-    if (P.mode == kModeRecall && lane < n) P.ws.miss_stage[P.ws.miss_f[r0 + lane]] = -1;
-  }
-  if (P.stats && used) atomicAdd(reinterpret_cast<unsigned long long *>(&P.stats->staged_used), used);
-
-  if (P.mode == kModeRecall) {
-    for (int f = blockIdx.x * blockDim.x + threadIdx.x; f < P.F; f += gridDim.x * blockDim.x) {
-      const int32_t p = P.sel[f];
-      int32_t o = -1;
-      if (p >= 0 && p < P.L_max) {
-        const int32_t h = P.req_to_host[static_cast<size_t>(f / (P.n_q * P.k)) * P.L_max + p];
-        if (h >= 0 && h < P.pool.n_h) {
-          const int32_t v = P.pool.h2g[h];
-          o = (v >= 0 && v < P.pool.n_g) ? v : -1;
-        }
-      }
-      P.out_slot[f] = o;
-    }
-    if (P.stage_count && blockIdx.x == 0)
-      for (int b = threadIdx.x; b < P.B; b += blockDim.x) P.stage_count[b] = 0;
-  }
 }
 
 // ---------------------------------------------------------------------------
@@ -572,13 +803,14 @@ __global__ void append_prepare_kernel(PoolView pool, Workspace ws, uint8_t *k_in
   __syncthreads();
   const int32_t h = sh_h, p = sh_p;
   if (h >= 0) {
-    // the host copy is written at generation (write-through), the GPU copy later by copy_kernel
+    // the host copy is written at generation (write-through); the GPU copy follows
+    // in the allocation kernel
     const int4 *src = reinterpret_cast<const int4 *>(new_kv) + static_cast<size_t>(b) * kKvChunks;
     int4 *hdst = reinterpret_cast<int4 *>(const_cast<uint16_t *>(pool.host_kv)) + static_cast<size_t>(h) * kKvChunks;
-    for (int c = threadIdx.x; c < kKvChunks; c += blockDim.x) hdst[c] = src[c];
+    for (int i = threadIdx.x; i < kKvChunks; i += blockDim.x) hdst[i] = src[i];
     const int4 *ksrc = reinterpret_cast<const int4 *>(new_k_index) + static_cast<size_t>(b) * (kDim / 16);
     int4 *kdst = reinterpret_cast<int4 *>(k_index + (static_cast<size_t>(b) * L_max + p) * kDim);
-    for (int c = threadIdx.x; c < kDim / 16; c += blockDim.x) kdst[c] = ksrc[c];
+    for (int i = threadIdx.x; i < kDim / 16; i += blockDim.x) kdst[i] = ksrc[i];
   }
   if (threadIdx.x == 0) {
     ws.entry_rows[b] = h;
@@ -596,7 +828,7 @@ __global__ void append_prepare_kernel(PoolView pool, Workspace ws, uint8_t *k_in
 }
 
 // ---------------------------------------------------------------------------
-// initialisation, EMA, clock
+// initialisation, EMA
 // ---------------------------------------------------------------------------
 __global__ void pool_init_kernel(PoolView pool) {
   const int tid = blockIdx.x * blockDim.x + threadIdx.x, nt = gridDim.x * blockDim.x;
@@ -619,25 +851,15 @@ __global__ void ws_init_kernel(Workspace ws, int n_g, int max_rows) {
   const int tid = blockIdx.x * blockDim.x + threadIdx.x, nt = gridDim.x * blockDim.x;
   for (int s = tid; s < n_g; s += nt) ws.slot_claim[s] = INT32_MAX;
   for (int i = tid; i < max_rows; i += nt) ws.miss_stage[i] = -1;
+  for (int i = tid; i < kHistLevels * kHistBins; i += nt) ws.hist[i] = 0;
+  for (int i = tid; i < kMaxGrid * kCVals; i += nt) ws.cta[i] = 0;
+  for (int i = tid; i < kGCount; i += nt) ws.glob[i] = (i == kGMin) ? 0xFFFFFFFFu : 0u;
   for (int i = tid; i < kCtrCount; i += nt) ws.ctr[i] = 0;
 }
 
-__global__ void ema_kernel(float *s_hat, const float *kth, int n, float alpha, int32_t *clock_dev, int advance) {
+__global__ void ema_kernel(float *s_hat, const float *kth, int n, float alpha) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < n) {
-    const float x = kth[i];
-    if (isfinite(x)) {
-      const float s = s_hat[i];
-      if (isinf(s) && s > 0.f) {
-        s_hat[i] = x;
-      } else {
-        const float a = __fmul_rn(alpha, s);
-        const float c = __fmul_rn(__fsub_rn(1.0f, alpha), x);
-        s_hat[i] = __fadd_rn(a, c);
-      }
-    }
-  }
-  if (i == 0 && clock_dev && advance) *clock_dev += 1;
+  if (i < n) ema_one(s_hat, kth, i, alpha);
 }
 
 }  // namespace echo
@@ -685,8 +907,8 @@ static int check(const char *what) {
 }
 
 int launch_workspace_init(const echo_workspace *w, cudaStream_t s) {
-  echo::ws_init_kernel<<<grid_for(w->n_g > w->max_rows ? w->n_g : w->max_rows, 256), 256, 0, s>>>(ws_of(w), w->n_g,
-                                                                                                w->max_rows);
+  const int n = w->n_g > w->max_rows ? w->n_g : w->max_rows;
+  echo::ws_init_kernel<<<grid_for(n > 65536 ? n : 65536, 256), 256, 0, s>>>(ws_of(w), w->n_g, w->max_rows);
   return check("workspace init");
 }
 
@@ -695,9 +917,9 @@ int launch_pool_init(const echo_pool *p, cudaStream_t s) {
   return check("pool init");
 }
 
-static echo::PlanParams base_params(const echo_pool *pool, const echo_workspace *ws, int mode, int32_t clock,
-                                    const int32_t *clock_dev, int32_t *status) {
-  echo::PlanParams P{};
+static echo::OpParams base_params(const echo_pool *pool, const echo_workspace *ws, int mode, int32_t clock,
+                                  const int32_t *clock_dev, int32_t *status) {
+  echo::OpParams P{};
   P.pool = view_of(pool);
   P.ws = ws_of(ws);
   P.mode = mode;
@@ -709,66 +931,47 @@ static echo::PlanParams base_params(const echo_pool *pool, const echo_workspace 
   return P;
 }
 
-// one cluster of 8 CTAs (16 for pools above 8 x kPlanMaxChunk slots)
-static int run_plan(const echo::PlanParams &P, cudaStream_t s) {
-  const int C = P.pool.n_g <= 8 * echo::kPlanMaxChunk ? 8 : 16;
-  const int chunk = (P.pool.n_g + C - 1) / C;
-  if (chunk > echo::kPlanMaxChunk) {
-    set_error("pool of %d slots exceeds the supported %d", P.pool.n_g, 16 * echo::kPlanMaxChunk);
-    return ECHO_ENOTSUP;
-  }
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(echo::plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(echo::plan_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return cuda_fail(e, "plan kernel attributes");
-    attr = true;
-  }
+// one cooperative launch over all SMs (one CTA each)
+static int run_op(const echo::OpParams &P, cudaStream_t s) {
+  const int grid = sm_count() < echo::kMaxGrid ? sm_count() : echo::kMaxGrid;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(C);
-  cfg.blockDim = dim3(echo::kSelThreads);
-  cfg.dynamicSmemBytes = sizeof(echo::SelSmem) + static_cast<size_t>(chunk) * sizeof(uint32_t);
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(echo::kCoopThreads);
+  cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = C;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
+  at[0].id = cudaLaunchAttributeCooperative;
+  at[0].val.cooperative = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, echo::plan_kernel, P);
-  return e == cudaSuccess ? ECHO_OK : cuda_fail(e, "cache-manager plan");
+  cudaError_t e = cudaLaunchKernelEx(&cfg, echo::cache_op_kernel, P);
+  return e == cudaSuccess ? ECHO_OK : cuda_fail(e, "cache-manager kernel");
 }
 
 int launch_pool_alloc(const echo_pool *pool, const echo_workspace *ws, const int32_t *host_idx, const int32_t *n_dev,
                       int32_t max_n, int32_t clock, const int32_t *clock_dev, int32_t *out_slots, int32_t *status,
                       cudaStream_t s) {
-  echo::PlanParams P = base_params(pool, ws, echo::kModeAlloc, clock, clock_dev, status);
+  echo::OpParams P = base_params(pool, ws, echo::kModeAlloc, clock, clock_dev, status);
   P.F = max_n;
   P.rows = host_idx;
   P.n_dev = n_dev;
   P.out_slots = out_slots;
-  if (max_n > 0) {
-    echo::claim_kernel<<<grid_for(max_n, 256), 256, 0, s>>>(P);
-    int r = check("allocate claim");
-    if (r) return r;
-  }
-  return run_plan(P, s);
+  return run_op(P, s);
 }
 
 int launch_pool_evict(const echo_pool *pool, const echo_workspace *ws, const int32_t *n_needed_dev, int32_t clock,
                       const int32_t *clock_dev, int32_t *status, cudaStream_t s) {
-  echo::PlanParams P = base_params(pool, ws, echo::kModeEvict, clock, clock_dev, status);
+  echo::OpParams P = base_params(pool, ws, echo::kModeEvict, clock, clock_dev, status);
   P.evict_n_dev = n_needed_dev;
-  return run_plan(P, s);
+  return run_op(P, s);
 }
 
 int launch_recall(const echo_pool *pool, const echo_workspace *ws, const int32_t *sel, const int32_t *req_to_host,
                   const int32_t *ctx_len, int B, int n_q, int k, int L_max, const echo_stage *stage, int32_t clock,
-                  const int32_t *clock_dev, int32_t *out_slot, echo_stats *stats, int32_t *status, cudaStream_t s) {
-  echo::PlanParams P = base_params(pool, ws, echo::kModeRecall, clock, clock_dev, status);
-  const int F = B * n_q * k;
-  P.F = F;
+                  const int32_t *clock_dev, int32_t *out_slot, echo_stats *stats, int32_t *status, cudaStream_t s,
+                  float *ema_s_hat, const float *ema_kth, int ema_n, float ema_alpha, int32_t *clock_advance) {
+  echo::OpParams P = base_params(pool, ws, echo::kModeRecall, clock, clock_dev, status);
+  P.F = B * n_q * k;
   P.sel = sel;
   P.req_to_host = req_to_host;
   P.n_q = n_q;
@@ -777,64 +980,40 @@ int launch_recall(const echo_pool *pool, const echo_workspace *ws, const int32_t
   P.B = B;
   P.ctx_len = ctx_len;
   P.stats = stats;
+  P.out_slot = out_slot;
   if (stage) {
     P.stage_host = stage->host_row;
     P.stage_count = stage->count;
+    P.stage_rows = stage->rows;
     P.stage_stride = stage->stride;
     P.cap_div = stage->cap_div;
   }
-  if (F > 0) {
-    echo::claim_kernel<<<grid_for(F, 256), 256, 0, s>>>(P);
-    int r = check("recall claim");
-    if (r) return r;
-  }
-  int r = run_plan(P, s);
-  if (r) return r;
-  echo::CopyParams C{};
-  C.pool = P.pool;
-  C.ws = P.ws;
-  C.mode = echo::kModeRecall;
-  C.stage_rows = stage ? stage->rows : nullptr;
-  C.sel = sel;
-  C.req_to_host = req_to_host;
-  C.F = F;
-  C.n_q = n_q;
-  C.k = k;
-  C.L_max = L_max;
-  C.out_slot = out_slot;
-  C.stage_count = stage ? stage->count : nullptr;
-  C.B = B;
-  C.stats = stats;
-  echo::copy_kernel<<<grid_for(F > 1024 ? F : 1024, 256), 256, 0, s>>>(C);
-  return check("recall copy");
+  P.s_hat = ema_s_hat;
+  P.kth = ema_kth;
+  P.n_ema = ema_s_hat ? ema_n : 0;
+  P.alpha = ema_alpha;
+  P.clock_advance = clock_advance;
+  return run_op(P, s);
 }
 
 int launch_append(const echo_pool *pool, const echo_workspace *ws, uint8_t *k_index, int32_t *ctx_len,
                   const int32_t *req_to_host, int B, int L_max, const uint16_t *new_kv, const uint8_t *new_k_index,
                   int32_t clock, const int32_t *clock_dev, echo_stats *stats, int32_t *status, cudaStream_t s) {
   if (B == 0) return ECHO_OK;
-  echo::PlanParams P = base_params(pool, ws, echo::kModeAppend, clock, clock_dev, status);
+  echo::OpParams P = base_params(pool, ws, echo::kModeAppend, clock, clock_dev, status);
   P.F = B;
   P.rows = P.ws.entry_rows;
+  P.new_kv = new_kv;
   P.stats = stats;
   echo::append_prepare_kernel<<<B, 128, 0, s>>>(P.pool, P.ws, k_index, ctx_len, req_to_host, B, L_max, new_kv,
                                                  new_k_index, status);
   int r = check("append prepare");
   if (r) return r;
-  r = run_plan(P, s);
-  if (r) return r;
-  echo::CopyParams C{};
-  C.pool = P.pool;
-  C.ws = P.ws;
-  C.mode = echo::kModeAppend;
-  C.new_kv = new_kv;
-  C.B = B;
-  echo::copy_kernel<<<grid_for(B * 32, 256), 256, 0, s>>>(C);
-  return check("append copy");
+  return run_op(P, s);
 }
 
-int launch_ema(float *s_hat, const float *kth, int n, float alpha, int32_t *clock_dev, int advance, cudaStream_t s) {
-  echo::ema_kernel<<<(n + 255) / 256 > 0 ? (n + 255) / 256 : 1, 256, 0, s>>>(s_hat, kth, n, alpha, clock_dev, advance);
+int launch_ema(float *s_hat, const float *kth, int n, float alpha, cudaStream_t s) {
+  echo::ema_kernel<<<(n + 255) / 256, 256, 0, s>>>(s_hat, kth, n, alpha);
   return check("ema");
 }
 

@@ -3,10 +3,11 @@
 // (the top-k of a score row; the arg-top-k of the lowest eviction priorities):
 //   - block and cluster prefix scans of two counters,
 //   - cluster min / max of the keys,
-//   - one radix step: per-CTA histogram of a digit (warp-aggregated atomics, so
-//     runs of equal digits do not serialise), cluster-wide reduction through
-//     distributed shared memory, and the digit where the running count reaches
-//     the requested rank.
+//   - one radix step: per-CTA histogram of a digit (one atomic per warp when the
+//     warp's digits agree), cluster-wide reduction through distributed shared
+//     memory (each CTA owns a slice of the bins; remote loads are issued together,
+//     never one after another), and the digit where the running count reaches the
+//     requested rank.
 // Keys are reduced to (key - min) first, so the digits cover only the bits in
 // which the keys differ (priority clocks usually span a few bits, fp32 scores of
 // one row about 25).
@@ -25,74 +26,126 @@ constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kDigitBits = 12;
 constexpr int kMaxBins = 1 << kDigitBits;
 
+constexpr int kScanVals = 4;  // counters a scan carries at most
+
 struct alignas(16) SelSmem {
   uint32_t hist[kMaxBins];
   uint32_t tot[kMaxBins];
-  uint32_t wa[kSelWarps], wb[kSelWarps];
-  uint32_t pub[4];      // values this CTA publishes to the cluster
-  uint32_t result[2];   // digit, count before it
+  uint32_t ws[kScanVals][kSelWarps];  // per-warp partial sums of a block scan
+  uint32_t pub[8];                    // values this CTA publishes to the cluster
+  uint32_t res[2 * kScanVals];        // results handed from warp 0 to the block
+  uint32_t result[2];                 // digit, count before it
 };
+
+// exclusive block scan of NV counters; block totals in tot
+template <int NV>
+__device__ __forceinline__ void sel_block_scan(const uint32_t (&v)[NV], uint32_t (&ex)[NV], uint32_t (&tot)[NV],
+                                               SelSmem *S) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t inc[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) inc[k] = v[k];
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const uint32_t u = __shfl_up_sync(0xffffffffu, inc[k], o);
+      if (lane >= o) inc[k] += u;
+    }
+  }
+  if (lane == 31) {
+#pragma unroll
+    for (int k = 0; k < NV; ++k) S->ws[k][warp] = inc[k];
+  }
+  __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      uint32_t x = S->ws[k][lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t u = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += u;
+      }
+      S->ws[k][lane] = x;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    ex[k] = (warp ? S->ws[k][warp - 1] : 0) + inc[k] - v[k];
+    tot[k] = S->ws[k][kSelWarps - 1];
+  }
+  __syncthreads();
+}
 
 // exclusive block scan of two counters; block totals in ta / tb
 __device__ __forceinline__ void sel_block_scan2(uint32_t a, uint32_t b, uint32_t &ea, uint32_t &eb, uint32_t &ta,
                                                 uint32_t &tb, SelSmem *S) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t ia = a, ib = b;
+  const uint32_t v[2] = {a, b};
+  uint32_t e[2], t[2];
+  sel_block_scan<2>(v, e, t, S);
+  ea = e[0];
+  eb = e[1];
+  ta = t[0];
+  tb = t[1];
+}
+
+constexpr int kMaxCluster = 16;
+
+// every CTA publishes NV counters; returns their sums over lower ranks (pre) and
+// over all ranks (all).  Warp 0 reads the C published vectors (one remote load per
+// lane and counter, all in flight at once), scans them, and hands the result to the
+// block through shared memory.
+template <int NV>
+__device__ __forceinline__ void sel_cluster_prefix(cg::cluster_group &cl, SelSmem *S, const uint32_t (&mine)[NV],
+                                                   uint32_t (&pre)[NV], uint32_t (&all)[NV]) {
+  if (threadIdx.x == 0) {
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t xa = __shfl_up_sync(0xffffffffu, ia, o), xb = __shfl_up_sync(0xffffffffu, ib, o);
-    if (lane >= o) {
-      ia += xa;
-      ib += xb;
-    }
+    for (int k = 0; k < NV; ++k) S->pub[k] = mine[k];
   }
-  if (lane == 31) {
-    S->wa[warp] = ia;
-    S->wb[warp] = ib;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    uint32_t x = S->wa[lane], y = S->wb[lane];
+  cl.sync();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int rank = static_cast<int>(cl.block_rank()), C = static_cast<int>(cl.num_blocks());
+    uint32_t x[NV];
+    const SelSmem *R = cl.map_shared_rank(S, lane < C ? lane : 0);
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t xa = __shfl_up_sync(0xffffffffu, x, o), xb = __shfl_up_sync(0xffffffffu, y, o);
-      if (lane >= o) {
-        x += xa;
-        y += xb;
+    for (int k = 0; k < NV; ++k) x[k] = lane < C ? R->pub[k] : 0u;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      uint32_t sx = x[k];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t u = __shfl_up_sync(0xffffffffu, sx, o);
+        if (lane >= o) sx += u;
+      }
+      const uint32_t e = __shfl_sync(0xffffffffu, sx - x[k], rank);
+      const uint32_t t = __shfl_sync(0xffffffffu, sx, 31);
+      if (lane == 0) {
+        S->res[k] = e;
+        S->res[kScanVals + k] = t;
       }
     }
-    S->wa[lane] = x;
-    S->wb[lane] = y;
   }
-  __syncthreads();
-  ea = (warp ? S->wa[warp - 1] : 0) + ia - a;
-  eb = (warp ? S->wb[warp - 1] : 0) + ib - b;
-  ta = S->wa[kSelWarps - 1];
-  tb = S->wb[kSelWarps - 1];
+  cl.sync();  // also orders the remote reads above before any CTA republishes
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    pre[k] = S->res[k];
+    all[k] = S->res[kScanVals + k];
+  }
   __syncthreads();
 }
 
-// every CTA publishes (a, b); returns the sums over lower ranks and over all ranks
 __device__ __forceinline__ void sel_cluster_prefix2(cg::cluster_group &cl, SelSmem *S, uint32_t a, uint32_t b,
                                                     uint32_t &pa, uint32_t &pb, uint32_t &ga, uint32_t &gb) {
-  if (threadIdx.x == 0) {
-    S->pub[0] = a;
-    S->pub[1] = b;
-  }
-  cl.sync();
-  const int rank = static_cast<int>(cl.block_rank()), C = static_cast<int>(cl.num_blocks());
-  pa = pb = ga = gb = 0;
-  for (int r = 0; r < C; ++r) {
-    const SelSmem *R = cl.map_shared_rank(S, r);
-    const uint32_t x = R->pub[0], y = R->pub[1];
-    if (r < rank) {
-      pa += x;
-      pb += y;
-    }
-    ga += x;
-    gb += y;
-  }
-  cl.sync();
+  const uint32_t m[2] = {a, b};
+  uint32_t p[2], g[2];
+  sel_cluster_prefix<2>(cl, S, m, p, g);
+  pa = p[0];
+  pb = p[1];
+  ga = g[0];
+  gb = g[1];
 }
 
 // cluster-wide min and max of per-thread values
@@ -105,35 +158,48 @@ __device__ __forceinline__ void sel_cluster_minmax(cg::cluster_group &cl, SelSme
     mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   }
   if (lane == 0) {
-    S->wa[warp] = mn;
-    S->wb[warp] = mx;
+    S->ws[0][warp] = mn;
+    S->ws[1][warp] = mx;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    uint32_t a = S->wa[0], b = S->wb[0];
-    for (int w = 1; w < kSelWarps; ++w) {
-      a = min(a, S->wa[w]);
-      b = max(b, S->wb[w]);
+  if (warp == 0) {
+    uint32_t a = S->ws[0][lane], b = S->ws[1][lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      a = min(a, __shfl_xor_sync(0xffffffffu, a, o));
+      b = max(b, __shfl_xor_sync(0xffffffffu, b, o));
     }
-    S->pub[2] = a;
-    S->pub[3] = b;
+    if (lane == 0) {
+      S->pub[4] = a;
+      S->pub[5] = b;
+    }
   }
   cl.sync();
-  const int C = static_cast<int>(cl.num_blocks());
-  gmn = 0xFFFFFFFFu;
-  gmx = 0;
-  for (int r = 0; r < C; ++r) {
-    const SelSmem *R = cl.map_shared_rank(S, r);
-    gmn = min(gmn, R->pub[2]);
-    gmx = max(gmx, R->pub[3]);
+  if (warp == 0) {
+    const int C = static_cast<int>(cl.num_blocks());
+    const SelSmem *R = cl.map_shared_rank(S, lane < C ? lane : 0);
+    uint32_t a = lane < C ? R->pub[4] : 0xFFFFFFFFu;
+    uint32_t b = lane < C ? R->pub[5] : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      a = min(a, __shfl_xor_sync(0xffffffffu, a, o));
+      b = max(b, __shfl_xor_sync(0xffffffffu, b, o));
+    }
+    if (lane == 0) {
+      S->res[0] = a;
+      S->res[1] = b;
+    }
   }
   cl.sync();
+  gmn = S->res[0];
+  gmx = S->res[1];
+  __syncthreads();
 }
 
 // Histogram of digit `(x >> shift) & (nb - 1)` over the slice's reduced keys x whose
 // bits above `hi` equal `prefix` (x >> hi == prefix >> hi).  `get(i, x)` returns
-// false for slots that do not take part.  Equal digits within a warp are merged
-// into one atomic.
+// false for slots that do not take part.  A warp whose taking-part lanes all hold
+// one digit adds once; otherwise each lane adds its own (bank-parallel).
 template <typename Get>
 __device__ __forceinline__ void sel_histogram(SelSmem *S, int n, int hi, int shift, int nb, uint32_t prefix,
                                               Get get) {
@@ -145,9 +211,16 @@ __device__ __forceinline__ void sel_histogram(SelSmem *S, int n, int hi, int shi
     uint32_t x = 0;
     bool act = i < n && get(i, x);
     if (act && hi < 32) act = (x >> hi) == (prefix >> hi);
-    const uint32_t bin = act ? (x >> shift) & static_cast<uint32_t>(nb - 1) : 0xFFFFFFFFu;
-    const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-    if (act && lane == __ffs(peers) - 1) atomicAdd(&S->hist[bin], static_cast<uint32_t>(__popc(peers)));
+    const uint32_t bin = (x >> shift) & static_cast<uint32_t>(nb - 1);
+    const uint32_t am = __ballot_sync(0xffffffffu, act);
+    if (am == 0) continue;
+    const int first = __ffs(am) - 1;
+    const uint32_t b0 = __shfl_sync(0xffffffffu, bin, first);
+    if (__all_sync(0xffffffffu, !act || bin == b0)) {
+      if (lane == first) atomicAdd(&S->hist[b0], static_cast<uint32_t>(__popc(am)));
+    } else if (act) {
+      atomicAdd(&S->hist[bin], 1u);
+    }
   }
   __syncthreads();
 }
@@ -159,12 +232,28 @@ __device__ __forceinline__ void sel_find_digit(cg::cluster_group &cl, SelSmem *S
                                                bool descending, uint32_t &digit, uint32_t &before) {
   cl.sync();  // every slice histogram complete
   const int C = static_cast<int>(cl.num_blocks());
-  for (int i = threadIdx.x; i < nb; i += kSelThreads) {
+  const int rank = static_cast<int>(cl.block_rank());
+  // 1. CTA `rank` owns bins [o0, o1) and sums them over the cluster (remote loads in flight together)
+  const int per_owner = (nb + C - 1) / C;
+  const int o0 = rank * per_owner < nb ? rank * per_owner : nb;
+  const int o1 = o0 + per_owner < nb ? o0 + per_owner : nb;
+  for (int i = o0 + static_cast<int>(threadIdx.x); i < o1; i += kSelThreads) {
+    uint32_t v[kMaxCluster];
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r) v[r] = r < C ? cl.map_shared_rank(S->hist, r)[i] : 0u;
     uint32_t s = 0;
-    for (int r = 0; r < C; ++r) s += cl.map_shared_rank(S->hist, r)[i];
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r) s += v[r];
     S->tot[i] = s;
   }
+  cl.sync();  // owners' totals complete
+  // 2. gather every owner's totals (rows of another owner are read remotely)
+  for (int i = threadIdx.x; i < nb; i += kSelThreads) {
+    const int owner = i / per_owner;
+    if (owner != rank) S->tot[i] = cl.map_shared_rank(S->tot, owner)[i];
+  }
   __syncthreads();
+  // 3. running count in the requested direction; the digit where it reaches `need`
   const int per = (nb + kSelThreads - 1) / kSelThreads;
   const int p0 = threadIdx.x * per;
   uint32_t c = 0;
@@ -189,7 +278,7 @@ __device__ __forceinline__ void sel_find_digit(cg::cluster_group &cl, SelSmem *S
   __syncthreads();
   digit = S->result[0];
   before = S->result[1];
-  cl.sync();  // remote reads of the histograms done before any CTA reuses them
+  cl.sync();  // remote reads of the histograms and totals done before any CTA reuses them
 }
 
 // Exact selection of the need-th key (1-based) in the given direction among the

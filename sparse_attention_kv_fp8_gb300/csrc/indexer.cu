@@ -9,7 +9,7 @@
 //
 // sm_103a design (one persistent CTA per SM, 10 warps):
 //   warp 0      TMA producer: 128-token K tiles (16 KB, 128B-swizzled) into a
-//               6-stage shared-memory ring; the request's q (64*n_q x 128 e4m3)
+//               10-stage shared-memory ring; the request's q (64*n_q x 128 e4m3)
 //               into one of two q buffers.
 //   warp 1      tensor-core issuer: per tile, 4 x tcgen05.mma kind::f8f6f4
 //               (M = 128 tokens, N = 64*n_q heads, K = 32) into one of two TMEM
@@ -29,9 +29,10 @@ namespace echo {
 
 constexpr int kTileTokens = 128;
 constexpr int kTileBytes = kTileTokens * kDim;  // 16 KB
-constexpr int kStages = 6;
-constexpr int kEpiWarps = 4;
-constexpr int kPfWarps = 4;
+constexpr int kStages = 10;
+constexpr int kEpiGroups = 2;                // epilogue warpgroups, alternating tiles
+constexpr int kEpiWarps = 4 * kEpiGroups;
+constexpr int kPfWarps = 4;                  // each serves kEpiWarps / kPfWarps queues
 constexpr int kIndexerThreads = 32 * (2 + kEpiWarps + kPfWarps);
 constexpr int kAcc = 4;            // TMEM accumulators (MMA runs up to 3 tiles ahead of the epilogue)
 constexpr int kQueueCap = 64;      // entries per epilogue -> prefetch queue
@@ -71,7 +72,7 @@ struct alignas(16) IndexerCtl {
   int queue_head[kEpiWarps];
   int queue_done[kEpiWarps];
   int queue[kEpiWarps][kQueueCap];  // token ids b * L_max + p that passed the threshold
-  float wsm[kEpiWarps][2 * kHeads];  // head weights of the current request, per epilogue warp
+  float4 wsm[kEpiWarps][2 * kHeads / 4];  // head weights of the current request, per epilogue warp
 };
 
 __device__ __forceinline__ int clamp_ctx(int32_t L, int L_max) { return L < 0 ? 0 : (L > L_max ? L_max : L); }
@@ -141,7 +142,7 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
     }
     for (int i = 0; i < kAcc; ++i) {
       mbar_init(&ctl->tmem_full[i], 1);
-      mbar_init(&ctl->tmem_empty[i], kEpiWarps);
+      mbar_init(&ctl->tmem_empty[i], 4);  // the four warps of the group that reads it
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl->q_full[i], 1);
@@ -229,18 +230,23 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
     }
   } else if (warp < 2 + kEpiWarps) {
     // ===================== epilogue =====================
+    // group g takes tiles g, g + kEpiGroups, ... so two warps per SM sub-partition
+    // hide each other's TMEM-load and FMA latency
     const int e = warp - 2;
+    const int grp = e / 4;
     const int quad = warp & 3;  // TMEM lanes this warp may read
     const int row = quad * 32 + lane;
-    float *wsm = ctl->wsm[e];
+    float4 *wsm4 = ctl->wsm[e];
     int b = ctl->first_b, t = ctl->first_t, cur_b = -1;
+    for (int u = 0; u < grp; ++u) next_tile(P, b, t);
     float shat[NQ];
     int valid[NQ];
     int tail = 0;  // queue tail, kept by every lane (lane 0 publishes it)
-    for (int i = 0; i < n_tiles; ++i) {
+    for (int i = grp; i < n_tiles; i += kEpiGroups) {
       if (b != cur_b) {
         __syncwarp();
-        for (int x = lane; x < N; x += 32) wsm[x] = __ldg(P.w + static_cast<size_t>(b) * N + x);
+        for (int x = lane; x < N / 4; x += 32)
+          wsm4[x] = __ldg(reinterpret_cast<const float4 *>(P.w + static_cast<size_t>(b) * N) + x);
         __syncwarp();
         const int L = clamp_ctx(__ldg(P.ctx_len + b), P.L_max);
 #pragma unroll
@@ -261,14 +267,20 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
         tmem_ld_32x32b_x32(taddr + j * kHeads, v0);
         tmem_ld_32x32b_x32(taddr + j * kHeads + 32, v1);
         tmem_wait_ld();
-        // four independent partial sums (heads 0-15, 16-31, 32-47, 48-63) shorten the FMA chain
+        // four independent partial sums shorten the FMA chain; weights come four at a time
+        const float4 *w4 = wsm4 + j * (kHeads / 4);
         float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
-        for (int h = 0; h < 16; ++h) {
-          s0 = fmaf(wsm[j * kHeads + h], fmaxf(v0[h], 0.f), s0);
-          s1 = fmaf(wsm[j * kHeads + 16 + h], fmaxf(v0[16 + h], 0.f), s1);
-          s2 = fmaf(wsm[j * kHeads + 32 + h], fmaxf(v1[h], 0.f), s2);
-          s3 = fmaf(wsm[j * kHeads + 48 + h], fmaxf(v1[16 + h], 0.f), s3);
+        for (int h4 = 0; h4 < 8; ++h4) {
+          const float4 wa = w4[h4], wb = w4[8 + h4];
+          s0 = fmaf(wa.x, fmaxf(v0[4 * h4 + 0], 0.f), s0);
+          s1 = fmaf(wa.y, fmaxf(v0[4 * h4 + 1], 0.f), s1);
+          s2 = fmaf(wa.z, fmaxf(v0[4 * h4 + 2], 0.f), s2);
+          s3 = fmaf(wa.w, fmaxf(v0[4 * h4 + 3], 0.f), s3);
+          s0 = fmaf(wb.x, fmaxf(v1[4 * h4 + 0], 0.f), s0);
+          s1 = fmaf(wb.y, fmaxf(v1[4 * h4 + 1], 0.f), s1);
+          s2 = fmaf(wb.z, fmaxf(v1[4 * h4 + 2], 0.f), s2);
+          s3 = fmaf(wb.w, fmaxf(v1[4 * h4 + 3], 0.f), s3);
         }
         sc[j] = (s0 + s1) + (s2 + s3);
       }
@@ -307,7 +319,7 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
           }
         }
       }
-      next_tile(P, b, t);
+      for (int u = 0; u < kEpiGroups; ++u) next_tile(P, b, t);
     }
     if (lane == 0) {
       __threadfence_block();
@@ -315,32 +327,51 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
     }
   } else if (prefetch) {
     // ===================== prefetch copies =====================
-    const int e = warp - 2 - kEpiWarps;
-    volatile int *vtail = &ctl->queue_tail[e];
-    volatile int *vhead = &ctl->queue_head[e];
-    volatile int *vdone = &ctl->queue_done[e];
+    // prefetch warp e serves the queues of epilogue warps e, e + kPfWarps, ...
+    const int pf = warp - 2 - kEpiWarps;
     const int4 *host = reinterpret_cast<const int4 *>(P.host_kv);
     int4 *stage = reinterpret_cast<int4 *>(P.stage_rows);
-    int head = 0;
+    constexpr int kQ = kEpiWarps / kPfWarps;
+    int heads[kQ];
+#pragma unroll
+    for (int u = 0; u < kQ; ++u) heads[u] = 0;
+    int turn = 0;
     uint64_t idle_since = 0;
     while (true) {
-      int tl = *vtail;
-      if (tl == head) {
-        if (*vdone) {
-          tl = *vtail;
-          if (tl == head) break;
-        } else {
-          const uint64_t now = globaltimer();
-          if (idle_since == 0) idle_since = now;
-          if (now - idle_since > kWaitLimitNs) {
-            set_status(P.status, ECHO_DEV_WAIT_TIMEOUT);
-            *abort = 1;
-            break;
+      // next queue with work, round robin; stop once every queue is done and drained
+      int e = -1, tl = 0, head = 0;
+      bool all_done = true;
+#pragma unroll
+      for (int u = 0; u < kQ; ++u) {
+        const int qi = (turn + u) % kQ;
+        const int q = pf + qi * kPfWarps;
+        const int done = *reinterpret_cast<volatile int *>(&ctl->queue_done[q]);
+        const int tq = *reinterpret_cast<volatile int *>(&ctl->queue_tail[q]);
+        if (tq != heads[qi]) {
+          if (e < 0) {
+            e = q;
+            tl = tq;
+            head = heads[qi];
+            turn = qi;
           }
-          __nanosleep(200);
-          continue;
+          all_done = false;
+        } else if (!done) {
+          all_done = false;
         }
       }
+      if (e < 0) {
+        if (all_done) break;
+        const uint64_t now = globaltimer();
+        if (idle_since == 0) idle_since = now;
+        if (now - idle_since > kWaitLimitNs) {
+          set_status(P.status, ECHO_DEV_WAIT_TIMEOUT);
+          *abort = 1;
+          break;
+        }
+        __nanosleep(200);
+        continue;
+      }
+      volatile int *vhead = &ctl->queue_head[e];
       idle_since = 0;
       // ---- up to 32 queued tokens: host row, residency, ticket (one lane each)
       const int n = (tl - head) < 32 ? (tl - head) : 32;
@@ -357,6 +388,8 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
         }
       }
       head += n;  // entries are in registers: hand the slots back to the epilogue
+      heads[turn] = head;
+      turn = (turn + 1) % kQ;
       __syncwarp();
       if (lane == 0) *vhead = head;
       const uint32_t cmask = __ballot_sync(0xffffffffu, cand);

@@ -19,7 +19,17 @@ ECHO_TRACE_UNIT(topk)
 namespace echo {
 
 constexpr int kTopkCluster = 8;
-constexpr int kMaxChunk = 48 * 1024;  // keys per CTA kept in shared memory
+constexpr int kMaxChunk = 44 * 1024;  // keys per CTA kept in shared memory
+constexpr int kCand = 1024;          // threshold-bin keys resolved by one CTA
+
+struct alignas(16) TopkExtra {
+  uint32_t cand_key[kCand];   // rank 0: keys of the threshold bin, from every CTA
+  uint32_t cand_src[kCand];   // rank 0: the CTA each candidate came from
+  uint32_t cand_n;            // rank 0: candidates received
+  uint32_t above[kMaxCluster];  // rank 0: per-CTA count of keys in bins above the threshold bin
+  uint32_t gc[kMaxCluster], ec[kMaxCluster];  // rank 0: per-CTA counts above / equal to T
+  uint32_t T, needT, pg, pe;  // written by rank 0 into every CTA: threshold and this CTA's offsets
+};
 
 __global__ void __launch_bounds__(kSelThreads, 1)
     topk_kernel(const float *__restrict__ scores, const int32_t *__restrict__ ctx_len, int n_q, int L_max, int k,
@@ -29,9 +39,11 @@ __global__ void __launch_bounds__(kSelThreads, 1)
   const int rank = static_cast<int>(cl.block_rank());
   const int row = blockIdx.x / C;
   const int b = row / n_q, j = row % n_q;
+  const int lane = threadIdx.x & 31;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SelSmem *S = reinterpret_cast<SelSmem *>(smem_raw);
-  uint32_t *keys = reinterpret_cast<uint32_t *>(smem_raw + sizeof(SelSmem));  // SelSmem is 16-byte aligned in size
+  TopkExtra *X = reinterpret_cast<TopkExtra *>(smem_raw + sizeof(SelSmem));
+  uint32_t *keys = reinterpret_cast<uint32_t *>(smem_raw + sizeof(SelSmem) + sizeof(TopkExtra));
 
   ECHO_TRACE_MARK(0);
   int L = __ldg(ctx_len + b);
@@ -71,25 +83,155 @@ __global__ void __launch_bounds__(kSelThreads, 1)
       mx = max(mx, a);
     }
   }
+  // the cluster-wide histogram is summed into every CTA's `tot`: clear it first
+  for (int i = threadIdx.x; i < kMaxBins; i += kSelThreads) S->tot[i] = 0;
+  if (threadIdx.x == 0) X->cand_n = 0;
   __syncthreads();
-
   ECHO_TRACE_MARK(1);
-  // ---- the target-th largest key T and how many keys equal to T are taken
-  uint32_t T = 0, need = 0;
+
+  // ---- the target-th largest key T, how many keys equal to T are taken (needT), and
+  // this CTA's output offsets (keys above T and equal to T in lower CTAs)
+  uint32_t T = 0, needT = 0, pg = 0, pe = 0;
+  bool offsets_known = false;
   if (target > 0) {
     uint32_t kmin, kmax;
-    sel_cluster_minmax(cl, S, mn, mx, kmin, kmax);
+    sel_cluster_minmax(cl, S, mn, mx, kmin, kmax);  // also orders the clearing above before remote adds
     ECHO_TRACE_MARK(2);
-    sel_radix_select(cl, S, n_local, kmin, kmax, static_cast<uint32_t>(target), true,
-                     [&](int i, uint32_t &key) {
-                       key = keys[i];
-                       return true;
-                     },
-                     T, need);
+    const uint32_t range = kmax - kmin;
+    const int hb = range == 0 ? 0 : 32 - __clz(range);
+    const int width = hb < kDigitBits ? hb : kDigitBits;
+    const int shift = hb - width;
+    const int nb = 1 << width;
+    // first digit: local histogram, added into every CTA's total
+    sel_histogram(S, n_local, 32, shift, nb, 0u, [&](int i, uint32_t &x) {
+      x = keys[i] - kmin;
+      return true;
+    });
+    for (int i = threadIdx.x; i < nb; i += kSelThreads) {
+      const uint32_t v = S->hist[i];
+      if (v)
+        for (int r = 0; r < C; ++r) atomicAdd(cl.map_shared_rank(&S->tot[i], r), v);
+    }
+    cl.sync();
+    ECHO_TRACE_MARK(3);
+    // digit d holding the target-th largest key (descending running count)
+    const int per = (nb + kSelThreads - 1) / kSelThreads;
+    const int p0 = threadIdx.x * per;
+    uint32_t cnt = 0, mine_above = 0;
+    for (int u = 0; u < per; ++u)
+      if (p0 + u < nb) cnt += S->tot[nb - 1 - (p0 + u)];
+    uint32_t ex, dz, tt, tz;
+    sel_block_scan2(cnt, 0, ex, dz, tt, tz, S);
+    uint32_t run = ex;
+    for (int u = 0; u < per; ++u) {
+      const int idx = p0 + u;
+      if (idx >= nb) break;
+      const int bin = nb - 1 - idx;
+      const uint32_t cb = S->tot[bin];
+      if (run < static_cast<uint32_t>(target) && run + cb >= static_cast<uint32_t>(target)) {
+        S->result[0] = static_cast<uint32_t>(bin);
+        S->result[1] = run;
+      }
+      run += cb;
+    }
+    __syncthreads();
+    const uint32_t d = S->result[0];
+    const uint32_t need_d = static_cast<uint32_t>(target) - S->result[1];
+    const uint32_t cnt_d = S->tot[d];
+    // this CTA's keys in bins above d, and in bin d
+    for (int i = threadIdx.x; i < nb; i += kSelThreads)
+      if (static_cast<uint32_t>(i) > d) mine_above += S->hist[i];
+    uint32_t in_d = S->hist[d];
+    uint32_t ea, eb0, ta, tb0;
+    sel_block_scan2(mine_above, 0, ea, eb0, ta, tb0, S);
+    mine_above = ta;
+    if (shift == 0) {
+      // one key value per bin: T is exact, the local histogram gives the counts
+      T = kmin + d;
+      needT = need_d;
+      sel_cluster_prefix2(cl, S, mine_above, in_d, pg, pe, tt, tz);
+      offsets_known = true;
+    } else if (cnt_d <= static_cast<uint32_t>(kCand)) {
+      // ship the bin's keys to rank 0, which resolves T and every CTA's offsets
+      TopkExtra *X0 = cl.map_shared_rank(X, 0);
+      for (int base = (threadIdx.x & ~31); base < n_local; base += kSelThreads) {
+        const int i = base + lane;
+        const uint32_t key = i < n_local ? keys[i] : 0u;
+        const bool cand = i < n_local && ((key - kmin) >> shift) == d;
+        const uint32_t m = __ballot_sync(0xffffffffu, cand);
+        if (!m) continue;
+        uint32_t slot = 0;
+        if (lane == __ffs(m) - 1) slot = atomicAdd(&X0->cand_n, static_cast<uint32_t>(__popc(m)));
+        slot = __shfl_sync(0xffffffffu, slot, __ffs(m) - 1);
+        if (cand) {
+          const uint32_t at = slot + __popc(m & ((1u << lane) - 1));
+          X0->cand_key[at] = key;
+          X0->cand_src[at] = static_cast<uint32_t>(rank);
+        }
+      }
+      if (threadIdx.x == 0) X0->above[rank] = mine_above;
+      cl.sync();
+      ECHO_TRACE_MARK(4);
+      if (rank == 0) {
+        const int nc = static_cast<int>(X->cand_n);
+        if (threadIdx.x < kMaxCluster) {
+          X->gc[threadIdx.x] = 0;
+          X->ec[threadIdx.x] = 0;
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < nc; i += kSelThreads) {
+          const uint32_t ki = X->cand_key[i];
+          uint32_t greater = 0, equal = 0;
+          for (int jj = 0; jj < nc; ++jj) {
+            const uint32_t kj = X->cand_key[jj];
+            greater += kj > ki;
+            equal += kj == ki;
+          }
+          if (greater < need_d && need_d <= greater + equal) {
+            S->result[0] = ki;
+            S->result[1] = need_d - greater;
+          }
+        }
+        __syncthreads();
+        const uint32_t Tk = S->result[0];
+        for (int i = threadIdx.x; i < nc; i += kSelThreads) {
+          const uint32_t ki = X->cand_key[i];
+          if (ki > Tk) atomicAdd(&X->gc[X->cand_src[i]], 1u);
+          if (ki == Tk) atomicAdd(&X->ec[X->cand_src[i]], 1u);
+        }
+        __syncthreads();
+        if (threadIdx.x < C) {
+          uint32_t g0 = 0, e0 = 0;
+          for (int r = 0; r < static_cast<int>(threadIdx.x); ++r) {
+            g0 += X->above[r] + X->gc[r];
+            e0 += X->ec[r];
+          }
+          TopkExtra *Xr = cl.map_shared_rank(X, static_cast<int>(threadIdx.x));
+          Xr->T = Tk;
+          Xr->needT = S->result[1];
+          Xr->pg = g0;
+          Xr->pe = e0;
+        }
+      }
+      cl.sync();
+      T = X->T;
+      needT = X->needT;
+      pg = X->pg;
+      pe = X->pe;
+      offsets_known = true;
+    } else {
+      // many keys share the threshold bin (ties or a clustered row): exact radix passes
+      sel_radix_select(cl, S, n_local, kmin, kmax, static_cast<uint32_t>(target), true,
+                       [&](int i, uint32_t &key) {
+                         key = keys[i];
+                         return true;
+                       },
+                       T, needT);
+    }
   }
+  ECHO_TRACE_MARK(5);
 
-  ECHO_TRACE_MARK(3);
-  // ---- ascending output: selected iff key > T, or key == T among the first `need`
+  // ---- ascending output: selected iff key > T, or key == T among the first needT
   // equal keys; per-thread segments (odd length: conflict-free shared-memory reads)
   int seg = (n_local + kSelThreads - 1) / kSelThreads;
   seg |= 1;
@@ -104,27 +246,28 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     }
   uint32_t eg, ee, tg, te;
   sel_block_scan2(g, e, eg, ee, tg, te, S);
-  uint32_t pg, pe, gg, ge;
-  sel_cluster_prefix2(cl, S, tg, te, pg, pe, gg, ge);
-  ECHO_TRACE_MARK(4);
+  if (target > 0 && !offsets_known) {
+    uint32_t gg, ge;
+    sel_cluster_prefix2(cl, S, tg, te, pg, pe, gg, ge);
+  }
+  ECHO_TRACE_MARK(6);
   if (target > 0) {
     uint32_t gb = pg + eg, eb = pe + ee;
     for (int i = s0; i < s1; ++i) {
       const uint32_t key = keys[i];
       if (key > T) {
-        out[gb + (eb < need ? eb : need)] = lo + i;
+        out[gb + (eb < needT ? eb : needT)] = lo + i;
         ++gb;
       } else if (key == T) {
-        if (eb < need) out[gb + eb] = lo + i;
+        if (eb < needT) out[gb + eb] = lo + i;
         ++eb;
       }
     }
   }
   for (int i = target + rank * kSelThreads + threadIdx.x; i < k; i += C * kSelThreads) out[i] = -1;
   if (rank == 0 && threadIdx.x == 0) kth[row] = target > 0 ? key_score(T) : -INFINITY;
-  ECHO_TRACE_MARK(5);
   cl.sync();  // no CTA leaves while others may still read its shared memory
-  ECHO_TRACE_MARK(6);
+  ECHO_TRACE_MARK(7);
 }
 
 }  // namespace echo
@@ -142,7 +285,8 @@ int launch_topk(const float *scores, const int32_t *ctx_len, int B, int n_q, int
     set_error("top-k: L_max %d exceeds the supported %d", L_max, C * echo::kMaxChunk);
     return ECHO_ENOTSUP;
   }
-  const size_t smem = sizeof(echo::SelSmem) + static_cast<size_t>(chunk > 0 ? chunk : 4) * sizeof(uint32_t);
+  const size_t smem = sizeof(echo::SelSmem) + sizeof(echo::TopkExtra) +
+                      static_cast<size_t>(chunk > 0 ? chunk : 4) * sizeof(uint32_t);
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(echo::topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
