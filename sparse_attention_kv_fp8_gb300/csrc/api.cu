@@ -40,7 +40,11 @@ int launch_pool_evict(const echo_pool *pool, const echo_workspace *ws, const int
 int launch_recall(const echo_pool *pool, const echo_workspace *ws, const int32_t *sel, const int32_t *req_to_host,
                   const int32_t *ctx_len, int B, int n_q, int k, int L_max, const echo_stage *stage, int32_t clock,
                   const int32_t *clock_dev, int32_t *out_slot, echo_stats *stats, int32_t *status, cudaStream_t s,
-                  float *ema_s_hat, const float *ema_kth, int ema_n, float ema_alpha, int32_t *clock_advance);
+                  float *ema_s_hat, const float *ema_kth, int ema_n, float ema_alpha, int32_t *clock_advance,
+                  int claimed);
+int launch_topk_claim(const float *scores, const int32_t *ctx_len, int B, int n_q, int L_max, int k, int32_t *sel,
+                      float *kth, const echo_pool *pool, const echo_workspace *ws, const int32_t *req_to_host,
+                      int32_t clock, const int32_t *clock_dev, int32_t *status, cudaStream_t stream);
 int launch_append(const echo_pool *pool, const echo_workspace *ws, uint8_t *k_index, int32_t *ctx_len,
                   const int32_t *req_to_host, int B, int L_max, const uint16_t *new_kv, const uint8_t *new_k_index,
                   int32_t clock, const int32_t *clock_dev, echo_stats *stats, int32_t *status, cudaStream_t s);
@@ -226,7 +230,7 @@ int echo_prefetch_recall(const echo_pool *pool, const echo_workspace *ws, const 
   TRY(check_ws(ws, pool, F));
   if (stage) TRY(check_stage(stage));
   return launch_recall(pool, ws, sel, req_to_host, ctx_len, B, n_q, k, L_max, stage, clock, clock_dev, out_slot, stats,
-                       dev_status, static_cast<cudaStream_t>(stream), nullptr, nullptr, 0, 0.f, nullptr);
+                       dev_status, static_cast<cudaStream_t>(stream), nullptr, nullptr, 0, 0.f, nullptr, 0);
 }
 
 int echo_append(const echo_pool *pool, const echo_workspace *ws, uint8_t *k_index, int32_t *ctx_len,
@@ -309,14 +313,16 @@ int echo_decode_step(const echo_step_args *a, void *stream) {
   }
   TRY(echo_indexer_score(&ia, stream));
   TRY(mark(ECHO_STAGE_TOPK));
-  TRY(echo_select_topk(a->scores, a->ctx_len, a->B, a->n_q, a->L_max, a->k, a->sel, a->kth, stream));
+  // the top-k kernel also makes the recall's claims for the entries it selects
+  TRY(launch_topk_claim(a->scores, a->ctx_len, a->B, a->n_q, a->L_max, a->k, a->sel, a->kth, a->pool, a->ws,
+                        a->req_to_host, a->clock, a->clock_dev, a->dev_status, s));
   TRY(mark(ECHO_STAGE_RECALL));
   {
-    // the recall's plan kernel also updates the EMA and advances the device clock
+    // the recall kernel also updates the EMA and advances the device clock
     TRY(launch_recall(a->pool, a->ws, a->sel, a->req_to_host, a->ctx_len, a->B, a->n_q, a->k, a->L_max,
                       prefetch ? a->stage : nullptr, a->clock, a->clock_dev, a->out_slot, a->stats, a->dev_status, s,
                       a->s_hat, a->kth, a->B * a->n_q, a->alpha,
-                      (a->clock_dev && a->advance_clock) ? a->clock_dev : nullptr));
+                      (a->clock_dev && a->advance_clock) ? a->clock_dev : nullptr, 1));
   }
   TRY(mark(ECHO_STAGE_EMA));  // the EMA ran inside the recall: this stage is empty
   TRY(mark(ECHO_NUM_STAGES));

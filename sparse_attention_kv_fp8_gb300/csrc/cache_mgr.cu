@@ -15,26 +15,24 @@
 // sm_103a design: every operation (recall, allocate, evict, the append's
 // allocation) is ONE cooperative kernel over all SMs, its phases separated by
 // bounded grid barriers:
-//   P1  claims: each selected entry maps to its host row (kept for the later
-//       phases); resident rows are hits (priority = clock: protected); missing rows
-//       are claimed in HostTokenToGPU with atomicMin(kClaim + f) so the first entry
-//       in (b, j, i) order owns each row.  Slot pass: bounds of the evictable
-//       priorities.
-//   P2  histogram of evictable priorities (4096 bins over the bits in which they
-//       differ); per-CTA counts of owned misses; staged-row lookup.
-//   P3  misses M = sum of the owned counts; every CTA finds the same threshold
-//       priority T (the E-th smallest, E = max(0, M - free)) from the histogram
-//       (refined while a bin is wider than one value); per-CTA counts of slots
-//       below / at T and free.
-//   P4  prefix sums over the per-CTA counts give each owned miss its rank and each
-//       slot its eviction and free-slot rank: victims are scattered (free = 1,
-//       priority = -1, maps to INF), the r-th free slot is recorded for miss r.
-//       This is the page's ticket order taken in slot order, so it is deterministic.
+//   P1  (only when no earlier kernel did it) claims of the entries, see
+//       cache_common.cuh; the decode step's top-k kernel claims what it selects.
+//   P2  histogram of the evictable slots by age (clock - 1 - priority, 4096 bins,
+//       the last one open-ended); each entry classified (owned miss, repeat, hit),
+//       owned misses counted per CTA; staged-row lookup.
+//   P3  misses M = sum of the owned counts, evictions E = max(0, M - free); every
+//       CTA finds the same threshold T (the E-th oldest priority, refined while the
+//       open bin holds it); owned misses listed in entry order; per-CTA counts of
+//       slots older than / at T and free.
+//   P4  prefix sums over the per-CTA counts give each slot its eviction and free-slot
+//       rank: victims are scattered (free = 1, priority = -1, maps to INF), the r-th
+//       free slot is recorded for miss r.  This is the page's ticket order taken in
+//       slot order, so the result is deterministic.
 //   P5  the r-th miss takes the r-th free slot (maps, priority = clock, indices
-//       buffer) and its KV row is copied (16-byte vectors, 4 rows in flight per
-//       warp) from the staging area or the pinned host pool.
-//   P6  (recall) out_slot of every entry; each hit counted and cleared by its owner.
-#include "echo_common.cuh"
+//       buffer), out_slot of every entry, and each recalled KV row is copied
+//       (16-byte vectors, 4 rows in flight per warp) from the staging area or the
+//       pinned host pool.
+#include "cache_common.cuh"
 
 ECHO_TRACE_UNIT(cache_mgr)
 
@@ -44,63 +42,6 @@ enum Mode { kModeRecall = 0, kModeAlloc = 1, kModeAppend = 2, kModeEvict = 3 };
 
 constexpr int kCoopThreads = 512;
 constexpr int kCoopWarps = kCoopThreads / 32;
-constexpr int kMaxGrid = 1024;
-constexpr int kHistBins = 4096;
-constexpr int kHistLevels = 3;  // 12 + 12 + 8 bits cover any int32 priority range
-
-// global scratch counters (zero between calls, except kGMin = UINT32_MAX)
-enum { kGValid = 0, kGMin, kGMax, kGBar, kGCount = 16 };
-// per-CTA counts
-enum { kCOwn = 0, kCLt, kCEq, kCFree, kCVals };
-// ws.ctr: results readable after a call
-enum { kCtrMisses = 0, kCtrGranted = 1, kCtrCount = 16 };
-
-struct Workspace {
-  int32_t *slot_claim;  // [n_g]  min entry index of this step's hits (INT32_MAX = none)
-  int32_t *entry_rows;  // [max_rows] host row per entry (append)
-  int32_t *entry_h;     // [max_rows] host row of every entry, -1 if none (filled in P1)
-  int32_t *miss_f;      // [max_rows] entry index of the r-th owned miss
-  int32_t *miss_h;      // [max_rows] host row of the r-th owned miss
-  int32_t *miss_stage;  // [max_rows] by entry: staging row index, -1 = not staged
-  int32_t *alloc_slot;  // [max_rows] the r-th free slot (taken by the r-th miss)
-  uint32_t *hist;       // [kHistLevels][kHistBins]
-  uint32_t *cta;        // [kMaxGrid][kCVals]
-  uint32_t *glob;       // [kGCount]
-  int32_t *ctr;         // [kCtrCount]
-};
-
-__host__ __device__ inline size_t ws_align(size_t x) { return (x + 255) & ~size_t(255); }
-
-__host__ __device__ inline size_t ws_layout(int32_t n_g, int32_t max_rows, uintptr_t base, Workspace *w) {
-  size_t off = 0;
-  auto take = [&](size_t n) {
-    size_t o = off;
-    off += ws_align(n * sizeof(int32_t));
-    return base + o;
-  };
-  Workspace x;
-  x.slot_claim = reinterpret_cast<int32_t *>(take(static_cast<size_t>(n_g)));
-  x.entry_rows = reinterpret_cast<int32_t *>(take(static_cast<size_t>(max_rows)));
-  x.entry_h = reinterpret_cast<int32_t *>(take(static_cast<size_t>(max_rows)));
-  x.miss_f = reinterpret_cast<int32_t *>(take(static_cast<size_t>(max_rows)));
-  x.miss_h = reinterpret_cast<int32_t *>(take(static_cast<size_t>(max_rows)));
-  x.miss_stage = reinterpret_cast<int32_t *>(take(static_cast<size_t>(max_rows)));
-  x.alloc_slot = reinterpret_cast<int32_t *>(take(static_cast<size_t>(max_rows)));
-  x.hist = reinterpret_cast<uint32_t *>(take(static_cast<size_t>(kHistLevels) * kHistBins));
-  x.cta = reinterpret_cast<uint32_t *>(take(static_cast<size_t>(kMaxGrid) * kCVals));
-  x.glob = reinterpret_cast<uint32_t *>(take(kGCount));
-  x.ctr = reinterpret_cast<int32_t *>(take(kCtrCount));
-  if (w) *w = x;
-  return off;
-}
-
-struct PoolView {
-  uint8_t *free_;
-  int32_t *prio, *idxbuf, *to_host, *h2g, *counters;
-  uint16_t *gpu_kv;
-  const uint16_t *host_kv;
-  int32_t n_g, n_h;
-};
 
 struct OpParams {
   PoolView pool;
@@ -131,6 +72,7 @@ struct OpParams {
   const int32_t *clock_dev;
   echo_stats *stats;
   int32_t *status;
+  int claimed;  // recall: the entries were already claimed (by the top-k kernel)
   // decode step only: EMA of the k-th score and the device clock's advance
   float *s_hat;
   const float *kth;
@@ -275,6 +217,38 @@ __device__ __forceinline__ void add_stat(echo_stats *st, int64_t echo_stats::*fi
 // ---------------------------------------------------------------------------
 // the cooperative kernel
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t slot_age(int32_t clock, int32_t pr) { return static_cast<uint32_t>(clock - 1 - pr); }
+
+// The bin at which the running count of `gh` taken from the top bin down reaches
+// `need`, and the count strictly above it (same answer in every CTA).
+__device__ __forceinline__ void find_from_top(const uint32_t *gh, uint32_t need, uint32_t &bin, uint32_t &above,
+                                              uint32_t &total, CoopSmem *S) {
+  constexpr int per = kHistBins / kCoopThreads;  // 8 bins per thread, highest first
+  uint32_t cnt[per];
+  uint32_t mine = 0;
+#pragma unroll
+  for (int u = 0; u < per; ++u) {
+    cnt[u] = __ldcg(gh + (kHistBins - 1 - (threadIdx.x * per + u)));
+    mine += cnt[u];
+  }
+  uint32_t v1[1] = {mine}, ex1[1], tot1[1];
+  coop_scan<1>(v1, ex1, tot1, S);
+  total = tot1[0];
+  uint32_t run = ex1[0];
+#pragma unroll
+  for (int u = 0; u < per; ++u) {
+    if (run < need && run + cnt[u] >= need) {
+      S->red[0] = static_cast<uint32_t>(kHistBins - 1 - (threadIdx.x * per + u));
+      S->red[1] = run;
+    }
+    run += cnt[u];
+  }
+  __syncthreads();
+  bin = S->red[0];
+  above = S->red[1];
+  __syncthreads();
+}
+
 __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParams P) {
   __shared__ CoopSmem S_;
   CoopSmem *S = &S_;
@@ -295,100 +269,74 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
   const int e_lo = static_cast<int>((static_cast<long long>(n) * c) / G);
   const int e_hi = static_cast<int>((static_cast<long long>(n) * (c + 1)) / G);
 
-  // ===== P1: claims (no atomic result waited on); bounds of the evictable priorities =====
-  if (P.mode != kModeEvict) {
-    uint32_t valid = 0;
+  // ===== P1: claims, unless the top-k kernel (recall) or the append already made them =====
+  if ((P.mode == kModeRecall && !P.claimed) || P.mode == kModeAlloc) {
     for (int f = gtid; f < n; f += gthreads) {
-      const int32_t h = entry_row(P, f, n, true);
-      P.ws.entry_h[f] = h;
-      if (h < 0) {
-        if (P.mode == kModeAlloc) P.out_slots[f] = -1;
-        continue;
-      }
-      ++valid;
-      if (P.mode == kModeAppend) continue;  // claimed when the token was written
-      const int32_t v = P.pool.h2g[h];
-      if (v >= 0 && v < n_g) {
-        if (P.mode == kModeRecall) {
-          P.pool.prio[v] = clock;              // protect + LRU clock
-          atomicMin(P.ws.slot_claim + v, f);   // first entry of the row owns the hit
-        } else {                               // allocate: already resident
-          set_status(P.status, ECHO_DEV_BAD_INDEX);
-          P.out_slots[f] = -1;
-          P.ws.entry_h[f] = -1;
+      int32_t h = entry_row(P, f, n, true);
+      if (P.mode == kModeAlloc) {
+        if (h >= 0) {
+          const int32_t v = P.pool.h2g[h];
+          if (v != kInf && v >= 0) {  // already resident (or corrupt): cannot allocate again
+            set_status(P.status, ECHO_DEV_BAD_INDEX);
+            h = -1;
+          } else {
+            atomicMin(P.pool.h2g + h, kClaim + f);
+          }
         }
-      } else if (v == kInf || v < 0) {
-        atomicMin(P.pool.h2g + h, kClaim + f);  // first entry of the row owns the miss
+        P.ws.entry_h[f] = h;
+        if (h < 0) P.out_slots[f] = -1;
       } else {
-        set_status(P.status, ECHO_DEV_BAD_INDEX);
-        P.ws.entry_h[f] = -1;
+        claim_entry(P.pool, P.ws, f, h, clock, P.status);
       }
     }
-    for (int o = 16; o > 0; o >>= 1) valid += __shfl_xor_sync(0xffffffffu, valid, o);
-    if (lane == 0 && valid) atomicAdd(glob + kGValid, valid);
+    ECHO_TRACE_MARK(1);
+    if (!grid_barrier(glob, P.status, S)) return;
   }
-  if (P.mode != kModeAlloc) {
-    uint32_t mn = 0xFFFFFFFFu, mx = 0;
-    for (int s = s_lo + threadIdx.x; s < s_hi; s += kCoopThreads) {
-      const int32_t pr = P.pool.prio[s];
-      if (evictable(P.pool.free_[s], pr, clock)) {
-        mn = min(mn, static_cast<uint32_t>(pr));
-        mx = max(mx, static_cast<uint32_t>(pr));
-      }
-    }
-    for (int o = 16; o > 0; o >>= 1) {
-      mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    }
-    if (lane == 0 && mn <= mx) {
-      atomicMin(glob + kGMin, mn);
-      atomicMax(glob + kGMax, mx);
-    }
-  }
-  ECHO_TRACE_MARK(1);
-  if (!grid_barrier(glob, P.status, S)) return;
   ECHO_TRACE_MARK(2);
 
-  // ===== P2: priority histogram; owned misses per CTA; staged rows =====
-  const uint32_t pmin = *reinterpret_cast<volatile uint32_t *>(glob + kGMin);
-  const uint32_t pmax = *reinterpret_cast<volatile uint32_t *>(glob + kGMax);
-  const bool any_evictable = P.mode != kModeAlloc && pmin <= pmax;
-  const uint32_t range = any_evictable ? pmax - pmin : 0u;
-  const int rbits = range == 0 ? 0 : 32 - __clz(range);
-  int shift = rbits > 12 ? rbits - 12 : 0;
-  if (any_evictable) {
+  // ===== P2: age histogram; entries classified; owned misses per CTA; staged rows =====
+  if (P.mode != kModeAlloc) {
     for (int i = threadIdx.x; i < kHistBins; i += kCoopThreads) S->hist[i] = 0;
     __syncthreads();
     for (int s = s_lo + threadIdx.x; s < s_hi; s += kCoopThreads) {
       const int32_t pr = P.pool.prio[s];
-      if (evictable(P.pool.free_[s], pr, clock))
-        atomicAdd(&S->hist[(static_cast<uint32_t>(pr) - pmin) >> shift], 1u);
+      if (evictable(P.pool.free_[s], pr, clock)) atomicAdd(&S->hist[min(slot_age(clock, pr), kHistBins - 1u)], 1u);
     }
     __syncthreads();
     for (int i = threadIdx.x; i < kHistBins; i += kCoopThreads)
       if (S->hist[i]) atomicAdd(P.ws.hist + i, S->hist[i]);
   }
   if (P.mode != kModeEvict) {
-    uint32_t own = 0;
+    uint32_t own = 0, hits = 0, valid = 0;
     for (int f = e_lo + threadIdx.x; f < e_hi; f += kCoopThreads) {
-      const int32_t h = P.ws.entry_h[f];
-      if (h < 0) continue;
-      const int32_t v = P.pool.h2g[h];
-      if (v == kClaim + f) {
-        ++own;
-      } else if (P.mode != kModeRecall && v < 0) {
-        // a repeat of a row an earlier entry claimed: rejected
-        if (P.mode == kModeAlloc) P.out_slots[f] = -1;
-        set_status(P.status, ECHO_DEV_BAD_INDEX);
+      const int32_t h = P.mode == kModeAppend ? P.ws.entry_rows[f] : P.ws.entry_h[f];
+      int32_t aux = -1;
+      if (h >= 0) {
+        ++valid;
+        const int32_t v = P.pool.h2g[h];
+        if (v == kClaim + f) {
+          ++own;
+          aux = -2;
+        } else if (v >= 0 && v < n_g) {  // recall hit
+          aux = v;
+          hits += P.ws.slot_claim[v] == f;
+        } else if (v < 0) {  // a repeat of a row an earlier entry claimed
+          if (P.mode == kModeRecall) {
+            aux = -3 - static_cast<int32_t>(static_cast<uint32_t>(v) - 0x80000000u);
+          } else {
+            if (P.mode == kModeAlloc) P.out_slots[f] = -1;
+            set_status(P.status, ECHO_DEV_BAD_INDEX);
+          }
+        }
       }
+      P.ws.ent_aux[f] = aux;
     }
-    for (int o = 16; o > 0; o >>= 1) own += __shfl_xor_sync(0xffffffffu, own, o);
-    if (lane == 0) S->ws[0][warp] = own;
-    __syncthreads();
+    uint32_t v3[3] = {own, hits, valid}, ex3[3], tot3[3];
+    coop_scan<3>(v3, ex3, tot3, S);
     if (threadIdx.x == 0) {
-      uint32_t t = 0;
-      for (int w = 0; w < kCoopWarps; ++w) t += S->ws[0][w];
-      P.ws.cta[c * kCVals + kCOwn] = t;
+      P.ws.cta[c * kCVals + kCOwn] = tot3[0];
+      if (tot3[1]) atomicAdd(glob + kGHits, tot3[1]);
+      if (tot3[2]) atomicAdd(glob + kGValid, tot3[2]);
     }
   }
   if (P.mode == kModeRecall && P.stage_count != nullptr) {
@@ -416,17 +364,19 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
   if (!grid_barrier(glob, P.status, S)) return;
   ECHO_TRACE_MARK(4);
 
-  // ===== P3: misses M and evictions E; threshold T (the E-th smallest evictable
-  // priority); per-CTA counts =====
-  uint32_t M = 0;
+  // ===== P3: M, E, threshold; owned misses listed in entry order; per-CTA slot counts =====
+  uint32_t M = 0, pre_own = 0;
   if (P.mode != kModeEvict) {
-    uint32_t m = 0;
-    for (int r = threadIdx.x; r < G; r += kCoopThreads) m += __ldcg(P.ws.cta + r * kCVals + kCOwn);
-    for (int o = 16; o > 0; o >>= 1) m += __shfl_xor_sync(0xffffffffu, m, o);
-    if (lane == 0) S->ws[0][warp] = m;
-    __syncthreads();
-    for (int w = 0; w < kCoopWarps; ++w) M += S->ws[0][w];
-    __syncthreads();
+    uint32_t m = 0, pm = 0;
+    for (int r = threadIdx.x; r < G; r += kCoopThreads) {
+      const uint32_t x = __ldcg(P.ws.cta + r * kCVals + kCOwn);
+      m += x;
+      if (r < c) pm += x;
+    }
+    uint32_t v2[2] = {m, pm}, ex2[2], tot2[2];
+    coop_scan<2>(v2, ex2, tot2, S);
+    M = tot2[0];
+    pre_own = tot2[1];
   }
   int32_t E = 0;
   if (P.mode == kModeEvict) {
@@ -436,66 +386,74 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     E = static_cast<int32_t>(M) - n_free0;
     E = E < 0 ? 0 : E;
   }
-  if (E > 0 && !any_evictable) {
-    if (c == 0 && threadIdx.x == 0) set_status(P.status, ECHO_DEV_POOL_EXHAUSTED);
-    E = 0;
-  }
-  uint32_t T = 0, needT = 0;
+  int32_t Tp = 0;  // threshold priority: victims have priority < Tp, or == Tp (the first needT)
+  uint32_t needT = 0;
+  uint32_t d = 0, above = 0;
   if (E > 0) {
-    uint32_t prefix = 0;  // priority - pmin, the digits above `shift` fixed so far
-    uint32_t need = static_cast<uint32_t>(E);
-    for (int lvl = 0;; ++lvl) {
-      const uint32_t *gh = P.ws.hist + lvl * kHistBins;
-      constexpr int per = kHistBins / kCoopThreads;  // 8 consecutive bins per thread
-      uint32_t cnt[per];
-      uint32_t mine = 0;
-#pragma unroll
-      for (int u = 0; u < per; ++u) {
-        cnt[u] = __ldcg(gh + threadIdx.x * per + u);
-        mine += cnt[u];
-      }
-      uint32_t v1[1] = {mine}, ex1[1], tot1[1];
-      coop_scan<1>(v1, ex1, tot1, S);
-      if (lvl == 0 && tot1[0] < need) {  // fewer evictable slots than asked
-        if (c == 0 && threadIdx.x == 0) set_status(P.status, ECHO_DEV_POOL_EXHAUSTED);
-        need = tot1[0];
-        E = static_cast<int32_t>(tot1[0]);
-      }
-      if (need == 0) break;  // nothing evictable after all (same answer in every CTA)
-      uint32_t run = ex1[0];
-#pragma unroll
-      for (int u = 0; u < per; ++u) {
-        if (run < need && run + cnt[u] >= need) {
-          S->red[0] = static_cast<uint32_t>(threadIdx.x * per + u);
-          S->red[1] = run;
-        }
-        run += cnt[u];
-      }
-      __syncthreads();
-      const uint32_t d = S->red[0];
-      need -= S->red[1];
-      prefix |= d << shift;
-      __syncthreads();
-      if (shift == 0) break;
-      // refine: the slots in bin d, by the next (up to 12) bits
-      const int nshift = shift > 12 ? shift - 12 : 0;
-      const uint32_t mask = (1u << (shift - nshift)) - 1u;
-      for (int i = threadIdx.x; i < kHistBins; i += kCoopThreads) S->hist[i] = 0;
-      __syncthreads();
-      for (int s = s_lo + threadIdx.x; s < s_hi; s += kCoopThreads) {
-        const int32_t pr = P.pool.prio[s];
-        if (!evictable(P.pool.free_[s], pr, clock)) continue;
-        const uint32_t x = static_cast<uint32_t>(pr) - pmin;
-        if ((x >> shift) == (prefix >> shift)) atomicAdd(&S->hist[(x >> nshift) & mask], 1u);
-      }
-      __syncthreads();
-      for (int i = threadIdx.x; i < kHistBins; i += kCoopThreads)
-        if (S->hist[i]) atomicAdd(P.ws.hist + (lvl + 1) * kHistBins + i, S->hist[i]);
-      shift = nshift;
-      if (!grid_barrier(glob, P.status, S)) return;
+    uint32_t total;
+    find_from_top(P.ws.hist, static_cast<uint32_t>(E), d, above, total, S);
+    if (total < static_cast<uint32_t>(E)) {  // fewer evictable slots than asked
+      if (c == 0 && threadIdx.x == 0) set_status(P.status, ECHO_DEV_POOL_EXHAUSTED);
+      E = static_cast<int32_t>(total);
+      if (E > 0) find_from_top(P.ws.hist, static_cast<uint32_t>(E), d, above, total, S);
     }
-    T = pmin + prefix;
+  }
+  if (E > 0) {
+    uint32_t need = static_cast<uint32_t>(E) - above;
+    uint32_t age_t = d;
+    if (d == kHistBins - 1) {
+      // the open bin (age >= 4095): refine x = age - 4095 by 12-bit digits, oldest first
+      const uint32_t xmax = static_cast<uint32_t>(clock) - static_cast<uint32_t>(kHistBins);
+      int hb = xmax == 0 ? 0 : 32 - __clz(xmax);
+      uint32_t prefix = 0;
+      for (int lvl = 1; hb > 0; ++lvl) {
+        const int width = hb < 12 ? hb : 12;
+        const int sh = hb - width;
+        for (int i = threadIdx.x; i < kHistBins; i += kCoopThreads) S->hist[i] = 0;
+        __syncthreads();
+        for (int s = s_lo + threadIdx.x; s < s_hi; s += kCoopThreads) {
+          const int32_t pr = P.pool.prio[s];
+          if (!evictable(P.pool.free_[s], pr, clock)) continue;
+          const uint32_t age = slot_age(clock, pr);
+          if (age < kHistBins - 1u) continue;
+          const uint32_t x = age - (kHistBins - 1u);
+          if (hb < 32 && (x >> hb) != (prefix >> hb)) continue;
+          atomicAdd(&S->hist[(x >> sh) & ((1u << width) - 1u)], 1u);
+        }
+        __syncthreads();
+        uint32_t *gl = P.ws.hist + lvl * kHistBins;
+        for (int i = threadIdx.x; i < kHistBins; i += kCoopThreads)
+          if (S->hist[i]) atomicAdd(gl + i, S->hist[i]);
+        if (!grid_barrier(glob, P.status, S)) return;
+        uint32_t dd, ab, tt;
+        find_from_top(gl, need, dd, ab, tt, S);
+        prefix |= dd << sh;
+        need -= ab;
+        hb = sh;
+      }
+      age_t = (kHistBins - 1u) + prefix;
+    }
+    Tp = clock - 1 - static_cast<int32_t>(age_t);
     needT = need;
+  }
+  // owned misses, in entry order (contiguous per-thread segments)
+  if (P.mode != kModeEvict) {
+    const int cnt = e_hi - e_lo;
+    const int per = (cnt + kCoopThreads - 1) / kCoopThreads;
+    const int f0 = e_lo + min(cnt, static_cast<int>(threadIdx.x) * per);
+    const int f1 = e_lo + min(cnt, static_cast<int>(threadIdx.x + 1) * per);
+    uint32_t own = 0;
+    for (int f = f0; f < f1; ++f) own += P.ws.ent_aux[f] == -2;
+    uint32_t v1[1] = {own}, ex1[1], tot1[1];
+    coop_scan<1>(v1, ex1, tot1, S);
+    uint32_t r = pre_own + ex1[0];
+    for (int f = f0; f < f1; ++f) {
+      if (P.ws.ent_aux[f] != -2) continue;
+      P.ws.miss_f[r] = f;
+      P.ws.miss_h[r] = P.mode == kModeAppend ? P.ws.entry_rows[f] : P.ws.entry_h[f];
+      P.ws.miss_rank[f] = static_cast<int32_t>(r);
+      ++r;
+    }
   }
   {
     uint32_t lt = 0, eq = 0, fr = 0;
@@ -506,8 +464,8 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
       } else if (E > 0) {
         const int32_t pr = P.pool.prio[s];
         if (evictable(0, pr, clock)) {
-          lt += static_cast<uint32_t>(pr) < T;
-          eq += static_cast<uint32_t>(pr) == T;
+          lt += pr < Tp;
+          eq += pr == Tp;
         }
       }
     }
@@ -523,76 +481,28 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
   if (!grid_barrier(glob, P.status, S)) return;
   ECHO_TRACE_MARK(6);
 
-  // ===== P4: ranks; owned misses listed in entry order; victims evicted; free-slot list =====
+  // ===== P4: victims evicted; free-slot list =====
+  uint32_t pre_lt = 0, pre_eq = 0, pre_fr = 0, free_total = 0;
   {
-    // sums over lower CTAs (pre) and over all CTAs (tot) of the per-CTA counts
-    uint32_t a[kCVals] = {0, 0, 0, 0}, t4[kCVals] = {0, 0, 0, 0};
+    uint32_t a3[3] = {0, 0, 0}, t1 = 0;
     for (int r = threadIdx.x; r < G; r += kCoopThreads) {
-#pragma unroll
-      for (int k = 0; k < kCVals; ++k) {
-        const uint32_t x = __ldcg(P.ws.cta + r * kCVals + k);
-        if (r < c) a[k] += x;
-        t4[k] += x;
+      const uint32_t lt = __ldcg(P.ws.cta + r * kCVals + kCLt), eq = __ldcg(P.ws.cta + r * kCVals + kCEq),
+                     fr = __ldcg(P.ws.cta + r * kCVals + kCFree);
+      if (r < c) {
+        a3[0] += lt;
+        a3[1] += eq;
+        a3[2] += fr;
       }
+      t1 += fr;
     }
-#pragma unroll
-    for (int k = 0; k < kCVals; ++k)
-      for (int o = 16; o > 0; o >>= 1) {
-        a[k] += __shfl_xor_sync(0xffffffffu, a[k], o);
-        t4[k] += __shfl_xor_sync(0xffffffffu, t4[k], o);
-      }
-    if (lane == 0)
-#pragma unroll
-      for (int k = 0; k < kCVals; ++k) {
-        S->ws[k][warp] = a[k];
-      }
-    __syncthreads();
-    if (threadIdx.x < kCVals) {
-      uint32_t x = 0;
-      for (int w = 0; w < kCoopWarps; ++w) x += S->ws[threadIdx.x][w];
-      S->pre[threadIdx.x] = x;
-    }
-    __syncthreads();
-    if (lane == 0)
-#pragma unroll
-      for (int k = 0; k < kCVals; ++k) S->ws[k][warp] = t4[k];
-    __syncthreads();
-    if (threadIdx.x < kCVals) {
-      uint32_t x = 0;
-      for (int w = 0; w < kCoopWarps; ++w) x += S->ws[threadIdx.x][w];
-      S->tot[threadIdx.x] = x;
-    }
-    __syncthreads();
+    uint32_t v4[4] = {a3[0], a3[1], a3[2], t1}, ex4[4], tot4[4];
+    coop_scan<4>(v4, ex4, tot4, S);
+    pre_lt = tot4[0];
+    pre_eq = tot4[1];
+    pre_fr = tot4[2];
+    free_total = tot4[3];
   }
-  const uint32_t pre_own = S->pre[kCOwn], pre_lt = S->pre[kCLt], pre_eq = S->pre[kCEq], pre_fr = S->pre[kCFree];
-  const uint32_t free_total = S->tot[kCFree];
   const int32_t A = (P.mode == kModeEvict) ? 0 : static_cast<int32_t>(min(M, free_total + static_cast<uint32_t>(E)));
-  __syncthreads();
-  // owned misses, in entry order (contiguous per-thread segments)
-  if (P.mode != kModeEvict) {
-    const int cnt = e_hi - e_lo;
-    const int per = (cnt + kCoopThreads - 1) / kCoopThreads;
-    const int f0 = e_lo + min(cnt, static_cast<int>(threadIdx.x) * per);
-    const int f1 = e_lo + min(cnt, static_cast<int>(threadIdx.x + 1) * per);
-    uint32_t own = 0;
-    for (int f = f0; f < f1; ++f) {
-      const int32_t h = P.ws.entry_h[f];
-      if (h >= 0 && P.pool.h2g[h] == kClaim + f) ++own;
-    }
-    uint32_t v1[1] = {own}, ex1[1], tot1[1];
-    coop_scan<1>(v1, ex1, tot1, S);
-    uint32_t r = pre_own + ex1[0];
-    for (int f = f0; f < f1; ++f) {
-      const int32_t h = P.ws.entry_h[f];
-      if (h >= 0 && P.pool.h2g[h] == kClaim + f) {
-        P.ws.miss_f[r] = f;
-        P.ws.miss_h[r] = h;
-        ++r;
-      }
-    }
-  }
-  // slots: victims (priority < T, or == T among the first needT in slot order) and
-  // free-slot ranks, in slot order (contiguous per-thread segments)
   {
     const int cnt = s_hi - s_lo;
     const int per = (cnt + kCoopThreads - 1) / kCoopThreads;
@@ -606,8 +516,8 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
       } else if (E > 0) {
         const int32_t pr = P.pool.prio[s];
         if (evictable(0, pr, clock)) {
-          lt += static_cast<uint32_t>(pr) < T;
-          eq += static_cast<uint32_t>(pr) == T;
+          lt += pr < Tp;
+          eq += pr == Tp;
         }
       }
     }
@@ -616,7 +526,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     uint32_t lt_b = pre_lt + ex3[0], eq_b = pre_eq + ex3[1], fr_b = pre_fr + ex3[2];
     for (int s = q0; s < q1; ++s) {
       const uint8_t f8 = P.pool.free_[s];
-      // victims before s (all evictable slots below T, the first needT at T), and
+      // victims before s (all evictable slots older than T, the first needT at T), and
       // the slots before s that are free after the eviction (free ones and victims)
       const uint32_t vb = lt_b + min(eq_b, needT);
       const uint32_t before = fr_b + vb;
@@ -629,10 +539,10 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
       const int32_t pr = P.pool.prio[s];
       if (!evictable(0, pr, clock)) continue;
       bool victim = false;
-      if (static_cast<uint32_t>(pr) < T) {
+      if (pr < Tp) {
         victim = true;
         ++lt_b;
-      } else if (static_cast<uint32_t>(pr) == T) {
+      } else if (pr == Tp) {
         victim = eq_b < needT;
         ++eq_b;
       }
@@ -650,7 +560,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
   if (!grid_barrier(glob, P.status, S)) return;
   ECHO_TRACE_MARK(8);
 
-  // ===== P5: the r-th miss takes the r-th free slot; KV rows copied =====
+  // ===== P5: the r-th miss takes the r-th free slot; out_slot; KV rows copied =====
   for (int r = gtid; r < static_cast<int>(M); r += gthreads) {
     const int32_t f = P.ws.miss_f[r], h = P.ws.miss_h[r];
     if (r < A) {
@@ -661,10 +571,29 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
       P.pool.h2g[h] = s;
       P.pool.idxbuf[r] = s;
       if (P.mode == kModeAlloc) P.out_slots[f] = s;
+      if (P.mode == kModeRecall) P.out_slot[f] = s;
     } else {  // no slot left: the row stays out of the pool
       P.pool.h2g[h] = kInf;
-      if (P.mode == kModeRecall) P.ws.miss_stage[f] = -1;
+      if (P.mode == kModeRecall) {
+        P.ws.miss_stage[f] = -1;
+        P.out_slot[f] = -1;
+      }
       if (P.mode == kModeAlloc) P.out_slots[f] = -1;
+    }
+  }
+  if (P.mode == kModeRecall) {
+    for (int f = gtid; f < n; f += gthreads) {
+      const int32_t aux = P.ws.ent_aux[f];
+      if (aux == -2) continue;  // owned miss: written above
+      int32_t o = -1;
+      if (aux >= 0) {
+        o = aux;
+        if (P.ws.slot_claim[aux] == f) P.ws.slot_claim[aux] = INT32_MAX;  // the owner clears its mark
+      } else if (aux <= -3) {
+        const int32_t r1 = P.ws.miss_rank[-3 - aux];
+        o = r1 < A ? P.ws.alloc_slot[r1] : -1;
+      }
+      P.out_slot[f] = o;
     }
   }
   if (static_cast<int32_t>(M) > A && c == 0 && threadIdx.x == 0) set_status(P.status, ECHO_DEV_POOL_EXHAUSTED);
@@ -727,14 +656,14 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     P.pool.counters[1] = list_len;
     P.ws.ctr[kCtrMisses] = static_cast<int32_t>(M);
     P.ws.ctr[kCtrGranted] = A;
-    const uint32_t valid = glob[kGValid];
+    const uint32_t valid = glob[kGValid], hits = glob[kGHits];
     glob[kGValid] = 0;
-    glob[kGMin] = 0xFFFFFFFFu;
-    glob[kGMax] = 0;
+    glob[kGHits] = 0;
     if (P.mode == kModeRecall) {
       add_stat(P.stats, &echo_stats::steps, 1ull);
       add_stat(P.stats, &echo_stats::selected, valid);
-      add_stat(P.stats, &echo_stats::unique_rows, static_cast<unsigned long long>(M));  // + hits, in P6
+      add_stat(P.stats, &echo_stats::unique_rows, static_cast<unsigned long long>(M) + hits);
+      add_stat(P.stats, &echo_stats::hits, hits);
       add_stat(P.stats, &echo_stats::misses, M);
       add_stat(P.stats, &echo_stats::recalled, static_cast<unsigned long long>(A));
       add_stat(P.stats, &echo_stats::unrecalled, static_cast<unsigned long long>(M - A));
@@ -743,37 +672,12 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     add_stat(P.stats, &echo_stats::evicted, static_cast<unsigned long long>(E));
     if (P.clock_advance) *P.clock_advance = clock + 1;  // every CTA read the clock at its start
   }
-  if (c == 0)
+  if (c == 0) {
     for (int i = threadIdx.x; i < P.n_ema; i += kCoopThreads) ema_one(P.s_hat, P.kth, i, P.alpha);
+    if (P.mode == kModeRecall && P.stage_count)
+      for (int b = threadIdx.x; b < P.B; b += kCoopThreads) P.stage_count[b] = 0;
+  }
   ECHO_TRACE_MARK(9);
-  if (P.mode != kModeRecall) return;
-  if (!grid_barrier(glob, P.status, S)) return;
-
-  // ===== P6 (recall): out_slot of every entry; each hit counted and cleared by its owner =====
-  uint32_t hits = 0;
-  for (int f = gtid; f < n; f += gthreads) {
-    const int32_t h = P.ws.entry_h[f];
-    int32_t o = -1;
-    if (h >= 0) {
-      const int32_t v = P.pool.h2g[h];
-      if (v >= 0 && v < n_g) {
-        o = v;
-        if (P.ws.slot_claim[v] == f) {
-          ++hits;
-          P.ws.slot_claim[v] = INT32_MAX;
-        }
-      }
-    }
-    P.out_slot[f] = o;
-  }
-  for (int o = 16; o > 0; o >>= 1) hits += __shfl_xor_sync(0xffffffffu, hits, o);
-  if (lane == 0 && hits) {
-    add_stat(P.stats, &echo_stats::hits, hits);
-    add_stat(P.stats, &echo_stats::unique_rows, hits);
-  }
-  if (P.stage_count && c == 0)
-    for (int b = threadIdx.x; b < P.B; b += kCoopThreads) P.stage_count[b] = 0;
-  ECHO_TRACE_MARK(10);
 }
 
 // ---------------------------------------------------------------------------
@@ -853,7 +757,7 @@ __global__ void ws_init_kernel(Workspace ws, int n_g, int max_rows) {
   for (int i = tid; i < max_rows; i += nt) ws.miss_stage[i] = -1;
   for (int i = tid; i < kHistLevels * kHistBins; i += nt) ws.hist[i] = 0;
   for (int i = tid; i < kMaxGrid * kCVals; i += nt) ws.cta[i] = 0;
-  for (int i = tid; i < kGCount; i += nt) ws.glob[i] = (i == kGMin) ? 0xFFFFFFFFu : 0u;
+  for (int i = tid; i < kGCount; i += nt) ws.glob[i] = 0u;
   for (int i = tid; i < kCtrCount; i += nt) ws.ctr[i] = 0;
 }
 
@@ -870,6 +774,9 @@ __global__ void ema_kernel(float *s_hat, const float *kth, int n, float alpha) {
 namespace echo_host {
 
 int sm_count();
+
+echo::PoolView pool_view(const echo_pool *p);
+echo::Workspace workspace_view(const echo_workspace *w);
 
 static echo::PoolView view_of(const echo_pool *p) {
   echo::PoolView v;
@@ -888,11 +795,15 @@ static echo::PoolView view_of(const echo_pool *p) {
 
 size_t workspace_bytes(int32_t n_g, int32_t max_rows) { return echo::ws_layout(n_g, max_rows, 0, nullptr); }
 
+echo::PoolView pool_view(const echo_pool *p) { return view_of(p); }
+
 static echo::Workspace ws_of(const echo_workspace *w) {
   echo::Workspace x;
   echo::ws_layout(w->n_g, w->max_rows, reinterpret_cast<uintptr_t>(w->base), &x);
   return x;
 }
+
+echo::Workspace workspace_view(const echo_workspace *w) { return ws_of(w); }
 
 static int grid_for(long long n, int block) {
   long long g = (n + block - 1) / block;
@@ -969,8 +880,10 @@ int launch_pool_evict(const echo_pool *pool, const echo_workspace *ws, const int
 int launch_recall(const echo_pool *pool, const echo_workspace *ws, const int32_t *sel, const int32_t *req_to_host,
                   const int32_t *ctx_len, int B, int n_q, int k, int L_max, const echo_stage *stage, int32_t clock,
                   const int32_t *clock_dev, int32_t *out_slot, echo_stats *stats, int32_t *status, cudaStream_t s,
-                  float *ema_s_hat, const float *ema_kth, int ema_n, float ema_alpha, int32_t *clock_advance) {
+                  float *ema_s_hat, const float *ema_kth, int ema_n, float ema_alpha, int32_t *clock_advance,
+                  int claimed) {
   echo::OpParams P = base_params(pool, ws, echo::kModeRecall, clock, clock_dev, status);
+  P.claimed = claimed;
   P.F = B * n_q * k;
   P.sel = sel;
   P.req_to_host = req_to_host;

@@ -12,6 +12,7 @@
 // pass writes the selected indices in ascending order: per-thread segment counts,
 // a block scan and a cluster scan give every selected token its output position
 // (ties at the k-th value go to the lower index).
+#include "cache_common.cuh"
 #include "cluster_select.cuh"
 
 ECHO_TRACE_UNIT(topk)
@@ -33,7 +34,7 @@ struct alignas(16) TopkExtra {
 
 __global__ void __launch_bounds__(kSelThreads, 1)
     topk_kernel(const float *__restrict__ scores, const int32_t *__restrict__ ctx_len, int n_q, int L_max, int k,
-                int chunk, int32_t *__restrict__ sel, float *__restrict__ kth) {
+                int chunk, int32_t *__restrict__ sel, float *__restrict__ kth, const ClaimArgs ca, int do_claim) {
   cg::cluster_group cl = cg::this_cluster();
   const int C = static_cast<int>(cl.num_blocks());
   const int rank = static_cast<int>(cl.block_rank());
@@ -251,20 +252,31 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     sel_cluster_prefix2(cl, S, tg, te, pg, pe, gg, ge);
   }
   ECHO_TRACE_MARK(6);
+  // the recall's claim of every selected entry (decode step): see cache_common.cuh
+  const int32_t clock = do_claim ? (ca.clock_dev ? *ca.clock_dev : ca.clock) : 0;
+  const int32_t *r2h = do_claim ? ca.req_to_host + static_cast<size_t>(b) * L_max : nullptr;
+  const int f_row = row * k;
   if (target > 0) {
     uint32_t gb = pg + eg, eb = pe + ee;
     for (int i = s0; i < s1; ++i) {
       const uint32_t key = keys[i];
+      int pos = -1;
       if (key > T) {
-        out[gb + (eb < needT ? eb : needT)] = lo + i;
+        pos = static_cast<int>(gb + (eb < needT ? eb : needT));
         ++gb;
       } else if (key == T) {
-        if (eb < needT) out[gb + eb] = lo + i;
+        if (eb < needT) pos = static_cast<int>(gb + eb);
         ++eb;
       }
+      if (pos < 0) continue;
+      out[pos] = lo + i;
+      if (do_claim) claim_entry(ca.pool, ca.ws, f_row + pos, __ldg(r2h + lo + i), clock, ca.status);
     }
   }
-  for (int i = target + rank * kSelThreads + threadIdx.x; i < k; i += C * kSelThreads) out[i] = -1;
+  for (int i = target + rank * kSelThreads + threadIdx.x; i < k; i += C * kSelThreads) {
+    out[i] = -1;
+    if (do_claim) ca.ws.entry_h[f_row + i] = -1;
+  }
   if (rank == 0 && threadIdx.x == 0) kth[row] = target > 0 ? key_score(T) : -INFINITY;
   cl.sync();  // no CTA leaves while others may still read its shared memory
   ECHO_TRACE_MARK(7);
@@ -274,8 +286,8 @@ __global__ void __launch_bounds__(kSelThreads, 1)
 
 namespace echo_host {
 
-int launch_topk(const float *scores, const int32_t *ctx_len, int B, int n_q, int L_max, int k, int32_t *sel,
-                float *kth, cudaStream_t stream) {
+static int launch_topk_impl(const float *scores, const int32_t *ctx_len, int B, int n_q, int L_max, int k,
+                            int32_t *sel, float *kth, const echo::ClaimArgs &ca, int do_claim, cudaStream_t stream) {
   const int rows = B * n_q;
   if (rows == 0) return ECHO_OK;
   const int C = echo::kTopkCluster;
@@ -305,9 +317,33 @@ int launch_topk(const float *scores, const int32_t *ctx_len, int B, int n_q, int
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, echo::topk_kernel, scores, ctx_len, n_q, L_max, k, chunk, sel, kth);
+  cudaError_t e =
+      cudaLaunchKernelEx(&cfg, echo::topk_kernel, scores, ctx_len, n_q, L_max, k, chunk, sel, kth, ca, do_claim);
   if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
   return ECHO_OK;
+}
+
+int launch_topk(const float *scores, const int32_t *ctx_len, int B, int n_q, int L_max, int k, int32_t *sel,
+                float *kth, cudaStream_t stream) {
+  echo::ClaimArgs none{};
+  return launch_topk_impl(scores, ctx_len, B, n_q, L_max, k, sel, kth, none, 0, stream);
+}
+
+echo::PoolView pool_view(const echo_pool *p);
+echo::Workspace workspace_view(const echo_workspace *w);
+
+// top-k of the decode step: also claims the selected entries for the recall
+int launch_topk_claim(const float *scores, const int32_t *ctx_len, int B, int n_q, int L_max, int k, int32_t *sel,
+                      float *kth, const echo_pool *pool, const echo_workspace *ws, const int32_t *req_to_host,
+                      int32_t clock, const int32_t *clock_dev, int32_t *status, cudaStream_t stream) {
+  echo::ClaimArgs ca{};
+  ca.pool = pool_view(pool);
+  ca.ws = workspace_view(ws);
+  ca.req_to_host = req_to_host;
+  ca.clock = clock;
+  ca.clock_dev = clock_dev;
+  ca.status = status;
+  return launch_topk_impl(scores, ctx_len, B, n_q, L_max, k, sel, kth, ca, 1, stream);
 }
 
 }  // namespace echo_host
