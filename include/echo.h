@@ -231,6 +231,29 @@ int echo_prefetch_recall(const echo_pool *pool, const echo_workspace *ws, const 
                          int32_t *dev_status, void *stream);
 
 /*
+ * The guaranteed recall above, for callers that cannot allocate device memory:
+ * it uses no caller workspace and makes no allocation of any kind (no cudaMalloc,
+ * no cudaFree, no allocating library call).  The page has no counterpart of this
+ * call; it exists for callers such as a memory-planned serving runtime that has
+ * already divided all device memory between weights and KV pools and may not grow
+ * it at run time, or a plugin behind a foreign-language boundary that is handed
+ * buffers but no allocator.
+ * Its scratch is one fixed array inside the library per device (4 MiB, held by
+ * every GPU that loads the library until the process exits), laid out for pools of
+ * at most 262144 slots and at most 32768 selected entries (B * n_q * k); larger
+ * calls return ECHO_EINVAL with a message.  The first call on a device looks up the
+ * array's device address, so make that first call before any stream capture.  Every
+ * call re-initialises the array before using it (one extra small kernel), and all
+ * calls share it: calls whose work overlaps on the GPU (other streams, other
+ * threads) race and must not be issued.  Arguments and results as in
+ * echo_prefetch_recall.
+ */
+int echo_prefetch_recall_noalloc(const echo_pool *pool, const int32_t *sel, const int32_t *req_to_host,
+                                 const int32_t *ctx_len, int32_t B, int32_t n_q, int32_t k, int32_t L_max,
+                                 const echo_stage *stage, int32_t clock, const int32_t *clock_dev,
+                                 int32_t *out_slot, echo_stats *stats, int32_t *dev_status, void *stream);
+
+/*
  * Write-through append of the token each request generated (section 2 "offload";
  * section 5.2 "Free" notes the host copy is made at generation): for request b,
  * p = ctx_len[b]; new_kv[b] is written to host row req_to_host[b][p] and to a newly

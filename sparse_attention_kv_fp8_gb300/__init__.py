@@ -92,6 +92,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                                   _I32, ctypes.POINTER(c_stage), _I32, _P, _P, _P, _P, _P], S),
         "echo_append": ([ctypes.POINTER(c_pool), ctypes.POINTER(c_workspace), _P, _P, _P, _I32, _I32, _P, _P, _I32,
                          _P, _P, _P, _P], S),
+        "echo_prefetch_recall_noalloc": ([ctypes.POINTER(c_pool), _P, _P, _P, _I32, _I32, _I32, _I32,
+                                          ctypes.POINTER(c_stage), _I32, _P, _P, _P, _P, _P], S),
         "echo_ema_update": ([_P, _P, _I32, ctypes.c_float, _P], S),
         "echo_decode_step": ([ctypes.POINTER(c_step_args), _P], S),
         "echo_last_error_string": ([], ctypes.c_char_p),
@@ -262,6 +264,18 @@ def echo_prefetch_recall(pool: Pool, ws: Workspace, sel, req_to_host, ctx_len, c
         ctypes.pointer(stage.c) if stage is not None else None, int(clock), _dev(clock_dev, "clock_dev"),
         _dev(out_slot, "out_slot"), _dev(stats.t, "stats") if stats is not None else None,
         _dev(dev_status, "dev_status"), _stream(stream)), "echo_prefetch_recall")
+
+
+def echo_prefetch_recall_noalloc(pool: Pool, sel, req_to_host, ctx_len, clock: int, out_slot,
+                                 stage: Stage | None = None, stats: Stats | None = None, dev_status=None,
+                                 clock_dev=None, stream=None):
+    """Guaranteed recall without a caller workspace (the library's own fixed scratch)."""
+    B, n_q, k = sel.shape
+    _check(load_library().echo_prefetch_recall_noalloc(
+        ctypes.byref(pool.c), _dev(sel, "sel"), _dev(req_to_host, "req_to_host"), _dev(ctx_len, "ctx_len"), B, n_q,
+        k, req_to_host.shape[1], ctypes.pointer(stage.c) if stage is not None else None, int(clock),
+        _dev(clock_dev, "clock_dev"), _dev(out_slot, "out_slot"), _dev(stats.t, "stats") if stats is not None else None,
+        _dev(dev_status, "dev_status"), _stream(stream)), "echo_prefetch_recall_noalloc")
 
 
 def echo_append(pool: Pool, ws: Workspace, k_index, ctx_len, req_to_host, new_kv, new_k_index, clock: int,

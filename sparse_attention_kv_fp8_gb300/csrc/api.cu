@@ -49,6 +49,7 @@ int launch_append(const echo_pool *pool, const echo_workspace *ws, uint8_t *k_in
                   const int32_t *req_to_host, int B, int L_max, const uint16_t *new_kv, const uint8_t *new_k_index,
                   int32_t clock, const int32_t *clock_dev, echo_stats *stats, int32_t *status, cudaStream_t s);
 int launch_ema(float *s_hat, const float *kth, int n, float alpha, cudaStream_t s);
+int noalloc_workspace(int32_t n_g, int32_t rows, echo_workspace *out);
 
 }  // namespace echo_host
 
@@ -231,6 +232,27 @@ int echo_prefetch_recall(const echo_pool *pool, const echo_workspace *ws, const 
   if (stage) TRY(check_stage(stage));
   return launch_recall(pool, ws, sel, req_to_host, ctx_len, B, n_q, k, L_max, stage, clock, clock_dev, out_slot, stats,
                        dev_status, static_cast<cudaStream_t>(stream), nullptr, nullptr, 0, 0.f, nullptr, 0);
+}
+
+int echo_prefetch_recall_noalloc(const echo_pool *pool, const int32_t *sel, const int32_t *req_to_host,
+                                 const int32_t *ctx_len, int32_t B, int32_t n_q, int32_t k, int32_t L_max,
+                                 const echo_stage *stage, int32_t clock, const int32_t *clock_dev, int32_t *out_slot,
+                                 echo_stats *stats, int32_t *dev_status, void *stream) {
+  g_err[0] = 0;
+  TRY(check_pool(pool));
+  REQUIRE(B >= 0 && L_max >= 0 && k >= 1, "bad sizes");
+  REQUIRE(n_q == 1 || n_q == 2, "n_q must be 1 or 2");
+  REQUIRE(B == 0 || (sel && req_to_host && out_slot && ctx_len), "recall pointer is NULL");
+  REQUIRE(clock >= 0 || clock_dev, "clock must be >= 0");
+  const long long F = static_cast<long long>(B) * n_q * k;
+  REQUIRE(F <= (1ll << 30), "B * n_q * k too large");
+  if (stage) TRY(check_stage(stage));
+  echo_workspace ws;
+  TRY(noalloc_workspace(pool->n_g, static_cast<int32_t>(F), &ws));
+  // the array keeps whatever the last call left: lay it out for this call and reset it
+  TRY(launch_workspace_init(&ws, static_cast<cudaStream_t>(stream)));
+  return launch_recall(pool, &ws, sel, req_to_host, ctx_len, B, n_q, k, L_max, stage, clock, clock_dev, out_slot,
+                       stats, dev_status, static_cast<cudaStream_t>(stream), nullptr, nullptr, 0, 0.f, nullptr, 0);
 }
 
 int echo_append(const echo_pool *pool, const echo_workspace *ws, uint8_t *k_index, int32_t *ctx_len,

@@ -925,6 +925,51 @@ int launch_append(const echo_pool *pool, const echo_workspace *ws, uint8_t *k_in
   return run_op(P, s);
 }
 
+// ---------------------------------------------------------------------------
+// scratch for callers that cannot allocate (echo_prefetch_recall_noalloc)
+// ---------------------------------------------------------------------------
+// One fixed array per device for the whole process: the recall's workspace laid
+// out for at most kNoAllocMaxSlots GPU-pool slots and kNoAllocMaxRows selected
+// entries.  It is shared by every call, so calls that overlap on the GPU race.
+constexpr int32_t kNoAllocMaxSlots = 262144;
+constexpr int32_t kNoAllocMaxRows = 32768;
+constexpr size_t kNoAllocBytes = 4u << 20;  // >= the layout of the two maxima (checked below)
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+// Device address of the array on the current device (resolved once per device,
+// with that device current; host code cannot use the symbol itself as an address).
+int noalloc_workspace(int32_t n_g, int32_t rows, echo_workspace *out) {
+  if (workspace_bytes(kNoAllocMaxSlots, kNoAllocMaxRows) > kNoAllocBytes) {
+    set_error("no-allocation scratch too small for its stated maxima");
+    return ECHO_ENOTSUP;
+  }
+  if (n_g > kNoAllocMaxSlots || rows > kNoAllocMaxRows) {
+    set_error("no-allocation recall supports pools of at most %d slots and at most %d selected entries "
+              "(got %d slots, %d entries); use echo_prefetch_recall with a caller workspace",
+              kNoAllocMaxSlots, kNoAllocMaxRows, n_g, rows);
+    return ECHO_EINVAL;
+  }
+  static void *addr[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) {
+    set_error("device index %d out of range", dev);
+    return ECHO_ENOTSUP;
+  }
+  if (!addr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the no-allocation scratch");
+    addr[dev] = p;
+  }
+  out->base = addr[dev];
+  out->bytes = kNoAllocBytes;
+  out->n_g = n_g;
+  out->max_rows = rows;
+  return ECHO_OK;
+}
+
 int launch_ema(float *s_hat, const float *kth, int n, float alpha, cudaStream_t s) {
   echo::ema_kernel<<<(n + 255) / 256, 256, 0, s>>>(s_hat, kth, n, alpha);
   return check("ema");
