@@ -391,7 +391,7 @@ def run_ours(args):
         "e2e": {"value": 1e3 / e2e_ms, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "echo_decode_step (C ABI, eager) with q/w copied in from pinned host and out_slot/status "
                        "copied back, per step"},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 3 * args.steps,
         "clocks": clk.summary(),
         "dev_status": status,
     }

@@ -255,6 +255,9 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
   const int G = gridDim.x, c = blockIdx.x;
   const int gtid = c * kCoopThreads + threadIdx.x, gthreads = G * kCoopThreads;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  ECHO_TRACE_FIRST(24);
+  pdl_wait();  // the selection and claims come from the kernel before (programmatic launch)
+  ECHO_TRACE_FIRST(26);
   const int32_t clock = read_clock(P);
   const int n_g = P.pool.n_g;
   const int32_t n_free0 = P.pool.counters[0];
@@ -678,6 +681,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
       for (int b = threadIdx.x; b < P.B; b += kCoopThreads) P.stage_count[b] = 0;
   }
   ECHO_TRACE_MARK(9);
+  ECHO_TRACE_LAST(25);
 }
 
 // ---------------------------------------------------------------------------
@@ -842,19 +846,22 @@ static echo::OpParams base_params(const echo_pool *pool, const echo_workspace *w
   return P;
 }
 
-// one cooperative launch over all SMs (one CTA each)
-static int run_op(const echo::OpParams &P, cudaStream_t s) {
+// one cooperative launch over all SMs (one CTA each); `pdl`: programmatic launch
+// after the kernel before it on the stream
+static int run_op(const echo::OpParams &P, cudaStream_t s, bool pdl = false) {
   const int grid = sm_count() < echo::kMaxGrid ? sm_count() : echo::kMaxGrid;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(echo::kCoopThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeCooperative;
   at[0].val.cooperative = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 2 : 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, echo::cache_op_kernel, P);
   return e == cudaSuccess ? ECHO_OK : cuda_fail(e, "cache-manager kernel");
 }
@@ -906,7 +913,7 @@ int launch_recall(const echo_pool *pool, const echo_workspace *ws, const int32_t
   P.n_ema = ema_s_hat ? ema_n : 0;
   P.alpha = ema_alpha;
   P.clock_advance = clock_advance;
-  return run_op(P, s);
+  return run_op(P, s, claimed != 0);  // after the decode step's top-k: programmatic launch
 }
 
 int launch_append(const echo_pool *pool, const echo_workspace *ws, uint8_t *k_index, int32_t *ctx_len,

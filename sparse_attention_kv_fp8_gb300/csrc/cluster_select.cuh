@@ -148,7 +148,8 @@ __device__ __forceinline__ void sel_cluster_prefix2(cg::cluster_group &cl, SelSm
   gb = g[1];
 }
 
-// cluster-wide min and max of per-thread values
+// cluster-wide min and max of per-thread values (at most once per launch: the
+// published pair is not overwritten afterwards, so remote readers need no second barrier)
 __device__ __forceinline__ void sel_cluster_minmax(cg::cluster_group &cl, SelSmem *S, uint32_t mn, uint32_t mx,
                                                    uint32_t &gmn, uint32_t &gmx) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -190,7 +191,7 @@ __device__ __forceinline__ void sel_cluster_minmax(cg::cluster_group &cl, SelSme
       S->res[1] = b;
     }
   }
-  cl.sync();
+  __syncthreads();  // pub[4..5] are written once per launch: no second cluster barrier
   gmn = S->res[0];
   gmx = S->res[1];
   __syncthreads();

@@ -35,24 +35,53 @@ __device__ __forceinline__ uint64_t globaltimer() {
 }
 
 // Phase tracing for development builds (-DECHO_TRACE): each translation unit keeps
-// a small array of %globaltimer stamps written by block 0, thread 0, readable
-// through echo_debug_trace_<unit>().  Product builds compile the marks away.
+// a small array of %globaltimer stamps, readable through echo_debug_trace_<unit>()
+// and set to all ones by echo_debug_trace_clear_<unit>().  ECHO_TRACE_MARK is
+// written by block 0, thread 0; ECHO_TRACE_FIRST keeps the earliest stamp of any
+// block; ECHO_TRACE_LAST keeps the latest, stored complemented.  Product builds
+// compile the marks away.
 #ifdef ECHO_TRACE
 static __device__ unsigned long long g_echo_trace[32];
-#define ECHO_TRACE_UNIT(name)                                                          \
-  extern "C" int echo_debug_trace_##name(unsigned long long *out) {                    \
+#define ECHO_TRACE_UNIT(name)                                                                      \
+  extern "C" int echo_debug_trace_##name(unsigned long long *out) {                                \
     return cudaMemcpyFromSymbol(out, echo::g_echo_trace, sizeof(echo::g_echo_trace)) == cudaSuccess \
-               ? 0                                                                     \
-               : 2;                                                                    \
+               ? 0                                                                                 \
+               : 2;                                                                                \
+  }                                                                                                \
+  extern "C" int echo_debug_trace_clear_##name() {                                                 \
+    unsigned long long ones[32];                                                                   \
+    for (int i = 0; i < 32; ++i) ones[i] = ~0ull;                                                  \
+    return cudaMemcpyToSymbol(echo::g_echo_trace, ones, sizeof(ones)) == cudaSuccess ? 0 : 2;      \
   }
 #define ECHO_TRACE_MARK(slot)                                                          \
   do {                                                                                 \
     if (blockIdx.x == 0 && threadIdx.x == 0) g_echo_trace[slot] = echo::globaltimer(); \
   } while (0)
+#define ECHO_TRACE_FIRST(slot)                                                 \
+  do {                                                                         \
+    if (threadIdx.x == 0) atomicMin(&g_echo_trace[slot], echo::globaltimer()); \
+  } while (0)
+#define ECHO_TRACE_LAST(slot)                                                   \
+  do {                                                                          \
+    if (threadIdx.x == 0) atomicMin(&g_echo_trace[slot], ~echo::globaltimer()); \
+  } while (0)
+#define ECHO_TRACE_LAST_HERE(slot)                           \
+  do {                                                       \
+    atomicMin(&g_echo_trace[slot], ~echo::globaltimer());    \
+  } while (0)
 #else
 #define ECHO_TRACE_UNIT(name)
 #define ECHO_TRACE_MARK(slot) \
   do {                        \
+  } while (0)
+#define ECHO_TRACE_FIRST(slot) \
+  do {                         \
+  } while (0)
+#define ECHO_TRACE_LAST(slot) \
+  do {                        \
+  } while (0)
+#define ECHO_TRACE_LAST_HERE(slot) \
+  do {                             \
   } while (0)
 #endif
 
@@ -61,6 +90,13 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
 }
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31; }
+
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the kernel before it finishes; pdl_wait() blocks
+// until that kernel has completed and its memory is visible (a no-op for an
+// ordinary launch).  pdl_launch_dependents() lets the next such kernel start early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ bool elect_one() {
   uint32_t pred = 0;

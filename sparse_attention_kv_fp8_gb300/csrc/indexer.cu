@@ -25,6 +25,8 @@
 
 #include "echo_common.cuh"
 
+ECHO_TRACE_UNIT(indexer)
+
 namespace echo {
 
 constexpr int kTileTokens = 128;
@@ -114,6 +116,8 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const bool prefetch = P.s_hat != nullptr;
+  pdl_launch_dependents();  // the top-k may be scheduled as SMs free up; it waits for completion
+  ECHO_TRACE_FIRST(24);
 
   // ---- work split: the non-empty tiles of all requests, evenly over the grid
   if (threadIdx.x == 0) {
@@ -325,6 +329,7 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
       __threadfence_block();
       *reinterpret_cast<volatile int *>(&ctl->queue_done[e]) = 1;
     }
+    if (lane == 0) ECHO_TRACE_LAST_HERE(26);
   } else if (prefetch) {
     // ===================== prefetch copies =====================
     // prefetch warp e serves the queues of epilogue warps e, e + kPfWarps, ...
@@ -442,10 +447,12 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
       }
       if (dst >= 0) P.stage_host[dst] = h;
     }
+    if (lane == 0) ECHO_TRACE_LAST_HERE(27);
   }
 
   tc_fence_before();
   __syncthreads();
+  ECHO_TRACE_LAST(25);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);

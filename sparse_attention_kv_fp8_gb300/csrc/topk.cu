@@ -5,13 +5,19 @@
 //
 // sm_103a design: one thread-block cluster of kTopkCluster CTAs per (request,
 // query) row.  Each CTA keeps its slice of the row in shared memory as
-// order-preserving uint32 keys (one global read).  Radix passes over the bits in
-// which the row's keys differ (12-bit digits of key - min) find the k-th largest
-// key exactly: each CTA histograms its slice, the cluster sums the histograms
-// through distributed shared memory, and every CTA picks the same digit.  A final
-// pass writes the selected indices in ascending order: per-thread segment counts,
-// a block scan and a cluster scan give every selected token its output position
-// (ties at the k-th value go to the lower index).
+// order-preserving uint32 keys (one global read).  The keys are reduced to
+// key - min (cluster min / max), and a 12-bit digit of the reduced key (the top
+// bits in which the row's keys differ) is histogrammed per CTA.  The cluster finds
+// the digit d holding the target-th largest key in two small gathers over
+// distributed shared memory: 64-bin coarse histograms first, then the 64 fine bins
+// of the chosen coarse bin -- a few KB per CTA instead of whole histograms.  Every
+// CTA then collects the keys of bin d from the whole cluster (usually a few dozen)
+// and resolves the exact k-th key T and its own output offsets by itself.  A final
+// pass writes the selected indices in ascending order (ties at T go to the lower
+// index).  In the decode step the same kernel makes the recall's claims for the
+// entries it selects, one entry per thread from a compacted list, with the
+// request's host rows staged in shared memory before the scores are ready.
+// A threshold bin with more than kCand keys falls back to full radix passes.
 #include "cache_common.cuh"
 #include "cluster_select.cuh"
 
@@ -21,42 +27,97 @@ namespace echo {
 
 constexpr int kTopkCluster = 8;
 constexpr int kMaxChunk = 44 * 1024;  // keys per CTA kept in shared memory
-constexpr int kCand = 1024;          // threshold-bin keys resolved by one CTA
+constexpr int kCand = 1024;           // threshold-bin keys resolved without more radix passes
+constexpr int kCoarse = 64;           // fine bins per coarse bin
+constexpr int kCoarseBins = kMaxBins / kCoarse;
+constexpr int kList = kMaxBins / 2;   // selected entries a CTA can list for the claims
+constexpr int kTopkSmemMax = 232448;
 
 struct alignas(16) TopkExtra {
-  uint32_t cand_key[kCand];   // rank 0: keys of the threshold bin, from every CTA
-  uint32_t cand_src[kCand];   // rank 0: the CTA each candidate came from
-  uint32_t cand_n;            // rank 0: candidates received
-  uint32_t above[kMaxCluster];  // rank 0: per-CTA count of keys in bins above the threshold bin
-  uint32_t gc[kMaxCluster], ec[kMaxCluster];  // rank 0: per-CTA counts above / equal to T
-  uint32_t T, needT, pg, pe;  // written by rank 0 into every CTA: threshold and this CTA's offsets
+  uint32_t cand_key[kCand];          // this CTA's keys in the threshold bin (read by the cluster)
+  uint32_t all_key[kCand];           // the threshold-bin keys of the whole cluster, in rank order
+  uint32_t coarse[kCoarseBins];      // this CTA's coarse histogram (read by the cluster)
+  uint32_t ctot[kCoarseBins];        // cluster totals of the coarse bins
+  uint32_t ftot[kCoarse];            // cluster totals of the fine bins of the chosen coarse bin
+  uint32_t off[kMaxCluster + 1];     // offsets of each rank's candidates in all_key
+  uint32_t cand_n, above;            // published: keys in the threshold bin, keys above it
+  uint32_t v[12];                    // block-wide values
 };
+
+// The bin at which the running count of 64 bins, taken from the highest bin down,
+// reaches `need` (warp 0 only; cnt(i) gives the count of bin i, 0 <= i < 64).
+// Writes the bin and the count above it to out[0], out[1].
+template <typename Cnt>
+__device__ __forceinline__ void warp_find_from_top64(uint32_t need, Cnt cnt, uint32_t *out) {
+  const int lane = threadIdx.x & 31;
+  const int b0 = 63 - 2 * lane, b1 = 62 - 2 * lane;
+  const uint32_t c0 = cnt(b0), c1 = cnt(b1);
+  const uint32_t s = c0 + c1;
+  uint32_t inc = s;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t u = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += u;
+  }
+  const uint32_t ex = inc - s;
+  if (ex < need && need <= ex + c0) {
+    out[0] = static_cast<uint32_t>(b0);
+    out[1] = ex;
+  } else if (ex + c0 < need && need <= ex + s) {
+    out[0] = static_cast<uint32_t>(b1);
+    out[1] = ex + c0;
+  }
+}
+
+__device__ __forceinline__ uint32_t block_sum(uint32_t v, uint32_t *acc) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if ((threadIdx.x & 31) == 0 && v) atomicAdd(acc, v);
+  __syncthreads();
+  const uint32_t r = *acc;
+  __syncthreads();
+  return r;
+}
 
 __global__ void __launch_bounds__(kSelThreads, 1)
     topk_kernel(const float *__restrict__ scores, const int32_t *__restrict__ ctx_len, int n_q, int L_max, int k,
-                int chunk, int32_t *__restrict__ sel, float *__restrict__ kth, const ClaimArgs ca, int do_claim) {
+                int chunk, int32_t *__restrict__ sel, float *__restrict__ kth, const ClaimArgs ca, int do_claim,
+                int stage_r2h) {
   cg::cluster_group cl = cg::this_cluster();
   const int C = static_cast<int>(cl.num_blocks());
   const int rank = static_cast<int>(cl.block_rank());
   const int row = blockIdx.x / C;
   const int b = row / n_q, j = row % n_q;
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SelSmem *S = reinterpret_cast<SelSmem *>(smem_raw);
   TopkExtra *X = reinterpret_cast<TopkExtra *>(smem_raw + sizeof(SelSmem));
   uint32_t *keys = reinterpret_cast<uint32_t *>(smem_raw + sizeof(SelSmem) + sizeof(TopkExtra));
+  int32_t *r2s = reinterpret_cast<int32_t *>(keys + chunk);  // staged host rows (stage_r2h)
+  uint32_t *list_pos = S->tot, *list_tok = S->tot + kList;   // claim list (tot is free by then)
+  ECHO_TRACE_FIRST(24);
 
-  ECHO_TRACE_MARK(0);
+  // ---- what does not come from the kernel before: the row's length, its host rows
   int L = __ldg(ctx_len + b);
   L = L < 0 ? 0 : (L > L_max ? L_max : L);
   const int Lr = query_valid_len(L, n_q, j);
   const int target = Lr < k ? Lr : k;
-  const float *srow = scores + static_cast<size_t>(row) * L_max;
-  int32_t *out = sel + static_cast<size_t>(row) * k;
-
   const int lo = rank * chunk;
   const int hi = lo + chunk < Lr ? lo + chunk : Lr;
   const int n_local = hi > lo ? hi - lo : 0;
+  const int32_t *r2h = do_claim ? ca.req_to_host + static_cast<size_t>(b) * L_max + lo : nullptr;
+  if (stage_r2h)
+    for (int i = threadIdx.x; i < n_local; i += kSelThreads) r2s[i] = __ldg(r2h + i);
+  for (int i = threadIdx.x; i < kCoarseBins; i += kSelThreads) X->ctot[i] = 0;
+  if (threadIdx.x < kCoarse) X->ftot[threadIdx.x] = 0;
+  if (threadIdx.x < 12) X->v[threadIdx.x] = 0;
+
+  pdl_wait();  // the scores come from the kernel before (programmatic launch)
+  pdl_launch_dependents();
+  ECHO_TRACE_FIRST(26);
+  ECHO_TRACE_MARK(0);
+  const float *srow = scores + static_cast<size_t>(row) * L_max;
+  int32_t *out = sel + static_cast<size_t>(row) * k;
 
   // ---- the slice as order-preserving keys (16-byte loads when aligned), with its min / max
   uint32_t mn = 0xFFFFFFFFu, mx = 0;
@@ -84,9 +145,6 @@ __global__ void __launch_bounds__(kSelThreads, 1)
       mx = max(mx, a);
     }
   }
-  // the cluster-wide histogram is summed into every CTA's `tot`: clear it first
-  for (int i = threadIdx.x; i < kMaxBins; i += kSelThreads) S->tot[i] = 0;
-  if (threadIdx.x == 0) X->cand_n = 0;
   __syncthreads();
   ECHO_TRACE_MARK(1);
 
@@ -96,65 +154,66 @@ __global__ void __launch_bounds__(kSelThreads, 1)
   bool offsets_known = false;
   if (target > 0) {
     uint32_t kmin, kmax;
-    sel_cluster_minmax(cl, S, mn, mx, kmin, kmax);  // also orders the clearing above before remote adds
+    sel_cluster_minmax(cl, S, mn, mx, kmin, kmax);
     ECHO_TRACE_MARK(2);
     const uint32_t range = kmax - kmin;
     const int hb = range == 0 ? 0 : 32 - __clz(range);
     const int width = hb < kDigitBits ? hb : kDigitBits;
     const int shift = hb - width;
     const int nb = 1 << width;
-    // first digit: local histogram, added into every CTA's total
+    const int nco = (nb + kCoarse - 1) / kCoarse;
     sel_histogram(S, n_local, 32, shift, nb, 0u, [&](int i, uint32_t &x) {
       x = keys[i] - kmin;
       return true;
     });
-    for (int i = threadIdx.x; i < nb; i += kSelThreads) {
-      const uint32_t v = S->hist[i];
-      if (v)
-        for (int r = 0; r < C; ++r) atomicAdd(cl.map_shared_rank(&S->tot[i], r), v);
+    // coarse histogram: one warp per coarse bin
+    for (int cb = warp; cb < nco; cb += kSelWarps) {
+      uint32_t c = 0;
+      for (int i = lane; i < kCoarse; i += 32) c += cb * kCoarse + i < nb ? S->hist[cb * kCoarse + i] : 0u;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+      if (lane == 0) X->coarse[cb] = c;
     }
-    cl.sync();
+    cl.sync();  // every CTA's fine and coarse histograms complete
     ECHO_TRACE_MARK(3);
-    // digit d holding the target-th largest key (descending running count)
-    const int per = (nb + kSelThreads - 1) / kSelThreads;
-    const int p0 = threadIdx.x * per;
-    uint32_t cnt = 0, mine_above = 0;
-    for (int u = 0; u < per; ++u)
-      if (p0 + u < nb) cnt += S->tot[nb - 1 - (p0 + u)];
-    uint32_t ex, dz, tt, tz;
-    sel_block_scan2(cnt, 0, ex, dz, tt, tz, S);
-    uint32_t run = ex;
-    for (int u = 0; u < per; ++u) {
-      const int idx = p0 + u;
-      if (idx >= nb) break;
-      const int bin = nb - 1 - idx;
-      const uint32_t cb = S->tot[bin];
-      if (run < static_cast<uint32_t>(target) && run + cb >= static_cast<uint32_t>(target)) {
-        S->result[0] = static_cast<uint32_t>(bin);
-        S->result[1] = run;
-      }
-      run += cb;
+    // cluster totals of the coarse bins; the coarse bin D holding the target-th key
+    if (threadIdx.x < C * nco) {
+      const int r = threadIdx.x / nco, cb = threadIdx.x % nco;
+      const uint32_t v = cl.map_shared_rank(X->coarse, r)[cb];
+      if (v) atomicAdd(&X->ctot[cb], v);
     }
     __syncthreads();
-    const uint32_t d = S->result[0];
-    const uint32_t need_d = static_cast<uint32_t>(target) - S->result[1];
-    const uint32_t cnt_d = S->tot[d];
-    // this CTA's keys in bins above d, and in bin d
+    if (warp == 0)
+      warp_find_from_top64(static_cast<uint32_t>(target), [&](int i) { return i < nco ? X->ctot[i] : 0u; },
+                           &X->v[0]);
+    __syncthreads();
+    const uint32_t D = X->v[0], above_D = X->v[1];
+    // cluster totals of D's fine bins; the digit d
+    if (threadIdx.x < C * kCoarse) {
+      const int r = threadIdx.x / kCoarse, i = threadIdx.x % kCoarse;
+      const int fb = static_cast<int>(D) * kCoarse + i;
+      if (fb < nb) {
+        const uint32_t v = cl.map_shared_rank(S->hist, r)[fb];
+        if (v) atomicAdd(&X->ftot[i], v);
+      }
+    }
+    __syncthreads();
+    if (warp == 0)
+      warp_find_from_top64(static_cast<uint32_t>(target) - above_D, [&](int i) { return X->ftot[i]; }, &X->v[2]);
+    __syncthreads();
+    const uint32_t d = D * kCoarse + X->v[2];
+    const uint32_t above_d = above_D + X->v[3];
+    const uint32_t cnt_d = X->ftot[X->v[2]];
+    const uint32_t need_d = static_cast<uint32_t>(target) - above_d;
+    // this CTA's keys above bin d, and in it
+    uint32_t mine = 0;
     for (int i = threadIdx.x; i < nb; i += kSelThreads)
-      if (static_cast<uint32_t>(i) > d) mine_above += S->hist[i];
-    uint32_t in_d = S->hist[d];
-    uint32_t ea, eb0, ta, tb0;
-    sel_block_scan2(mine_above, 0, ea, eb0, ta, tb0, S);
-    mine_above = ta;
-    if (shift == 0) {
-      // one key value per bin: T is exact, the local histogram gives the counts
-      T = kmin + d;
-      needT = need_d;
-      sel_cluster_prefix2(cl, S, mine_above, in_d, pg, pe, tt, tz);
-      offsets_known = true;
-    } else if (cnt_d <= static_cast<uint32_t>(kCand)) {
-      // ship the bin's keys to rank 0, which resolves T and every CTA's offsets
-      TopkExtra *X0 = cl.map_shared_rank(X, 0);
+      if (static_cast<uint32_t>(i) > d) mine += S->hist[i];
+    const uint32_t mine_above = block_sum(mine, &X->v[4]);
+    const uint32_t in_d = S->hist[d];
+    ECHO_TRACE_MARK(4);
+    if (cnt_d <= static_cast<uint32_t>(kCand)) {
+      // collect the bin's keys from the whole cluster; every CTA resolves T itself
       for (int base = (threadIdx.x & ~31); base < n_local; base += kSelThreads) {
         const int i = base + lane;
         const uint32_t key = i < n_local ? keys[i] : 0u;
@@ -162,66 +221,78 @@ __global__ void __launch_bounds__(kSelThreads, 1)
         const uint32_t m = __ballot_sync(0xffffffffu, cand);
         if (!m) continue;
         uint32_t slot = 0;
-        if (lane == __ffs(m) - 1) slot = atomicAdd(&X0->cand_n, static_cast<uint32_t>(__popc(m)));
+        if (lane == __ffs(m) - 1) slot = atomicAdd(&X->v[5], static_cast<uint32_t>(__popc(m)));
         slot = __shfl_sync(0xffffffffu, slot, __ffs(m) - 1);
-        if (cand) {
-          const uint32_t at = slot + __popc(m & ((1u << lane) - 1));
-          X0->cand_key[at] = key;
-          X0->cand_src[at] = static_cast<uint32_t>(rank);
+        if (cand) X->cand_key[slot + __popc(m & ((1u << lane) - 1))] = key;
+      }
+      if (threadIdx.x == 0) {
+        X->cand_n = in_d;
+        X->above = mine_above;
+      }
+      cl.sync();  // every CTA's candidates published
+      if (warp == 0) {
+        const TopkExtra *R = cl.map_shared_rank(X, lane < C ? lane : 0);
+        const uint32_t n = lane < C ? R->cand_n : 0u, a = lane < C ? R->above : 0u;
+        uint32_t inc = n, ia = a;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t u = __shfl_up_sync(0xffffffffu, inc, o);
+          const uint32_t ua = __shfl_up_sync(0xffffffffu, ia, o);
+          if (lane >= o) {
+            inc += u;
+            ia += ua;
+          }
+        }
+        if (lane <= C) X->off[lane] = inc - n;  // lane C: the total
+        if (lane == rank) X->v[6] = ia - a;     // keys above bin d in lower CTAs
+      }
+      __syncthreads();
+      const int nc = static_cast<int>(X->off[C]);
+      for (int g = threadIdx.x; g < nc; g += kSelThreads) {
+        int r = 0;
+        while (r + 1 < C && X->off[r + 1] <= static_cast<uint32_t>(g)) ++r;
+        X->all_key[g] = cl.map_shared_rank(X->cand_key, r)[g - static_cast<int>(X->off[r])];
+      }
+      __syncthreads();
+      for (int i = threadIdx.x; i < nc; i += kSelThreads) {
+        const uint32_t ki = X->all_key[i];
+        uint32_t greater = 0, equal = 0;
+        for (int jj = 0; jj < nc; ++jj) {
+          const uint32_t kj = X->all_key[jj];
+          greater += kj > ki;
+          equal += kj == ki;
+        }
+        if (greater < need_d && need_d <= greater + equal) {  // every such thread holds the same key
+          X->v[7] = ki;
+          X->v[8] = need_d - greater;
         }
       }
-      if (threadIdx.x == 0) X0->above[rank] = mine_above;
-      cl.sync();
-      ECHO_TRACE_MARK(4);
-      if (rank == 0) {
-        const int nc = static_cast<int>(X->cand_n);
-        if (threadIdx.x < kMaxCluster) {
-          X->gc[threadIdx.x] = 0;
-          X->ec[threadIdx.x] = 0;
-        }
-        __syncthreads();
-        for (int i = threadIdx.x; i < nc; i += kSelThreads) {
-          const uint32_t ki = X->cand_key[i];
-          uint32_t greater = 0, equal = 0;
-          for (int jj = 0; jj < nc; ++jj) {
-            const uint32_t kj = X->cand_key[jj];
-            greater += kj > ki;
-            equal += kj == ki;
-          }
-          if (greater < need_d && need_d <= greater + equal) {
-            S->result[0] = ki;
-            S->result[1] = need_d - greater;
-          }
-        }
-        __syncthreads();
-        const uint32_t Tk = S->result[0];
-        for (int i = threadIdx.x; i < nc; i += kSelThreads) {
-          const uint32_t ki = X->cand_key[i];
-          if (ki > Tk) atomicAdd(&X->gc[X->cand_src[i]], 1u);
-          if (ki == Tk) atomicAdd(&X->ec[X->cand_src[i]], 1u);
-        }
-        __syncthreads();
-        if (threadIdx.x < C) {
-          uint32_t g0 = 0, e0 = 0;
-          for (int r = 0; r < static_cast<int>(threadIdx.x); ++r) {
-            g0 += X->above[r] + X->gc[r];
-            e0 += X->ec[r];
-          }
-          TopkExtra *Xr = cl.map_shared_rank(X, static_cast<int>(threadIdx.x));
-          Xr->T = Tk;
-          Xr->needT = S->result[1];
-          Xr->pg = g0;
-          Xr->pe = e0;
-        }
+      __syncthreads();
+      T = X->v[7];
+      needT = X->v[8];
+      // keys of lower CTAs' candidates above / equal to T
+      const int n_lower = static_cast<int>(X->off[rank]);
+      uint32_t g = 0, e = 0;
+      for (int i = threadIdx.x; i < n_lower; i += kSelThreads) {
+        const uint32_t ki = X->all_key[i];
+        g += ki > T;
+        e += ki == T;
       }
-      cl.sync();
-      T = X->T;
-      needT = X->needT;
-      pg = X->pg;
-      pe = X->pe;
+      g = block_sum(g, &X->v[9]);
+      e = block_sum(e, &X->v[10]);
+      pg = X->v[6] + g;
+      pe = e;
+      offsets_known = true;
+    } else if (shift == 0) {
+      // every key of bin d equals T: counts of the histogram are exact
+      T = kmin + d;
+      needT = need_d;
+      uint32_t ga, gb;
+      sel_cluster_prefix2(cl, S, mine_above, in_d, pg, pe, ga, gb);
       offsets_known = true;
     } else {
       // many keys share the threshold bin (ties or a clustered row): exact radix passes
+      cl.sync();  // no CTA still reads this CTA's histogram
       sel_radix_select(cl, S, n_local, kmin, kmax, static_cast<uint32_t>(target), true,
                        [&](int i, uint32_t &key) {
                          key = keys[i];
@@ -254,23 +325,44 @@ __global__ void __launch_bounds__(kSelThreads, 1)
   ECHO_TRACE_MARK(6);
   // the recall's claim of every selected entry (decode step): see cache_common.cuh
   const int32_t clock = do_claim ? (ca.clock_dev ? *ca.clock_dev : ca.clock) : 0;
-  const int32_t *r2h = do_claim ? ca.req_to_host + static_cast<size_t>(b) * L_max : nullptr;
   const int f_row = row * k;
+  const uint32_t mpe = pe < needT ? pe : needT;
+  const uint32_t te_taken = (pe + te < needT ? pe + te : needT) - mpe;
+  const uint32_t n_sel = target > 0 ? tg + te_taken : 0u;
+  const bool use_list = do_claim && n_sel <= static_cast<uint32_t>(kList);
   if (target > 0) {
     uint32_t gb = pg + eg, eb = pe + ee;
     for (int i = s0; i < s1; ++i) {
       const uint32_t key = keys[i];
       int pos = -1;
+      uint32_t li = 0;
       if (key > T) {
+        li = (gb - pg) + ((eb < needT ? eb : needT) - mpe);
         pos = static_cast<int>(gb + (eb < needT ? eb : needT));
         ++gb;
       } else if (key == T) {
-        if (eb < needT) pos = static_cast<int>(gb + eb);
+        if (eb < needT) {
+          li = (gb - pg) + (eb - mpe);
+          pos = static_cast<int>(gb + eb);
+        }
         ++eb;
       }
       if (pos < 0) continue;
       out[pos] = lo + i;
-      if (do_claim) claim_entry(ca.pool, ca.ws, f_row + pos, __ldg(r2h + lo + i), clock, ca.status);
+      if (use_list) {
+        list_pos[li] = static_cast<uint32_t>(pos);
+        list_tok[li] = static_cast<uint32_t>(i);
+      } else if (do_claim) {
+        claim_entry(ca.pool, ca.ws, f_row + pos, __ldg(r2h + i), clock, ca.status);
+      }
+    }
+  }
+  if (use_list) {
+    __syncthreads();
+    for (int li = threadIdx.x; li < static_cast<int>(n_sel); li += kSelThreads) {
+      const int i = static_cast<int>(list_tok[li]);
+      const int32_t h = stage_r2h ? r2s[i] : __ldg(r2h + i);
+      claim_entry(ca.pool, ca.ws, f_row + static_cast<int>(list_pos[li]), h, clock, ca.status);
     }
   }
   for (int i = target + rank * kSelThreads + threadIdx.x; i < k; i += C * kSelThreads) {
@@ -280,6 +372,7 @@ __global__ void __launch_bounds__(kSelThreads, 1)
   if (rank == 0 && threadIdx.x == 0) kth[row] = target > 0 ? key_score(T) : -INFINITY;
   cl.sync();  // no CTA leaves while others may still read its shared memory
   ECHO_TRACE_MARK(7);
+  ECHO_TRACE_LAST(25);
 }
 
 }  // namespace echo
@@ -287,7 +380,8 @@ __global__ void __launch_bounds__(kSelThreads, 1)
 namespace echo_host {
 
 static int launch_topk_impl(const float *scores, const int32_t *ctx_len, int B, int n_q, int L_max, int k,
-                            int32_t *sel, float *kth, const echo::ClaimArgs &ca, int do_claim, cudaStream_t stream) {
+                            int32_t *sel, float *kth, const echo::ClaimArgs &ca, int do_claim, cudaStream_t stream,
+                            bool pdl) {
   const int rows = B * n_q;
   if (rows == 0) return ECHO_OK;
   const int C = echo::kTopkCluster;
@@ -297,11 +391,22 @@ static int launch_topk_impl(const float *scores, const int32_t *ctx_len, int B, 
     set_error("top-k: L_max %d exceeds the supported %d", L_max, C * echo::kMaxChunk);
     return ECHO_ENOTSUP;
   }
-  const size_t smem = sizeof(echo::SelSmem) + sizeof(echo::TopkExtra) +
-                      static_cast<size_t>(chunk > 0 ? chunk : 4) * sizeof(uint32_t);
+  const size_t fixed = sizeof(echo::SelSmem) + sizeof(echo::TopkExtra);
+  size_t smem = fixed + static_cast<size_t>(chunk > 0 ? chunk : 4) * sizeof(uint32_t);
+  if (smem > static_cast<size_t>(echo::kTopkSmemMax)) {
+    set_error("top-k: L_max %d needs more shared memory than a CTA has", L_max);
+    return ECHO_ENOTSUP;
+  }
+  // the host rows of the slice go to shared memory too when they fit
+  int stage_r2h = 0;
+  if (do_claim && smem + static_cast<size_t>(chunk) * sizeof(int32_t) <= static_cast<size_t>(echo::kTopkSmemMax)) {
+    smem += static_cast<size_t>(chunk) * sizeof(int32_t);
+    stage_r2h = 1;
+  }
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(echo::topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    cudaError_t e = cudaFuncSetAttribute(echo::topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         echo::kTopkSmemMax);
     if (e != cudaSuccess) return cuda_fail(e, "top-k smem attribute");
     attr = true;
   }
@@ -310,15 +415,18 @@ static int launch_topk_impl(const float *scores, const int32_t *ctx_len, int B, 
   cfg.blockDim = dim3(echo::kSelThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = C;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 2 : 1;
   cudaError_t e =
-      cudaLaunchKernelEx(&cfg, echo::topk_kernel, scores, ctx_len, n_q, L_max, k, chunk, sel, kth, ca, do_claim);
+      cudaLaunchKernelEx(&cfg, echo::topk_kernel, scores, ctx_len, n_q, L_max, k, chunk, sel, kth, ca, do_claim,
+                         stage_r2h);
   if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
   return ECHO_OK;
 }
@@ -326,13 +434,14 @@ static int launch_topk_impl(const float *scores, const int32_t *ctx_len, int B, 
 int launch_topk(const float *scores, const int32_t *ctx_len, int B, int n_q, int L_max, int k, int32_t *sel,
                 float *kth, cudaStream_t stream) {
   echo::ClaimArgs none{};
-  return launch_topk_impl(scores, ctx_len, B, n_q, L_max, k, sel, kth, none, 0, stream);
+  return launch_topk_impl(scores, ctx_len, B, n_q, L_max, k, sel, kth, none, 0, stream, false);
 }
 
 echo::PoolView pool_view(const echo_pool *p);
 echo::Workspace workspace_view(const echo_workspace *w);
 
-// top-k of the decode step: also claims the selected entries for the recall
+// top-k of the decode step: also claims the selected entries for the recall, and
+// is launched programmatically after the indexer
 int launch_topk_claim(const float *scores, const int32_t *ctx_len, int B, int n_q, int L_max, int k, int32_t *sel,
                       float *kth, const echo_pool *pool, const echo_workspace *ws, const int32_t *req_to_host,
                       int32_t clock, const int32_t *clock_dev, int32_t *status, cudaStream_t stream) {
@@ -343,7 +452,7 @@ int launch_topk_claim(const float *scores, const int32_t *ctx_len, int B, int n_
   ca.clock = clock;
   ca.clock_dev = clock_dev;
   ca.status = status;
-  return launch_topk_impl(scores, ctx_len, B, n_q, L_max, k, sel, kth, ca, 1, stream);
+  return launch_topk_impl(scores, ctx_len, B, n_q, L_max, k, sel, kth, ca, 1, stream, true);
 }
 
 }  // namespace echo_host

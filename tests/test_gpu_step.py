@@ -107,6 +107,30 @@ def test_decode_steps_match_oracle(B, n_q, L, ctx0, k, n_g, res, append, seed):
         check_step_against_oracle(c, R, q, kv, ki, append, kI_o, ctx_o, s_hat_o, 1000 + step)
 
 
+def test_decode_step_rows_beyond_the_claim_list_and_unstaged_host_rows():
+    """Two top-k claim paths the workloads above do not reach: one CTA's slice holding
+    more selected entries than its claim list (k = 4096 with every positive score in the
+    first slice), and rows too long for the host rows of a slice to be staged in shared
+    memory (L = 200000)."""
+    for B, L, k, concentrate in ((2, 20000, 4096, True), (1, 200000, 2048, False)):
+        c = Case(B, 1, L, L, 3 * B * k, 2 * B * k, clock=700, seed=41, k=k)
+        if concentrate:
+            ki = c.inp.k_index.copy()
+            ki[:, L // 8:, :] = 0          # e4m3 code 0 is +0: these tokens score exactly 0
+            c.inp.k_index[...] = ki
+            c.k_index.copy_(dev(ki))
+        R = StepRunner(c, s_hat0=float("inf"), append=False)
+        kI_o, ctx_o = c.inp.k_index.copy(), c.inp.ctx_len.copy()
+        s_hat_o = np.full((B, 1), np.inf, np.float32)
+        qf = c.inp.q_float
+        for step in range(2):
+            qf, q, kv, ki2 = step_inputs(c, step, qf)
+            R.set_inputs(q)
+            R.out.dev_status.zero_()
+            R.run()
+            check_step_against_oracle(c, R, q, kv, ki2, False, kI_o, ctx_o, s_hat_o, 700 + step)
+
+
 def test_prefetch_stages_exactly_the_candidates_tiny():
     """Tiny workload, threshold at the oracle's 90th-percentile score: the staged set is
     the candidate set (non-resident tokens scoring above the threshold, decided on the

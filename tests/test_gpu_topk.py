@@ -65,3 +65,19 @@ def test_topk_degenerate_rows():
     sel, kth = gpu_topk(s, [0, 1, 5, 300], 8)
     assert list(sel[0, 0]) == [-1] * 8 and kth[0, 0] == -np.inf
     assert list(sel[1, 0]) == [0] + [-1] * 7
+
+
+def test_topk_massive_ties_and_clustered_rows():
+    """Threshold bins with more than a thousand keys: a row of three values (exact bins,
+    ties at the k-th value decided by index) and a row whose keys crowd into one bin
+    between two far outliers (more radix passes)."""
+    L = 20000
+    g = np.random.default_rng(8)
+    s = np.empty((3, 1, L), np.float32)
+    s[0, 0] = g.integers(0, 3, size=L).astype(np.float32)
+    s[1, 0] = (1.0 + 1e-3 * g.standard_normal(L)).astype(np.float32)
+    s[1, 0, 17] = np.float32(1e30)
+    s[1, 0, 18] = np.float32(-1e30)
+    s[2, 0] = np.float32(5.0)
+    check(s, [L, L, L], 2048)
+    check(s, [L, L - 3, 4097], 4096)
