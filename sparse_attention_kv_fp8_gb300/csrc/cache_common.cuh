@@ -36,6 +36,7 @@ struct Workspace {
   int32_t *miss_h;      // [max_rows] host row of the r-th owned miss
   int32_t *miss_rank;   // [max_rows] by entry: rank of an owned miss
   int32_t *miss_stage;  // [max_rows] by entry: staging row index, -1 = not staged
+  int32_t *miss_src;    // [max_rows] staging row index of the r-th owned miss, -1 = host pool
   int32_t *alloc_slot;  // [max_rows] the r-th free slot (taken by the r-th miss)
   uint32_t *hist;       // [kHistLevels][kHistBins]
   uint32_t *cta;        // [kMaxGrid][kCVals]
@@ -62,6 +63,7 @@ __host__ __device__ inline size_t ws_layout(int32_t n_g, int32_t max_rows, uintp
   x.miss_h = reinterpret_cast<int32_t *>(take(R));
   x.miss_rank = reinterpret_cast<int32_t *>(take(R));
   x.miss_stage = reinterpret_cast<int32_t *>(take(R));
+  x.miss_src = reinterpret_cast<int32_t *>(take(R));
   x.alloc_slot = reinterpret_cast<int32_t *>(take(R));
   x.hist = reinterpret_cast<uint32_t *>(take(static_cast<size_t>(kHistLevels) * kHistBins));
   x.cta = reinterpret_cast<uint32_t *>(take(static_cast<size_t>(kMaxGrid) * kCVals));

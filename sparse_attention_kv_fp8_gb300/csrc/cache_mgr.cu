@@ -17,21 +17,24 @@
 // bounded grid barriers:
 //   P1  (only when no earlier kernel did it) claims of the entries, see
 //       cache_common.cuh; the decode step's top-k kernel claims what it selects.
-//   P2  histogram of the evictable slots by age (clock - 1 - priority, 4096 bins,
-//       the last one open-ended); each entry classified (owned miss, repeat, hit),
-//       owned misses counted per CTA; staged-row lookup.
+//   P2  three warp roles at once: the slot scan (states cached in shared memory,
+//       histogram of the evictable slots by age = clock - 1 - priority, 4096 bins,
+//       the last one open-ended); the entries (classified as owned miss, repeat or
+//       hit, hits' out_slot written, owned misses counted per CTA); the lookup of
+//       the rows the prefetch staged.
 //   P3  misses M = sum of the owned counts, evictions E = max(0, M - free); every
 //       CTA finds the same threshold T (the E-th oldest priority, refined while the
-//       open bin holds it); owned misses listed in entry order; per-CTA counts of
-//       slots older than / at T and free.
-//   P4  prefix sums over the per-CTA counts give each slot its eviction and free-slot
-//       rank: victims are scattered (free = 1, priority = -1, maps to INF), the r-th
-//       free slot is recorded for miss r.  This is the page's ticket order taken in
-//       slot order, so the result is deterministic.
+//       open bin holds it); owned misses listed in entry order with their sources;
+//       per-CTA counts of slots older than / at T and free.
+//   P4  each warp starts reading the KV rows of its first misses; prefix sums over
+//       the per-CTA counts give each slot its eviction and free-slot rank: victims
+//       are scattered (free = 1, priority = -1, maps to INF), the r-th free slot is
+//       recorded for miss r.  This is the page's ticket order taken in slot order,
+//       so the result is deterministic.
 //   P5  the r-th miss takes the r-th free slot (maps, priority = clock, indices
-//       buffer), out_slot of every entry, and each recalled KV row is copied
-//       (16-byte vectors, 4 rows in flight per warp) from the staging area or the
-//       pinned host pool.
+//       buffer, out_slot) and its row, already in registers, is stored (16-byte
+//       vectors, 4 rows per warp, from the staging area or the pinned host pool);
+//       repeats of a miss take its slot.
 #include "cache_common.cuh"
 
 ECHO_TRACE_UNIT(cache_mgr)
@@ -79,6 +82,8 @@ struct OpParams {
   int n_ema;
   float alpha;
   int32_t *clock_advance;
+  // shared-memory caches (entries per CTA they hold; 0 = not cached)
+  int slot_cache_cap, ent_cache_cap;
 };
 
 __device__ __forceinline__ int32_t read_clock(const OpParams &P) { return P.clock_dev ? *P.clock_dev : P.clock; }
@@ -249,9 +254,47 @@ __device__ __forceinline__ void find_from_top(const uint32_t *gh, uint32_t need,
   __syncthreads();
 }
 
+constexpr int32_t kFreeMark = INT32_MIN;  // slot-cache value of a free slot
+constexpr int kSlotWarps = 8;              // P2 roles: slot scan, entries, staged rows
+constexpr int kEntWarps = 6;
+constexpr int kStageWarps = kCoopWarps - kSlotWarps - kEntWarps;
+constexpr int kRows = 4;                   // KV rows a warp copies at once
+constexpr int kRowVecs = (kRows * kKvChunks + 31) / 32;  // 16-byte vectors per lane
+
+// Loads of up to kRows KV rows (one warp): row u of the group comes from src[u].
+__device__ __forceinline__ void rows_load(const int4 *const (&src)[kRows], int nr, int4 (&buf)[kRowVecs]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int m = 0; m < kRowVecs; ++m) {
+    const int idx = m * 32 + lane;
+    const int u = idx / kKvChunks, ch = idx % kKvChunks;
+    if (u < nr) buf[m] = __ldcs(pick_reg(src, u) + ch);
+  }
+}
+
+__device__ __forceinline__ void rows_store(int4 *dst, const int32_t (&slot)[kRows], int n_keep,
+                                           const int4 (&buf)[kRowVecs]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int m = 0; m < kRowVecs; ++m) {
+    const int idx = m * 32 + lane;
+    const int u = idx / kKvChunks, ch = idx % kKvChunks;
+    if (u < n_keep) dst[static_cast<size_t>(pick_reg(slot, u)) * kKvChunks + ch] = buf[m];
+  }
+}
+
+// Source of the KV row of miss (entry f, host row h, staging index st): the
+// generated token (append), the staging area, or the pinned host pool.
+__device__ __forceinline__ const int4 *row_source(const OpParams &P, int32_t f, int32_t h, int32_t st) {
+  if (P.mode == kModeAppend) return reinterpret_cast<const int4 *>(P.new_kv) + static_cast<size_t>(f) * kKvChunks;
+  if (st >= 0) return reinterpret_cast<const int4 *>(P.stage_rows) + static_cast<size_t>(st) * kKvChunks;
+  return reinterpret_cast<const int4 *>(P.pool.host_kv) + static_cast<size_t>(h) * kKvChunks;
+}
+
 __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParams P) {
   __shared__ CoopSmem S_;
   CoopSmem *S = &S_;
+  extern __shared__ __align__(16) int32_t dyn_smem[];
   const int G = gridDim.x, c = blockIdx.x;
   const int gtid = c * kCoopThreads + threadIdx.x, gthreads = G * kCoopThreads;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -271,6 +314,18 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
   const int s_hi = static_cast<int>((static_cast<long long>(n_g) * (c + 1)) / G);
   const int e_lo = static_cast<int>((static_cast<long long>(n) * c) / G);
   const int e_hi = static_cast<int>((static_cast<long long>(n) * (c + 1)) / G);
+  // shared-memory copies of the slot states (priority, kFreeMark if free) and of the
+  // entries' classification, when they fit; the slots do not change from P2 to P4
+  int32_t *slot_cache = (s_hi - s_lo) <= P.slot_cache_cap ? dyn_smem : nullptr;
+  int32_t *host_cache = slot_cache ? dyn_smem + P.slot_cache_cap : nullptr;  // GPUTokenToHost of the slots
+  int32_t *aux_cache = (e_hi - e_lo) <= P.ent_cache_cap ? dyn_smem + 2 * P.slot_cache_cap : nullptr;
+  int32_t *h_cache = aux_cache ? aux_cache + P.ent_cache_cap : nullptr;     // host row of the entries
+  auto slot_val = [&](int s) -> int32_t {
+    if (slot_cache) return slot_cache[s - s_lo];
+    return P.pool.free_[s] ? kFreeMark : P.pool.prio[s];
+  };
+  auto aux_of = [&](int f) -> int32_t { return aux_cache ? aux_cache[f - e_lo] : P.ws.ent_aux[f]; };
+  const bool copies = P.mode == kModeRecall || P.mode == kModeAppend;
 
   // ===== P1: claims, unless the top-k kernel (recall) or the append already made them =====
   if ((P.mode == kModeRecall && !P.claimed) || P.mode == kModeAlloc) {
@@ -297,54 +352,109 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
   }
   ECHO_TRACE_MARK(2);
 
-  // ===== P2: age histogram; entries classified; owned misses per CTA; staged rows =====
-  if (P.mode != kModeAlloc) {
-    for (int i = threadIdx.x; i < kHistBins; i += kCoopThreads) S->hist[i] = 0;
-    __syncthreads();
-    for (int s = s_lo + threadIdx.x; s < s_hi; s += kCoopThreads) {
-      const int32_t pr = P.pool.prio[s];
-      if (evictable(P.pool.free_[s], pr, clock)) atomicAdd(&S->hist[min(slot_age(clock, pr), kHistBins - 1u)], 1u);
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < kHistBins; i += kCoopThreads)
-      if (S->hist[i]) atomicAdd(P.ws.hist + i, S->hist[i]);
-  }
-  if (P.mode != kModeEvict) {
-    uint32_t own = 0, hits = 0, valid = 0;
-    for (int f = e_lo + threadIdx.x; f < e_hi; f += kCoopThreads) {
-      const int32_t h = P.mode == kModeAppend ? P.ws.entry_rows[f] : P.ws.entry_h[f];
-      int32_t aux = -1;
-      if (h >= 0) {
-        ++valid;
-        const int32_t v = P.pool.h2g[h];
-        if (v == kClaim + f) {
-          ++own;
-          aux = -2;
-        } else if (v >= 0 && v < n_g) {  // recall hit
-          aux = v;
-          hits += P.ws.slot_claim[v] == f;
-        } else if (v < 0) {  // a repeat of a row an earlier entry claimed
-          if (P.mode == kModeRecall) {
-            aux = -3 - static_cast<int32_t>(static_cast<uint32_t>(v) - 0x80000000u);
-          } else {
-            if (P.mode == kModeAlloc) P.out_slots[f] = -1;
-            set_status(P.status, ECHO_DEV_BAD_INDEX);
-          }
+  // ===== P2: three roles at once -- slot scan (states, age histogram), entries
+  // (classification, out_slot of hits), staged-row lookup =====
+  if (c == G - 1)  // the EMA needs only this step's k-th scores (complete before this kernel)
+    for (int i = threadIdx.x; i < P.n_ema; i += kCoopThreads) ema_one(P.s_hat, P.kth, i, P.alpha);
+  for (int i = threadIdx.x; i < kHistBins; i += kCoopThreads) S->hist[i] = 0;
+  if (threadIdx.x < 8) S->red[threadIdx.x] = 0;
+  __syncthreads();
+  if (warp < kSlotWarps) {
+    constexpr int kT = kSlotWarps * 32, kU = 4;
+    const bool hist_on = P.mode != kModeAlloc;
+    for (int s0 = s_lo + static_cast<int>(threadIdx.x); s0 < s_hi; s0 += kT * kU) {
+      uint8_t fr[kU];
+      int32_t pr[kU], th[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int s = s0 + u * kT;
+        fr[u] = 1;
+        pr[u] = 0;
+        th[u] = 0;
+        if (s < s_hi) {
+          fr[u] = P.pool.free_[s];
+          pr[u] = P.pool.prio[s];
+          if (host_cache) th[u] = P.pool.to_host[s];
         }
       }
-      P.ws.ent_aux[f] = aux;
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int s = s0 + u * kT;
+        if (s >= s_hi) continue;
+        const int32_t v = fr[u] ? kFreeMark : pr[u];
+        if (slot_cache) {
+          slot_cache[s - s_lo] = v;
+          host_cache[s - s_lo] = th[u];
+        }
+        if (hist_on && v >= 0 && v < clock) atomicAdd(&S->hist[min(slot_age(clock, v), kHistBins - 1u)], 1u);
+      }
     }
-    uint32_t v3[3] = {own, hits, valid}, ex3[3], tot3[3];
-    coop_scan<3>(v3, ex3, tot3, S);
-    if (threadIdx.x == 0) {
-      P.ws.cta[c * kCVals + kCOwn] = tot3[0];
-      if (tot3[1]) atomicAdd(glob + kGHits, tot3[1]);
-      if (tot3[2]) atomicAdd(glob + kGValid, tot3[2]);
+  } else if (warp < kSlotWarps + kEntWarps) {
+    if (P.mode != kModeEvict) {
+      constexpr int kT = kEntWarps * 32, kU = 2;
+      const int t = static_cast<int>(threadIdx.x) - kSlotWarps * 32;
+      uint32_t own = 0, hits = 0, valid = 0;
+      for (int f0 = e_lo + t; f0 < e_hi; f0 += kT * kU) {
+        int32_t h[kU], v[kU], sc[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int f = f0 + u * kT;
+          h[u] = -1;
+          if (f < e_hi) h[u] = P.mode == kModeAppend ? P.ws.entry_rows[f] : P.ws.entry_h[f];
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) v[u] = h[u] >= 0 ? P.pool.h2g[h[u]] : kInf;
+#pragma unroll
+        for (int u = 0; u < kU; ++u) sc[u] = (h[u] >= 0 && v[u] >= 0 && v[u] < n_g) ? P.ws.slot_claim[v[u]] : -1;
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int f = f0 + u * kT;
+          if (f >= e_hi) continue;
+          int32_t aux = -1;
+          if (h[u] >= 0) {
+            ++valid;
+            if (v[u] == kClaim + f) {
+              ++own;
+              aux = -2;
+            } else if (v[u] >= 0 && v[u] < n_g) {  // recall hit
+              aux = v[u];
+              if (sc[u] == f) {  // the first entry of the row: count it, clear its mark
+                ++hits;
+                P.ws.slot_claim[v[u]] = INT32_MAX;
+              }
+            } else if (v[u] < 0) {  // a repeat of a row an earlier entry claimed
+              if (P.mode == kModeRecall) {
+                aux = -3 - static_cast<int32_t>(static_cast<uint32_t>(v[u]) - 0x80000000u);
+              } else {
+                if (P.mode == kModeAlloc) P.out_slots[f] = -1;
+                set_status(P.status, ECHO_DEV_BAD_INDEX);
+              }
+            }
+          }
+          P.ws.ent_aux[f] = aux;
+          if (aux_cache) {
+            aux_cache[f - e_lo] = aux;
+            h_cache[f - e_lo] = h[u];
+          }
+          if (P.mode == kModeRecall && aux >= -1) P.out_slot[f] = aux;  // hit slot, or -1
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        own += __shfl_xor_sync(0xffffffffu, own, o);
+        hits += __shfl_xor_sync(0xffffffffu, hits, o);
+        valid += __shfl_xor_sync(0xffffffffu, valid, o);
+      }
+      if (lane == 0) {
+        if (own) atomicAdd(&S->red[0], own);
+        if (hits) atomicAdd(&S->red[1], hits);
+        if (valid) atomicAdd(&S->red[2], valid);
+      }
     }
-  }
-  if (P.mode == kModeRecall && P.stage_count != nullptr) {
+  } else if (P.mode == kModeRecall && P.stage_count != nullptr) {
     // which claimed misses the prefetch staged this step (one warp per request)
-    for (int b = c * kCoopWarps + warp; b < P.B; b += G * kCoopWarps) {
+    const int sw = warp - kSlotWarps - kEntWarps;
+    for (int b = c * kStageWarps + sw; b < P.B; b += G * kStageWarps) {
       int L = P.ctx_len[b];
       L = L < 0 ? 0 : (L > P.L_max ? P.L_max : L);
       int cap = (L + P.cap_div - 1) / P.cap_div;
@@ -363,23 +473,61 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
       if (lane == 0) add_stat(P.stats, &echo_stats::staged, static_cast<unsigned long long>(nb));
     }
   }
+  __syncthreads();
+  if (P.mode != kModeAlloc)
+    for (int i = threadIdx.x; i < kHistBins; i += kCoopThreads)
+      if (S->hist[i]) atomicAdd(P.ws.hist + i, S->hist[i]);
+  if (threadIdx.x == 0 && P.mode != kModeEvict) {
+    P.ws.cta[c * kCVals + kCOwn] = S->red[0];
+    if (S->red[1]) atomicAdd(glob + kGHits, S->red[1]);
+    if (S->red[2]) atomicAdd(glob + kGValid, S->red[2]);
+  }
   ECHO_TRACE_MARK(3);
   if (!grid_barrier(glob, P.status, S)) return;
   ECHO_TRACE_MARK(4);
 
   // ===== P3: M, E, threshold; owned misses listed in entry order; per-CTA slot counts =====
-  uint32_t M = 0, pre_own = 0;
-  if (P.mode != kModeEvict) {
-    uint32_t m = 0, pm = 0;
+  // the per-CTA owned counts and the age histogram (highest bin first) load together
+  constexpr int kPerBin = kHistBins / kCoopThreads;
+  uint32_t hcnt[kPerBin];
+  uint32_t m = 0, pm = 0, hmine = 0;
+  if (P.mode != kModeEvict)
     for (int r = threadIdx.x; r < G; r += kCoopThreads) {
       const uint32_t x = __ldcg(P.ws.cta + r * kCVals + kCOwn);
       m += x;
       if (r < c) pm += x;
     }
-    uint32_t v2[2] = {m, pm}, ex2[2], tot2[2];
-    coop_scan<2>(v2, ex2, tot2, S);
-    M = tot2[0];
-    pre_own = tot2[1];
+#pragma unroll
+  for (int u = 0; u < kPerBin; ++u) {
+    hcnt[u] = P.mode != kModeAlloc ? __ldcg(P.ws.hist + (kHistBins - 1 - (threadIdx.x * kPerBin + u))) : 0u;
+    hmine += hcnt[u];
+  }
+  // final after the barrier: the step's valid entries and hits (for the stats)
+  uint32_t g_valid = 0, g_hits = 0;
+  if (c == 0 && threadIdx.x == 0) {
+    g_valid = __ldcg(glob + kGValid);
+    g_hits = __ldcg(glob + kGHits);
+    glob[kGValid] = 0;
+    glob[kGHits] = 0;
+  }
+  // this thread's segment of the entries; the staging rows of its owned misses
+  const int e_cnt = e_hi - e_lo;
+  const int e_per = (e_cnt + kCoopThreads - 1) / kCoopThreads;
+  const int ef0 = e_lo + min(e_cnt, static_cast<int>(threadIdx.x) * e_per);
+  const int ef1 = e_lo + min(e_cnt, static_cast<int>(threadIdx.x + 1) * e_per);
+  constexpr int kStg = 8;
+  int32_t stg[kStg];
+#pragma unroll
+  for (int u = 0; u < kStg; ++u)
+    stg[u] = (P.mode == kModeRecall && ef0 + u < ef1 && aux_of(ef0 + u) == -2) ? P.ws.miss_stage[ef0 + u] : -1;
+  uint32_t M = 0, pre_own = 0, hist_total = 0, hist_ex = 0;
+  {
+    uint32_t v3[3] = {m, pm, hmine}, ex3[3], tot3[3];
+    coop_scan<3>(v3, ex3, tot3, S);
+    M = tot3[0];
+    pre_own = tot3[1];
+    hist_total = tot3[2];
+    hist_ex = ex3[2];
   }
   int32_t E = 0;
   if (P.mode == kModeEvict) {
@@ -389,19 +537,26 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     E = static_cast<int32_t>(M) - n_free0;
     E = E < 0 ? 0 : E;
   }
+  if (E > 0 && hist_total < static_cast<uint32_t>(E)) {  // fewer evictable slots than asked
+    if (c == 0 && threadIdx.x == 0) set_status(P.status, ECHO_DEV_POOL_EXHAUSTED);
+    E = static_cast<int32_t>(hist_total);
+  }
   int32_t Tp = 0;  // threshold priority: victims have priority < Tp, or == Tp (the first needT)
   uint32_t needT = 0;
-  uint32_t d = 0, above = 0;
   if (E > 0) {
-    uint32_t total;
-    find_from_top(P.ws.hist, static_cast<uint32_t>(E), d, above, total, S);
-    if (total < static_cast<uint32_t>(E)) {  // fewer evictable slots than asked
-      if (c == 0 && threadIdx.x == 0) set_status(P.status, ECHO_DEV_POOL_EXHAUSTED);
-      E = static_cast<int32_t>(total);
-      if (E > 0) find_from_top(P.ws.hist, static_cast<uint32_t>(E), d, above, total, S);
+    // the age bin where the count from the oldest bin down reaches E
+    uint32_t run = hist_ex;
+#pragma unroll
+    for (int u = 0; u < kPerBin; ++u) {
+      if (run < static_cast<uint32_t>(E) && run + hcnt[u] >= static_cast<uint32_t>(E)) {
+        S->red[0] = static_cast<uint32_t>(kHistBins - 1 - (threadIdx.x * kPerBin + u));
+        S->red[1] = run;
+      }
+      run += hcnt[u];
     }
-  }
-  if (E > 0) {
+    __syncthreads();
+    const uint32_t d = S->red[0], above = S->red[1];
+    __syncthreads();
     uint32_t need = static_cast<uint32_t>(E) - above;
     uint32_t age_t = d;
     if (d == kHistBins - 1) {
@@ -415,8 +570,8 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
         for (int i = threadIdx.x; i < kHistBins; i += kCoopThreads) S->hist[i] = 0;
         __syncthreads();
         for (int s = s_lo + threadIdx.x; s < s_hi; s += kCoopThreads) {
-          const int32_t pr = P.pool.prio[s];
-          if (!evictable(P.pool.free_[s], pr, clock)) continue;
+          const int32_t pr = slot_val(s);
+          if (!(pr >= 0 && pr < clock)) continue;
           const uint32_t age = slot_age(clock, pr);
           if (age < kHistBins - 1u) continue;
           const uint32_t x = age - (kHistBins - 1u);
@@ -439,21 +594,28 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     Tp = clock - 1 - static_cast<int32_t>(age_t);
     needT = need;
   }
-  // owned misses, in entry order (contiguous per-thread segments)
+  // owned misses, in entry order (contiguous per-thread segments), with their sources
   if (P.mode != kModeEvict) {
-    const int cnt = e_hi - e_lo;
-    const int per = (cnt + kCoopThreads - 1) / kCoopThreads;
-    const int f0 = e_lo + min(cnt, static_cast<int>(threadIdx.x) * per);
-    const int f1 = e_lo + min(cnt, static_cast<int>(threadIdx.x + 1) * per);
     uint32_t own = 0;
-    for (int f = f0; f < f1; ++f) own += P.ws.ent_aux[f] == -2;
+    for (int f = ef0; f < ef1; ++f) own += aux_of(f) == -2;
     uint32_t v1[1] = {own}, ex1[1], tot1[1];
     coop_scan<1>(v1, ex1, tot1, S);
     uint32_t r = pre_own + ex1[0];
-    for (int f = f0; f < f1; ++f) {
-      if (P.ws.ent_aux[f] != -2) continue;
+#pragma unroll
+    for (int u = 0; u < kStg; ++u) {
+      const int f = ef0 + u;
+      if (f >= ef1 || aux_of(f) != -2) continue;
       P.ws.miss_f[r] = f;
-      P.ws.miss_h[r] = P.mode == kModeAppend ? P.ws.entry_rows[f] : P.ws.entry_h[f];
+      P.ws.miss_h[r] = h_cache ? h_cache[f - e_lo] : (P.mode == kModeAppend ? P.ws.entry_rows[f] : P.ws.entry_h[f]);
+      P.ws.miss_src[r] = stg[u];
+      P.ws.miss_rank[f] = static_cast<int32_t>(r);
+      ++r;
+    }
+    for (int f = ef0 + kStg; f < ef1; ++f) {
+      if (aux_of(f) != -2) continue;
+      P.ws.miss_f[r] = f;
+      P.ws.miss_h[r] = h_cache ? h_cache[f - e_lo] : (P.mode == kModeAppend ? P.ws.entry_rows[f] : P.ws.entry_h[f]);
+      P.ws.miss_src[r] = P.mode == kModeRecall ? P.ws.miss_stage[f] : -1;
       P.ws.miss_rank[f] = static_cast<int32_t>(r);
       ++r;
     }
@@ -461,15 +623,12 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
   {
     uint32_t lt = 0, eq = 0, fr = 0;
     for (int s = s_lo + threadIdx.x; s < s_hi; s += kCoopThreads) {
-      const uint8_t f8 = P.pool.free_[s];
-      if (f8) {
+      const int32_t v = slot_val(s);
+      if (v == kFreeMark) {
         ++fr;
-      } else if (E > 0) {
-        const int32_t pr = P.pool.prio[s];
-        if (evictable(0, pr, clock)) {
-          lt += pr < Tp;
-          eq += pr == Tp;
-        }
+      } else if (E > 0 && v >= 0 && v < clock) {
+        lt += v < Tp;
+        eq += v == Tp;
       }
     }
     uint32_t v3[3] = {lt, eq, fr}, ex3[3], tot3[3];
@@ -484,7 +643,18 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
   if (!grid_barrier(glob, P.status, S)) return;
   ECHO_TRACE_MARK(6);
 
-  // ===== P4: victims evicted; free-slot list =====
+  // ===== P4: victims evicted; free-slot list.  Each warp first loads its first KV
+  // rows (misses gw * kRows ...), so that the host reads overlap this phase =====
+  const int gw = gtid >> 5, nw = gthreads >> 5;
+  int4 buf[kRowVecs];
+  int32_t my_f = -1, my_h = -1, my_src = -1;  // lane u < kRows: row gw * kRows + u
+  const int my_r0 = gw * kRows;
+  const int my_nr = M > static_cast<uint32_t>(my_r0) ? min(kRows, static_cast<int>(M) - my_r0) : 0;
+  if (lane < my_nr) {
+    my_f = P.ws.miss_f[my_r0 + lane];
+    my_h = P.ws.miss_h[my_r0 + lane];
+    my_src = P.ws.miss_src[my_r0 + lane];
+  }
   uint32_t pre_lt = 0, pre_eq = 0, pre_fr = 0, free_total = 0;
   {
     uint32_t a3[3] = {0, 0, 0}, t1 = 0;
@@ -505,6 +675,16 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     pre_fr = tot4[2];
     free_total = tot4[3];
   }
+  if (copies && my_nr > 0) {
+    const int4 *src[kRows];
+#pragma unroll
+    for (int u = 0; u < kRows; ++u) {
+      const int32_t f = __shfl_sync(0xffffffffu, my_f, u), h = __shfl_sync(0xffffffffu, my_h, u),
+                    st = __shfl_sync(0xffffffffu, my_src, u);
+      src[u] = u < my_nr ? row_source(P, f, h, st) : nullptr;
+    }
+    rows_load(src, my_nr, buf);
+  }
   const int32_t A = (P.mode == kModeEvict) ? 0 : static_cast<int32_t>(min(M, free_total + static_cast<uint32_t>(E)));
   {
     const int cnt = s_hi - s_lo;
@@ -513,44 +693,39 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     const int q1 = s_lo + min(cnt, static_cast<int>(threadIdx.x + 1) * per);
     uint32_t lt = 0, eq = 0, fr = 0;
     for (int s = q0; s < q1; ++s) {
-      const uint8_t f8 = P.pool.free_[s];
-      if (f8) {
+      const int32_t v = slot_val(s);
+      if (v == kFreeMark) {
         ++fr;
-      } else if (E > 0) {
-        const int32_t pr = P.pool.prio[s];
-        if (evictable(0, pr, clock)) {
-          lt += pr < Tp;
-          eq += pr == Tp;
-        }
+      } else if (E > 0 && v >= 0 && v < clock) {
+        lt += v < Tp;
+        eq += v == Tp;
       }
     }
     uint32_t v3[3] = {lt, eq, fr}, ex3[3], tot3[3];
     coop_scan<3>(v3, ex3, tot3, S);
     uint32_t lt_b = pre_lt + ex3[0], eq_b = pre_eq + ex3[1], fr_b = pre_fr + ex3[2];
     for (int s = q0; s < q1; ++s) {
-      const uint8_t f8 = P.pool.free_[s];
+      const int32_t v = slot_val(s);
       // victims before s (all evictable slots older than T, the first needT at T), and
       // the slots before s that are free after the eviction (free ones and victims)
       const uint32_t vb = lt_b + min(eq_b, needT);
       const uint32_t before = fr_b + vb;
-      if (f8) {
+      if (v == kFreeMark) {
         if (before < static_cast<uint32_t>(A)) P.ws.alloc_slot[before] = s;
         ++fr_b;
         continue;
       }
-      if (E == 0) continue;
-      const int32_t pr = P.pool.prio[s];
-      if (!evictable(0, pr, clock)) continue;
+      if (E == 0 || !(v >= 0 && v < clock)) continue;
       bool victim = false;
-      if (pr < Tp) {
+      if (v < Tp) {
         victim = true;
         ++lt_b;
-      } else if (pr == Tp) {
+      } else if (v == Tp) {
         victim = eq_b < needT;
         ++eq_b;
       }
       if (!victim) continue;
-      const int32_t h = P.pool.to_host[s];
+      const int32_t h = host_cache ? host_cache[s - s_lo] : P.pool.to_host[s];
       P.pool.free_[s] = 1;
       P.pool.prio[s] = -1;
       if (h >= 0 && h < P.pool.n_h) P.pool.h2g[h] = kInf;
@@ -563,94 +738,74 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
   if (!grid_barrier(glob, P.status, S)) return;
   ECHO_TRACE_MARK(8);
 
-  // ===== P5: the r-th miss takes the r-th free slot; out_slot; KV rows copied =====
-  for (int r = gtid; r < static_cast<int>(M); r += gthreads) {
-    const int32_t f = P.ws.miss_f[r], h = P.ws.miss_h[r];
-    if (r < A) {
-      const int32_t s = P.ws.alloc_slot[r];
-      P.pool.free_[s] = 0;
-      P.pool.prio[s] = clock;
-      P.pool.to_host[s] = h;
-      P.pool.h2g[h] = s;
-      P.pool.idxbuf[r] = s;
-      if (P.mode == kModeAlloc) P.out_slots[f] = s;
-      if (P.mode == kModeRecall) P.out_slot[f] = s;
-    } else {  // no slot left: the row stays out of the pool
-      P.pool.h2g[h] = kInf;
-      if (P.mode == kModeRecall) {
-        P.ws.miss_stage[f] = -1;
-        P.out_slot[f] = -1;
+  // ===== P5: the r-th miss takes the r-th free slot (maps, priority, indices buffer,
+  // out_slot, bytes); then the repeats of misses take their first entry's slot =====
+  unsigned long long used = 0;
+  for (int r0 = gw * kRows; r0 < static_cast<int>(M); r0 += nw * kRows) {
+    const int nr = min(kRows, static_cast<int>(M) - r0);
+    const bool first = r0 == gw * kRows;  // rows loaded in P4
+    int32_t f = -1, h = -1, st = -1, s = -1;
+    if (lane < nr) {
+      if (first) {
+        f = my_f;
+        h = my_h;
+        st = my_src;
+      } else {
+        f = P.ws.miss_f[r0 + lane];
+        h = P.ws.miss_h[r0 + lane];
+        st = P.ws.miss_src[r0 + lane];
       }
-      if (P.mode == kModeAlloc) P.out_slots[f] = -1;
+      const int r = r0 + lane;
+      if (r < A) {
+        s = P.ws.alloc_slot[r];
+        P.pool.free_[s] = 0;
+        P.pool.prio[s] = clock;
+        P.pool.to_host[s] = h;
+        P.pool.h2g[h] = s;
+        P.pool.idxbuf[r] = s;
+        if (P.mode == kModeAlloc) P.out_slots[f] = s;
+        if (P.mode == kModeRecall) {
+          P.out_slot[f] = s;
+          used += st >= 0;
+        }
+      } else {  // no slot left: the row stays out of the pool
+        P.pool.h2g[h] = kInf;
+        if (P.mode == kModeRecall) P.out_slot[f] = -1;
+        if (P.mode == kModeAlloc) P.out_slots[f] = -1;
+      }
+      if (P.mode == kModeRecall) P.ws.miss_stage[f] = -1;  // staging lookup back to its resting state
+    }
+    if (copies) {
+      int32_t slot[kRows];
+      const int4 *src[kRows];
+#pragma unroll
+      for (int u = 0; u < kRows; ++u) {
+        slot[u] = __shfl_sync(0xffffffffu, s, u);
+        const int32_t fu = __shfl_sync(0xffffffffu, f, u), hu = __shfl_sync(0xffffffffu, h, u),
+                      su = __shfl_sync(0xffffffffu, st, u);
+        src[u] = u < nr ? row_source(P, fu, hu, su) : nullptr;
+      }
+      if (!first) rows_load(src, nr, buf);
+      // rows r0 .. r0 + n_keep - 1 were granted a slot
+      const int n_keep = A - r0 < nr ? (A - r0 > 0 ? A - r0 : 0) : nr;
+      rows_store(reinterpret_cast<int4 *>(P.pool.gpu_kv), slot, n_keep, buf);
     }
   }
   if (P.mode == kModeRecall) {
-    for (int f = gtid; f < n; f += gthreads) {
-      const int32_t aux = P.ws.ent_aux[f];
-      if (aux == -2) continue;  // owned miss: written above
-      int32_t o = -1;
-      if (aux >= 0) {
-        o = aux;
-        if (P.ws.slot_claim[aux] == f) P.ws.slot_claim[aux] = INT32_MAX;  // the owner clears its mark
-      } else if (aux <= -3) {
-        const int32_t r1 = P.ws.miss_rank[-3 - aux];
-        o = r1 < A ? P.ws.alloc_slot[r1] : -1;
-      }
-      P.out_slot[f] = o;
+    for (int f = e_lo + static_cast<int>(threadIdx.x); f < e_hi; f += kCoopThreads) {
+      const int32_t aux = aux_of(f);
+      if (aux > -3) continue;
+      const int32_t r1 = P.ws.miss_rank[-3 - aux];
+      P.out_slot[f] = r1 < A ? P.ws.alloc_slot[r1] : -1;
     }
   }
   if (static_cast<int32_t>(M) > A && c == 0 && threadIdx.x == 0) set_status(P.status, ECHO_DEV_POOL_EXHAUSTED);
   const int32_t list_len = P.mode == kModeEvict ? E : A;
   for (int i = list_len + gtid; i < prev_idx && i < n_g; i += gthreads) P.pool.idxbuf[i] = -1;
-  if (P.mode == kModeRecall || P.mode == kModeAppend) {
-    constexpr int kRows = 4;  // rows a warp moves at once (9 16-byte vectors in flight per lane)
-    const int4 *host = reinterpret_cast<const int4 *>(P.pool.host_kv);
-    const int4 *stg = reinterpret_cast<const int4 *>(P.stage_rows);
-    const int4 *nkv = reinterpret_cast<const int4 *>(P.new_kv);
-    int4 *dst = reinterpret_cast<int4 *>(P.pool.gpu_kv);
-    unsigned long long used = 0;
-    const int gw = gtid >> 5, nw = gthreads >> 5;
-    for (int r0 = gw * kRows; r0 < A; r0 += nw * kRows) {
-      const int nr = A - r0 < kRows ? A - r0 : kRows;
-      const int4 *src[kRows];
-      int32_t slot[kRows];
+  if (P.mode == kModeRecall) {
 #pragma unroll
-      for (int u = 0; u < kRows; ++u) {
-        src[u] = nullptr;
-        slot[u] = 0;
-        if (u < nr) {
-          const int32_t f = P.ws.miss_f[r0 + u];
-          slot[u] = P.ws.alloc_slot[r0 + u];
-          if (P.mode == kModeAppend) {
-            src[u] = nkv + static_cast<size_t>(f) * kKvChunks;
-          } else {
-            const int32_t st = P.ws.miss_stage[f];
-            if (st >= 0) {
-              src[u] = stg + static_cast<size_t>(st) * kKvChunks;
-              used += lane == 0;
-            } else {
-              src[u] = host + static_cast<size_t>(P.ws.miss_h[r0 + u]) * kKvChunks;
-            }
-          }
-        }
-      }
-      constexpr int kPer = (kRows * kKvChunks + 31) / 32;
-      int4 buf[kPer];
-#pragma unroll
-      for (int m = 0; m < kPer; ++m) {
-        const int idx = m * 32 + lane;
-        const int u = idx / kKvChunks, ch = idx % kKvChunks;
-        if (u < nr) buf[m] = __ldcs(src[u] + ch);
-      }
-#pragma unroll
-      for (int m = 0; m < kPer; ++m) {
-        const int idx = m * 32 + lane;
-        const int u = idx / kKvChunks, ch = idx % kKvChunks;
-        if (u < nr) dst[static_cast<size_t>(slot[u]) * kKvChunks + ch] = buf[m];
-      }
-      if (P.mode == kModeRecall && lane < nr) P.ws.miss_stage[P.ws.miss_f[r0 + lane]] = -1;
-    }
-    add_stat(P.stats, &echo_stats::staged_used, used);
+    for (int o = 16; o > 0; o >>= 1) used += __shfl_xor_sync(0xffffffffu, used, o);
+    if (lane == 0) add_stat(P.stats, &echo_stats::staged_used, used);
   }
   // scratch back to its resting state (nothing reads it any more)
   for (int i = gtid; i < kHistLevels * kHistBins; i += gthreads) P.ws.hist[i] = 0;
@@ -659,9 +814,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     P.pool.counters[1] = list_len;
     P.ws.ctr[kCtrMisses] = static_cast<int32_t>(M);
     P.ws.ctr[kCtrGranted] = A;
-    const uint32_t valid = glob[kGValid], hits = glob[kGHits];
-    glob[kGValid] = 0;
-    glob[kGHits] = 0;
+    const uint32_t valid = g_valid, hits = g_hits;
     if (P.mode == kModeRecall) {
       add_stat(P.stats, &echo_stats::steps, 1ull);
       add_stat(P.stats, &echo_stats::selected, valid);
@@ -675,11 +828,8 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     add_stat(P.stats, &echo_stats::evicted, static_cast<unsigned long long>(E));
     if (P.clock_advance) *P.clock_advance = clock + 1;  // every CTA read the clock at its start
   }
-  if (c == 0) {
-    for (int i = threadIdx.x; i < P.n_ema; i += kCoopThreads) ema_one(P.s_hat, P.kth, i, P.alpha);
-    if (P.mode == kModeRecall && P.stage_count)
-      for (int b = threadIdx.x; b < P.B; b += kCoopThreads) P.stage_count[b] = 0;
-  }
+  if (c == 0 && P.mode == kModeRecall && P.stage_count)
+    for (int b = threadIdx.x; b < P.B; b += kCoopThreads) P.stage_count[b] = 0;
   ECHO_TRACE_MARK(9);
   ECHO_TRACE_LAST(25);
 }
@@ -848,12 +998,27 @@ static echo::OpParams base_params(const echo_pool *pool, const echo_workspace *w
 
 // one cooperative launch over all SMs (one CTA each); `pdl`: programmatic launch
 // after the kernel before it on the stream
-static int run_op(const echo::OpParams &P, cudaStream_t s, bool pdl = false) {
+constexpr int kSlotCacheMax = 16384;  // slots per CTA whose states P2 keeps in shared memory
+constexpr int kEntCacheMax = 4096;    // entries per CTA whose classification P2 keeps
+
+static int run_op(const echo::OpParams &P0, cudaStream_t s, bool pdl = false) {
   const int grid = sm_count() < echo::kMaxGrid ? sm_count() : echo::kMaxGrid;
+  echo::OpParams P = P0;
+  const long long spc = (static_cast<long long>(P.pool.n_g) + grid - 1) / grid;
+  const long long epc = (static_cast<long long>(P.mode == echo::kModeEvict ? 0 : P.F) + grid - 1) / grid;
+  P.slot_cache_cap = spc <= kSlotCacheMax ? static_cast<int>(spc) : 0;
+  P.ent_cache_cap = epc <= kEntCacheMax ? static_cast<int>(epc) : 0;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(echo::cache_op_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         2 * (kSlotCacheMax + kEntCacheMax) * static_cast<int>(sizeof(int32_t)));
+    if (e != cudaSuccess) return cuda_fail(e, "cache-manager smem attribute");
+    attr = true;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(echo::kCoopThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = static_cast<size_t>(2 * P.slot_cache_cap + 2 * P.ent_cache_cap) * sizeof(int32_t);
   cfg.stream = s;
   cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeCooperative;

@@ -91,6 +91,16 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31; }
 
+// element u of a small register array, u not known at compile time (a select
+// chain keeps the array in registers instead of local memory)
+template <typename T, int N>
+__device__ __forceinline__ T pick_reg(const T (&a)[N], int u) {
+  T x = a[0];
+#pragma unroll
+  for (int i = 1; i < N; ++i) x = u == i ? a[i] : x;
+  return x;
+}
+
 // Programmatic dependent launch: a kernel launched with programmatic stream
 // serialization may start while the kernel before it finishes; pdl_wait() blocks
 // until that kernel has completed and its memory is visible (a no-op for an

@@ -27,6 +27,22 @@
 
 ECHO_TRACE_UNIT(indexer)
 
+#ifdef ECHO_TRACE
+// development builds: per-CTA prefetch figures (rows copied, batches, slowest
+// batch in ns, sum of batch times in ns)
+static __device__ unsigned long long g_pf_diag[1024][4];
+extern "C" int echo_debug_pf_indexer(unsigned long long *out, int n) {
+  return cudaMemcpyFromSymbol(out, g_pf_diag, sizeof(unsigned long long) * 4 * (n < 1024 ? n : 1024)) ==
+                 cudaSuccess
+             ? 0
+             : 2;
+}
+extern "C" int echo_debug_pf_clear_indexer() {
+  static unsigned long long zeros[1024][4];
+  return cudaMemcpyToSymbol(g_pf_diag, zeros, sizeof(zeros)) == cudaSuccess ? 0 : 2;
+}
+#endif
+
 namespace echo {
 
 constexpr int kTileTokens = 128;
@@ -398,26 +414,21 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
       __syncwarp();
       if (lane == 0) *vhead = head;
       const uint32_t cmask = __ballot_sync(0xffffffffu, cand);
+      // tickets: one atomic per request among the candidates; its result is needed
+      // only for the destinations, so the first host loads below start before it returns
+      uint32_t grp = 0;
+      int leader = 0, base = 0;
       if (cand) {
-        const uint32_t grp = __match_any_sync(cmask, b);  // candidates of the same request
-        const int leader = __ffs(grp) - 1;
-        int base = 0;
+        grp = __match_any_sync(cmask, b);  // candidates of the same request
+        leader = __ffs(grp) - 1;
         if (lane == leader) base = atomicAdd(P.stage_count + b, __popc(grp));
-        base = __shfl_sync(grp, base, leader);
-        const int ticket = base + __popc(grp & ((1u << lane) - 1));
-        const int L = clamp_ctx(__ldg(P.ctx_len + b), P.L_max);
-        int cap = (L + P.cap_div - 1) / P.cap_div;
-        cap = cap < P.stage_stride ? cap : P.stage_stride;
-        if (ticket < cap) {
-          dst = b * P.stage_stride + ticket;
-        } else if (ticket == cap) {
-          set_status(P.status, ECHO_DEV_PREFETCH_CAP_HIT);
-        }
       }
-      // ---- copy the staged rows, kPfRowsPerBatch at a time (9 16-byte loads in flight per lane)
-      uint32_t rem = __ballot_sync(0xffffffffu, dst >= 0);
+      // ---- copy the candidate rows, kPfRowsPerBatch at a time (9 16-byte loads in flight
+      // per lane); a row whose ticket is past the cap is read but not stored
+      uint32_t rem = cmask;
+      bool have_tickets = false;
       while (rem) {
-        int32_t hr[kPfRowsPerBatch], dr[kPfRowsPerBatch];
+        int32_t hr[kPfRowsPerBatch], sl[kPfRowsPerBatch], dr[kPfRowsPerBatch];
         int cnt = 0;
 #pragma unroll
         for (int r = 0; r < kPfRowsPerBatch; ++r) {
@@ -427,23 +438,54 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
             rem &= rem - 1;
             ++cnt;
           }
+          sl[r] = src_lane;
           hr[r] = __shfl_sync(0xffffffffu, h, src_lane);
-          dr[r] = __shfl_sync(0xffffffffu, dst, src_lane);
         }
         constexpr int kPer = (kPfRowsPerBatch * kKvChunks + 31) / 32;
         int4 buf[kPer];
+#ifdef ECHO_TRACE
+        const uint64_t tb0 = globaltimer();
+#endif
 #pragma unroll
         for (int m = 0; m < kPer; ++m) {
           const int idx = m * 32 + lane;
           const int r = idx / kKvChunks, c = idx % kKvChunks;
-          if (r < cnt) buf[m] = __ldcs(host + static_cast<size_t>(hr[r]) * kKvChunks + c);
+          if (r < cnt) buf[m] = __ldcs(host + static_cast<size_t>(pick_reg(hr, r)) * kKvChunks + c);
         }
+        if (!have_tickets) {
+          have_tickets = true;
+          if (cand) {
+            base = __shfl_sync(grp, base, leader);
+            const int ticket = base + __popc(grp & ((1u << lane) - 1));
+            const int L = clamp_ctx(__ldg(P.ctx_len + b), P.L_max);
+            int cap = (L + P.cap_div - 1) / P.cap_div;
+            cap = cap < P.stage_stride ? cap : P.stage_stride;
+            if (ticket < cap) {
+              dst = b * P.stage_stride + ticket;
+            } else if (ticket == cap) {
+              set_status(P.status, ECHO_DEV_PREFETCH_CAP_HIT);
+            }
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < kPfRowsPerBatch; ++r) dr[r] = __shfl_sync(0xffffffffu, dst, sl[r]);
 #pragma unroll
         for (int m = 0; m < kPer; ++m) {
           const int idx = m * 32 + lane;
           const int r = idx / kKvChunks, c = idx % kKvChunks;
-          if (r < cnt) stage[static_cast<size_t>(dr[r]) * kKvChunks + c] = buf[m];
+          const int32_t d = pick_reg(dr, r);
+          if (r < cnt && d >= 0) stage[static_cast<size_t>(d) * kKvChunks + c] = buf[m];
         }
+#ifdef ECHO_TRACE
+        __syncwarp();
+        if (lane == 0) {
+          const unsigned long long dt = globaltimer() - tb0;
+          atomicAdd(&g_pf_diag[blockIdx.x][0], static_cast<unsigned long long>(cnt));
+          atomicAdd(&g_pf_diag[blockIdx.x][1], 1ull);
+          atomicMax(&g_pf_diag[blockIdx.x][2], dt);
+          atomicAdd(&g_pf_diag[blockIdx.x][3], dt);
+        }
+#endif
       }
       if (dst >= 0) P.stage_host[dst] = h;
     }
