@@ -69,16 +69,6 @@ __device__ __forceinline__ void warp_find_from_top64(uint32_t need, Cnt cnt, uin
   }
 }
 
-__device__ __forceinline__ uint32_t block_sum(uint32_t v, uint32_t *acc) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  if ((threadIdx.x & 31) == 0 && v) atomicAdd(acc, v);
-  __syncthreads();
-  const uint32_t r = *acc;
-  __syncthreads();
-  return r;
-}
-
 __global__ void __launch_bounds__(kSelThreads, 1)
     topk_kernel(const float *__restrict__ scores, const int32_t *__restrict__ ctx_len, int n_q, int L_max, int k,
                 int chunk, int32_t *__restrict__ sel, float *__restrict__ kth, const ClaimArgs ca, int do_claim,
@@ -93,11 +83,13 @@ __global__ void __launch_bounds__(kSelThreads, 1)
   SelSmem *S = reinterpret_cast<SelSmem *>(smem_raw);
   TopkExtra *X = reinterpret_cast<TopkExtra *>(smem_raw + sizeof(SelSmem));
   uint32_t *keys = reinterpret_cast<uint32_t *>(smem_raw + sizeof(SelSmem) + sizeof(TopkExtra));
+  const uint4 *keys4 = reinterpret_cast<const uint4 *>(keys);
   int32_t *r2s = reinterpret_cast<int32_t *>(keys + chunk);  // staged host rows (stage_r2h)
   uint32_t *list_pos = S->tot, *list_tok = S->tot + kList;   // claim list (tot is free by then)
   ECHO_TRACE_FIRST(24);
 
-  // ---- what does not come from the kernel before: the row's length, its host rows
+  // ---- what does not come from the kernel before: the row's length, its host rows,
+  // the step clock
   int L = __ldg(ctx_len + b);
   L = L < 0 ? 0 : (L > L_max ? L_max : L);
   const int Lr = query_valid_len(L, n_q, j);
@@ -106,6 +98,7 @@ __global__ void __launch_bounds__(kSelThreads, 1)
   const int hi = lo + chunk < Lr ? lo + chunk : Lr;
   const int n_local = hi > lo ? hi - lo : 0;
   const int32_t *r2h = do_claim ? ca.req_to_host + static_cast<size_t>(b) * L_max + lo : nullptr;
+  const int32_t clock = do_claim ? (ca.clock_dev ? *ca.clock_dev : ca.clock) : 0;
   if (stage_r2h)
     for (int i = threadIdx.x; i < n_local; i += kSelThreads) r2s[i] = __ldg(r2h + i);
   for (int i = threadIdx.x; i < kCoarseBins; i += kSelThreads) X->ctot[i] = 0;
@@ -145,6 +138,11 @@ __global__ void __launch_bounds__(kSelThreads, 1)
       mx = max(mx, a);
     }
   }
+  // this thread's segment of the slice: [s0, s1), read as 16-byte vectors
+  int seg = (n_local + kSelThreads - 1) / kSelThreads;
+  seg = (seg + 3) & ~3;
+  const int s0 = threadIdx.x * seg < n_local ? threadIdx.x * seg : n_local;
+  const int s1 = s0 + seg < n_local ? s0 + seg : n_local;
   __syncthreads();
   ECHO_TRACE_MARK(1);
 
@@ -162,10 +160,21 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     const int shift = hb - width;
     const int nb = 1 << width;
     const int nco = (nb + kCoarse - 1) / kCoarse;
-    sel_histogram(S, n_local, 32, shift, nb, 0u, [&](int i, uint32_t &x) {
-      x = keys[i] - kmin;
-      return true;
-    });
+    // fine histogram of the digit (key - kmin) >> shift, one shared-memory atomic per key
+    for (int i = threadIdx.x; i < nb; i += kSelThreads) S->hist[i] = 0;
+    __syncthreads();
+    if (nb == 1) {
+      if (threadIdx.x == 0) S->hist[0] = static_cast<uint32_t>(n_local);
+    } else {
+      for (int i = s0; i < s1; i += 4) {
+        const uint4 v = keys4[i >> 2];
+        atomicAdd(&S->hist[(v.x - kmin) >> shift], 1u);
+        if (i + 1 < s1) atomicAdd(&S->hist[(v.y - kmin) >> shift], 1u);
+        if (i + 2 < s1) atomicAdd(&S->hist[(v.z - kmin) >> shift], 1u);
+        if (i + 3 < s1) atomicAdd(&S->hist[(v.w - kmin) >> shift], 1u);
+      }
+    }
+    __syncthreads();
     // coarse histogram: one warp per coarse bin
     for (int cb = warp; cb < nco; cb += kSelWarps) {
       uint32_t c = 0;
@@ -198,36 +207,47 @@ __global__ void __launch_bounds__(kSelThreads, 1)
       }
     }
     __syncthreads();
-    if (warp == 0)
+    if (warp == 0) {
       warp_find_from_top64(static_cast<uint32_t>(target) - above_D, [&](int i) { return X->ftot[i]; }, &X->v[2]);
+      __syncwarp();
+      // this CTA's keys above bin d: coarse bins above D, then D's fine bins above d
+      const uint32_t dd = D * kCoarse + X->v[2];
+      uint32_t a = 0;
+      for (int cb = static_cast<int>(D) + 1 + lane; cb < nco; cb += 32) a += X->coarse[cb];
+      for (int i = lane; i < kCoarse; i += 32) {
+        const uint32_t fb = D * kCoarse + i;
+        if (fb > dd && fb < static_cast<uint32_t>(nb)) a += S->hist[fb];
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+      if (lane == 0) {
+        X->above = a;
+        X->cand_n = S->hist[dd];
+      }
+    }
     __syncthreads();
     const uint32_t d = D * kCoarse + X->v[2];
     const uint32_t above_d = above_D + X->v[3];
     const uint32_t cnt_d = X->ftot[X->v[2]];
     const uint32_t need_d = static_cast<uint32_t>(target) - above_d;
-    // this CTA's keys above bin d, and in it
-    uint32_t mine = 0;
-    for (int i = threadIdx.x; i < nb; i += kSelThreads)
-      if (static_cast<uint32_t>(i) > d) mine += S->hist[i];
-    const uint32_t mine_above = block_sum(mine, &X->v[4]);
-    const uint32_t in_d = S->hist[d];
     ECHO_TRACE_MARK(4);
     if (cnt_d <= static_cast<uint32_t>(kCand)) {
-      // collect the bin's keys from the whole cluster; every CTA resolves T itself
-      for (int base = (threadIdx.x & ~31); base < n_local; base += kSelThreads) {
-        const int i = base + lane;
-        const uint32_t key = i < n_local ? keys[i] : 0u;
-        const bool cand = i < n_local && ((key - kmin) >> shift) == d;
-        const uint32_t m = __ballot_sync(0xffffffffu, cand);
-        if (!m) continue;
-        uint32_t slot = 0;
-        if (lane == __ffs(m) - 1) slot = atomicAdd(&X->v[5], static_cast<uint32_t>(__popc(m)));
-        slot = __shfl_sync(0xffffffffu, slot, __ffs(m) - 1);
-        if (cand) X->cand_key[slot + __popc(m & ((1u << lane) - 1))] = key;
-      }
-      if (threadIdx.x == 0) {
-        X->cand_n = in_d;
-        X->above = mine_above;
+      // publish this CTA's keys of bin d; every CTA collects the cluster's and resolves T
+      {
+        uint32_t c = 0;
+        for (int i = s0; i < s1; i += 4) {
+          const uint4 v = keys4[i >> 2];
+          const uint32_t kv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) c += (i + u < s1 && ((kv[u] - kmin) >> shift) == d);
+        }
+        if (c) {  // rare: a second pass over the segment writes them
+          const uint32_t slot = atomicAdd(&X->v[5], c);
+          for (int i = s0, q = 0; i < s1 && q < static_cast<int>(c); ++i) {
+            const uint32_t key = keys[i];
+            if (((key - kmin) >> shift) == d) X->cand_key[slot + q++] = key;
+          }
+        }
       }
       cl.sync();  // every CTA's candidates published
       if (warp == 0) {
@@ -270,25 +290,28 @@ __global__ void __launch_bounds__(kSelThreads, 1)
       __syncthreads();
       T = X->v[7];
       needT = X->v[8];
-      // keys of lower CTAs' candidates above / equal to T
+      // lower CTAs' candidates above / equal to T (one warp-wide count per 32 candidates)
       const int n_lower = static_cast<int>(X->off[rank]);
-      uint32_t g = 0, e = 0;
-      for (int i = threadIdx.x; i < n_lower; i += kSelThreads) {
-        const uint32_t ki = X->all_key[i];
-        g += ki > T;
-        e += ki == T;
+      for (int base = warp * 32; base < n_lower; base += kSelThreads) {
+        const int i = base + lane;
+        const uint32_t ki = i < n_lower ? X->all_key[i] : 0u;
+        const uint32_t gm = __ballot_sync(0xffffffffu, i < n_lower && ki > T);
+        const uint32_t em = __ballot_sync(0xffffffffu, i < n_lower && ki == T);
+        if (lane == 0) {
+          if (gm) atomicAdd(&X->v[9], static_cast<uint32_t>(__popc(gm)));
+          if (em) atomicAdd(&X->v[10], static_cast<uint32_t>(__popc(em)));
+        }
       }
-      g = block_sum(g, &X->v[9]);
-      e = block_sum(e, &X->v[10]);
-      pg = X->v[6] + g;
-      pe = e;
+      __syncthreads();
+      pg = X->v[6] + X->v[9];
+      pe = X->v[10];
       offsets_known = true;
     } else if (shift == 0) {
       // every key of bin d equals T: counts of the histogram are exact
       T = kmin + d;
       needT = need_d;
       uint32_t ga, gb;
-      sel_cluster_prefix2(cl, S, mine_above, in_d, pg, pe, ga, gb);
+      sel_cluster_prefix2(cl, S, X->above, S->hist[d], pg, pe, ga, gb);
       offsets_known = true;
     } else {
       // many keys share the threshold bin (ties or a clustered row): exact radix passes
@@ -304,17 +327,18 @@ __global__ void __launch_bounds__(kSelThreads, 1)
   ECHO_TRACE_MARK(5);
 
   // ---- ascending output: selected iff key > T, or key == T among the first needT
-  // equal keys; per-thread segments (odd length: conflict-free shared-memory reads)
-  int seg = (n_local + kSelThreads - 1) / kSelThreads;
-  seg |= 1;
-  const int s0 = threadIdx.x * seg < n_local ? threadIdx.x * seg : n_local;
-  const int s1 = s0 + seg < n_local ? s0 + seg : n_local;
+  // equal keys; each thread's segment is contiguous, so a block scan orders them
   uint32_t g = 0, e = 0;
   if (target > 0)
-    for (int i = s0; i < s1; ++i) {
-      const uint32_t key = keys[i];
-      g += key > T;
-      e += key == T;
+    for (int i = s0; i < s1; i += 4) {
+      const uint4 v = keys4[i >> 2];
+      const uint32_t kv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (i + u < s1) {
+          g += kv[u] > T;
+          e += kv[u] == T;
+        }
     }
   uint32_t eg, ee, tg, te;
   sel_block_scan2(g, e, eg, ee, tg, te, S);
@@ -324,36 +348,42 @@ __global__ void __launch_bounds__(kSelThreads, 1)
   }
   ECHO_TRACE_MARK(6);
   // the recall's claim of every selected entry (decode step): see cache_common.cuh
-  const int32_t clock = do_claim ? (ca.clock_dev ? *ca.clock_dev : ca.clock) : 0;
   const int f_row = row * k;
   const uint32_t mpe = pe < needT ? pe : needT;
   const uint32_t te_taken = (pe + te < needT ? pe + te : needT) - mpe;
   const uint32_t n_sel = target > 0 ? tg + te_taken : 0u;
   const bool use_list = do_claim && n_sel <= static_cast<uint32_t>(kList);
-  if (target > 0) {
+  if (target > 0 && (g | e)) {
     uint32_t gb = pg + eg, eb = pe + ee;
-    for (int i = s0; i < s1; ++i) {
-      const uint32_t key = keys[i];
-      int pos = -1;
-      uint32_t li = 0;
-      if (key > T) {
-        li = (gb - pg) + ((eb < needT ? eb : needT) - mpe);
-        pos = static_cast<int>(gb + (eb < needT ? eb : needT));
-        ++gb;
-      } else if (key == T) {
-        if (eb < needT) {
-          li = (gb - pg) + (eb - mpe);
-          pos = static_cast<int>(gb + eb);
+    for (int i0 = s0; i0 < s1; i0 += 4) {
+      const uint4 v = keys4[i0 >> 2];
+      const uint32_t kv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u;
+        if (i >= s1) break;
+        const uint32_t key = kv[u];
+        int pos = -1;
+        uint32_t li = 0;
+        if (key > T) {
+          li = (gb - pg) + ((eb < needT ? eb : needT) - mpe);
+          pos = static_cast<int>(gb + (eb < needT ? eb : needT));
+          ++gb;
+        } else if (key == T) {
+          if (eb < needT) {
+            li = (gb - pg) + (eb - mpe);
+            pos = static_cast<int>(gb + eb);
+          }
+          ++eb;
         }
-        ++eb;
-      }
-      if (pos < 0) continue;
-      out[pos] = lo + i;
-      if (use_list) {
-        list_pos[li] = static_cast<uint32_t>(pos);
-        list_tok[li] = static_cast<uint32_t>(i);
-      } else if (do_claim) {
-        claim_entry(ca.pool, ca.ws, f_row + pos, __ldg(r2h + i), clock, ca.status);
+        if (pos < 0) continue;
+        out[pos] = lo + i;
+        if (use_list) {
+          list_pos[li] = static_cast<uint32_t>(pos);
+          list_tok[li] = static_cast<uint32_t>(i);
+        } else if (do_claim) {
+          claim_entry(ca.pool, ca.ws, f_row + pos, __ldg(r2h + i), clock, ca.status);
+        }
       }
     }
   }
