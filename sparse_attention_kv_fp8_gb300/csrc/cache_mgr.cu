@@ -26,15 +26,16 @@
 //       CTA finds the same threshold T (the E-th oldest priority, refined while the
 //       open bin holds it); owned misses listed in entry order with their sources;
 //       per-CTA counts of slots older than / at T and free.
-//   P4  each warp starts reading the KV rows of its first misses; prefix sums over
-//       the per-CTA counts give each slot its eviction and free-slot rank: victims
-//       are scattered (free = 1, priority = -1, maps to INF), the r-th free slot is
-//       recorded for miss r.  This is the page's ticket order taken in slot order,
-//       so the result is deterministic.
-//   P5  the r-th miss takes the r-th free slot (maps, priority = clock, indices
-//       buffer, out_slot) and its row, already in registers, is stored (16-byte
-//       vectors, 4 rows per warp, from the staging area or the pinned host pool);
-//       repeats of a miss take its slot.
+//   P4  evictions and allocations together: prefix sums over the per-CTA counts
+//       rank every free slot and every victim (slot order); the r-th of them takes
+//       miss r.  The CTA that owns a slot writes all of it: the evicted row's map,
+//       the new row's maps, priority = clock, indices-buffer entry, out_slot and the
+//       KV row (16-byte vectors, 4 rows per warp, from the staging area or the
+//       pinned host pool, read before the ranking so the host reads overlap it).
+//       Every victim is taken (E never exceeds M - free), so no two CTAs write one
+//       slot.  This is the page's ticket order taken in slot order: deterministic.
+//   P5  only when a row was selected by several entries: after one more barrier,
+//       the repeats take the slot of the row's first entry.
 #include "cache_common.cuh"
 
 ECHO_TRACE_UNIT(cache_mgr)
@@ -320,6 +321,8 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
   int32_t *host_cache = slot_cache ? dyn_smem + P.slot_cache_cap : nullptr;  // GPUTokenToHost of the slots
   int32_t *aux_cache = (e_hi - e_lo) <= P.ent_cache_cap ? dyn_smem + 2 * P.slot_cache_cap : nullptr;
   int32_t *h_cache = aux_cache ? aux_cache + P.ent_cache_cap : nullptr;     // host row of the entries
+  // slots this CTA's phase P4 hands to misses, by rank (same capacity as the slot cache)
+  int32_t *take_cache = slot_cache ? dyn_smem + 2 * P.slot_cache_cap + 2 * P.ent_cache_cap : nullptr;
   auto slot_val = [&](int s) -> int32_t {
     if (slot_cache) return slot_cache[s - s_lo];
     return P.pool.free_[s] ? kFreeMark : P.pool.prio[s];
@@ -393,7 +396,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     if (P.mode != kModeEvict) {
       constexpr int kT = kEntWarps * 32, kU = 2;
       const int t = static_cast<int>(threadIdx.x) - kSlotWarps * 32;
-      uint32_t own = 0, hits = 0, valid = 0;
+      uint32_t own = 0, hits = 0, valid = 0, reps = 0;
       for (int f0 = e_lo + t; f0 < e_hi; f0 += kT * kU) {
         int32_t h[kU], v[kU], sc[kU];
 #pragma unroll
@@ -425,6 +428,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
             } else if (v[u] < 0) {  // a repeat of a row an earlier entry claimed
               if (P.mode == kModeRecall) {
                 aux = -3 - static_cast<int32_t>(static_cast<uint32_t>(v[u]) - 0x80000000u);
+                ++reps;
               } else {
                 if (P.mode == kModeAlloc) P.out_slots[f] = -1;
                 set_status(P.status, ECHO_DEV_BAD_INDEX);
@@ -444,11 +448,13 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
         own += __shfl_xor_sync(0xffffffffu, own, o);
         hits += __shfl_xor_sync(0xffffffffu, hits, o);
         valid += __shfl_xor_sync(0xffffffffu, valid, o);
+        reps += __shfl_xor_sync(0xffffffffu, reps, o);
       }
       if (lane == 0) {
         if (own) atomicAdd(&S->red[0], own);
         if (hits) atomicAdd(&S->red[1], hits);
         if (valid) atomicAdd(&S->red[2], valid);
+        if (reps) atomicAdd(&S->red[3], reps);
       }
     }
   } else if (P.mode == kModeRecall && P.stage_count != nullptr) {
@@ -481,6 +487,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     P.ws.cta[c * kCVals + kCOwn] = S->red[0];
     if (S->red[1]) atomicAdd(glob + kGHits, S->red[1]);
     if (S->red[2]) atomicAdd(glob + kGValid, S->red[2]);
+    if (S->red[3]) atomicAdd(glob + kGRepeats, S->red[3]);
   }
   ECHO_TRACE_MARK(3);
   if (!grid_barrier(glob, P.status, S)) return;
@@ -510,6 +517,8 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     glob[kGValid] = 0;
     glob[kGHits] = 0;
   }
+  // repeats of a missed row exist: their out_slot needs one more grid barrier
+  const bool any_repeats = P.mode == kModeRecall && __ldcg(glob + kGRepeats) != 0;
   // this thread's segment of the entries; the staging rows of its owned misses
   const int e_cnt = e_hi - e_lo;
   const int e_per = (e_cnt + kCoopThreads - 1) / kCoopThreads;
@@ -594,6 +603,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     Tp = clock - 1 - static_cast<int32_t>(age_t);
     needT = need;
   }
+  uint32_t my_lt = 0, my_eq = 0, my_fr = 0;  // this CTA's slots older than / at T, free
   // owned misses, in entry order (contiguous per-thread segments), with their sources
   if (P.mode != kModeEvict) {
     uint32_t own = 0;
@@ -633,6 +643,9 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     }
     uint32_t v3[3] = {lt, eq, fr}, ex3[3], tot3[3];
     coop_scan<3>(v3, ex3, tot3, S);
+    my_lt = tot3[0];
+    my_eq = tot3[1];
+    my_fr = tot3[2];
     if (threadIdx.x == 0) {
       P.ws.cta[c * kCVals + kCLt] = tot3[0];
       P.ws.cta[c * kCVals + kCEq] = tot3[1];
@@ -643,18 +656,10 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
   if (!grid_barrier(glob, P.status, S)) return;
   ECHO_TRACE_MARK(6);
 
-  // ===== P4: victims evicted; free-slot list.  Each warp first loads its first KV
-  // rows (misses gw * kRows ...), so that the host reads overlap this phase =====
-  const int gw = gtid >> 5, nw = gthreads >> 5;
-  int4 buf[kRowVecs];
-  int32_t my_f = -1, my_h = -1, my_src = -1;  // lane u < kRows: row gw * kRows + u
-  const int my_r0 = gw * kRows;
-  const int my_nr = M > static_cast<uint32_t>(my_r0) ? min(kRows, static_cast<int>(M) - my_r0) : 0;
-  if (lane < my_nr) {
-    my_f = P.ws.miss_f[my_r0 + lane];
-    my_h = P.ws.miss_h[my_r0 + lane];
-    my_src = P.ws.miss_src[my_r0 + lane];
-  }
+  // ===== P4: evictions and allocations together.  Free slots and victims, in slot
+  // order, form the list of slots to take; the r-th of them takes miss r, and the CTA
+  // that owns the slot writes everything about it: the evicted row's map, the new
+  // row's maps, priority, indices-buffer entry, out_slot and KV bytes =====
   uint32_t pre_lt = 0, pre_eq = 0, pre_fr = 0, free_total = 0;
   {
     uint32_t a3[3] = {0, 0, 0}, t1 = 0;
@@ -675,6 +680,23 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     pre_fr = tot4[2];
     free_total = tot4[3];
   }
+  const int32_t A = (P.mode == kModeEvict) ? 0 : static_cast<int32_t>(min(M, free_total + static_cast<uint32_t>(E)));
+  // this CTA's slots to take have ranks [a_lo, a_lo + n_mine); those below A get a miss
+  const uint32_t a_lo = pre_fr + pre_lt + min(pre_eq, needT);
+  const uint32_t n_mine = my_fr + my_lt + (min(pre_eq + my_eq, needT) - min(pre_eq, needT));
+  const int n_take = static_cast<int>(min(a_lo + n_mine, static_cast<uint32_t>(A)) - min(a_lo, static_cast<uint32_t>(A)));
+  // each warp's first four misses: entry, host row, source, and the KV rows themselves,
+  // loaded now so that the host reads overlap the ranking below
+  int4 buf[kRowVecs];
+  int32_t my_f = -1, my_h = -1, my_src = -1;  // lane u < kRows: rank a_lo + warp * kRows + u
+  const int my_t0 = warp * kRows;
+  const int my_nr = n_take > my_t0 ? min(kRows, n_take - my_t0) : 0;
+  if (lane < my_nr) {
+    const int r = static_cast<int>(a_lo) + my_t0 + lane;
+    my_f = P.ws.miss_f[r];
+    my_h = P.ws.miss_h[r];
+    my_src = P.ws.miss_src[r];
+  }
   if (copies && my_nr > 0) {
     const int4 *src[kRows];
 #pragma unroll
@@ -685,7 +707,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     }
     rows_load(src, my_nr, buf);
   }
-  const int32_t A = (P.mode == kModeEvict) ? 0 : static_cast<int32_t>(min(M, free_total + static_cast<uint32_t>(E)));
+  // rank this CTA's slots (contiguous per-thread segments); victims lose their maps
   {
     const int cnt = s_hi - s_lo;
     const int per = (cnt + kCoopThreads - 1) / kCoopThreads;
@@ -707,11 +729,14 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     for (int s = q0; s < q1; ++s) {
       const int32_t v = slot_val(s);
       // victims before s (all evictable slots older than T, the first needT at T), and
-      // the slots before s that are free after the eviction (free ones and victims)
+      // the slots to take before s (free ones and victims)
       const uint32_t vb = lt_b + min(eq_b, needT);
       const uint32_t before = fr_b + vb;
       if (v == kFreeMark) {
-        if (before < static_cast<uint32_t>(A)) P.ws.alloc_slot[before] = s;
+        if (before < static_cast<uint32_t>(A)) {
+          P.ws.alloc_slot[before] = s;
+          if (take_cache) take_cache[before - a_lo] = s;
+        }
         ++fr_b;
         continue;
       }
@@ -726,54 +751,49 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
       }
       if (!victim) continue;
       const int32_t h = host_cache ? host_cache[s - s_lo] : P.pool.to_host[s];
-      P.pool.free_[s] = 1;
-      P.pool.prio[s] = -1;
       if (h >= 0 && h < P.pool.n_h) P.pool.h2g[h] = kInf;
-      P.pool.to_host[s] = kInf;
       if (P.mode == kModeEvict) P.pool.idxbuf[vb] = s;  // evicted slots in ascending order
-      if (before < static_cast<uint32_t>(A)) P.ws.alloc_slot[before] = s;
+      if (before < static_cast<uint32_t>(A)) {
+        P.ws.alloc_slot[before] = s;
+        if (take_cache) take_cache[before - a_lo] = s;
+      } else {  // nobody takes it: free
+        P.pool.free_[s] = 1;
+        P.pool.prio[s] = -1;
+        P.pool.to_host[s] = kInf;
+      }
     }
   }
+  __syncthreads();  // this CTA's slot table complete
   ECHO_TRACE_MARK(7);
-  if (!grid_barrier(glob, P.status, S)) return;
-  ECHO_TRACE_MARK(8);
-
-  // ===== P5: the r-th miss takes the r-th free slot (maps, priority, indices buffer,
-  // out_slot, bytes); then the repeats of misses take their first entry's slot =====
+  // the misses this CTA's slots take: four per warp (the first four already loaded)
   unsigned long long used = 0;
-  for (int r0 = gw * kRows; r0 < static_cast<int>(M); r0 += nw * kRows) {
-    const int nr = min(kRows, static_cast<int>(M) - r0);
-    const bool first = r0 == gw * kRows;  // rows loaded in P4
+  for (int t0 = my_t0; t0 < n_take; t0 += kCoopWarps * kRows) {
+    const int nr = min(kRows, n_take - t0);
+    const bool first = t0 == my_t0;
     int32_t f = -1, h = -1, st = -1, s = -1;
     if (lane < nr) {
+      const int r = static_cast<int>(a_lo) + t0 + lane;
       if (first) {
         f = my_f;
         h = my_h;
         st = my_src;
       } else {
-        f = P.ws.miss_f[r0 + lane];
-        h = P.ws.miss_h[r0 + lane];
-        st = P.ws.miss_src[r0 + lane];
+        f = P.ws.miss_f[r];
+        h = P.ws.miss_h[r];
+        st = P.ws.miss_src[r];
       }
-      const int r = r0 + lane;
-      if (r < A) {
-        s = P.ws.alloc_slot[r];
-        P.pool.free_[s] = 0;
-        P.pool.prio[s] = clock;
-        P.pool.to_host[s] = h;
-        P.pool.h2g[h] = s;
-        P.pool.idxbuf[r] = s;
-        if (P.mode == kModeAlloc) P.out_slots[f] = s;
-        if (P.mode == kModeRecall) {
-          P.out_slot[f] = s;
-          used += st >= 0;
-        }
-      } else {  // no slot left: the row stays out of the pool
-        P.pool.h2g[h] = kInf;
-        if (P.mode == kModeRecall) P.out_slot[f] = -1;
-        if (P.mode == kModeAlloc) P.out_slots[f] = -1;
+      s = take_cache ? take_cache[t0 + lane] : __ldcg(P.ws.alloc_slot + r);
+      P.pool.free_[s] = 0;
+      P.pool.prio[s] = clock;
+      P.pool.to_host[s] = h;
+      P.pool.h2g[h] = s;
+      P.pool.idxbuf[r] = s;
+      if (P.mode == kModeAlloc) P.out_slots[f] = s;
+      if (P.mode == kModeRecall) {
+        P.out_slot[f] = s;
+        P.ws.miss_stage[f] = -1;  // staging lookup back to its resting state
+        used += st >= 0;
       }
-      if (P.mode == kModeRecall) P.ws.miss_stage[f] = -1;  // staging lookup back to its resting state
     }
     if (copies) {
       int32_t slot[kRows];
@@ -786,18 +806,30 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
         src[u] = u < nr ? row_source(P, fu, hu, su) : nullptr;
       }
       if (!first) rows_load(src, nr, buf);
-      // rows r0 .. r0 + n_keep - 1 were granted a slot
-      const int n_keep = A - r0 < nr ? (A - r0 > 0 ? A - r0 : 0) : nr;
-      rows_store(reinterpret_cast<int4 *>(P.pool.gpu_kv), slot, n_keep, buf);
+      rows_store(reinterpret_cast<int4 *>(P.pool.gpu_kv), slot, nr, buf);
     }
   }
-  if (P.mode == kModeRecall) {
+  // misses beyond the pool's capacity stay out of it
+  for (int r = A + gtid; r < static_cast<int>(M); r += gthreads) {
+    const int32_t f = P.ws.miss_f[r], h = P.ws.miss_h[r];
+    P.pool.h2g[h] = kInf;
+    if (P.mode == kModeRecall) {
+      P.out_slot[f] = -1;
+      P.ws.miss_stage[f] = -1;
+    }
+    if (P.mode == kModeAlloc) P.out_slots[f] = -1;
+  }
+  ECHO_TRACE_MARK(8);
+  if (any_repeats) {
+    // repeats of a missed row take the slot of the row's first entry
+    if (!grid_barrier(glob, P.status, S)) return;
     for (int f = e_lo + static_cast<int>(threadIdx.x); f < e_hi; f += kCoopThreads) {
       const int32_t aux = aux_of(f);
       if (aux > -3) continue;
       const int32_t r1 = P.ws.miss_rank[-3 - aux];
-      P.out_slot[f] = r1 < A ? P.ws.alloc_slot[r1] : -1;
+      P.out_slot[f] = r1 < A ? __ldcg(P.ws.alloc_slot + r1) : -1;
     }
+    if (c == 0 && threadIdx.x == 0) glob[kGRepeats] = 0;  // every CTA read it before the barrier
   }
   if (static_cast<int32_t>(M) > A && c == 0 && threadIdx.x == 0) set_status(P.status, ECHO_DEV_POOL_EXHAUSTED);
   const int32_t list_len = P.mode == kModeEvict ? E : A;
@@ -998,7 +1030,7 @@ static echo::OpParams base_params(const echo_pool *pool, const echo_workspace *w
 
 // one cooperative launch over all SMs (one CTA each); `pdl`: programmatic launch
 // after the kernel before it on the stream
-constexpr int kSlotCacheMax = 16384;  // slots per CTA whose states P2 keeps in shared memory
+constexpr int kSlotCacheMax = 12288;  // slots per CTA whose states P2 keeps in shared memory
 constexpr int kEntCacheMax = 4096;    // entries per CTA whose classification P2 keeps
 
 static int run_op(const echo::OpParams &P0, cudaStream_t s, bool pdl = false) {
@@ -1011,14 +1043,14 @@ static int run_op(const echo::OpParams &P0, cudaStream_t s, bool pdl = false) {
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(echo::cache_op_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         2 * (kSlotCacheMax + kEntCacheMax) * static_cast<int>(sizeof(int32_t)));
+                                         (3 * kSlotCacheMax + 2 * kEntCacheMax) * static_cast<int>(sizeof(int32_t)));
     if (e != cudaSuccess) return cuda_fail(e, "cache-manager smem attribute");
     attr = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(echo::kCoopThreads);
-  cfg.dynamicSmemBytes = static_cast<size_t>(2 * P.slot_cache_cap + 2 * P.ent_cache_cap) * sizeof(int32_t);
+  cfg.dynamicSmemBytes = static_cast<size_t>(3 * P.slot_cache_cap + 2 * P.ent_cache_cap) * sizeof(int32_t);
   cfg.stream = s;
   cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeCooperative;
