@@ -291,8 +291,10 @@ int echo_ema_update(float *s_hat, const float *kth, int32_t n, float alpha, void
  * the kernels read the clock there and, if advance_clock != 0, the recall advances
  * it by one, so one captured graph can be replayed step after step.  All arguments
  * are checked before the first launch: a rejected step enqueues nothing.
- * Launches: 4 kernels (indexer, top-k, recall plan, recall copy), plus 3 for the
- * append.  stage_events: optional array of
+ * Launches: 3 kernels (indexer; top-k, which also makes the recall's claims; the
+ * cooperative cache-manager kernel, which also updates the EMA), the last two as
+ * programmatic dependent launches; plus 2 for the append (write-through kernel,
+ * cache-manager kernel).  stage_events: optional array of
  * ECHO_NUM_STAGES + 1 cudaEvent_t (timing-enabled) recorded around the stages
  * (as external event nodes under capture).
  */
