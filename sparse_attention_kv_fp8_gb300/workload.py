@@ -41,7 +41,7 @@ def rng(seed: int, stream: int) -> np.random.Generator:
 # storage encodings (input formats, not the method)
 # ---------------------------------------------------------------------------
 
-def e4m3_encode(x: np.ndarray) -> np.ndarray:
+def e4m3_encode_direct(x: np.ndarray) -> np.ndarray:
     """Round to the nearest e4m3fn code (1 sign, 4 exponent bits with bias 7, 3 mantissa
     bits; subnormal step 2^-9; largest finite 448), ties to even, saturating at +-448.
     The input is first rounded to float32 (the draws are float32 or float64)."""
@@ -57,6 +57,29 @@ def e4m3_encode(x: np.ndarray) -> np.ndarray:
     code = np.where(sub, np.rint(a * np.float32(512.0)).astype(np.int32), code)
     sign = np.where(np.signbit(xf), 0x80, 0)
     return (code | sign).astype(np.uint8)
+
+
+_E4M3_TABLE = None
+
+
+def _e4m3_table() -> np.ndarray:
+    """The code of every float32 class (top 16 bits, whether any of the low 16 bits is
+    set), from the direct encoder.  The rounding decision reads the round bit (bit 19
+    or higher) and whether any lower bit is set, so the class decides the code."""
+    global _E4M3_TABLE
+    if _E4M3_TABLE is None:
+        hi = np.arange(1 << 16, dtype=np.uint32) << np.uint32(16)
+        reps = np.stack([hi, hi | np.uint32(1)], axis=1).reshape(-1)
+        with np.errstate(invalid="ignore"):
+            _E4M3_TABLE = e4m3_encode_direct(reps.view(np.float32))
+    return _E4M3_TABLE
+
+
+def e4m3_encode(x: np.ndarray) -> np.ndarray:
+    """e4m3_encode_direct through a 128K-entry table (same codes for finite inputs)."""
+    u = np.ascontiguousarray(np.asarray(x, dtype=np.float32)).view(np.uint32)
+    idx = ((u >> np.uint32(16)) << np.uint32(1)) | ((u & np.uint32(0xFFFF)) != 0).astype(np.uint32)
+    return _e4m3_table()[idx]
 
 
 def bf16_encode(x: np.ndarray) -> np.ndarray:

@@ -79,6 +79,22 @@ def test_generator_e4m3_encoding_matches_torch():
                         [0.0, -0.0, 448.0, 449.0, -1000.0, 2.0 ** -10, 3 * 2.0 ** -10]]).astype(np.float32)
     ref = torch.from_numpy(x).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     assert np.array_equal(wl.e4m3_encode(x), ref)
+    assert np.array_equal(wl.e4m3_encode_direct(x), ref)
+
+
+def test_generator_table_encoder_equals_torch_on_random_bit_patterns():
+    """The table-driven encoder against torch on random finite float32 bit patterns,
+    every rounding tie between e4m3 codes, and one ulp either side of each tie."""
+    g = np.random.default_rng(8)
+    u = g.integers(0, 1 << 32, size=200000, dtype=np.uint64).astype(np.uint32)
+    x = u.view(np.float32)
+    x = x[np.isfinite(x)]
+    mids = (torch_e4m3_to_f64(np.arange(0, 126, dtype=np.uint8)) + torch_e4m3_to_f64(np.arange(1, 127, dtype=np.uint8))) / 2
+    mids = mids.astype(np.float32)
+    near = np.concatenate([mids, np.nextafter(mids, np.float32(0)), np.nextafter(mids, np.float32(1000))])
+    x = np.concatenate([x, near, -near]).astype(np.float32)
+    ref = torch.from_numpy(x).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(wl.e4m3_encode(x), ref)
 
 
 # ---------------------------------------------------------------------------
