@@ -516,6 +516,16 @@ int orc_append(orc_pool *P, uint8_t *k_index, int32_t *ctx_len, const int32_t *r
                sizeof(uint16_t) * (size_t)P->row_elems);
         memcpy(k_index + ((size_t)b * L_max + p) * D, new_k_index + (size_t)b * D, (size_t)D);
         ctx_len[b] = p + 1;
+        /* A new token's row has no GPU copy yet.  One that is already resident, or that
+           an earlier request of this call appends too, is written through but takes no
+           slot and frees none (flagged). */
+        int repeat = 0;
+        for (int i = 0; i < n; ++i)
+            repeat |= rows[i] == h;
+        if (P->HostTokenToGPU[h] != ORC_INF || repeat) {
+            status |= ORC_BAD_INDEX;
+            continue;
+        }
         rows[n] = h;
         src[n] = b;
         ++n;

@@ -22,6 +22,7 @@
 // The kernel is HBM-bound: 128 + 4*n_q bytes per token against 2*64*128*n_q
 // FLOP, far below the FP8 ridge point.
 #include <cstdio>
+#include <cstring>
 
 #include "echo_common.cuh"
 
@@ -55,6 +56,11 @@ constexpr int kIndexerThreads = 32 * (2 + kEpiWarps + kPfWarps);
 constexpr int kAcc = 4;            // TMEM accumulators (MMA runs up to 3 tiles ahead of the epilogue)
 constexpr int kQueueCap = 64;      // entries per epilogue -> prefetch queue
 constexpr int kPfRowsPerBatch = 4; // rows one prefetch warp keeps in flight
+// host rows of the tiles (req_to_host slices, 128 x int32) staged by TMA for the
+// epilogue: a ring the producer may refill only after the epilogue read the tile
+// kR tiles back, which the k^I ring and the TMEM accumulators already guarantee
+constexpr int kR = kStages + kAcc;
+constexpr int kRowMapBytes = kTileTokens * 4;
 
 struct IndexerParams {
   const float *w;
@@ -73,6 +79,7 @@ struct IndexerParams {
   int32_t stage_stride;
   int32_t cap_div;
   int32_t *status;
+  int32_t r2h_tma;  // the tiles' host rows come by TMA (needs L_max % 4 == 0)
 };
 
 struct alignas(16) IndexerCtl {
@@ -83,13 +90,15 @@ struct alignas(16) IndexerCtl {
   uint64_t q_full[2];
   uint64_t q_empty[2];
   uint64_t drain;
+  uint64_t r2h_full[kR];
   uint32_t tmem_base;
   int abort;
   int first_b, first_t, n_tiles;
   int queue_tail[kEpiWarps];
   int queue_head[kEpiWarps];
   int queue_done[kEpiWarps];
-  int queue[kEpiWarps][kQueueCap];  // token ids b * L_max + p that passed the threshold
+  int queue[kEpiWarps][kQueueCap];    // token ids b * L_max + p that passed the threshold
+  int queue_h[kEpiWarps][kQueueCap];  // their host rows (when the tiles' host rows are staged)
   float4 wsm[kEpiWarps][2 * kHeads / 4];  // head weights of the current request, per epilogue warp
 };
 
@@ -115,8 +124,8 @@ __device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
 
 template <int NQ>
 __global__ void __launch_bounds__(kIndexerThreads, 1)
-    indexer_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                   const __grid_constant__ CUtensorMap tmap_q, const IndexerParams P) {
+    indexer_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
+                   const __grid_constant__ CUtensorMap tmap_r, const IndexerParams P) {
   constexpr int N = kHeads * NQ;               // MMA N: all heads of all queries
   constexpr uint32_t kQBytes = N * kDim;       // q of one request
   constexpr uint32_t kTmemCols = kAcc * N;     // 256 (NQ = 1) or 512 (NQ = 2) columns
@@ -126,7 +135,8 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *k_smem = smem;                                  // kStages x 16 KB
   uint8_t *q_smem = smem + kStages * kTileBytes;           // 2 x kQBytes
-  IndexerCtl *ctl = reinterpret_cast<IndexerCtl *>(q_smem + 2 * kQBytes);
+  int32_t *r_smem = reinterpret_cast<int32_t *>(q_smem + 2 * kQBytes);  // kR x 128 host rows
+  IndexerCtl *ctl = reinterpret_cast<IndexerCtl *>(q_smem + 2 * kQBytes + kR * kRowMapBytes);
   volatile int *abort = &ctl->abort;
 
   const int warp = threadIdx.x >> 5;
@@ -169,6 +179,7 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
       mbar_init(&ctl->q_empty[i], 1);
     }
     mbar_init(&ctl->drain, 1);
+    for (int i = 0; i < kR; ++i) mbar_init(&ctl->r2h_full[i], 1);
     for (int e = 0; e < kEpiWarps; ++e) {
       ctl->queue_tail[e] = 0;
       ctl->queue_head[e] = 0;
@@ -192,6 +203,8 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
     if (elect_one()) {
       tma_prefetch_desc(&tmap_k);
       tma_prefetch_desc(&tmap_q);
+      const bool rows_by_tma = prefetch && P.r2h_tma;
+      if (rows_by_tma) tma_prefetch_desc(&tmap_r);
       const uint64_t policy = l2_policy_evict_first();
       int b = ctl->first_b, t = ctl->first_t, cur_b = -1, qcount = 0, issued = 0;
       for (int i = 0; i < n_tiles; ++i) {
@@ -207,6 +220,11 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
         if (i >= kStages && !mbar_wait(&ctl->empty[s], ((i / kStages) & 1) ^ 1, abort, P.status)) break;
         mbar_arrive_expect_tx(&ctl->full[s], kTileBytes);
         tma_load_3d_evict_first(k_smem + s * kTileBytes, &tmap_k, &ctl->full[s], 0, t * kTileTokens, b, policy);
+        if (rows_by_tma) {  // the tile's host rows, for the epilogue's prefetch candidates
+          const int rs = i % kR;
+          mbar_arrive_expect_tx(&ctl->r2h_full[rs], kRowMapBytes);
+          tma_load_2d(r_smem + rs * kTileTokens, &tmap_r, &ctl->r2h_full[rs], t * kTileTokens, b);
+        }
         ++issued;
         next_tile(P, b, t);
       }
@@ -215,6 +233,9 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
         for (int i = issued - kStages < 0 ? 0 : issued - kStages; i < issued; ++i)
           mbar_drain(&ctl->full[i % kStages], (i / kStages) & 1);
         for (int c = qcount - 2 < 0 ? 0 : qcount - 2; c < qcount; ++c) mbar_drain(&ctl->q_full[c & 1], (c >> 1) & 1);
+        if (rows_by_tma)
+          for (int i = issued - kR < 0 ? 0 : issued - kR; i < issued; ++i)
+            mbar_drain(&ctl->r2h_full[i % kR], (i / kR) & 1);
       }
     }
   } else if (warp == 1) {
@@ -304,6 +325,14 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
         }
         sc[j] = (s0 + s1) + (s2 + s3);
       }
+      // this token's host row (read before the accumulator is handed back, which is
+      // what lets the producer reuse the ring slot)
+      int32_t hrow = -1;
+      if (prefetch && P.r2h_tma) {
+        const int rs = i % kR;
+        if (!mbar_wait(&ctl->r2h_full[rs], (i / kR) & 1, abort, P.status)) break;
+        hrow = r_smem[rs * kTileTokens + row];
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->tmem_empty[ab]);
@@ -314,8 +343,8 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
         if (p < valid[j]) P.scores[(static_cast<size_t>(b) * NQ + j) * P.L_max + p] = sc[j];
 
       if (prefetch) {
-        // threshold test only; the host-row lookup, residency test, ticket and copy
-        // happen in the prefetch warps so that no global load sits on this path
+        // threshold test only; the residency test, ticket and copy happen in the
+        // prefetch warps so that no global load sits on this path
         bool pass = false;
 #pragma unroll
         for (int j = 0; j < NQ; ++j) pass |= (p < valid[j]) && (sc[j] > shat[j]);
@@ -330,7 +359,10 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
           }
           n = __shfl_sync(0xffffffffu, n, 0);
           const int rank = __popc(mask & ((1u << lane) - 1));
-          if (pass && rank < n) ctl->queue[e][(tail + rank) % kQueueCap] = b * P.L_max + p;
+          if (pass && rank < n) {
+            ctl->queue[e][(tail + rank) % kQueueCap] = b * P.L_max + p;
+            ctl->queue_h[e][(tail + rank) % kQueueCap] = hrow;
+          }
           __syncwarp();
           tail += n;
           if (lane == 0 && n > 0) {
@@ -401,7 +433,9 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
       if (lane < n) {
         const int tok = *reinterpret_cast<volatile int *>(&ctl->queue[e][(head + lane) % kQueueCap]);
         b = tok / P.L_max;
-        h = __ldg(P.req_to_host + tok);  // req_to_host is [B][L_max]: index b * L_max + p
+        // req_to_host is [B][L_max]: index b * L_max + p (staged with the tile when possible)
+        h = P.r2h_tma ? *reinterpret_cast<volatile int *>(&ctl->queue_h[e][(head + lane) % kQueueCap])
+                      : __ldg(P.req_to_host + tok);
         if (h >= 0 && h < P.n_h) {
           cand = P.host_to_gpu[h] == kInf;
         } else {
@@ -544,7 +578,8 @@ int sm_count() {
 }
 
 static size_t indexer_smem_bytes(int nq) {
-  return 1024 + echo::kStages * echo::kTileBytes + 2 * (echo::kHeads * nq * echo::kDim) + sizeof(IndexerCtl);
+  return 1024 + echo::kStages * echo::kTileBytes + 2 * (echo::kHeads * nq * echo::kDim) +
+         echo::kR * echo::kRowMapBytes + sizeof(IndexerCtl);
 }
 
 int launch_indexer(const echo_indexer_args *a, cudaStream_t stream) {
@@ -584,7 +619,21 @@ int launch_indexer(const echo_indexer_args *a, cudaStream_t stream) {
       return ECHO_ECUDA;
     }
   }
+  // the host rows of each tile by TMA: 128 int32 per box, rows of L_max int32
+  CUtensorMap tr;
+  memset(&tr, 0, sizeof(tr));
+  bool r2h_tma = false;
+  if (a->s_hat && a->L_max % 4 == 0 && (reinterpret_cast<uintptr_t>(a->req_to_host) & 15) == 0) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(a->L_max), static_cast<cuuint64_t>(a->B)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(a->L_max) * 4};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(echo::kTileTokens), 1};
+    cuuint32_t es[2] = {1, 1};
+    r2h_tma = enc(&tr, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<int32_t *>(a->req_to_host), dims, strides, box,
+                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
   echo::IndexerParams P{};
+  P.r2h_tma = r2h_tma ? 1 : 0;
   P.w = a->w;
   P.ctx_len = a->ctx_len;
   P.scores = a->scores;
@@ -615,7 +664,7 @@ int launch_indexer(const echo_indexer_args *a, cudaStream_t stream) {
       if (e != cudaSuccess) return cuda_fail(e, "indexer smem attribute");
       attr1 = true;
     }
-    echo::indexer_kernel<1><<<grid, echo::kIndexerThreads, smem, stream>>>(tk, tq, P);
+    echo::indexer_kernel<1><<<grid, echo::kIndexerThreads, smem, stream>>>(tk, tq, tr, P);
   } else {
     static bool attr2 = false;
     if (!attr2) {
@@ -623,7 +672,7 @@ int launch_indexer(const echo_indexer_args *a, cudaStream_t stream) {
       if (e != cudaSuccess) return cuda_fail(e, "indexer smem attribute");
       attr2 = true;
     }
-    echo::indexer_kernel<2><<<grid, echo::kIndexerThreads, smem, stream>>>(tk, tq, P);
+    echo::indexer_kernel<2><<<grid, echo::kIndexerThreads, smem, stream>>>(tk, tq, tr, P);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "indexer launch");

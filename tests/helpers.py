@@ -41,7 +41,11 @@ class Case:
         self.n_h = n_h or B * L_max
         self.host_np = wl.host_kv_pool(self.n_h, seed, n_random=min(self.n_h, B * L_max))
         self.r2h = wl.req_to_host(B, L_max)
-        rows = wl.random_resident_rows(min(self.n_h, B * L_max), n_resident, seed)
+        # resident rows are rows of tokens that exist: position p < ctx of their request
+        ctx_b = np.broadcast_to(np.asarray(ctx, np.int64), (B,))
+        exist = np.concatenate([b * L_max + np.arange(int(ctx_b[b]), dtype=np.int64) for b in range(B)])
+        exist = exist[exist < self.n_h]
+        rows = np.sort(exist[wl.random_resident_rows(exist.size, min(n_resident, exist.size), seed)])
         self.state = wl.resident_pool(n_g, self.n_h, rows, wl.random_clocks(n_resident, clock, seed), seed,
                                       scatter=scatter)
         self.host_t = pinned_host_pool(self.host_np)

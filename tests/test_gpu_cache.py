@@ -122,3 +122,31 @@ def test_append_matches_oracle():
         c.assert_pool_equal(c.orc_pool, f"append {step}")
         assert stats.as_dict()["appended"] == ost.as_dict()["appended"]
         assert stats.as_dict()["evicted"] == ost.as_dict()["evicted"]
+
+
+def test_append_of_a_resident_row_matches_oracle():
+    """A caller state in which a new token's host row is already resident: both sides
+    write the row through, flag BAD_INDEX, and take or free no slot for it."""
+    B, L = 3, 400
+    c = Case(B, 1, L, [100, 200, 300], 200, 199, clock=9, seed=8, k=32)
+    future = np.array([c.r2h[0, 100]], np.int32)            # request 0's next token
+    out = torch.empty(1, dtype=torch.int32, device="cuda")
+    echo.echo_pool_alloc(c.pool, c.ws, dev(future), dev(np.array([1], np.int32)), 9, out)
+    slots, rs0 = c.orc_pool.alloc(future, 9)
+    torch.cuda.synchronize()
+    assert rs0 == 0 and int(out.item()) == int(slots[0])
+    kI, ctx = c.inp.k_index.copy(), c.inp.ctx_len.copy()
+    kv, kn = wl.new_tokens(B, 8, 0)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stats = echo.Stats()
+    echo.echo_append(c.pool, c.ws, c.k_index, c.ctx, c.r2h_t, dev(kv.view(np.int16)), dev(kn), 10, stats=stats,
+                     dev_status=st)
+    ost = oracle.Stats()
+    rs = c.orc_pool.append(kI, ctx, c.r2h, kv, kn, 10, ost)
+    torch.cuda.synchronize()
+    assert rs & oracle.BAD_INDEX and int(st.item()) == rs
+    assert np.array_equal(c.ctx.cpu().numpy(), ctx) and np.array_equal(c.k_index.cpu().numpy(), kI)
+    assert np.array_equal(c.host_t.numpy().view(np.uint16), c.orc_pool.host_kv)
+    c.assert_pool_equal(c.orc_pool, "append with a resident row")
+    assert stats.as_dict()["appended"] == ost.as_dict()["appended"] == 2
+    assert stats.as_dict()["evicted"] == ost.as_dict()["evicted"] == 2

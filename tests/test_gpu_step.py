@@ -92,6 +92,7 @@ def check_step_against_oracle(c: Case, R: StepRunner, q, kv, ki, append, kI_o, c
     (1, 1, 4096, 4096, 256, 1024, 512, False, 1),          # the tiny workload
     (4, 1, 3000, 2900, 256, 1200, 1200, True, 2),          # full pool, write-through append
     (3, 2, 2000, 1990, 200, 1500, 1400, True, 3),          # two query tokens
+    (2, 1, 2501, 2480, 128, 900, 800, True, 4),            # rows of host rows not 16-byte aligned
 ])
 def test_decode_steps_match_oracle(B, n_q, L, ctx0, k, n_g, res, append, seed):
     c = Case(B, n_q, L, ctx0, n_g, res, clock=1000, seed=seed, k=k)

@@ -406,6 +406,34 @@ def test_append_is_write_through():
     check_invariants(P)
 
 
+def test_append_of_a_resident_or_repeated_row_takes_and_frees_no_slot():
+    """A new token's row cannot already be resident; if the caller's state says it is
+    (or two requests append the same row), the row is written through, flagged, and
+    neither evicts nor allocates: only the valid appends change the pool."""
+    B, L_max, n_g = 3, 16, 4
+    n_h = B * L_max
+    host = _host(n_h, 3)
+    P = oracle.Pool.empty(n_g, n_h, host)
+    r2h = wl.req_to_host(B, L_max)
+    r2h[2, 7] = r2h[1, 5]                     # request 2 appends request 1's row too
+    ctx = np.array([3, 5, 7], np.int32)
+    # full pool, oldest first: 40, then 41 and 42, then request 0's new row (resident)
+    for rows, clock in (([40], 1), ([41, 42], 2), ([r2h[0, 3]], 3)):
+        got, st = P.alloc(np.array(rows, np.int32), clock=clock)
+        assert st == 0
+    slot0 = int(got[0])
+    assert P.n_free == 0
+    kI = np.zeros((B, L_max, 128), np.uint8)
+    kv, kn = wl.new_tokens(B, 2, 0)
+    status = P.append(kI, ctx, r2h, kv, kn, clock=5)
+    assert status & oracle.BAD_INDEX and list(ctx) == [4, 6, 8]
+    # only request 1's row was allocated, evicting exactly one slot (the oldest: 40's)
+    assert P.HostTokenToGPU[40] == oracle.INF and P.HostTokenToGPU[r2h[0, 3]] == slot0
+    s1 = P.HostTokenToGPU[r2h[1, 5]]
+    assert s1 >= 0 and P.GPUTokenPriority[s1] == 5 and P.n_free == 0
+    assert np.array_equal(host[r2h[0, 3]], kv[0])    # written through all the same
+
+
 # ---------------------------------------------------------------------------
 # EMA, prefetch, lossless
 # ---------------------------------------------------------------------------
