@@ -285,6 +285,7 @@ def run_ours(args):
                                    stage=stage, s_hat=s_hat, clock_dev=clock, advance_clock=True, stats=stats,
                                    events=events)
 
+    warm_host_translations(echo, torch, host_t)
     # step 0 eagerly (first calls set kernel attributes), then one graph per step:
     # plain graphs for the headline loop, graphs with stage events (external event
     # nodes, about 2 us each) for the per-stage breakdown loop that follows it
@@ -430,6 +431,24 @@ def run_ours(args):
     if pg:
         pg.destroy_process_group()
     return 0
+
+
+def warm_host_translations(echo, torch, host_t, page_bytes=65536):
+    """Read one row per page of the pinned host pool through the recall kernel, so the
+    GPU has translated every page once before timing (in serving the pool is read every
+    step; a cold translation costs far more than the read)."""
+    n_h = host_t.shape[0]
+    step = max(1, page_bytes // (host_t.shape[1] * 2))
+    rows = np.arange(0, n_h, step, dtype=np.int32)
+    pool = echo.Pool(rows.size, host_t)
+    echo.echo_pool_init(pool)
+    ws = echo.Workspace(rows.size, rows.size)
+    r2h = torch.from_numpy(rows.reshape(1, -1)).cuda()
+    sel = torch.arange(rows.size, dtype=torch.int32, device="cuda").view(1, 1, -1)
+    ctx = torch.tensor([rows.size], dtype=torch.int32, device="cuda")
+    out = torch.empty_like(sel)
+    echo.echo_prefetch_recall(pool, ws, sel, r2h, ctx, 1, out)
+    torch.cuda.synchronize()
 
 
 def recall_bandwidth_probe(echo, torch, host_t, flush_l2, rows=65536, n_g=65536):
