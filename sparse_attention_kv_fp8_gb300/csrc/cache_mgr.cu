@@ -529,14 +529,19 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
 #pragma unroll
   for (int u = 0; u < kStg; ++u)
     stg[u] = (P.mode == kModeRecall && ef0 + u < ef1 && aux_of(ef0 + u) == -2) ? P.ws.miss_stage[ef0 + u] : -1;
-  uint32_t M = 0, pre_own = 0, hist_total = 0, hist_ex = 0;
+  // this thread's owned misses (their ranks follow the same scan)
+  uint32_t own_seg = 0;
+  if (P.mode != kModeEvict)
+    for (int f = ef0; f < ef1; ++f) own_seg += aux_of(f) == -2;
+  uint32_t M = 0, pre_own = 0, hist_total = 0, hist_ex = 0, own_ex = 0;
   {
-    uint32_t v3[3] = {m, pm, hmine}, ex3[3], tot3[3];
-    coop_scan<3>(v3, ex3, tot3, S);
-    M = tot3[0];
-    pre_own = tot3[1];
-    hist_total = tot3[2];
-    hist_ex = ex3[2];
+    uint32_t v4[4] = {m, pm, hmine, own_seg}, ex4[4], tot4[4];
+    coop_scan<4>(v4, ex4, tot4, S);
+    M = tot4[0];
+    pre_own = tot4[1];
+    hist_total = tot4[2];
+    hist_ex = ex4[2];
+    own_ex = ex4[3];
   }
   int32_t E = 0;
   if (P.mode == kModeEvict) {
@@ -606,11 +611,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
   uint32_t my_lt = 0, my_eq = 0, my_fr = 0;  // this CTA's slots older than / at T, free
   // owned misses, in entry order (contiguous per-thread segments), with their sources
   if (P.mode != kModeEvict) {
-    uint32_t own = 0;
-    for (int f = ef0; f < ef1; ++f) own += aux_of(f) == -2;
-    uint32_t v1[1] = {own}, ex1[1], tot1[1];
-    coop_scan<1>(v1, ex1, tot1, S);
-    uint32_t r = pre_own + ex1[0];
+    uint32_t r = pre_own + own_ex;
 #pragma unroll
     for (int u = 0; u < kStg; ++u) {
       const int f = ef0 + u;
@@ -630,9 +631,16 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
       ++r;
     }
   }
+  // this CTA's slots older than / at T and free, counted over contiguous per-thread
+  // segments: the exclusive prefixes stay in registers for phase P4's ranking
+  const int s_cnt = s_hi - s_lo;
+  const int s_per = (s_cnt + kCoopThreads - 1) / kCoopThreads;
+  const int q0 = s_lo + min(s_cnt, static_cast<int>(threadIdx.x) * s_per);
+  const int q1 = s_lo + min(s_cnt, static_cast<int>(threadIdx.x + 1) * s_per);
+  uint32_t seg_lt_ex = 0, seg_eq_ex = 0, seg_fr_ex = 0;
   {
     uint32_t lt = 0, eq = 0, fr = 0;
-    for (int s = s_lo + threadIdx.x; s < s_hi; s += kCoopThreads) {
+    for (int s = q0; s < q1; ++s) {
       const int32_t v = slot_val(s);
       if (v == kFreeMark) {
         ++fr;
@@ -643,6 +651,9 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     }
     uint32_t v3[3] = {lt, eq, fr}, ex3[3], tot3[3];
     coop_scan<3>(v3, ex3, tot3, S);
+    seg_lt_ex = ex3[0];
+    seg_eq_ex = ex3[1];
+    seg_fr_ex = ex3[2];
     my_lt = tot3[0];
     my_eq = tot3[1];
     my_fr = tot3[2];
@@ -707,25 +718,10 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     }
     rows_load(src, my_nr, buf);
   }
-  // rank this CTA's slots (contiguous per-thread segments); victims lose their maps
+  // rank this CTA's slots (the per-thread segments and prefixes of P3); victims lose
+  // their maps
   {
-    const int cnt = s_hi - s_lo;
-    const int per = (cnt + kCoopThreads - 1) / kCoopThreads;
-    const int q0 = s_lo + min(cnt, static_cast<int>(threadIdx.x) * per);
-    const int q1 = s_lo + min(cnt, static_cast<int>(threadIdx.x + 1) * per);
-    uint32_t lt = 0, eq = 0, fr = 0;
-    for (int s = q0; s < q1; ++s) {
-      const int32_t v = slot_val(s);
-      if (v == kFreeMark) {
-        ++fr;
-      } else if (E > 0 && v >= 0 && v < clock) {
-        lt += v < Tp;
-        eq += v == Tp;
-      }
-    }
-    uint32_t v3[3] = {lt, eq, fr}, ex3[3], tot3[3];
-    coop_scan<3>(v3, ex3, tot3, S);
-    uint32_t lt_b = pre_lt + ex3[0], eq_b = pre_eq + ex3[1], fr_b = pre_fr + ex3[2];
+    uint32_t lt_b = pre_lt + seg_lt_ex, eq_b = pre_eq + seg_eq_ex, fr_b = pre_fr + seg_fr_ex;
     for (int s = q0; s < q1; ++s) {
       const int32_t v = slot_val(s);
       // victims before s (all evictable slots older than T, the first needT at T), and

@@ -49,9 +49,9 @@ namespace echo {
 constexpr int kTileTokens = 128;
 constexpr int kTileBytes = kTileTokens * kDim;  // 16 KB
 constexpr int kStages = 10;
-constexpr int kEpiGroups = 2;                // epilogue warpgroups, alternating tiles
+constexpr int kEpiGroups = 2;                // epilogue warpgroups, taking tiles in turn
 constexpr int kEpiWarps = 4 * kEpiGroups;
-constexpr int kPfWarps = 4;                  // each serves kEpiWarps / kPfWarps queues
+constexpr int kPfWarps = 8;                  // each serves kEpiWarps / kPfWarps queues
 constexpr int kIndexerThreads = 32 * (2 + kEpiWarps + kPfWarps);
 constexpr int kAcc = 4;            // TMEM accumulators (MMA runs up to 3 tiles ahead of the epilogue)
 constexpr int kQueueCap = 64;      // entries per epilogue -> prefetch queue

@@ -387,8 +387,10 @@ __global__ void __launch_bounds__(kSelThreads, 1)
       }
     }
   }
+  ECHO_TRACE_MARK(8);
   if (use_list) {
     __syncthreads();
+    ECHO_TRACE_MARK(9);
     for (int li = threadIdx.x; li < static_cast<int>(n_sel); li += kSelThreads) {
       const int i = static_cast<int>(list_tok[li]);
       const int32_t h = stage_r2h ? r2s[i] : __ldg(r2h + i);
@@ -400,6 +402,7 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     if (do_claim) ca.ws.entry_h[f_row + i] = -1;
   }
   if (rank == 0 && threadIdx.x == 0) kth[row] = target > 0 ? key_score(T) : -INFINITY;
+  ECHO_TRACE_MARK(10);
   cl.sync();  // no CTA leaves while others may still read its shared memory
   ECHO_TRACE_MARK(7);
   ECHO_TRACE_LAST(25);
