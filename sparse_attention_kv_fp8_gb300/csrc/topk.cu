@@ -329,6 +329,8 @@ __global__ void __launch_bounds__(kSelThreads, 1)
   // ---- ascending output: selected iff key > T, or key == T among the first needT
   // equal keys; each thread's segment is contiguous, so a block scan orders them
   uint32_t g = 0, e = 0;
+  uint64_t sel_mask = 0;  // bit j: key s0 + j is above or equal to T (segments of at most 64)
+  const bool masks = s1 - s0 <= 64;
   if (target > 0)
     for (int i = s0; i < s1; i += 4) {
       const uint4 v = keys4[i >> 2];
@@ -338,6 +340,7 @@ __global__ void __launch_bounds__(kSelThreads, 1)
         if (i + u < s1) {
           g += kv[u] > T;
           e += kv[u] == T;
+          if (masks && kv[u] >= T) sel_mask |= 1ull << (i + u - s0);
         }
     }
   uint32_t eg, ee, tg, te;
@@ -353,38 +356,52 @@ __global__ void __launch_bounds__(kSelThreads, 1)
   const uint32_t te_taken = (pe + te < needT ? pe + te : needT) - mpe;
   const uint32_t n_sel = target > 0 ? tg + te_taken : 0u;
   const bool use_list = do_claim && n_sel <= static_cast<uint32_t>(kList);
+  // one compact pass over the keys at or above T only: positions, output, claim list
   if (target > 0 && (g | e)) {
     uint32_t gb = pg + eg, eb = pe + ee;
-    for (int i0 = s0; i0 < s1; i0 += 4) {
-      const uint4 v = keys4[i0 >> 2];
-      const uint32_t kv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = i0 + u;
-        if (i >= s1) break;
-        const uint32_t key = kv[u];
-        int pos = -1;
-        uint32_t li = 0;
-        if (key > T) {
-          li = (gb - pg) + ((eb < needT ? eb : needT) - mpe);
-          pos = static_cast<int>(gb + (eb < needT ? eb : needT));
-          ++gb;
-        } else if (key == T) {
-          if (eb < needT) {
-            li = (gb - pg) + (eb - mpe);
-            pos = static_cast<int>(gb + eb);
-          }
-          ++eb;
-        }
-        if (pos < 0) continue;
-        out[pos] = lo + i;
-        if (use_list) {
-          list_pos[li] = static_cast<uint32_t>(pos);
-          list_tok[li] = static_cast<uint32_t>(i);
-        } else if (do_claim) {
-          claim_entry(ca.pool, ca.ws, f_row + pos, __ldg(r2h + i), clock, ca.status);
-        }
+    uint64_t todo = masks ? sel_mask : ~0ull;
+    for (int i = s0; i < s1 && todo; ++i) {
+      if (masks) {
+        i = s0 + __ffsll(static_cast<long long>(todo)) - 1;
+        todo &= todo - 1;
       }
+      const uint32_t key = keys[i];
+      int pos = -1;
+      uint32_t li = 0;
+      if (key > T) {
+        const uint32_t t_before = eb < needT ? eb : needT;
+        li = (gb - pg) + (t_before - mpe);
+        pos = static_cast<int>(gb + t_before);
+        ++gb;
+      } else if (key == T) {
+        if (eb < needT) {
+          li = (gb - pg) + (eb - mpe);
+          pos = static_cast<int>(gb + eb);
+        }
+        ++eb;
+      }
+      if (pos < 0) continue;
+      out[pos] = lo + i;
+      if (use_list) {
+        list_pos[li] = static_cast<uint32_t>(pos);
+        list_tok[li] = static_cast<uint32_t>(i);
+      }
+    }
+  }
+  if (do_claim && !use_list && target > 0 && (g | e)) {
+    // more selected entries in this CTA than the list holds: claim in a second pass
+    uint32_t gb = pg + eg, eb = pe + ee;
+    for (int i = s0; i < s1; ++i) {
+      const uint32_t key = keys[i];
+      int pos = -1;
+      if (key > T) {
+        pos = static_cast<int>(gb + (eb < needT ? eb : needT));
+        ++gb;
+      } else if (key == T) {
+        if (eb < needT) pos = static_cast<int>(gb + eb);
+        ++eb;
+      }
+      if (pos >= 0) claim_entry(ca.pool, ca.ws, f_row + pos, __ldg(r2h + i), clock, ca.status);
     }
   }
   ECHO_TRACE_MARK(8);
