@@ -31,7 +31,8 @@ struct Workspace {
   int32_t *slot_claim;  // [n_g]  lowest entry index of this step's hits (INT32_MAX = none)
   int32_t *entry_rows;  // [max_rows] host row per entry (append)
   int32_t *entry_h;     // [max_rows] host row of every entry, -1 if none
-  int32_t *ent_aux;     // [max_rows] >= 0 hit slot, -1 none, -2 owned miss, -3 - f1 repeat of entry f1
+  int32_t *ent_aux;     // [max_rows] after a claim: HostTokenToGPU as the claim saw it; after the
+                        // classification: >= 0 hit slot, -1 none, -2 owned miss, -3 - f1 repeat of f1
   int32_t *miss_f;      // [max_rows] entry index of the r-th owned miss
   int32_t *miss_h;      // [max_rows] host row of the r-th owned miss
   int32_t *miss_rank;   // [max_rows] by entry: rank of an owned miss
@@ -114,6 +115,7 @@ __device__ __forceinline__ void claim_entry(const PoolView &pool, const Workspac
     h = -1;
   }
   ws.entry_h[f] = h;
+  ws.ent_aux[f] = v;  // the map entry seen here: a hit's slot stays valid for the step
 }
 
 }  // namespace echo

@@ -399,16 +399,34 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
       uint32_t own = 0, hits = 0, valid = 0, reps = 0;
       for (int f0 = e_lo + t; f0 < e_hi; f0 += kT * kU) {
         int32_t h[kU], v[kU], sc[kU];
+        // recall: the claim recorded the map entry it saw, so a hit's slot (protected,
+        // unchanged since) needs no second lookup; a miss reads the map for the winner
+        const bool seen = P.mode == kModeRecall;
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
           const int f = f0 + u * kT;
           h[u] = -1;
-          if (f < e_hi) h[u] = P.mode == kModeAppend ? P.ws.entry_rows[f] : P.ws.entry_h[f];
+          v[u] = kInf;
+          if (f < e_hi) {
+            h[u] = P.mode == kModeAppend ? P.ws.entry_rows[f] : P.ws.entry_h[f];
+            if (seen) v[u] = P.ws.ent_aux[f];
+          }
         }
 #pragma unroll
-        for (int u = 0; u < kU; ++u) v[u] = h[u] >= 0 ? P.pool.h2g[h[u]] : kInf;
+        for (int u = 0; u < kU; ++u) {
+          const bool hit = h[u] >= 0 && v[u] >= 0 && v[u] < n_g;
+          sc[u] = -1;
+          if (seen && hit) {
+            sc[u] = P.ws.slot_claim[v[u]];
+          } else if (h[u] >= 0) {
+            v[u] = P.pool.h2g[h[u]];
+          }
+        }
+        if (!seen) {
 #pragma unroll
-        for (int u = 0; u < kU; ++u) sc[u] = (h[u] >= 0 && v[u] >= 0 && v[u] < n_g) ? P.ws.slot_claim[v[u]] : -1;
+          for (int u = 0; u < kU; ++u)
+            sc[u] = (h[u] >= 0 && v[u] >= 0 && v[u] < n_g) ? P.ws.slot_claim[v[u]] : -1;
+        }
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
           const int f = f0 + u * kT;
@@ -460,15 +478,23 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
   } else if (P.mode == kModeRecall && P.stage_count != nullptr) {
     // which claimed misses the prefetch staged this step (one warp per request)
     const int sw = warp - kSlotWarps - kEntWarps;
+    constexpr int kSpec = 4;  // staged rows per lane read together with the count
     for (int b = c * kStageWarps + sw; b < P.B; b += G * kStageWarps) {
       int L = P.ctx_len[b];
+      int nb = P.stage_count[b];
+      int32_t hs[kSpec];
+#pragma unroll
+      for (int j = 0; j < kSpec; ++j) {
+        const int i = lane + 32 * j;
+        hs[j] = i < P.stage_stride ? P.stage_host[static_cast<size_t>(b) * P.stage_stride + i] : -1;
+      }
       L = L < 0 ? 0 : (L > P.L_max ? P.L_max : L);
       int cap = (L + P.cap_div - 1) / P.cap_div;
       cap = cap < P.stage_stride ? cap : P.stage_stride;
-      int nb = P.stage_count[b];
       nb = nb < cap ? nb : cap;
       for (int i = lane; i < nb; i += 32) {
-        const int32_t h = P.stage_host[static_cast<size_t>(b) * P.stage_stride + i];
+        const int j = i >> 5;
+        const int32_t h = j < kSpec ? pick_reg(hs, j) : P.stage_host[static_cast<size_t>(b) * P.stage_stride + i];
         if (h < 0 || h >= P.pool.n_h) continue;
         const int32_t v = P.pool.h2g[h];
         if (v < 0) {
