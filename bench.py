@@ -509,6 +509,7 @@ def run_kernel_case(args):
     rows = rows[:pool.n_g]
     ws = echo.Workspace(pool.n_g, len(rows))
     out = torch.empty(len(rows), dtype=torch.int32, device="cuda")
+    warm_host_translations(echo, torch, host_t)
     echo.echo_pool_alloc(pool, ws, torch.tensor(rows, dtype=torch.int32, device="cuda"),
                          torch.tensor([len(rows)], dtype=torch.int32, device="cuda"), 1, out)
     for _ in range(args.reps):
