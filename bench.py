@@ -381,6 +381,7 @@ def run_ours(args):
         best = min(best, a0.elapsed_time(a1))
     h2d_gbs = (256 << 20) / (best * 1e-3) / 1e9
     recall_probe = recall_bandwidth_probe(echo, torch, host_t, flush_l2)
+    volume_probe = indexer_volume_probe(echo, torch, inp, flush_l2, hbm_peak)
 
     # ---- roofline of the dominant kernel (the indexer) ----
     idx_ms = float(np.mean(stage_ms["indexer"]))
@@ -418,6 +419,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": traffic, "kernel": "indexer_kernel<1>",
                      "peak_source": peak_src, "bytes_per_launch": idx_bytes},
+        "indexer_volume": volume_probe,
         "cpu_baseline": cpu,
         "e2e": {"value": 1e3 / e2e_ms, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "echo_decode_step (C ABI, eager) with q/w copied in from pinned host and out_slot/status "
@@ -475,6 +477,37 @@ def recall_bandwidth_probe(echo, torch, host_t, flush_l2, rows=65536, n_g=65536)
         best = min(best, a0.elapsed_time(a1))
     ok = bool((out >= 0).all().item())
     return {"rows": rows, "bytes": rows * 1152, "ms": best, "gbs": rows * 1152 / (best * 1e-3) / 1e9, "all_recalled": ok}
+
+
+def indexer_volume_probe(echo, torch, inp, flush_l2, hbm_peak, batches=(8, 24, 64), reps=5):
+    """The indexer alone (scoring, no prefetch) at growing per-launch volume: the decode
+    batch's keys tiled to B requests, L2 flushed before each launch, median of `reps`
+    CUDA-event timings.  Shows the fixed launch cost giving way to bandwidth."""
+    res = []
+    B0, L_ = inp.k_index.shape[0], inp.k_index.shape[1]
+    for Bv in batches:
+        idx = np.arange(Bv) % B0
+        k_t = torch.from_numpy(np.ascontiguousarray(inp.k_index[idx])).cuda()
+        q_t = torch.from_numpy(np.ascontiguousarray(inp.q[idx])).cuda()
+        w_t = torch.from_numpy(np.ascontiguousarray(inp.w[idx])).cuda()
+        ctx_t = torch.full((Bv,), L_, dtype=torch.int32, device="cuda")
+        sc = torch.empty((Bv, 1, L_), dtype=torch.float32, device="cuda")
+        echo.echo_indexer_score(q_t, w_t, k_t, ctx_t, sc)
+        ts = []
+        for _ in range(reps):
+            flush_l2()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record()
+            echo.echo_indexer_score(q_t, w_t, k_t, ctx_t, sc)
+            a1.record()
+            torch.cuda.synchronize()
+            ts.append(a0.elapsed_time(a1))
+        ms = float(np.median(ts))
+        nbytes = Bv * L_ * 128 + Bv * L_ * 4 + Bv * (64 * 128 + 64 * 4)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res.append({"B": Bv, "L": L_, "bytes": nbytes, "us": ms * 1e3, "gbs": gbs, "frac": gbs / hbm_peak})
+        del k_t, sc
+    return res
 
 
 def run_kernel_case(args):
