@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
   if (threadIdx.x < 8) S->red[threadIdx.x] = 0;
   __syncthreads();
   if (warp < kSlotWarps) {
-    constexpr int kT = kSlotWarps * 32, kU = 4;
+    constexpr int kT = kSlotWarps * 32, kU = 8;  // one round of loads covers 2048 slots per CTA
     const bool hist_on = P.mode != kModeAlloc;
     for (int s0 = s_lo + static_cast<int>(threadIdx.x); s0 < s_hi; s0 += kT * kU) {
       uint8_t fr[kU];
@@ -392,6 +392,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
         if (hist_on && v >= 0 && v < clock) atomicAdd(&S->hist[min(slot_age(clock, v), kHistBins - 1u)], 1u);
       }
     }
+    if (lane == 0) ECHO_TRACE_LAST_HERE(11);
   } else if (warp < kSlotWarps + kEntWarps) {
     if (P.mode != kModeEvict) {
       constexpr int kT = kEntWarps * 32, kU = 2;
@@ -475,6 +476,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
         if (reps) atomicAdd(&S->red[3], reps);
       }
     }
+    if (lane == 0) ECHO_TRACE_LAST_HERE(12);
   } else if (P.mode == kModeRecall && P.stage_count != nullptr) {
     // which claimed misses the prefetch staged this step (one warp per request)
     const int sw = warp - kSlotWarps - kEntWarps;
@@ -492,18 +494,33 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
       int cap = (L + P.cap_div - 1) / P.cap_div;
       cap = cap < P.stage_stride ? cap : P.stage_stride;
       nb = nb < cap ? nb : cap;
-      for (int i = lane; i < nb; i += 32) {
-        const int j = i >> 5;
-        const int32_t h = j < kSpec ? pick_reg(hs, j) : P.stage_host[static_cast<size_t>(b) * P.stage_stride + i];
+      // the first kSpec * 32 staged rows: all their map lookups in flight together
+      int32_t vs[kSpec];
+#pragma unroll
+      for (int j = 0; j < kSpec; ++j) {
+        const int i = lane + 32 * j;
+        vs[j] = (i < nb && hs[j] >= 0 && hs[j] < P.pool.n_h) ? P.pool.h2g[hs[j]] : 0;
+      }
+#pragma unroll
+      for (int j = 0; j < kSpec; ++j) {
+        const int i = lane + 32 * j;
+        if (i < nb && vs[j] < 0) {
+          const uint32_t f = static_cast<uint32_t>(vs[j]) - 0x80000000u;  // v = kClaim + f
+          if (f < static_cast<uint32_t>(P.F)) P.ws.miss_stage[f] = b * P.stage_stride + i;
+        }
+      }
+      for (int i = lane + 32 * kSpec; i < nb; i += 32) {  // beyond: one at a time
+        const int32_t h = P.stage_host[static_cast<size_t>(b) * P.stage_stride + i];
         if (h < 0 || h >= P.pool.n_h) continue;
         const int32_t v = P.pool.h2g[h];
         if (v < 0) {
-          const uint32_t f = static_cast<uint32_t>(v) - 0x80000000u;  // v = kClaim + f
+          const uint32_t f = static_cast<uint32_t>(v) - 0x80000000u;
           if (f < static_cast<uint32_t>(P.F)) P.ws.miss_stage[f] = b * P.stage_stride + i;
         }
       }
       if (lane == 0) add_stat(P.stats, &echo_stats::staged, static_cast<unsigned long long>(nb));
     }
+    if (lane == 0) ECHO_TRACE_LAST_HERE(13);
   }
   __syncthreads();
   if (P.mode != kModeAlloc)
