@@ -326,6 +326,16 @@ typedef struct echo_step_args {
 
 int echo_decode_step(const echo_step_args *args, void *stream);
 
+/*
+ * Self-test of the failure detection (no counterpart on the pages): launches a
+ * kernel whose wait nothing will satisfy -- which = 0: an mbarrier wait (the wait the
+ * indexer's roles use), which = 1: a grid barrier of a cooperative launch that one CTA
+ * never reaches (the barrier the cache-manager kernel uses).  The wait gives up after
+ * one second, ECHO_DEV_WAIT_TIMEOUT is OR-ed into *dev_status (device memory) and
+ * every CTA returns; the context stays usable.  Takes about one second of GPU time.
+ */
+int echo_selftest_wait_timeout(int32_t which, int32_t *dev_status, void *stream);
+
 /* Description of the calling thread's last error ("" if none). */
 const char *echo_last_error_string(void);
 

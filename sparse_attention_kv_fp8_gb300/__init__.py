@@ -84,6 +84,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "echo_indexer_score": ([ctypes.POINTER(c_indexer_args), _P], S),
         "echo_select_topk": ([_P, _P, _I32, _I32, _I32, _I32, _P, _P, _P], S),
         "echo_workspace_bytes": ([_I32, _I32, ctypes.POINTER(ctypes.c_size_t)], S),
+        "echo_selftest_wait_timeout": ([_I32, _P, _P], S),
         "echo_workspace_init": ([ctypes.POINTER(c_workspace), _P], S),
         "echo_pool_init": ([ctypes.POINTER(c_pool), _P], S),
         "echo_pool_alloc": ([ctypes.POINTER(c_pool), ctypes.POINTER(c_workspace), _P, _P, _I32, _I32, _P, _P, _P, _P], S),
@@ -276,6 +277,12 @@ def echo_prefetch_recall_noalloc(pool: Pool, sel, req_to_host, ctx_len, clock: i
         k, req_to_host.shape[1], ctypes.pointer(stage.c) if stage is not None else None, int(clock),
         _dev(clock_dev, "clock_dev"), _dev(out_slot, "out_slot"), _dev(stats.t, "stats") if stats is not None else None,
         _dev(dev_status, "dev_status"), _stream(stream)), "echo_prefetch_recall_noalloc")
+
+
+def echo_selftest_wait_timeout(which: int, dev_status, stream=None):
+    """A wait nothing satisfies gives up after a second and flags WAIT_TIMEOUT."""
+    _check(load_library().echo_selftest_wait_timeout(int(which), _dev(dev_status, "dev_status"), _stream(stream)),
+           "echo_selftest_wait_timeout")
 
 
 def echo_append(pool: Pool, ws: Workspace, k_index, ctx_len, req_to_host, new_kv, new_k_index, clock: int,

@@ -45,6 +45,7 @@ int launch_recall(const echo_pool *pool, const echo_workspace *ws, const int32_t
 int launch_topk_claim(const float *scores, const int32_t *ctx_len, int B, int n_q, int L_max, int k, int32_t *sel,
                       float *kth, const echo_pool *pool, const echo_workspace *ws, const int32_t *req_to_host,
                       int32_t clock, const int32_t *clock_dev, int32_t *status, cudaStream_t stream);
+int launch_wait_probe(int which, int32_t *status, cudaStream_t s);
 int launch_append(const echo_pool *pool, const echo_workspace *ws, uint8_t *k_index, int32_t *ctx_len,
                   const int32_t *req_to_host, int B, int L_max, const uint16_t *new_kv, const uint8_t *new_k_index,
                   int32_t clock, const int32_t *clock_dev, echo_stats *stats, int32_t *status, cudaStream_t s);
@@ -131,6 +132,12 @@ static int check_stage(const echo_stage *st) {
 extern "C" {
 
 const char *echo_last_error_string(void) { return g_err; }
+
+int echo_selftest_wait_timeout(int32_t which, int32_t *dev_status, void *stream) {
+  REQUIRE(which == 0 || which == 1, "which must be 0 (mbarrier wait) or 1 (grid barrier)");
+  REQUIRE(dev_status, "dev_status is NULL");
+  return launch_wait_probe(which, dev_status, static_cast<cudaStream_t>(stream));
+}
 
 int32_t echo_version(void) { return (1 << 16) | 0; }
 

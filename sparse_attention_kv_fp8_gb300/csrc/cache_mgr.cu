@@ -986,6 +986,29 @@ __global__ void ws_init_kernel(Workspace ws, int n_g, int max_rows) {
   for (int i = tid; i < kCtrCount; i += nt) ws.ctr[i] = 0;
 }
 
+// Self-test of the bounded waits (no counterpart on the pages).  which = 0: one
+// thread waits on an mbarrier nothing arrives on; which = 1: a cooperative grid
+// barrier that CTA 0 never reaches.  Either wait gives up after kWaitLimitNs and sets
+// WAIT_TIMEOUT; every CTA returns, so the context stays usable.
+__global__ void __launch_bounds__(kCoopThreads, 1) wait_probe_kernel(int which, uint32_t *glob, int32_t *status) {
+  __shared__ CoopSmem S_;
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (which == 0) {
+    if (blockIdx.x != 0) return;
+    if (threadIdx.x == 0) {
+      mbar_init(&bar, 1);
+      abort_flag = 0;
+      fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort_flag, status);
+    return;
+  }
+  if (blockIdx.x == 0) return;  // the CTA the others wait for
+  grid_barrier(glob, status, &S_);
+}
+
 __global__ void ema_kernel(float *s_hat, const float *kth, int n, float alpha) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) ema_one(s_hat, kth, i, alpha);
@@ -1150,6 +1173,32 @@ int launch_recall(const echo_pool *pool, const echo_workspace *ws, const int32_t
   P.alpha = ema_alpha;
   P.clock_advance = clock_advance;
   return run_op(P, s, claimed != 0);  // after the decode step's top-k: programmatic launch
+}
+
+// the probes' grid barrier counts in its own 4-byte device word (never reset: a
+// barrier that gave up leaves it off a multiple of the grid, which only this probe uses)
+static __device__ uint32_t g_probe_barrier[echo::kGCount];
+
+int launch_wait_probe(int which, int32_t *status, cudaStream_t s) {
+  uint32_t *glob = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void **>(&glob), g_probe_barrier);
+  if (e != cudaSuccess) return cuda_fail(e, "wait probe scratch");
+  if (which == 0) {
+    echo::wait_probe_kernel<<<1, echo::kCoopThreads, 0, s>>>(0, glob, status);
+    return check("wait probe");
+  }
+  const int grid = sm_count() < 8 ? sm_count() : 8;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(echo::kCoopThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeCooperative;
+  at[0].val.cooperative = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, echo::wait_probe_kernel, 1, glob, status);
+  return e == cudaSuccess ? ECHO_OK : cuda_fail(e, "wait probe");
 }
 
 int launch_append(const echo_pool *pool, const echo_workspace *ws, uint8_t *k_index, int32_t *ctx_len,

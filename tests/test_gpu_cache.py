@@ -150,3 +150,26 @@ def test_append_of_a_resident_row_matches_oracle():
     c.assert_pool_equal(c.orc_pool, "append with a resident row")
     assert stats.as_dict()["appended"] == ost.as_dict()["appended"] == 2
     assert stats.as_dict()["evicted"] == ost.as_dict()["evicted"] == 2
+
+
+@pytest.mark.parametrize("which", [0, 1])
+def test_bounded_wait_gives_up_and_the_context_stays_usable(which):
+    """A wait nothing satisfies (an mbarrier with no arrivals; a grid barrier one CTA
+    never reaches) gives up after about a second with WAIT_TIMEOUT; work launched
+    afterwards runs normally."""
+    import time
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.perf_counter()
+    echo.echo_selftest_wait_timeout(which, st)
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    assert int(st.item()) & echo.DEV_WAIT_TIMEOUT
+    assert 0.5 < dt < 30.0
+    c = Case(1, 1, 512, 512, 64, 32, clock=5, seed=9, k=16)
+    scores = torch.empty((1, 1, 512), dtype=torch.float32, device="cuda")
+    st2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    echo.echo_indexer_score(c.q, c.w, c.k_index, c.ctx, scores, dev_status=st2)
+    torch.cuda.synchronize()
+    ref = oracle.indexer_score(c.inp.q, c.inp.w, c.inp.k_index, c.inp.ctx_len)
+    assert int(st2.item()) == 0
+    assert np.allclose(scores.cpu().numpy(), ref, rtol=1e-3, atol=1e-6)
