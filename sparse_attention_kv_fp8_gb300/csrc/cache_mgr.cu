@@ -1102,13 +1102,11 @@ static int run_op(const echo::OpParams &P0, cudaStream_t s, bool pdl = false) {
   const long long epc = (static_cast<long long>(P.mode == echo::kModeEvict ? 0 : P.F) + grid - 1) / grid;
   P.slot_cache_cap = spc <= kSlotCacheMax ? static_cast<int>(spc) : 0;
   P.ent_cache_cap = epc <= kEntCacheMax ? static_cast<int>(epc) : 0;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(echo::cache_op_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (3 * kSlotCacheMax + 2 * kEntCacheMax) * static_cast<int>(sizeof(int32_t)));
-    if (e != cudaSuccess) return cuda_fail(e, "cache-manager smem attribute");
-    attr = true;
-  }
+  static bool attr[64] = {false};
+  if (int r = smem_limit_once(attr, echo::cache_op_kernel,
+                              (3 * kSlotCacheMax + 2 * kEntCacheMax) * static_cast<int>(sizeof(int32_t)),
+                              "cache-manager smem attribute"))
+    return r;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(echo::kCoopThreads);

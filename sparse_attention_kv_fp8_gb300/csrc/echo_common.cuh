@@ -320,4 +320,18 @@ __device__ __forceinline__ int query_valid_len(int L, int n_q, int j) {
 namespace echo_host {
 void set_error(const char *fmt, ...);
 int cuda_fail(cudaError_t e, const char *what);
+
+// Raises a kernel's dynamic shared-memory limit once per device (the first call on a
+// device must come before any stream capture on it).
+template <typename K>
+inline int smem_limit_once(bool (&done)[64], K kernel, int bytes, const char *what) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (done[dev]) return 0;
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  done[dev] = true;
+  return 0;
+}
 }  // namespace echo_host

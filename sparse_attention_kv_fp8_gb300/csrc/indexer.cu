@@ -658,20 +658,14 @@ int launch_indexer(const echo_indexer_args *a, cudaStream_t stream) {
   const size_t smem = indexer_smem_bytes(nq);
   cudaError_t e;
   if (nq == 1) {
-    static bool attr1 = false;
-    if (!attr1) {
-      e = cudaFuncSetAttribute(echo::indexer_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-      if (e != cudaSuccess) return cuda_fail(e, "indexer smem attribute");
-      attr1 = true;
-    }
+    static bool attr1[64] = {false};
+    if (int r = smem_limit_once(attr1, echo::indexer_kernel<1>, static_cast<int>(smem), "indexer smem attribute"))
+      return r;
     echo::indexer_kernel<1><<<grid, echo::kIndexerThreads, smem, stream>>>(tk, tq, tr, P);
   } else {
-    static bool attr2 = false;
-    if (!attr2) {
-      e = cudaFuncSetAttribute(echo::indexer_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-      if (e != cudaSuccess) return cuda_fail(e, "indexer smem attribute");
-      attr2 = true;
-    }
+    static bool attr2[64] = {false};
+    if (int r = smem_limit_once(attr2, echo::indexer_kernel<2>, static_cast<int>(smem), "indexer smem attribute"))
+      return r;
     echo::indexer_kernel<2><<<grid, echo::kIndexerThreads, smem, stream>>>(tk, tq, tr, P);
   }
   e = cudaGetLastError();

@@ -453,13 +453,8 @@ static int launch_topk_impl(const float *scores, const int32_t *ctx_len, int B, 
     smem += static_cast<size_t>(chunk) * sizeof(int32_t);
     stage_r2h = 1;
   }
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(echo::topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         echo::kTopkSmemMax);
-    if (e != cudaSuccess) return cuda_fail(e, "top-k smem attribute");
-    attr = true;
-  }
+  static bool attr[64] = {false};
+  if (int r = smem_limit_once(attr, echo::topk_kernel, echo::kTopkSmemMax, "top-k smem attribute")) return r;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(rows * C);
   cfg.blockDim = dim3(echo::kSelThreads);
