@@ -145,27 +145,51 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
   pdl_launch_dependents();  // the top-k may be scheduled as SMs free up; it waits for completion
   ECHO_TRACE_FIRST(24);
 
-  // ---- work split: the non-empty tiles of all requests, evenly over the grid
-  if (threadIdx.x == 0) {
+  // ---- work split: the non-empty tiles of all requests, evenly over the grid.  Warp
+  // 0 reads the context lengths 32 at a time (one round trip for up to 32 requests).
+  if (warp == 0) {
     int total = 0;
-    for (int b = 0; b < P.B; ++b) {
-      int32_t L = __ldg(P.ctx_len + b);
-      if (L < 0 || L > P.L_max) set_status(P.status, ECHO_DEV_BAD_INDEX);
-      total += tiles_of(clamp_ctx(L, P.L_max));
+    for (int b0 = 0; b0 < P.B; b0 += 32) {
+      const int b = b0 + lane;
+      int nt = 0;
+      if (b < P.B) {
+        const int32_t L = __ldg(P.ctx_len + b);
+        if (L < 0 || L > P.L_max) set_status(P.status, ECHO_DEV_BAD_INDEX);
+        nt = tiles_of(clamp_ctx(L, P.L_max));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) nt += __shfl_xor_sync(0xffffffffu, nt, o);
+      total += nt;
     }
     const int v0 = static_cast<int>((static_cast<long long>(total) * blockIdx.x) / gridDim.x);
     const int v1 = static_cast<int>((static_cast<long long>(total) * (blockIdx.x + 1)) / gridDim.x);
-    int b = 0, acc = 0;
-    while (b < P.B) {
-      int nt = tiles_of(clamp_ctx(__ldg(P.ctx_len + b), P.L_max));
-      if (v0 < acc + nt) break;
-      acc += nt;
-      ++b;
+    // the request holding tile v0: the first whose inclusive tile count passes v0
+    int acc = 0, first_b = P.B, first_t = 0;
+    for (int b0 = 0; b0 < P.B && first_b == P.B; b0 += 32) {
+      const int b = b0 + lane;
+      const int nt = b < P.B ? tiles_of(clamp_ctx(__ldg(P.ctx_len + b), P.L_max)) : 0;
+      int inc = nt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += u;
+      }
+      const uint32_t hit = __ballot_sync(0xffffffffu, b < P.B && v0 < acc + inc);
+      if (hit) {
+        const int l = __ffs(hit) - 1;
+        first_b = b0 + l;
+        first_t = v0 - (acc + __shfl_sync(0xffffffffu, inc - nt, l));
+      }
+      acc += __shfl_sync(0xffffffffu, inc, 31);
     }
-    ctl->first_b = b;
-    ctl->first_t = v0 - acc;
-    ctl->n_tiles = v1 - v0;
-    ctl->abort = 0;
+    if (lane == 0) {
+      ctl->first_b = first_b;
+      ctl->first_t = first_b < P.B ? first_t : 0;
+      ctl->n_tiles = v1 - v0;
+      ctl->abort = 0;
+    }
+  }
+  if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&ctl->full[s], 1);
       mbar_init(&ctl->empty[s], 1);
