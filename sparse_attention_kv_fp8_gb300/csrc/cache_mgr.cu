@@ -216,6 +216,17 @@ __device__ __forceinline__ bool grid_barrier(uint32_t *glob, int32_t *status, Co
   return S->red[7] != 0;
 }
 
+// Adds a CTA's histogram into the global one.  Every CTA starts at a different
+// 128-byte line, so the 152 CTAs' atomics spread over all lines at once instead of
+// queueing on one line after another.
+__device__ __forceinline__ void hist_flush(const uint32_t *local, uint32_t *global, int cta) {
+  const int start = (cta * 32) & (kHistBins - 1);
+  for (int k = threadIdx.x; k < kHistBins; k += kCoopThreads) {
+    const int i = (k + start) & (kHistBins - 1);
+    if (local[i]) atomicAdd(global + i, local[i]);
+  }
+}
+
 __device__ __forceinline__ void add_stat(echo_stats *st, int64_t echo_stats::*field, unsigned long long v) {
   if (st && v) atomicAdd(reinterpret_cast<unsigned long long *>(&(st->*field)), v);
 }
@@ -523,9 +534,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     if (lane == 0) ECHO_TRACE_LAST_HERE(13);
   }
   __syncthreads();
-  if (P.mode != kModeAlloc)
-    for (int i = threadIdx.x; i < kHistBins; i += kCoopThreads)
-      if (S->hist[i]) atomicAdd(P.ws.hist + i, S->hist[i]);
+  if (P.mode != kModeAlloc) hist_flush(S->hist, P.ws.hist, c);
   if (threadIdx.x == 0 && P.mode != kModeEvict) {
     P.ws.cta[c * kCVals + kCOwn] = S->red[0];
     if (S->red[1]) atomicAdd(glob + kGHits, S->red[1]);
@@ -560,8 +569,9 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     glob[kGValid] = 0;
     glob[kGHits] = 0;
   }
-  // repeats of a missed row exist: their out_slot needs one more grid barrier
-  const bool any_repeats = P.mode == kModeRecall && __ldcg(glob + kGRepeats) != 0;
+  // repeats of a missed row exist: their out_slot needs one more grid barrier (one
+  // thread per CTA reads the count; the scan below hands it to the rest)
+  if (threadIdx.x == 0) S->red[6] = P.mode == kModeRecall ? __ldcg(glob + kGRepeats) : 0u;
   // this thread's segment of the entries; the staging rows of its owned misses
   const int e_cnt = e_hi - e_lo;
   const int e_per = (e_cnt + kCoopThreads - 1) / kCoopThreads;
@@ -586,6 +596,8 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     hist_ex = ex4[2];
     own_ex = ex4[3];
   }
+  const bool any_repeats = S->red[6] != 0;  // written before the scan's barriers
+  ECHO_TRACE_MARK(14);
   int32_t E = 0;
   if (P.mode == kModeEvict) {
     E = *P.evict_n_dev;
@@ -637,8 +649,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
         }
         __syncthreads();
         uint32_t *gl = P.ws.hist + lvl * kHistBins;
-        for (int i = threadIdx.x; i < kHistBins; i += kCoopThreads)
-          if (S->hist[i]) atomicAdd(gl + i, S->hist[i]);
+        hist_flush(S->hist, gl, c);
         if (!grid_barrier(glob, P.status, S)) return;
         uint32_t dd, ab, tt;
         find_from_top(gl, need, dd, ab, tt, S);
@@ -651,6 +662,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     Tp = clock - 1 - static_cast<int32_t>(age_t);
     needT = need;
   }
+  ECHO_TRACE_MARK(15);
   uint32_t my_lt = 0, my_eq = 0, my_fr = 0;  // this CTA's slots older than / at T, free
   // owned misses, in entry order (contiguous per-thread segments), with their sources
   if (P.mode != kModeEvict) {
