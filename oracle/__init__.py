@@ -29,6 +29,7 @@ _lib = None
 
 INF = 2**31 - 1
 POOL_EXHAUSTED, BAD_INDEX, PREFETCH_CAP_HIT = 1, 2, 8
+RESERVED = -2   # priority of a slot set aside for the direct-to-slot prefetch
 
 
 def build(force: bool = False) -> str:
@@ -81,9 +82,11 @@ def lib():
             L.orc_pool_alloc.restype = I
             L.orc_pool_evict.argtypes = [P, I, ctypes.c_int32, P]
             L.orc_pool_evict.restype = I
-            L.orc_prefetch_recall.argtypes = [P, P, P, I, I, I, I, P, P, I, ctypes.c_int32, P, P]
+            L.orc_prefetch_recall.argtypes = [P, P, P, I, I, I, I, P, P, I, ctypes.c_int32, P, P, I, P, P]
             L.orc_prefetch_recall.restype = I
-            L.orc_append.argtypes = [P, P, P, P, I, I, I, P, P, ctypes.c_int32, P]
+            L.orc_append.argtypes = [P, P, P, P, I, I, I, P, P, ctypes.c_int32, P, I, P, P]
+            L.orc_prefetch_direct.argtypes = [P, P, P, I, ctypes.c_int32]
+            L.orc_prefetch_direct.restype = I
             L.orc_append.restype = I
             L.orc_prefetch_candidates.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P, P, P]
             L.orc_prefetch_candidates.restype = None
@@ -260,8 +263,11 @@ class Pool:
             status = lib().orc_pool_evict(ctypes.byref(c), int(n_needed), int(clock), _p(n))
         return int(n[0]), status
 
-    def prefetch_recall(self, sel, req_to_host, clock: int, staged=None, stats: Stats | None = None):
-        """staged: list (per request) of host rows the prefetch staged, or None."""
+    def prefetch_recall(self, sel, req_to_host, clock: int, staged=None, stats: Stats | None = None,
+                        reserve_cap: int = -1):
+        """staged: list (per request) of host rows the prefetch staged, or None.  With
+        reserve_cap >= 0 (direct-to-slot mode) `staged` lists the rows the prefetch put
+        into reserved slots, and the call returns (out_slot, status, next reserve)."""
         sel = _arr(sel, np.int32)
         req_to_host = _arr(req_to_host, np.int32)
         B, n_q, k = sel.shape
@@ -277,24 +283,44 @@ class Pool:
                 srows[b, :len(rows)] = rows
                 scnt[b] = len(rows)
         st = stats if stats is not None else Stats()
+        res = np.full(max(reserve_cap, 1), -1, np.int32)
+        res_n = np.zeros(1, np.int32)
         with self._c() as c:
             status = lib().orc_prefetch_recall(ctypes.byref(c), _p(sel), _p(req_to_host), B, n_q, k, L_max,
                                                _p(srows), _p(scnt), stride, int(clock), _p(out),
-                                               ctypes.byref(st))
+                                               ctypes.byref(st), int(reserve_cap), _p(res), _p(res_n))
+        if reserve_cap >= 0:
+            return out, status, res[:int(res_n[0])].copy()
         return out, status
 
     def append(self, k_index: np.ndarray, ctx_len: np.ndarray, req_to_host, new_kv, new_k_index,
-               clock: int, stats: Stats | None = None):
-        """In place on k_index, ctx_len and the host pool (write-through)."""
+               clock: int, stats: Stats | None = None, reserve_cap: int = -1):
+        """In place on k_index, ctx_len and the host pool (write-through).  With
+        reserve_cap >= 0 the reserve is rebuilt as in prefetch_recall and the call
+        returns (status, next reserve)."""
         req_to_host = _arr(req_to_host, np.int32)
         new_kv = _arr(new_kv, np.uint16)
         new_k_index = _arr(new_k_index, np.uint8)
         B, L_max, D = k_index.shape
         st = stats if stats is not None else Stats()
+        res = np.full(max(reserve_cap, 1), -1, np.int32)
+        res_n = np.zeros(1, np.int32)
         with self._c() as c:
             status = lib().orc_append(ctypes.byref(c), _p(k_index), _p(ctx_len), _p(req_to_host), B, L_max, D,
-                                      _p(new_kv), _p(new_k_index), int(clock), ctypes.byref(st))
+                                      _p(new_kv), _p(new_k_index), int(clock), ctypes.byref(st),
+                                      int(reserve_cap), _p(res), _p(res_n))
+        if reserve_cap >= 0:
+            return status, res[:int(res_n[0])].copy()
         return status
+
+    def prefetch_direct(self, slots, rows, clock: int):
+        """The direct-to-slot prefetch of one step as the GPU assigned it: rows[i] went
+        into reserved slot slots[i].  Returns the status (BAD_INDEX for invalid pairs)."""
+        slots = _arr(slots, np.int32)
+        rows = _arr(rows, np.int32)
+        assert slots.shape == rows.shape
+        with self._c() as c:
+            return lib().orc_prefetch_direct(ctypes.byref(c), _p(slots), _p(rows), slots.size, int(clock))
 
     def metadata(self):
         return dict(free=self.GPUTokenFree.copy(), prio=self.GPUTokenPriority.copy(),
@@ -307,26 +333,61 @@ class Pool:
 # section 4 step list
 # ---------------------------------------------------------------------------
 
+@dataclasses.dataclass
+class Reserve:
+    """Direct-to-slot prefetch state: `cap` slots are set aside per call; `slots` is
+    the current reserve (lowest-index free slots after the last recall or append)."""
+    cap: int
+    slots: np.ndarray = dataclasses.field(default_factory=lambda: np.zeros(0, np.int32))
+
+
 def decode_step(pool: Pool, q, w, k_index, ctx_len, req_to_host, s_hat, k: int, clock: int,
                 stage_stride: int, cap_div: int = 16, alpha: float = 0.5, new_kv=None,
-                new_k_index=None, stats: Stats | None = None, staged=None):
+                new_k_index=None, stats: Stats | None = None, staged=None, reserve: Reserve | None = None,
+                assigned=None):
     """One layer's decode step on the oracle's own state (k_index, ctx_len, s_hat and
     pool are updated in place).  `staged` overrides the modelled prefetch set (the
     GPU's staged rows, for comparing stats); by default the candidate set truncated
-    to the cap in token order is used.  Returns a dict of the step's outputs."""
+    to the cap in token order is used.
+    With `reserve` (direct-to-slot mode) prefetched rows go straight into the reserved
+    slots: `assigned` = (slots, rows) as the GPU's tickets placed them, else the
+    candidates in (request, token) order take the reserve in order; the per-request
+    cap does not apply (the reserve bounds the prefetch).  Returns a dict of the
+    step's outputs."""
     status = 0
     st = stats if stats is not None else Stats()
     if new_kv is not None:
-        status |= pool.append(k_index, ctx_len, req_to_host, new_kv, new_k_index, clock, st)
+        if reserve is not None:
+            s1, reserve.slots = pool.append(k_index, ctx_len, req_to_host, new_kv, new_k_index, clock, st,
+                                            reserve_cap=reserve.cap)
+            status |= s1
+        else:
+            status |= pool.append(k_index, ctx_len, req_to_host, new_kv, new_k_index, clock, st)
     scores = indexer_score(q, w, k_index, ctx_len)
     cand, cap = prefetch_candidates(scores, s_hat, ctx_len, req_to_host, pool.HostTokenToGPU,
                                     stage_stride, cap_div)
-    if staged is None:
-        staged = [np.asarray(req_to_host[b][c[:cap[b]]], np.int32) for b, c in enumerate(cand)]
-    if any(len(c) > cp for c, cp in zip(cand, cap)):
-        status |= PREFETCH_CAP_HIT
-    sel, kth = select_topk(scores, ctx_len, k)
-    out_slot, s2 = pool.prefetch_recall(sel, req_to_host, clock, staged=staged, stats=st)
+    if reserve is not None:
+        B = len(cand)
+        if assigned is None:
+            rows = np.concatenate([np.asarray(req_to_host[b][c], np.int32) for b, c in enumerate(cand)] +
+                                  [np.zeros(0, np.int32)])
+            n = min(rows.size, reserve.slots.size)
+            if rows.size > n:
+                status |= PREFETCH_CAP_HIT
+            assigned = (reserve.slots[:n].copy(), rows[:n])
+        slots_a, rows_a = (_arr(x, np.int32) for x in assigned)
+        status |= pool.prefetch_direct(slots_a, rows_a, clock)
+        staged = [rows_a] + [np.zeros(0, np.int32)] * (B - 1)   # the recall's count needs no request split
+        sel, kth = select_topk(scores, ctx_len, k)
+        out_slot, s2, reserve.slots = pool.prefetch_recall(sel, req_to_host, clock, staged=staged, stats=st,
+                                                           reserve_cap=reserve.cap)
+    else:
+        if staged is None:
+            staged = [np.asarray(req_to_host[b][c[:cap[b]]], np.int32) for b, c in enumerate(cand)]
+        if any(len(c) > cp for c, cp in zip(cand, cap)):
+            status |= PREFETCH_CAP_HIT
+        sel, kth = select_topk(scores, ctx_len, k)
+        out_slot, s2 = pool.prefetch_recall(sel, req_to_host, clock, staged=staged, stats=st)
     status |= s2
     s_hat[...] = ema_update(s_hat, kth, alpha)
     return dict(scores=scores, sel=sel, kth=kth, out_slot=out_slot, status=status, candidates=cand,

@@ -46,6 +46,9 @@
 #include <string.h>
 
 #define ORC_INF INT32_MAX
+/* priority of a slot set aside for the direct-to-slot prefetch: not free, not
+   evictable, not mapped */
+#define ORC_RESERVED (-2)
 
 enum {
     ORC_POOL_EXHAUSTED = 1,
@@ -325,7 +328,7 @@ int orc_pool_evict(orc_pool *P, int n_needed, int32_t clock, int32_t *n_evicted)
     orc_ps *c = (orc_ps *)malloc(sizeof(orc_ps) * (size_t)(P->n_g > 0 ? P->n_g : 1));
     int nc = 0;
     for (int s = 0; s < P->n_g; ++s)
-        if (!P->GPUTokenFree[s] && P->GPUTokenPriority[s] < clock) {
+        if (!P->GPUTokenFree[s] && P->GPUTokenPriority[s] >= 0 && P->GPUTokenPriority[s] < clock) {
             c[nc].prio = P->GPUTokenPriority[s];
             c[nc].slot = s;
             ++nc;
@@ -358,10 +361,78 @@ int orc_pool_evict(orc_pool *P, int n_needed, int32_t clock, int32_t *n_evicted)
     return status;
 }
 
+/*
+ * Direct-to-slot prefetch (the pages' likely landing place for prefetched rows,
+ * section 6.1 with the pool of section 5): a cache-manager call sets aside the
+ * reserve_cap lowest-index slots that are free after it (evicting for them like for
+ * misses, misses first); the next step's prefetch puts rows straight into them.
+ * Reserved slots are neither free nor evictable; the next call in direct mode
+ * returns the ones the prefetch left unused to the free slots before it starts.
+ */
+/* occupied slots that may be evicted at this clock */
+static int orc_evictable(const orc_pool *P, int32_t clock)
+{
+    int n = 0;
+    for (int s = 0; s < P->n_g; ++s)
+        n += !P->GPUTokenFree[s] && P->GPUTokenPriority[s] >= 0 && P->GPUTokenPriority[s] < clock;
+    return n;
+}
+
+static int orc_reserve_release(orc_pool *P)
+{
+    int n = 0;
+    for (int s = 0; s < P->n_g; ++s)
+        if (!P->GPUTokenFree[s] && P->GPUTokenPriority[s] == ORC_RESERVED) {
+            P->GPUTokenFree[s] = 1;
+            P->GPUTokenPriority[s] = -1;
+            P->GPUTokenToHost[s] = ORC_INF;
+            ++n;
+        }
+    P->n_free += n;
+    return n;
+}
+
+static int orc_reserve_take(orc_pool *P, int cap, int32_t *list)
+{
+    int n = 0;
+    for (int s = 0; s < P->n_g && n < cap; ++s)
+        if (P->GPUTokenFree[s]) {
+            P->GPUTokenFree[s] = 0;
+            P->GPUTokenPriority[s] = ORC_RESERVED;
+            list[n++] = s;
+        }
+    P->n_free -= n;
+    return n;
+}
+
 /* copy one latent-KV row host -> GPU pool */
 static void copy_row(orc_pool *P, int32_t slot, const uint16_t *src)
 {
     memcpy(P->gpu_kv + (size_t)slot * P->row_elems, src, sizeof(uint16_t) * (size_t)P->row_elems);
+}
+
+/*
+ * The direct-to-slot prefetch of one step, as the GPU's racing tickets assigned it:
+ * rows[i] went into slots[i].  Each slot must be reserved and each row a distinct
+ * non-resident host row (else BAD_INDEX and the pair is skipped).  The row becomes
+ * resident with priority clock (fetched this step) and its bytes are copied.
+ */
+int orc_prefetch_direct(orc_pool *P, const int32_t *slots, const int32_t *rows, int n, int32_t clock)
+{
+    int status = 0;
+    for (int i = 0; i < n; ++i) {
+        int32_t s = slots[i], h = rows[i];
+        if (s < 0 || s >= P->n_g || P->GPUTokenFree[s] || P->GPUTokenPriority[s] != ORC_RESERVED ||
+            h < 0 || h >= P->n_h || P->HostTokenToGPU[h] != ORC_INF) {
+            status |= ORC_BAD_INDEX;
+            continue;
+        }
+        P->GPUTokenPriority[s] = clock;
+        P->GPUTokenToHost[s] = h;
+        P->HostTokenToGPU[h] = s;
+        copy_row(P, s, P->host_kv + (size_t)h * P->row_elems);
+    }
+    return status;
 }
 
 /*
@@ -377,11 +448,20 @@ static void copy_row(orc_pool *P, int32_t slot, const uint16_t *src)
  *         that found no slot.
  * staged_rows[b*stage_stride + i], i < staged_count[b]: host rows the prefetch
  * staged for request b this step (may be NULL).
+ * reserve_cap >= 0 selects direct-to-slot mode: the rows listed in staged_rows are
+ * the ones this step's prefetch already put into reserved slots (they are hits, and
+ * staged_used counts those selected); before (iii) the reserve left unused returns
+ * to the free slots, (iii) evicts for the misses plus reserve_cap more slots (as far
+ * as evictable slots go: a short reserve is no exhaustion), and after (iv) the
+ * reserve_cap lowest-index free slots become the next reserve, listed in
+ * reserve_out (count in *reserve_n_out).  reserve_cap < 0: reserved slots are left
+ * as they are (neither free nor evictable).
  */
 int orc_prefetch_recall(orc_pool *P, const int32_t *sel, const int32_t *req_to_host, int B,
                         int n_q, int k, int L_max, const int32_t *staged_rows,
                         const int32_t *staged_count, int stage_stride, int32_t clock,
-                        int32_t *out_slot, orc_stats *st)
+                        int32_t *out_slot, orc_stats *st, int reserve_cap, int32_t *reserve_out,
+                        int32_t *reserve_n_out)
 {
     int status = 0;
     size_t F = (size_t)B * n_q * k;
@@ -390,6 +470,20 @@ int orc_prefetch_recall(orc_pool *P, const int32_t *sel, const int32_t *req_to_h
     int32_t *miss_req = (int32_t *)malloc(sizeof(int32_t) * (F > 0 ? F : 1));
     int n_miss = 0;
     int64_t n_sel = 0, n_unique = 0, n_hits = 0;
+
+    /* direct-to-slot mode: the rows this step's prefetch put into slots (any request) */
+    const int direct = reserve_cap >= 0;
+    uint8_t *pref = NULL;
+    int64_t used_hits = 0;
+    if (direct && staged_rows && staged_count) {
+        pref = (uint8_t *)calloc((size_t)P->n_h, 1);
+        for (int b = 0; b < B; ++b)
+            for (int t = 0; t < staged_count[b]; ++t) {
+                int32_t h = staged_rows[(size_t)b * stage_stride + t];
+                if (h >= 0 && h < P->n_h)
+                    pref[h] = 1;
+            }
+    }
 
     /* (i) + (ii) */
     for (size_t f = 0; f < F; ++f) {
@@ -415,6 +509,8 @@ int orc_prefetch_recall(orc_pool *P, const int32_t *sel, const int32_t *req_to_h
         if (g != ORC_INF) {
             ++n_hits;
             P->GPUTokenPriority[g] = clock;
+            if (pref && pref[h])
+                ++used_hits;  /* a miss the direct prefetch turned into a hit */
         } else {
             miss[n_miss] = h;
             miss_req[n_miss] = b;
@@ -422,16 +518,29 @@ int orc_prefetch_recall(orc_pool *P, const int32_t *sel, const int32_t *req_to_h
         }
     }
     free(seen);
+    free(pref);
 
-    /* (iii) */
+    /* (iii); in direct-to-slot mode the unused reserve returns to the free slots and
+       the evictions also cover the next reserve */
+    if (direct)
+        orc_reserve_release(P);
     int32_t n_ev = 0;
-    int need = n_miss - P->n_free;
+    int need = n_miss + (direct ? reserve_cap : 0) - P->n_free;
+    if (direct) {  /* a short reserve is not an exhaustion: only misses left out are */
+        int nc = orc_evictable(P, clock);
+        need = need < nc ? need : nc;
+    }
     if (need > 0)
         status |= orc_pool_evict(P, need, clock, &n_ev);
 
     /* (iv) */
     int32_t *slots = (int32_t *)malloc(sizeof(int32_t) * (size_t)(n_miss > 0 ? n_miss : 1));
     status |= orc_pool_alloc(P, miss, n_miss, clock, NULL, slots);
+    if (direct) {
+        int nr = orc_reserve_take(P, reserve_cap, reserve_out);
+        if (reserve_n_out)
+            *reserve_n_out = nr;
+    }
 
     /* (v) */
     int64_t recalled = 0, used = 0, staged_total = 0;
@@ -440,7 +549,7 @@ int orc_prefetch_recall(orc_pool *P, const int32_t *sel, const int32_t *req_to_h
             continue;
         ++recalled;
         copy_row(P, slots[i], P->host_kv + (size_t)miss[i] * P->row_elems);
-        if (staged_rows && staged_count) {
+        if (!direct && staged_rows && staged_count) {
             int b = miss_req[i];
             for (int t = 0; t < staged_count[b]; ++t)
                 if (staged_rows[(size_t)b * stage_stride + t] == miss[i]) {
@@ -477,7 +586,7 @@ int orc_prefetch_recall(orc_pool *P, const int32_t *sel, const int32_t *req_to_h
         st->unrecalled += n_miss - recalled;
         st->evicted += n_ev;
         st->staged += staged_total;
-        st->staged_used += used;
+        st->staged_used += direct ? used_hits : used;
     }
     free(slots);
     free(miss);
@@ -495,7 +604,8 @@ int orc_prefetch_recall(orc_pool *P, const int32_t *sel, const int32_t *req_to_h
  */
 int orc_append(orc_pool *P, uint8_t *k_index, int32_t *ctx_len, const int32_t *req_to_host,
                int B, int L_max, int D, const uint16_t *new_kv, const uint8_t *new_k_index,
-               int32_t clock, orc_stats *st)
+               int32_t clock, orc_stats *st, int reserve_cap, int32_t *reserve_out,
+               int32_t *reserve_n_out)
 {
     int status = 0;
     int32_t *rows = (int32_t *)malloc(sizeof(int32_t) * (size_t)(B > 0 ? B : 1));
@@ -530,12 +640,24 @@ int orc_append(orc_pool *P, uint8_t *k_index, int32_t *ctx_len, const int32_t *r
         src[n] = b;
         ++n;
     }
+    const int direct = reserve_cap >= 0;
+    if (direct)
+        orc_reserve_release(P);
     int32_t n_ev = 0;
-    int need = n - P->n_free;
+    int need = n + (direct ? reserve_cap : 0) - P->n_free;
+    if (direct) {
+        int nc = orc_evictable(P, clock);
+        need = need < nc ? need : nc;
+    }
     if (need > 0)
         status |= orc_pool_evict(P, need, clock, &n_ev);
     int32_t *slots = (int32_t *)malloc(sizeof(int32_t) * (size_t)(n > 0 ? n : 1));
     status |= orc_pool_alloc(P, rows, n, clock, NULL, slots);
+    if (direct) {
+        int nr = orc_reserve_take(P, reserve_cap, reserve_out);
+        if (reserve_n_out)
+            *reserve_n_out = nr;
+    }
     for (int i = 0; i < n; ++i)
         if (slots[i] >= 0)
             copy_row(P, slots[i], new_kv + (size_t)src[i] * P->row_elems);
