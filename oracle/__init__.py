@@ -84,7 +84,7 @@ def lib():
             L.orc_pool_evict.restype = I
             L.orc_prefetch_recall.argtypes = [P, P, P, I, I, I, I, P, P, I, ctypes.c_int32, P, P, I, P, P]
             L.orc_prefetch_recall.restype = I
-            L.orc_append.argtypes = [P, P, P, P, I, I, I, P, P, ctypes.c_int32, P, I, P, P]
+            L.orc_append.argtypes = [P, P, P, P, I, I, I, P, P, ctypes.c_int32, P]
             L.orc_prefetch_direct.argtypes = [P, P, P, I, ctypes.c_int32]
             L.orc_prefetch_direct.restype = I
             L.orc_append.restype = I
@@ -294,23 +294,17 @@ class Pool:
         return out, status
 
     def append(self, k_index: np.ndarray, ctx_len: np.ndarray, req_to_host, new_kv, new_k_index,
-               clock: int, stats: Stats | None = None, reserve_cap: int = -1):
-        """In place on k_index, ctx_len and the host pool (write-through).  With
-        reserve_cap >= 0 the reserve is rebuilt as in prefetch_recall and the call
-        returns (status, next reserve)."""
+               clock: int, stats: Stats | None = None):
+        """In place on k_index, ctx_len and the host pool (write-through).  Reserved
+        slots (direct-to-slot prefetch) are left as they are."""
         req_to_host = _arr(req_to_host, np.int32)
         new_kv = _arr(new_kv, np.uint16)
         new_k_index = _arr(new_k_index, np.uint8)
         B, L_max, D = k_index.shape
         st = stats if stats is not None else Stats()
-        res = np.full(max(reserve_cap, 1), -1, np.int32)
-        res_n = np.zeros(1, np.int32)
         with self._c() as c:
             status = lib().orc_append(ctypes.byref(c), _p(k_index), _p(ctx_len), _p(req_to_host), B, L_max, D,
-                                      _p(new_kv), _p(new_k_index), int(clock), ctypes.byref(st),
-                                      int(reserve_cap), _p(res), _p(res_n))
-        if reserve_cap >= 0:
-            return status, res[:int(res_n[0])].copy()
+                                      _p(new_kv), _p(new_k_index), int(clock), ctypes.byref(st))
         return status
 
     def prefetch_direct(self, slots, rows, clock: int):
@@ -335,8 +329,8 @@ class Pool:
 
 @dataclasses.dataclass
 class Reserve:
-    """Direct-to-slot prefetch state: `cap` slots are set aside per call; `slots` is
-    the current reserve (lowest-index free slots after the last recall or append)."""
+    """Direct-to-slot prefetch state: each recall sets aside `cap` slots; `slots` is
+    the current reserve (the lowest-index free slots after the last recall)."""
     cap: int
     slots: np.ndarray = dataclasses.field(default_factory=lambda: np.zeros(0, np.int32))
 
@@ -357,12 +351,7 @@ def decode_step(pool: Pool, q, w, k_index, ctx_len, req_to_host, s_hat, k: int, 
     status = 0
     st = stats if stats is not None else Stats()
     if new_kv is not None:
-        if reserve is not None:
-            s1, reserve.slots = pool.append(k_index, ctx_len, req_to_host, new_kv, new_k_index, clock, st,
-                                            reserve_cap=reserve.cap)
-            status |= s1
-        else:
-            status |= pool.append(k_index, ctx_len, req_to_host, new_kv, new_k_index, clock, st)
+        status |= pool.append(k_index, ctx_len, req_to_host, new_kv, new_k_index, clock, st)
     scores = indexer_score(q, w, k_index, ctx_len)
     cand, cap = prefetch_candidates(scores, s_hat, ctx_len, req_to_host, pool.HostTokenToGPU,
                                     stage_stride, cap_div)

@@ -363,11 +363,12 @@ int orc_pool_evict(orc_pool *P, int n_needed, int32_t clock, int32_t *n_evicted)
 
 /*
  * Direct-to-slot prefetch (the pages' likely landing place for prefetched rows,
- * section 6.1 with the pool of section 5): a cache-manager call sets aside the
- * reserve_cap lowest-index slots that are free after it (evicting for them like for
- * misses, misses first); the next step's prefetch puts rows straight into them.
- * Reserved slots are neither free nor evictable; the next call in direct mode
- * returns the ones the prefetch left unused to the free slots before it starts.
+ * section 6.1 with the pool of section 5): a recall sets aside the reserve_cap
+ * lowest-index slots that are free after it (evicting for them like for misses,
+ * misses first); the next step's prefetch puts rows straight into them.  Reserved
+ * slots are neither free nor evictable (allocate, evict and append leave them
+ * alone); the next recall in direct mode returns the ones the prefetch left unused
+ * to the free slots before it starts.
  */
 /* occupied slots that may be evicted at this clock */
 static int orc_evictable(const orc_pool *P, int32_t clock)
@@ -604,8 +605,7 @@ int orc_prefetch_recall(orc_pool *P, const int32_t *sel, const int32_t *req_to_h
  */
 int orc_append(orc_pool *P, uint8_t *k_index, int32_t *ctx_len, const int32_t *req_to_host,
                int B, int L_max, int D, const uint16_t *new_kv, const uint8_t *new_k_index,
-               int32_t clock, orc_stats *st, int reserve_cap, int32_t *reserve_out,
-               int32_t *reserve_n_out)
+               int32_t clock, orc_stats *st)
 {
     int status = 0;
     int32_t *rows = (int32_t *)malloc(sizeof(int32_t) * (size_t)(B > 0 ? B : 1));
@@ -640,24 +640,11 @@ int orc_append(orc_pool *P, uint8_t *k_index, int32_t *ctx_len, const int32_t *r
         src[n] = b;
         ++n;
     }
-    const int direct = reserve_cap >= 0;
-    if (direct)
-        orc_reserve_release(P);
     int32_t n_ev = 0;
-    int need = n + (direct ? reserve_cap : 0) - P->n_free;
-    if (direct) {
-        int nc = orc_evictable(P, clock);
-        need = need < nc ? need : nc;
-    }
-    if (need > 0)
-        status |= orc_pool_evict(P, need, clock, &n_ev);
+    if (n > P->n_free)
+        status |= orc_pool_evict(P, n - P->n_free, clock, &n_ev);
     int32_t *slots = (int32_t *)malloc(sizeof(int32_t) * (size_t)(n > 0 ? n : 1));
     status |= orc_pool_alloc(P, rows, n, clock, NULL, slots);
-    if (direct) {
-        int nr = orc_reserve_take(P, reserve_cap, reserve_out);
-        if (reserve_n_out)
-            *reserve_n_out = nr;
-    }
     for (int i = 0; i < n; ++i)
         if (slots[i] >= 0)
             copy_row(P, slots[i], new_kv + (size_t)src[i] * P->row_elems);

@@ -3,9 +3,9 @@
 The ECHO review (marsggbo.github.io, "OSDI'26 | ECHO", section 6.1 with the pool of
 section 5) has the prefetch copy rows into the GPU pool while scoring runs; read
 literally, prefetched rows take real slots.  The oracle models that with a reserve:
-a recall or append sets aside the lowest-index free slots left after its own
-allocation (evicting for them like for misses), the next step's prefetch fills
-them, the rows become resident, and the next call returns what was left unused.
+a recall sets aside the lowest-index free slots left after its own allocation
+(evicting for them like for misses), the next step's prefetch fills them, the rows
+become resident, and the next recall returns what was left unused.
 Each test below derives the expected pool from the definitions by brute force
 (sorted lists, sets), not from the oracle's own code.
 """
@@ -167,7 +167,7 @@ def test_invalid_prefetch_pairs_are_flagged_and_skipped():
     assert P.HostTokenToGPU[absent[1]] == reserve[0] and P.GPUTokenPriority[reserve[1]] == oracle.RESERVED
 
 
-def test_append_rebuilds_the_reserve():
+def test_append_leaves_the_reserve_alone():
     B, L_max, n_g = 2, 16, 10
     n_h = B * L_max
     P = oracle.Pool.empty(n_g, n_h, _host(n_h, 5))
@@ -175,21 +175,14 @@ def test_append_rebuilds_the_reserve():
     ctx = np.array([3, 5], np.int32)
     r2h = wl.req_to_host(B, L_max)
     P.alloc(np.array([10, 11, 12, 13, 14, 15, 28, 29], np.int32), clock=1)   # slots 0..7, rows no append touches
+    sel = np.full((B, 1, 4), -1, np.int32)
+    _, status, reserve = P.prefetch_recall(sel, r2h, clock=2, reserve_cap=3)
+    # two free slots (8, 9) and one eviction (slot 0, the lowest of the priority-1 slots)
+    assert status == 0 and reserve.tolist() == [0, 8, 9] and P.n_free == 0
     kv, kn = wl.new_tokens(B, 1, 0)
-    status, reserve = P.append(kI, ctx, r2h, kv, kn, clock=4, reserve_cap=3)
-    # 2 new rows + 3 reserved = 5 slots; 2 free (8, 9) -> 3 evicted, the oldest (0, 1, 2)
-    assert status == 0
-    assert P.HostTokenToGPU[r2h[0, 3]] == 0 and P.HostTokenToGPU[r2h[1, 5]] == 1
-    assert reserve.tolist() == [2, 8, 9] and P.n_free == 0
-    check_invariants_with_reserve(P, reserve, bytes_too=False)
-    kv, kn = wl.new_tokens(B, 1, 1)
-    status, reserve = P.append(kI, ctx, r2h, kv, kn, clock=5, reserve_cap=3)
-    # the old reserve returns first (2, 8, 9 free), 2 + 3 slots are needed, so the 2
-    # oldest occupied slots go (3, 4: priority 1); the new rows take the lowest free
-    # slots (2, 3) and the reserve the next three (4, 8, 9)
-    assert status == 0 and reserve.tolist() == [4, 8, 9]
-    assert P.HostTokenToGPU[r2h[0, 4]] == 2 and P.HostTokenToGPU[r2h[1, 6]] == 3
-    assert P.HostTokenToGPU[13] == oracle.INF and P.HostTokenToGPU[14] == oracle.INF
+    status = P.append(kI, ctx, r2h, kv, kn, clock=4)
+    # the new rows evict the two oldest occupied slots (1, 2) instead of taking reserved ones
+    assert status == 0 and P.HostTokenToGPU[r2h[0, 3]] == 1 and P.HostTokenToGPU[r2h[1, 5]] == 2
     check_invariants_with_reserve(P, reserve, bytes_too=False)
 
 
