@@ -399,6 +399,10 @@ def run_ours(args):
     h2d_gbs = (256 << 20) / (best * 1e-3) / 1e9
     recall_probe = recall_bandwidth_probe(echo, torch, host_t, flush_l2)
     volume_probe = indexer_volume_probe(echo, torch, inp, flush_l2, hbm_peak)
+    direct = None
+    if args.reserve > 0:
+        direct = direct_to_slot_leg(echo, torch, st, host_t, q_ring, w, k_index, ctx, r2h_t, flush_l2,
+                                    args.warmup, args.steps, n_stage, args.reserve)
 
     # ---- roofline of the dominant kernel (the indexer) ----
     idx_ms = float(np.mean(stage_ms["indexer"]))
@@ -429,6 +433,8 @@ def run_ours(args):
         "recalled_rows_per_step": recalled_rows / args.steps,
         "staged_rows_per_step": st_vals["staged"] / args.steps,
         "staged_used_per_step": st_vals["staged_used"] / args.steps,
+        "evicted_per_step": st_vals["evicted"] / args.steps,
+        "direct_to_slot": direct,
         "stage_ms": {k: float(np.mean(v)) for k, v in stage_ms.items()},
         "stage_ms_note": f"from {n_stage} further steps replayed with stage events ({float(np.mean(staged_total_ms)):.4f} ms/step with the events)",
         "recall": {"bytes_per_step": recalled_rows / args.steps * 1152, "ms": recall_ms,
@@ -453,6 +459,79 @@ def run_ours(args):
     if pg:
         pg.destroy_process_group()
     return 0
+
+
+def direct_to_slot_leg(echo, torch, st, host_t, q_ring, w, k_index, ctx, r2h_t, flush_l2, warmup, n_timed, n_stage,
+                       reserve):
+    """The same steps (same start state, same queries) with the direct-to-slot
+    prefetch: rows land in `reserve` slots each recall sets aside, instead of the
+    staging area.  Whole steps and the per-stage split, timed as in the main loop."""
+    pool = echo.Pool(N_G, host_t)
+    pool.load_state(st)
+    ws = echo.Workspace(N_G, B * K_TOP)
+    stage = echo.Stage(B, reserve=reserve)
+    out = echo.StepBuffers(B, 1, L, K_TOP)
+    stats = echo.Stats()
+    s_hat = torch.full((B, 1), float("inf"), dtype=torch.float32, device="cuda")
+    clock = torch.tensor([T0], dtype=torch.int32, device="cuda")
+
+    def args_for(t, events=None):
+        return echo.make_step_args(pool, ws, q_ring[t], w, k_index, ctx, r2h_t, K_TOP, out, stage=stage,
+                                   s_hat=s_hat, clock_dev=clock, advance_clock=True, stats=stats, events=events)
+
+    steps = warmup + n_timed
+    echo.echo_decode_step(args_for(0))
+    torch.cuda.synchronize()
+    graphs, evs, keep = {}, {}, []
+    cap = torch.cuda.Stream()
+    for t in range(1, steps + n_stage):
+        e = None
+        if t >= steps:
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(echo.NUM_STAGES + 1)]
+            for x in e:
+                x.record()
+        a = args_for(t, events=e)
+        g = torch.cuda.CUDAGraph()
+        cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                echo.echo_decode_step(a)
+        torch.cuda.current_stream().wait_stream(cap)
+        graphs[t], evs[t] = g, e
+        keep.append(a)
+    for t in range(1, warmup):
+        flush_l2()
+        graphs[t].replay()
+    torch.cuda.synchronize()
+    stats.t.zero_()
+    out.dev_status.zero_()
+
+    def loop(ts):
+        a = [torch.cuda.Event(enable_timing=True) for _ in ts]
+        b = [torch.cuda.Event(enable_timing=True) for _ in ts]
+        for i, t in enumerate(ts):
+            flush_l2()
+            a[i].record()
+            graphs[t].replay()
+            b[i].record()
+        torch.cuda.synchronize()
+        return [x.elapsed_time(y) for x, y in zip(a, b)]
+
+    ms = loop(list(range(warmup, steps)))
+    sv = stats.as_dict()
+    status = int(out.dev_status.item())
+    st_steps = list(range(steps, steps + n_stage))
+    loop(st_steps)
+    stage_ms = {name: float(np.mean([evs[t][i].elapsed_time(evs[t][i + 1]) for t in st_steps]))
+                for i, name in enumerate(("append", "indexer", "topk", "recall", "ema"))}
+    per = float(np.mean(ms))
+    return {"reserve_slots": reserve, "value": 1e3 / per, "unit": "steps/s", "ms_per_step": per,
+            "hit_rate": sv["hits"] / max(1, sv["unique_rows"]),
+            "recalled_rows_per_step": sv["recalled"] / n_timed,
+            "prefetched_rows_per_step": sv["staged"] / n_timed,
+            "prefetched_selected_per_step": sv["staged_used"] / n_timed,
+            "evicted_per_step": sv["evicted"] / n_timed,
+            "stage_ms": stage_ms, "dev_status": status}
 
 
 def warm_host_translations(echo, torch, host_t, page_bytes=65536):
@@ -582,6 +661,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-requests", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--reserve", type=int, default=8192,
+                    help="slots per recall for the direct-to-slot comparison leg (0: skip the leg)")
     ap.add_argument("--kernel", default=None, choices=[None, "indexer"],
                     help="run one kernel on a small case (for profilers) instead of the benchmark")
     ap.add_argument("--B", type=int, default=24)

@@ -47,7 +47,8 @@ extern "C" {
 #define ECHO_DEV_POOL_EXHAUSTED 1   /* too few evictable slots: rows left out   */
 #define ECHO_DEV_BAD_INDEX 2        /* an index outside its array was skipped   */
 #define ECHO_DEV_WAIT_TIMEOUT 4     /* a pipeline wait gave up (kernel aborted) */
-#define ECHO_DEV_PREFETCH_CAP_HIT 8 /* info: prefetch candidates exceeded the cap */
+#define ECHO_DEV_PREFETCH_CAP_HIT 8 /* info: prefetch candidates exceeded the cap
+                                       (staging) or the reserve (direct to slot) */
 
 #define ECHO_INF 0x7fffffff
 #define ECHO_H_INDEX 64      /* indexer heads            */
@@ -102,10 +103,12 @@ typedef struct echo_workspace {
 /*
  * Cumulative counters (device memory, int64 each; the caller zeroes them).
  * selected/unique_rows/hits/misses count the selected rows of a recall (hits and
- * misses after de-duplication, residency at step start); recalled = misses that
- * got a slot; unrecalled = misses left out (pool exhausted); evicted = slots freed;
- * staged = rows the prefetch copied; staged_used = recalled rows taken from the
- * staging area; appended = tokens written through by append.
+ * misses after de-duplication, residency when the recall starts: a row the
+ * direct-to-slot prefetch placed is a hit); recalled = misses that got a slot;
+ * unrecalled = misses left out (pool exhausted); evicted = slots freed; staged =
+ * rows the prefetch copied; staged_used = recalled rows taken from the staging
+ * area (staging) or prefetched rows that were selected (direct to slot); appended
+ * = tokens written through by append.
  */
 typedef struct echo_stats {
     int64_t steps, selected, unique_rows, hits, misses, recalled, unrecalled, evicted,
@@ -113,8 +116,11 @@ typedef struct echo_stats {
 } echo_stats;
 
 /*
- * Prefetch staging area (section 6.1 intra-query prefetch; the page leaves the
- * landing place of prefetched rows open, this library stages them in HBM):
+ * Where the fused prefetch puts rows (section 6.1 intra-query prefetch; the page
+ * leaves the landing place open).  Two modes:
+ *
+ * Staging (reserve == NULL): a staging area in HBM; the recall copies the staged
+ * rows that were selected into their slots, the rest are dropped.
  *   rows        [B][stride][576] bf16 device
  *   host_row    [B][stride] int32 device  host row held by each staged row
  *   count       [B] int32 device          prefetch counter of each request; must
@@ -123,6 +129,27 @@ typedef struct echo_stats {
  *   stride      rows reserved per request
  *   cap_div     request b stages at most min(stride, ceil(ctx_len[b] / cap_div))
  *               rows (cap proportional to the context length)
+ *
+ * Direct to slot (reserve != NULL): prefetched rows go straight into GPU-pool slots
+ * that the previous recall set aside, and stay resident whether selected or not.
+ * Reserved slots have gpu_token_free = 0, gpu_token_priority = -2 and no host row;
+ * allocate, evict and append leave them alone.  Each prefetched row takes the next
+ * ticket of reserve_ctl[0]; ticket t < reserve_ctl[1] puts it into slot reserve[t]
+ * (host_token_to_gpu is claimed with a compare-and-swap, so a row is placed once).
+ * A recall with this stage then counts the filled slots (stats staged; the
+ * selected ones in staged_used), gives the unselected ones priority = clock,
+ * returns the unused reserve to the free slots, evicts for its misses plus
+ * reserve_cap more slots (as far as evictable slots go), and sets aside the
+ * reserve_cap lowest-index free slots left after its allocation as the next
+ * reserve.  A recall with reserve_cap = 0 returns the whole reserve.  An indexer
+ * call with a direct stage must be followed by a recall with the same stage.
+ *   reserve     int32 device, as long as the largest reserve_cap used with it:
+ *               the reserved slots, in ticket order
+ *   reserve_ctl [2] int32 device   [0] tickets drawn, [1] reserve length; zero both
+ *                                  before first use
+ *   reserve_cap slots each recall sets aside (0 <= reserve_cap <= n_g); may change
+ *               between recalls
+ *   count       may be NULL; rows, host_row, stride and cap_div are not used
  */
 typedef struct echo_stage {
     uint16_t *rows;
@@ -130,6 +157,9 @@ typedef struct echo_stage {
     int32_t *count;
     int32_t stride;
     int32_t cap_div;
+    int32_t *reserve;
+    int32_t *reserve_ctl;
+    int32_t reserve_cap;
 } echo_stage;
 
 /*
@@ -147,9 +177,11 @@ typedef struct echo_stage {
  * Fused prefetch (enabled when s_hat != NULL; section 6.1): a token whose score
  * exceeds s_hat[b][j] for some j and whose host row req_to_host[b][p] is not
  * resident takes a ticket from stage->count[b]; tickets below the cap copy the
- * host row into stage->rows[b][ticket] and record it in stage->host_row.  The
- * prefetch never changes what is selected.  Needs pool (read-only here),
- * req_to_host [B][L_max] int32 device, stage.
+ * host row into stage->rows[b][ticket] and record it in stage->host_row.  With a
+ * direct-to-slot stage the row goes into the next reserved slot instead (see
+ * echo_stage) and the pool's maps are updated.  The prefetch never changes what
+ * is selected.  Needs pool (read-only in staging mode), req_to_host [B][L_max]
+ * int32 device, stage.
  */
 typedef struct echo_indexer_args {
     const uint8_t *q;
@@ -339,7 +371,7 @@ int echo_selftest_wait_timeout(int32_t which, int32_t *dev_status, void *stream)
 /* Description of the calling thread's last error ("" if none). */
 const char *echo_last_error_string(void);
 
-/* Library version, (major << 16) | minor. */
+/* Library version, (major << 16) | minor (1.1: echo_stage's direct-to-slot fields). */
 int32_t echo_version(void);
 
 /* Storage law of the metadata arrays of one pool (section 5.1): 4*n_h + 13*n_g. */

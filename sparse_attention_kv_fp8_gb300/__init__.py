@@ -48,7 +48,8 @@ class c_workspace(ctypes.Structure):
 
 
 class c_stage(ctypes.Structure):
-    _fields_ = [("rows", _P), ("host_row", _P), ("count", _P), ("stride", _I32), ("cap_div", _I32)]
+    _fields_ = [("rows", _P), ("host_row", _P), ("count", _P), ("stride", _I32), ("cap_div", _I32),
+                ("reserve", _P), ("reserve_ctl", _P), ("reserve_cap", _I32)]
 
 
 class c_indexer_args(ctypes.Structure):
@@ -198,12 +199,40 @@ class Workspace:
 
 
 class Stage:
-    def __init__(self, B: int, stride: int, cap_div: int = 16, device="cuda"):
-        self.rows = torch.zeros((B, stride, KV_ELEMS), dtype=torch.int16, device=device)
-        self.host_row = torch.full((B, stride), -1, dtype=torch.int32, device=device)
-        self.count = torch.zeros(B, dtype=torch.int32, device=device)
+    """Where the prefetch puts rows: a staging area of `stride` rows per request, or,
+    with reserve=R, straight into R GPU-pool slots each recall sets aside (direct to
+    slot; the staging buffers are not allocated then)."""
+
+    def __init__(self, B: int, stride: int = 1, cap_div: int = 16, device="cuda", reserve: int | None = None):
+        self.direct = reserve is not None
         self.stride, self.cap_div = int(stride), int(cap_div)
-        self.c = c_stage(_ptr(self.rows), _ptr(self.host_row), _ptr(self.count), self.stride, self.cap_div)
+        self.count = torch.zeros(B, dtype=torch.int32, device=device)
+        if self.direct:
+            self.rows = self.host_row = None
+            self.reserve_cap = int(reserve)
+            self.reserve = torch.full((max(self.reserve_cap, 1),), -1, dtype=torch.int32, device=device)
+            self.reserve_ctl = torch.zeros(2, dtype=torch.int32, device=device)
+            self.c = c_stage(None, None, _ptr(self.count), self.stride, self.cap_div, _ptr(self.reserve),
+                             _ptr(self.reserve_ctl), self.reserve_cap)
+        else:
+            self.rows = torch.zeros((B, stride, KV_ELEMS), dtype=torch.int16, device=device)
+            self.host_row = torch.full((B, stride), -1, dtype=torch.int32, device=device)
+            self.reserve = self.reserve_ctl = None
+            self.reserve_cap = 0
+            self.c = c_stage(_ptr(self.rows), _ptr(self.host_row), _ptr(self.count), self.stride, self.cap_div,
+                             None, None, 0)
+
+    def set_reserve_cap(self, R: int):
+        """Slots each recall sets aside from now on (at most the capacity allocated)."""
+        if not self.direct or not 0 <= R <= self.reserve.numel():
+            raise EchoError(f"reserve_cap {R} outside [0, {self.reserve.numel()}] or stage not direct")
+        self.reserve_cap = int(R)
+        self.c.reserve_cap = int(R)
+
+    def reserved_slots(self):
+        """The current reserve (direct to slot), as a numpy array."""
+        n = int(self.reserve_ctl[1])
+        return self.reserve[:n].cpu().numpy()
 
 
 class Stats:
@@ -304,7 +333,8 @@ class StepBuffers:
     """Device outputs of one decode step for B requests, n_q queries, k."""
 
     def __init__(self, B: int, n_q: int, L_max: int, k: int, device="cuda"):
-        self.scores = torch.empty((B, n_q, L_max), dtype=torch.float32, device=device)
+        # entries past each row's context are never written: NaN marks them
+        self.scores = torch.full((B, n_q, L_max), float("nan"), dtype=torch.float32, device=device)
         self.sel = torch.empty((B, n_q, k), dtype=torch.int32, device=device)
         self.kth = torch.empty((B, n_q), dtype=torch.float32, device=device)
         self.out_slot = torch.empty((B, n_q, k), dtype=torch.int32, device=device)

@@ -122,7 +122,13 @@ static int check_ws(const echo_workspace *w, const echo_pool *p, long long rows)
   return ECHO_OK;
 }
 
-static int check_stage(const echo_stage *st) {
+static int check_stage(const echo_stage *st, const echo_pool *pool) {
+  if (st->reserve) {  // direct to slot
+    REQUIRE(st->reserve_ctl, "direct-to-slot stage without reserve_ctl");
+    REQUIRE(st->reserve_cap >= 0 && st->reserve_cap <= pool->n_g,
+            "reserve_cap must be in [0, n_g] (got %d, n_g %d)", st->reserve_cap, pool->n_g);
+    return ECHO_OK;
+  }
   REQUIRE(st->rows && st->host_row && st->count, "stage pointer is NULL");
   REQUIRE(aligned(st->rows, 16), "stage rows must be 16-byte aligned");
   REQUIRE(st->stride > 0 && st->cap_div > 0, "stage stride and cap_div must be positive");
@@ -139,7 +145,7 @@ int echo_selftest_wait_timeout(int32_t which, int32_t *dev_status, void *stream)
   return launch_wait_probe(which, dev_status, static_cast<cudaStream_t>(stream));
 }
 
-int32_t echo_version(void) { return (1 << 16) | 0; }
+int32_t echo_version(void) { return (1 << 16) | 1; }
 
 int64_t echo_metadata_bytes(int64_t n_h, int64_t n_g) {
   return static_cast<int64_t>(sizeof(int32_t)) * n_h +
@@ -158,8 +164,9 @@ int echo_indexer_score(const echo_indexer_args *a, void *stream) {
   if (a->s_hat) {
     REQUIRE(a->req_to_host && a->pool && a->stage, "prefetch needs req_to_host, pool and stage");
     TRY(check_pool(a->pool));
-    TRY(check_stage(a->stage));
-    REQUIRE(static_cast<long long>(a->B) * a->stage->stride <= (1ll << 31) - 1, "stage too large");
+    TRY(check_stage(a->stage, a->pool));
+    REQUIRE(a->stage->reserve || static_cast<long long>(a->B) * a->stage->stride <= (1ll << 31) - 1,
+            "stage too large");
   }
   if (a->B == 0 || a->L_max == 0) return ECHO_OK;
   return launch_indexer(a, static_cast<cudaStream_t>(stream));
@@ -236,7 +243,7 @@ int echo_prefetch_recall(const echo_pool *pool, const echo_workspace *ws, const 
   const long long F = static_cast<long long>(B) * n_q * k;
   REQUIRE(F <= (1ll << 30), "B * n_q * k too large");
   TRY(check_ws(ws, pool, F));
-  if (stage) TRY(check_stage(stage));
+  if (stage) TRY(check_stage(stage, pool));
   return launch_recall(pool, ws, sel, req_to_host, ctx_len, B, n_q, k, L_max, stage, clock, clock_dev, out_slot, stats,
                        dev_status, static_cast<cudaStream_t>(stream), nullptr, nullptr, 0, 0.f, nullptr, 0);
 }
@@ -253,7 +260,7 @@ int echo_prefetch_recall_noalloc(const echo_pool *pool, const int32_t *sel, cons
   REQUIRE(clock >= 0 || clock_dev, "clock must be >= 0");
   const long long F = static_cast<long long>(B) * n_q * k;
   REQUIRE(F <= (1ll << 30), "B * n_q * k too large");
-  if (stage) TRY(check_stage(stage));
+  if (stage) TRY(check_stage(stage, pool));
   echo_workspace ws;
   TRY(noalloc_workspace(pool->n_g, static_cast<int32_t>(F), &ws));
   // the array keeps whatever the last call left: lay it out for this call and reset it
@@ -307,7 +314,7 @@ int echo_decode_step(const echo_step_args *a, void *stream) {
   REQUIRE(F <= (1ll << 30), "B * n_q * k too large");
   TRY(check_ws(a->ws, a->pool, F > a->B ? F : a->B));
   REQUIRE(a->alpha >= 0.f && a->alpha <= 1.f, "alpha must be in [0, 1]");
-  if (prefetch) TRY(check_stage(a->stage));
+  if (prefetch) TRY(check_stage(a->stage, a->pool));
   if (a->new_kv) {
     REQUIRE(a->new_k_index, "new_kv given without new_k_index");
     REQUIRE(aligned(a->new_kv, 16) && aligned(a->new_k_index, 16), "append buffers must be 16-byte aligned");

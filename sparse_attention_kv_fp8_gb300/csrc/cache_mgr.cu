@@ -36,6 +36,10 @@
 //       slot.  This is the page's ticket order taken in slot order: deterministic.
 //   P5  only when a row was selected by several entries: after one more barrier,
 //       the repeats take the slot of the row's first entry.
+// Direct-to-slot prefetch (recall with a reserve): the slots the last recall set
+// aside count as free here unless this step's prefetch filled them (P2's third role
+// counts the filled ones and gives the unselected ones the step clock); E also
+// covers the next reserve, and P4 hands the ranks after the misses' to it.
 #include "cache_common.cuh"
 
 ECHO_TRACE_UNIT(cache_mgr)
@@ -85,6 +89,11 @@ struct OpParams {
   int32_t *clock_advance;
   // shared-memory caches (entries per CTA they hold; 0 = not cached)
   int slot_cache_cap, ent_cache_cap;
+  // direct-to-slot prefetch (recall; reserve != nullptr): slots set aside, [tickets
+  // drawn, reserve length], slots to set aside for the next step
+  int32_t *reserve;
+  int32_t *reserve_ctl;
+  int reserve_cap;
 };
 
 __device__ __forceinline__ int32_t read_clock(const OpParams &P) { return P.clock_dev ? *P.clock_dev : P.clock; }
@@ -266,7 +275,8 @@ __device__ __forceinline__ void find_from_top(const uint32_t *gh, uint32_t need,
   __syncthreads();
 }
 
-constexpr int32_t kFreeMark = INT32_MIN;  // slot-cache value of a free slot
+constexpr int32_t kFreeMark = INT32_MIN;      // slot-cache value of a free slot
+constexpr int32_t kResMark = INT32_MIN + 1;   // of a reserved slot the recall may hand out
 constexpr int kSlotWarps = 8;              // P2 roles: slot scan, entries, staged rows
 constexpr int kEntWarps = 6;
 constexpr int kStageWarps = kCoopWarps - kSlotWarps - kEntWarps;
@@ -319,6 +329,13 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
   const int32_t prev_idx = P.pool.counters[1];
   const int n = entries_count(P);
   uint32_t *glob = P.ws.glob;
+  // direct to slot: the reserve and how many of its tickets the prefetch drew
+  const bool direct = P.mode == kModeRecall && P.reserve != nullptr;
+  int32_t res_len = 0, res_taken = 0;
+  if (direct) {
+    res_len = P.reserve_ctl[1];
+    res_taken = min(P.reserve_ctl[0], res_len);
+  }
   ECHO_TRACE_MARK(0);
 
   // this CTA's slots and entries (contiguous ranges, for the ordered phases)
@@ -336,7 +353,9 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
   int32_t *take_cache = slot_cache ? dyn_smem + 2 * P.slot_cache_cap + 2 * P.ent_cache_cap : nullptr;
   auto slot_val = [&](int s) -> int32_t {
     if (slot_cache) return slot_cache[s - s_lo];
-    return P.pool.free_[s] ? kFreeMark : P.pool.prio[s];
+    if (P.pool.free_[s]) return kFreeMark;
+    const int32_t pr = P.pool.prio[s];
+    return (direct && pr == kReservedPrio) ? kResMark : pr;
   };
   auto aux_of = [&](int f) -> int32_t { return aux_cache ? aux_cache[f - e_lo] : P.ws.ent_aux[f]; };
   const bool copies = P.mode == kModeRecall || P.mode == kModeAppend;
@@ -395,7 +414,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
       for (int u = 0; u < kU; ++u) {
         const int s = s0 + u * kT;
         if (s >= s_hi) continue;
-        const int32_t v = fr[u] ? kFreeMark : pr[u];
+        const int32_t v = fr[u] ? kFreeMark : ((direct && pr[u] == kReservedPrio) ? kResMark : pr[u]);
         if (slot_cache) {
           slot_cache[s - s_lo] = v;
           host_cache[s - s_lo] = th[u];
@@ -488,6 +507,33 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
       }
     }
     if (lane == 0) ECHO_TRACE_LAST_HERE(12);
+  } else if (direct) {
+    // the reserve slots this step's prefetch filled (a slot whose ticket lost the row
+    // to another request's stays reserved); the unselected ones take the step clock
+    const int t = static_cast<int>(threadIdx.x) - (kSlotWarps + kEntWarps) * 32;
+    constexpr int kT = kStageWarps * 32;
+    uint32_t filled = 0, used = 0;
+    for (int i = c * kT + t; i < res_taken; i += G * kT) {
+      const int32_t s = P.reserve[i];
+      if (s < 0 || s >= n_g) continue;
+      const int32_t pr = P.pool.prio[s];
+      if (pr == kReservedPrio) continue;
+      ++filled;
+      if (pr == kPrefetchedPrio) {
+        P.pool.prio[s] = clock;
+      } else {
+        ++used;  // selected: the claim gave it the clock
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      filled += __shfl_xor_sync(0xffffffffu, filled, o);
+      used += __shfl_xor_sync(0xffffffffu, used, o);
+    }
+    if (lane == 0) {
+      if (filled) atomicAdd(&S->red[4], filled);
+      if (used) atomicAdd(&S->red[5], used);
+    }
   } else if (P.mode == kModeRecall && P.stage_count != nullptr) {
     // which claimed misses the prefetch staged this step (one warp per request)
     const int sw = warp - kSlotWarps - kEntWarps;
@@ -540,6 +586,9 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     if (S->red[1]) atomicAdd(glob + kGHits, S->red[1]);
     if (S->red[2]) atomicAdd(glob + kGValid, S->red[2]);
     if (S->red[3]) atomicAdd(glob + kGRepeats, S->red[3]);
+    if (S->red[4]) atomicAdd(glob + kGFilled, S->red[4]);
+    add_stat(P.stats, &echo_stats::staged, S->red[4]);
+    add_stat(P.stats, &echo_stats::staged_used, S->red[5]);
   }
   ECHO_TRACE_MARK(3);
   if (!grid_barrier(glob, P.status, S)) return;
@@ -571,7 +620,10 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
   }
   // repeats of a missed row exist: their out_slot needs one more grid barrier (one
   // thread per CTA reads the count; the scan below hands it to the rest)
-  if (threadIdx.x == 0) S->red[6] = P.mode == kModeRecall ? __ldcg(glob + kGRepeats) : 0u;
+  if (threadIdx.x == 0) {
+    S->red[6] = P.mode == kModeRecall ? __ldcg(glob + kGRepeats) : 0u;
+    S->red[5] = direct ? __ldcg(glob + kGFilled) : 0u;
+  }
   // this thread's segment of the entries; the staging rows of its owned misses
   const int e_cnt = e_hi - e_lo;
   const int e_per = (e_cnt + kCoopThreads - 1) / kCoopThreads;
@@ -597,17 +649,22 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     own_ex = ex4[3];
   }
   const bool any_repeats = S->red[6] != 0;  // written before the scan's barriers
+  // direct to slot: reserved slots the prefetch left unused return to the free ones
+  const int32_t released = direct ? res_len - static_cast<int32_t>(S->red[5]) : 0;
+  const int32_t res_want = direct ? max(P.reserve_cap, 0) : 0;
   ECHO_TRACE_MARK(14);
   int32_t E = 0;
   if (P.mode == kModeEvict) {
     E = *P.evict_n_dev;
     E = E < 0 ? 0 : E;
   } else if (P.mode != kModeAlloc) {
-    E = static_cast<int32_t>(M) - n_free0;
+    // direct to slot: evict for the next reserve too
+    E = static_cast<int32_t>(M) + res_want - (n_free0 + released);
     E = E < 0 ? 0 : E;
   }
   if (E > 0 && hist_total < static_cast<uint32_t>(E)) {  // fewer evictable slots than asked
-    if (c == 0 && threadIdx.x == 0) set_status(P.status, ECHO_DEV_POOL_EXHAUSTED);
+    // (a short reserve is no exhaustion: misses left out are flagged after P4)
+    if (c == 0 && threadIdx.x == 0 && !direct) set_status(P.status, ECHO_DEV_POOL_EXHAUSTED);
     E = static_cast<int32_t>(hist_total);
   }
   int32_t Tp = 0;  // threshold priority: victims have priority < Tp, or == Tp (the first needT)
@@ -697,7 +754,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     uint32_t lt = 0, eq = 0, fr = 0;
     for (int s = q0; s < q1; ++s) {
       const int32_t v = slot_val(s);
-      if (v == kFreeMark) {
+      if (v == kFreeMark || v == kResMark) {
         ++fr;
       } else if (E > 0 && v >= 0 && v < clock) {
         lt += v < Tp;
@@ -747,6 +804,8 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     free_total = tot4[3];
   }
   const int32_t A = (P.mode == kModeEvict) ? 0 : static_cast<int32_t>(min(M, free_total + static_cast<uint32_t>(E)));
+  // the next reserve: the ranks after the misses'
+  const int32_t R = min(res_want, static_cast<int32_t>(free_total + static_cast<uint32_t>(E)) - A);
   // this CTA's slots to take have ranks [a_lo, a_lo + n_mine); those below A get a miss
   const uint32_t a_lo = pre_fr + pre_lt + min(pre_eq, needT);
   const uint32_t n_mine = my_fr + my_lt + (min(pre_eq + my_eq, needT) - min(pre_eq, needT));
@@ -783,10 +842,19 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
       // the slots to take before s (free ones and victims)
       const uint32_t vb = lt_b + min(eq_b, needT);
       const uint32_t before = fr_b + vb;
-      if (v == kFreeMark) {
+      if (v == kFreeMark || v == kResMark) {
         if (before < static_cast<uint32_t>(A)) {
           P.ws.alloc_slot[before] = s;
           if (take_cache) take_cache[before - a_lo] = s;
+        } else if (before < static_cast<uint32_t>(A + R)) {  // into the next reserve
+          P.reserve[before - A] = s;
+          if (v == kFreeMark) {
+            P.pool.free_[s] = 0;
+            P.pool.prio[s] = kReservedPrio;
+          }
+        } else if (v == kResMark) {  // an unused reserved slot nobody takes: free
+          P.pool.free_[s] = 1;
+          P.pool.prio[s] = -1;
         }
         ++fr_b;
         continue;
@@ -807,6 +875,10 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
       if (before < static_cast<uint32_t>(A)) {
         P.ws.alloc_slot[before] = s;
         if (take_cache) take_cache[before - a_lo] = s;
+      } else if (before < static_cast<uint32_t>(A + R)) {  // into the next reserve
+        P.reserve[before - A] = s;
+        P.pool.prio[s] = kReservedPrio;
+        P.pool.to_host[s] = kInf;
       } else {  // nobody takes it: free
         P.pool.free_[s] = 1;
         P.pool.prio[s] = -1;
@@ -893,8 +965,13 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
   // scratch back to its resting state (nothing reads it any more)
   for (int i = gtid; i < kHistLevels * kHistBins; i += gthreads) P.ws.hist[i] = 0;
   if (c == 0 && threadIdx.x == 0) {
-    P.pool.counters[0] = n_free0 + E - A;
+    P.pool.counters[0] = n_free0 + released + E - A - R;
     P.pool.counters[1] = list_len;
+    if (direct) {  // every CTA read these at its start and the filled count after P2
+      P.reserve_ctl[0] = 0;
+      P.reserve_ctl[1] = R;
+      glob[kGFilled] = 0;
+    }
     P.ws.ctr[kCtrMisses] = static_cast<int32_t>(M);
     P.ws.ctr[kCtrGranted] = A;
     const uint32_t valid = g_valid, hits = g_hits;
@@ -1170,7 +1247,11 @@ int launch_recall(const echo_pool *pool, const echo_workspace *ws, const int32_t
   P.ctx_len = ctx_len;
   P.stats = stats;
   P.out_slot = out_slot;
-  if (stage) {
+  if (stage && stage->reserve) {  // direct to slot
+    P.reserve = stage->reserve;
+    P.reserve_ctl = stage->reserve_ctl;
+    P.reserve_cap = stage->reserve_cap;
+  } else if (stage) {
     P.stage_host = stage->host_row;
     P.stage_count = stage->count;
     P.stage_rows = stage->rows;

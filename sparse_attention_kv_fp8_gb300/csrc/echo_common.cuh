@@ -19,6 +19,11 @@ constexpr int kKvChunks = kKvBytes / 16;  // 72 16-byte vectors per latent-KV ro
 constexpr int32_t kInf = ECHO_INF;
 // a host row claimed by the selected entry f during recall: kClaim + f (< 0)
 constexpr int32_t kClaim = INT32_MIN;
+// GPUTokenPriority of a slot set aside for the direct-to-slot prefetch (not free,
+// not evictable, no row), and of a slot the prefetch filled in this step until the
+// recall gives it the step clock
+constexpr int32_t kReservedPrio = -2;
+constexpr int32_t kPrefetchedPrio = -3;
 
 // wall-clock limit of every spin-wait (a second), after which the kernel flags
 // ECHO_DEV_WAIT_TIMEOUT and unwinds

@@ -7,18 +7,21 @@
 // compare scores with the predicted k-th score and load rows from host memory),
 // one SM per query vector and a slice of the K cache.
 //
-// sm_103a design (one persistent CTA per SM, 10 warps):
+// sm_103a design (one persistent CTA per SM, 18 warps):
 //   warp 0      TMA producer: 128-token K tiles (16 KB, 128B-swizzled) into a
 //               10-stage shared-memory ring; the request's q (64*n_q x 128 e4m3)
-//               into one of two q buffers.
+//               into one of two q buffers; the tiles' host rows (req_to_host).
 //   warp 1      tensor-core issuer: per tile, 4 x tcgen05.mma kind::f8f6f4
-//               (M = 128 tokens, N = 64*n_q heads, K = 32) into one of two TMEM
-//               accumulators, so the next tile's MMA overlaps this tile's epilogue.
-//   warps 2-5   epilogue: tcgen05.ld one token row per thread, ReLU, weight, sum
-//               over heads in fp32, store the score; threshold test against the
-//               predicted k-th score; candidates take tickets and go to a queue.
-//   warps 6-9   prefetch: copy queued host rows (1152 B, 16-byte loads of the
-//               pinned, mapped host pool) into the HBM staging area.
+//               (M = 128 tokens, N = 64*n_q heads, K = 32) into one of four TMEM
+//               accumulators, so the MMA runs ahead of the epilogue.
+//   warps 2-9   epilogue, two warpgroups taking tiles in turn: tcgen05.ld one token
+//               row per thread, ReLU, weight, sum over heads in fp32, store the
+//               score; threshold test against the predicted k-th score;
+//               candidates go to a per-warp queue.
+//   warps 10-17 prefetch: residency test and tickets for the queued tokens, then
+//               copy their host rows (1152 B, 16-byte loads of the pinned, mapped
+//               host pool) into the HBM staging area, or straight into the GPU-pool
+//               slots the last recall set aside (direct to slot).
 // The kernel is HBM-bound: 128 + 4*n_q bytes per token against 2*64*128*n_q
 // FLOP, far below the FP8 ridge point.
 #include <cstdio>
@@ -70,7 +73,7 @@ struct IndexerParams {
   // fused prefetch (enabled when s_hat != nullptr)
   const float *s_hat;
   const int32_t *req_to_host;
-  const int32_t *host_to_gpu;
+  int32_t *host_to_gpu;  // written only by the direct-to-slot prefetch
   int32_t n_h;
   const uint16_t *host_kv;
   uint16_t *stage_rows;
@@ -78,6 +81,14 @@ struct IndexerParams {
   int32_t *stage_count;
   int32_t stage_stride;
   int32_t cap_div;
+  // direct-to-slot prefetch (reserve != nullptr): the reserved slots, the ticket
+  // counter / reserve length, and the pool arrays a placed row updates
+  const int32_t *reserve;
+  int32_t *reserve_ctl;
+  int32_t *to_host;
+  int32_t *prio;
+  uint16_t *gpu_kv;
+  int32_t n_g;
   int32_t *status;
   int32_t r2h_tma;  // the tiles' host rows come by TMA (needs L_max % 4 == 0)
 };
@@ -407,7 +418,13 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
     // prefetch warp e serves the queues of epilogue warps e, e + kPfWarps, ...
     const int pf = warp - 2 - kEpiWarps;
     const int4 *host = reinterpret_cast<const int4 *>(P.host_kv);
-    int4 *stage = reinterpret_cast<int4 *>(P.stage_rows);
+    const bool direct = P.reserve != nullptr;
+    // destination rows: the staging area, or the GPU pool itself (direct to slot)
+    int4 *dst_rows = reinterpret_cast<int4 *>(direct ? P.gpu_kv : P.stage_rows);
+    // reserve length (written by the recall before this kernel); once this warp has
+    // seen the tickets pass it, later candidates are dropped without being read
+    const int32_t res_len = direct ? __ldg(P.reserve_ctl + 1) : 0;
+    bool res_full = false;
     constexpr int kQ = kEpiWarps / kPfWarps;
     int heads[kQ];
 #pragma unroll
@@ -472,14 +489,19 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
       __syncwarp();
       if (lane == 0) *vhead = head;
       const uint32_t cmask = __ballot_sync(0xffffffffu, cand);
-      // tickets: one atomic per request among the candidates; its result is needed
-      // only for the destinations, so the first host loads below start before it returns
+      if (direct && res_full) {
+        if (cmask && lane == 0) set_status(P.status, ECHO_DEV_PREFETCH_CAP_HIT);
+        continue;
+      }
+      // tickets: one atomic per request among the candidates (staging) or one for the
+      // warp's candidates (direct to slot); the result is needed only for the
+      // destinations, so the first host loads below start before it returns
       uint32_t grp = 0;
       int leader = 0, base = 0;
       if (cand) {
-        grp = __match_any_sync(cmask, b);  // candidates of the same request
+        grp = direct ? cmask : __match_any_sync(cmask, b);  // candidates sharing a counter
         leader = __ffs(grp) - 1;
-        if (lane == leader) base = atomicAdd(P.stage_count + b, __popc(grp));
+        if (lane == leader) base = atomicAdd(direct ? P.reserve_ctl : P.stage_count + b, __popc(grp));
       }
       // ---- copy the candidate rows, kPfRowsPerBatch at a time (9 16-byte loads in flight
       // per lane); a row whose ticket is past the cap is read but not stored
@@ -512,16 +534,33 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
         }
         if (!have_tickets) {
           have_tickets = true;
-          if (cand) {
+          if (direct) {
+            // ticket t places the row in reserved slot reserve[t]; the row's map entry
+            // is claimed first, so a row two requests share is placed once (the other
+            // ticket's slot stays reserved and the recall returns it)
+            const int base_w = __shfl_sync(0xffffffffu, base, __ffs(cmask) - 1);  // cmask != 0 here
+            res_full = base_w + __popc(cmask) >= res_len;
+            if (cand) {
+              const int ticket = base_w + __popc(cmask & ((1u << lane) - 1));
+              if (ticket < res_len) {
+                const int32_t s = __ldg(P.reserve + ticket);
+                if (s >= 0 && s < P.n_g && atomicCAS(P.host_to_gpu + h, kInf, s) == kInf) dst = s;
+              } else if (ticket == res_len) {
+                set_status(P.status, ECHO_DEV_PREFETCH_CAP_HIT);
+              }
+            }
+          } else if (cand) {
             base = __shfl_sync(grp, base, leader);
             const int ticket = base + __popc(grp & ((1u << lane) - 1));
-            const int L = clamp_ctx(__ldg(P.ctx_len + b), P.L_max);
-            int cap = (L + P.cap_div - 1) / P.cap_div;
-            cap = cap < P.stage_stride ? cap : P.stage_stride;
-            if (ticket < cap) {
-              dst = b * P.stage_stride + ticket;
-            } else if (ticket == cap) {
-              set_status(P.status, ECHO_DEV_PREFETCH_CAP_HIT);
+            {
+              const int L = clamp_ctx(__ldg(P.ctx_len + b), P.L_max);
+              int cap = (L + P.cap_div - 1) / P.cap_div;
+              cap = cap < P.stage_stride ? cap : P.stage_stride;
+              if (ticket < cap) {
+                dst = b * P.stage_stride + ticket;
+              } else if (ticket == cap) {
+                set_status(P.status, ECHO_DEV_PREFETCH_CAP_HIT);
+              }
             }
           }
         }
@@ -532,7 +571,7 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
           const int idx = m * 32 + lane;
           const int r = idx / kKvChunks, c = idx % kKvChunks;
           const int32_t d = pick_reg(dr, r);
-          if (r < cnt && d >= 0) stage[static_cast<size_t>(d) * kKvChunks + c] = buf[m];
+          if (r < cnt && d >= 0) dst_rows[static_cast<size_t>(d) * kKvChunks + c] = buf[m];
         }
 #ifdef ECHO_TRACE
         __syncwarp();
@@ -545,7 +584,14 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
         }
 #endif
       }
-      if (dst >= 0) P.stage_host[dst] = h;
+      if (dst >= 0) {
+        if (direct) {  // the row is resident from here on (its bytes are stored above)
+          P.to_host[dst] = h;
+          P.prio[dst] = kPrefetchedPrio;
+        } else {
+          P.stage_host[dst] = h;
+        }
+      }
     }
     if (lane == 0) ECHO_TRACE_LAST_HERE(27);
   }
@@ -670,11 +716,20 @@ int launch_indexer(const echo_indexer_args *a, cudaStream_t stream) {
     P.host_to_gpu = a->pool->host_token_to_gpu;
     P.n_h = a->pool->n_h;
     P.host_kv = a->pool->host_kv;
-    P.stage_rows = a->stage->rows;
-    P.stage_host = a->stage->host_row;
-    P.stage_count = a->stage->count;
-    P.stage_stride = a->stage->stride;
-    P.cap_div = a->stage->cap_div;
+    if (a->stage->reserve) {
+      P.reserve = a->stage->reserve;
+      P.reserve_ctl = a->stage->reserve_ctl;
+      P.to_host = a->pool->gpu_token_to_host;
+      P.prio = a->pool->gpu_token_priority;
+      P.gpu_kv = a->pool->gpu_kv;
+      P.n_g = a->pool->n_g;
+    } else {
+      P.stage_rows = a->stage->rows;
+      P.stage_host = a->stage->host_row;
+      P.stage_count = a->stage->count;
+      P.stage_stride = a->stage->stride;
+      P.cap_div = a->stage->cap_div;
+    }
   }
   const long long tiles = static_cast<long long>(a->B) * ((a->L_max + echo::kTileTokens - 1) / echo::kTileTokens);
   if (tiles == 0) return ECHO_OK;
