@@ -31,10 +31,13 @@ sys.path.insert(0, ROOT)
 B, L, K_TOP, N_H, N_G = 8, 65536, 2048, 1_800_000, 200_000
 CAP_DIV = 16
 T0 = 1000                  # step clock at the start (pre-resident rows carry older clocks)
-TARGET_OVERLAP = 0.9
-WORKLOAD = ("DeepSeek-V3.2 decode shape: 1 layer, B=8, L=65536, H_index=64, d_index=128 e4m3, k=2048, "
+TARGET_OVERLAP = 0.9       # the workload's; --overlap picks 0.5, 0.7 or 0.99 instead (calibrated)
+
+
+def workload_name(overlap: float) -> str:
+    return ("DeepSeek-V3.2 decode shape: 1 layer, B=8, L=65536, H_index=64, d_index=128 e4m3, k=2048, "
             "latent KV 576 bf16, host pool 1.8M rows pinned, GPU pool 200K slots full at start, "
-            "consecutive top-k overlap 0.9")
+            f"consecutive top-k overlap {overlap:g}")
 METRIC = "decode steps/s (indexer+select+recall, one layer)"
 L2_NOTE = "L2 flushed between steps outside the timed events (256 MB write, then 256 MB read)"
 
@@ -152,10 +155,10 @@ def aggregate_replicas(local_total_ms: float, steps: int, pg=None, device="cpu")
 # ---------------------------------------------------------------------------
 # workload
 # ---------------------------------------------------------------------------
-def build_inputs(n_steps: int, seed: int, host_out=None):
+def build_inputs(n_steps: int, seed: int, host_out=None, overlap: float = TARGET_OVERLAP):
     from sparse_attention_kv_fp8_gb300 import workload as wl
     inp = wl.indexer_inputs(B, 1, L, L, seed=seed)
-    rho = rho_for(L, TARGET_OVERLAP)
+    rho = rho_for(L, overlap)
     qs = [inp.q]
     qf = inp.q_float
     for t in range(1, n_steps):
@@ -191,7 +194,7 @@ def run_reference(args):
     oracle.build()
     steps = args.warmup + args.steps
     host = np.zeros((N_H, 576), np.uint16)
-    inp, qs, host, r2h, st, rho = build_inputs(steps, seed=1, host_out=host)
+    inp, qs, host, r2h, st, rho = build_inputs(steps, seed=1, host_out=host, overlap=args.overlap)
     times = []
     for t in range(steps):
         dt = cpu_baseline_sample(inp, qs[t], host, r2h, st, requests=1)
@@ -202,7 +205,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "rho": rho},
+            "config": {"workload": workload_name(args.overlap), "rho": rho},
             "cpu_baseline": {"value": v, "unit": "steps/s", "cores": 1, "kind": "oracle",
                              "sample": f"1 of the {B} requests per step (L={L}), scaled x{B}"},
             "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -240,7 +243,7 @@ def run_ours(args):
     seed = 1 + rank
     host_t = torch.empty((N_H, echo.KV_ELEMS), dtype=torch.int16, pin_memory=True)
     inp, qs, host_np, r2h, st, rho = build_inputs(steps + min(args.steps, 10) + 2 * n_e2e + 1, seed,
-                                                  host_out=host_t.numpy().view(np.uint16))
+                                                  host_out=host_t.numpy().view(np.uint16), overlap=args.overlap)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -399,10 +402,12 @@ def run_ours(args):
     h2d_gbs = (256 << 20) / (best * 1e-3) / 1e9
     recall_probe = recall_bandwidth_probe(echo, torch, host_t, flush_l2)
     volume_probe = indexer_volume_probe(echo, torch, inp, flush_l2, hbm_peak)
-    direct = None
+    direct = off = None
     if args.reserve > 0:
-        direct = direct_to_slot_leg(echo, torch, st, host_t, q_ring, w, k_index, ctx, r2h_t, flush_l2,
-                                    args.warmup, args.steps, n_stage, args.reserve)
+        direct = prefetch_mode_leg(echo, torch, st, host_t, q_ring, w, k_index, ctx, r2h_t, flush_l2,
+                                   args.warmup, args.steps, n_stage, args.reserve)
+        off = prefetch_mode_leg(echo, torch, st, host_t, q_ring, w, k_index, ctx, r2h_t, flush_l2,
+                                args.warmup, args.steps, n_stage, 0)
 
     # ---- roofline of the dominant kernel (the indexer) ----
     idx_ms = float(np.mean(stage_ms["indexer"]))
@@ -426,7 +431,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 (indexer); int32 metadata; bf16 bytes",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "l2": L2_NOTE, "rho": rho, "graph": "one CUDA graph per step",
+        "config": {"workload": workload_name(args.overlap), "l2": L2_NOTE, "rho": rho, "graph": "one CUDA graph per step",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "scored_tokens_per_s": value * B * L,
         "hit_rate": hits / uniq,
@@ -435,6 +440,7 @@ def run_ours(args):
         "staged_used_per_step": st_vals["staged_used"] / args.steps,
         "evicted_per_step": st_vals["evicted"] / args.steps,
         "direct_to_slot": direct,
+        "prefetch_off": off,
         "stage_ms": {k: float(np.mean(v)) for k, v in stage_ms.items()},
         "stage_ms_note": f"from {n_stage} further steps replayed with stage events ({float(np.mean(staged_total_ms)):.4f} ms/step with the events)",
         "recall": {"bytes_per_step": recalled_rows / args.steps * 1152, "ms": recall_ms,
@@ -461,15 +467,17 @@ def run_ours(args):
     return 0
 
 
-def direct_to_slot_leg(echo, torch, st, host_t, q_ring, w, k_index, ctx, r2h_t, flush_l2, warmup, n_timed, n_stage,
-                       reserve):
-    """The same steps (same start state, same queries) with the direct-to-slot
-    prefetch: rows land in `reserve` slots each recall sets aside, instead of the
-    staging area.  Whole steps and the per-stage split, timed as in the main loop."""
+def prefetch_mode_leg(echo, torch, st, host_t, q_ring, w, k_index, ctx, r2h_t, flush_l2, warmup, n_timed, n_stage,
+                      reserve):
+    """The same steps (same start state, same queries) with another prefetch mode:
+    reserve > 0, direct to slot (rows land in `reserve` slots each recall sets aside,
+    instead of the staging area); reserve = 0, no prefetch at all (the whole miss set
+    is recalled after the top-k).  Whole steps and the per-stage split, timed as in
+    the main loop."""
     pool = echo.Pool(N_G, host_t)
     pool.load_state(st)
     ws = echo.Workspace(N_G, B * K_TOP)
-    stage = echo.Stage(B, reserve=reserve)
+    stage = echo.Stage(B, reserve=reserve) if reserve > 0 else None
     out = echo.StepBuffers(B, 1, L, K_TOP)
     stats = echo.Stats()
     s_hat = torch.full((B, 1), float("inf"), dtype=torch.float32, device="cuda")
@@ -525,7 +533,8 @@ def direct_to_slot_leg(echo, torch, st, host_t, q_ring, w, k_index, ctx, r2h_t, 
     stage_ms = {name: float(np.mean([evs[t][i].elapsed_time(evs[t][i + 1]) for t in st_steps]))
                 for i, name in enumerate(("append", "indexer", "topk", "recall", "ema"))}
     per = float(np.mean(ms))
-    return {"reserve_slots": reserve, "value": 1e3 / per, "unit": "steps/s", "ms_per_step": per,
+    return {"mode": "direct to slot" if reserve > 0 else "no prefetch", "reserve_slots": reserve,
+            "value": 1e3 / per, "unit": "steps/s", "ms_per_step": per,
             "hit_rate": sv["hits"] / max(1, sv["unique_rows"]),
             "recalled_rows_per_step": sv["recalled"] / n_timed,
             "prefetched_rows_per_step": sv["staged"] / n_timed,
@@ -661,8 +670,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-requests", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--overlap", type=float, default=TARGET_OVERLAP,
+                    help="consecutive top-k overlap of the synthetic queries (0.5, 0.7, 0.9 or 0.99)")
     ap.add_argument("--reserve", type=int, default=8192,
-                    help="slots per recall for the direct-to-slot comparison leg (0: skip the leg)")
+                    help="slots per recall for the direct-to-slot comparison leg (0: skip it and the "
+                         "no-prefetch leg)")
     ap.add_argument("--kernel", default=None, choices=[None, "indexer"],
                     help="run one kernel on a small case (for profilers) instead of the benchmark")
     ap.add_argument("--B", type=int, default=24)

@@ -697,6 +697,96 @@ void orc_prefetch_candidates(const float *scores, const float *s_hat, const int3
     }
 }
 
+/* ------------------------------------------------------------------------- */
+/* Inter-query prefetch (section 6.2)                                         */
+/* ------------------------------------------------------------------------- */
+
+/* order-preserving 32-bit key of an fp32 value (a larger value has a larger key;
+   -0 is folded onto +0) */
+static uint32_t orc_order_key(float x)
+{
+    if (x == 0.0f)
+        x = 0.0f;
+    uint32_t u;
+    memcpy(&u, &x, sizeof(u));
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+/*
+ * Approximate top-k of one query's scores (section 6.2): each score is shifted by the
+ * predicted k-th score, x = s - s_hat (fp32), and binned by the top 8 bits of x's
+ * order-preserving key into S_0 .. S_255 (S_255 holds the largest values).  The top j
+ * bins are taken, j the largest with S_{256-j} + ... + S_255 <= k; bin 255 - j is the
+ * threshold bin (-1 when every bin fits).  Returns the threshold bin; hist receives
+ * S_0 .. S_255 and *subset_n the count of the taken bins, which by construction obeys
+ * the section's inequality k - S_{255-j} < subset_n <= k (when the threshold bin exists).
+ */
+int orc_approx_topk_bins(const float *scores, int L, float s_hat, int k, int32_t *hist, int32_t *subset_n)
+{
+    for (int i = 0; i < 256; ++i)
+        hist[i] = 0;
+    for (int p = 0; p < L; ++p) {
+        float x = scores[p] - s_hat;
+        hist[orc_order_key(x) >> 24] += 1;
+    }
+    int64_t sum = 0;
+    int bin = 255;
+    while (bin >= 0 && sum + hist[bin] <= k) {
+        sum += hist[bin];
+        --bin;
+    }
+    *subset_n = (int32_t)sum;
+    return bin;
+}
+
+/*
+ * Prefill chunk (section 6.2 with the prefill kernel of section 6.3): request b scores
+ * its last C tokens as queries (query i sees valid_len(ctx_len[b], C, i) keys, as in
+ * orc_indexer_score with n_q = C).  Queries are taken in blocks of qb; when a block is
+ * scored, its prefetch candidates are the tokens that some query of the block puts
+ * above its threshold bin (the approximate top-k above, shift s_hat[b]) and whose host
+ * row is not resident, in ascending token order, once per block.
+ *   thr_bin, subset_n [B][C]; cand [B][n_blocks][L_max], cand_count [B][n_blocks],
+ *   n_blocks = ceil(C / qb).
+ */
+void orc_prefill_candidates(const float *scores, const float *s_hat, const int32_t *ctx_len, int B, int C,
+                            int L_max, int k, int qb, const int32_t *req_to_host,
+                            const int32_t *HostTokenToGPU, int n_h, int32_t *thr_bin, int32_t *subset_n,
+                            int32_t *cand, int32_t *cand_count)
+{
+    int32_t hist[256];
+    const int nb = (C + qb - 1) / qb;
+    for (int b = 0; b < B; ++b) {
+        for (int i = 0; i < C; ++i) {
+            size_t row = (size_t)b * C + i;
+            int L = valid_len(ctx_len[b], C, i);
+            thr_bin[row] = orc_approx_topk_bins(scores + row * L_max, L, s_hat[b], k, hist, &subset_n[row]);
+        }
+        for (int blk = 0; blk < nb; ++blk) {
+            int n = 0;
+            int32_t *out = cand + ((size_t)b * nb + blk) * L_max;
+            for (int p = 0; p < L_max; ++p) {
+                int pass = 0;
+                for (int i = blk * qb; i < C && i < (blk + 1) * qb; ++i) {
+                    size_t row = (size_t)b * C + i;
+                    if (p >= valid_len(ctx_len[b], C, i))
+                        continue;
+                    float x = scores[row * L_max + p] - s_hat[b];
+                    if ((int)(orc_order_key(x) >> 24) > thr_bin[row])
+                        pass = 1;
+                }
+                if (!pass)
+                    continue;
+                int32_t h = req_to_host[(size_t)b * L_max + p];
+                if (h < 0 || h >= n_h || HostTokenToGPU[h] != ORC_INF)
+                    continue;
+                out[n++] = p;
+            }
+            cand_count[(size_t)b * nb + blk] = n;
+        }
+    }
+}
+
 /* s_hat <- alpha s_hat + (1 - alpha) kth, in fp32; the first finite observation
    replaces the +inf start value; a non-finite kth (empty context) is skipped */
 void orc_ema_update(float *s_hat, const float *kth, int n, float alpha)
