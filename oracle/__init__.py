@@ -90,6 +90,10 @@ def lib():
             L.orc_append.restype = I
             L.orc_prefetch_candidates.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P, P, P]
             L.orc_prefetch_candidates.restype = None
+            L.orc_approx_topk_bins.argtypes = [P, I, F, I, P, P]
+            L.orc_approx_topk_bins.restype = I
+            L.orc_prefill_candidates.argtypes = [P, P, P, I, I, I, I, I, P, P, I, P, P, P, P]
+            L.orc_prefill_candidates.restype = None
             L.orc_ema_update.argtypes = [P, P, I, F]
             L.orc_ema_update.restype = None
             L.orc_metadata_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64]
@@ -177,6 +181,38 @@ def prefetch_candidates(scores, s_hat, ctx_len, req_to_host, host_token_to_gpu, 
                                   h2g.size, B, n_q, L_max, stage_stride, cap_div,
                                   _p(cand), _p(cnt), _p(cap))
     return [cand[b, :cnt[b]].copy() for b in range(B)], cap
+
+
+def approx_topk_bins(scores_row, s_hat: float, k: int):
+    """Approximate top-k of one query's scores (section 6.2): (threshold bin, 256-bin
+    histogram of the shifted scores, size of the subset above the threshold bin)."""
+    row = _arr(scores_row, np.float32)
+    hist = np.zeros(256, np.int32)
+    n = np.zeros(1, np.int32)
+    t = lib().orc_approx_topk_bins(_p(row), row.size, float(np.float32(s_hat)), int(k), _p(hist), _p(n))
+    return int(t), hist, int(n[0])
+
+
+def prefill_candidates(scores, s_hat, ctx_len, k: int, qb: int, req_to_host, host_token_to_gpu):
+    """Prefill chunk of C = scores.shape[1] query tokens per request (section 6.2):
+    per query the threshold bin and subset size; per (request, query block) the
+    prefetch candidates (tokens some query of the block puts above its threshold bin,
+    host row not resident), ascending.  Returns (thr_bin [B][C], subset_n [B][C],
+    list over requests of lists over blocks of token arrays)."""
+    scores = _arr(scores, np.float32)
+    s_hat = _arr(s_hat, np.float32).reshape(-1)
+    ctx_len = _arr(ctx_len, np.int32)
+    req_to_host = _arr(req_to_host, np.int32)
+    h2g = _arr(host_token_to_gpu, np.int32)
+    B, C, L_max = scores.shape
+    nb = (C + qb - 1) // qb
+    thr = np.empty((B, C), np.int32)
+    sub = np.empty((B, C), np.int32)
+    cand = np.empty((B, nb, L_max), np.int32)
+    cnt = np.empty((B, nb), np.int32)
+    lib().orc_prefill_candidates(_p(scores), _p(s_hat), _p(ctx_len), B, C, L_max, int(k), int(qb),
+                                 _p(req_to_host), _p(h2g), h2g.size, _p(thr), _p(sub), _p(cand), _p(cnt))
+    return thr, sub, [[cand[b, i, :cnt[b, i]].copy() for i in range(nb)] for b in range(B)]
 
 
 # ---------------------------------------------------------------------------
