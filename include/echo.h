@@ -201,13 +201,60 @@ typedef struct echo_indexer_args {
 int echo_indexer_score(const echo_indexer_args *args, void *stream);
 
 /*
+ * Indexer score of a prefill chunk with the fused inter-query prefetch (section 6.2;
+ * section 6.3, prefill kernel).  Request b scores its last C tokens as queries: query
+ * i sees ctx_len[b] - (C - 1 - i) keys (the chunk's own k^I rows are already in
+ * k_index), and scores[b][i][p] is the formula of echo_indexer_score; other entries
+ * are left untouched.  Queries are taken in blocks of 4 (one 4 x 64-head tensor-core
+ * operand); each CTA owns whole blocks and all their keys.
+ * Approximate top-k (s_shift != NULL): every score of query i is shifted by the
+ * predicted k-th score, x = s - s_shift[b] (fp32), and binned by the top 8 bits of
+ * x's order-preserving 32-bit key (bin 255 = the largest values); the top j bins with
+ * S_255 + ... + S_{256-j} <= k are taken, bin 255 - j is the threshold bin
+ * (thr_bin[b][i], -1 when all bins fit) and subset_n[b][i] counts the taken scores.
+ * When a block is finished, the tokens some query of the block puts above its
+ * threshold bin whose host row is not resident are prefetched as in the decode
+ * indexer (staging or direct to slot, see echo_stage; once per block, a staged row
+ * may repeat across blocks), while the following blocks are being scored.  Without
+ * a stage only thr_bin / subset_n are produced.
+ *   q        [B][C][64][128] e4m3 device, 16-byte aligned
+ *   w        [B][C][64] fp32 device, 16-byte aligned
+ *   k_index  [B][L_max][128] e4m3 device, 16-byte aligned
+ *   ctx_len  [B] int32 device, 0 <= ctx_len[b] <= L_max (a context shorter than C
+ *            gives the first queries no keys)
+ *   scores   [B][C][L_max] fp32 device
+ *   s_shift  [B] fp32 device, optional; k >= 1 with it
+ *   thr_bin, subset_n  [B][C] int32 device, optional
+ *   req_to_host [B][L_max] int32 device, pool, stage: optional (prefetch)
+ */
+typedef struct echo_prefill_args {
+    const uint8_t *q;
+    const float *w;
+    const uint8_t *k_index;
+    const int32_t *ctx_len;
+    int32_t B, C, L_max;
+    float *scores;
+    const float *s_shift;
+    int32_t k;
+    int32_t *thr_bin;
+    int32_t *subset_n;
+    const int32_t *req_to_host;
+    const echo_pool *pool;
+    const echo_stage *stage;
+    int32_t *dev_status;
+} echo_prefill_args;
+
+int echo_prefill_indexer_score(const echo_prefill_args *args, void *stream);
+
+/*
  * Exact top-k per (b, j) row of `scores` over its first
  * ctx_len[b] - (n_q - 1 - j) entries (section 2: top-k with k = 2048).  Ties at the
  * k-th value go to the lower token index.  sel[b][j][0..k) lists the selected
  * token indices in ascending order, -1 padded when fewer than k tokens exist;
  * kth[b][j] is the min(k, L)-th largest score (-inf for an empty row).
  *   scores [B][n_q][L_max] fp32 device (no NaN); sel [B][n_q][k] int32; kth [B][n_q] fp32
- * Limits: 1 <= k <= 8192, L_max <= 360448.
+ * Limits: 1 <= k <= 8192, L_max <= 360448, 1 <= n_q <= 65536 (the queries of a
+ * prefill chunk are rows too).
  */
 int echo_select_topk(const float *scores, const int32_t *ctx_len, int32_t B, int32_t n_q,
                      int32_t L_max, int32_t k, int32_t *sel, float *kth, void *stream);
@@ -305,6 +352,11 @@ int echo_append(const echo_pool *pool, const echo_workspace *ws, uint8_t *k_inde
  */
 int echo_ema_update(float *s_hat, const float *kth, int32_t n, float alpha, void *stream);
 
+/* The same EMA reading kth[i * kth_stride] (a prefill chunk updates its request's
+   prediction from the k-th score of the chunk's last query: kth + C - 1, stride C). */
+int echo_ema_update_strided(float *s_hat, const float *kth, int32_t n, int32_t kth_stride, float alpha,
+                            void *stream);
+
 /* Stages of echo_decode_step, in order (timing events are recorded before each
    stage and after the last).  The EMA is computed by the recall's last kernel, so
    the ECHO_STAGE_EMA interval is empty; the constant is kept for the event layout. */
@@ -371,7 +423,9 @@ int echo_selftest_wait_timeout(int32_t which, int32_t *dev_status, void *stream)
 /* Description of the calling thread's last error ("" if none). */
 const char *echo_last_error_string(void);
 
-/* Library version, (major << 16) | minor (1.1: echo_stage's direct-to-slot fields). */
+/* Library version, (major << 16) | minor (1.1: echo_stage's direct-to-slot fields;
+   1.2: echo_prefill_indexer_score, echo_ema_update_strided, n_q up to 65536 in
+   top-k and recall). */
 int32_t echo_version(void);
 
 /* Storage law of the metadata arrays of one pool (section 5.1): 4*n_h + 13*n_g. */

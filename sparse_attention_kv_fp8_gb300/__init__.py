@@ -58,6 +58,13 @@ class c_indexer_args(ctypes.Structure):
                 ("pool", ctypes.POINTER(c_pool)), ("stage", ctypes.POINTER(c_stage)), ("dev_status", _P)]
 
 
+class c_prefill_args(ctypes.Structure):
+    _fields_ = [("q", _P), ("w", _P), ("k_index", _P), ("ctx_len", _P), ("B", _I32), ("C", _I32),
+                ("L_max", _I32), ("scores", _P), ("s_shift", _P), ("k", _I32), ("thr_bin", _P), ("subset_n", _P),
+                ("req_to_host", _P), ("pool", ctypes.POINTER(c_pool)), ("stage", ctypes.POINTER(c_stage)),
+                ("dev_status", _P)]
+
+
 class c_step_args(ctypes.Structure):
     _fields_ = [("pool", ctypes.POINTER(c_pool)), ("ws", ctypes.POINTER(c_workspace)),
                 ("stage", ctypes.POINTER(c_stage)), ("q", _P), ("w", _P), ("k_index", _P), ("ctx_len", _P),
@@ -97,6 +104,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "echo_prefetch_recall_noalloc": ([ctypes.POINTER(c_pool), _P, _P, _P, _I32, _I32, _I32, _I32,
                                           ctypes.POINTER(c_stage), _I32, _P, _P, _P, _P, _P], S),
         "echo_ema_update": ([_P, _P, _I32, ctypes.c_float, _P], S),
+        "echo_ema_update_strided": ([_P, _P, _I32, _I32, ctypes.c_float, _P], S),
+        "echo_prefill_indexer_score": ([ctypes.POINTER(c_prefill_args), _P], S),
         "echo_decode_step": ([ctypes.POINTER(c_step_args), _P], S),
         "echo_last_error_string": ([], ctypes.c_char_p),
         "echo_version": ([], _I32),
@@ -259,6 +268,20 @@ def echo_indexer_score(q, w, k_index, ctx_len, scores, s_hat=None, req_to_host=N
     _check(load_library().echo_indexer_score(ctypes.byref(a), _stream(stream)), "echo_indexer_score")
 
 
+def echo_prefill_indexer_score(q, w, k_index, ctx_len, scores, s_shift=None, k: int = 0, thr_bin=None,
+                               subset_n=None, req_to_host=None, pool: Pool | None = None,
+                               stage: Stage | None = None, dev_status=None, stream=None):
+    """q [B][C][64][128] e4m3: the chunk's C queries per request (see include/echo.h)."""
+    B, C = q.shape[0], q.shape[1]
+    a = c_prefill_args(_dev(q, "q"), _dev(w, "w"), _dev(k_index, "k_index"), _dev(ctx_len, "ctx_len"), B, C,
+                       k_index.shape[1], _dev(scores, "scores"), _dev(s_shift, "s_shift"), int(k),
+                       _dev(thr_bin, "thr_bin"), _dev(subset_n, "subset_n"), _dev(req_to_host, "req_to_host"),
+                       ctypes.pointer(pool.c) if pool is not None else None,
+                       ctypes.pointer(stage.c) if stage is not None else None, _dev(dev_status, "dev_status"))
+    _check(load_library().echo_prefill_indexer_score(ctypes.byref(a), _stream(stream)),
+           "echo_prefill_indexer_score")
+
+
 def echo_select_topk(scores, ctx_len, k: int, sel, kth, stream=None):
     B, n_q, L_max = scores.shape
     _check(load_library().echo_select_topk(_dev(scores, "scores"), _dev(ctx_len, "ctx_len"), B, n_q, L_max, k,
@@ -327,6 +350,13 @@ def echo_append(pool: Pool, ws: Workspace, k_index, ctx_len, req_to_host, new_kv
 def echo_ema_update(s_hat, kth, alpha: float = 0.5, stream=None):
     _check(load_library().echo_ema_update(_dev(s_hat, "s_hat"), _dev(kth, "kth"), int(s_hat.numel()),
                                           float(alpha), _stream(stream)), "echo_ema_update")
+
+
+def echo_ema_update_strided(s_hat, kth, kth_stride: int, alpha: float = 0.5, stream=None):
+    """s_hat[i] from kth[i * kth_stride] (kth a flat device tensor view)."""
+    _check(load_library().echo_ema_update_strided(_dev(s_hat, "s_hat"), _dev(kth, "kth"), int(s_hat.numel()),
+                                                  int(kth_stride), float(alpha), _stream(stream)),
+           "echo_ema_update_strided")
 
 
 class StepBuffers:

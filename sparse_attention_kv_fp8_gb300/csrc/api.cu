@@ -49,7 +49,8 @@ int launch_wait_probe(int which, int32_t *status, cudaStream_t s);
 int launch_append(const echo_pool *pool, const echo_workspace *ws, uint8_t *k_index, int32_t *ctx_len,
                   const int32_t *req_to_host, int B, int L_max, const uint16_t *new_kv, const uint8_t *new_k_index,
                   int32_t clock, const int32_t *clock_dev, echo_stats *stats, int32_t *status, cudaStream_t s);
-int launch_ema(float *s_hat, const float *kth, int n, float alpha, cudaStream_t s);
+int launch_ema(float *s_hat, const float *kth, int n, int stride, float alpha, cudaStream_t s);
+int launch_prefill_indexer(const echo_prefill_args *a, cudaStream_t stream);
 int noalloc_workspace(int32_t n_g, int32_t rows, echo_workspace *out);
 
 }  // namespace echo_host
@@ -145,7 +146,7 @@ int echo_selftest_wait_timeout(int32_t which, int32_t *dev_status, void *stream)
   return launch_wait_probe(which, dev_status, static_cast<cudaStream_t>(stream));
 }
 
-int32_t echo_version(void) { return (1 << 16) | 1; }
+int32_t echo_version(void) { return (1 << 16) | 2; }
 
 int64_t echo_metadata_bytes(int64_t n_h, int64_t n_g) {
   return static_cast<int64_t>(sizeof(int32_t)) * n_h +
@@ -177,7 +178,7 @@ int echo_select_topk(const float *scores, const int32_t *ctx_len, int32_t B, int
   g_err[0] = 0;
   REQUIRE(scores && ctx_len && sel && kth, "top-k pointer is NULL");
   REQUIRE(B >= 0 && L_max >= 0, "negative size");
-  REQUIRE(n_q == 1 || n_q == 2, "n_q must be 1 or 2 (got %d)", n_q);
+  REQUIRE(n_q >= 1 && n_q <= 65536, "n_q must be in [1, 65536] (got %d)", n_q);
   REQUIRE(k >= 1 && k <= 8192, "k must be in [1, 8192] (got %d)", k);
   REQUIRE(static_cast<long long>(B) * n_q * 8 <= (1ll << 31) - 1, "B too large");
   if (B == 0) return ECHO_OK;
@@ -237,7 +238,7 @@ int echo_prefetch_recall(const echo_pool *pool, const echo_workspace *ws, const 
   g_err[0] = 0;
   TRY(check_pool(pool));
   REQUIRE(B >= 0 && L_max >= 0 && k >= 1, "bad sizes");
-  REQUIRE(n_q == 1 || n_q == 2, "n_q must be 1 or 2");
+  REQUIRE(n_q >= 1 && n_q <= 65536, "n_q must be in [1, 65536]");
   REQUIRE(B == 0 || (sel && req_to_host && out_slot && ctx_len), "recall pointer is NULL");
   REQUIRE(clock >= 0 || clock_dev, "clock must be >= 0");
   const long long F = static_cast<long long>(B) * n_q * k;
@@ -255,7 +256,7 @@ int echo_prefetch_recall_noalloc(const echo_pool *pool, const int32_t *sel, cons
   g_err[0] = 0;
   TRY(check_pool(pool));
   REQUIRE(B >= 0 && L_max >= 0 && k >= 1, "bad sizes");
-  REQUIRE(n_q == 1 || n_q == 2, "n_q must be 1 or 2");
+  REQUIRE(n_q >= 1 && n_q <= 65536, "n_q must be in [1, 65536]");
   REQUIRE(B == 0 || (sel && req_to_host && out_slot && ctx_len), "recall pointer is NULL");
   REQUIRE(clock >= 0 || clock_dev, "clock must be >= 0");
   const long long F = static_cast<long long>(B) * n_q * k;
@@ -290,7 +291,42 @@ int echo_ema_update(float *s_hat, const float *kth, int32_t n, float alpha, void
   REQUIRE(n == 0 || (s_hat && kth), "EMA pointer is NULL");
   REQUIRE(alpha >= 0.f && alpha <= 1.f, "alpha must be in [0, 1]");
   if (n == 0) return ECHO_OK;
-  return launch_ema(s_hat, kth, n, alpha, static_cast<cudaStream_t>(stream));
+  return launch_ema(s_hat, kth, n, 1, alpha, static_cast<cudaStream_t>(stream));
+}
+
+int echo_ema_update_strided(float *s_hat, const float *kth, int32_t n, int32_t kth_stride, float alpha,
+                            void *stream) {
+  g_err[0] = 0;
+  REQUIRE(n >= 0, "n must be >= 0");
+  REQUIRE(kth_stride >= 1, "kth_stride must be >= 1");
+  REQUIRE(n == 0 || (s_hat && kth), "EMA pointer is NULL");
+  REQUIRE(alpha >= 0.f && alpha <= 1.f, "alpha must be in [0, 1]");
+  REQUIRE(static_cast<long long>(n) * kth_stride <= (1ll << 31) - 1, "n * kth_stride too large");
+  if (n == 0) return ECHO_OK;
+  return launch_ema(s_hat, kth, n, kth_stride, alpha, static_cast<cudaStream_t>(stream));
+}
+
+int echo_prefill_indexer_score(const echo_prefill_args *a, void *stream) {
+  g_err[0] = 0;
+  REQUIRE(a, "args is NULL");
+  REQUIRE(a->q && a->w && a->k_index && a->ctx_len && a->scores, "prefill indexer pointer is NULL");
+  REQUIRE(a->B >= 0 && a->L_max >= 0, "negative size");
+  REQUIRE(a->C >= 1 && a->C <= 65536, "C must be in [1, 65536] (got %d)", a->C);
+  REQUIRE(aligned(a->q, 16) && aligned(a->k_index, 16) && aligned(a->w, 16),
+          "q, w and k_index must be 16-byte aligned");
+  REQUIRE(static_cast<long long>(a->B) * a->L_max <= (1ll << 31) - 1, "B * L_max too large");
+  REQUIRE(static_cast<long long>(a->B) * a->C * echo::kHeads <= (1ll << 31) - 1, "B * C too large");
+  REQUIRE(static_cast<long long>(a->B) * a->C * a->L_max <= (1ll << 40), "scores too large");
+  if (a->s_shift) {
+    REQUIRE(a->k >= 1, "k must be >= 1 with s_shift");
+    if (a->stage) {
+      REQUIRE(a->req_to_host && a->pool, "prefetch needs req_to_host and pool");
+      TRY(check_pool(a->pool));
+      TRY(check_stage(a->stage, a->pool));
+    }
+  }
+  if (a->B == 0 || a->L_max == 0) return ECHO_OK;
+  return launch_prefill_indexer(a, static_cast<cudaStream_t>(stream));
 }
 
 int echo_decode_step(const echo_step_args *a, void *stream) {

@@ -131,15 +131,18 @@ __device__ __forceinline__ int entries_count(const OpParams &P) {
 }
 
 // EMA of the k-th score (fp32, each operation rounded; +inf start takes kth)
-__device__ __forceinline__ void ema_one(float *s_hat, const float *kth, int i, float alpha) {
-  const float x = kth[i];
+__device__ __forceinline__ void ema_apply(float *s_hat, float x, float alpha) {
   if (!isfinite(x)) return;
-  const float s = s_hat[i];
+  const float s = *s_hat;
   if (isinf(s) && s > 0.f) {
-    s_hat[i] = x;
+    *s_hat = x;
   } else {
-    s_hat[i] = __fadd_rn(__fmul_rn(alpha, s), __fmul_rn(__fsub_rn(1.0f, alpha), x));
+    *s_hat = __fadd_rn(__fmul_rn(alpha, s), __fmul_rn(__fsub_rn(1.0f, alpha), x));
   }
+}
+
+__device__ __forceinline__ void ema_one(float *s_hat, const float *kth, int i, float alpha) {
+  ema_apply(s_hat + i, kth[i], alpha);
 }
 
 __device__ __forceinline__ bool evictable(uint8_t fr, int32_t pr, int32_t clock) {
@@ -1098,9 +1101,9 @@ __global__ void __launch_bounds__(kCoopThreads, 1) wait_probe_kernel(int which, 
   grid_barrier(glob, status, &S_);
 }
 
-__global__ void ema_kernel(float *s_hat, const float *kth, int n, float alpha) {
+__global__ void ema_kernel(float *s_hat, const float *kth, int n, int stride, float alpha) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < n) ema_one(s_hat, kth, i, alpha);
+  if (i < n) ema_apply(s_hat + i, kth[static_cast<size_t>(i) * stride], alpha);
 }
 
 }  // namespace echo
@@ -1353,8 +1356,8 @@ int noalloc_workspace(int32_t n_g, int32_t rows, echo_workspace *out) {
   return ECHO_OK;
 }
 
-int launch_ema(float *s_hat, const float *kth, int n, float alpha, cudaStream_t s) {
-  echo::ema_kernel<<<(n + 255) / 256, 256, 0, s>>>(s_hat, kth, n, alpha);
+int launch_ema(float *s_hat, const float *kth, int n, int stride, float alpha, cudaStream_t s) {
+  echo::ema_kernel<<<(n + 255) / 256, 256, 0, s>>>(s_hat, kth, n, stride, alpha);
   return check("ema");
 }
 

@@ -189,7 +189,7 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
       : "memory");
 }
 
-__device__ __forceinline__ void tma_load_3d_evict_first(void *dst, const CUtensorMap *map,
+__device__ __forceinline__ void tma_load_3d_hint(void *dst, const CUtensorMap *map,
                                                         uint64_t *bar, int32_t x, int32_t y,
                                                         int32_t z, uint64_t policy) {
   asm volatile(
@@ -203,6 +203,12 @@ __device__ __forceinline__ void tma_load_3d_evict_first(void *dst, const CUtenso
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
 

@@ -28,24 +28,9 @@
 #include <cstring>
 
 #include "echo_common.cuh"
+#include "prefetch_rows.cuh"
 
 ECHO_TRACE_UNIT(indexer)
-
-#ifdef ECHO_TRACE
-// development builds: per-CTA prefetch figures (rows copied, batches, slowest
-// batch in ns, sum of batch times in ns)
-static __device__ unsigned long long g_pf_diag[1024][4];
-extern "C" int echo_debug_pf_indexer(unsigned long long *out, int n) {
-  return cudaMemcpyFromSymbol(out, g_pf_diag, sizeof(unsigned long long) * 4 * (n < 1024 ? n : 1024)) ==
-                 cudaSuccess
-             ? 0
-             : 2;
-}
-extern "C" int echo_debug_pf_clear_indexer() {
-  static unsigned long long zeros[1024][4];
-  return cudaMemcpyToSymbol(g_pf_diag, zeros, sizeof(zeros)) == cudaSuccess ? 0 : 2;
-}
-#endif
 
 namespace echo {
 
@@ -58,7 +43,6 @@ constexpr int kPfWarps = 8;                  // each serves kEpiWarps / kPfWarps
 constexpr int kIndexerThreads = 32 * (2 + kEpiWarps + kPfWarps);
 constexpr int kAcc = 4;            // TMEM accumulators (MMA runs up to 3 tiles ahead of the epilogue)
 constexpr int kQueueCap = 64;      // entries per epilogue -> prefetch queue
-constexpr int kPfRowsPerBatch = 4; // rows one prefetch warp keeps in flight
 // host rows of the tiles (req_to_host slices, 128 x int32) staged by TMA for the
 // epilogue: a ring the producer may refill only after the epilogue read the tile
 // kR tiles back, which the k^I ring and the TMEM accumulators already guarantee
@@ -112,8 +96,6 @@ struct alignas(16) IndexerCtl {
   int queue_h[kEpiWarps][kQueueCap];  // their host rows (when the tiles' host rows are staged)
   float4 wsm[kEpiWarps][2 * kHeads / 4];  // head weights of the current request, per epilogue warp
 };
-
-__device__ __forceinline__ int clamp_ctx(int32_t L, int L_max) { return L < 0 ? 0 : (L > L_max ? L_max : L); }
 
 __device__ __forceinline__ int tiles_of(int L) { return (L + kTileTokens - 1) / kTileTokens; }
 
@@ -254,7 +236,7 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
         const int s = i % kStages;
         if (i >= kStages && !mbar_wait(&ctl->empty[s], ((i / kStages) & 1) ^ 1, abort, P.status)) break;
         mbar_arrive_expect_tx(&ctl->full[s], kTileBytes);
-        tma_load_3d_evict_first(k_smem + s * kTileBytes, &tmap_k, &ctl->full[s], 0, t * kTileTokens, b, policy);
+        tma_load_3d_hint(k_smem + s * kTileBytes, &tmap_k, &ctl->full[s], 0, t * kTileTokens, b, policy);
         if (rows_by_tma) {  // the tile's host rows, for the epilogue's prefetch candidates
           const int rs = i % kR;
           mbar_arrive_expect_tx(&ctl->r2h_full[rs], kRowMapBytes);
@@ -417,10 +399,7 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
     // ===================== prefetch copies =====================
     // prefetch warp e serves the queues of epilogue warps e, e + kPfWarps, ...
     const int pf = warp - 2 - kEpiWarps;
-    const int4 *host = reinterpret_cast<const int4 *>(P.host_kv);
     const bool direct = P.reserve != nullptr;
-    // destination rows: the staging area, or the GPU pool itself (direct to slot)
-    int4 *dst_rows = reinterpret_cast<int4 *>(direct ? P.gpu_kv : P.stage_rows);
     // reserve length (written by the recall before this kernel); once this warp has
     // seen the tickets pass it, later candidates are dropped without being read
     const int32_t res_len = direct ? __ldg(P.reserve_ctl + 1) : 0;
@@ -469,7 +448,7 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
       idle_since = 0;
       // ---- up to 32 queued tokens: host row, residency, ticket (one lane each)
       const int n = (tl - head) < 32 ? (tl - head) : 32;
-      int32_t h = -1, b = 0, dst = -1;
+      int32_t h = -1, b = 0;
       bool cand = false;
       if (lane < n) {
         const int tok = *reinterpret_cast<volatile int *>(&ctl->queue[e][(head + lane) % kQueueCap]);
@@ -488,110 +467,7 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
       turn = (turn + 1) % kQ;
       __syncwarp();
       if (lane == 0) *vhead = head;
-      const uint32_t cmask = __ballot_sync(0xffffffffu, cand);
-      if (direct && res_full) {
-        if (cmask && lane == 0) set_status(P.status, ECHO_DEV_PREFETCH_CAP_HIT);
-        continue;
-      }
-      // tickets: one atomic per request among the candidates (staging) or one for the
-      // warp's candidates (direct to slot); the result is needed only for the
-      // destinations, so the first host loads below start before it returns
-      uint32_t grp = 0;
-      int leader = 0, base = 0;
-      if (cand) {
-        grp = direct ? cmask : __match_any_sync(cmask, b);  // candidates sharing a counter
-        leader = __ffs(grp) - 1;
-        if (lane == leader) base = atomicAdd(direct ? P.reserve_ctl : P.stage_count + b, __popc(grp));
-      }
-      // ---- copy the candidate rows, kPfRowsPerBatch at a time (9 16-byte loads in flight
-      // per lane); a row whose ticket is past the cap is read but not stored
-      uint32_t rem = cmask;
-      bool have_tickets = false;
-      while (rem) {
-        int32_t hr[kPfRowsPerBatch], sl[kPfRowsPerBatch], dr[kPfRowsPerBatch];
-        int cnt = 0;
-#pragma unroll
-        for (int r = 0; r < kPfRowsPerBatch; ++r) {
-          int src_lane = 0;
-          if (rem) {
-            src_lane = __ffs(rem) - 1;
-            rem &= rem - 1;
-            ++cnt;
-          }
-          sl[r] = src_lane;
-          hr[r] = __shfl_sync(0xffffffffu, h, src_lane);
-        }
-        constexpr int kPer = (kPfRowsPerBatch * kKvChunks + 31) / 32;
-        int4 buf[kPer];
-#ifdef ECHO_TRACE
-        const uint64_t tb0 = globaltimer();
-#endif
-#pragma unroll
-        for (int m = 0; m < kPer; ++m) {
-          const int idx = m * 32 + lane;
-          const int r = idx / kKvChunks, c = idx % kKvChunks;
-          if (r < cnt) buf[m] = __ldcs(host + static_cast<size_t>(pick_reg(hr, r)) * kKvChunks + c);
-        }
-        if (!have_tickets) {
-          have_tickets = true;
-          if (direct) {
-            // ticket t places the row in reserved slot reserve[t]; the row's map entry
-            // is claimed first, so a row two requests share is placed once (the other
-            // ticket's slot stays reserved and the recall returns it)
-            const int base_w = __shfl_sync(0xffffffffu, base, __ffs(cmask) - 1);  // cmask != 0 here
-            res_full = base_w + __popc(cmask) >= res_len;
-            if (cand) {
-              const int ticket = base_w + __popc(cmask & ((1u << lane) - 1));
-              if (ticket < res_len) {
-                const int32_t s = __ldg(P.reserve + ticket);
-                if (s >= 0 && s < P.n_g && atomicCAS(P.host_to_gpu + h, kInf, s) == kInf) dst = s;
-              } else if (ticket == res_len) {
-                set_status(P.status, ECHO_DEV_PREFETCH_CAP_HIT);
-              }
-            }
-          } else if (cand) {
-            base = __shfl_sync(grp, base, leader);
-            const int ticket = base + __popc(grp & ((1u << lane) - 1));
-            {
-              const int L = clamp_ctx(__ldg(P.ctx_len + b), P.L_max);
-              int cap = (L + P.cap_div - 1) / P.cap_div;
-              cap = cap < P.stage_stride ? cap : P.stage_stride;
-              if (ticket < cap) {
-                dst = b * P.stage_stride + ticket;
-              } else if (ticket == cap) {
-                set_status(P.status, ECHO_DEV_PREFETCH_CAP_HIT);
-              }
-            }
-          }
-        }
-#pragma unroll
-        for (int r = 0; r < kPfRowsPerBatch; ++r) dr[r] = __shfl_sync(0xffffffffu, dst, sl[r]);
-#pragma unroll
-        for (int m = 0; m < kPer; ++m) {
-          const int idx = m * 32 + lane;
-          const int r = idx / kKvChunks, c = idx % kKvChunks;
-          const int32_t d = pick_reg(dr, r);
-          if (r < cnt && d >= 0) dst_rows[static_cast<size_t>(d) * kKvChunks + c] = buf[m];
-        }
-#ifdef ECHO_TRACE
-        __syncwarp();
-        if (lane == 0) {
-          const unsigned long long dt = globaltimer() - tb0;
-          atomicAdd(&g_pf_diag[blockIdx.x][0], static_cast<unsigned long long>(cnt));
-          atomicAdd(&g_pf_diag[blockIdx.x][1], 1ull);
-          atomicMax(&g_pf_diag[blockIdx.x][2], dt);
-          atomicAdd(&g_pf_diag[blockIdx.x][3], dt);
-        }
-#endif
-      }
-      if (dst >= 0) {
-        if (direct) {  // the row is resident from here on (its bytes are stored above)
-          P.to_host[dst] = h;
-          P.prio[dst] = kPrefetchedPrio;
-        } else {
-          P.stage_host[dst] = h;
-        }
-      }
+      prefetch_copy_batch(P, cand, h, b, res_len, res_full);
     }
     if (lane == 0) ECHO_TRACE_LAST_HERE(27);
   }

@@ -56,7 +56,11 @@ int main(void) {
   printf("echo_stage %zu\n", sizeof(echo_stage));
   printf("echo_indexer_args %zu\n", sizeof(echo_indexer_args));
   printf("echo_step_args %zu\n", sizeof(echo_step_args));
+  printf("echo_prefill_args %zu\n", sizeof(echo_prefill_args));
   P(echo_pool, counters) P(echo_pool, host_kv) P(echo_workspace, max_rows) P(echo_stage, cap_div)
+  P(echo_stage, reserve) P(echo_stage, reserve_ctl) P(echo_stage, reserve_cap)
+  P(echo_prefill_args, scores) P(echo_prefill_args, s_shift) P(echo_prefill_args, k) P(echo_prefill_args, thr_bin)
+  P(echo_prefill_args, stage) P(echo_prefill_args, dev_status)
   P(echo_indexer_args, scores) P(echo_indexer_args, dev_status) P(echo_step_args, k) P(echo_step_args, alpha)
   P(echo_step_args, clock) P(echo_step_args, advance_clock) P(echo_step_args, stage_events)
   return 0;
@@ -69,7 +73,8 @@ int main(void) {
         subprocess.check_call(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), c, "-o", exe])
         lines = dict(l.rsplit(" ", 1) for l in subprocess.check_output([exe], text=True).splitlines())
     sizes = {"echo_pool": echo.c_pool, "echo_workspace": echo.c_workspace, "echo_stage": echo.c_stage,
-             "echo_indexer_args": echo.c_indexer_args, "echo_step_args": echo.c_step_args}
+             "echo_indexer_args": echo.c_indexer_args, "echo_step_args": echo.c_step_args,
+             "echo_prefill_args": echo.c_prefill_args}
     for name, cls in sizes.items():
         assert int(lines[name]) == ctypes.sizeof(cls), name
     assert int(lines["echo_stats"]) == 8 * len(echo.STAT_FIELDS)
@@ -88,7 +93,8 @@ def test_argument_checks_reject_before_any_launch(lib):
     P = ctypes.c_void_p
     assert lib.echo_select_topk(16, 16, 1, 1, 10, 0, 16, 16, None) == echo.ECHO_EINVAL        # k = 0
     assert b"k must be" in lib.echo_last_error_string()
-    assert lib.echo_select_topk(16, 16, 1, 3, 10, 8, 16, 16, None) == echo.ECHO_EINVAL        # n_q = 3
+    assert lib.echo_select_topk(16, 16, 1, 0, 10, 8, 16, 16, None) == echo.ECHO_EINVAL        # n_q = 0
+    assert lib.echo_select_topk(16, 16, 1, 65537, 10, 8, 16, 16, None) == echo.ECHO_EINVAL    # n_q too large
     assert lib.echo_select_topk(None, 16, 1, 1, 10, 8, 16, 16, None) == echo.ECHO_EINVAL      # NULL
     a = echo.c_indexer_args(16, 16, 24, 16, 1, 1, 128, 16, None, None, None, None, None)       # misaligned k
     assert lib.echo_indexer_score(ctypes.byref(a), None) == echo.ECHO_EINVAL
@@ -96,6 +102,13 @@ def test_argument_checks_reject_before_any_launch(lib):
     a = echo.c_indexer_args(16, 16, 32, 16, 1, 1, 128, 16, 16, None, None, None, None)         # prefetch w/o pool
     assert lib.echo_indexer_score(ctypes.byref(a), None) == echo.ECHO_EINVAL
     assert lib.echo_ema_update(16, 16, 4, ctypes.c_float(1.5), None) == echo.ECHO_EINVAL       # alpha > 1
+    assert lib.echo_ema_update_strided(16, 16, 4, 0, ctypes.c_float(0.5), None) == echo.ECHO_EINVAL  # stride 0
+    a = echo.c_prefill_args(16, 16, 16, 16, 1, 0, 128, 16)                                     # C = 0
+    assert lib.echo_prefill_indexer_score(ctypes.byref(a), None) == echo.ECHO_EINVAL
+    a = echo.c_prefill_args(16, 24, 16, 16, 1, 4, 128, 16)                                     # misaligned w
+    assert lib.echo_prefill_indexer_score(ctypes.byref(a), None) == echo.ECHO_EINVAL
+    a = echo.c_prefill_args(16, 16, 16, 16, 1, 4, 128, 16, 16, 0)                               # s_shift, k = 0
+    assert lib.echo_prefill_indexer_score(ctypes.byref(a), None) == echo.ECHO_EINVAL
     n = ctypes.c_size_t()
     assert lib.echo_workspace_bytes(0, 10, ctypes.byref(n)) == echo.ECHO_EINVAL
     assert lib.echo_workspace_bytes(1000, 10, ctypes.byref(n)) == echo.ECHO_OK and n.value >= 4 * 1010
