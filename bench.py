@@ -402,6 +402,13 @@ def run_ours(args):
     h2d_gbs = (256 << 20) / (best * 1e-3) / 1e9
     recall_probe = recall_bandwidth_probe(echo, torch, host_t, flush_l2)
     volume_probe = indexer_volume_probe(echo, torch, inp, flush_l2, hbm_peak)
+    # the prefill chunk indexer (inter-query prefetch row): 1216 queries = 304 blocks of 4,
+    # two full waves on 152 SMs; FP8 tensor peak = the measured bf16 peak x 2
+    pre = prefill_probe(echo, torch, flush_l2, B=1, L_=32768, C=1216)
+    fp8_peak = 2.0 * float(peaks.get("bf16_tflops", 1900.0))
+    pre["roofline"] = {"bound": "tensor", "peak": fp8_peak, "unit": "TFLOP/s",
+                       "frac_scores": pre["tflops_scores"] / fp8_peak,
+                       "peak_source": ("measured bf16 x 2" if "bf16_tflops" in peaks else "fallback bf16 x 2")}
     direct = off = None
     if args.reserve > 0:
         direct = prefetch_mode_leg(echo, torch, st, host_t, q_ring, w, k_index, ctx, r2h_t, flush_l2,
@@ -439,6 +446,7 @@ def run_ours(args):
         "staged_rows_per_step": st_vals["staged"] / args.steps,
         "staged_used_per_step": st_vals["staged_used"] / args.steps,
         "evicted_per_step": st_vals["evicted"] / args.steps,
+        "prefill_chunk": pre,
         "direct_to_slot": direct,
         "prefetch_off": off,
         "stage_ms": {k: float(np.mean(v)) for k, v in stage_ms.items()},
@@ -472,12 +480,13 @@ def prefetch_mode_leg(echo, torch, st, host_t, q_ring, w, k_index, ctx, r2h_t, f
     """The same steps (same start state, same queries) with another prefetch mode:
     reserve > 0, direct to slot (rows land in `reserve` slots each recall sets aside,
     instead of the staging area); reserve = 0, no prefetch at all (the whole miss set
-    is recalled after the top-k).  Whole steps and the per-stage split, timed as in
-    the main loop."""
+    is recalled after the top-k); reserve < 0, the staging area again.  Whole steps
+    and the per-stage split, timed as in the main loop."""
     pool = echo.Pool(N_G, host_t)
     pool.load_state(st)
     ws = echo.Workspace(N_G, B * K_TOP)
-    stage = echo.Stage(B, reserve=reserve) if reserve > 0 else None
+    stage = echo.Stage(B, reserve=reserve) if reserve > 0 else (
+        echo.Stage(B, L // CAP_DIV, CAP_DIV) if reserve < 0 else None)
     out = echo.StepBuffers(B, 1, L, K_TOP)
     stats = echo.Stats()
     s_hat = torch.full((B, 1), float("inf"), dtype=torch.float32, device="cuda")
@@ -533,7 +542,8 @@ def prefetch_mode_leg(echo, torch, st, host_t, q_ring, w, k_index, ctx, r2h_t, f
     stage_ms = {name: float(np.mean([evs[t][i].elapsed_time(evs[t][i + 1]) for t in st_steps]))
                 for i, name in enumerate(("append", "indexer", "topk", "recall", "ema"))}
     per = float(np.mean(ms))
-    return {"mode": "direct to slot" if reserve > 0 else "no prefetch", "reserve_slots": reserve,
+    return {"mode": "direct to slot" if reserve > 0 else ("no prefetch" if reserve == 0 else "staging"),
+            "reserve_slots": max(reserve, 0),
             "value": 1e3 / per, "unit": "steps/s", "ms_per_step": per,
             "hit_rate": sv["hits"] / max(1, sv["unique_rows"]),
             "recalled_rows_per_step": sv["recalled"] / n_timed,
@@ -543,10 +553,13 @@ def prefetch_mode_leg(echo, torch, st, host_t, q_ring, w, k_index, ctx, r2h_t, f
             "stage_ms": stage_ms, "dev_status": status}
 
 
-def warm_host_translations(echo, torch, host_t, page_bytes=65536):
-    """Read one row per page of the pinned host pool through the recall kernel, so the
-    GPU has translated every page once before timing (in serving the pool is read every
-    step; a cold translation costs far more than the read)."""
+def warm_host_translations(echo, torch, host_t, page_bytes=0):
+    """Read the pinned host pool through the recall kernel before timing -- every row by
+    default, else one row per `page_bytes` -- so the GPU has translated every page and
+    the pool's lines have made one trip over the host link since the CPU wrote them (in
+    serving the pool is read every step; a cold translation costs far more than the
+    read, and on freshly written pages the first reads were seen to run several times
+    slower for about a second)."""
     n_h = host_t.shape[0]
     step = max(1, page_bytes // (host_t.shape[1] * 2))
     rows = np.arange(0, n_h, step, dtype=np.int32)
@@ -618,6 +631,47 @@ def indexer_volume_probe(echo, torch, inp, flush_l2, hbm_peak, batches=(8, 24, 6
     return res
 
 
+def prefill_probe(echo, torch, flush_l2, B=1, L_=32768, C=512, k=K_TOP, reps=3, seed=21):
+    """The prefill chunk indexer (the last C tokens of each request as queries, causal):
+    scores only, then with the approximate top-k (shift = the k-th score of the chunk's
+    last query).  Median CUDA-event time of `reps` launches, L2 flushed before each.
+    FLOP = 2 * 64 * 128 per (query, visible key)."""
+    from sparse_attention_kv_fp8_gb300 import workload as wl
+    inp = wl.indexer_inputs(B, C, L_, L_, seed=seed)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    q, w, k_index, ctx = dev(inp.q), dev(inp.w), dev(inp.k_index), dev(inp.ctx_len)
+    scores = torch.empty((B, C, L_), dtype=torch.float32, device="cuda")
+    thr = torch.empty((B, C), dtype=torch.int32, device="cuda")
+    sub = torch.empty((B, C), dtype=torch.int32, device="cuda")
+    echo.echo_prefill_indexer_score(q, w, k_index, ctx, scores)
+    torch.cuda.synchronize()
+    last = scores[:, C - 1, :].cpu().numpy()
+    shift = torch.from_numpy(np.array([np.sort(last[b])[::-1][k - 1] for b in range(B)], np.float32)).cuda()
+
+    def timed(fn):
+        ts = []
+        for _ in range(reps):
+            flush_l2()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record()
+            fn()
+            a1.record()
+            torch.cuda.synchronize()
+            ts.append(a0.elapsed_time(a1))
+        return float(np.median(ts))
+
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        ms_plain = timed(lambda: echo.echo_prefill_indexer_score(q, w, k_index, ctx, scores))
+        ms_approx = timed(lambda: echo.echo_prefill_indexer_score(q, w, k_index, ctx, scores, s_shift=shift, k=k,
+                                                                  thr_bin=thr, subset_n=sub))
+    pairs = int(sum(max(0, int(inp.ctx_len[b]) - (C - 1 - i)) for b in range(B) for i in range(C)))
+    flop = 2.0 * 64 * 128 * pairs
+    return {"B": B, "L": L_, "C": C, "k": k, "query_key_pairs": pairs, "flop": flop,
+            "ms_scores": ms_plain, "tflops_scores": flop / (ms_plain * 1e-3) / 1e12,
+            "ms_with_approx_topk": ms_approx, "tflops_with_approx_topk": flop / (ms_approx * 1e-3) / 1e12,
+            "mean_subset_of_k": float(sub.float().mean().item()) / k, "clocks": clk.summary()}
+
+
 def run_kernel_case(args):
     """Single-kernel case for profilers: the indexer with the fused prefetch
     (threshold = each row's k-th score, 97% of the top-k resident) on B x L tokens,
@@ -629,6 +683,11 @@ def run_kernel_case(args):
     import sparse_attention_kv_fp8_gb300 as echo
     from sparse_attention_kv_fp8_gb300 import workload as wl
     Bk, Lk = args.B, args.L
+    if args.kernel == "prefill":
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        res = prefill_probe(echo, torch, flush.zero_, B=Bk, L_=Lk, C=args.C, reps=args.reps)
+        print(json.dumps({"kernel_case": "prefill", **res}))
+        return 0
     inp = wl.indexer_inputs(Bk, 1, Lk, Lk, seed=3)
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     n_h = Bk * Lk
@@ -675,11 +734,12 @@ def main():
     ap.add_argument("--reserve", type=int, default=8192,
                     help="slots per recall for the direct-to-slot comparison leg (0: skip it and the "
                          "no-prefetch leg)")
-    ap.add_argument("--kernel", default=None, choices=[None, "indexer"],
+    ap.add_argument("--kernel", default=None, choices=[None, "indexer", "prefill"],
                     help="run one kernel on a small case (for profilers) instead of the benchmark")
     ap.add_argument("--B", type=int, default=24)
     ap.add_argument("--L", type=int, default=65536)
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--C", type=int, default=512, help="queries per request of the prefill kernel case")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.kernel:

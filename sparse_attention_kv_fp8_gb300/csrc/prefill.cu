@@ -276,6 +276,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
           tmem_ld_32x32b_x32(taddr + j * kHeads, v0);
           tmem_ld_32x32b_x32(taddr + j * kHeads + 32, v1);
           tmem_wait_ld();
+          reg_fence_32(v0);
+          reg_fence_32(v1);
           const float4 *w4 = wsm4 + j * (kHeads / 4);
           float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
