@@ -94,6 +94,8 @@ def lib():
             L.orc_approx_topk_bins.restype = I
             L.orc_prefill_candidates.argtypes = [P, P, P, I, I, I, I, I, P, P, I, P, P, P, P]
             L.orc_prefill_candidates.restype = None
+            L.orc_sparse_mla_decode.argtypes = [P, P, I, P, I, I, I, I, I, I, I, ctypes.c_double, P, P]
+            L.orc_sparse_mla_decode.restype = None
             L.orc_ema_update.argtypes = [P, P, I, F]
             L.orc_ema_update.restype = None
             L.orc_metadata_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64]
@@ -213,6 +215,22 @@ def prefill_candidates(scores, s_hat, ctx_len, k: int, qb: int, req_to_host, hos
     lib().orc_prefill_candidates(_p(scores), _p(s_hat), _p(ctx_len), B, C, L_max, int(k), int(qb),
                                  _p(req_to_host), _p(h2g), h2g.size, _p(thr), _p(sub), _p(cand), _p(cnt))
     return thr, sub, [[cand[b, i, :cnt[b, i]].copy() for i in range(nb)] for b in range(B)]
+
+
+def sparse_mla_decode(q, gpu_kv, out_slot, scale: float, dv: int = 512):
+    """Attention of each query token's heads over its selected latent rows (fp64):
+    q [B][n_q][H][dqk] bf16 bits (uint16), gpu_kv [n_g][row] bf16 bits, out_slot
+    [B][n_q][k] (-1 = skipped).  Returns (o [B][n_q][H][dv], lse [B][n_q][H]) float64."""
+    q = _arr(q, np.uint16)
+    kv = _arr(gpu_kv, np.uint16)
+    sl = _arr(out_slot, np.int32)
+    B, n_q, H, dqk = q.shape
+    k = sl.shape[2]
+    o = np.empty((B, n_q, H, dv), np.float64)
+    lse = np.empty((B, n_q, H), np.float64)
+    lib().orc_sparse_mla_decode(_p(q), _p(kv), kv.shape[1], _p(sl), B, n_q, H, dqk, dv, k, kv.shape[0],
+                                float(scale), _p(o), _p(lse))
+    return o, lse
 
 
 # ---------------------------------------------------------------------------

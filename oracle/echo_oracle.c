@@ -805,6 +805,75 @@ void orc_ema_update(float *s_hat, const float *kth, int n, float alpha)
     }
 }
 
+/* ------------------------------------------------------------------------- */
+/* Sparse MLA decode over the selected rows (section 2, MLA; section 3.2)     */
+/* ------------------------------------------------------------------------- */
+
+/* bf16 bits -> double (exact) */
+static double orc_bf16(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof(f));
+    return (double)f;
+}
+
+/*
+ * Attention of query token (b, j) over its selected latent rows (MLA with the key
+ * and value up-projections absorbed into the query and the output: every head reads
+ * the same d_c + rope latent row).  For head h:
+ *   s_i = scale * sum_{d < dqk} q[b][j][h][d] * kv[slot_i][d]     (dqk = 576)
+ *   o[d] = sum_i softmax(s)_i * kv[slot_i][d]                      (d < dv = 512)
+ *   lse = log(sum_i exp(s_i))
+ * over the selected entries i < k whose slot (out_slot[b][j][i]) is >= 0; a row with
+ * no such entry gives o = 0 and lse = -inf.  Everything in fp64 from the bf16 inputs.
+ *   q [B][n_q][H][dqk] bf16; kv [n_g][row] bf16; out_slot [B][n_q][k];
+ *   o [B][n_q][H][dv] double; lse [B][n_q][H] double.
+ */
+void orc_sparse_mla_decode(const uint16_t *q, const uint16_t *kv, int row, const int32_t *out_slot, int B,
+                           int n_q, int H, int dqk, int dv, int k, int n_g, double scale, double *o, double *lse)
+{
+    double *s = (double *)malloc(sizeof(double) * (size_t)(k > 0 ? k : 1));
+    for (int b = 0; b < B; ++b)
+        for (int j = 0; j < n_q; ++j)
+            for (int h = 0; h < H; ++h) {
+                const uint16_t *qh = q + (((size_t)b * n_q + j) * H + h) * dqk;
+                const int32_t *sl = out_slot + ((size_t)b * n_q + j) * k;
+                double *oh = o + (((size_t)b * n_q + j) * H + h) * dv;
+                double m = -INFINITY;
+                for (int i = 0; i < k; ++i) {
+                    s[i] = -INFINITY;
+                    if (sl[i] < 0 || sl[i] >= n_g)
+                        continue;
+                    const uint16_t *r = kv + (size_t)sl[i] * row;
+                    double acc = 0.0;
+                    for (int d = 0; d < dqk; ++d)
+                        acc += orc_bf16(qh[d]) * orc_bf16(r[d]);
+                    s[i] = scale * acc;
+                    if (s[i] > m)
+                        m = s[i];
+                }
+                for (int d = 0; d < dv; ++d)
+                    oh[d] = 0.0;
+                double l = 0.0;
+                if (m != -INFINITY) {
+                    for (int i = 0; i < k; ++i) {
+                        if (s[i] == -INFINITY)
+                            continue;
+                        double p = exp(s[i] - m);
+                        l += p;
+                        const uint16_t *r = kv + (size_t)sl[i] * row;
+                        for (int d = 0; d < dv; ++d)
+                            oh[d] += p * orc_bf16(r[d]);
+                    }
+                    for (int d = 0; d < dv; ++d)
+                        oh[d] /= l;
+                }
+                lse[((size_t)b * n_q + j) * H + h] = m == -INFINITY ? -INFINITY : m + log(l);
+            }
+    free(s);
+}
+
 /* storage law of the five metadata arrays (section 5.1): 4 N_H + 13 N_G bytes */
 int64_t orc_metadata_bytes(int64_t n_h, int64_t n_g)
 {

@@ -30,7 +30,7 @@ KV_BYTES = KV_ELEMS * 2
 INF_I32 = 2**31 - 1   # the "empty" sentinel of the residency maps
 
 # stream ids, so that every array has its own independent draw
-_S_Q, _S_W, _S_K, _S_KV, _S_POOL, _S_EPS, _S_NEWKV, _S_NEWK = range(1, 9)
+_S_Q, _S_W, _S_K, _S_KV, _S_POOL, _S_EPS, _S_NEWKV, _S_NEWK, _S_MLAQ = range(1, 10)
 
 
 def rng(seed: int, stream: int) -> np.random.Generator:
@@ -167,6 +167,13 @@ def new_tokens(B: int, seed: int, step: int):
     kv = bf16_encode(rng(seed * 1000003 + step, _S_NEWKV).standard_normal(size=(B, KV_ELEMS), dtype=np.float32))
     kI = fp8_normal(rng(seed * 1000003 + step, _S_NEWK), (B, D_INDEX))
     return kv, kI
+
+
+def mla_queries(B: int, n_q: int, seed: int, heads: int = 128) -> np.ndarray:
+    """Absorbed MLA queries [B][n_q][heads][576] bf16 bits, N(0,1) draws (section 2: the
+    attention has 128 heads over the 512 + 64 latent row)."""
+    g = rng(seed, _S_MLAQ)
+    return bf16_encode(g.standard_normal(size=(B, n_q, heads, KV_ELEMS), dtype=np.float32))
 
 
 def req_to_host(B: int, L_max: int, base: int = 0) -> np.ndarray:
