@@ -357,6 +357,42 @@ int echo_ema_update(float *s_hat, const float *kth, int32_t n, float alpha, void
 int echo_ema_update_strided(float *s_hat, const float *kth, int32_t n, int32_t kth_stride, float alpha,
                             void *stream);
 
+/*
+ * Sparse MLA decode over the selected rows (section 2: MLA's latent row of d_c = 512 +
+ * 64 rope dims is shared by all 128 heads; the indexer's top-k feeds sparse attention).
+ * With the up-projections absorbed, head h of query token (b, j) attends over the
+ * rows out_slot[b][j][0..k) names in the GPU pool:
+ *   s_i = scale * q[b][j][h] . gpu_kv[slot_i]            (576 dims, fp32 accumulate)
+ *   out[b][j][h] = sum_i softmax(s)_i * gpu_kv[slot_i][0..512)
+ *   lse[b][j][h] = log sum_i exp(s_i)
+ * Entries with slot < 0 are skipped (slot >= n_g: also ECHO_DEV_BAD_INDEX); a head
+ * with no row gives out = 0, lse = -inf.  The softmax weights enter the value product
+ * rounded to bf16 (the tensor cores' operand type); everything else is fp32.
+ *   q       [B][n_q][128][576] bf16 device, 16-byte aligned
+ *   gpu_kv  [n_g][576] bf16 device (the pool's rows)
+ *   out_slot [B][n_q][k] int32 device, 1 <= k <= 8192
+ *   out     [B][n_q][128][512] fp32 device;  lse [B][n_q][128] fp32 device
+ *   workspace  device, 256-byte aligned, echo_mla_workspace_bytes() bytes
+ * Launches 2 kernels (one CTA per 128 selected rows of each query token, then the
+ * merge of their partial results).
+ */
+typedef struct echo_mla_args {
+    const uint16_t *q;
+    const uint16_t *gpu_kv;
+    int32_t n_g;
+    const int32_t *out_slot;
+    int32_t B, n_q, k;
+    float scale;
+    float *out;
+    float *lse;
+    void *workspace;
+    size_t workspace_bytes;
+    int32_t *dev_status;
+} echo_mla_args;
+
+int echo_mla_workspace_bytes(int32_t B, int32_t n_q, int32_t k, size_t *bytes);
+int echo_sparse_mla_decode(const echo_mla_args *args, void *stream);
+
 /* Stages of echo_decode_step, in order (timing events are recorded before each
    stage and after the last).  The EMA is computed by the recall's last kernel, so
    the ECHO_STAGE_EMA interval is empty; the constant is kept for the event layout. */
@@ -425,7 +461,7 @@ const char *echo_last_error_string(void);
 
 /* Library version, (major << 16) | minor (1.1: echo_stage's direct-to-slot fields;
    1.2: echo_prefill_indexer_score, echo_ema_update_strided, n_q up to 65536 in
-   top-k and recall). */
+   top-k and recall; 1.3: echo_sparse_mla_decode). */
 int32_t echo_version(void);
 
 /* Storage law of the metadata arrays of one pool (section 5.1): 4*n_h + 13*n_g. */

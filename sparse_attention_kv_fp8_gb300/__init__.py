@@ -65,6 +65,12 @@ class c_prefill_args(ctypes.Structure):
                 ("dev_status", _P)]
 
 
+class c_mla_args(ctypes.Structure):
+    _fields_ = [("q", _P), ("gpu_kv", _P), ("n_g", _I32), ("out_slot", _P), ("B", _I32), ("n_q", _I32),
+                ("k", _I32), ("scale", ctypes.c_float), ("out", _P), ("lse", _P), ("workspace", _P),
+                ("workspace_bytes", ctypes.c_size_t), ("dev_status", _P)]
+
+
 class c_step_args(ctypes.Structure):
     _fields_ = [("pool", ctypes.POINTER(c_pool)), ("ws", ctypes.POINTER(c_workspace)),
                 ("stage", ctypes.POINTER(c_stage)), ("q", _P), ("w", _P), ("k_index", _P), ("ctx_len", _P),
@@ -106,6 +112,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "echo_ema_update": ([_P, _P, _I32, ctypes.c_float, _P], S),
         "echo_ema_update_strided": ([_P, _P, _I32, _I32, ctypes.c_float, _P], S),
         "echo_prefill_indexer_score": ([ctypes.POINTER(c_prefill_args), _P], S),
+        "echo_mla_workspace_bytes": ([_I32, _I32, _I32, ctypes.POINTER(ctypes.c_size_t)], S),
+        "echo_sparse_mla_decode": ([ctypes.POINTER(c_mla_args), _P], S),
         "echo_decode_step": ([ctypes.POINTER(c_step_args), _P], S),
         "echo_last_error_string": ([], ctypes.c_char_p),
         "echo_version": ([], _I32),
@@ -350,6 +358,28 @@ def echo_append(pool: Pool, ws: Workspace, k_index, ctx_len, req_to_host, new_kv
 def echo_ema_update(s_hat, kth, alpha: float = 0.5, stream=None):
     _check(load_library().echo_ema_update(_dev(s_hat, "s_hat"), _dev(kth, "kth"), int(s_hat.numel()),
                                           float(alpha), _stream(stream)), "echo_ema_update")
+
+
+class MlaWorkspace:
+    """Scratch of echo_sparse_mla_decode for B requests, n_q queries, k selected rows."""
+
+    def __init__(self, B: int, n_q: int, k: int, device="cuda"):
+        n = ctypes.c_size_t()
+        _check(load_library().echo_mla_workspace_bytes(B, n_q, k, ctypes.byref(n)), "echo_mla_workspace_bytes")
+        self.buf = torch.empty(n.value + 256, dtype=torch.uint8, device=device)
+        self.base = (self.buf.data_ptr() + 255) & ~255
+        self.bytes = n.value
+
+
+def echo_sparse_mla_decode(q, gpu_kv, out_slot, scale: float, out, lse, ws: MlaWorkspace, dev_status=None,
+                           stream=None):
+    """q [B][n_q][128][576] bf16 (int16 bits), gpu_kv [n_g][576] (the pool's rows),
+    out_slot [B][n_q][k]; out [B][n_q][128][512] fp32, lse [B][n_q][128] fp32."""
+    B, n_q, k = out_slot.shape
+    a = c_mla_args(_dev(q, "q"), _dev(gpu_kv, "gpu_kv"), int(gpu_kv.shape[0]), _dev(out_slot, "out_slot"), B, n_q,
+                   k, float(scale), _dev(out, "out"), _dev(lse, "lse"), ws.base, ws.bytes,
+                   _dev(dev_status, "dev_status"))
+    _check(load_library().echo_sparse_mla_decode(ctypes.byref(a), _stream(stream)), "echo_sparse_mla_decode")
 
 
 def echo_ema_update_strided(s_hat, kth, kth_stride: int, alpha: float = 0.5, stream=None):

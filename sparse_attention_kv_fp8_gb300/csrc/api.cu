@@ -51,6 +51,8 @@ int launch_append(const echo_pool *pool, const echo_workspace *ws, uint8_t *k_in
                   int32_t clock, const int32_t *clock_dev, echo_stats *stats, int32_t *status, cudaStream_t s);
 int launch_ema(float *s_hat, const float *kth, int n, int stride, float alpha, cudaStream_t s);
 int launch_prefill_indexer(const echo_prefill_args *a, cudaStream_t stream);
+size_t mla_workspace_bytes(int32_t B, int32_t n_q, int32_t k);
+int launch_sparse_mla(const echo_mla_args *a, cudaStream_t stream);
 int noalloc_workspace(int32_t n_g, int32_t rows, echo_workspace *out);
 
 }  // namespace echo_host
@@ -146,7 +148,7 @@ int echo_selftest_wait_timeout(int32_t which, int32_t *dev_status, void *stream)
   return launch_wait_probe(which, dev_status, static_cast<cudaStream_t>(stream));
 }
 
-int32_t echo_version(void) { return (1 << 16) | 2; }
+int32_t echo_version(void) { return (1 << 16) | 3; }
 
 int64_t echo_metadata_bytes(int64_t n_h, int64_t n_g) {
   return static_cast<int64_t>(sizeof(int32_t)) * n_h +
@@ -304,6 +306,31 @@ int echo_ema_update_strided(float *s_hat, const float *kth, int32_t n, int32_t k
   REQUIRE(static_cast<long long>(n) * kth_stride <= (1ll << 31) - 1, "n * kth_stride too large");
   if (n == 0) return ECHO_OK;
   return launch_ema(s_hat, kth, n, kth_stride, alpha, static_cast<cudaStream_t>(stream));
+}
+
+int echo_mla_workspace_bytes(int32_t B, int32_t n_q, int32_t k, size_t *bytes) {
+  g_err[0] = 0;
+  REQUIRE(bytes, "bytes is NULL");
+  REQUIRE(B >= 0 && n_q >= 1 && n_q <= 65536 && k >= 1 && k <= 8192, "bad sizes (B %d, n_q %d, k %d)", B, n_q, k);
+  *bytes = mla_workspace_bytes(B, n_q, k);
+  return ECHO_OK;
+}
+
+int echo_sparse_mla_decode(const echo_mla_args *a, void *stream) {
+  g_err[0] = 0;
+  REQUIRE(a, "args is NULL");
+  REQUIRE(a->B >= 0 && a->n_q >= 1 && a->n_q <= 65536, "bad sizes (B %d, n_q %d)", a->B, a->n_q);
+  REQUIRE(a->k >= 1 && a->k <= 8192, "k must be in [1, 8192] (got %d)", a->k);
+  REQUIRE(a->n_g >= 1, "n_g must be >= 1");
+  if (a->B == 0) return ECHO_OK;
+  REQUIRE(a->q && a->gpu_kv && a->out_slot && a->out && a->lse && a->workspace, "MLA pointer is NULL");
+  REQUIRE(aligned(a->q, 16) && aligned(a->gpu_kv, 16), "q and gpu_kv must be 16-byte aligned");
+  REQUIRE(aligned(a->out, 16) && aligned(a->workspace, 256), "out must be 16-byte and workspace 256-byte aligned");
+  REQUIRE(static_cast<long long>(a->B) * a->n_q * 128 <= (1ll << 31) - 1, "B * n_q too large");
+  REQUIRE(std::isfinite(a->scale), "scale must be finite");
+  REQUIRE(a->workspace_bytes >= mla_workspace_bytes(a->B, a->n_q, a->k), "workspace smaller than "
+          "echo_mla_workspace_bytes()");
+  return launch_sparse_mla(a, static_cast<cudaStream_t>(stream));
 }
 
 int echo_prefill_indexer_score(const echo_prefill_args *a, void *stream) {

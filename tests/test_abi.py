@@ -57,10 +57,12 @@ int main(void) {
   printf("echo_indexer_args %zu\n", sizeof(echo_indexer_args));
   printf("echo_step_args %zu\n", sizeof(echo_step_args));
   printf("echo_prefill_args %zu\n", sizeof(echo_prefill_args));
+  printf("echo_mla_args %zu\n", sizeof(echo_mla_args));
   P(echo_pool, counters) P(echo_pool, host_kv) P(echo_workspace, max_rows) P(echo_stage, cap_div)
   P(echo_stage, reserve) P(echo_stage, reserve_ctl) P(echo_stage, reserve_cap)
   P(echo_prefill_args, scores) P(echo_prefill_args, s_shift) P(echo_prefill_args, k) P(echo_prefill_args, thr_bin)
   P(echo_prefill_args, stage) P(echo_prefill_args, dev_status)
+  P(echo_mla_args, scale) P(echo_mla_args, workspace_bytes) P(echo_mla_args, dev_status)
   P(echo_indexer_args, scores) P(echo_indexer_args, dev_status) P(echo_step_args, k) P(echo_step_args, alpha)
   P(echo_step_args, clock) P(echo_step_args, advance_clock) P(echo_step_args, stage_events)
   return 0;
@@ -74,7 +76,7 @@ int main(void) {
         lines = dict(l.rsplit(" ", 1) for l in subprocess.check_output([exe], text=True).splitlines())
     sizes = {"echo_pool": echo.c_pool, "echo_workspace": echo.c_workspace, "echo_stage": echo.c_stage,
              "echo_indexer_args": echo.c_indexer_args, "echo_step_args": echo.c_step_args,
-             "echo_prefill_args": echo.c_prefill_args}
+             "echo_prefill_args": echo.c_prefill_args, "echo_mla_args": echo.c_mla_args}
     for name, cls in sizes.items():
         assert int(lines[name]) == ctypes.sizeof(cls), name
     assert int(lines["echo_stats"]) == 8 * len(echo.STAT_FIELDS)
@@ -109,6 +111,11 @@ def test_argument_checks_reject_before_any_launch(lib):
     assert lib.echo_prefill_indexer_score(ctypes.byref(a), None) == echo.ECHO_EINVAL
     a = echo.c_prefill_args(16, 16, 16, 16, 1, 4, 128, 16, 16, 0)                               # s_shift, k = 0
     assert lib.echo_prefill_indexer_score(ctypes.byref(a), None) == echo.ECHO_EINVAL
+    m = echo.c_mla_args(16, 16, 10, 16, 1, 1, 0, ctypes.c_float(0.1), 16, 16, 256, 1 << 30)      # k = 0
+    assert lib.echo_sparse_mla_decode(ctypes.byref(m), None) == echo.ECHO_EINVAL
+    m = echo.c_mla_args(16, 16, 10, 16, 1, 1, 64, ctypes.c_float(0.1), 16, 16, 256, 16)          # small workspace
+    assert lib.echo_sparse_mla_decode(ctypes.byref(m), None) == echo.ECHO_EINVAL
+    assert b"workspace" in lib.echo_last_error_string()
     n = ctypes.c_size_t()
     assert lib.echo_workspace_bytes(0, 10, ctypes.byref(n)) == echo.ECHO_EINVAL
     assert lib.echo_workspace_bytes(1000, 10, ctypes.byref(n)) == echo.ECHO_OK and n.value >= 4 * 1010
