@@ -405,6 +405,7 @@ def run_ours(args):
     # the prefill chunk indexer (inter-query prefetch row): 1216 queries = 304 blocks of 4,
     # two full waves on 152 SMs; FP8 tensor peak = the measured bf16 peak x 2
     pre = prefill_probe(echo, torch, flush_l2, B=1, L_=32768, C=1216)
+    mla = mla_probe(echo, torch, flush_l2, pool, out.out_slot, hbm_peak, float(peaks.get("bf16_tflops", 1900.0)))
     fp8_peak = 2.0 * float(peaks.get("bf16_tflops", 1900.0))
     pre["roofline"] = {"bound": "tensor", "peak": fp8_peak, "unit": "TFLOP/s",
                        "frac_scores": pre["tflops_scores"] / fp8_peak,
@@ -447,6 +448,7 @@ def run_ours(args):
         "staged_used_per_step": st_vals["staged_used"] / args.steps,
         "evicted_per_step": st_vals["evicted"] / args.steps,
         "prefill_chunk": pre,
+        "sparse_mla_decode": mla,
         "direct_to_slot": direct,
         "prefetch_off": off,
         "stage_ms": {k: float(np.mean(v)) for k, v in stage_ms.items()},
@@ -672,6 +674,50 @@ def prefill_probe(echo, torch, flush_l2, B=1, L_=32768, C=512, k=K_TOP, reps=3, 
             "mean_subset_of_k": float(sub.float().mean().item()) / k, "clocks": clk.summary()}
 
 
+def mla_probe(echo, torch, flush_l2, pool, out_slot, hbm_peak, bf16_peak, reps=5, seed=31):
+    """Sparse MLA decode over the decode step's own selection (out_slot of the last
+    timed step, rows in the step's GPU pool): 128 heads x 576-dim absorbed queries.
+    Median CUDA-event time of `reps` graph replays (both kernels), L2 flushed before each.
+    FLOP = 2 * 128 * (576 + 512) per (query token, selected row); algorithmic bytes =
+    the selected rows (1152 B each) + q + out + lse."""
+    from sparse_attention_kv_fp8_gb300 import workload as wl
+    Bq, n_q, k = out_slot.shape
+    q = torch.from_numpy(wl.mla_queries(Bq, n_q, seed).view(np.int16)).cuda()
+    out = torch.empty((Bq, n_q, 128, 512), dtype=torch.float32, device="cuda")
+    lse = torch.empty((Bq, n_q, 128), dtype=torch.float32, device="cuda")
+    ws = echo.MlaWorkspace(Bq, n_q, k)
+    scale = 1.0 / float(np.sqrt(192.0))
+    echo.echo_sparse_mla_decode(q, pool.gpu_kv, out_slot, scale, out, lse, ws)
+    torch.cuda.synchronize()
+    # replayed from a CUDA graph, as inside a captured decode step (no host launch work
+    # between the events)
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g, stream=cap):
+            echo.echo_sparse_mla_decode(q, pool.gpu_kv, out_slot, scale, out, lse, ws)
+    torch.cuda.current_stream().wait_stream(cap)
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        flush_l2()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record()
+        g.replay()
+        a1.record()
+        torch.cuda.synchronize()
+        ts.append(a0.elapsed_time(a1))
+    ms = float(np.median(ts))
+    rows = int((out_slot >= 0).sum().item())
+    flop = 2.0 * 128 * (576 + 512) * rows
+    nbytes = rows * 1152 + q.numel() * 2 + out.numel() * 4 + lse.numel() * 4
+    return {"B": Bq, "n_q": n_q, "k": k, "rows": rows, "us": ms * 1e3,
+            "tflops": flop / (ms * 1e-3) / 1e12, "frac_bf16_peak": flop / (ms * 1e-3) / 1e12 / bf16_peak,
+            "gbs": nbytes / (ms * 1e-3) / 1e9, "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm_peak,
+            "workspace_bytes": ws.bytes}
+
+
 def run_kernel_case(args):
     """Single-kernel case for profilers: the indexer with the fused prefetch
     (threshold = each row's k-th score, 97% of the top-k resident) on B x L tokens,
@@ -683,6 +729,22 @@ def run_kernel_case(args):
     import sparse_attention_kv_fp8_gb300 as echo
     from sparse_attention_kv_fp8_gb300 import workload as wl
     Bk, Lk = args.B, args.L
+    if args.kernel == "mla":
+        # the decode shape's selection over a full 200K-slot pool of random rows
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        pool_kv = torch.from_numpy(wl.bf16_encode(np.random.default_rng(7).standard_normal(
+            (N_G, echo.KV_ELEMS), dtype=np.float32)).view(np.int16)).cuda()
+
+        class _Pool:
+            gpu_kv = pool_kv
+        g = np.random.default_rng(8)
+        sl = torch.from_numpy(np.stack([g.choice(N_G, size=args.k, replace=False) for _ in range(Bk)])
+                              .astype(np.int32)[:, None, :]).cuda()
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        res = mla_probe(echo, torch, flush.zero_, _Pool, sl, float(peaks["hbm_gbs"]), float(peaks["bf16_tflops"]),
+                        reps=args.reps)
+        print(json.dumps({"kernel_case": "mla", **res}))
+        return 0
     if args.kernel == "prefill":
         flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
         res = prefill_probe(echo, torch, flush.zero_, B=Bk, L_=Lk, C=args.C, reps=args.reps)
@@ -734,12 +796,13 @@ def main():
     ap.add_argument("--reserve", type=int, default=8192,
                     help="slots per recall for the direct-to-slot comparison leg (0: skip it and the "
                          "no-prefetch leg)")
-    ap.add_argument("--kernel", default=None, choices=[None, "indexer", "prefill"],
+    ap.add_argument("--kernel", default=None, choices=[None, "indexer", "prefill", "mla"],
                     help="run one kernel on a small case (for profilers) instead of the benchmark")
     ap.add_argument("--B", type=int, default=24)
     ap.add_argument("--L", type=int, default=65536)
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--C", type=int, default=512, help="queries per request of the prefill kernel case")
+    ap.add_argument("--k", type=int, default=K_TOP, help="selected rows per query of the MLA kernel case")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.kernel:

@@ -10,22 +10,32 @@
 // slot_i = out_slot[b][j][i]; entries with slot < 0 are skipped.
 //
 // sm_103a design (split over the selected rows, then a combine kernel):
-//   one CTA (4 warps) per (b, j, 128 selected rows):
-//     q    128 heads x 576 bf16 by TMA into nine 128-byte-swizzled 64-dim blocks;
-//     pass A  the 128 rows gathered 16 at a time (16-byte loads by slot, written in the
-//          same swizzled layout, double buffered) and S = q . rows^T on tcgen05
-//          (kind::f16, bf16 x bf16 -> fp32, M = 128 heads, N = 16 rows, K = 576) into
-//          TMEM columns 0..127;
-//     softmax  one thread per head: its S row from TMEM, scale, mask, max, exp, sum;
-//          P (bf16) into shared memory as the next MMA's K-major operand;
-//     pass B  the rows gathered again (512 dims; they are in L2) and O += P . V on
-//          tcgen05 with V as an MN-major operand (the same swizzled tile, read along
-//          the rows), two N = 256 MMAs per 16 rows into all 512 TMEM columns;
-//     partial O, max and sum per head to a workspace;
-//   combine: per (b, j, head) the splits' partials merged with their maxima.
+//   one CTA (8 warps: two per TMEM lane quadrant, splitting the columns) per
+//   (b, j, 128 selected rows):
+//     rows   the 128 rows (576 bf16 each) copied by slot straight into shared memory
+//          with cp.async (every 16-byte piece in flight at once), as nine 64-dim blocks
+//          in the 128-byte swizzle: one tile that serves both products;
+//     pass A  q's nine 64-dim blocks (128 heads each) stream in by TMA through a
+//          5-stage ring (a stage is refilled once the MMAs of the block before the
+//          current one are done); four tcgen05 MMAs per block (kind::f16, bf16 x
+//          bf16 -> fp32, M = 128 heads, N = 128 rows, K = 16) accumulate S in TMEM
+//          columns 0..127;
+//     softmax  two threads per head, 64 columns each (maxima and sums exchanged
+//          through shared memory): S from TMEM, scale, mask, max, exp, sum;
+//          P (bf16) into shared memory (where the q ring was) as the next MMA's
+//          K-major operand;
+//     pass B  O += P . V on tcgen05 with V the first eight blocks of the same row tile
+//          read as an MN-major operand, two N = 256 halves of 8 MMAs into all 512 TMEM
+//          columns (S has been consumed);
+//     partial O divided by the split's sum, in fp16, stored dims-major (a warp writes
+//          32 heads of one dim: coalesced), max and sum per head;
+//   combine: per (b, j) and 4-dim slice, one thread per two heads merges the splits.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "echo_common.cuh"
+
+ECHO_TRACE_UNIT(sparse_mla)
 
 namespace echo {
 
@@ -33,14 +43,14 @@ constexpr int kMlaHeads = 128;                   // MMA M
 constexpr int kMlaDqk = kKvElems;                // 576
 constexpr int kMlaDv = 512;
 constexpr int kMlaBlocks = kMlaDqk / 64;         // 9 swizzled 64-dim blocks
-constexpr int kMlaSplit = 128;                   // selected rows per CTA
-constexpr int kMlaChunk = 16;                    // rows per gathered chunk
-constexpr int kMlaChunks = kMlaSplit / kMlaChunk;
-constexpr int kMlaThreads = 128;
-constexpr uint32_t kMlaQBytes = kMlaBlocks * kMlaHeads * 128;    // 147456
-constexpr uint32_t kMlaBlockBytes = kMlaChunk * 128;            // one 64-dim block of a chunk: 2048
-constexpr uint32_t kMlaChunkBytes = kMlaBlocks * kMlaBlockBytes;  // 18432
-constexpr uint32_t kMlaPBytes = 2 * kMlaHeads * 128;             // 128 heads x 128 rows bf16
+constexpr int kMlaSplit = 128;                   // selected rows per CTA (MMA N of pass A)
+constexpr int kMlaThreads = 256;
+constexpr int kMlaStages = 5;                    // ring of q blocks
+constexpr uint32_t kMlaTile = 128 * 128;         // 128 rows (or heads) x one 64-dim block: 16 KB
+constexpr uint32_t kMlaRowsBytes = kMlaBlocks * kMlaTile;        // the 128 rows: 144 KB
+constexpr uint32_t kMlaVHalf = 4 * kMlaTile;                     // 256 value dims of the 128 rows
+constexpr uint32_t kMlaRingBytes = kMlaStages * kMlaTile;
+constexpr uint32_t kMlaPBytes = 2 * kMlaTile;                    // P: 128 heads x 128 rows bf16
 constexpr uint32_t kMlaTmemCols = 512;
 
 struct MlaParams {
@@ -48,7 +58,7 @@ struct MlaParams {
   const int32_t *out_slot;   // [B][n_q][k]
   int32_t n_g, n_q, k, nsplit;
   float scale;
-  float *part_o;             // [units][128][512]
+  __half *part_o;            // [units][512][128] (dims-major), divided by the split's sum
   float *part_ml;            // [units][2][128]: max, sum
   int32_t *status;
 };
@@ -97,32 +107,27 @@ __device__ __forceinline__ bool cta_wait(uint64_t *bar, uint32_t parity, volatil
   return ok;
 }
 
-// Gathers rows [r0, r0 + 16) of this CTA's selection (the slots in s_slot) into a
-// chunk buffer: block d (64 dims) of row r at d * 2048 + r * 128, its 16-byte chunks
-// swizzled by r % 8.  Rows past the selection or with no slot are zero.
-template <int NB>
-__device__ __forceinline__ void gather_chunk(uint8_t *buf, const int4 *kv, const int32_t *s_slot, int r0, int nrows) {
-  constexpr int kPer = NB * 8;  // 16-byte chunks per row
-  for (int t = threadIdx.x; t < kMlaChunk * kPer; t += kMlaThreads) {
-    const int r = t / kPer, ch = t % kPer;
-    const int row = r0 + r;
-    const int32_t slot = row < nrows ? s_slot[row] : -1;
-    int4 v = make_int4(0, 0, 0, 0);
-    if (slot >= 0) v = __ldg(kv + static_cast<size_t>(slot) * kKvChunks + ch);
-    const int blk = ch >> 3, c = ch & 7;
-    *reinterpret_cast<int4 *>(buf + blk * kMlaBlockBytes + r * 128 + ((c ^ (r & 7)) << 4)) = v;
-  }
+// 16-byte asynchronous copy global -> shared (zero-filled when src_bytes = 0)
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
 }
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __global__ void __launch_bounds__(kMlaThreads, 1)
     sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const MlaParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *q_smem = smem;                                   // 9 blocks x 128 heads x 128 B
-  uint8_t *kv_smem = q_smem + kMlaQBytes;                   // 2 chunk buffers
-  uint8_t *p_smem = kv_smem + 2 * kMlaChunkBytes;           // 2 blocks x 128 heads x 128 B
-  uint64_t *bars = reinterpret_cast<uint64_t *>(p_smem + kMlaPBytes);  // q_full, mma[2]
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 4);
+  uint8_t *rows_smem = smem;                                // 9 blocks x 128 rows x 128 B
+  uint8_t *ring = rows_smem + kMlaRowsBytes;                // 5 stages of q blocks
+  uint8_t *p_smem = ring;                                   // after pass A: 2 blocks x 128 heads x 128 B
+  // barriers: q landed per stage, MMAs of the stage's block done per stage, pass B, drain
+  // (a stage's barriers never run more than one phase ahead of their waiter)
+  constexpr int kBarMma = kMlaStages, kBarPv = 2 * kMlaStages, kBarDrain = 2 * kMlaStages + 1;
+  constexpr int kNumBars = 2 * kMlaStages + 2;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(ring + kMlaRingBytes);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
   int32_t *s_slot = reinterpret_cast<int32_t *>(tmem_slot + 4);       // [128]
   int *abort_flag = s_slot + kMlaSplit;
   int *wait_flag = abort_flag + 1;
@@ -132,12 +137,13 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
   const int bj = unit / P.nsplit, split = unit % P.nsplit;
   const int row0 = split * kMlaSplit;
   const int nrows = min(kMlaSplit, P.k - row0);
-  const int nch = (nrows + kMlaChunk - 1) / kMlaChunk;
-  const int h = threadIdx.x;  // head = TMEM lane
   const int warp = threadIdx.x >> 5;
+  const int h = (warp & 3) * 32 + (threadIdx.x & 31);  // head = TMEM lane (the warp's quadrant)
+  const int half = warp >> 2;                           // which half of the columns
+  ECHO_TRACE_FIRST(0);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < kNumBars; ++i) mbar_init(&bars[i], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -157,185 +163,261 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int4 *kv = reinterpret_cast<const int4 *>(P.gpu_kv);
-
-  if (threadIdx.x == 0) {
-    mbar_arrive_expect_tx(&bars[0], kMlaQBytes);
-    for (int blk = 0; blk < kMlaBlocks; ++blk)
-      tma_load_2d(q_smem + blk * kMlaHeads * 128, &tmap_q, &bars[0], blk * 64, bj * kMlaHeads);
+  const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+  // q's first blocks by TMA; the rows by cp.async, every piece in flight together
+  if (threadIdx.x == 0)
+    for (int d = 0; d < kMlaStages; ++d) {
+      mbar_arrive_expect_tx(&bars[d], kMlaTile);
+      tma_load_2d(ring + d * kMlaTile, &tmap_q, &bars[d], d * 64, bj * kMlaHeads);
+    }
+  {
+    const int4 *kv = reinterpret_cast<const int4 *>(P.gpu_kv);
+#pragma unroll 8
+    for (int t = threadIdx.x; t < kMlaSplit * kKvChunks; t += kMlaThreads) {
+      const int r = t / kKvChunks, ch = t % kKvChunks;  // a warp copies 512 consecutive bytes of a row
+      const int32_t slot = s_slot[r];
+      const int blk = ch >> 3, c = ch & 7;
+      cp_async16(rows_smem + blk * kMlaTile + r * 128 + ((c ^ (r & 7)) << 4),
+                 kv + static_cast<size_t>(slot >= 0 ? slot : 0) * kKvChunks + ch, slot >= 0 ? 16u : 0u);
+    }
+    cp_async_wait_all();
   }
+  fence_async_smem();
+  __syncthreads();
+  ECHO_TRACE_LAST(1);
   bool ok = true;
-  uint32_t mma_uses[2] = {0, 0};  // commits so far on each chunk buffer's barrier
+  bool issued = false;  // thread 0 issued tcgen05 work (drained on a failure)
 
-  // ===== pass A: S[:, rows] = q . rows^T =====
-  constexpr uint32_t kIdescA = idesc_bf16_f32(kMlaHeads, kMlaChunk, 0);
-  for (int c = 0; c < nch && ok; ++c) {
-    const int bi = c & 1;
-    uint8_t *buf = kv_smem + bi * kMlaChunkBytes;
-    // the buffer's previous MMAs are done before it is overwritten
-    if (mma_uses[bi] > 0 && !cta_wait(&bars[1 + bi], (mma_uses[bi] - 1) & 1, abort, P.status, wait_flag)) {
-      ok = false;
-      break;
-    }
-    gather_chunk<kMlaBlocks>(buf, kv, s_slot, c * kMlaChunk, nrows);
-    fence_async_smem();
-    if (c == 0 && !cta_wait(&bars[0], 0, abort, P.status, wait_flag)) {  // q landed (also the barrier)
-      ok = false;
-      break;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      tc_fence_after();
-      const uint32_t qa = smem_u32(q_smem), ba = smem_u32(buf);
-#pragma unroll 4
-      for (int kk = 0; kk < kMlaBlocks * 4; ++kk) {
-        const uint32_t blk = kk >> 2, kin = (kk & 3) * 32;
-        mma_bf16(tmem + c * kMlaChunk, kmajor_sw128_desc(qa + blk * kMlaHeads * 128 + kin),
-                 kmajor_sw128_desc(ba + blk * kMlaBlockBytes + kin), kIdescA, kk > 0);
+  // ===== pass A: S = q . rows^T, one 64-dim block of q per ring stage (thread 0) =====
+  constexpr uint32_t kIdescA = idesc_bf16_f32(kMlaHeads, kMlaSplit, 0);
+  if (threadIdx.x == 0) {
+    tc_fence_after();
+    const uint32_t ra = smem_u32(rows_smem);
+    int waited = 0;  // blocks whose MMAs were seen done, in order
+    for (int d = 0; d < kMlaBlocks; ++d) {
+      const int st = d % kMlaStages;
+      if (!mbar_wait(&bars[st], (d / kMlaStages) & 1, abort, P.status)) {  // q's block d landed
+        ok = false;
+        break;
       }
-      mma_commit(&bars[1 + bi]);
+      const uint32_t qa = smem_u32(ring + st * kMlaTile);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_bf16(tmem, kmajor_sw128_desc(qa + kk * 32), kmajor_sw128_desc(ra + d * kMlaTile + kk * 32), kIdescA,
+                 (d | kk) != 0);
+      mma_commit(&bars[kBarMma + st]);
+      issued = true;
+      // refill the stage of block d - 1 (its MMAs ran while these were queued) with
+      // block d - 1 + kMlaStages
+      const int nb = d - 1 + kMlaStages;
+      if (d >= 1 && nb < kMlaBlocks) {
+        const int pd = d - 1;
+        if (!mbar_wait(&bars[kBarMma + pd % kMlaStages], (pd / kMlaStages) & 1, abort, P.status)) {
+          ok = false;
+          break;
+        }
+        waited = d;
+        const int s2 = nb % kMlaStages;
+        mbar_arrive_expect_tx(&bars[s2], kMlaTile);
+        tma_load_2d(ring + s2 * kMlaTile, &tmap_q, &bars[s2], nb * 64, bj * kMlaHeads);
+      }
     }
-    ++mma_uses[bi];
+    for (; ok && waited < kMlaBlocks; ++waited)  // every pass-A MMA is done
+      if (!mbar_wait(&bars[kBarMma + waited % kMlaStages], (waited / kMlaStages) & 1, abort, P.status)) ok = false;
+    *wait_flag = ok ? 1 : 0;
   }
-  // every pass-A MMA has completed once both buffers' last commits have
-  for (int bi = 0; bi < 2 && ok; ++bi)
-    if (mma_uses[bi] > 0 && !cta_wait(&bars[1 + bi], (mma_uses[bi] - 1) & 1, abort, P.status, wait_flag))
-      ok = false;
+  __syncthreads();
+  ok = *reinterpret_cast<volatile int *>(wait_flag) != 0;
+  __syncthreads();
+  ECHO_TRACE_LAST(2);
 
-  // ===== softmax over this CTA's rows, one thread per head =====
-  float m = -INFINITY, l = 0.f;
+  // ===== softmax over this CTA's rows: two threads per head, 64 columns each =====
+  float *red = reinterpret_cast<float *>(ring + 2 * kMlaTile);  // [2][2][128] maxima, sums (free stages)
+  float l_sum = 0.f;
   if (ok) {
     tc_fence_after();
-    const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    float s[kMlaSplit];
+    const int cb = half * 64;
+    float s[64];
 #pragma unroll
-    for (int c4 = 0; c4 < kMlaSplit / 32; ++c4) {
+    for (int c2 = 0; c2 < 2; ++c2) {
       float v[32];
-      tmem_ld_32x32b_x32(trow + c4 * 32, v);
+      tmem_ld_32x32b_x32(trow + cb + c2 * 32, v);
       tmem_wait_ld();
       reg_fence_32(v);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) s[c4 * 32 + i] = v[i];
+      for (int i = 0; i < 32; ++i) s[c2 * 32 + i] = v[i];
     }
+    float mh = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < kMlaSplit; ++i) {
-      s[i] = s_slot[i] >= 0 ? s[i] * P.scale : -INFINITY;
-      m = fmaxf(m, s[i]);
+    for (int i = 0; i < 64; ++i) {
+      s[i] = s_slot[cb + i] >= 0 ? s[i] * P.scale : -INFINITY;
+      mh = fmaxf(mh, s[i]);
     }
-    // P = exp(s - m) in bf16 (K-major operand: head row h, rows in two 64-row blocks)
+    red[half * kMlaHeads + h] = mh;
+    __syncthreads();
+    const float m = fmaxf(red[h], red[kMlaHeads + h]);
+    // P = exp(s - m) in bf16 (K-major operand: head row h, this half's 64 rows = one block)
+    float lh = 0.f;
 #pragma unroll
-    for (int c8 = 0; c8 < kMlaSplit / 8; ++c8) {
+    for (int c8 = 0; c8 < 8; ++c8) {
       uint32_t w[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const float a = m == -INFINITY ? 0.f : __expf(s[c8 * 8 + 2 * u] - m);
         const float b = m == -INFINITY ? 0.f : __expf(s[c8 * 8 + 2 * u + 1] - m);
-        l += a + b;
+        lh += a + b;
         const __nv_bfloat162 pr = __floats2bfloat162_rn(a, b);
         w[u] = *reinterpret_cast<const uint32_t *>(&pr);
       }
-      const int blk = c8 >> 3, c = c8 & 7;
-      *reinterpret_cast<uint4 *>(p_smem + blk * kMlaHeads * 128 + h * 128 + ((c ^ (h & 7)) << 4)) =
+      *reinterpret_cast<uint4 *>(p_smem + half * kMlaTile + h * 128 + ((c8 ^ (h & 7)) << 4)) =
           make_uint4(w[0], w[1], w[2], w[3]);
     }
-    P.part_ml[static_cast<size_t>(unit) * 2 * kMlaHeads + h] = m;
-    P.part_ml[static_cast<size_t>(unit) * 2 * kMlaHeads + kMlaHeads + h] = l;
+    red[2 * kMlaHeads + half * kMlaHeads + h] = lh;
+    __syncthreads();
+    l_sum = red[2 * kMlaHeads + h] + red[3 * kMlaHeads + h];
+    if (half == 0) {
+      P.part_ml[static_cast<size_t>(unit) * 2 * kMlaHeads + h] = m;
+      P.part_ml[static_cast<size_t>(unit) * 2 * kMlaHeads + kMlaHeads + h] = l_sum;
+    }
   }
   tc_fence_before();
   fence_async_smem();
   __syncthreads();
+  ECHO_TRACE_LAST(3);
 
-  // ===== pass B: O += P[:, rows] . V[rows] (V read along the rows: MN-major) =====
+  // ===== pass B: O += P . V (V = the row tile's first 512 dims, read along the rows:
+  // MN-major), two halves of 256 dims =====
   constexpr uint32_t kIdescB = idesc_bf16_f32(kMlaHeads, 256, 1);
-  for (int c = 0; c < nch && ok; ++c) {
-    const int bi = c & 1;
-    uint8_t *buf = kv_smem + bi * kMlaChunkBytes;
-    if (mma_uses[bi] > 0 && !cta_wait(&bars[1 + bi], (mma_uses[bi] - 1) & 1, abort, P.status, wait_flag)) {
-      ok = false;
-      break;
-    }
-    gather_chunk<kMlaDv / 64>(buf, kv, s_slot, c * kMlaChunk, nrows);
-    fence_async_smem();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      tc_fence_after();
-      const uint32_t pa = smem_u32(p_smem) + (c >> 2) * kMlaHeads * 128 + (c & 3) * 32;
-      const uint32_t va = smem_u32(buf);
+  if (ok && threadIdx.x == 0) {
+    tc_fence_after();
+    const uint32_t pa = smem_u32(p_smem);
+    for (int half = 0; half < 2; ++half) {
+      const uint32_t va = smem_u32(rows_smem + half * kMlaVHalf);
 #pragma unroll
-      for (int nh = 0; nh < 2; ++nh)
-        mma_bf16(tmem + nh * 256, kmajor_sw128_desc(pa),
-                 mnmajor_sw128_desc(va + nh * 4 * kMlaBlockBytes, kMlaBlockBytes, 1024), kIdescB, c > 0);
-      mma_commit(&bars[1 + bi]);
+      for (int kk = 0; kk < kMlaSplit / 16; ++kk)
+        mma_bf16(tmem + half * 256, kmajor_sw128_desc(pa + (kk >> 2) * kMlaTile + (kk & 3) * 32),
+                 mnmajor_sw128_desc(va + kk * 16 * 128, kMlaTile, 1024), kIdescB, kk > 0);
     }
-    ++mma_uses[bi];
+    mma_commit(&bars[kBarPv]);
+    issued = true;
   }
-  for (int bi = 0; bi < 2 && ok; ++bi)
-    if (mma_uses[bi] > 0 && !cta_wait(&bars[1 + bi], (mma_uses[bi] - 1) & 1, abort, P.status, wait_flag))
-      ok = false;
+  if (ok && !cta_wait(&bars[kBarPv], 0, abort, P.status, wait_flag)) ok = false;
+  ECHO_TRACE_LAST(4);
 
-  // ===== partial O of this CTA's rows =====
+  // ===== partial O of this CTA's rows, dims-major: a warp stores 32 heads of one dim
+  // (coalesced); the two warps of a lane quadrant take 256 dims each =====
   if (ok) {
     tc_fence_after();
-    const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    float4 *dst = reinterpret_cast<float4 *>(P.part_o + (static_cast<size_t>(unit) * kMlaHeads + h) * kMlaDv);
-    for (int c32 = 0; c32 < kMlaDv / 32; ++c32) {
+    __half *dst = P.part_o + static_cast<size_t>(unit) * kMlaDv * kMlaHeads + h;
+    const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+#pragma unroll 1
+    for (int c32 = 0; c32 < kMlaDv / 2 / 32; ++c32) {
+      const int d0 = half * (kMlaDv / 2) + c32 * 32;
       float v[32];
-      tmem_ld_32x32b_x32(trow + c32 * 32, v);
+      tmem_ld_32x32b_x32(trow + d0, v);
       tmem_wait_ld();
       reg_fence_32(v);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) dst[c32 * 8 + i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      for (int i = 0; i < 32; ++i) dst[static_cast<size_t>(d0 + i) * kMlaHeads] = __float2half_rn(v[i] * inv);
     }
   }
   if (!ok && threadIdx.x == 0) {
-    // a wait gave up: let the copies and MMAs this CTA started finish before it exits
-    const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(&bars[0], 0) && globaltimer() - t0 < kWaitLimitNs) {
-    }
-    for (int bi = 0; bi < 2; ++bi)
-      if (mma_uses[bi] > 0) {
-        const uint64_t t1 = globaltimer();
-        while (!mbar_try_wait(&bars[1 + bi], (mma_uses[bi] - 1) & 1) && globaltimer() - t1 < kWaitLimitNs) {
-        }
+    // a wait gave up: let the q copy and every MMA this CTA started finish before it
+    // frees TMEM and exits (one commit after them all, waited on with a limit)
+    for (int st = 0; st < kMlaStages; ++st) {  // q copies that may still be in flight
+      const uint64_t t2 = globaltimer();
+      while (!mbar_try_wait(&bars[st], 0) && globaltimer() - t2 < kWaitLimitNs) {
       }
+    }
+    if (issued) {
+      mma_commit(&bars[kBarDrain]);
+      const uint64_t t1 = globaltimer();
+      while (!mbar_try_wait(&bars[kBarDrain], 0) && globaltimer() - t1 < kWaitLimitNs) {
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
+  ECHO_TRACE_LAST(5);
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, kMlaTmemCols);
   }
 }
 
-// o = sum_s w_s O_s / sum_s w_s l_s, w_s = exp(m_s - max_s m_s); lse = max + log(sum)
-__global__ void sparse_mla_combine_kernel(const float *part_o, const float *part_ml, int nsplit, int n_rows,
-                                          float *out, float *lse) {
-  const int r = blockIdx.x;  // (b, j, head)
-  if (r >= n_rows) return;
-  const int bj = r / kMlaHeads, h = r % kMlaHeads;
-  __shared__ float wts[64];
-  __shared__ float s_inv;
-  if (threadIdx.x == 0) {
-    float M = -INFINITY;
-    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, part_ml[(static_cast<size_t>(bj) * nsplit + s) * 2 * kMlaHeads + h]);
-    float L = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
-      const size_t base = (static_cast<size_t>(bj) * nsplit + s) * 2 * kMlaHeads;
-      const float ms = part_ml[base + h];
-      const float w = M == -INFINITY ? 0.f : __expf(ms - M);
-      wts[s] = w;
-      L += w * part_ml[base + kMlaHeads + h];
+// o = sum_s w_s l_s o_s / sum_s w_s l_s (o_s the split's normalised partial),
+// w_s = exp(m_s - max_s m_s); lse = max + log(sum).  Block (bj, slice of 4 dims), 64
+// threads of two heads each: a warp reads 64 consecutive heads of one dim (128 bytes of
+// fp16 pairs) per load; eight splits' loads are in flight together.
+constexpr int kCombDims = 4;
+constexpr int kCombThreads = kMlaHeads / 2;
+
+__global__ void __launch_bounds__(kCombThreads) sparse_mla_combine_kernel(const __half *part_o, const float *part_ml,
+                                                                           int nsplit, float *out, float *lse) {
+  const int bj = blockIdx.x, d0 = blockIdx.y * kCombDims, h0 = 2 * threadIdx.x;
+  ECHO_TRACE_FIRST(6);
+  const float2 *ml = reinterpret_cast<const float2 *>(part_ml);  // [unit][2][64 pairs]
+  // the maxima: sixteen splits' loads in flight together
+  float2 M = make_float2(-INFINITY, -INFINITY);
+  for (int s0 = 0; s0 < nsplit; s0 += 16) {
+    float2 m[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+      m[q] = s0 + q < nsplit ? ml[(static_cast<size_t>(bj) * nsplit + s0 + q) * kMlaHeads + threadIdx.x]
+                             : make_float2(-INFINITY, -INFINITY);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      M.x = fmaxf(M.x, m[q].x);
+      M.y = fmaxf(M.y, m[q].y);
     }
-    s_inv = L > 0.f ? 1.f / L : 0.f;
-    lse[r] = M == -INFINITY ? -INFINITY : M + logf(L);
   }
-  __syncthreads();
-  for (int d = threadIdx.x; d < kMlaDv; d += blockDim.x) {
-    float acc = 0.f;
-    for (int s = 0; s < nsplit; ++s)
-      acc += wts[s] * part_o[((static_cast<size_t>(bj) * nsplit + s) * kMlaHeads + h) * kMlaDv + d];
-    out[static_cast<size_t>(r) * kMlaDv + d] = acc * s_inv;
+  float2 acc[kCombDims];
+#pragma unroll
+  for (int i = 0; i < kCombDims; ++i) acc[i] = make_float2(0.f, 0.f);
+  float2 L = make_float2(0.f, 0.f);
+  for (int s0 = 0; s0 < nsplit; s0 += 8) {
+    float2 w[8];
+    __half2 v[8][kCombDims];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int s = s0 + q;
+      w[q] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < kCombDims; ++i) v[q][i] = __floats2half2_rn(0.f, 0.f);
+      if (s < nsplit) {
+        const size_t u = static_cast<size_t>(bj) * nsplit + s;
+        const float2 m = ml[u * kMlaHeads + threadIdx.x];
+        const float2 l = ml[u * kMlaHeads + kMlaHeads / 2 + threadIdx.x];
+        w[q].x = M.x == -INFINITY ? 0.f : __expf(m.x - M.x) * l.x;
+        w[q].y = M.y == -INFINITY ? 0.f : __expf(m.y - M.y) * l.y;
+        const __half2 *src = reinterpret_cast<const __half2 *>(part_o + (u * kMlaDv + d0) * kMlaHeads + h0);
+#pragma unroll
+        for (int i = 0; i < kCombDims; ++i) v[q][i] = __ldcs(src + static_cast<size_t>(i) * (kMlaHeads / 2));
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      L.x += w[q].x;
+      L.y += w[q].y;
+#pragma unroll
+      for (int i = 0; i < kCombDims; ++i) {
+        const float2 f = __half22float2(v[q][i]);
+        acc[i].x = fmaf(w[q].x, f.x, acc[i].x);
+        acc[i].y = fmaf(w[q].y, f.y, acc[i].y);
+      }
+    }
   }
+  const float ix = L.x > 0.f ? 1.f / L.x : 0.f, iy = L.y > 0.f ? 1.f / L.y : 0.f;
+  float4 ox, oy;
+  ox = make_float4(acc[0].x * ix, acc[1].x * ix, acc[2].x * ix, acc[3].x * ix);
+  oy = make_float4(acc[0].y * iy, acc[1].y * iy, acc[2].y * iy, acc[3].y * iy);
+  *reinterpret_cast<float4 *>(out + (static_cast<size_t>(bj) * kMlaHeads + h0) * kMlaDv + d0) = ox;
+  *reinterpret_cast<float4 *>(out + (static_cast<size_t>(bj) * kMlaHeads + h0 + 1) * kMlaDv + d0) = oy;
+  if (blockIdx.y == 0) {
+    lse[static_cast<size_t>(bj) * kMlaHeads + h0] = M.x == -INFINITY ? -INFINITY : M.x + logf(L.x);
+    lse[static_cast<size_t>(bj) * kMlaHeads + h0 + 1] = M.y == -INFINITY ? -INFINITY : M.y + logf(L.y);
+  }
+  ECHO_TRACE_LAST(7);
 }
 
 }  // namespace echo
@@ -366,7 +448,7 @@ static PFN_encodeTiledM encode_fn_m() {
 size_t mla_workspace_bytes(int32_t B, int32_t n_q, int32_t k) {
   const size_t nsplit = (static_cast<size_t>(k) + echo::kMlaSplit - 1) / echo::kMlaSplit;
   const size_t units = static_cast<size_t>(B) * n_q * nsplit;
-  return units * echo::kMlaHeads * (echo::kMlaDv + 2) * sizeof(float);
+  return units * echo::kMlaHeads * (echo::kMlaDv * sizeof(__half) + 2 * sizeof(float));
 }
 
 int mla_max_splits() { return 64; }
@@ -399,19 +481,23 @@ int launch_sparse_mla(const echo_mla_args *a, cudaStream_t stream) {
   P.nsplit = (a->k + echo::kMlaSplit - 1) / echo::kMlaSplit;
   P.scale = a->scale;
   const size_t units = static_cast<size_t>(a->B) * a->n_q * P.nsplit;
-  P.part_o = reinterpret_cast<float *>(a->workspace);
-  P.part_ml = P.part_o + units * echo::kMlaHeads * echo::kMlaDv;
+  P.part_o = reinterpret_cast<__half *>(a->workspace);
+  P.part_ml = reinterpret_cast<float *>(P.part_o + units * echo::kMlaHeads * echo::kMlaDv);
   P.status = a->dev_status;
-  const size_t smem = 1024 + echo::kMlaQBytes + 2 * echo::kMlaChunkBytes + echo::kMlaPBytes + 64 +
-                      echo::kMlaSplit * sizeof(int32_t) + 32;
+  static_assert(echo::kMlaPBytes <= echo::kMlaRingBytes, "P lives in the q ring");
+  const size_t smem = 1024 + echo::kMlaRowsBytes + echo::kMlaRingBytes + (2 * echo::kMlaStages + 2) * 8 + 16 +
+                      echo::kMlaSplit * sizeof(int32_t) + 16;
   static bool attr[64] = {false};
   if (int rr = smem_limit_once(attr, echo::sparse_mla_kernel, static_cast<int>(smem), "sparse MLA smem attribute"))
     return rr;
   echo::sparse_mla_kernel<<<static_cast<unsigned>(units), echo::kMlaThreads, smem, stream>>>(tq, P);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "sparse MLA launch");
-  const int rows = a->B * a->n_q * echo::kMlaHeads;
-  echo::sparse_mla_combine_kernel<<<rows, 128, 0, stream>>>(P.part_o, P.part_ml, P.nsplit, rows, a->out, a->lse);
+  // an ordinary launch: as a programmatic dependent launch the merge started sooner
+  // but ran slower (its blocks were placed while the main kernel held the SMs)
+  const dim3 cgrid(static_cast<unsigned>(a->B * a->n_q), echo::kMlaDv / echo::kCombDims);
+  echo::sparse_mla_combine_kernel<<<cgrid, echo::kCombThreads, 0, stream>>>(P.part_o, P.part_ml, P.nsplit, a->out,
+                                                                            a->lse);
   e = cudaGetLastError();
   return e == cudaSuccess ? ECHO_OK : cuda_fail(e, "sparse MLA combine launch");
 }
