@@ -90,52 +90,85 @@ def dist_env():
 # clocks sampled during the timed region
 # ---------------------------------------------------------------------------
 class ClockSampler:
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-         "clocks_event_reasons.sw_power_cap")
+    """nvidia-smi sampling of SM clocks and throttle reasons every 50 ms.  It is started
+    before the timed region and waited on until its first sample is in (its start-up
+    must not overlap the timed steps); `window(t0, t1)` selects the samples taken while
+    the timed steps ran (wall-clock times of nvidia-smi's own timestamps)."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, period_ms: int = 50):
         self.idx = gpu_index
+        self.period = period_ms
         self.p = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def _reader(self):
+        for line in self.p.stdout:
+            self.lines.append(line)
 
     def __enter__(self):
+        import threading
         try:
             self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
-                                       "--format=csv,noheader,nounits", "-lms", "200"],
-                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                                       "--format=csv,noheader,nounits", "-lms", str(self.period)],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
         except OSError:
             self.p = None
+            return self
+        threading.Thread(target=self._reader, daemon=True).start()
+        t = time.time()
+        while not self.lines and time.time() - t < 15.0 and self.p.poll() is None:
+            time.sleep(0.02)
+        time.sleep(0.3)
         return self
 
+    def window(self, t0: float, t1: float):
+        self.t0, self.t1 = t0, t1
+
     def __exit__(self, *exc):
-        self.out = ""
         if self.p is not None:
-            time.sleep(0.25)
+            time.sleep(2.5 * self.period / 1000.0)
             self.p.terminate()
             try:
-                self.out, _ = self.p.communicate(timeout=5)
+                self.p.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.p.kill()
-                self.out = ""
         return False
 
+    @staticmethod
+    def _when(stamp: str):
+        try:
+            main, _, frac = stamp.strip().partition(".")
+            return time.mktime(time.strptime(main, "%Y/%m/%d %H:%M:%S")) + (float("0." + frac) if frac else 0.0)
+        except ValueError:
+            return None
+
     def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in (self.out or "").strip().splitlines():
+        rows = []
+        for line in list(self.lines):
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
+                rows.append((self._when(f[0]), float(f[2]), float(f[3]), f[6:10]))
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
+        inside = [r for r in rows if r[0] is not None and self.t0 is not None
+                  and self.t0 - 0.06 <= r[0] <= self.t1 + 0.06]
+        use = inside or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in use:
+            for n, v in zip(names, r[3]):
                 if v.lower() == "active":
                     reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return {"sm_mhz": statistics.median([r[1] for r in use]) if use else None,
+                "sm_max_mhz": use[-1][2] if use else None, "reasons": sorted(reasons),
+                "samples": len(use), "samples_in_timed_region": len(inside),
+                "timed_region_s": (self.t1 - self.t0) if self.t0 is not None else None}
 
 
 def aggregate_replicas(local_total_ms: float, steps: int, pg=None, device="cpu"):
@@ -192,13 +225,15 @@ def run_reference(args):
         return 0
     import oracle
     oracle.build()
-    steps = args.warmup + args.steps
+    # a bounded sample: at most 3 warm-up and 20 timed steps of the K (about 0.3 s of
+    # single-core work each), one of the B requests per step, scaled to the batch
+    n_w, n_t = min(args.warmup, 3), min(args.steps, 20)
     host = np.zeros((N_H, 576), np.uint16)
-    inp, qs, host, r2h, st, rho = build_inputs(steps, seed=1, host_out=host, overlap=args.overlap)
+    inp, qs, host, r2h, st, rho = build_inputs(n_w + n_t, seed=1, host_out=host, overlap=args.overlap)
     times = []
-    for t in range(steps):
+    for t in range(n_w + n_t):
         dt = cpu_baseline_sample(inp, qs[t], host, r2h, st, requests=1)
-        if t >= args.warmup:
+        if t >= n_w:
             times.append(dt)
     per_step = float(np.mean(times)) * B     # one request sampled per step: scale to the batch
     v = 1.0 / per_step
@@ -207,7 +242,8 @@ def run_reference(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": workload_name(args.overlap), "rho": rho},
             "cpu_baseline": {"value": v, "unit": "steps/s", "cores": 1, "kind": "oracle",
-                             "sample": f"1 of the {B} requests per step (L={L}), scaled x{B}"},
+                             "sample": f"1 of the {B} requests per step (L={L}), scaled x{B}, on the first "
+                                       f"{n_t} of the {args.steps} steps after {n_w} warm-up"},
             "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -334,7 +370,9 @@ def run_ours(args):
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         nvtx_push("echo_timed_steps")  # lets a profiler pick out the timed steps' launches
+        t_start = time.time()
         step_ms = timed_loop(timed)
+        clk.window(t_start, time.time())
         nvtx_pop()
     if pg:
         pg.barrier()
@@ -663,9 +701,11 @@ def prefill_probe(echo, torch, flush_l2, B=1, L_=32768, C=512, k=K_TOP, reps=3, 
         return float(np.median(ts))
 
     with ClockSampler(torch.cuda.current_device()) as clk:
+        t0 = time.time()
         ms_plain = timed(lambda: echo.echo_prefill_indexer_score(q, w, k_index, ctx, scores))
         ms_approx = timed(lambda: echo.echo_prefill_indexer_score(q, w, k_index, ctx, scores, s_shift=shift, k=k,
                                                                   thr_bin=thr, subset_n=sub))
+        clk.window(t0, time.time())
     pairs = int(sum(max(0, int(inp.ctx_len[b]) - (C - 1 - i)) for b in range(B) for i in range(C)))
     flop = 2.0 * 64 * 128 * pairs
     return {"B": B, "L": L_, "C": C, "k": k, "query_key_pairs": pairs, "flop": flop,
@@ -786,7 +826,7 @@ def run_kernel_case(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-requests", type=int, default=1)
