@@ -439,6 +439,7 @@ def run_ours(args):
         best = min(best, a0.elapsed_time(a1))
     h2d_gbs = (256 << 20) / (best * 1e-3) / 1e9
     recall_probe = recall_bandwidth_probe(echo, torch, host_t, flush_l2)
+    block_probe = block_recall_probe(echo, torch, flush_l2, h2d_gbs)
     volume_probe = indexer_volume_probe(echo, torch, inp, flush_l2, hbm_peak)
     # the prefill chunk indexer (inter-query prefetch row): 1216 queries = 304 blocks of 4,
     # two full waves on 152 SMs; FP8 tensor peak = the measured bf16 peak x 2
@@ -487,6 +488,7 @@ def run_ours(args):
         "evicted_per_step": st_vals["evicted"] / args.steps,
         "prefill_chunk": pre,
         "sparse_mla_decode": mla,
+        "block_gqa_recall": block_probe,
         "direct_to_slot": direct,
         "prefetch_off": off,
         "stage_ms": {k: float(np.mean(v)) for k, v in stage_ms.items()},
@@ -638,6 +640,76 @@ def recall_bandwidth_probe(echo, torch, host_t, flush_l2, rows=65536, n_g=65536)
         best = min(best, a0.elapsed_time(a1))
     ok = bool((out >= 0).all().item())
     return {"rows": rows, "bytes": rows * 1152, "ms": best, "gbs": rows * 1152 / (best * 1e-3) / 1e9, "all_recalled": ok}
+
+
+def block_recall_probe(echo, torch, flush_l2, h2d_gbs, B_req=4, n_blocks=1024, n_g=8192, reps=4):
+    """The block-level / GQA variant of the cache manager: a pool row is one block of 64
+    tokens of one KV head (K and V, 128 dims: 32 KB), a selection row one (request, KV
+    head) pair: 4 requests x 8 KV heads, 1024 blocks each (64K tokens).
+    cold: 64 blocks per selection row (2048 rows, 64 MiB) recalled into an empty pool,
+      all misses: host-link bytes over the call's time, best of `reps`.
+    steady: the pool full of older blocks at the start (every miss evicts); NSA-style 16
+      blocks per row, block scores of consecutive steps correlated (rho 0.9); GPU top-k
+      plus recall per step, median over the steps after the first 4."""
+    from sparse_attention_kv_fp8_gb300 import workload as wl
+    R = wl.block_row_elems()
+    rows = B_req * wl.GQA_KV_HEADS
+    n_h = rows * n_blocks
+    host = torch.empty((n_h, R), dtype=torch.int16, pin_memory=True)
+    host[:, :8] = torch.arange(n_h, dtype=torch.int32).view(-1, 1).to(torch.int16)   # rows told apart
+    host[:, 8:] = 1
+    pool = echo.Pool(n_g, host)
+    echo.echo_pool_init(pool)
+    ws = echo.Workspace(n_g, rows * 64)
+    r2h = torch.from_numpy(wl.req_to_host(rows, n_blocks)).cuda()
+    ctx = torch.full((rows,), n_blocks, dtype=torch.int32, device="cuda")
+    g = np.random.default_rng(6)
+    sel = torch.from_numpy(np.sort(np.stack([g.choice(n_blocks, 64, replace=False) for _ in range(rows)]), axis=1)
+                           .astype(np.int32)[:, None, :]).cuda()
+    out = torch.empty_like(sel)
+    best = 1e9
+    for it in range(reps):
+        echo.echo_pool_init(pool)
+        flush_l2()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record()
+        echo.echo_prefetch_recall(pool, ws, sel, r2h, ctx, 10 + it, out)
+        a1.record()
+        torch.cuda.synchronize()
+        best = min(best, a0.elapsed_time(a1))
+    cold_ok = bool((out >= 0).all().item())
+    cold_bytes = rows * 64 * R * 2
+    # steady decode steps at block granularity, from a full pool
+    res = wl.random_resident_rows(n_h, n_g, 6)
+    pool.load_state(wl.resident_pool(n_g, n_h, res, wl.random_clocks(n_g, 100, 6), 6))
+    k = wl.GQA_TOPK_BLOCKS
+    scores = [torch.from_numpy(sc).cuda() for sc in wl.block_scores(rows, n_blocks, 7, 12, 0.9)]
+    sel_k = torch.empty((rows, 1, k), dtype=torch.int32, device="cuda")
+    kth = torch.empty((rows, 1), dtype=torch.float32, device="cuda")
+    out_k = torch.empty_like(sel_k)
+    stats = echo.Stats()
+    ts, before = [], None
+    for t, sc in enumerate(scores):
+        if t == 4:
+            torch.cuda.synchronize()
+            before = stats.as_dict()
+        flush_l2()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record()
+        echo.echo_select_topk(sc, ctx, k, sel_k, kth)
+        echo.echo_prefetch_recall(pool, ws, sel_k, r2h, ctx, 100 + t, out_k, stats=stats)
+        a1.record()
+        torch.cuda.synchronize()
+        if t >= 4:
+            ts.append(a0.elapsed_time(a1))
+    after = stats.as_dict()
+    uniq = max(1, after["unique_rows"] - before["unique_rows"])
+    return {"row_bytes": R * 2, "selection_rows": rows, "blocks_per_row": n_blocks,
+            "cold": {"rows": rows * 64, "bytes": cold_bytes, "ms": best, "gbs": cold_bytes / (best * 1e-3) / 1e9,
+                     "frac_h2d": cold_bytes / (best * 1e-3) / 1e9 / h2d_gbs, "all_recalled": cold_ok},
+            "steady": {"k_blocks": k, "us_per_step": float(np.median(ts)) * 1e3,
+                       "hit_rate": (after["hits"] - before["hits"]) / uniq,
+                       "recalled_rows_per_step": (after["recalled"] - before["recalled"]) / len(ts)}}
 
 
 def indexer_volume_probe(echo, torch, inp, flush_l2, hbm_peak, batches=(8, 24, 64), reps=5):

@@ -66,10 +66,23 @@ extern "C" {
  *                                    allocate (or evict) call, -1 beyond
  *   gpu_token_to_host   [n_g] int32  GPUTokenToHost: INF when empty
  *   host_token_to_gpu   [n_h] int32  HostTokenToGPU: INF when not resident
- *   gpu_kv              [n_g][576] bf16  device latent-KV pool
- *   host_kv             [n_h][576] bf16  pinned, mapped host pool (device pointer)
+ *   gpu_kv              [n_g][R] bf16  device KV pool, one row per slot
+ *   host_kv             [n_h][R] bf16  pinned, mapped host pool (device pointer)
  *   counters            [4] int32 device: [0] free slots, [1] entries in use in
  *                       gpu_indices_buffer, [2..3] reserved
+ *   row_elems           R, the bf16 elements of one row (the unit the metadata
+ *                       tracks): 0 means 576, MLA's latent row of one token (512 +
+ *                       64 rope).  Any multiple of 8 up to 65536 serves the
+ *                       block-level / GQA variant (section 8: the cache manager
+ *                       carries over to block-level sparsity by coarser metadata and
+ *                       a KV-head dimension): a row is then one block of tokens of
+ *                       one KV head (tokens x head dim x {K, V}), and a selection
+ *                       per (request, KV head) folds the KV heads into the request
+ *                       dimension of the calls below.  The cache-manager calls
+ *                       (init, allocate, evict, recall without a stage, append)
+ *                       take any R; the calls that prefetch (indexer or prefill
+ *                       with a pool, recall with a stage, the decode step) need
+ *                       R = 576.
  * Slots and host rows are plain indices; the pool is consistent when
  * host_token_to_gpu[gpu_token_to_host[s]] == s for every occupied slot s.
  */
@@ -84,6 +97,7 @@ typedef struct echo_pool {
     uint16_t *gpu_kv;
     uint16_t *host_kv;
     int32_t *counters;
+    int32_t row_elems;
 } echo_pool;
 
 /*
@@ -338,7 +352,7 @@ int echo_prefetch_recall_noalloc(const echo_pool *pool, const int32_t *sel, cons
  * p = ctx_len[b]; new_kv[b] is written to host row req_to_host[b][p] and to a newly
  * allocated GPU slot (priority = clock, evicting first if the pool is short),
  * new_k_index[b] to k_index[b][p]; then ctx_len[b] = p + 1.
- *   new_kv [B][576] bf16 device; new_k_index [B][128] e4m3 device.
+ *   new_kv [B][R] bf16 device (R = the pool's row_elems); new_k_index [B][128] e4m3 device.
  */
 int echo_append(const echo_pool *pool, const echo_workspace *ws, uint8_t *k_index, int32_t *ctx_len,
                 const int32_t *req_to_host, int32_t B, int32_t L_max, const uint16_t *new_kv,
@@ -461,7 +475,7 @@ const char *echo_last_error_string(void);
 
 /* Library version, (major << 16) | minor (1.1: echo_stage's direct-to-slot fields;
    1.2: echo_prefill_indexer_score, echo_ema_update_strided, n_q up to 65536 in
-   top-k and recall; 1.3: echo_sparse_mla_decode). */
+   top-k and recall; 1.3: echo_sparse_mla_decode; 1.4: echo_pool.row_elems). */
 int32_t echo_version(void);
 
 /* Storage law of the metadata arrays of one pool (section 5.1): 4*n_h + 13*n_g. */

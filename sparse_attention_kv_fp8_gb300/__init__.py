@@ -40,7 +40,7 @@ class EchoError(RuntimeError):
 class c_pool(ctypes.Structure):
     _fields_ = [("n_g", _I32), ("n_h", _I32), ("gpu_token_free", _P), ("gpu_token_priority", _P),
                 ("gpu_indices_buffer", _P), ("gpu_token_to_host", _P), ("host_token_to_gpu", _P),
-                ("gpu_kv", _P), ("host_kv", _P), ("counters", _P)]
+                ("gpu_kv", _P), ("host_kv", _P), ("counters", _P), ("row_elems", _I32)]
 
 
 class c_workspace(ctypes.Structure):
@@ -158,26 +158,31 @@ def _stream(stream):
 # ---------------------------------------------------------------------------
 
 class Pool:
-    """One layer's GPU pool plus a view of the (per-model) pinned host pool."""
+    """One layer's GPU pool plus a view of the (per-model) pinned host pool.  A row is
+    host_kv's last dimension: 576 (MLA's latent row of one token) or, for the
+    block-level / GQA variant, any multiple of 8 up to 65536 bf16 (a block of tokens
+    of one KV head)."""
 
     def __init__(self, n_g: int, host_kv: torch.Tensor, device="cuda"):
         if host_kv.device.type != "cpu" or not host_kv.is_pinned():
             raise EchoError("host_kv must be a pinned CPU tensor")
-        if host_kv.dtype not in (torch.int16, torch.uint16, torch.bfloat16) or host_kv.shape[-1] != KV_ELEMS:
-            raise EchoError("host_kv must be [n_h][576] 16-bit")
+        R = int(host_kv.shape[-1]) if host_kv.dim() == 2 else -1
+        if host_kv.dtype not in (torch.int16, torch.uint16, torch.bfloat16) or R <= 0 or R % 8 or R > 65536:
+            raise EchoError("host_kv must be [n_h][R] 16-bit with R a multiple of 8 up to 65536")
         self.n_g = int(n_g)
         self.n_h = int(host_kv.shape[0])
+        self.row_elems = R
         self.host_kv = host_kv
         self.free = torch.empty(n_g, dtype=torch.uint8, device=device)
         self.prio = torch.empty(n_g, dtype=torch.int32, device=device)
         self.idxbuf = torch.empty(n_g, dtype=torch.int32, device=device)
         self.to_host = torch.empty(n_g, dtype=torch.int32, device=device)
         self.host_to_gpu = torch.empty(self.n_h, dtype=torch.int32, device=device)
-        self.gpu_kv = torch.zeros((n_g, KV_ELEMS), dtype=torch.int16, device=device)
+        self.gpu_kv = torch.zeros((n_g, R), dtype=torch.int16, device=device)
         self.counters = torch.zeros(4, dtype=torch.int32, device=device)
         self.c = c_pool(self.n_g, self.n_h, _ptr(self.free), _ptr(self.prio), _ptr(self.idxbuf),
                         _ptr(self.to_host), _ptr(self.host_to_gpu), _ptr(self.gpu_kv), _ptr(host_kv),
-                        _ptr(self.counters))
+                        _ptr(self.counters), R)
 
     def load_state(self, st, gpu_kv=None):
         """Install a workload.PoolState (metadata arrays + counters); gpu_kv defaults
@@ -191,7 +196,7 @@ class Pool:
         self.counters.copy_(torch.tensor([st.n_free, st.idx_count, 0, 0], dtype=torch.int32))
         if gpu_kv is None:
             occ = np.nonzero(st.gpu_token_free == 0)[0]
-            kv = torch.zeros((self.n_g, KV_ELEMS), dtype=torch.int16)
+            kv = torch.zeros((self.n_g, self.row_elems), dtype=torch.int16)
             if occ.size:
                 hk = self.host_kv.view(torch.int16)
                 kv[torch.from_numpy(occ)] = hk[torch.from_numpy(st.gpu_token_to_host[occ].astype(np.int64))]

@@ -108,12 +108,21 @@ static int check_device_accessible(const void *p, const char *name) {
 static int check_pool(const echo_pool *p) {
   REQUIRE(p, "pool is NULL");
   REQUIRE(p->n_g > 0 && p->n_h > 0, "pool sizes must be positive (n_g=%d, n_h=%d)", p->n_g, p->n_h);
+  REQUIRE(p->row_elems >= 0 && p->row_elems <= 65536 && p->row_elems % 8 == 0,
+          "row_elems must be 0 (576) or a multiple of 8 up to 65536 (got %d)", p->row_elems);
   REQUIRE(p->gpu_token_free && p->gpu_token_priority && p->gpu_indices_buffer && p->gpu_token_to_host &&
               p->host_token_to_gpu && p->counters,
           "pool metadata pointer is NULL");
   REQUIRE(p->gpu_kv && p->host_kv, "pool KV pointer is NULL");
   REQUIRE(aligned(p->gpu_kv, 16) && aligned(p->host_kv, 16), "pool KV pools must be 16-byte aligned");
   return check_device_accessible(p->host_kv, "pool.host_kv");
+}
+
+// The calls that prefetch copy MLA latent rows (576 bf16) by a fixed layout.
+static int check_latent_rows(const echo_pool *p, const char *what) {
+  REQUIRE(p->row_elems == 0 || p->row_elems == ECHO_KV_ELEMS, "%s needs a pool of %d-element rows (row_elems %d)",
+          what, ECHO_KV_ELEMS, p->row_elems);
+  return ECHO_OK;
 }
 
 static int check_ws(const echo_workspace *w, const echo_pool *p, long long rows) {
@@ -148,7 +157,7 @@ int echo_selftest_wait_timeout(int32_t which, int32_t *dev_status, void *stream)
   return launch_wait_probe(which, dev_status, static_cast<cudaStream_t>(stream));
 }
 
-int32_t echo_version(void) { return (1 << 16) | 3; }
+int32_t echo_version(void) { return (1 << 16) | 4; }
 
 int64_t echo_metadata_bytes(int64_t n_h, int64_t n_g) {
   return static_cast<int64_t>(sizeof(int32_t)) * n_h +
@@ -167,6 +176,7 @@ int echo_indexer_score(const echo_indexer_args *a, void *stream) {
   if (a->s_hat) {
     REQUIRE(a->req_to_host && a->pool && a->stage, "prefetch needs req_to_host, pool and stage");
     TRY(check_pool(a->pool));
+    TRY(check_latent_rows(a->pool, "the indexer's prefetch"));
     TRY(check_stage(a->stage, a->pool));
     REQUIRE(a->stage->reserve || static_cast<long long>(a->B) * a->stage->stride <= (1ll << 31) - 1,
             "stage too large");
@@ -246,7 +256,10 @@ int echo_prefetch_recall(const echo_pool *pool, const echo_workspace *ws, const 
   const long long F = static_cast<long long>(B) * n_q * k;
   REQUIRE(F <= (1ll << 30), "B * n_q * k too large");
   TRY(check_ws(ws, pool, F));
-  if (stage) TRY(check_stage(stage, pool));
+  if (stage) {
+    TRY(check_latent_rows(pool, "a recall with a stage"));
+    TRY(check_stage(stage, pool));
+  }
   return launch_recall(pool, ws, sel, req_to_host, ctx_len, B, n_q, k, L_max, stage, clock, clock_dev, out_slot, stats,
                        dev_status, static_cast<cudaStream_t>(stream), nullptr, nullptr, 0, 0.f, nullptr, 0);
 }
@@ -263,7 +276,10 @@ int echo_prefetch_recall_noalloc(const echo_pool *pool, const int32_t *sel, cons
   REQUIRE(clock >= 0 || clock_dev, "clock must be >= 0");
   const long long F = static_cast<long long>(B) * n_q * k;
   REQUIRE(F <= (1ll << 30), "B * n_q * k too large");
-  if (stage) TRY(check_stage(stage, pool));
+  if (stage) {
+    TRY(check_latent_rows(pool, "a recall with a stage"));
+    TRY(check_stage(stage, pool));
+  }
   echo_workspace ws;
   TRY(noalloc_workspace(pool->n_g, static_cast<int32_t>(F), &ws));
   // the array keeps whatever the last call left: lay it out for this call and reset it
@@ -349,6 +365,7 @@ int echo_prefill_indexer_score(const echo_prefill_args *a, void *stream) {
     if (a->stage) {
       REQUIRE(a->req_to_host && a->pool, "prefetch needs req_to_host and pool");
       TRY(check_pool(a->pool));
+      TRY(check_latent_rows(a->pool, "the prefill prefetch"));
       TRY(check_stage(a->stage, a->pool));
     }
   }
@@ -368,6 +385,7 @@ int echo_decode_step(const echo_step_args *a, void *stream) {
   const bool prefetch = a->s_hat && a->stage;
   // everything is checked before the first launch, so a rejected step enqueues nothing
   TRY(check_pool(a->pool));
+  TRY(check_latent_rows(a->pool, "the decode step"));
   REQUIRE(a->B >= 0 && a->L_max >= 0, "negative size");
   REQUIRE(a->n_q == 1 || a->n_q == 2, "n_q must be 1 or 2 (got %d)", a->n_q);
   REQUIRE(a->k >= 1 && a->k <= 8192, "k must be in [1, 8192] (got %d)", a->k);

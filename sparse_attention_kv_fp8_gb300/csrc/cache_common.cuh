@@ -80,6 +80,7 @@ struct PoolView {
   uint16_t *gpu_kv;
   const uint16_t *host_kv;
   int32_t n_g, n_h;
+  int32_t row_chunks;  // 16-byte pieces of a row (72 for MLA's latent row)
 };
 
 // What the top-k kernel needs to claim the entries it selects.

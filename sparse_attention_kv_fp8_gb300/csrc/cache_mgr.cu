@@ -311,9 +311,10 @@ __device__ __forceinline__ void rows_store(int4 *dst, const int32_t (&slot)[kRow
 // Source of the KV row of miss (entry f, host row h, staging index st): the
 // generated token (append), the staging area, or the pinned host pool.
 __device__ __forceinline__ const int4 *row_source(const OpParams &P, int32_t f, int32_t h, int32_t st) {
-  if (P.mode == kModeAppend) return reinterpret_cast<const int4 *>(P.new_kv) + static_cast<size_t>(f) * kKvChunks;
+  const size_t rc = static_cast<size_t>(P.pool.row_chunks);
+  if (P.mode == kModeAppend) return reinterpret_cast<const int4 *>(P.new_kv) + static_cast<size_t>(f) * rc;
   if (st >= 0) return reinterpret_cast<const int4 *>(P.stage_rows) + static_cast<size_t>(st) * kKvChunks;
-  return reinterpret_cast<const int4 *>(P.pool.host_kv) + static_cast<size_t>(h) * kKvChunks;
+  return reinterpret_cast<const int4 *>(P.pool.host_kv) + static_cast<size_t>(h) * rc;
 }
 
 __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParams P) {
@@ -825,7 +826,8 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     my_h = P.ws.miss_h[r];
     my_src = P.ws.miss_src[r];
   }
-  if (copies && my_nr > 0) {
+  const bool latent_rows = P.pool.row_chunks == kKvChunks;  // rows of other lengths copy after the ranking
+  if (copies && latent_rows && my_nr > 0) {
     const int4 *src[kRows];
 #pragma unroll
     for (int u = 0; u < kRows; ++u) {
@@ -921,7 +923,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
         used += st >= 0;
       }
     }
-    if (copies) {
+    if (copies && latent_rows) {
       int32_t slot[kRows];
       const int4 *src[kRows];
 #pragma unroll
@@ -933,6 +935,32 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
       }
       if (!first) rows_load(src, nr, buf);
       rows_store(reinterpret_cast<int4 *>(P.pool.gpu_kv), slot, nr, buf);
+    }
+  }
+  // rows of other lengths (block rows): every warp of the CTA copies 4 KB segments of
+  // the rows this CTA's slots take, so that a few large rows still keep all the warps'
+  // loads in flight
+  if (copies && !latent_rows && n_take > 0) {
+    const int rc = P.pool.row_chunks;
+    const int nseg = (rc + 32 * 8 - 1) / (32 * 8);
+    int4 *kv = reinterpret_cast<int4 *>(P.pool.gpu_kv);
+    for (int it = warp; it < n_take * nseg; it += kCoopWarps) {
+      const int t = it / nseg, c0 = (it % nseg) * (32 * 8);
+      const int r = static_cast<int>(a_lo) + t;
+      const int32_t s = take_cache ? take_cache[t] : __ldcg(P.ws.alloc_slot + r);
+      const int4 *src = row_source(P, P.ws.miss_f[r], P.ws.miss_h[r], P.ws.miss_src[r]);
+      int4 *dst = kv + static_cast<size_t>(s) * rc;
+      int4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = c0 + j * 32 + lane;
+        if (i < rc) v[j] = __ldcs(src + i);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = c0 + j * 32 + lane;
+        if (i < rc) dst[i] = v[j];
+      }
     }
   }
   // misses beyond the pool's capacity stay out of it
@@ -1026,9 +1054,10 @@ __global__ void append_prepare_kernel(PoolView pool, Workspace ws, uint8_t *k_in
   if (h >= 0) {
     // the host copy is written at generation (write-through); the GPU copy follows
     // in the allocation kernel
-    const int4 *src = reinterpret_cast<const int4 *>(new_kv) + static_cast<size_t>(b) * kKvChunks;
-    int4 *hdst = reinterpret_cast<int4 *>(const_cast<uint16_t *>(pool.host_kv)) + static_cast<size_t>(h) * kKvChunks;
-    for (int i = threadIdx.x; i < kKvChunks; i += blockDim.x) hdst[i] = src[i];
+    const int rc = pool.row_chunks;
+    const int4 *src = reinterpret_cast<const int4 *>(new_kv) + static_cast<size_t>(b) * rc;
+    int4 *hdst = reinterpret_cast<int4 *>(const_cast<uint16_t *>(pool.host_kv)) + static_cast<size_t>(h) * rc;
+    for (int i = threadIdx.x; i < rc; i += blockDim.x) hdst[i] = src[i];
     const int4 *ksrc = reinterpret_cast<const int4 *>(new_k_index) + static_cast<size_t>(b) * (kDim / 16);
     int4 *kdst = reinterpret_cast<int4 *>(k_index + (static_cast<size_t>(b) * L_max + p) * kDim);
     for (int i = threadIdx.x; i < kDim / 16; i += blockDim.x) kdst[i] = ksrc[i];
@@ -1130,6 +1159,7 @@ static echo::PoolView view_of(const echo_pool *p) {
   v.host_kv = p->host_kv;
   v.n_g = p->n_g;
   v.n_h = p->n_h;
+  v.row_chunks = (p->row_elems > 0 ? p->row_elems : echo::kKvElems) / 8;
   return v;
 }
 

@@ -30,7 +30,7 @@ KV_BYTES = KV_ELEMS * 2
 INF_I32 = 2**31 - 1   # the "empty" sentinel of the residency maps
 
 # stream ids, so that every array has its own independent draw
-_S_Q, _S_W, _S_K, _S_KV, _S_POOL, _S_EPS, _S_NEWKV, _S_NEWK, _S_MLAQ = range(1, 10)
+_S_Q, _S_W, _S_K, _S_KV, _S_POOL, _S_EPS, _S_NEWKV, _S_NEWK, _S_MLAQ, _S_BKV, _S_BSC = range(1, 12)
 
 
 def rng(seed: int, stream: int) -> np.random.Generator:
@@ -174,6 +174,47 @@ def mla_queries(B: int, n_q: int, seed: int, heads: int = 128) -> np.ndarray:
     attention has 128 heads over the 512 + 64 latent row)."""
     g = rng(seed, _S_MLAQ)
     return bf16_encode(g.standard_normal(size=(B, n_q, heads, KV_ELEMS), dtype=np.float32))
+
+
+# ---------------------------------------------------------------------------
+# block-level / GQA variant of the cache manager (the review's section 8: the cache
+# manager carries over to block-sparse attention with coarser metadata and a KV-head
+# dimension).  A pool row is one block of `block` tokens of one KV head, K and V of
+# head_dim each in bf16; a selection row is one (request, KV head) pair.  The shapes
+# of a GQA model with 8 KV heads of 128 dims and an NSA-style choice of 16 blocks of
+# 64 tokens stand in for a real model.
+# ---------------------------------------------------------------------------
+GQA_KV_HEADS, GQA_HEAD_DIM, GQA_BLOCK, GQA_TOPK_BLOCKS = 8, 128, 64, 16
+
+
+def block_row_elems(block: int = GQA_BLOCK, head_dim: int = GQA_HEAD_DIM) -> int:
+    """bf16 elements of one block row: K and V of `block` tokens of one KV head."""
+    return 2 * block * head_dim
+
+
+def block_kv_pool(n_units: int, row_elems: int, seed: int, out: np.ndarray | None = None,
+                  chunk_rows: int = 4096) -> np.ndarray:
+    """Host pool of block rows [n_units][row_elems] bf16 bits, N(0,1) draws."""
+    out = np.empty((n_units, row_elems), np.uint16) if out is None else out
+    g = rng(seed, _S_BKV)
+    for r0 in range(0, n_units, chunk_rows):
+        r1 = min(n_units, r0 + chunk_rows)
+        out[r0:r1] = bf16_encode(g.standard_normal((r1 - r0, row_elems), dtype=np.float32))
+    return out
+
+
+def block_scores(rows: int, n_blocks: int, seed: int, steps: int, rho: float) -> list[np.ndarray]:
+    """Scores of every block for `steps` consecutive decode steps, [rows][1][n_blocks]
+    fp32 each; step t+1 = rho * step t + sqrt(1 - rho^2) * fresh N(0,1), so that the
+    top blocks of consecutive steps overlap (rho = 0: independent steps)."""
+    g = rng(seed, _S_BSC)
+    s = g.standard_normal((rows, 1, n_blocks), dtype=np.float32)
+    out = [s.copy()]
+    c = np.float32(math.sqrt(max(0.0, 1.0 - rho * rho)))
+    for _ in range(steps - 1):
+        s = np.float32(rho) * s + c * g.standard_normal((rows, 1, n_blocks), dtype=np.float32)
+        out.append(s.astype(np.float32))
+    return out
 
 
 def req_to_host(B: int, L_max: int, base: int = 0) -> np.ndarray:

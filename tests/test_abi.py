@@ -58,7 +58,8 @@ int main(void) {
   printf("echo_step_args %zu\n", sizeof(echo_step_args));
   printf("echo_prefill_args %zu\n", sizeof(echo_prefill_args));
   printf("echo_mla_args %zu\n", sizeof(echo_mla_args));
-  P(echo_pool, counters) P(echo_pool, host_kv) P(echo_workspace, max_rows) P(echo_stage, cap_div)
+  P(echo_pool, counters) P(echo_pool, host_kv) P(echo_pool, row_elems) P(echo_workspace, max_rows)
+  P(echo_stage, cap_div)
   P(echo_stage, reserve) P(echo_stage, reserve_ctl) P(echo_stage, reserve_cap)
   P(echo_prefill_args, scores) P(echo_prefill_args, s_shift) P(echo_prefill_args, k) P(echo_prefill_args, thr_bin)
   P(echo_prefill_args, stage) P(echo_prefill_args, dev_status)
@@ -117,10 +118,21 @@ def test_argument_checks_reject_before_any_launch(lib):
     assert lib.echo_sparse_mla_decode(ctypes.byref(m), None) == echo.ECHO_EINVAL
     assert b"workspace" in lib.echo_last_error_string()
     n = ctypes.c_size_t()
+    # MLA scratch: per CTA of 128 selected rows its 128 x 512 fp16 partial output and
+    # its max / sum per head (fp32)
+    assert lib.echo_mla_workspace_bytes(8, 1, 2048, ctypes.byref(n)) == echo.ECHO_OK
+    assert n.value == 8 * 16 * 128 * (512 * 2 + 2 * 4)
+    assert lib.echo_mla_workspace_bytes(2, 1, 300, ctypes.byref(n)) == echo.ECHO_OK       # 3 CTAs each
+    assert n.value == 2 * 3 * 128 * (512 * 2 + 2 * 4)
+    assert lib.echo_mla_workspace_bytes(1, 1, 8193, ctypes.byref(n)) == echo.ECHO_EINVAL
     assert lib.echo_workspace_bytes(0, 10, ctypes.byref(n)) == echo.ECHO_EINVAL
     assert lib.echo_workspace_bytes(1000, 10, ctypes.byref(n)) == echo.ECHO_OK and n.value >= 4 * 1010
     pool = echo.c_pool(0, 10, 16, 16, 16, 16, 16, 16, 16, 16)                                  # n_g = 0
     assert lib.echo_pool_init(ctypes.byref(pool), None) == echo.ECHO_EINVAL
+    for bad in (12, -8, 65544):                                                               # row sizes
+        pool = echo.c_pool(10, 10, 16, 16, 16, 16, 16, 16, 16, 16, bad)
+        assert lib.echo_pool_init(ctypes.byref(pool), None) == echo.ECHO_EINVAL
+        assert b"row_elems" in lib.echo_last_error_string()
     assert lib.echo_decode_step(None, None) == echo.ECHO_EINVAL
 
 

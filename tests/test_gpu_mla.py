@@ -23,14 +23,14 @@ def bf16_f64(bits):
     return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-def run_mla(q, kv, sl, scale=SCALE):
+def run_mla(q, kv, sl, scale=SCALE, ws=None):
     B, n_q, k = sl.shape
     q_t = dev(q.view(np.int16))
     kv_t = kv if isinstance(kv, torch.Tensor) else dev(kv.view(np.int16))
     out = torch.full((B, n_q, 128, 512), float("nan"), dtype=torch.float32, device="cuda")
     lse = torch.full((B, n_q, 128), float("nan"), dtype=torch.float32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    ws = echo.MlaWorkspace(B, n_q, k)
+    ws = ws or echo.MlaWorkspace(B, n_q, k)
     echo.echo_sparse_mla_decode(q_t, kv_t, dev(sl), scale, out, lse, ws, dev_status=st)
     torch.cuda.synchronize()
     return out.cpu().numpy(), lse.cpu().numpy(), int(st.item())
@@ -65,9 +65,11 @@ def pool_rows(n_g, seed):
     (2, 1, 256, 2),       # two full splits
     (2, 2, 300, 3),       # MTP, a ragged last split (44 rows: a partial chunk)
     (3, 1, 2048, 4),      # sixteen splits
+    (2, 1, 1100, 8),      # nine splits, the last of 76 rows
+    (2, 2, 8192, 9),      # 64 splits per query token, 256 CTAs
 ])
 def test_sparse_mla_matches_oracle(B, n_q, k, seed):
-    n_g = 5000
+    n_g = max(5000, k + 1000)
     kv = pool_rows(n_g, seed)
     q = wl.mla_queries(B, n_q, seed)
     g = np.random.default_rng(seed)
@@ -126,3 +128,19 @@ def test_attention_over_a_decode_step_reads_the_host_rows():
     host = c.host_t.numpy().view(np.uint16)
     rows = np.where(sel >= 0, c.r2h[np.arange(2)[:, None, None], np.maximum(sel, 0)], -1).astype(np.int32)
     check(q, host, rows, o, lse)
+
+
+def test_workspace_reused_across_calls_and_shapes():
+    """One workspace, sized for the largest call, serves repeated calls of several
+    shapes (more CTAs than SMs, and fewer)."""
+    n_g = 6000
+    kv = pool_rows(n_g, 10)
+    ws = echo.MlaWorkspace(3, 2, 4096)
+    g = np.random.default_rng(10)
+    for rep, (B, n_q, k) in enumerate([(3, 2, 4096), (3, 2, 4096), (2, 1, 300), (3, 1, 2048), (3, 2, 4096)]):
+        q = wl.mla_queries(B, n_q, 100 + rep)
+        sl = np.stack([np.stack([g.choice(n_g, size=k, replace=False) for _ in range(n_q)]) for _ in range(B)])
+        sl = sl.astype(np.int32)
+        out, lse, st = run_mla(q, kv, sl, ws=ws)
+        assert st == 0
+        check(q, kv, sl, out, lse)
