@@ -94,3 +94,56 @@ def test_prefetching_calls_need_latent_rows():
     out = torch.empty((2, 1, 4), dtype=torch.int32, device="cuda")
     with pytest.raises(echo.EchoError, match="576"):
         echo.echo_prefetch_recall(c.pool, c.ws, sel, c.r2h_t, c.ctx, 1, out, stage=stage)
+
+
+def test_block_recall_at_the_bench_size():
+    """The bench's block probe configuration: 4 requests x 8 KV heads, 1024 blocks of
+    32 KB each (1 GiB host pool), 8192 slots; a cold recall of 64 blocks per selection
+    row (2048 rows into an empty pool), then steady steps of 16 blocks from a full pool.
+    Rows carry a per-row pattern over every element, so any misplaced piece shows."""
+    R, rows, n_blocks, n_g = wl.block_row_elems(), 4 * wl.GQA_KV_HEADS, 1024, 8192
+    n_h = rows * n_blocks
+    host_np = np.empty((n_h, R), np.uint16)
+    cols = np.arange(R, dtype=np.uint16)[None, :]
+    for r0 in range(0, n_h, 2048):                       # (row * 7919 + col) mod 2^16
+        host_np[r0:r0 + 2048] = np.arange(r0, r0 + 2048, dtype=np.uint16)[:, None] * np.uint16(7919) + cols
+    host_t = pinned_host_pool(host_np)
+    r2h = wl.req_to_host(rows, n_blocks)
+    ctx_np = np.full(rows, n_blocks, np.int32)
+    pool = echo.Pool(n_g, host_t)
+    echo.echo_pool_init(pool)
+    ws = echo.Workspace(n_g, rows * 64)
+    orc = oracle.Pool.empty(n_g, n_h, host_np, row_elems=R)
+    g = np.random.default_rng(6)
+    sel = np.sort(np.stack([g.choice(n_blocks, 64, replace=False) for _ in range(rows)]), axis=1)
+    sel = sel.astype(np.int32)[:, None, :]
+    out = torch.empty(sel.shape, dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    echo.echo_prefetch_recall(pool, ws, dev(sel), dev(r2h), dev(ctx_np), 10, out, dev_status=st)
+    ref, rs = orc.prefetch_recall(sel, r2h, 10)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy(), ref) and int(st.item()) == rs == 0
+    m, o = pool.metadata(), orc.metadata()
+    for key in o:
+        assert np.array_equal(m[key], o[key]), key
+    slots = ref.reshape(-1)
+    gkv = pool.gpu_kv[torch.from_numpy(slots.astype(np.int64)).cuda()].cpu().numpy().view(np.uint16)
+    assert np.array_equal(gkv, host_np[r2h[np.repeat(np.arange(rows), 64), sel.reshape(-1)]])
+    # steady steps from a full pool: every miss evicts
+    res = wl.random_resident_rows(n_h, n_g, 6)
+    state = wl.resident_pool(n_g, n_h, res, wl.random_clocks(n_g, 100, 6), 6)
+    pool.load_state(state)
+    orc = oracle.Pool.from_state(state, host_np)
+    for t, sc in enumerate(wl.block_scores(rows, n_blocks, 7, 3, 0.9)):
+        sel, _ = oracle.select_topk(sc, ctx_np, wl.GQA_TOPK_BLOCKS)
+        out = torch.empty(sel.shape, dtype=torch.int32, device="cuda")
+        echo.echo_prefetch_recall(pool, ws, dev(sel), dev(r2h), dev(ctx_np), 100 + t, out, dev_status=st)
+        ref, rs = orc.prefetch_recall(sel, r2h, 100 + t)
+        torch.cuda.synchronize()
+        assert np.array_equal(out.cpu().numpy(), ref) and int(st.item()) == rs == 0
+        m, o = pool.metadata(), orc.metadata()
+        for key in o:
+            assert np.array_equal(m[key], o[key]), (t, key)
+        slots = ref.reshape(-1)
+        gkv = pool.gpu_kv[torch.from_numpy(slots.astype(np.int64)).cuda()].cpu().numpy().view(np.uint16)
+        assert np.array_equal(gkv, orc.gpu_kv[slots])

@@ -144,3 +144,18 @@ def test_workspace_reused_across_calls_and_shapes():
         out, lse, st = run_mla(q, kv, sl, ws=ws)
         assert st == 0
         check(q, kv, sl, out, lse)
+
+
+def test_decode_shape_sampled():
+    """The bench's configuration: 8 query tokens x 2048 selected rows drawn from a
+    200K-slot pool of random rows; two of the eight query tokens checked against the
+    oracle element by element."""
+    n_g, B, k = 200_000, 8, 2048
+    kv = pool_rows(n_g, 7)
+    g = np.random.default_rng(8)
+    sl = np.stack([g.choice(n_g, size=k, replace=False) for _ in range(B)]).astype(np.int32)[:, None, :]
+    q = wl.mla_queries(B, 1, 31)
+    out, lse, st = run_mla(q, kv, sl)
+    assert st == 0 and np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
+    for b in (0, 5):
+        check(q[b:b + 1], kv, sl[b:b + 1], out[b:b + 1], lse[b:b + 1])
