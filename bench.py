@@ -294,7 +294,7 @@ def run_ours(args):
     pool = echo.Pool(N_G, host_t)
     pool.load_state(st)
     ws = echo.Workspace(N_G, B * K_TOP)
-    stage = echo.Stage(B, L // CAP_DIV, CAP_DIV)
+    stage = echo.Stage(B, L // CAP_DIV, CAP_DIV, while_scoring=not args.prefetch_tail)
     out = echo.StepBuffers(B, 1, L, K_TOP)
     stats = echo.Stats()
     q_ring = dev(np.stack(qs))                       # [steps][B][1][64][128]
@@ -452,7 +452,7 @@ def run_ours(args):
     direct = off = None
     if args.reserve > 0:
         direct = prefetch_mode_leg(echo, torch, st, host_t, q_ring, w, k_index, ctx, r2h_t, flush_l2,
-                                   args.warmup, args.steps, n_stage, args.reserve)
+                                   args.warmup, args.steps, n_stage, args.reserve, not args.prefetch_tail)
         off = prefetch_mode_leg(echo, torch, st, host_t, q_ring, w, k_index, ctx, r2h_t, flush_l2,
                                 args.warmup, args.steps, n_stage, 0)
 
@@ -479,6 +479,8 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 (indexer); int32 metadata; bf16 bytes",
         "data": "synthetic",
         "config": {"workload": workload_name(args.overlap), "l2": L2_NOTE, "rho": rho, "graph": "one CUDA graph per step",
+                   "prefetch": "staging area" + ("" if args.prefetch_tail else
+                                                 "; candidates still queued when a CTA's scoring ends are dropped"),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "scored_tokens_per_s": value * B * L,
         "hit_rate": hits / uniq,
@@ -518,7 +520,7 @@ def run_ours(args):
 
 
 def prefetch_mode_leg(echo, torch, st, host_t, q_ring, w, k_index, ctx, r2h_t, flush_l2, warmup, n_timed, n_stage,
-                      reserve):
+                      reserve, while_scoring=True):
     """The same steps (same start state, same queries) with another prefetch mode:
     reserve > 0, direct to slot (rows land in `reserve` slots each recall sets aside,
     instead of the staging area); reserve = 0, no prefetch at all (the whole miss set
@@ -527,8 +529,8 @@ def prefetch_mode_leg(echo, torch, st, host_t, q_ring, w, k_index, ctx, r2h_t, f
     pool = echo.Pool(N_G, host_t)
     pool.load_state(st)
     ws = echo.Workspace(N_G, B * K_TOP)
-    stage = echo.Stage(B, reserve=reserve) if reserve > 0 else (
-        echo.Stage(B, L // CAP_DIV, CAP_DIV) if reserve < 0 else None)
+    stage = echo.Stage(B, reserve=reserve, while_scoring=while_scoring) if reserve > 0 else (
+        echo.Stage(B, L // CAP_DIV, CAP_DIV, while_scoring=while_scoring) if reserve < 0 else None)
     out = echo.StepBuffers(B, 1, L, K_TOP)
     stats = echo.Stats()
     s_hat = torch.full((B, 1), float("inf"), dtype=torch.float32, device="cuda")
@@ -908,6 +910,9 @@ def main():
     ap.add_argument("--reserve", type=int, default=8192,
                     help="slots per recall for the direct-to-slot comparison leg (0: skip it and the "
                          "no-prefetch leg)")
+    ap.add_argument("--prefetch-tail", action="store_true",
+                    help="let the prefetch also copy candidates still queued when scoring ends (default: "
+                         "dropped, the recall fetches them if selected)")
     ap.add_argument("--kernel", default=None, choices=[None, "indexer", "prefill", "mla"],
                     help="run one kernel on a small case (for profilers) instead of the benchmark")
     ap.add_argument("--B", type=int, default=24)

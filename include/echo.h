@@ -164,7 +164,17 @@ typedef struct echo_stats {
  *   reserve_cap slots each recall sets aside (0 <= reserve_cap <= n_g); may change
  *               between recalls
  *   count       may be NULL; rows, host_row, stride and cap_div are not used
+ *
+ * Both modes:
+ *   flags       0, or ECHO_PREFETCH_WHILE_SCORING: the decode indexer's prefetch reads
+ *               no host row for a candidate still queued when its CTA has scored its
+ *               last tile (the copy would only lengthen the kernel; the recall fetches
+ *               the row if it is selected).  Which rows are prefetched then depends on
+ *               timing; selections, slots of selected rows and their bytes do not.
+ *               The prefill indexer ignores the flag.
  */
+#define ECHO_PREFETCH_WHILE_SCORING 1
+
 typedef struct echo_stage {
     uint16_t *rows;
     int32_t *host_row;
@@ -174,6 +184,7 @@ typedef struct echo_stage {
     int32_t *reserve;
     int32_t *reserve_ctl;
     int32_t reserve_cap;
+    int32_t flags;
 } echo_stage;
 
 /*
@@ -475,7 +486,8 @@ const char *echo_last_error_string(void);
 
 /* Library version, (major << 16) | minor (1.1: echo_stage's direct-to-slot fields;
    1.2: echo_prefill_indexer_score, echo_ema_update_strided, n_q up to 65536 in
-   top-k and recall; 1.3: echo_sparse_mla_decode; 1.4: echo_pool.row_elems). */
+   top-k and recall; 1.3: echo_sparse_mla_decode; 1.4: echo_pool.row_elems,
+   echo_stage.flags). */
 int32_t echo_version(void);
 
 /* Storage law of the metadata arrays of one pool (section 5.1): 4*n_h + 13*n_g. */

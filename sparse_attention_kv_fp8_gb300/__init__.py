@@ -49,7 +49,7 @@ class c_workspace(ctypes.Structure):
 
 class c_stage(ctypes.Structure):
     _fields_ = [("rows", _P), ("host_row", _P), ("count", _P), ("stride", _I32), ("cap_div", _I32),
-                ("reserve", _P), ("reserve_ctl", _P), ("reserve_cap", _I32)]
+                ("reserve", _P), ("reserve_ctl", _P), ("reserve_cap", _I32), ("flags", _I32)]
 
 
 class c_indexer_args(ctypes.Structure):
@@ -223,9 +223,11 @@ class Workspace:
 class Stage:
     """Where the prefetch puts rows: a staging area of `stride` rows per request, or,
     with reserve=R, straight into R GPU-pool slots each recall sets aside (direct to
-    slot; the staging buffers are not allocated then)."""
+    slot; the staging buffers are not allocated then).  while_scoring: the decode
+    indexer drops candidates still queued when a CTA's scoring ends."""
 
-    def __init__(self, B: int, stride: int = 1, cap_div: int = 16, device="cuda", reserve: int | None = None):
+    def __init__(self, B: int, stride: int = 1, cap_div: int = 16, device="cuda", reserve: int | None = None,
+                 while_scoring: bool = False):
         self.direct = reserve is not None
         self.stride, self.cap_div = int(stride), int(cap_div)
         self.count = torch.zeros(B, dtype=torch.int32, device=device)
@@ -235,14 +237,14 @@ class Stage:
             self.reserve = torch.full((max(self.reserve_cap, 1),), -1, dtype=torch.int32, device=device)
             self.reserve_ctl = torch.zeros(2, dtype=torch.int32, device=device)
             self.c = c_stage(None, None, _ptr(self.count), self.stride, self.cap_div, _ptr(self.reserve),
-                             _ptr(self.reserve_ctl), self.reserve_cap)
+                             _ptr(self.reserve_ctl), self.reserve_cap, int(bool(while_scoring)))
         else:
             self.rows = torch.zeros((B, stride, KV_ELEMS), dtype=torch.int16, device=device)
             self.host_row = torch.full((B, stride), -1, dtype=torch.int32, device=device)
             self.reserve = self.reserve_ctl = None
             self.reserve_cap = 0
             self.c = c_stage(_ptr(self.rows), _ptr(self.host_row), _ptr(self.count), self.stride, self.cap_div,
-                             None, None, 0)
+                             None, None, 0, int(bool(while_scoring)))
 
     def set_reserve_cap(self, R: int):
         """Slots each recall sets aside from now on (at most the capacity allocated)."""

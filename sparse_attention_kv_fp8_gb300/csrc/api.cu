@@ -135,6 +135,7 @@ static int check_ws(const echo_workspace *w, const echo_pool *p, long long rows)
 }
 
 static int check_stage(const echo_stage *st, const echo_pool *pool) {
+  REQUIRE((st->flags & ~ECHO_PREFETCH_WHILE_SCORING) == 0, "unknown stage flags 0x%x", st->flags);
   if (st->reserve) {  // direct to slot
     REQUIRE(st->reserve_ctl, "direct-to-slot stage without reserve_ctl");
     REQUIRE(st->reserve_cap >= 0 && st->reserve_cap <= pool->n_g,

@@ -65,6 +65,7 @@ struct IndexerParams {
   int32_t *stage_count;
   int32_t stage_stride;
   int32_t cap_div;
+  int32_t pf_while_scoring;  // drop candidates still queued once the CTA's scoring is done
   // direct-to-slot prefetch (reserve != nullptr): the reserved slots, the ticket
   // counter / reserve length, and the pool arrays a placed row updates
   const int32_t *reserve;
@@ -415,13 +416,14 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
     while (true) {
       // next queue with work, round robin; stop once every queue is done and drained
       int e = -1, tl = 0, head = 0;
-      bool all_done = true;
+      bool all_done = true, scored = true;
 #pragma unroll
       for (int u = 0; u < kQ; ++u) {
         const int qi = (turn + u) % kQ;
         const int q = pf + qi * kPfWarps;
         const int done = *reinterpret_cast<volatile int *>(&ctl->queue_done[q]);
         const int tq = *reinterpret_cast<volatile int *>(&ctl->queue_tail[q]);
+        scored = scored && done != 0;
         if (tq != heads[qi]) {
           if (e < 0) {
             e = q;
@@ -434,6 +436,10 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
           all_done = false;
         }
       }
+      // prefetch while scoring: the epilogue warps this warp serves have scored their
+      // last tiles, so what is still queued is dropped unread (nobody refills a queue
+      // once its epilogue warp is done)
+      if (P.pf_while_scoring && scored) break;
       if (e < 0) {
         if (all_done) break;
         const uint64_t now = globaltimer();
@@ -594,6 +600,7 @@ int launch_indexer(const echo_indexer_args *a, cudaStream_t stream) {
     P.host_to_gpu = a->pool->host_token_to_gpu;
     P.n_h = a->pool->n_h;
     P.host_kv = a->pool->host_kv;
+    P.pf_while_scoring = (a->stage->flags & ECHO_PREFETCH_WHILE_SCORING) != 0;
     if (a->stage->reserve) {
       P.reserve = a->stage->reserve;
       P.reserve_ctl = a->stage->reserve_ctl;

@@ -60,7 +60,7 @@ int main(void) {
   printf("echo_mla_args %zu\n", sizeof(echo_mla_args));
   P(echo_pool, counters) P(echo_pool, host_kv) P(echo_pool, row_elems) P(echo_workspace, max_rows)
   P(echo_stage, cap_div)
-  P(echo_stage, reserve) P(echo_stage, reserve_ctl) P(echo_stage, reserve_cap)
+  P(echo_stage, reserve) P(echo_stage, reserve_ctl) P(echo_stage, reserve_cap) P(echo_stage, flags)
   P(echo_prefill_args, scores) P(echo_prefill_args, s_shift) P(echo_prefill_args, k) P(echo_prefill_args, thr_bin)
   P(echo_prefill_args, stage) P(echo_prefill_args, dev_status)
   P(echo_mla_args, scale) P(echo_mla_args, workspace_bytes) P(echo_mla_args, dev_status)

@@ -21,9 +21,9 @@ pytestmark = pytest.mark.gpu
 RHO = 0.9
 
 
-def direct_case(B, n_q, L, ctx, n_g, res, clock, seed, k, R):
+def direct_case(B, n_q, L, ctx, n_g, res, clock, seed, k, R, while_scoring=False):
     c = Case(B, n_q, L, ctx, n_g, res, clock=clock, seed=seed, k=k)
-    c.stage = echo.Stage(B, reserve=R)
+    c.stage = echo.Stage(B, reserve=R, while_scoring=while_scoring)
     c.reserve = oracle.Reserve(R)
     return c
 
@@ -40,13 +40,16 @@ def gpu_assignment(c: Case, old_reserve: np.ndarray, staged: int):
     return slots, rows
 
 
-def check_assignment(c: Case, slots, rows, candidates, old_reserve):
+def check_assignment(c: Case, slots, rows, candidates, old_reserve, every=True):
+    """every=False (prefetch while scoring): candidates still queued when scoring ended
+    may be left out, so the placed rows are a subset of the candidates."""
     cand_rows = set()
     for b, toks in enumerate(candidates):
         cand_rows.update(int(c.r2h[b, p]) for p in toks)
     assert len(set(rows.tolist())) == rows.size, "a row placed twice"
     assert set(rows.tolist()) <= cand_rows, "a placed row was no candidate"
-    assert rows.size == min(len(old_reserve), len(cand_rows)), (rows.size, len(old_reserve), len(cand_rows))
+    want = min(len(old_reserve), len(cand_rows))
+    assert rows.size == want if every else rows.size <= want, (rows.size, len(old_reserve), len(cand_rows))
     gkv = c.pool.gpu_kv.cpu().numpy().view(np.uint16)
     host = c.host_t.numpy().view(np.uint16)          # the live pool: appends write through
     assert np.array_equal(gkv[slots], host[rows])
@@ -167,20 +170,21 @@ class DirectRunner:
         self.graph.replay()
 
 
-@pytest.mark.parametrize("B,n_q,L,ctx0,k,n_g,res,R,append,seed,graph", [
-    (1, 1, 4096, 4096, 256, 1024, 512, 64, False, 61, False),     # the tiny workload
-    (4, 1, 3000, 2900, 256, 1200, 1150, 300, True, 62, False),    # full pool: the reserve is evicted for
-    (3, 2, 2000, 1990, 200, 1500, 1400, 100, True, 63, False),    # two query tokens
-    (2, 1, 2501, 2480, 128, 900, 800, 900, True, 64, False),      # reserve larger than the pool can give
-    (2, 1, 3000, 2990, 256, 1000, 1000, 250, True, 65, True),     # steps 1.. replayed from one graph
+@pytest.mark.parametrize("B,n_q,L,ctx0,k,n_g,res,R,append,seed,graph,ws", [
+    (1, 1, 4096, 4096, 256, 1024, 512, 64, False, 61, False, False),     # the tiny workload
+    (4, 1, 3000, 2900, 256, 1200, 1150, 300, True, 62, False, False),    # full pool: the reserve is evicted for
+    (3, 2, 2000, 1990, 200, 1500, 1400, 100, True, 63, False, False),    # two query tokens
+    (2, 1, 2501, 2480, 128, 900, 800, 900, True, 64, False, False),      # reserve larger than the pool can give
+    (2, 1, 3000, 2990, 256, 1000, 1000, 250, True, 65, True, False),     # steps 1.. replayed from one graph
+    (4, 1, 3000, 2900, 256, 1200, 1150, 300, True, 66, True, True),      # prefetch while scoring, graph
 ])
-def test_direct_decode_steps_match_oracle(B, n_q, L, ctx0, k, n_g, res, R, append, seed, graph):
+def test_direct_decode_steps_match_oracle(B, n_q, L, ctx0, k, n_g, res, R, append, seed, graph, ws):
     """The oracle follows the GPU step by step on the GPU's scores (the threshold test
     and the selection are decided in fp32; the scores themselves are compared with
     the oracle's in the staging-mode step tests).  Which reserved slot a prefetched
     row lands in is a race, so a graph replay is checked the same way, not against an
     eager run."""
-    c = direct_case(B, n_q, L, ctx0, n_g, res, clock=1000, seed=seed, k=k, R=R)
+    c = direct_case(B, n_q, L, ctx0, n_g, res, clock=1000, seed=seed, k=k, R=R, while_scoring=ws)
     run = DirectRunner(c, append)
     O = c.orc_pool
     kI_o, ctx_o = c.inp.k_index.copy(), c.inp.ctx_len.copy()
@@ -207,7 +211,7 @@ def test_direct_decode_steps_match_oracle(B, n_q, L, ctx0, k, n_g, res, R, appen
         scores_g = run.out.scores.cpu().numpy()
         cand, _ = oracle.prefetch_candidates(scores_g, s_hat_o, ctx_o, c.r2h, O.HostTokenToGPU, L, 1)
         slots, rows = gpu_assignment(c, old, run.stats.as_dict()["staged"] - staged0)
-        check_assignment(c, slots, rows, cand, old)
+        check_assignment(c, slots, rows, cand, old, every=not ws)
         status_o |= O.prefetch_direct(slots, rows, clock)
         sel_g, kth_g = run.out.sel.cpu().numpy(), run.out.kth.cpu().numpy()
         sel_og, kth_og = oracle.select_topk(scores_g, ctx_o, k)
@@ -232,13 +236,18 @@ def test_direct_decode_steps_match_oracle(B, n_q, L, ctx0, k, n_g, res, R, appen
 
 def test_direct_lossless():
     """Selections are the same with the direct prefetch, the staging prefetch and no
-    prefetch, and every selected token's slot holds its host row's bytes."""
+    prefetch (each prefetch also while scoring only), and every selected token's slot
+    holds its host row's bytes."""
     B, L, k, n_g, res = 2, 6000, 400, 3000, 2900
     runs = []
-    for mode in ("direct", "staging", "none"):
+    for mode in ("direct", "staging", "none", "direct_while_scoring", "staging_while_scoring"):
         c = Case(B, 1, L, L - 10, n_g, res, clock=500, seed=71, k=k)
         if mode == "direct":
             c.stage = echo.Stage(B, reserve=500)
+        if mode == "direct_while_scoring":
+            c.stage = echo.Stage(B, reserve=500, while_scoring=True)
+        if mode == "staging_while_scoring":
+            c.stage = echo.Stage(B, c.stage_stride, c.cap_div, while_scoring=True)
         runner = DirectRunner(c, append=True, s_hat0=float("inf"))
         if mode == "none":
             runner.args = echo.make_step_args(c.pool, c.ws, runner.q_buf, c.w, c.k_index, c.ctx, c.r2h_t, k,
