@@ -28,7 +28,7 @@ class BlockCase:
         self.host_t = pinned_host_pool(self.host_np)
         self.pool = echo.Pool(n_g, self.host_t)
         self.pool.load_state(self.state)
-        self.ws = echo.Workspace(n_g, max(rows * k, rows))
+        self.ws = echo.Workspace(n_g, max(2 * rows * k, rows))
         self.ctx_np = np.full(rows, n_blocks, np.int32)
         self.ctx = dev(self.ctx_np)
         self.r2h_t = dev(self.r2h)
@@ -147,3 +147,28 @@ def test_block_recall_at_the_bench_size():
         slots = ref.reshape(-1)
         gkv = pool.gpu_kv[torch.from_numpy(slots.astype(np.int64)).cuda()].cpu().numpy().view(np.uint16)
         assert np.array_equal(gkv, orc.gpu_kv[slots])
+
+
+def test_block_recall_exhaustion_and_repeats():
+    """Block rows when the pool cannot hold every miss (POOL_EXHAUSTED, misses left
+    out with out_slot -1) and with two query tokens per (request, KV head) selecting
+    overlapping blocks (repeats take the slot of the block's first entry, no copy)."""
+    R, rows, n_blocks, k = 2048, 3, 128, 24
+    # two query tokens per selection row: the second token's blocks overlap the first's
+    c = BlockCase(rows, n_blocks, R, n_g=50, n_resident=20, clock=30, seed=13, k=k)
+    g = np.random.default_rng(13)
+    for t in range(3):
+        sc = g.standard_normal((rows, 2, n_blocks)).astype(np.float32)
+        sc[:, 1] = 0.7 * sc[:, 0] + 0.3 * sc[:, 1]
+        sel, _ = oracle.select_topk(sc, c.ctx_np, k)
+        out = torch.empty(sel.shape, dtype=torch.int32, device="cuda")
+        stats, st = echo.Stats(), torch.zeros(1, dtype=torch.int32, device="cuda")
+        echo.echo_prefetch_recall(c.pool, c.ws, dev(sel), c.r2h_t, c.ctx, 30 + t, out, stats=stats, dev_status=st)
+        ost = oracle.Stats()
+        ref, rs = c.orc.prefetch_recall(sel, c.r2h, 30 + t, stats=ost)
+        torch.cuda.synchronize()
+        assert np.array_equal(out.cpu().numpy(), ref), t
+        assert int(st.item()) == rs and rs & echo.DEV_POOL_EXHAUSTED
+        assert stats.as_dict() == ost.as_dict()
+        assert ost.as_dict()["unrecalled"] > 0
+        c.assert_equal(f"exhaustion step {t}")
