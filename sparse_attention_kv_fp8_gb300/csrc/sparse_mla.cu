@@ -451,8 +451,6 @@ size_t mla_workspace_bytes(int32_t B, int32_t n_q, int32_t k) {
   return units * echo::kMlaHeads * (echo::kMlaDv * sizeof(__half) + 2 * sizeof(float));
 }
 
-int mla_max_splits() { return 64; }
-
 int launch_sparse_mla(const echo_mla_args *a, cudaStream_t stream) {
   PFN_encodeTiledM enc = encode_fn_m();
   if (!enc) {
