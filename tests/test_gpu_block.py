@@ -172,3 +172,13 @@ def test_block_recall_exhaustion_and_repeats():
         assert stats.as_dict() == ost.as_dict()
         assert ost.as_dict()["unrecalled"] > 0
         c.assert_equal(f"exhaustion step {t}")
+
+
+def test_unknown_stage_flags_are_rejected():
+    c = BlockCase(2, 64, 576, n_g=32, n_resident=0, clock=1, seed=14, k=4)
+    stage = echo.Stage(2, 8, 16)
+    stage.c.flags = 2
+    sel = dev(np.zeros((2, 1, 4), np.int32))
+    out = torch.empty((2, 1, 4), dtype=torch.int32, device="cuda")
+    with pytest.raises(echo.EchoError, match="flags"):
+        echo.echo_prefetch_recall(c.pool, c.ws, sel, c.r2h_t, c.ctx, 1, out, stage=stage)
