@@ -483,6 +483,10 @@ def run_ours(args):
                                                  "; candidates still queued when a CTA's scoring ends are dropped"),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "scored_tokens_per_s": value * B * L,
+        "step_us": {"p10": float(np.percentile(step_ms, 10)) * 1e3, "p50": float(np.median(step_ms)) * 1e3,
+                    "p90": float(np.percentile(step_ms, 90)) * 1e3,
+                    "first_tenth_mean": float(np.mean(step_ms[:max(1, len(step_ms) // 10)])) * 1e3,
+                    "last_tenth_mean": float(np.mean(step_ms[-max(1, len(step_ms) // 10):])) * 1e3},
         "hit_rate": hits / uniq,
         "recalled_rows_per_step": recalled_rows / args.steps,
         "staged_rows_per_step": st_vals["staged"] / args.steps,
