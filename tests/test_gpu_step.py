@@ -240,3 +240,36 @@ def test_graph_replay_equals_eager():
             assert np.array_equal(ma[key], mb[key]), (step, key)
         assert torch.equal(cases[0].pool.gpu_kv, cases[1].pool.gpu_kv)
         assert torch.equal(a.s_hat, b.s_hat) and int(a.clock.item()) == int(b.clock.item()) == 301 + step
+
+
+def test_results_written_straight_into_pinned_host_memory():
+    """out_slot and the status word may live in pinned host memory (zero-copy results):
+    the same steps give the same slots, selections and pool as device-resident results."""
+    runs = []
+    for host_out in (False, True):
+        c = Case(2, 1, 3000, 2990, 1000, 1000, clock=300, seed=41, k=256)
+        R = StepRunner(c, s_hat0=float("inf"), append=True)
+        if host_out:
+            res = torch.zeros(2 * 256 + 1, dtype=torch.int32, pin_memory=True)
+            R.out.out_slot = res[:2 * 256].view(2, 1, 256)
+            R.out.dev_status = res[2 * 256:]
+            R.args = echo.make_step_args(c.pool, c.ws, R.q_buf, c.w, c.k_index, c.ctx, c.r2h_t, c.k, R.out,
+                                         stage=c.stage, s_hat=R.s_hat, new_kv=R.new_kv, new_k_index=R.new_ki,
+                                         clock_dev=R.clock, advance_clock=True, stats=R.stats)
+        qf = c.inp.q_float
+        outs = []
+        for step in range(4):
+            qf, q, kv, ki = step_inputs(c, step, qf)
+            R.set_inputs(q, kv, ki)
+            R.run()
+            torch.cuda.synchronize()
+            outs.append((R.out.sel.cpu().numpy().copy(), R.out.out_slot.cpu().numpy().copy(),
+                         int(R.out.dev_status.cpu().item())))
+        runs.append((outs, c.gpu_meta(), c.pool.gpu_kv.cpu().numpy()))
+    (a, ma, ka), (b, mb, kb) = runs
+    for (s0, o0, st0), (s1, o1, st1) in zip(a, b):
+        assert np.array_equal(s0, s1) and np.array_equal(o0, o1) and st0 == st1
+        assert np.all(o1[s1 >= 0] >= 0)
+    for key in ma:
+        assert np.array_equal(ma[key], mb[key]), key
+    assert np.array_equal(ka, kb)
