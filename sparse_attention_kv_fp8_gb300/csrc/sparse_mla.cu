@@ -29,7 +29,8 @@
 //          columns (S has been consumed);
 //     partial O divided by the split's sum, in fp16, stored dims-major (a warp writes
 //          32 heads of one dim: coalesced), max and sum per head;
-//   combine: per (b, j) and 4-dim slice, one thread per two heads merges the splits.
+//   combine: per (b, j) and 16-dim slice, the split weights once per block in shared
+//          memory, 16-byte partial loads, the result transposed for float4 stores.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -44,6 +45,7 @@ constexpr int kMlaDqk = kKvElems;                // 576
 constexpr int kMlaDv = 512;
 constexpr int kMlaBlocks = kMlaDqk / 64;         // 9 swizzled 64-dim blocks
 constexpr int kMlaSplit = 128;                   // selected rows per CTA (MMA N of pass A)
+constexpr int kMlaMaxK = 8192;                   // the largest k the C ABI accepts
 constexpr int kMlaThreads = 256;
 constexpr int kMlaStages = 5;                    // ring of q blocks
 constexpr uint32_t kMlaTile = 128 * 128;         // 128 rows (or heads) x one 64-dim block: 16 KB
@@ -346,76 +348,103 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
 }
 
 // o = sum_s w_s l_s o_s / sum_s w_s l_s (o_s the split's normalised partial),
-// w_s = exp(m_s - max_s m_s); lse = max + log(sum).  Block (bj, slice of 4 dims), 64
-// threads of two heads each: a warp reads 64 consecutive heads of one dim (128 bytes of
-// fp16 pairs) per load; eight splits' loads are in flight together.
-constexpr int kCombDims = 4;
-constexpr int kCombThreads = kMlaHeads / 2;
+// w_s = exp(m_s - max_s m_s); lse = max + log(sum).  Block (bj, slice of 16 dims), 256
+// threads: thread (dim d, group g of 8 heads) reads 16 bytes of one split's partial per
+// load (16 threads cover a dim's 128 heads: 256 contiguous bytes), sixteen splits' loads
+// issued before the weights are known.  The split weights of all 128 heads are computed
+// once per block into shared memory; the result tile is transposed in shared memory so
+// each head's 16 dims leave as four float4 stores.
+constexpr int kCombDims = 16;
+constexpr int kCombThreads = 256;
+constexpr int kCombChunk = 16;                      // splits whose loads are in flight together
+constexpr int kCombMaxSplits = kMlaMaxK / kMlaSplit;
 
 __global__ void __launch_bounds__(kCombThreads) sparse_mla_combine_kernel(const __half *part_o, const float *part_ml,
                                                                            int nsplit, float *out, float *lse) {
-  const int bj = blockIdx.x, d0 = blockIdx.y * kCombDims, h0 = 2 * threadIdx.x;
+  __shared__ __align__(16) float w_s[kCombMaxSplits][kMlaHeads];
+  __shared__ __align__(16) float o_s[kCombDims][kMlaHeads + 4];
+  __shared__ float il_s[kMlaHeads];
+  const int bj = blockIdx.x, d0 = blockIdx.y * kCombDims, t = threadIdx.x;
+  const int d = t / 16, h8 = 8 * (t % 16);
   ECHO_TRACE_FIRST(6);
-  const float2 *ml = reinterpret_cast<const float2 *>(part_ml);  // [unit][2][64 pairs]
-  // the maxima: sixteen splits' loads in flight together
-  float2 M = make_float2(-INFINITY, -INFINITY);
-  for (int s0 = 0; s0 < nsplit; s0 += 16) {
-    float2 m[16];
+  const uint4 *src = reinterpret_cast<const uint4 *>(part_o + (static_cast<size_t>(bj) * nsplit * kMlaDv + d0 + d) *
+                                                                   kMlaHeads + h8);
+  const size_t split_stride = static_cast<size_t>(kMlaDv) * kMlaHeads / 8;   // in uint4
+  uint4 v[kCombChunk];
 #pragma unroll
-    for (int q = 0; q < 16; ++q)
-      m[q] = s0 + q < nsplit ? ml[(static_cast<size_t>(bj) * nsplit + s0 + q) * kMlaHeads + threadIdx.x]
-                             : make_float2(-INFINITY, -INFINITY);
+  for (int q = 0; q < kCombChunk; ++q)
+    v[q] = q < nsplit ? __ldcs(src + q * split_stride) : make_uint4(0u, 0u, 0u, 0u);
+  if (t < kMlaHeads) {
+    // head t: the maximum over the splits, then each split's weight w_s l_s
+    const float *ml = part_ml + static_cast<size_t>(bj) * nsplit * 2 * kMlaHeads + t;
+    float M = -INFINITY;
+    for (int s0 = 0; s0 < nsplit; s0 += kCombChunk) {
+      float m[kCombChunk];
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      M.x = fmaxf(M.x, m[q].x);
-      M.y = fmaxf(M.y, m[q].y);
+      for (int q = 0; q < kCombChunk; ++q) m[q] = s0 + q < nsplit ? ml[(s0 + q) * 2 * kMlaHeads] : -INFINITY;
+#pragma unroll
+      for (int q = 0; q < kCombChunk; ++q) M = fmaxf(M, m[q]);
     }
-  }
-  float2 acc[kCombDims];
+    float L = 0.f;
+    for (int s0 = 0; s0 < nsplit; s0 += kCombChunk) {
+      float m[kCombChunk], l[kCombChunk];
 #pragma unroll
-  for (int i = 0; i < kCombDims; ++i) acc[i] = make_float2(0.f, 0.f);
-  float2 L = make_float2(0.f, 0.f);
-  for (int s0 = 0; s0 < nsplit; s0 += 8) {
-    float2 w[8];
-    __half2 v[8][kCombDims];
+      for (int q = 0; q < kCombChunk; ++q) {
+        const bool in = s0 + q < nsplit;
+        m[q] = in ? ml[(s0 + q) * 2 * kMlaHeads] : -INFINITY;
+        l[q] = in ? ml[(s0 + q) * 2 * kMlaHeads + kMlaHeads] : 0.f;
+      }
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int s = s0 + q;
-      w[q] = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int i = 0; i < kCombDims; ++i) v[q][i] = __floats2half2_rn(0.f, 0.f);
-      if (s < nsplit) {
-        const size_t u = static_cast<size_t>(bj) * nsplit + s;
-        const float2 m = ml[u * kMlaHeads + threadIdx.x];
-        const float2 l = ml[u * kMlaHeads + kMlaHeads / 2 + threadIdx.x];
-        w[q].x = M.x == -INFINITY ? 0.f : __expf(m.x - M.x) * l.x;
-        w[q].y = M.y == -INFINITY ? 0.f : __expf(m.y - M.y) * l.y;
-        const __half2 *src = reinterpret_cast<const __half2 *>(part_o + (u * kMlaDv + d0) * kMlaHeads + h0);
-#pragma unroll
-        for (int i = 0; i < kCombDims; ++i) v[q][i] = __ldcs(src + static_cast<size_t>(i) * (kMlaHeads / 2));
+      for (int q = 0; q < kCombChunk; ++q) {
+        if (s0 + q < nsplit) {
+          const float w = M == -INFINITY ? 0.f : __expf(m[q] - M) * l[q];
+          w_s[s0 + q][t] = w;
+          L += w;
+        }
       }
     }
+    il_s[t] = L > 0.f ? 1.f / L : 0.f;
+    if (blockIdx.y == 0) lse[static_cast<size_t>(bj) * kMlaHeads + t] = M == -INFINITY ? -INFINITY : M + logf(L);
+  }
+  __syncthreads();
+  float acc[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      L.x += w[q].x;
-      L.y += w[q].y;
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  for (int s0 = 0;; s0 += kCombChunk) {
 #pragma unroll
-      for (int i = 0; i < kCombDims; ++i) {
-        const float2 f = __half22float2(v[q][i]);
-        acc[i].x = fmaf(w[q].x, f.x, acc[i].x);
-        acc[i].y = fmaf(w[q].y, f.y, acc[i].y);
+    for (int q = 0; q < kCombChunk; ++q) {
+      if (s0 + q < nsplit) {
+        const float4 wa = *reinterpret_cast<const float4 *>(&w_s[s0 + q][h8]);
+        const float4 wb = *reinterpret_cast<const float4 *>(&w_s[s0 + q][h8 + 4]);
+        const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&v[q].x));
+        const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&v[q].y));
+        const float2 f2 = __half22float2(*reinterpret_cast<const __half2 *>(&v[q].z));
+        const float2 f3 = __half22float2(*reinterpret_cast<const __half2 *>(&v[q].w));
+        acc[0] = fmaf(wa.x, f0.x, acc[0]);
+        acc[1] = fmaf(wa.y, f0.y, acc[1]);
+        acc[2] = fmaf(wa.z, f1.x, acc[2]);
+        acc[3] = fmaf(wa.w, f1.y, acc[3]);
+        acc[4] = fmaf(wb.x, f2.x, acc[4]);
+        acc[5] = fmaf(wb.y, f2.y, acc[5]);
+        acc[6] = fmaf(wb.z, f3.x, acc[6]);
+        acc[7] = fmaf(wb.w, f3.y, acc[7]);
       }
     }
+    if (s0 + kCombChunk >= nsplit) break;
+#pragma unroll
+    for (int q = 0; q < kCombChunk; ++q)
+      v[q] = s0 + kCombChunk + q < nsplit ? __ldcs(src + (s0 + kCombChunk + q) * split_stride)
+                                          : make_uint4(0u, 0u, 0u, 0u);
   }
-  const float ix = L.x > 0.f ? 1.f / L.x : 0.f, iy = L.y > 0.f ? 1.f / L.y : 0.f;
-  float4 ox, oy;
-  ox = make_float4(acc[0].x * ix, acc[1].x * ix, acc[2].x * ix, acc[3].x * ix);
-  oy = make_float4(acc[0].y * iy, acc[1].y * iy, acc[2].y * iy, acc[3].y * iy);
-  *reinterpret_cast<float4 *>(out + (static_cast<size_t>(bj) * kMlaHeads + h0) * kMlaDv + d0) = ox;
-  *reinterpret_cast<float4 *>(out + (static_cast<size_t>(bj) * kMlaHeads + h0 + 1) * kMlaDv + d0) = oy;
-  if (blockIdx.y == 0) {
-    lse[static_cast<size_t>(bj) * kMlaHeads + h0] = M.x == -INFINITY ? -INFINITY : M.x + logf(L.x);
-    lse[static_cast<size_t>(bj) * kMlaHeads + h0 + 1] = M.y == -INFINITY ? -INFINITY : M.y + logf(L.y);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) o_s[d][h8 + i] = acc[i] * il_s[h8 + i];
+  __syncthreads();
+  // out[bj][h][d0 .. d0 + 16): 128 heads x 4 float4
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int f = t + kCombThreads * r, h = f / 4, c = 4 * (f % 4);
+    const float4 o = make_float4(o_s[c][h], o_s[c + 1][h], o_s[c + 2][h], o_s[c + 3][h]);
+    *reinterpret_cast<float4 *>(out + (static_cast<size_t>(bj) * kMlaHeads + h) * kMlaDv + d0 + c) = o;
   }
   ECHO_TRACE_LAST(7);
 }
@@ -477,6 +506,10 @@ int launch_sparse_mla(const echo_mla_args *a, cudaStream_t stream) {
   P.n_q = a->n_q;
   P.k = a->k;
   P.nsplit = (a->k + echo::kMlaSplit - 1) / echo::kMlaSplit;
+  if (P.nsplit > echo::kCombMaxSplits) {
+    set_error("sparse MLA: k above %d", echo::kMlaMaxK);
+    return ECHO_EINVAL;
+  }
   P.scale = a->scale;
   const size_t units = static_cast<size_t>(a->B) * a->n_q * P.nsplit;
   P.part_o = reinterpret_cast<__half *>(a->workspace);
