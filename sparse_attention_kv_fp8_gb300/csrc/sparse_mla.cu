@@ -48,6 +48,9 @@ constexpr int kMlaSplit = 128;                   // selected rows per CTA (MMA N
 constexpr int kMlaMaxK = 8192;                   // the largest k the C ABI accepts
 constexpr int kMlaThreads = 256;
 constexpr int kMlaStages = 5;                    // ring of q blocks
+constexpr int kMlaGroups = 3;                    // commit groups of the row gather
+constexpr int kMlaGroupBlocks = 3;               // 64-dim blocks per group
+static_assert(kMlaGroups * kMlaGroupBlocks == 576 / 64 && kMlaGroups == 3, "the gather's waits cover 3 groups");
 constexpr uint32_t kMlaTile = 128 * 128;         // 128 rows (or heads) x one 64-dim block: 16 KB
 constexpr uint32_t kMlaRowsBytes = kMlaBlocks * kMlaTile;        // the 128 rows: 144 KB
 constexpr uint32_t kMlaVHalf = 4 * kMlaTile;                     // 256 value dims of the 128 rows
@@ -116,6 +119,11 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t 
 }
 
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 __global__ void __launch_bounds__(kMlaThreads, 1)
     sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const MlaParams P) {
@@ -166,7 +174,9 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-  // q's first blocks by TMA; the rows by cp.async, every piece in flight together
+  // q's first blocks by TMA; the rows by cp.async, every piece in flight together, issued
+  // block by block (64 dims of all 128 rows) in kMlaGroups commit groups so that pass A
+  // starts on the first blocks while the later ones are still on their way
   if (threadIdx.x == 0)
     for (int d = 0; d < kMlaStages; ++d) {
       mbar_arrive_expect_tx(&bars[d], kMlaTile);
@@ -174,29 +184,40 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     }
   {
     const int4 *kv = reinterpret_cast<const int4 *>(P.gpu_kv);
-#pragma unroll 8
-    for (int t = threadIdx.x; t < kMlaSplit * kKvChunks; t += kMlaThreads) {
-      const int r = t / kKvChunks, ch = t % kKvChunks;  // a warp copies 512 consecutive bytes of a row
-      const int32_t slot = s_slot[r];
-      const int blk = ch >> 3, c = ch & 7;
-      cp_async16(rows_smem + blk * kMlaTile + r * 128 + ((c ^ (r & 7)) << 4),
-                 kv + static_cast<size_t>(slot >= 0 ? slot : 0) * kKvChunks + ch, slot >= 0 ? 16u : 0u);
+#pragma unroll
+    for (int g = 0; g < kMlaGroups; ++g) {
+#pragma unroll
+      for (int blk = g * kMlaGroupBlocks; blk < (g + 1) * kMlaGroupBlocks; ++blk) {
+#pragma unroll
+        for (int t = threadIdx.x; t < kMlaSplit * 8; t += kMlaThreads) {
+          const int r = t >> 3, c = t & 7;  // a warp copies 128 bytes of each of 4 rows
+          const int32_t slot = s_slot[r];
+          cp_async16(rows_smem + blk * kMlaTile + r * 128 + ((c ^ (r & 7)) << 4),
+                     kv + static_cast<size_t>(slot >= 0 ? slot : 0) * kKvChunks + blk * 8 + c, slot >= 0 ? 16u : 0u);
+        }
+      }
+      cp_async_commit();
     }
-    cp_async_wait_all();
   }
-  fence_async_smem();
-  __syncthreads();
-  ECHO_TRACE_LAST(1);
   bool ok = true;
   bool issued = false;  // thread 0 issued tcgen05 work (drained on a failure)
 
-  // ===== pass A: S = q . rows^T, one 64-dim block of q per ring stage (thread 0) =====
+  // ===== pass A: S = q . rows^T, one 64-dim block of q per ring stage (thread 0), each
+  // group of row blocks as soon as every thread's copies of it have landed =====
   constexpr uint32_t kIdescA = idesc_bf16_f32(kMlaHeads, kMlaSplit, 0);
-  if (threadIdx.x == 0) {
+  int waited = 0;  // (thread 0) blocks whose MMAs were seen done, in order
+#pragma unroll
+  for (int g = 0; g < kMlaGroups; ++g) {
+    if (g == 0) cp_async_wait_group<kMlaGroups - 1>();
+    else if (g == 1) cp_async_wait_group<kMlaGroups - 2>();
+    else cp_async_wait_all();
+    fence_async_smem();
+    __syncthreads();
+    if (g == kMlaGroups - 1) ECHO_TRACE_LAST(1);
+    if (threadIdx.x != 0 || !ok) continue;
     tc_fence_after();
     const uint32_t ra = smem_u32(rows_smem);
-    int waited = 0;  // blocks whose MMAs were seen done, in order
-    for (int d = 0; d < kMlaBlocks; ++d) {
+    for (int d = g * kMlaGroupBlocks; d < (g + 1) * kMlaGroupBlocks; ++d) {
       const int st = d % kMlaStages;
       if (!mbar_wait(&bars[st], (d / kMlaStages) & 1, abort, P.status)) {  // q's block d landed
         ok = false;
@@ -224,6 +245,8 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         tma_load_2d(ring + s2 * kMlaTile, &tmap_q, &bars[s2], nb * 64, bj * kMlaHeads);
       }
     }
+  }
+  if (threadIdx.x == 0) {
     for (; ok && waited < kMlaBlocks; ++waited)  // every pass-A MMA is done
       if (!mbar_wait(&bars[kBarMma + waited % kMlaStages], (waited / kMlaStages) & 1, abort, P.status)) ok = false;
     *wait_flag = ok ? 1 : 0;
