@@ -49,6 +49,7 @@ extern "C" {
 #define ECHO_DEV_WAIT_TIMEOUT 4     /* a pipeline wait gave up (kernel aborted) */
 #define ECHO_DEV_PREFETCH_CAP_HIT 8 /* info: prefetch candidates exceeded the cap
                                        (staging) or the reserve (direct to slot) */
+#define ECHO_DEV_INVARIANT 16       /* echo_pool_validate found a broken invariant */
 
 #define ECHO_INF 0x7fffffff
 #define ECHO_H_INDEX 64      /* indexer heads            */
@@ -345,8 +346,11 @@ int echo_prefetch_recall(const echo_pool *pool, const echo_workspace *ws, const 
  * Its scratch is one fixed array inside the library per device (4 MiB, held by
  * every GPU that loads the library until the process exits), laid out for pools of
  * at most 262144 slots and at most 32768 selected entries (B * n_q * k); larger
- * calls return ECHO_EINVAL with a message.  The first call on a device looks up the
- * array's device address, so make that first call before any stream capture.  Every
+ * calls return ECHO_EINVAL with a message.  A call made outside stream capture looks
+ * up the array's device address on the current device (so a context re-created after
+ * cudaDeviceReset is served too); a call made while the stream is capturing reuses the
+ * address found by the last such lookup on that device, so make the first call on each
+ * device before any stream capture.  Devices 0..63 are served (ECHO_ENOTSUP beyond).  Every
  * call re-initialises the array before using it (one extra small kernel), and all
  * calls share it: calls whose work overlaps on the GPU (other streams, other
  * threads) race and must not be issued.  Arguments and results as in
@@ -472,6 +476,60 @@ typedef struct echo_step_args {
 int echo_decode_step(const echo_step_args *args, void *stream);
 
 /*
+ * Metadata invariants of one pool (section 5.1 metadata table; section 5.2 "Free":
+ * a freed slot has free = 1, priority = -1 and no host row).  Every slot is in one
+ * state:
+ *   free       gpu_token_free = 1, priority = -1, gpu_token_to_host = INF
+ *   occupied   free = 0, priority >= 0 (or the prefetch's mark -3 between a
+ *              direct-to-slot indexer and its recall), gpu_token_to_host = h in
+ *              [0, n_h) with host_token_to_gpu[h] = s
+ *   reserved   free = 0, priority = -2, gpu_token_to_host = INF (direct to slot)
+ * and every host row is absent (host_token_to_gpu = INF) or maps to a slot that maps
+ * back.  counters[0] must equal the number of free slots; with a direct-to-slot
+ * stage the reserve's first reserve_ctl[1] entries must be reserved slots and no
+ * other slot may be.  Meant for quiescent points (between steps): inside a recall
+ * the maps hold claim marks by design.
+ * report receives ECHO_VAL_COUNT int32 values (indices below): the first five count
+ * violations, the next four the slots / rows seen in each state, the last one is the
+ * reserve's index balance (a non-zero balance counts as a reserve violation).
+ */
+#define ECHO_VAL_SLOT_STATE 0 /* slots whose free flag, priority and host row disagree  */
+#define ECHO_VAL_SLOT_MAP 1   /* occupied slots whose host row maps elsewhere           */
+#define ECHO_VAL_ROW_MAP 2    /* resident rows whose slot is out of range or elsewhere  */
+#define ECHO_VAL_COUNTER 3    /* 1 when counters[0] differs from the free slots         */
+#define ECHO_VAL_RESERVE 4    /* reserve entries that are not reserved slots, plus 1
+                                 when the reserved slots and the reserve's length differ */
+#define ECHO_VAL_FREE 5       /* free slots                                            */
+#define ECHO_VAL_OCCUPIED 6   /* occupied slots                                        */
+#define ECHO_VAL_RESERVED 7   /* reserved slots                                        */
+#define ECHO_VAL_RESIDENT 8   /* host rows with a slot                                 */
+#define ECHO_VAL_BALANCE 9    /* sum of the reserved slots' indices minus the sum of
+                                 the reserve's entries (mod 2^32): 0 unless the reserve
+                                 repeats a slot and leaves another out               */
+#define ECHO_VAL_COUNT 10
+
+/*
+ * The check on the device, in stream order: report [ECHO_VAL_COUNT] int32 device
+ * memory (overwritten); ECHO_DEV_INVARIANT is OR-ed into *dev_status when a violation
+ * count is non-zero.  stage: NULL, or a direct-to-slot stage whose reserve is checked.
+ * The reserve array is read only up to stage->reserve_cap entries (its length by the
+ * echo_stage contract); a recorded length above that counts as a reserve violation.
+ * Launches 2 kernels after clearing report; capturable.
+ */
+int echo_pool_validate(const echo_pool *pool, const echo_stage *stage, int32_t *report, int32_t *dev_status,
+                       void *stream);
+
+/*
+ * The same check over HOST copies of the arrays (every pointer in *pool_host is a
+ * host pointer; gpu_kv and host_kv are not read), for a snapshot taken with
+ * cudaMemcpy or for tools without a GPU.  reserve: NULL or reserve_len host int32.
+ * Fills report [ECHO_VAL_COUNT] (host) and returns ECHO_DEV_INVARIANT when a
+ * violation was found, else 0 (a negative value: bad arguments).
+ */
+int echo_pool_validate_host(const echo_pool *pool_host, const int32_t *reserve, int32_t reserve_len,
+                            int32_t *report);
+
+/*
  * Self-test of the failure detection (no counterpart on the pages): launches a
  * kernel whose wait nothing will satisfy -- which = 0: an mbarrier wait (the wait the
  * indexer's roles use), which = 1: a grid barrier of a cooperative launch that one CTA
@@ -487,7 +545,7 @@ const char *echo_last_error_string(void);
 /* Library version, (major << 16) | minor (1.1: echo_stage's direct-to-slot fields;
    1.2: echo_prefill_indexer_score, echo_ema_update_strided, n_q up to 65536 in
    top-k and recall; 1.3: echo_sparse_mla_decode; 1.4: echo_pool.row_elems,
-   echo_stage.flags). */
+   echo_stage.flags; 1.5: echo_pool_validate, echo_pool_validate_host). */
 int32_t echo_version(void);
 
 /* Storage law of the metadata arrays of one pool (section 5.1): 4*n_h + 13*n_g. */

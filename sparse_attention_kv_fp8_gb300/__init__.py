@@ -22,7 +22,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, f"libecho_gb300_{platform.machine()}.so")
 
 ECHO_OK, ECHO_EINVAL, ECHO_ECUDA, ECHO_ENOTSUP = 0, 1, 2, 3
-DEV_POOL_EXHAUSTED, DEV_BAD_INDEX, DEV_WAIT_TIMEOUT, DEV_PREFETCH_CAP_HIT = 1, 2, 4, 8
+DEV_POOL_EXHAUSTED, DEV_BAD_INDEX, DEV_WAIT_TIMEOUT, DEV_PREFETCH_CAP_HIT, DEV_INVARIANT = 1, 2, 4, 8, 16
+VAL_FIELDS = ("slot_state", "slot_map", "row_map", "counter", "reserve", "free", "occupied", "reserved",
+              "resident", "reserve_balance")
 INF = 0x7FFFFFFF
 H_INDEX, D_INDEX, KV_ELEMS, KV_BYTES = 64, 128, 576, 1152
 STAGE_APPEND, STAGE_INDEXER, STAGE_TOPK, STAGE_RECALL, STAGE_EMA, NUM_STAGES = range(6)
@@ -115,6 +117,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "echo_mla_workspace_bytes": ([_I32, _I32, _I32, ctypes.POINTER(ctypes.c_size_t)], S),
         "echo_sparse_mla_decode": ([ctypes.POINTER(c_mla_args), _P], S),
         "echo_decode_step": ([ctypes.POINTER(c_step_args), _P], S),
+        "echo_pool_validate": ([ctypes.POINTER(c_pool), ctypes.POINTER(c_stage), _P, _P, _P], S),
+        "echo_pool_validate_host": ([ctypes.POINTER(c_pool), _P, _I32, _P], S),
         "echo_last_error_string": ([], ctypes.c_char_p),
         "echo_version": ([], _I32),
         "echo_metadata_bytes": ([ctypes.c_int64, ctypes.c_int64], ctypes.c_int64),
@@ -439,6 +443,34 @@ def make_step_args(pool: Pool, ws: Workspace, q, w, k_index, ctx_len, req_to_hos
     a._keep = (pool, ws, stage, q, w, k_index, ctx_len, req_to_host, out, s_hat, new_kv, new_k_index, clock_dev,
                stats)
     return a
+
+
+def echo_pool_validate(pool: Pool, report, dev_status, stage: Stage | None = None, stream=None):
+    """Metadata invariants on the device: report [len(VAL_FIELDS)] int32 (device) gets the
+    counts, DEV_INVARIANT is OR-ed into dev_status when one is broken."""
+    _check(load_library().echo_pool_validate(ctypes.byref(pool.c), ctypes.pointer(stage.c) if stage is not None
+                                             else None, _dev(report, "report"), _dev(dev_status, "dev_status"),
+                                             _stream(stream)), "echo_pool_validate")
+
+
+def echo_pool_validate_host(free, prio, to_host, host_to_gpu, n_free: int, reserve=None):
+    """The same invariants over host copies (numpy arrays: free uint8 [n_g], prio /
+    to_host int32 [n_g], host_to_gpu int32 [n_h]).  Returns (violation found, counts)."""
+    import numpy as np
+    arrs = [np.ascontiguousarray(free, np.uint8), np.ascontiguousarray(prio, np.int32),
+            np.ascontiguousarray(to_host, np.int32), np.ascontiguousarray(host_to_gpu, np.int32)]
+    counters = np.array([n_free, 0, 0, 0], np.int32)
+    idx = np.full(arrs[0].size, -1, np.int32)
+    res = None if reserve is None else np.ascontiguousarray(reserve, np.int32)
+    report = np.zeros(len(VAL_FIELDS), np.int32)
+    ptr = lambda a: a.ctypes.data if a is not None and a.size else None
+    c = c_pool(arrs[0].size, arrs[3].size, ptr(arrs[0]), ptr(arrs[1]), ptr(idx), ptr(arrs[2]), ptr(arrs[3]),
+               None, None, ptr(counters), 0)
+    rc = load_library().echo_pool_validate_host(ctypes.byref(c), ptr(res), 0 if res is None else res.size,
+                                                ptr(report))
+    if rc < 0:
+        _check(-rc, "echo_pool_validate_host")
+    return rc == DEV_INVARIANT, dict(zip(VAL_FIELDS, report.tolist()))
 
 
 def echo_decode_step(args: c_step_args, stream=None):

@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build", platform.machine())
 LIB_PATH = os.path.join(HERE, f"libecho_gb300_{platform.machine()}.so")
-SOURCES = ["api.cu", "indexer.cu", "prefill.cu", "topk.cu", "cache_mgr.cu", "sparse_mla.cu"]
+SOURCES = ["api.cu", "indexer.cu", "prefill.cu", "topk.cu", "cache_mgr.cu", "sparse_mla.cu", "validate.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

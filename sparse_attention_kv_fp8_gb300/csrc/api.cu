@@ -53,7 +53,9 @@ int launch_ema(float *s_hat, const float *kth, int n, int stride, float alpha, c
 int launch_prefill_indexer(const echo_prefill_args *a, cudaStream_t stream);
 size_t mla_workspace_bytes(int32_t B, int32_t n_q, int32_t k);
 int launch_sparse_mla(const echo_mla_args *a, cudaStream_t stream);
-int noalloc_workspace(int32_t n_g, int32_t rows, echo_workspace *out);
+int noalloc_workspace(int32_t n_g, int32_t rows, cudaStream_t stream, echo_workspace *out);
+int launch_validate(const echo_pool *p, const echo_stage *stage, int32_t *report, int32_t *status, cudaStream_t s);
+int validate_host(const echo_pool *p, const int32_t *reserve, int32_t reserve_len, int32_t *report);
 
 }  // namespace echo_host
 
@@ -158,11 +160,31 @@ int echo_selftest_wait_timeout(int32_t which, int32_t *dev_status, void *stream)
   return launch_wait_probe(which, dev_status, static_cast<cudaStream_t>(stream));
 }
 
-int32_t echo_version(void) { return (1 << 16) | 4; }
+int32_t echo_version(void) { return (1 << 16) | 5; }
 
 int64_t echo_metadata_bytes(int64_t n_h, int64_t n_g) {
   return static_cast<int64_t>(sizeof(int32_t)) * n_h +
          static_cast<int64_t>(sizeof(uint8_t) + 3 * sizeof(int32_t)) * n_g;
+}
+
+int echo_pool_validate(const echo_pool *pool, const echo_stage *stage, int32_t *report, int32_t *dev_status,
+                       void *stream) {
+  g_err[0] = 0;
+  TRY(check_pool(pool));
+  REQUIRE(report && dev_status, "validate needs report and dev_status");
+  REQUIRE(!stage || (stage->reserve && stage->reserve_ctl), "validate's stage must be a direct-to-slot stage");
+  return launch_validate(pool, stage, report, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+int echo_pool_validate_host(const echo_pool *p, const int32_t *reserve, int32_t reserve_len, int32_t *report) {
+  g_err[0] = 0;
+  if (!p || !report || p->n_g <= 0 || p->n_h <= 0 || !p->gpu_token_free || !p->gpu_token_priority ||
+      !p->gpu_token_to_host || !p->host_token_to_gpu || !p->counters || reserve_len < 0 ||
+      (reserve_len > 0 && !reserve)) {
+    set_error("echo_pool_validate_host: bad arguments");
+    return -ECHO_EINVAL;
+  }
+  return validate_host(p, reserve, reserve_len, report);
 }
 
 int echo_indexer_score(const echo_indexer_args *a, void *stream) {
@@ -282,7 +304,7 @@ int echo_prefetch_recall_noalloc(const echo_pool *pool, const int32_t *sel, cons
     TRY(check_stage(stage, pool));
   }
   echo_workspace ws;
-  TRY(noalloc_workspace(pool->n_g, static_cast<int32_t>(F), &ws));
+  TRY(noalloc_workspace(pool->n_g, static_cast<int32_t>(F), static_cast<cudaStream_t>(stream), &ws));
   // the array keeps whatever the last call left: lay it out for this call and reset it
   TRY(launch_workspace_init(&ws, static_cast<cudaStream_t>(stream)));
   return launch_recall(pool, &ws, sel, req_to_host, ctx_len, B, n_q, k, L_max, stage, clock, clock_dev, out_slot,

@@ -21,7 +21,8 @@ constexpr int kHistLevels = 4;  // level 0 by age (12 bits); refinements of 12, 
 constexpr int kMaxGrid = 1024;
 
 // global scratch counters (zero between calls)
-enum { kGValid = 0, kGHits, kGBar, kGRepeats, kGFilled, kGCount = 16 };
+// kGBar / kGGen: the grid barrier's arrival count and generation
+enum { kGValid = 0, kGHits, kGBar, kGRepeats, kGFilled, kGGen, kGCount = 16 };
 // per-CTA counts
 enum { kCOwn = 0, kCLt, kCEq, kCFree, kCVals };
 // ws.ctr: results readable after a call

@@ -40,6 +40,8 @@
 // aside count as free here unless this step's prefetch filled them (P2's third role
 // counts the filled ones and gives the unselected ones the step clock); E also
 // covers the next reserve, and P4 hands the ranks after the misses' to it.
+#include <atomic>
+
 #include "cache_common.cuh"
 
 ECHO_TRACE_UNIT(cache_mgr)
@@ -198,28 +200,37 @@ __device__ __forceinline__ void coop_scan(const uint32_t (&v)[NV], uint32_t (&ex
   __syncthreads();
 }
 
-// Bounded grid barrier of a cooperative launch (every CTA is resident).  One
-// monotone arrival counter that is never reset: a CTA arriving with old value v
-// waits until the counter reaches the next multiple of the grid size.  A CTA that
-// waits longer than kWaitLimitNs sets WAIT_TIMEOUT and reports failure; the caller
-// then skips the remaining phases (the workspace must be re-initialised).
+// Bounded grid barrier of a cooperative launch (every CTA is resident), counted in
+// two words of the workspace: an arrival count that is back at 0 between barriers
+// and a generation number.  A CTA reads the generation, then arrives; the last of
+// the G arrivals resets the count and publishes generation + 1, which the others
+// wait for.  Nothing grows without bound (the generation compares by equality, so
+// its wrap-around is harmless), so a workspace serves any number of calls.  A CTA
+// that waits longer than kWaitLimitNs sets WAIT_TIMEOUT and reports failure; the
+// caller then skips the remaining phases (the workspace must be re-initialised).
 __device__ __forceinline__ bool grid_barrier(uint32_t *glob, int32_t *status, CoopSmem *S) {
   __syncthreads();
   if (threadIdx.x == 0) {
     uint32_t ok = 1;
     const uint32_t G = gridDim.x;
-    uint32_t old;
-    asm volatile("atom.add.release.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(glob + kGBar) : "memory");
-    const uint32_t target = (old / G + 1) * G;  // counts stay multiples of G between barriers
-    const uint64_t t0 = globaltimer();
-    for (;;) {
-      uint32_t cur;
-      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(cur) : "l"(glob + kGBar) : "memory");
-      if (static_cast<int32_t>(cur - target) >= 0) break;
-      if (globaltimer() - t0 > kWaitLimitNs) {
-        set_status(status, ECHO_DEV_WAIT_TIMEOUT);
-        ok = 0;
-        break;
+    uint32_t gen, old;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(gen) : "l"(glob + kGGen) : "memory");
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(glob + kGBar) : "memory");
+    if (old == G - 1) {
+      // every CTA has arrived: the count restarts for the next barrier before this one opens
+      asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(glob + kGBar), "r"(0u) : "memory");
+      asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(glob + kGGen), "r"(gen + 1u) : "memory");
+    } else {
+      const uint64_t t0 = globaltimer();
+      for (;;) {
+        uint32_t cur;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(cur) : "l"(glob + kGGen) : "memory");
+        if (cur != gen) break;
+        if (globaltimer() - t0 > kWaitLimitNs) {
+          set_status(status, ECHO_DEV_WAIT_TIMEOUT);
+          ok = 0;
+          break;
+        }
       }
     }
     S->red[7] = ok;
@@ -1224,7 +1235,7 @@ static int run_op(const echo::OpParams &P0, cudaStream_t s, bool pdl = false) {
   const long long epc = (static_cast<long long>(P.mode == echo::kModeEvict ? 0 : P.F) + grid - 1) / grid;
   P.slot_cache_cap = spc <= kSlotCacheMax ? static_cast<int>(spc) : 0;
   P.ent_cache_cap = epc <= kEntCacheMax ? static_cast<int>(epc) : 0;
-  static bool attr[64] = {false};
+  static std::atomic<bool> attr[kMaxDevices];
   if (int r = smem_limit_once(attr, echo::cache_op_kernel,
                               (3 * kSlotCacheMax + 2 * kEntCacheMax) * static_cast<int>(sizeof(int32_t)),
                               "cache-manager smem attribute"))
@@ -1299,8 +1310,8 @@ int launch_recall(const echo_pool *pool, const echo_workspace *ws, const int32_t
   return run_op(P, s, claimed != 0);  // after the decode step's top-k: programmatic launch
 }
 
-// the probes' grid barrier counts in its own 4-byte device word (never reset: a
-// barrier that gave up leaves it off a multiple of the grid, which only this probe uses)
+// the probe's grid barrier counts in words of its own, set back to zero before each
+// probe (a barrier that gave up leaves its arrival count short of the grid)
 static __device__ uint32_t g_probe_barrier[echo::kGCount];
 
 int launch_wait_probe(int which, int32_t *status, cudaStream_t s) {
@@ -1311,6 +1322,8 @@ int launch_wait_probe(int which, int32_t *status, cudaStream_t s) {
     echo::wait_probe_kernel<<<1, echo::kCoopThreads, 0, s>>>(0, glob, status);
     return check("wait probe");
   }
+  e = cudaMemsetAsync(glob, 0, sizeof(g_probe_barrier), s);
+  if (e != cudaSuccess) return cuda_fail(e, "wait probe reset");
   const int grid = sm_count() < 8 ? sm_count() : 8;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -1352,9 +1365,14 @@ constexpr int32_t kNoAllocMaxRows = 32768;
 constexpr size_t kNoAllocBytes = 4u << 20;  // >= the layout of the two maxima (checked below)
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
-// Device address of the array on the current device (resolved once per device,
-// with that device current; host code cannot use the symbol itself as an address).
-int noalloc_workspace(int32_t n_g, int32_t rows, echo_workspace *out) {
+// Device address of the array on the current device.  Host code cannot use the
+// symbol itself as an address, so the address is looked up with that device
+// current: on every call made outside stream capture (a context re-created after
+// cudaDeviceReset gets its own address), and kept per device for calls made while
+// the stream is capturing, which may not make the lookup.
+static std::atomic<void *> g_noalloc_addr[kMaxDevices];
+
+int noalloc_workspace(int32_t n_g, int32_t rows, cudaStream_t stream, echo_workspace *out) {
   if (workspace_bytes(kNoAllocMaxSlots, kNoAllocMaxRows) > kNoAllocBytes) {
     set_error("no-allocation scratch too small for its stated maxima");
     return ECHO_ENOTSUP;
@@ -1365,21 +1383,29 @@ int noalloc_workspace(int32_t n_g, int32_t rows, echo_workspace *out) {
               kNoAllocMaxSlots, kNoAllocMaxRows, n_g, rows);
     return ECHO_EINVAL;
   }
-  static void *addr[64] = {nullptr};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (dev < 0 || dev >= 64) {
-    set_error("device index %d out of range", dev);
+  if (dev < 0 || dev >= kMaxDevices) {
+    set_error("device index %d out of range (the library serves devices 0..%d)", dev, kMaxDevices - 1);
     return ECHO_ENOTSUP;
   }
-  if (!addr[dev]) {
-    void *p = nullptr;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(stream, &cs);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+  void *p = nullptr;
+  if (cs == cudaStreamCaptureStatusNone) {
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the no-allocation scratch");
-    addr[dev] = p;
+    g_noalloc_addr[dev].store(p, std::memory_order_release);
+  } else {
+    p = g_noalloc_addr[dev].load(std::memory_order_acquire);
+    if (!p) {
+      set_error("echo_prefetch_recall_noalloc: the first call on device %d must come before stream capture", dev);
+      return ECHO_EINVAL;
+    }
   }
-  out->base = addr[dev];
+  out->base = p;
   out->bytes = kNoAllocBytes;
   out->n_g = n_g;
   out->max_rows = rows;

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/echo.h"
 
 namespace echo {
@@ -347,17 +349,24 @@ namespace echo_host {
 void set_error(const char *fmt, ...);
 int cuda_fail(cudaError_t e, const char *what);
 
+// Devices a process may use with the library (per-device caches are this long).
+constexpr int kMaxDevices = 64;
+
 // Raises a kernel's dynamic shared-memory limit once per device (the first call on a
-// device must come before any stream capture on it).
+// device must come before any stream capture on it).  Threads making their first
+// call together may both set the attribute; the flag is atomic, so that is harmless.
 template <typename K>
-inline int smem_limit_once(bool (&done)[64], K kernel, int bytes, const char *what) {
+inline int smem_limit_once(std::atomic<bool> (&done)[kMaxDevices], K kernel, int bytes, const char *what) {
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) dev = 0;
-  if (done[dev]) return 0;
+  if (dev < 0 || dev >= kMaxDevices) {
+    set_error("device index %d out of range (the library serves devices 0..%d)", dev, kMaxDevices - 1);
+    return ECHO_ENOTSUP;
+  }
+  if (done[dev].load(std::memory_order_acquire)) return 0;
   const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return cuda_fail(e, what);
-  done[dev] = true;
+  done[dev].store(true, std::memory_order_release);
   return 0;
 }
 }  // namespace echo_host

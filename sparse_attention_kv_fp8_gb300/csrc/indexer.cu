@@ -519,16 +519,17 @@ static PFN_encodeTiled encode_fn() {
 // SM count of the current device (queried once per device, so that launches
 // made during stream capture issue no attribute queries)
 int sm_count() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[kMaxDevices];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) dev = 0;
-  if (cached[dev] == 0) {
-    int n = 0;
+  if (dev < 0 || dev >= kMaxDevices) dev = 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    cached[dev] = n > 0 ? n : 1;
+    n = n > 0 ? n : 1;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
 }
 
 static size_t indexer_smem_bytes(int nq) {
@@ -622,12 +623,12 @@ int launch_indexer(const echo_indexer_args *a, cudaStream_t stream) {
   const size_t smem = indexer_smem_bytes(nq);
   cudaError_t e;
   if (nq == 1) {
-    static bool attr1[64] = {false};
+    static std::atomic<bool> attr1[kMaxDevices];
     if (int r = smem_limit_once(attr1, echo::indexer_kernel<1>, static_cast<int>(smem), "indexer smem attribute"))
       return r;
     echo::indexer_kernel<1><<<grid, echo::kIndexerThreads, smem, stream>>>(tk, tq, tr, P);
   } else {
-    static bool attr2[64] = {false};
+    static std::atomic<bool> attr2[kMaxDevices];
     if (int r = smem_limit_once(attr2, echo::indexer_kernel<2>, static_cast<int>(smem), "indexer smem attribute"))
       return r;
     echo::indexer_kernel<2><<<grid, echo::kIndexerThreads, smem, stream>>>(tk, tq, tr, P);

@@ -532,7 +532,7 @@ int launch_prefill_indexer(const echo_prefill_args *a, cudaStream_t stream) {
   if (P.n_units == 0) return ECHO_OK;
   const int grid = P.n_units < sm_count() ? P.n_units : sm_count();
   const size_t smem = prefill_smem_bytes();
-  static bool attr[64] = {false};
+  static std::atomic<bool> attr[kMaxDevices];
   if (int r = smem_limit_once(attr, echo::prefill_indexer_kernel, static_cast<int>(smem), "prefill smem attribute"))
     return r;
   echo::prefill_indexer_kernel<<<grid, echo::kPThreads, smem, stream>>>(tk, tq, P);

@@ -541,7 +541,7 @@ int launch_sparse_mla(const echo_mla_args *a, cudaStream_t stream) {
   static_assert(echo::kMlaPBytes <= echo::kMlaRingBytes, "P lives in the q ring");
   const size_t smem = 1024 + echo::kMlaRowsBytes + echo::kMlaRingBytes + (2 * echo::kMlaStages + 2) * 8 + 16 +
                       echo::kMlaSplit * sizeof(int32_t) + 16;
-  static bool attr[64] = {false};
+  static std::atomic<bool> attr[kMaxDevices];
   if (int rr = smem_limit_once(attr, echo::sparse_mla_kernel, static_cast<int>(smem), "sparse MLA smem attribute"))
     return rr;
   echo::sparse_mla_kernel<<<static_cast<unsigned>(units), echo::kMlaThreads, smem, stream>>>(tq, P);

@@ -453,7 +453,7 @@ static int launch_topk_impl(const float *scores, const int32_t *ctx_len, int B, 
     smem += static_cast<size_t>(chunk) * sizeof(int32_t);
     stage_r2h = 1;
   }
-  static bool attr[64] = {false};
+  static std::atomic<bool> attr[kMaxDevices];
   if (int r = smem_limit_once(attr, echo::topk_kernel, echo::kTopkSmemMax, "top-k smem attribute")) return r;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(rows * C);

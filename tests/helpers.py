@@ -23,6 +23,26 @@ def pinned_host_pool(host_np: np.ndarray) -> torch.Tensor:
     return t
 
 
+def stamp_host_rows(hv: np.ndarray):
+    """Fill a [n][R] uint16 host pool so that every 16-byte vector of every row is
+    distinct: elements 0-1 hold the row index, element 2 the vector's index in the
+    row, the rest a bf16 1.0.  A copy that moves only part of a row, takes a vector
+    from the wrong row, or shifts vectors within a row leaves a visible difference."""
+    n, R = hv.shape
+    v = hv.reshape(n, R // 8, 8)
+    ids = np.arange(n, dtype=np.uint32)
+    v[:, :, 0] = (ids & np.uint32(0xFFFF)).astype(np.uint16)[:, None]
+    v[:, :, 1] = (ids >> np.uint32(16)).astype(np.uint16)[:, None]
+    v[:, :, 2] = np.arange(R // 8, dtype=np.uint16)[None, :]
+    v[:, :, 3:] = 0x3F80
+
+
+def assert_recall_stats_equal(gpu: dict, orc: dict, msg=""):
+    """The recall's counters that do not depend on the prefetch's timing."""
+    for key in ("steps", "selected", "unique_rows", "hits", "misses", "recalled", "unrecalled", "evicted"):
+        assert gpu[key] == orc[key], f"{msg} stats {key}: gpu {gpu[key]} oracle {orc[key]}"
+
+
 def assert_scores_close(gpu: np.ndarray, ref: np.ndarray, what="scores"):
     gpu = np.asarray(gpu, np.float64)
     ref = np.asarray(ref, np.float64)

@@ -173,3 +173,40 @@ def test_bounded_wait_gives_up_and_the_context_stays_usable(which):
     ref = oracle.indexer_score(c.inp.q, c.inp.w, c.inp.k_index, c.inp.ctx_len)
     assert int(st2.item()) == 0
     assert np.allclose(scores.cpu().numpy(), ref, rtol=1e-3, atol=1e-6)
+
+
+def _barrier_words(ws: echo.Workspace):
+    """The grid barrier's arrival count and generation inside a recall workspace: the
+    scratch layout puts 256-byte-aligned int32 arrays in this order: slot claims [n_g],
+    nine per-entry arrays [max_rows], histograms [4][4096], per-CTA counts [1024][4],
+    then the global words (arrival count at index 2, generation at index 5)."""
+    a = lambda n: (n * 4 + 255) // 256 * 256
+    off = (ws.c.base - ws.buf.data_ptr()) + a(ws.c.n_g) + 9 * a(ws.c.max_rows) + a(4 * 4096) + a(1024 * 4)
+    glob = ws.buf[off:off + 64].view(torch.int32)
+    return glob
+
+
+def test_recalls_across_the_barrier_generation_wrap_match_oracle():
+    """The cache manager's grid barrier counts arrivals back to zero at every barrier
+    and numbers its generations modulo 2^32: with the generation word set just below
+    the wrap, consecutive recalls still match the oracle and leave the arrival count
+    at rest."""
+    c = Case(4, 1, 3000, 3000, 1000, 1000, clock=400, seed=46, k=200)
+    glob = _barrier_words(c.ws)
+    torch.cuda.synchronize()
+    assert int(glob[2]) == 0 and int(glob[5]) == 0       # a fresh workspace
+    glob[5] = -3                                          # 0xFFFFFFFD: wraps within the next calls
+    g = np.random.default_rng(46)
+    for call in range(4):
+        scores = g.standard_normal((c.B, 1, c.L_max)).astype(np.float32)
+        sel_np, _ = oracle.select_topk(scores, c.inp.ctx_len, c.k)
+        out = torch.full(sel_np.shape, -7, dtype=torch.int32, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        echo.echo_prefetch_recall(c.pool, c.ws, dev(sel_np), c.r2h_t, c.ctx, 400 + call, out, dev_status=st)
+        torch.cuda.synchronize()
+        out_o, status_o = c.orc_pool.prefetch_recall(sel_np, c.r2h, 400 + call)
+        assert np.array_equal(out.cpu().numpy(), out_o), f"call {call}"
+        assert int(st.item()) == status_o
+        c.assert_pool_equal(c.orc_pool, f"call {call}")
+        assert int(glob[2]) == 0, "the arrival count did not return to rest"
+    assert 0 <= int(glob[5]) < 100, "the generation did not wrap"

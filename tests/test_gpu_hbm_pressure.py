@@ -7,7 +7,8 @@ recall runs in four sub-batches of eight requests (at most 32768 entries each), 
 its own clock: a sub-batch's rows are protected while it is recalled and become
 evictable for the next one (its attention would run in between).  After every
 sub-batch: out_slot, the five metadata arrays, the counters and the bytes of every
-occupied slot bit-exact against the oracle run on the GPU's selection.  The selection
+occupied slot bit-exact against the oracle run on the GPU's selection (every 16-byte
+vector of every host row is distinct), and the recall's statistics equal the oracle's.  The selection
 is bit-exact against the oracle's top-k on the GPU's scores (sampled requests), and one
 request's scores are within 1e-3 of the oracle's."""
 import numpy as np
@@ -17,7 +18,7 @@ import torch
 import oracle
 import sparse_attention_kv_fp8_gb300 as echo
 from sparse_attention_kv_fp8_gb300 import workload as wl
-from helpers import assert_scores_close, dev
+from helpers import assert_recall_stats_equal, assert_scores_close, dev, stamp_host_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -60,13 +61,10 @@ def test_mtp_recall_in_sub_batches_under_hbm_pressure():
     others = np.setdiff1d(g.choice(N_H, size=3 * N_G, replace=False), rows_sel)[: N_G - keep.size]
     resident = np.concatenate([keep, others])
     st = wl.resident_pool(N_G, N_H, resident, wl.random_clocks(N_G, T0, seed), seed)
-    # host pool: every row distinct through its index in the first two elements
-    host_t = torch.zeros((N_H, echo.KV_ELEMS), dtype=torch.int16, pin_memory=True)
+    # host pool: every 16-byte vector of every row distinct (row index, vector index)
+    host_t = torch.empty((N_H, echo.KV_ELEMS), dtype=torch.int16, pin_memory=True)
     hv = host_t.numpy().view(np.uint16)
-    ids = np.arange(N_H, dtype=np.uint32)
-    hv[:, 0] = (ids & np.uint32(0xFFFF)).astype(np.uint16)
-    hv[:, 1] = (ids >> np.uint32(16)).astype(np.uint16)
-    hv[:, 2:8] = 0x3F80
+    stamp_host_rows(hv)
     pool = echo.Pool(N_G, host_t)
     pool.load_state(st)
     orc = oracle.Pool.from_state(st, hv)                    # reads the same host rows
@@ -80,12 +78,14 @@ def test_mtp_recall_in_sub_batches_under_hbm_pressure():
         bs = slice(s * SUB, (s + 1) * SUB)
         clock = T0 + s
         status.zero_()
+        before = stats.as_dict()
         ev[0].record()
         echo.echo_prefetch_recall(pool, ws, sel_t[bs], r2h_t[bs], ctx_t[bs], clock, out[bs], stats=stats,
                                   dev_status=status)
         ev[1].record()
         torch.cuda.synchronize()
-        out_o, rs = orc.prefetch_recall(sel[bs], r2h[bs], clock)
+        ostats = oracle.Stats()
+        out_o, rs = orc.prefetch_recall(sel[bs], r2h[bs], clock, stats=ostats)
         assert np.array_equal(out[bs].cpu().numpy(), out_o), f"sub-batch {s}: out_slot differs"
         assert int(status.item()) == rs
         m, o = pool.metadata(), orc.metadata()
@@ -95,6 +95,7 @@ def test_mtp_recall_in_sub_batches_under_hbm_pressure():
         gkv = pool.gpu_kv.cpu().numpy().view(np.uint16)
         assert np.array_equal(gkv[occ], hv[o["to_host"][occ]]), f"sub-batch {s}: bytes differ"
         st_d = stats.as_dict()
+        assert_recall_stats_equal({k_: st_d[k_] - before[k_] for k_ in st_d}, ostats.as_dict(), f"sub-batch {s}")
         rec = st_d["recalled"] - recalled_before
         recalled_before = st_d["recalled"]
         print(f"sub-batch {s}: recalled {rec} rows ({rec * 1152 / 1e6:.1f} MB) in "

@@ -116,6 +116,14 @@ def test_multi_step_four_layers_graph_replay_with_appends():
         st = L.stats.as_dict()
         assert st["steps"] == STEPS and st["appended"] == STEPS * B and st["unrecalled"] == 0
         assert st["evicted"] >= st["recalled"] > 0
+        # the library's own invariant check finds every pool consistent after the run
+        report = torch.zeros(len(echo.VAL_FIELDS), dtype=torch.int32, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        echo.echo_pool_validate(L.pool, report, status)
+        torch.cuda.synchronize()
+        rep = dict(zip(echo.VAL_FIELDS, report.cpu().tolist()))
+        assert int(status.item()) == 0, rep
+        assert rep["occupied"] == N_G - int(L.pool.counters[0]) == rep["resident"], rep
 
 
 def check_step(layers, r2h, t):

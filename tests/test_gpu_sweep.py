@@ -3,8 +3,9 @@ k = 2048, GPU pool 200K slots, host pool B*L rows pinned): two decode steps each
 second with step-correlated queries (the calibrated overlap sets the hit rate) and the
 prefetch driven by the EMA of the first.
 
-Per step: out_slot, the metadata arrays, counters and pool bytes bit-exact against the
-oracle's recall on the GPU's selection; the selection bit-exact against the oracle's
+Per step: out_slot, the metadata arrays, counters, the recall's statistics (so the hit
+rate) and the bytes of every occupied slot bit-exact against the oracle's recall on the
+GPU's selection (every 16-byte vector of every host row is distinct); the selection bit-exact against the oracle's
 top-k on the GPU's scores (every request up to B = 4, three sampled beyond); one
 request's scores within 1e-3 of the oracle's; the EMA bit-exact."""
 import json
@@ -17,7 +18,7 @@ import torch
 import oracle
 import sparse_attention_kv_fp8_gb300 as echo
 from sparse_attention_kv_fp8_gb300 import workload as wl
-from helpers import assert_scores_close, dev
+from helpers import assert_recall_stats_equal, assert_scores_close, dev, stamp_host_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -30,7 +31,8 @@ def rho_for(L, overlap):
     return next(p["rho"] for p in pts if p["L"] == L and abs(p["target_overlap"] - overlap) < 1e-9)
 
 
-@pytest.mark.parametrize("B,L,overlap", [(1, 16384, 0.5), (2, 32768, 0.9), (16, 65536, 0.7), (32, 131072, 0.99)])
+@pytest.mark.parametrize("B,L,overlap", [(1, 16384, 0.5), (2, 32768, 0.9), (16, 65536, 0.7), (32, 131072, 0.99),
+                                         (8, 131072, 0.5), (32, 16384, 0.7)])
 def test_sweep_corner_two_steps(B, L, overlap):
     seed = 90 + B
     g = np.random.default_rng(seed)
@@ -43,12 +45,9 @@ def test_sweep_corner_two_steps(B, L, overlap):
     ctx = np.full(B, L, np.int32)
     n_h = B * L
     r2h = wl.req_to_host(B, L)
-    host_t = torch.zeros((n_h, echo.KV_ELEMS), dtype=torch.int16, pin_memory=True)
+    host_t = torch.empty((n_h, echo.KV_ELEMS), dtype=torch.int16, pin_memory=True)
     hv = host_t.numpy().view(np.uint16)
-    ids = np.arange(n_h, dtype=np.uint32)
-    hv[:, 0] = (ids & np.uint32(0xFFFF)).astype(np.uint16)
-    hv[:, 1] = (ids >> np.uint32(16)).astype(np.uint16)
-    hv[:, 5] = 0x4000
+    stamp_host_rows(hv)
     n_res = min(N_G, n_h // 2)
     st = wl.resident_pool(N_G, n_h, wl.random_resident_rows(n_h, n_res, seed), wl.random_clocks(n_res, T0, seed),
                           seed)
@@ -66,7 +65,6 @@ def test_sweep_corner_two_steps(B, L, overlap):
     args = echo.make_step_args(pool, ws, q_buf, w_t, k_t, ctx_t, r2h_t, K, out, stage=stage, s_hat=s_hat,
                                clock=T0, stats=stats)
     qf, q = inp.q_float, inp.q
-    hits_before = uniq_before = 0
     for step in range(2):
         if step:
             qf, q = wl.next_query(qf, rho, seed, step)
@@ -74,6 +72,7 @@ def test_sweep_corner_two_steps(B, L, overlap):
             args = echo.make_step_args(pool, ws, q_buf, w_t, k_t, ctx_t, r2h_t, K, out, stage=stage, s_hat=s_hat,
                                        clock=T0 + step, stats=stats)
         out.dev_status.zero_()
+        before = stats.as_dict()
         echo.echo_decode_step(args)
         torch.cuda.synchronize()
         scores_g, sel, kth = out.scores.cpu().numpy(), out.sel.cpu().numpy(), out.kth.cpu().numpy()
@@ -83,7 +82,8 @@ def test_sweep_corner_two_steps(B, L, overlap):
         b = step % B
         ref = oracle.indexer_score(q[b:b + 1], inp.w[b:b + 1], k_index[b:b + 1], ctx[b:b + 1])
         assert_scores_close(scores_g[b, 0], ref[0, 0], f"step {step} scores")
-        out_o, rs = orc.prefetch_recall(sel, r2h, T0 + step)
+        ostats = oracle.Stats()
+        out_o, rs = orc.prefetch_recall(sel, r2h, T0 + step, stats=ostats)
         assert np.array_equal(out.out_slot.cpu().numpy(), out_o), f"step {step}: out_slot differs"
         assert (int(out.dev_status.item()) & ~echo.DEV_PREFETCH_CAP_HIT) == rs
         m, o = pool.metadata(), orc.metadata()
@@ -95,8 +95,7 @@ def test_sweep_corner_two_steps(B, L, overlap):
         s_hat_o[...] = oracle.ema_update(s_hat_o, kth)
         assert np.array_equal(s_hat.cpu().numpy(), s_hat_o)
         d = stats.as_dict()
-        hit = (d["hits"] - hits_before) / max(1, d["unique_rows"] - uniq_before)
-        hits_before, uniq_before = d["hits"], d["unique_rows"]
-        print(f"B={B} L={L} target overlap {overlap}: step {step} hit rate {hit:.3f}, "
+        assert_recall_stats_equal({k_: d[k_] - before[k_] for k_ in d}, ostats.as_dict(), f"step {step}")
+        hit = ostats.hits / max(1, ostats.unique_rows)
+        print(f"B={B} L={L} target overlap {overlap}: step {step} hit rate {hit:.3f} (= the oracle's), "
               f"staged {d['staged']}, staged used {d['staged_used']}")
-    assert hit > overlap - 0.2   # the second step's hits come from the first step's recall
