@@ -7,7 +7,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "echo_common.cuh"
+#include "cache_common.cuh"
 
 namespace echo_host {
 
@@ -27,6 +27,8 @@ int cuda_fail(cudaError_t e, const char *what) {
 
 // launchers (indexer.cu, topk.cu, cache_mgr.cu)
 int launch_indexer(const echo_indexer_args *a, cudaStream_t stream);
+int launch_indexer(const echo_indexer_args *a, cudaStream_t stream, uint32_t *sel_hist, const int4 *sel_hint);
+echo::Workspace workspace_view(const echo_workspace *w);
 int launch_topk(const float *scores, const int32_t *ctx_len, int B, int n_q, int L_max, int k, int32_t *sel,
                 float *kth, cudaStream_t stream);
 size_t workspace_bytes(int32_t n_g, int32_t max_rows);
@@ -187,8 +189,9 @@ int echo_pool_validate_host(const echo_pool *p, const int32_t *reserve, int32_t 
   return validate_host(p, reserve, reserve_len, report);
 }
 
-int echo_indexer_score(const echo_indexer_args *a, void *stream) {
-  g_err[0] = 0;
+// the indexer's checks and launch; the decode step also hands it the workspace's
+// selection histograms (sel_hist / sel_hint, null for the public call)
+static int indexer_call(const echo_indexer_args *a, void *stream, uint32_t *sel_hist, const int4 *sel_hint) {
   REQUIRE(a, "args is NULL");
   REQUIRE(a->q && a->w && a->k_index && a->ctx_len && a->scores, "indexer pointer is NULL");
   REQUIRE(a->B >= 0 && a->L_max >= 0, "negative size");
@@ -205,7 +208,12 @@ int echo_indexer_score(const echo_indexer_args *a, void *stream) {
             "stage too large");
   }
   if (a->B == 0 || a->L_max == 0) return ECHO_OK;
-  return launch_indexer(a, static_cast<cudaStream_t>(stream));
+  return launch_indexer(a, static_cast<cudaStream_t>(stream), sel_hist, sel_hint);
+}
+
+extern "C" int echo_indexer_score(const echo_indexer_args *a, void *stream) {
+  g_err[0] = 0;
+  return indexer_call(a, stream, nullptr, nullptr);
 }
 
 int echo_select_topk(const float *scores, const int32_t *ctx_len, int32_t B, int32_t n_q, int32_t L_max, int32_t k,
@@ -451,7 +459,11 @@ int echo_decode_step(const echo_step_args *a, void *stream) {
     ia.pool = a->pool;
     ia.stage = a->stage;
   }
-  TRY(echo_indexer_score(&ia, stream));
+  {
+    // the indexer also fills the score histograms the top-k starts from
+    const echo::Workspace wv = workspace_view(a->ws);
+    TRY(indexer_call(&ia, stream, wv.sel_hist, wv.sel_hint));
+  }
   TRY(mark(ECHO_STAGE_TOPK));
   // the top-k kernel also makes the recall's claims for the entries it selects
   TRY(launch_topk_claim(a->scores, a->ctx_len, a->B, a->n_q, a->L_max, a->k, a->sel, a->kth, a->pool, a->ws,

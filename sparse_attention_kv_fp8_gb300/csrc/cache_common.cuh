@@ -17,6 +17,12 @@
 namespace echo {
 
 constexpr int kHistBins = 4096;
+// Score histograms the decode step's indexer fills for its top-k: one per score row
+// (request, query) for the first kSelHintRows rows, kSelBins bins over a window of
+// the order-preserving score keys predicted from the row's previous step
+constexpr int kSelBins = 2048;
+constexpr int kSelBinBits = 11;
+constexpr int kSelHintRows = 64;
 constexpr int kHistLevels = 4;  // level 0 by age (12 bits); refinements of 12, 12, 8 bits
 constexpr int kMaxGrid = 1024;
 
@@ -44,6 +50,8 @@ struct Workspace {
   uint32_t *cta;        // [kMaxGrid][kCVals]
   uint32_t *glob;       // [kGCount]
   int32_t *ctr;         // [kCtrCount]
+  uint32_t *sel_hist;   // [kSelHintRows][kSelBins] scores per key bin (zero between steps)
+  int4 *sel_hint;       // [kSelHintRows] window of each row's bins: {low key, shift, valid, 0}
 };
 
 __host__ __device__ inline size_t ws_align(size_t x) { return (x + 255) & ~size_t(255); }
@@ -71,6 +79,8 @@ __host__ __device__ inline size_t ws_layout(int32_t n_g, int32_t max_rows, uintp
   x.cta = reinterpret_cast<uint32_t *>(take(static_cast<size_t>(kMaxGrid) * kCVals));
   x.glob = reinterpret_cast<uint32_t *>(take(kGCount));
   x.ctr = reinterpret_cast<int32_t *>(take(kCtrCount));
+  x.sel_hist = reinterpret_cast<uint32_t *>(take(static_cast<size_t>(kSelHintRows) * kSelBins));
+  x.sel_hint = reinterpret_cast<int4 *>(take(static_cast<size_t>(kSelHintRows) * 4));
   if (w) *w = x;
   return off;
 }
@@ -96,6 +106,14 @@ struct ClaimArgs {
 
 // Claim of entry f (token p of request b); h = -1 for padding.  Records the
 // entry's host row in ws.entry_h.
+// Bin of score key `key` in a row's histogram window {lo, shift}: -1 below the
+// window, the last bin for every key above it (so the bins stay ordered like the keys)
+__device__ __forceinline__ int sel_bin(uint32_t key, uint32_t lo, uint32_t shift) {
+  if (key < lo) return -1;
+  const uint32_t b = (key - lo) >> shift;
+  return b < static_cast<uint32_t>(kSelBins) ? static_cast<int>(b) : kSelBins - 1;
+}
+
 __device__ __forceinline__ void claim_entry(const PoolView &pool, const Workspace &ws, int f, int32_t h,
                                             int32_t clock, int32_t *status) {
   if (h >= pool.n_h) {
@@ -109,9 +127,9 @@ __device__ __forceinline__ void claim_entry(const PoolView &pool, const Workspac
   const int32_t v = pool.h2g[h];
   if (v >= 0 && v < pool.n_g) {
     pool.prio[v] = clock;              // protect + LRU clock
-    atomicMin(ws.slot_claim + v, f);   // the first entry of the row owns the hit
+    red_min(ws.slot_claim + v, f);   // the first entry of the row owns the hit
   } else if (v == kInf || v < 0) {
-    atomicMin(pool.h2g + h, kClaim + f);  // the first entry of the row owns the miss
+    red_min(pool.h2g + h, kClaim + f);  // the first entry of the row owns the miss
   } else {
     set_status(status, ECHO_DEV_BAD_INDEX);
     h = -1;

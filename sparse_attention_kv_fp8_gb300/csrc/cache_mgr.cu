@@ -246,12 +246,12 @@ __device__ __forceinline__ void hist_flush(const uint32_t *local, uint32_t *glob
   const int start = (cta * 32) & (kHistBins - 1);
   for (int k = threadIdx.x; k < kHistBins; k += kCoopThreads) {
     const int i = (k + start) & (kHistBins - 1);
-    if (local[i]) atomicAdd(global + i, local[i]);
+    if (local[i]) red_add(global + i, local[i]);
   }
 }
 
 __device__ __forceinline__ void add_stat(echo_stats *st, int64_t echo_stats::*field, unsigned long long v) {
-  if (st && v) atomicAdd(reinterpret_cast<unsigned long long *>(&(st->*field)), v);
+  if (st && v) red_add(reinterpret_cast<unsigned long long *>(&(st->*field)), v);
 }
 
 // ---------------------------------------------------------------------------
@@ -386,7 +386,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
             set_status(P.status, ECHO_DEV_BAD_INDEX);
             h = -1;
           } else {
-            atomicMin(P.pool.h2g + h, kClaim + f);
+            red_min(P.pool.h2g + h, kClaim + f);
           }
         }
         P.ws.entry_h[f] = h;
@@ -598,10 +598,10 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
   if (P.mode != kModeAlloc) hist_flush(S->hist, P.ws.hist, c);
   if (threadIdx.x == 0 && P.mode != kModeEvict) {
     P.ws.cta[c * kCVals + kCOwn] = S->red[0];
-    if (S->red[1]) atomicAdd(glob + kGHits, S->red[1]);
-    if (S->red[2]) atomicAdd(glob + kGValid, S->red[2]);
-    if (S->red[3]) atomicAdd(glob + kGRepeats, S->red[3]);
-    if (S->red[4]) atomicAdd(glob + kGFilled, S->red[4]);
+    if (S->red[1]) red_add(glob + kGHits, S->red[1]);
+    if (S->red[2]) red_add(glob + kGValid, S->red[2]);
+    if (S->red[3]) red_add(glob + kGRepeats, S->red[3]);
+    if (S->red[4]) red_add(glob + kGFilled, S->red[4]);
     add_stat(P.stats, &echo_stats::staged, S->red[4]);
     add_stat(P.stats, &echo_stats::staged_used, S->red[5]);
   }
@@ -1082,7 +1082,7 @@ __global__ void append_prepare_kernel(PoolView pool, Workspace ws, uint8_t *k_in
         set_status(status, ECHO_DEV_BAD_INDEX);  // the new token's row is already resident
         ws.entry_rows[b] = -1;
       } else {
-        atomicMin(pool.h2g + h, kClaim + b);
+        red_min(pool.h2g + h, kClaim + b);
       }
     }
   }
@@ -1116,6 +1116,8 @@ __global__ void ws_init_kernel(Workspace ws, int n_g, int max_rows) {
   for (int i = tid; i < kMaxGrid * kCVals; i += nt) ws.cta[i] = 0;
   for (int i = tid; i < kGCount; i += nt) ws.glob[i] = 0u;
   for (int i = tid; i < kCtrCount; i += nt) ws.ctr[i] = 0;
+  for (int i = tid; i < kSelHintRows * kSelBins; i += nt) ws.sel_hist[i] = 0;
+  for (int i = tid; i < kSelHintRows; i += nt) ws.sel_hint[i] = make_int4(0, 0, 0, 0);
 }
 
 // Self-test of the bounded waits (no counterpart on the pages).  which = 0: one

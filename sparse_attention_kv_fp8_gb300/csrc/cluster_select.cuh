@@ -28,6 +28,14 @@ constexpr int kMaxBins = 1 << kDigitBits;
 
 constexpr int kScanVals = 4;  // counters a scan carries at most
 
+// The two halves of a cluster barrier (every thread of every CTA of the cluster
+// executes each once per barrier): arrive when this thread's last read of another
+// CTA's shared memory is done, wait before the shared memory may go away.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
 struct alignas(16) SelSmem {
   uint32_t hist[kMaxBins];
   uint32_t tot[kMaxBins];

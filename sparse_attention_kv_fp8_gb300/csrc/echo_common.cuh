@@ -35,6 +35,19 @@ __device__ __forceinline__ void set_status(int32_t *st, int32_t bits) {
   if (st) atomicOr(st, bits);
 }
 
+// Global reductions whose old value nobody needs: `red` lets the thread go on at once
+// (an atomicAdd / atomicMin whose result is dropped may still be issued as a
+// returning atomic, which waits a memory round trip).  Device memory only.
+__device__ __forceinline__ void red_add(uint32_t *p, uint32_t v) {
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_add(unsigned long long *p, unsigned long long v) {
+  asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void red_min(int32_t *p, int32_t v) {
+  asm volatile("red.relaxed.gpu.global.min.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
@@ -76,6 +89,18 @@ static __device__ unsigned long long g_echo_trace[32];
   do {                                                       \
     atomicMin(&g_echo_trace[slot], ~echo::globaltimer());    \
   } while (0)
+#define ECHO_TRACE_FIRST_HERE(slot)                          \
+  do {                                                       \
+    atomicMin(&g_echo_trace[slot], echo::globaltimer());     \
+  } while (0)
+#define ECHO_TRACE_VALUE(slot, v)                                                        \
+  do {                                                                                   \
+    if (blockIdx.x == 0 && threadIdx.x == 0) g_echo_trace[slot] = (unsigned long long)(v); \
+  } while (0)
+#define ECHO_TRACE_LAST_BLOCK(slot)                                                                   \
+  do {                                                                                                \
+    atomicMin(&g_echo_trace[slot], ~(((echo::globaltimer() & ((1ull << 56) - 1)) << 8) | (unsigned long long)blockIdx.x)); \
+  } while (0)
 #else
 #define ECHO_TRACE_UNIT(name)
 #define ECHO_TRACE_MARK(slot) \
@@ -89,6 +114,15 @@ static __device__ unsigned long long g_echo_trace[32];
   } while (0)
 #define ECHO_TRACE_LAST_HERE(slot) \
   do {                             \
+  } while (0)
+#define ECHO_TRACE_FIRST_HERE(slot) \
+  do {                              \
+  } while (0)
+#define ECHO_TRACE_VALUE(slot, v) \
+  do {                            \
+  } while (0)
+#define ECHO_TRACE_LAST_BLOCK(slot) \
+  do {                              \
   } while (0)
 #endif
 
@@ -353,8 +387,12 @@ int cuda_fail(cudaError_t e, const char *what);
 constexpr int kMaxDevices = 64;
 
 // Raises a kernel's dynamic shared-memory limit once per device (the first call on a
-// device must come before any stream capture on it).  Threads making their first
-// call together may both set the attribute; the flag is atomic, so that is harmless.
+// device must come before any stream capture on it), and asks for the largest
+// shared-memory carveout: the kernels of a step then share one L1 / shared-memory
+// split, so a kernel launched programmatically can start on an SM where the one
+// before it still runs instead of waiting for the SM to drain and be reconfigured.
+// Threads making their first call together may both set the attributes; the flag is
+// atomic, so that is harmless.
 template <typename K>
 inline int smem_limit_once(std::atomic<bool> (&done)[kMaxDevices], K kernel, int bytes, const char *what) {
   int dev = 0;
@@ -364,7 +402,9 @@ inline int smem_limit_once(std::atomic<bool> (&done)[kMaxDevices], K kernel, int
     return ECHO_ENOTSUP;
   }
   if (done[dev].load(std::memory_order_acquire)) return 0;
-  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return cuda_fail(e, what);
   done[dev].store(true, std::memory_order_release);
   return 0;

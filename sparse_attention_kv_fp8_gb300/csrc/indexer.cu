@@ -27,7 +27,7 @@
 #include <cstdio>
 #include <cstring>
 
-#include "echo_common.cuh"
+#include "cache_common.cuh"
 #include "prefetch_rows.cuh"
 
 ECHO_TRACE_UNIT(indexer)
@@ -76,6 +76,10 @@ struct IndexerParams {
   int32_t n_g;
   int32_t *status;
   int32_t r2h_tma;  // the tiles' host rows come by TMA (needs L_max % 4 == 0)
+  // decode step: per score row (b * n_q + j < kSelHintRows) a histogram of the score
+  // keys over the window sel_hint[row] (when valid), read by the top-k that follows
+  uint32_t *sel_hist;
+  const int4 *sel_hint;
 };
 
 struct alignas(16) IndexerCtl {
@@ -96,6 +100,7 @@ struct alignas(16) IndexerCtl {
   int queue[kEpiWarps][kQueueCap];    // token ids b * L_max + p that passed the threshold
   int queue_h[kEpiWarps][kQueueCap];  // their host rows (when the tiles' host rows are staged)
   float4 wsm[kEpiWarps][2 * kHeads / 4];  // head weights of the current request, per epilogue warp
+  uint32_t hwin[kEpiWarps][2][2];         // the current request's histogram windows {low key, shift}
 };
 
 __device__ __forceinline__ int tiles_of(int L) { return (L + kTileTokens - 1) / kTileTokens; }
@@ -212,6 +217,8 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  ECHO_TRACE_FIRST(28);
+  ECHO_TRACE_LAST(29);
 
   const int n_tiles = ctl->n_tiles;
   const uint32_t tmem_base = ctl->tmem_base;
@@ -270,6 +277,7 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
         }
         const int s = i % kStages;
         if (!mbar_wait(&ctl->full[s], (i / kStages) & 1, abort, P.status)) break;
+        if (i == 0) ECHO_TRACE_LAST_HERE(30);
         const int ab = i % kAcc;
         if (i >= kAcc && !mbar_wait(&ctl->tmem_empty[ab], ((i / kAcc) & 1) ^ 1, abort, P.status)) break;
         tc_fence_after();
@@ -300,6 +308,7 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
     for (int u = 0; u < grp; ++u) next_tile(P, b, t);
     float shat[NQ];
     int valid[NQ];
+    uint32_t hist_on = 0;  // bit j: query j's row has a selection histogram (window in hwin[e][j])
     int tail = 0;  // queue tail, kept by every lane (lane 0 publishes it)
     for (int i = grp; i < n_tiles; i += kEpiGroups) {
       if (b != cur_b) {
@@ -312,6 +321,19 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
         for (int j = 0; j < NQ; ++j) {
           valid[j] = query_valid_len(L, NQ, j);
           shat[j] = prefetch ? __ldg(P.s_hat + b * NQ + j) : 0.f;
+        }
+        hist_on = 0;
+        if (P.sel_hist && (b + 1) * NQ <= kSelHintRows) {
+          __syncwarp();
+          if (lane < NQ) {
+            const int4 h = P.sel_hint[b * NQ + lane];
+            ctl->hwin[e][lane][0] = static_cast<uint32_t>(h.x);
+            ctl->hwin[e][lane][1] = static_cast<uint32_t>(h.y);
+            hist_on = h.z ? 1u << lane : 0u;
+          }
+          __syncwarp();  // the windows are in shared memory before any lane reads them
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) hist_on |= __shfl_xor_sync(0xffffffffu, hist_on, o);
         }
         cur_b = b;
       }
@@ -360,7 +382,14 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
       const int p = t * kTileTokens + row;
 #pragma unroll
       for (int j = 0; j < NQ; ++j)
-        if (p < valid[j]) P.scores[(static_cast<size_t>(b) * NQ + j) * P.L_max + p] = sc[j];
+        if (p < valid[j]) {
+          P.scores[(static_cast<size_t>(b) * NQ + j) * P.L_max + p] = sc[j];
+          // the top-k's first radix step: count the score in its row's key window
+          if (hist_on >> j & 1) {
+            const int bin = sel_bin(score_key(sc[j]), ctl->hwin[e][j][0], ctl->hwin[e][j][1]);
+            if (bin >= 0) red_add(P.sel_hist + static_cast<size_t>(b * NQ + j) * kSelBins + bin, 1u);
+          }
+        }
 
       if (prefetch) {
         // threshold test only; the residency test, ticket and copy happen in the
@@ -397,7 +426,8 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
       __threadfence_block();
       *reinterpret_cast<volatile int *>(&ctl->queue_done[e]) = 1;
     }
-    if (lane == 0) ECHO_TRACE_LAST_HERE(26);
+    if (lane == 0) ECHO_TRACE_LAST_BLOCK(26);
+    if (lane == 0) ECHO_TRACE_FIRST_HERE(31);
   } else if (prefetch) {
     // ===================== prefetch copies =====================
     // prefetch warp e serves the queues of epilogue warps e, e + kPfWarps, ...
@@ -537,7 +567,7 @@ static size_t indexer_smem_bytes(int nq) {
          echo::kR * echo::kRowMapBytes + sizeof(IndexerCtl);
 }
 
-int launch_indexer(const echo_indexer_args *a, cudaStream_t stream) {
+int launch_indexer(const echo_indexer_args *a, cudaStream_t stream, uint32_t *sel_hist, const int4 *sel_hint) {
   PFN_encodeTiled enc = encode_fn();
   if (!enc) {
     set_error("cuTensorMapEncodeTiled unavailable from the driver");
@@ -589,6 +619,8 @@ int launch_indexer(const echo_indexer_args *a, cudaStream_t stream) {
   }
   echo::IndexerParams P{};
   P.r2h_tma = r2h_tma ? 1 : 0;
+  P.sel_hist = sel_hist;
+  P.sel_hint = sel_hint;
   P.w = a->w;
   P.ctx_len = a->ctx_len;
   P.scores = a->scores;
@@ -637,5 +669,7 @@ int launch_indexer(const echo_indexer_args *a, cudaStream_t stream) {
   if (e != cudaSuccess) return cuda_fail(e, "indexer launch");
   return ECHO_OK;
 }
+
+int launch_indexer(const echo_indexer_args *a, cudaStream_t stream) { return launch_indexer(a, stream, nullptr, nullptr); }
 
 }  // namespace echo_host

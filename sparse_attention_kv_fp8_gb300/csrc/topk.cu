@@ -18,6 +18,15 @@
 // entries it selects, one entry per thread from a compacted list, with the
 // request's host rows staged in shared memory before the scores are ready.
 // A threshold bin with more than kCand keys falls back to full radix passes.
+//
+// In the decode step the indexer has already made the first radix step: it counts
+// every score of the row in a kSelBins-bin histogram over a window of score keys
+// this kernel chose from the row's previous step (just below the k-th key up to the
+// largest).  The threshold bin then comes from that histogram directly -- no min /
+// max round, no local histogram, no coarse / fine gathers -- and the keys of that bin
+// are resolved as above.  Any window is exact (the bins are ordered like the keys);
+// when it misses (fewer keys in it than k, or its threshold bin too full) the kernel
+// takes the path above instead.
 #include "cache_common.cuh"
 #include "cluster_select.cuh"
 
@@ -41,7 +50,9 @@ struct alignas(16) TopkExtra {
   uint32_t ftot[kCoarse];            // cluster totals of the fine bins of the chosen coarse bin
   uint32_t off[kMaxCluster + 1];     // offsets of each rank's candidates in all_key
   uint32_t cand_n, above;            // published: keys in the threshold bin, keys above it
+  uint32_t kmax_pub;                 // published: this CTA's largest key (histogram path)
   uint32_t v[12];                    // block-wide values
+  uint32_t hv[4];                    // histogram path: threshold bin, keys above it, keys in it, row max
 };
 
 // The bin at which the running count of 64 bins, taken from the highest bin down,
@@ -104,9 +115,23 @@ __global__ void __launch_bounds__(kSelThreads, 1)
   for (int i = threadIdx.x; i < kCoarseBins; i += kSelThreads) X->ctot[i] = 0;
   if (threadIdx.x < kCoarse) X->ftot[threadIdx.x] = 0;
   if (threadIdx.x < 12) X->v[threadIdx.x] = 0;
+  if (threadIdx.x < 4) X->hv[threadIdx.x] = 0;
+  // decode step: the histogram of this row's scores the indexer made over the key
+  // window the last step chose (written by this kernel's previous launch, so it is
+  // read before the programmatic wait)
+  int4 hint = make_int4(0, 0, 0, 0);
+  if (do_claim && row < kSelHintRows) hint = ca.ws.sel_hint[row];
+  const uint32_t *hist_row = hint.z ? ca.ws.sel_hist + static_cast<size_t>(row) * kSelBins : nullptr;
+  const uint32_t hlo = static_cast<uint32_t>(hint.x), hsh = static_cast<uint32_t>(hint.y);
 
   pdl_wait();  // the scores come from the kernel before (programmatic launch)
   pdl_launch_dependents();
+  // this thread's two bins of the histogram (highest first), loaded while the keys load
+  uint32_t hc0 = 0, hc1 = 0;
+  if (hist_row && target > 0) {
+    hc0 = __ldcg(hist_row + (kSelBins - 1 - 2 * static_cast<int>(threadIdx.x)));
+    hc1 = __ldcg(hist_row + (kSelBins - 2 - 2 * static_cast<int>(threadIdx.x)));
+  }
   ECHO_TRACE_FIRST(26);
   ECHO_TRACE_MARK(0);
   const float *srow = scores + static_cast<size_t>(row) * L_max;
@@ -149,15 +174,53 @@ __global__ void __launch_bounds__(kSelThreads, 1)
   // ---- the target-th largest key T, how many keys equal to T are taken (needT), and
   // this CTA's output offsets (keys above T and equal to T in lower CTAs)
   uint32_t T = 0, needT = 0, pg = 0, pe = 0;
+  uint32_t row_max = 0;  // the row's largest key (for the next step's histogram window)
   bool offsets_known = false;
+  // candidate path: bit j of this thread's segment lies above the threshold bin
+  // (selected whatever T is) / in it; thr_above counts the first kind
+  const bool masks = s1 - s0 <= 64;
+  uint64_t above_mask = 0, cand_mask = 0;
+  uint32_t thr_above = 0;
+  bool classified = false;  // the candidate path filled the masks above
+  bool arrived = false;  // this CTA has made its last remote shared-memory read
   if (target > 0) {
-    uint32_t kmin, kmax;
+    // (1) the indexer's histogram: the bin d where the count from the top bin down
+    // reaches the target.  Every CTA reads the same counts, so every CTA takes the
+    // same branch; a window that misses (fewer keys in it than the target, or a
+    // threshold bin too full to resolve directly) falls back to (2).
+    bool fast = false;
+    if (hist_row) {
+      static_assert(kSelBins == 2 * kSelThreads, "two histogram bins per thread");
+      uint32_t ex, dz, tot, tz;
+      sel_block_scan2(hc0 + hc1, 0u, ex, dz, tot, tz, S);
+      const uint32_t tgt = static_cast<uint32_t>(target);
+      if (ex < tgt && tgt <= ex + hc0) {
+        X->hv[0] = kSelBins - 1 - 2 * threadIdx.x;
+        X->hv[1] = ex;
+        X->hv[2] = hc0;
+      } else if (ex + hc0 < tgt && tgt <= ex + hc0 + hc1) {
+        X->hv[0] = kSelBins - 2 - 2 * threadIdx.x;
+        X->hv[1] = ex + hc0;
+        X->hv[2] = hc1;
+      }
+      __syncthreads();
+      fast = tot >= tgt && X->hv[2] <= static_cast<uint32_t>(kCand);
+    }
+    uint32_t kmin = 0, kmax = 0, d = 0, above_d = 0, cnt_d = 0;
+    int shift = 0;
+    if (fast) {
+      d = X->hv[0];
+      above_d = X->hv[1];
+      cnt_d = X->hv[2];
+    } else {
+    // (2) cluster min / max, a 12-bit digit of key - min, coarse and fine bins
     sel_cluster_minmax(cl, S, mn, mx, kmin, kmax);
+    row_max = kmax;
     ECHO_TRACE_MARK(2);
     const uint32_t range = kmax - kmin;
     const int hb = range == 0 ? 0 : 32 - __clz(range);
     const int width = hb < kDigitBits ? hb : kDigitBits;
-    const int shift = hb - width;
+    shift = hb - width;
     const int nb = 1 << width;
     const int nco = (nb + kCoarse - 1) / kCoarse;
     // fine histogram of the digit (key - kmin) >> shift, one shared-memory atomic per key
@@ -220,39 +283,90 @@ __global__ void __launch_bounds__(kSelThreads, 1)
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-      if (lane == 0) {
-        X->above = a;
-        X->cand_n = S->hist[dd];
-      }
+      if (lane == 0) X->above = a;
     }
     __syncthreads();
-    const uint32_t d = D * kCoarse + X->v[2];
-    const uint32_t above_d = above_D + X->v[3];
-    const uint32_t cnt_d = X->ftot[X->v[2]];
+    d = D * kCoarse + X->v[2];
+    above_d = above_D + X->v[3];
+    cnt_d = X->ftot[X->v[2]];
+    }
     const uint32_t need_d = static_cast<uint32_t>(target) - above_d;
+    ECHO_TRACE_VALUE(27, cnt_d);
+    ECHO_TRACE_VALUE(28, (fast ? 1u : 0u) | (hist_row ? 2u : 0u));
+    ECHO_TRACE_VALUE(29, hsh);
+    ECHO_TRACE_VALUE(30, hlo);
+    ECHO_TRACE_VALUE(31, d);
+    // bin d as a key range [blo, bhi] in either form (the last histogram bin is open above)
+    const unsigned long long base = fast ? hlo : kmin;
+    const int bsh = fast ? static_cast<int>(hsh) : shift;
+    const unsigned long long top = 0xFFFFFFFFull;
+    const uint32_t blo = static_cast<uint32_t>(min(base + (static_cast<unsigned long long>(d) << bsh), top));
+    const uint32_t bhi =
+        (fast && d == kSelBins - 1)
+            ? 0xFFFFFFFFu
+            : static_cast<uint32_t>(min(base + (static_cast<unsigned long long>(d + 1) << bsh) - 1ull, top));
     ECHO_TRACE_MARK(4);
     if (cnt_d <= static_cast<uint32_t>(kCand)) {
-      // publish this CTA's keys of bin d; every CTA collects the cluster's and resolves T
+      // publish this CTA's keys of bin d (and, histogram path, how many of its keys lie
+      // above bin d and its largest key); every CTA collects the cluster's and resolves T
       {
-        uint32_t c = 0;
+        uint32_t c = 0, a = 0;
         for (int i = s0; i < s1; i += 4) {
           const uint4 v = keys4[i >> 2];
           const uint32_t kv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int u = 0; u < 4; ++u) c += (i + u < s1 && ((kv[u] - kmin) >> shift) == d);
+          for (int u = 0; u < 4; ++u)
+            if (i + u < s1) {
+              const bool above = kv[u] > bhi, in = !above && kv[u] >= blo;
+              c += in;
+              a += above;
+              if (masks) {
+                above_mask |= static_cast<uint64_t>(above) << (i + u - s0);
+                cand_mask |= static_cast<uint64_t>(in) << (i + u - s0);
+              }
+            }
         }
+        thr_above = a;
+        classified = masks;
         if (c) {  // rare: a second pass over the segment writes them
           const uint32_t slot = atomicAdd(&X->v[5], c);
           for (int i = s0, q = 0; i < s1 && q < static_cast<int>(c); ++i) {
             const uint32_t key = keys[i];
-            if (((key - kmin) >> shift) == d) X->cand_key[slot + q++] = key;
+            if (key >= blo && key <= bhi) X->cand_key[slot + q++] = key;
+          }
+        }
+        if (fast) {
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            a += __shfl_xor_sync(0xffffffffu, a, o);
+            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          }
+          if (lane == 0) {
+            if (a) atomicAdd(&X->v[11], a);
+            atomicMax(&X->hv[3], mx);
+          }
+        }
+        __syncthreads();
+        ECHO_TRACE_MARK(11);
+        if (threadIdx.x == 0) {
+          X->cand_n = X->v[5];
+          if (fast) {
+            X->above = X->v[11];
+            X->kmax_pub = X->hv[3];
           }
         }
       }
       cl.sync();  // every CTA's candidates published
+      ECHO_TRACE_MARK(12);
       if (warp == 0) {
         const TopkExtra *R = cl.map_shared_rank(X, lane < C ? lane : 0);
         const uint32_t n = lane < C ? R->cand_n : 0u, a = lane < C ? R->above : 0u;
+        if (fast) {  // the row's largest key
+          uint32_t m = lane < C ? R->kmax_pub : 0u;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+          if (lane == 0) X->hv[3] = m;
+        }
         uint32_t inc = n, ia = a;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -267,6 +381,7 @@ __global__ void __launch_bounds__(kSelThreads, 1)
         if (lane == rank) X->v[6] = ia - a;     // keys above bin d in lower CTAs
       }
       __syncthreads();
+      ECHO_TRACE_MARK(13);
       const int nc = static_cast<int>(X->off[C]);
       for (int g = threadIdx.x; g < nc; g += kSelThreads) {
         int r = 0;
@@ -274,6 +389,11 @@ __global__ void __launch_bounds__(kSelThreads, 1)
         X->all_key[g] = cl.map_shared_rank(X->cand_key, r)[g - static_cast<int>(X->off[r])];
       }
       __syncthreads();
+      // the last read of another CTA's shared memory on this path: arrive at the cluster
+      // barrier that lets the CTAs exit, wait for it only at the end
+      cluster_arrive();
+      arrived = true;
+      ECHO_TRACE_MARK(14);
       for (int i = threadIdx.x; i < nc; i += kSelThreads) {
         const uint32_t ki = X->all_key[i];
         uint32_t greater = 0, equal = 0;
@@ -288,6 +408,7 @@ __global__ void __launch_bounds__(kSelThreads, 1)
         }
       }
       __syncthreads();
+      ECHO_TRACE_MARK(15);
       T = X->v[7];
       needT = X->v[8];
       // lower CTAs' candidates above / equal to T (one warp-wide count per 32 candidates)
@@ -306,6 +427,7 @@ __global__ void __launch_bounds__(kSelThreads, 1)
       pg = X->v[6] + X->v[9];
       pe = X->v[10];
       offsets_known = true;
+      if (fast) row_max = X->hv[3];
     } else if (shift == 0) {
       // every key of bin d equals T: counts of the histogram are exact
       T = kmin + d;
@@ -330,8 +452,19 @@ __global__ void __launch_bounds__(kSelThreads, 1)
   // equal keys; each thread's segment is contiguous, so a block scan orders them
   uint32_t g = 0, e = 0;
   uint64_t sel_mask = 0;  // bit j: key s0 + j is above or equal to T (segments of at most 64)
-  const bool masks = s1 - s0 <= 64;
-  if (target > 0)
+  if (target > 0 && classified) {
+    // the candidate path classified every key already: only the threshold bin's keys
+    // (a handful per CTA) need comparing with T
+    g = thr_above;
+    sel_mask = above_mask;
+    for (uint64_t m = cand_mask; m; m &= m - 1) {
+      const int j = __ffsll(static_cast<long long>(m)) - 1;
+      const uint32_t key = keys[s0 + j];
+      g += key > T;
+      e += key == T;
+      if (key >= T) sel_mask |= 1ull << j;
+    }
+  } else if (target > 0)
     for (int i = s0; i < s1; i += 4) {
       const uint4 v = keys4[i >> 2];
       const uint32_t kv[4] = {v.x, v.y, v.z, v.w};
@@ -343,8 +476,10 @@ __global__ void __launch_bounds__(kSelThreads, 1)
           if (masks && kv[u] >= T) sel_mask |= 1ull << (i + u - s0);
         }
     }
+  ECHO_TRACE_MARK(16);
   uint32_t eg, ee, tg, te;
   sel_block_scan2(g, e, eg, ee, tg, te, S);
+  ECHO_TRACE_MARK(17);
   if (target > 0 && !offsets_known) {
     uint32_t gg, ge;
     sel_cluster_prefix2(cl, S, tg, te, pg, pe, gg, ge);
@@ -418,9 +553,32 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     out[i] = -1;
     if (do_claim) ca.ws.entry_h[f_row + i] = -1;
   }
-  if (rank == 0 && threadIdx.x == 0) kth[row] = target > 0 ? key_score(T) : -INFINITY;
+  if (rank == 0 && threadIdx.x == 0) {
+    kth[row] = target > 0 ? key_score(T) : -INFINITY;
+    // the window of this row's histogram in the next step, in key space:
+    // [T - max((max - T) / 4, 256), max], cut into kSelBins bins of 2^shift keys (keys
+    // above it count in the last bin)
+    if (do_claim && row < kSelHintRows) {
+      int4 h = make_int4(0, 0, 0, 0);
+      if (target > 0) {
+        const uint32_t span = row_max - T;
+        const uint32_t delta = max(span / 4u, 256u);
+        const uint32_t lo = T > delta ? T - delta : 0u;
+        const uint32_t width = row_max - lo;
+        const int hb = 32 - __clz(width | 1u);
+        h = make_int4(static_cast<int32_t>(lo), hb > kSelBinBits ? hb - kSelBinBits : 0, 1, 0);
+      }
+      ca.ws.sel_hint[row] = h;
+    }
+  }
   ECHO_TRACE_MARK(10);
-  cl.sync();  // no CTA leaves while others may still read its shared memory
+  // no CTA leaves while others may still read its shared memory
+  if (!arrived) cluster_arrive();
+  cluster_wait();
+  // every CTA of the cluster has read the histogram: back to zero for the next step
+  if (hist_row)
+    for (int i = rank * (kSelBins / C) + threadIdx.x; i < (rank + 1) * (kSelBins / C); i += kSelThreads)
+      ca.ws.sel_hist[static_cast<size_t>(row) * kSelBins + i] = 0u;
   ECHO_TRACE_MARK(7);
   ECHO_TRACE_LAST(25);
 }
