@@ -610,7 +610,17 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
   ECHO_TRACE_MARK(4);
 
   // ===== P3: M, E, threshold; owned misses listed in entry order; per-CTA slot counts =====
-  // the per-CTA owned counts and the age histogram (highest bin first) load together
+  // the global words, the per-CTA owned counts and the age histogram (highest bin
+  // first) load together
+  uint32_t g_valid = 0, g_hits = 0, g_rep = 0, g_fill = 0;
+  if (threadIdx.x == 0) {
+    if (c == 0) {
+      g_valid = __ldcg(glob + kGValid);
+      g_hits = __ldcg(glob + kGHits);
+    }
+    g_rep = P.mode == kModeRecall ? __ldcg(glob + kGRepeats) : 0u;
+    g_fill = direct ? __ldcg(glob + kGFilled) : 0u;
+  }
   constexpr int kPerBin = kHistBins / kCoopThreads;
   uint32_t hcnt[kPerBin];
   uint32_t m = 0, pm = 0, hmine = 0;
@@ -625,19 +635,16 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     hcnt[u] = P.mode != kModeAlloc ? __ldcg(P.ws.hist + (kHistBins - 1 - (threadIdx.x * kPerBin + u))) : 0u;
     hmine += hcnt[u];
   }
-  // final after the barrier: the step's valid entries and hits (for the stats)
-  uint32_t g_valid = 0, g_hits = 0;
-  if (c == 0 && threadIdx.x == 0) {
-    g_valid = __ldcg(glob + kGValid);
-    g_hits = __ldcg(glob + kGHits);
-    glob[kGValid] = 0;
-    glob[kGHits] = 0;
-  }
-  // repeats of a missed row exist: their out_slot needs one more grid barrier (one
-  // thread per CTA reads the count; the scan below hands it to the rest)
+  // final after the barrier: the step's valid entries and hits (for the stats); repeats
+  // of a missed row need one more grid barrier (thread 0 read the count, the scan below
+  // hands it to the rest)
   if (threadIdx.x == 0) {
-    S->red[6] = P.mode == kModeRecall ? __ldcg(glob + kGRepeats) : 0u;
-    S->red[5] = direct ? __ldcg(glob + kGFilled) : 0u;
+    if (c == 0) {
+      glob[kGValid] = 0;
+      glob[kGHits] = 0;
+    }
+    S->red[6] = g_rep;
+    S->red[5] = g_fill;
   }
   // this thread's segment of the entries; the staging rows of its owned misses
   const int e_cnt = e_hi - e_lo;
