@@ -60,7 +60,7 @@ def rho_for(L_: int, target: float) -> float:
 def indexer_source_sha256() -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in ("indexer.cu", "echo_common.cuh"):
+    for f in ("indexer.cu", "echo_common.cuh", "cache_common.cuh", "prefetch_rows.cuh"):
         with open(os.path.join(ROOT, "sparse_attention_kv_fp8_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
