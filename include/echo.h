@@ -169,9 +169,12 @@ typedef struct echo_stats {
  * Both modes:
  *   flags       0, or ECHO_PREFETCH_WHILE_SCORING: the decode indexer's prefetch reads
  *               no host row for a candidate still queued when its CTA has scored its
- *               last tile (the copy would only lengthen the kernel; the recall fetches
- *               the row if it is selected).  Which rows are prefetched then depends on
- *               timing; selections, slots of selected rows and their bytes do not.
+ *               last tile, and takes no candidate from the last two tiles each of its
+ *               epilogue warpgroups scores when a group scores at least eight (those
+ *               copies would only lengthen the kernel; the recall fetches the rows that
+ *               are selected).  Which rows are
+ *               prefetched then depends on timing; selections, slots of selected rows
+ *               and their bytes do not.
  *               The prefill indexer ignores the flag.
  */
 #define ECHO_PREFETCH_WHILE_SCORING 1

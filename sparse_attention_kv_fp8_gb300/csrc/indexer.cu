@@ -43,6 +43,12 @@ constexpr int kPfWarps = 8;                  // each serves kEpiWarps / kPfWarps
 constexpr int kIndexerThreads = 32 * (2 + kEpiWarps + kPfWarps);
 constexpr int kAcc = 4;            // TMEM accumulators (MMA runs up to 3 tiles ahead of the epilogue)
 constexpr int kQueueCap = 64;      // entries per epilogue -> prefetch queue
+// prefetching while scoring: each epilogue warpgroup of a CTA with at least
+// kPfTailMin tiles per group queues no candidate from its last kPfTailTiles tiles
+// (their host reads would land after the CTA's scoring ends and only lengthen the
+// kernel; the recall fetches such rows if they are selected)
+constexpr int kPfTailTiles = 2;
+constexpr int kPfTailMin = 8;
 // host rows of the tiles (req_to_host slices, 128 x int32) staged by TMA for the
 // epilogue: a ring the producer may refill only after the epilogue read the tile
 // kR tiles back, which the k^I ring and the TMEM accumulators already guarantee
@@ -306,6 +312,7 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
     float4 *wsm4 = ctl->wsm[e];
     int b = ctl->first_b, t = ctl->first_t, cur_b = -1;
     for (int u = 0; u < grp; ++u) next_tile(P, b, t);
+    const bool pf_cut = P.pf_while_scoring && n_tiles >= kPfTailMin * kEpiGroups;
     float shat[NQ];
     int valid[NQ];
     uint32_t hist_on = 0;  // bit j: query j's row has a selection histogram (window in hwin[e][j])
@@ -391,7 +398,7 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
           }
         }
 
-      if (prefetch) {
+      if (prefetch && !(pf_cut && i + kPfTailTiles * kEpiGroups >= n_tiles)) {
         // threshold test only; the residency test, ticket and copy happen in the
         // prefetch warps so that no global load sits on this path
         bool pass = false;
