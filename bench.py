@@ -463,9 +463,11 @@ def run_ours(args):
     out_e.dev_status = res_host[B * K_TOP:]
     ea = echo.make_step_args(pool, ws, q_dev, w_dev, k_index, ctx, r2h_t, K_TOP, out_e, stage=stage, s_hat=s_hat,
                              clock_dev=clock, advance_clock=True, stats=stats)
-    def e2e_body():
-        qw_dev.copy_(qw_host, non_blocking=True)
-        echo.echo_decode_step(ea)
+    w_host = qw_host[q_bytes:].view(torch.float32)
+
+    def e2e_body(wait=False):
+        # the C ABI's host-input step: the copy of q and w and the step's launches in one call
+        echo.echo_decode_step_host(ea, q_host, w_host, wait=wait)
 
     def e2e_loop(run, first):
         e_s = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
@@ -480,23 +482,13 @@ def run_ours(args):
             torch.cuda.synchronize()   # the host reads this step's out_slot and status
         return float(np.mean([s.elapsed_time(e) for s, e in zip(e_s, e_e)]))
 
-    # eager calls, then the same step with its copies captured in one graph (the way a
-    # serving loop runs it: the API is capturable and the clock lives on the device)
+    # direct calls, then the library's step graph (the way a serving loop runs it: the
+    # step captured once, the clock on the device, the input copy issued before each launch)
     e2e_eager_ms = e2e_loop(e2e_body, steps + n_stage)
-    # the step in a graph, the input copy issued before it (a copy node inside the graph
-    # ran several times slower on some boxes)
-    eg = torch.cuda.CUDAGraph()
-    cap = torch.cuda.Stream()
-    cap.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(cap):
-        with torch.cuda.graph(eg, stream=cap):
-            echo.echo_decode_step(ea)
-    torch.cuda.current_stream().wait_stream(cap)
-    torch.cuda.synchronize()
+    eg = echo.StepGraph(ea)
 
-    def e2e_graph():
-        qw_dev.copy_(qw_host, non_blocking=True)
-        eg.replay()
+    def e2e_graph(wait=False):
+        eg.launch(q_host, w_host, wait=wait)
 
     q_host.numpy()[...] = qs[steps + n_stage + 2 * n_e2e]  # one untimed replay first
     e2e_graph()
@@ -517,8 +509,7 @@ def run_ours(args):
             flush_l2()
             torch.cuda.synchronize()
             t0 = time.perf_counter()
-            run()
-            torch.cuda.current_stream().synchronize()
+            run(wait=True)   # returns once the stream has finished the step
             got = res_host.numpy().copy()
             ts.append(time.perf_counter() - t0)
         del got
@@ -626,9 +617,10 @@ def run_ours(args):
         "e2e": {"value": 1e6 / float(np.median(wall_direct)), "unit": "steps/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "how": ("host wall clock (median of %d steps) from inputs in pinned host memory to results "
-                        "read by the host: one copy of q and w from one pinned buffer, echo_decode_step "
-                        "through the C ABI, stream synchronisation, host read of out_slot and status "
-                        "(written by the kernels straight into pinned host memory)" % n_wall),
+                        "read by the host: echo_decode_step_host through the C ABI (one copy of q and w "
+                        "from one pinned buffer, the step's launches, a wait for the stream), then the "
+                        "host read of out_slot and status (written by the kernels straight into pinned "
+                        "host memory)" % n_wall),
                 "wall_us": {"p10": float(np.percentile(wall_direct, 10)), "p50": float(np.median(wall_direct)),
                             "p90": float(np.percentile(wall_direct, 90))},
                 "all_slots_valid": bool((out_e.out_slot >= 0).all().item()),
@@ -640,7 +632,8 @@ def run_ours(args):
                                       "p50": float(np.median(wall_graph)),
                                       "p90": float(np.percentile(wall_graph, 90))},
                           "device_value": 1e3 / e2e_ms,
-                          "how": "the same, the step replayed from a CUDA graph after the input copy"}},
+                          "how": "the same through the library's step graph (echo_step_graph_launch: the "
+                                 "input copy, then the captured step)"}},
         **extra,
         "gpu_launches": 3 * args.steps,
         "clocks": clk.summary(),

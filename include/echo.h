@@ -17,7 +17,9 @@
  *     the legacy default stream).  No call synchronises, allocates device or host
  *     memory, or reads device memory on the host, so every call can be captured
  *     into a CUDA graph (the first call of a process also sets kernel attributes;
- *     make one call outside capture first).
+ *     make one call outside capture first).  The exceptions are the host-input
+ *     calls echo_decode_step_host and echo_step_graph_* (they may wait for their
+ *     stream, and the graph calls own a captured graph).
  *   - The caller owns all memory.  Device pointers come from cudaMalloc or
  *     PyTorch; the host KV pool must be pinned and mapped (cudaHostAlloc with
  *     cudaHostAllocMapped, or any pinned allocation under unified addressing) and is
@@ -477,6 +479,40 @@ typedef struct echo_step_args {
 } echo_step_args;
 
 int echo_decode_step(const echo_step_args *args, void *stream);
+
+/*
+ * The same step with its per-step inputs taken from host memory, for callers whose
+ * query and head weights are produced on the host.  q_host holds B * n_q * 64 * 128
+ * e4m3 bytes laid out as args->q, w_host B * n_q * 64 floats laid out as args->w;
+ * both are copied on `stream` into args->q and args->w (one copy when w follows q
+ * directly in both buffers), then the step runs exactly as echo_decode_step.  The host
+ * buffers should be pinned (pageable memory makes the copy synchronous) and must stay
+ * unchanged until the copy has run.  wait != 0: the call returns once the stream has
+ * finished the step, so results the kernels wrote into pinned host memory (out_slot,
+ * dev_status) can be read at once.  Unlike the calls above, this one may synchronise
+ * (wait != 0).  Errors: as echo_decode_step, plus ECHO_EINVAL for a NULL q_host or
+ * w_host and ECHO_ECUDA when the copy or the synchronisation fails.
+ */
+int echo_decode_step_host(const echo_step_args *args, const void *q_host, const float *w_host, void *stream,
+                          int32_t wait);
+
+/*
+ * A decode step captured once into a CUDA graph owned by the library, then launched
+ * step after step: the serving loop's form of echo_decode_step_host.  create checks
+ * args as echo_decode_step does, requires the device clock (clock_dev != NULL; with
+ * advance_clock != 0 each launch is the next step) and no stage events, and captures
+ * the step's launches on a stream of its own (nothing runs).  The graph keeps the
+ * pointers in args: every buffer must outlive it.  launch copies q_host / w_host (as
+ * in echo_decode_step_host; both NULL: the inputs are already in args->q and args->w)
+ * and launches the graph on `stream`, waiting for it when wait != 0.  destroy frees
+ * the graph (NULL is accepted).  create allocates host memory and graph objects; a
+ * failed create returns no graph (*out = NULL).
+ */
+typedef struct echo_step_graph echo_step_graph;
+int echo_step_graph_create(const echo_step_args *args, echo_step_graph **out);
+int echo_step_graph_launch(echo_step_graph *graph, const void *q_host, const float *w_host, void *stream,
+                           int32_t wait);
+int echo_step_graph_destroy(echo_step_graph *graph);
 
 /*
  * Metadata invariants of one pool (section 5.1 metadata table; section 5.2 "Free":

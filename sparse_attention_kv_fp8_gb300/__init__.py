@@ -117,6 +117,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "echo_mla_workspace_bytes": ([_I32, _I32, _I32, ctypes.POINTER(ctypes.c_size_t)], S),
         "echo_sparse_mla_decode": ([ctypes.POINTER(c_mla_args), _P], S),
         "echo_decode_step": ([ctypes.POINTER(c_step_args), _P], S),
+        "echo_decode_step_host": ([ctypes.POINTER(c_step_args), _P, _P, _P, _I32], S),
+        "echo_step_graph_create": ([ctypes.POINTER(c_step_args), ctypes.POINTER(_P)], S),
+        "echo_step_graph_launch": ([_P, _P, _P, _P, _I32], S),
+        "echo_step_graph_destroy": ([_P], S),
         "echo_pool_validate": ([ctypes.POINTER(c_pool), ctypes.POINTER(c_stage), _P, _P, _P], S),
         "echo_pool_validate_host": ([ctypes.POINTER(c_pool), _P, _I32, _P], S),
         "echo_last_error_string": ([], ctypes.c_char_p),
@@ -151,9 +155,22 @@ def _dev(t: torch.Tensor | None, name: str):
     return _ptr(t)
 
 
+def _current_stream_handle():
+    return torch.cuda.current_stream().cuda_stream
+
+
+try:  # the raw handle of the current stream without building a Stream object
+    _raw_stream, _cur_device = torch._C._cuda_getCurrentRawStream, torch._C._cuda_getDevice
+
+    def _current_stream_handle():  # noqa: F811
+        return _raw_stream(_cur_device())
+except AttributeError:
+    pass
+
+
 def _stream(stream):
     if stream is None:
-        return torch.cuda.current_stream().cuda_stream
+        return _current_stream_handle()
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
@@ -474,7 +491,49 @@ def echo_pool_validate_host(free, prio, to_host, host_to_gpu, n_free: int, reser
 
 
 def echo_decode_step(args: c_step_args, stream=None):
-    _check(load_library().echo_decode_step(ctypes.byref(args), _stream(stream)), "echo_decode_step")
+    _check((_lib or load_library()).echo_decode_step(ctypes.byref(args), _stream(stream)), "echo_decode_step")
+
+
+def _host_inputs(q_host, w_host):
+    for t, name in ((q_host, "q_host"), (w_host, "w_host")):
+        if t.is_cuda or not t.is_contiguous():
+            raise EchoError(f"{name} must be a contiguous host tensor")
+    return q_host.data_ptr(), w_host.data_ptr()
+
+
+def echo_decode_step_host(args: c_step_args, q_host, w_host, stream=None, wait: bool = True):
+    """One decode step whose q and w come from host tensors (pinned for an asynchronous
+    copy) laid out as the step's device q and w; wait: return after the step is done."""
+    qp, wp = _host_inputs(q_host, w_host)
+    _check((_lib or load_library()).echo_decode_step_host(ctypes.byref(args), qp, wp, _stream(stream),
+                                                          1 if wait else 0), "echo_decode_step_host")
+
+
+class StepGraph:
+    """A decode step captured into a CUDA graph by the library (echo_step_graph_*).
+    The step's arguments (and every buffer they name) are kept alive with it."""
+
+    def __init__(self, args: c_step_args):
+        h = _P()
+        _check(load_library().echo_step_graph_create(ctypes.byref(args), ctypes.byref(h)), "echo_step_graph_create")
+        self._h, self._args = h, args
+
+    def launch(self, q_host=None, w_host=None, stream=None, wait: bool = True):
+        qp, wp = _host_inputs(q_host, w_host) if q_host is not None else (None, None)
+        _check(_lib.echo_step_graph_launch(self._h, qp, wp, _stream(stream), 1 if wait else 0),
+               "echo_step_graph_launch")
+
+    def close(self):
+        if self._h:
+            _check(_lib.echo_step_graph_destroy(self._h), "echo_step_graph_destroy")
+            self._h = _P()
+
+    def __del__(self):
+        try:
+            if self._h and _lib is not None:
+                _lib.echo_step_graph_destroy(self._h)
+        except Exception:
+            pass
 
 
 def version() -> int:

@@ -6,6 +6,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <new>
 
 #include "cache_common.cuh"
 
@@ -404,17 +405,15 @@ int echo_prefill_indexer_score(const echo_prefill_args *a, void *stream) {
   return launch_prefill_indexer(a, static_cast<cudaStream_t>(stream));
 }
 
-int echo_decode_step(const echo_step_args *a, void *stream) {
-  g_err[0] = 0;
+// the decode step's argument checks (everything, before anything is enqueued)
+static int step_check(const echo_step_args *a) {
   REQUIRE(a, "args is NULL");
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   REQUIRE(a->pool && a->ws, "step needs pool and workspace");
   REQUIRE(a->q && a->w && a->k_index && a->ctx_len && a->req_to_host && a->scores && a->sel && a->kth &&
               a->out_slot,
           "step pointer is NULL");
   REQUIRE(a->clock >= 0 || a->clock_dev, "clock must be >= 0");
   const bool prefetch = a->s_hat && a->stage;
-  // everything is checked before the first launch, so a rejected step enqueues nothing
   TRY(check_pool(a->pool));
   TRY(check_latent_rows(a->pool, "the decode step"));
   REQUIRE(a->B >= 0 && a->L_max >= 0, "negative size");
@@ -431,6 +430,13 @@ int echo_decode_step(const echo_step_args *a, void *stream) {
     REQUIRE(a->new_k_index, "new_kv given without new_k_index");
     REQUIRE(aligned(a->new_kv, 16) && aligned(a->new_k_index, 16), "append buffers must be 16-byte aligned");
   }
+  return ECHO_OK;
+}
+
+// the decode step's launches (arguments already checked)
+static int step_enqueue(const echo_step_args *a, cudaStream_t s) {
+  void *stream = s;
+  const bool prefetch = a->s_hat && a->stage;
   cudaEvent_t *ev = reinterpret_cast<cudaEvent_t *>(a->stage_events);
   auto mark = [&](int i) -> int {
     if (!ev || !ev[i]) return ECHO_OK;
@@ -479,6 +485,128 @@ int echo_decode_step(const echo_step_args *a, void *stream) {
   TRY(mark(ECHO_STAGE_EMA));  // the EMA ran inside the recall: this stage is empty
   TRY(mark(ECHO_NUM_STAGES));
   return ECHO_OK;
+}
+
+int echo_decode_step(const echo_step_args *a, void *stream) {
+  g_err[0] = 0;
+  // everything is checked before the first launch, so a rejected step enqueues nothing
+  TRY(step_check(a));
+  return step_enqueue(a, static_cast<cudaStream_t>(stream));
+}
+
+// The step's inputs from host memory: q (B * n_q * 64 * 128 bytes) into a->q and w
+// (B * n_q * 64 floats) into a->w, in one copy when both sides hold w right after q.
+static int copy_step_inputs(const echo_step_args *a, const void *q_host, const float *w_host, cudaStream_t s) {
+  const size_t qb = static_cast<size_t>(a->B) * a->n_q * 64 * 128;
+  const size_t wb = static_cast<size_t>(a->B) * a->n_q * 64 * sizeof(float);
+  if (qb == 0) return ECHO_OK;
+  const uint8_t *qh = static_cast<const uint8_t *>(q_host);
+  const uint8_t *qd = a->q;
+  cudaError_t e;
+  if (reinterpret_cast<const uint8_t *>(w_host) == qh + qb && reinterpret_cast<const uint8_t *>(a->w) == qd + qb) {
+    e = cudaMemcpyAsync(const_cast<uint8_t *>(qd), qh, qb + wb, cudaMemcpyHostToDevice, s);
+  } else {
+    e = cudaMemcpyAsync(const_cast<uint8_t *>(qd), qh, qb, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(const_cast<float *>(a->w), w_host, wb, cudaMemcpyHostToDevice, s);
+  }
+  return e == cudaSuccess ? ECHO_OK : cuda_fail(e, "input copy");
+}
+
+static int wait_stream(cudaStream_t s) {
+  const cudaError_t e = cudaStreamSynchronize(s);
+  return e == cudaSuccess ? ECHO_OK : cuda_fail(e, "stream synchronisation");
+}
+
+int echo_decode_step_host(const echo_step_args *a, const void *q_host, const float *w_host, void *stream,
+                          int32_t wait) {
+  g_err[0] = 0;
+  REQUIRE(q_host && w_host, "q_host and w_host are required");
+  TRY(step_check(a));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  TRY(copy_step_inputs(a, q_host, w_host, s));
+  TRY(step_enqueue(a, s));
+  return wait ? wait_stream(s) : ECHO_OK;
+}
+
+}  // extern "C"
+
+// A decode step captured once into a CUDA graph by the library (its own capture
+// stream), replayed by echo_step_graph_launch.
+struct echo_step_graph {
+  cudaGraph_t graph;
+  cudaGraphExec_t exec;
+  echo_step_args args;
+};
+
+extern "C" {
+
+int echo_step_graph_create(const echo_step_args *a, echo_step_graph **out) {
+  g_err[0] = 0;
+  REQUIRE(out, "out is NULL");
+  *out = nullptr;
+  REQUIRE(a, "args is NULL");
+  REQUIRE(a->clock_dev, "a step graph needs the device clock (clock_dev) so that each launch is the next step");
+  REQUIRE(!a->stage_events, "a step graph takes no stage events");
+  TRY(step_check(a));
+  cudaStream_t cs = nullptr;
+  cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
+  if (e != cudaSuccess) return cuda_fail(e, "capture stream");
+  // relaxed: the first launches of a process set kernel attributes inside the capture
+  e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed);
+  if (e != cudaSuccess) {
+    cudaStreamDestroy(cs);
+    return cuda_fail(e, "begin capture");
+  }
+  const int rc = step_enqueue(a, cs);
+  cudaGraph_t g = nullptr;
+  e = cudaStreamEndCapture(cs, &g);
+  cudaStreamDestroy(cs);
+  if (rc != ECHO_OK || e != cudaSuccess) {
+    if (g) cudaGraphDestroy(g);
+    cudaGetLastError();
+    return rc != ECHO_OK ? rc : cuda_fail(e, "end capture");
+  }
+  cudaGraphExec_t x = nullptr;
+  e = cudaGraphInstantiate(&x, g, 0);
+  if (e != cudaSuccess) {
+    cudaGraphDestroy(g);
+    return cuda_fail(e, "graph instantiation");
+  }
+  echo_step_graph *h = new (std::nothrow) echo_step_graph;
+  if (!h) {
+    cudaGraphExecDestroy(x);
+    cudaGraphDestroy(g);
+    set_error("out of host memory");
+    return ECHO_EINVAL;
+  }
+  h->graph = g;
+  h->exec = x;
+  h->args = *a;
+  *out = h;
+  return ECHO_OK;
+}
+
+int echo_step_graph_launch(echo_step_graph *h, const void *q_host, const float *w_host, void *stream,
+                           int32_t wait) {
+  g_err[0] = 0;
+  REQUIRE(h, "graph is NULL");
+  REQUIRE((q_host == nullptr) == (w_host == nullptr), "give both q_host and w_host, or neither");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (q_host) TRY(copy_step_inputs(&h->args, q_host, w_host, s));
+  const cudaError_t e = cudaGraphLaunch(h->exec, s);
+  if (e != cudaSuccess) return cuda_fail(e, "graph launch");
+  return wait ? wait_stream(s) : ECHO_OK;
+}
+
+int echo_step_graph_destroy(echo_step_graph *h) {
+  g_err[0] = 0;
+  if (!h) return ECHO_OK;
+  const cudaError_t e1 = cudaGraphExecDestroy(h->exec);
+  const cudaError_t e2 = cudaGraphDestroy(h->graph);
+  delete h;
+  if (e1 != cudaSuccess) return cuda_fail(e1, "graph destroy");
+  return e2 == cudaSuccess ? ECHO_OK : cuda_fail(e2, "graph destroy");
 }
 
 }  // extern "C"

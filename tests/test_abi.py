@@ -136,6 +136,24 @@ def test_argument_checks_reject_before_any_launch(lib):
     assert lib.echo_decode_step(None, None) == echo.ECHO_EINVAL
 
 
+def test_host_input_calls_reject_bad_arguments_before_any_cuda_work():
+    """The host-input step and the step graph check their arguments on the host: no
+    args, no host buffers, no device clock, a missing graph; destroying NULL is a no-op."""
+    lib = echo.load_library()
+    buf = (ctypes.c_uint8 * 64)()
+    assert lib.echo_decode_step_host(None, buf, buf, None, 1) == echo.ECHO_EINVAL
+    a = echo.c_step_args()
+    assert lib.echo_decode_step_host(ctypes.byref(a), None, buf, None, 1) == echo.ECHO_EINVAL
+    assert b"q_host" in lib.echo_last_error_string()
+    h = ctypes.c_void_p(1234)
+    assert lib.echo_step_graph_create(None, ctypes.byref(h)) == echo.ECHO_EINVAL and h.value is None
+    assert lib.echo_step_graph_create(ctypes.byref(a), None) == echo.ECHO_EINVAL
+    assert lib.echo_step_graph_create(ctypes.byref(a), ctypes.byref(h)) == echo.ECHO_EINVAL
+    assert b"clock_dev" in lib.echo_last_error_string() and h.value is None
+    assert lib.echo_step_graph_launch(None, None, None, None, 0) == echo.ECHO_EINVAL
+    assert lib.echo_step_graph_destroy(None) == echo.ECHO_OK
+
+
 def test_product_path_fails_loudly_without_the_library(tmp_path):
     code = ("import sparse_attention_kv_fp8_gb300 as e\n"
             "try:\n    e.load_library(%r)\nexcept e.EchoError as x:\n    print('raised', x)\n" % str(tmp_path / "nope.so"))
