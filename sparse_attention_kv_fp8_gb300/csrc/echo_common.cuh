@@ -371,6 +371,12 @@ __device__ __forceinline__ float key_score(uint32_t k) {
   return __uint_as_float(u);
 }
 
+// acc + (wx, wy) * (relu(vx), relu(vy)): two heads of the indexer's weighted ReLU sum in
+// one paired fp32 FMA (each half rounds exactly as fmaf does)
+__device__ __forceinline__ float2 fma_relu2(float wx, float wy, float vx, float vy, float2 acc) {
+  return __ffma2_rn(make_float2(wx, wy), make_float2(fmaxf(vx, 0.f), fmaxf(vy, 0.f)), acc);
+}
+
 __device__ __forceinline__ int query_valid_len(int L, int n_q, int j) {
   int v = L - (n_q - 1 - j);
   return v < 0 ? 0 : v;

@@ -279,20 +279,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
           reg_fence_32(v0);
           reg_fence_32(v1);
           const float4 *w4 = wsm4 + j * (kHeads / 4);
-          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+          float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);  // partial sums (0, 1), (2, 3)
 #pragma unroll
           for (int h4 = 0; h4 < 8; ++h4) {
             const float4 wa = w4[h4], wb = w4[8 + h4];
-            s0 = fmaf(wa.x, fmaxf(v0[4 * h4 + 0], 0.f), s0);
-            s1 = fmaf(wa.y, fmaxf(v0[4 * h4 + 1], 0.f), s1);
-            s2 = fmaf(wa.z, fmaxf(v0[4 * h4 + 2], 0.f), s2);
-            s3 = fmaf(wa.w, fmaxf(v0[4 * h4 + 3], 0.f), s3);
-            s0 = fmaf(wb.x, fmaxf(v1[4 * h4 + 0], 0.f), s0);
-            s1 = fmaf(wb.y, fmaxf(v1[4 * h4 + 1], 0.f), s1);
-            s2 = fmaf(wb.z, fmaxf(v1[4 * h4 + 2], 0.f), s2);
-            s3 = fmaf(wb.w, fmaxf(v1[4 * h4 + 3], 0.f), s3);
+            s01 = fma_relu2(wa.x, wa.y, v0[4 * h4 + 0], v0[4 * h4 + 1], s01);
+            s23 = fma_relu2(wa.z, wa.w, v0[4 * h4 + 2], v0[4 * h4 + 3], s23);
+            s01 = fma_relu2(wb.x, wb.y, v1[4 * h4 + 0], v1[4 * h4 + 1], s01);
+            s23 = fma_relu2(wb.z, wb.w, v1[4 * h4 + 2], v1[4 * h4 + 3], s23);
           }
-          sc[j] = (s0 + s1) + (s2 + s3);
+          sc[j] = (s01.x + s01.y) + (s23.x + s23.y);
         }
         tc_fence_before();
         __syncwarp();
