@@ -11,8 +11,9 @@
 // fetch the tokens above the threshold while the TMA and tensor-core warps already
 // work on the next query block.
 //
-// sm_103a design (one persistent CTA per SM, 18 warps; query blocks of 4 tokens, so
-// one tcgen05.mma of M = 128 keys x N = 256 = 4 queries x 64 heads x K = 32):
+// sm_103a design (one persistent CTA per SM, 16 warps, so 128 registers a thread and
+// no spills; query blocks of 4 tokens, so one tcgen05.mma of M = 128 keys x N = 256 =
+// 4 queries x 64 heads x K = 32):
 //   warp 0      TMA: the block's q (256 x 128 e4m3, two buffers) and its causal
 //               range of 128-token k^I tiles into a 6-stage ring.
 //   warp 1      tensor-core issuer: 4 MMAs per tile into one of two TMEM
@@ -20,7 +21,7 @@
 //   warps 2-9   epilogue, two warpgroups on alternate tiles: ReLU, weight and head
 //               sum per (token, query) in fp32, causal mask, score store, and the
 //               block's histograms of shifted scores (shared memory, two buffers).
-//   warps 10-17 prefetch: per finished block, the threshold bin of each query, then
+//   warps 10-15 prefetch: per finished block, the threshold bin of each query, then
 //               a scan of the block's scores (just written, in L2) for the tokens
 //               above it, residency test, tickets and host-row copies
 //               (prefetch_rows.cuh), while the next block is being scored.
@@ -37,7 +38,7 @@ constexpr int kPStages = 6;
 constexpr int kPAcc = 2;                       // TMEM accumulators of kPN columns
 constexpr int kPEpiGroups = 2;
 constexpr int kPEpiWarps = 4 * kPEpiGroups;
-constexpr int kPPfWarps = 8;
+constexpr int kPPfWarps = 6;                  // 16 warps in all: 128 registers a thread
 constexpr int kPThreads = 32 * (2 + kPEpiWarps + kPPfWarps);
 constexpr uint32_t kPQBytes = kPN * kDim;      // 32 KB
 constexpr int kBins = 256;
