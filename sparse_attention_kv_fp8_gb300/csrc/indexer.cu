@@ -7,7 +7,7 @@
 // compare scores with the predicted k-th score and load rows from host memory),
 // one SM per query vector and a slice of the K cache.
 //
-// sm_103a design (one persistent CTA per SM, 18 warps):
+// sm_103a design (one persistent CTA per SM, 14 warps, up to 128 registers a thread):
 //   warp 0      TMA producer: 128-token K tiles (16 KB, 128B-swizzled) into a
 //               10-stage shared-memory ring; the request's q (64*n_q x 128 e4m3)
 //               into one of two q buffers; the tiles' host rows (req_to_host).
@@ -18,7 +18,8 @@
 //               row per thread, ReLU, weight, sum over heads in fp32, store the
 //               score; threshold test against the predicted k-th score;
 //               candidates go to a per-warp queue.
-//   warps 10-17 prefetch: residency test and tickets for the queued tokens, then
+//   warps 10-13 prefetch, each serving two epilogue warps' queues: residency
+//               test and tickets for the queued tokens, then
 //               copy their host rows (1152 B, 16-byte loads of the pinned, mapped
 //               host pool) into the HBM staging area, or straight into the GPU-pool
 //               slots the last recall set aside (direct to slot).
@@ -39,7 +40,7 @@ constexpr int kTileBytes = kTileTokens * kDim;  // 16 KB
 constexpr int kStages = 10;
 constexpr int kEpiGroups = 2;                // epilogue warpgroups, taking tiles in turn
 constexpr int kEpiWarps = 4 * kEpiGroups;
-constexpr int kPfWarps = 8;                  // each serves kEpiWarps / kPfWarps queues
+constexpr int kPfWarps = 4;                  // each serves kEpiWarps / kPfWarps queues
 constexpr int kIndexerThreads = 32 * (2 + kEpiWarps + kPfWarps);
 constexpr int kAcc = 4;            // TMEM accumulators (MMA runs up to 3 tiles ahead of the epilogue)
 constexpr int kQueueCap = 64;      // entries per epilogue -> prefetch queue
