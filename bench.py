@@ -726,6 +726,8 @@ def prefetch_mode_leg(echo, torch, st, host_t, q_ring, w, k_index, ctx, r2h_t, f
     return {"mode": "direct to slot" if reserve > 0 else ("no prefetch" if reserve == 0 else "staging"),
             "reserve_slots": max(reserve, 0),
             "value": 1e3 / per, "unit": "steps/s", "ms_per_step": per,
+            "step_us": {"p10": float(np.percentile(ms, 10)) * 1e3, "p50": float(np.median(ms)) * 1e3,
+                        "p90": float(np.percentile(ms, 90)) * 1e3, "max": float(np.max(ms)) * 1e3},
             "hit_rate": sv["hits"] / max(1, sv["unique_rows"]),
             "recalled_rows_per_step": sv["recalled"] / n_timed,
             "prefetched_rows_per_step": sv["staged"] / n_timed,
@@ -860,7 +862,8 @@ def decode_config_leg(echo, torch, flush_l2, host_big, B_, L_, overlap, mode, n_
     rec_gbs = rec_rows * 1152 / (stage_ms["recall"] * 1e-3) / 1e9
     res = {"B": B_, "L": L_, "overlap": overlap, "rho": rho, "mode": mode, "steps": n_timed,
            "value": 1e3 / float(np.mean(ms)), "unit": "steps/s", "ms_per_step": float(np.mean(ms)),
-           "step_us_p50": float(np.median(ms)) * 1e3, "scored_tokens_per_s": B_ * L_ * 1e3 / float(np.mean(ms)),
+           "step_us_p50": float(np.median(ms)) * 1e3, "step_us_p90": float(np.percentile(ms, 90)) * 1e3,
+           "step_us_max": float(np.max(ms)) * 1e3, "scored_tokens_per_s": B_ * L_ * 1e3 / float(np.mean(ms)),
            "hit_rate": sv["hits"] / max(1, sv["unique_rows"]), "recalled_rows_per_step": rec_rows,
            "prefetched_rows_per_step": sv["staged"] / n_timed, "stage_ms": stage_ms,
            "indexer": {"bytes": idx_bytes, "gbs": idx_bytes / (stage_ms["indexer"] * 1e-3) / 1e9,
