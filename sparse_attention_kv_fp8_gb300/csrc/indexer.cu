@@ -25,8 +25,10 @@
 //               slots the last recall set aside (direct to slot).
 // The kernel is HBM-bound: 128 + 4*n_q bytes per token against 2*64*128*n_q
 // FLOP, far below the FP8 ridge point.
+#include <atomic>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "cache_common.cuh"
 #include "prefetch_rows.cuh"
@@ -538,16 +540,76 @@ typedef CUresult (*PFN_encodeTiled)(CUtensorMap *, CUtensorMapDataType, cuuint32
                                     CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 static PFN_encodeTiled encode_fn() {
-  static PFN_encodeTiled fn = nullptr;
-  if (!fn) {
+  static std::atomic<PFN_encodeTiled> fn{nullptr};
+  PFN_encodeTiled f = fn.load(std::memory_order_acquire);
+  if (!f) {
     void *p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_encodeTiled>(p);
+        q == cudaDriverEntryPointSuccess) {
+      f = reinterpret_cast<PFN_encodeTiled>(p);
+      fn.store(f, std::memory_order_release);
+    }
   }
-  return fn;
+  return f;
+}
+
+// Tensor maps of recent launches.  A map depends only on its parameters (device, data
+// type, base pointer, extents, strides, box, swizzle, L2 promotion), so a launch over the
+// same buffers and shape reuses the encoding instead of encoding again on the host.
+struct TmapKey {
+  int dev;
+  CUtensorMapDataType dt;
+  cuuint32_t rank;
+  const void *ptr;
+  cuuint64_t dims[3], strides[2];
+  cuuint32_t box[3];
+  CUtensorMapSwizzle sw;
+  CUtensorMapL2promotion l2;
+};
+constexpr int kTmapCache = 16;
+
+static CUresult encode_cached(PFN_encodeTiled enc, CUtensorMap *out, CUtensorMapDataType dt, cuuint32_t rank,
+                              const void *ptr, const cuuint64_t *dims, const cuuint64_t *strides,
+                              const cuuint32_t *box, CUtensorMapSwizzle sw, CUtensorMapL2promotion l2) {
+  TmapKey k;
+  memset(&k, 0, sizeof(k));  // padding too: keys compare bytewise
+  cudaGetDevice(&k.dev);
+  k.dt = dt;
+  k.rank = rank;
+  k.ptr = ptr;
+  for (cuuint32_t i = 0; i < rank; ++i) {
+    k.dims[i] = dims[i];
+    k.box[i] = box[i];
+    if (i + 1 < rank) k.strides[i] = strides[i];
+  }
+  k.sw = sw;
+  k.l2 = l2;
+  static std::mutex mu;
+  static TmapKey keys[kTmapCache];
+  static CUtensorMap maps[kTmapCache];
+  static bool used[kTmapCache];
+  static int next = 0;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < kTmapCache; ++i)
+      if (used[i] && memcmp(&keys[i], &k, sizeof(k)) == 0) {
+        *out = maps[i];
+        return CUDA_SUCCESS;
+      }
+  }
+  const cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = enc(out, dt, rank, const_cast<void *>(ptr), dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, sw, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r == CUDA_SUCCESS) {
+    std::lock_guard<std::mutex> lk(mu);
+    keys[next] = k;
+    maps[next] = *out;
+    used[next] = true;
+    next = (next + 1) % kTmapCache;
+  }
+  return r;
 }
 
 // SM count of the current device (queried once per device, so that launches
@@ -585,10 +647,8 @@ int launch_indexer(const echo_indexer_args *a, cudaStream_t stream, uint32_t *se
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(echo::kDim),
                              static_cast<cuuint64_t>(a->L_max) * echo::kDim};
     cuuint32_t box[3] = {static_cast<cuuint32_t>(echo::kDim), static_cast<cuuint32_t>(echo::kTileTokens), 1};
-    cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = enc(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(a->k_index), dims, strides,
-                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = encode_cached(enc, &tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a->k_index, dims, strides, box,
+                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     if (r != CUDA_SUCCESS) {
       set_error("tensor map for k_index failed (CUresult %d)", static_cast<int>(r));
       return ECHO_ECUDA;
@@ -599,10 +659,8 @@ int launch_indexer(const echo_indexer_args *a, cudaStream_t stream, uint32_t *se
                           static_cast<cuuint64_t>(a->B) * nq * echo::kHeads};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(echo::kDim)};
     cuuint32_t box[2] = {static_cast<cuuint32_t>(echo::kDim), static_cast<cuuint32_t>(nq * echo::kHeads)};
-    cuuint32_t es[2] = {1, 1};
-    CUresult r = enc(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(a->q), dims, strides, box, es,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = encode_cached(enc, &tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a->q, dims, strides, box,
+                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     if (r != CUDA_SUCCESS) {
       set_error("tensor map for q failed (CUresult %d)", static_cast<int>(r));
       return ECHO_ECUDA;
@@ -616,10 +674,8 @@ int launch_indexer(const echo_indexer_args *a, cudaStream_t stream, uint32_t *se
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(a->L_max), static_cast<cuuint64_t>(a->B)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(a->L_max) * 4};
     cuuint32_t box[2] = {static_cast<cuuint32_t>(echo::kTileTokens), 1};
-    cuuint32_t es[2] = {1, 1};
-    r2h_tma = enc(&tr, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<int32_t *>(a->req_to_host), dims, strides, box,
-                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    r2h_tma = encode_cached(enc, &tr, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, a->req_to_host, dims, strides, box,
+                            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE) == CUDA_SUCCESS;
   }
   echo::IndexerParams P{};
   P.r2h_tma = r2h_tma ? 1 : 0;
