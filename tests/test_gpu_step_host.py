@@ -117,3 +117,46 @@ def test_library_step_graph_matches_eager_steps():
         assert_same_layer(ref, cr, got, cg, step)
     g.close()
     g.close()   # a second close is a no-op
+
+
+def test_host_input_step_two_query_tokens_without_prefetch():
+    """The MTP form (two query tokens per request, each with its own top-k, one recall of
+    the union) through echo_decode_step_host with separate q and w host buffers (two
+    copies), prefetch off, no append: bit-identical to echo_decode_step."""
+    b, nq, l, ctx, k = 4, 2, 6000, 5990, 256
+    cr = Case(b, nq, l, ctx, 4000, 3500, clock=700, seed=83, k=k)
+    cg = Case(b, nq, l, ctx, 4000, 3500, clock=700, seed=83, k=k)
+    outs = []
+    for c, host in ((cr, False), (cg, True)):
+        out = echo.StepBuffers(b, nq, l, k)
+        clock = torch.tensor([c.clock], dtype=torch.int32, device="cuda")
+        q_dev = torch.empty((b, nq, 64, 128), dtype=torch.uint8, device="cuda")
+        w_dev = torch.empty((b, nq, 64), dtype=torch.float32, device="cuda")
+        q_host = torch.empty((b, nq, 64, 128), dtype=torch.uint8, pin_memory=True)
+        w_host = torch.empty((b, nq, 64), dtype=torch.float32, pin_memory=True)
+        args = echo.make_step_args(c.pool, c.ws, q_dev, w_dev, c.k_index, c.ctx, c.r2h_t, k, out,
+                                   clock_dev=clock, advance_clock=True)
+        qf = c.inp.q_float
+        for step in range(3):
+            qf, q, _, _ = step_inputs(c, step, qf)
+            if host:
+                q_host.numpy()[...] = q
+                w_host.copy_(c.w.cpu())
+                echo.echo_decode_step_host(args, q_host, w_host, wait=True)
+            else:
+                q_dev.copy_(torch.from_numpy(q).cuda())
+                w_dev.copy_(c.w)
+                echo.echo_decode_step(args)
+                torch.cuda.synchronize()
+            res = {n: getattr(out, n).cpu().numpy().copy() for n in ("scores", "sel", "kth", "out_slot")}
+            outs.append((host, step, res, int(clock.item()), int(out.dev_status.item())))
+    ref = [o for o in outs if not o[0]]
+    got = [o for o in outs if o[0]]
+    for (_, step, a, ca, sa), (_, _, g, cg_, sg) in zip(ref, got):
+        for n in a:
+            assert np.array_equal(a[n], g[n], equal_nan=(n == "scores")), (step, n)
+        assert ca == cg_ and sa == sg, step
+    ma, mb = cr.gpu_meta(), cg.gpu_meta()
+    for key in ma:
+        assert np.array_equal(ma[key], mb[key]), key
+    assert torch.equal(cr.pool.gpu_kv, cg.pool.gpu_kv)
