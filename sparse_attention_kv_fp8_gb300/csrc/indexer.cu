@@ -7,22 +7,23 @@
 // compare scores with the predicted k-th score and load rows from host memory),
 // one SM per query vector and a slice of the K cache.
 //
-// sm_103a design (one persistent CTA per SM, 14 warps, up to 128 registers a thread):
+// sm_103a design (one persistent CTA per SM, 14 warps for one query token, 16 for two;
+// up to 128 registers a thread):
 //   warp 0      TMA producer: 128-token K tiles (16 KB, 128B-swizzled) into a
 //               10-stage shared-memory ring; the request's q (64*n_q x 128 e4m3)
 //               into one of two q buffers; the tiles' host rows (req_to_host).
 //   warp 1      tensor-core issuer: per tile, 4 x tcgen05.mma kind::f8f6f4
 //               (M = 128 tokens, N = 64*n_q heads, K = 32) into one of four TMEM
 //               accumulators, so the MMA runs ahead of the epilogue.
-//   warps 2-9   epilogue, two warpgroups taking tiles in turn: tcgen05.ld one token
-//               row per thread, ReLU, weight, sum over heads in fp32, store the
-//               score; threshold test against the predicted k-th score;
-//               candidates go to a per-warp queue.
-//   warps 10-13 prefetch, each serving two epilogue warps' queues: residency
-//               test and tickets for the queued tokens, then
-//               copy their host rows (1152 B, 16-byte loads of the pinned, mapped
-//               host pool) into the HBM staging area, or straight into the GPU-pool
-//               slots the last recall set aside (direct to slot).
+//   warps 2-9   epilogue (2-13 for two query tokens), two (three) warpgroups taking
+//               tiles in turn: tcgen05.ld one token row per thread, ReLU, weight, sum
+//               over heads in fp32, store the score; threshold test against the
+//               predicted k-th score; candidates go to a per-warp queue.
+//   warps 10-13 prefetch (14-15 for two query tokens), each serving two (six)
+//               epilogue warps' queues: residency test and tickets for the queued
+//               tokens, then copy their host rows (1152 B, 16-byte loads of the
+//               pinned, mapped host pool) into the HBM staging area, or straight into
+//               the GPU-pool slots the last recall set aside (direct to slot).
 // The kernel is HBM-bound: 128 + 4*n_q bytes per token against 2*64*128*n_q
 // FLOP, far below the FP8 ridge point.
 #include <atomic>
@@ -40,10 +41,20 @@ namespace echo {
 constexpr int kTileTokens = 128;
 constexpr int kTileBytes = kTileTokens * kDim;  // 16 KB
 constexpr int kStages = 10;
-constexpr int kEpiGroups = 2;                // epilogue warpgroups, taking tiles in turn
-constexpr int kEpiWarps = 4 * kEpiGroups;
-constexpr int kPfWarps = 4;                  // each serves kEpiWarps / kPfWarps queues
-constexpr int kIndexerThreads = 32 * (2 + kEpiWarps + kPfWarps);
+// Warp roles per query count: epilogue warpgroups taking tiles in turn, and prefetch
+// warps each serving kEpiWarps / kPfWarps queues.  Two query tokens double the epilogue's
+// TMEM reads and sums per tile, so that kernel has a third epilogue warpgroup (the four
+// TMEM accumulators cover three groups and the MMA) and two prefetch warps: 16 warps,
+// 128 registers a thread.
+template <int NQ>
+struct Roles {
+  static constexpr int kEpiGroups = NQ == 1 ? 2 : 3;
+  static constexpr int kEpiWarps = 4 * kEpiGroups;
+  static constexpr int kPfWarps = NQ == 1 ? 4 : 2;
+  static constexpr int kThreads = 32 * (2 + kEpiWarps + kPfWarps);
+  static_assert(kEpiWarps % kPfWarps == 0, "whole queues per prefetch warp");
+};
+
 constexpr int kAcc = 4;            // TMEM accumulators (MMA runs up to 3 tiles ahead of the epilogue)
 constexpr int kQueueCap = 64;      // entries per epilogue -> prefetch queue
 // prefetching while scoring: each epilogue warpgroup of a CTA with at least
@@ -91,6 +102,7 @@ struct IndexerParams {
   const int4 *sel_hint;
 };
 
+template <int EW>  // epilogue warps
 struct alignas(16) IndexerCtl {
   uint64_t full[kStages];
   uint64_t empty[kStages];
@@ -103,13 +115,13 @@ struct alignas(16) IndexerCtl {
   uint32_t tmem_base;
   int abort;
   int first_b, first_t, n_tiles;
-  int queue_tail[kEpiWarps];
-  int queue_head[kEpiWarps];
-  int queue_done[kEpiWarps];
-  int queue[kEpiWarps][kQueueCap];    // token ids b * L_max + p that passed the threshold
-  int queue_h[kEpiWarps][kQueueCap];  // their host rows (when the tiles' host rows are staged)
-  float4 wsm[kEpiWarps][2 * kHeads / 4];  // head weights of the current request, per epilogue warp
-  uint32_t hwin[kEpiWarps][2][2];         // the current request's histogram windows {low key, shift}
+  int queue_tail[EW];
+  int queue_head[EW];
+  int queue_done[EW];
+  int queue[EW][kQueueCap];    // token ids b * L_max + p that passed the threshold
+  int queue_h[EW][kQueueCap];  // their host rows (when the tiles' host rows are staged)
+  float4 wsm[EW][2 * kHeads / 4];  // head weights of the current request, per epilogue warp
+  uint32_t hwin[EW][2][2];         // the current request's histogram windows {low key, shift}
 };
 
 __device__ __forceinline__ int tiles_of(int L) { return (L + kTileTokens - 1) / kTileTokens; }
@@ -131,10 +143,12 @@ __device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
 }
 
 template <int NQ>
-__global__ void __launch_bounds__(kIndexerThreads, 1)
+__global__ void __launch_bounds__(Roles<NQ>::kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
                    const __grid_constant__ CUtensorMap tmap_r, const IndexerParams P) {
   constexpr int N = kHeads * NQ;               // MMA N: all heads of all queries
+  constexpr int kEpiGroups = Roles<NQ>::kEpiGroups, kEpiWarps = Roles<NQ>::kEpiWarps;
+  constexpr int kPfWarps = Roles<NQ>::kPfWarps;
   constexpr uint32_t kQBytes = N * kDim;       // q of one request
   constexpr uint32_t kTmemCols = kAcc * N;     // 256 (NQ = 1) or 512 (NQ = 2) columns
   constexpr uint32_t kIdesc = idesc_e4m3_f32(kTileTokens, N);
@@ -144,7 +158,8 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
   uint8_t *k_smem = smem;                                  // kStages x 16 KB
   uint8_t *q_smem = smem + kStages * kTileBytes;           // 2 x kQBytes
   int32_t *r_smem = reinterpret_cast<int32_t *>(q_smem + 2 * kQBytes);  // kR x 128 host rows
-  IndexerCtl *ctl = reinterpret_cast<IndexerCtl *>(q_smem + 2 * kQBytes + kR * kRowMapBytes);
+  using Ctl = IndexerCtl<Roles<NQ>::kEpiWarps>;
+  Ctl *ctl = reinterpret_cast<Ctl *>(q_smem + 2 * kQBytes + kR * kRowMapBytes);
   volatile int *abort = &ctl->abort;
 
   const int warp = threadIdx.x >> 5;
@@ -306,7 +321,7 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
     }
   } else if (warp < 2 + kEpiWarps) {
     // ===================== epilogue =====================
-    // group g takes tiles g, g + kEpiGroups, ... so two warps per SM sub-partition
+    // group g takes tiles g, g + kEpiGroups, ... so two or three warps per SM sub-partition
     // hide each other's TMEM-load and FMA latency
     const int e = warp - 2;
     const int grp = e / 4;
@@ -532,7 +547,6 @@ __global__ void __launch_bounds__(kIndexerThreads, 1)
 // ---------------------------------------------------------------------------
 namespace echo_host {
 
-using echo::IndexerCtl;
 
 typedef CUresult (*PFN_encodeTiled)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                     const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -630,7 +644,8 @@ int sm_count() {
 
 static size_t indexer_smem_bytes(int nq) {
   return 1024 + echo::kStages * echo::kTileBytes + 2 * (echo::kHeads * nq * echo::kDim) +
-         echo::kR * echo::kRowMapBytes + sizeof(IndexerCtl);
+         echo::kR * echo::kRowMapBytes +
+         (nq == 1 ? sizeof(echo::IndexerCtl<echo::Roles<1>::kEpiWarps>) : sizeof(echo::IndexerCtl<echo::Roles<2>::kEpiWarps>));
 }
 
 int launch_indexer(const echo_indexer_args *a, cudaStream_t stream, uint32_t *sel_hist, const int4 *sel_hint) {
@@ -718,12 +733,12 @@ int launch_indexer(const echo_indexer_args *a, cudaStream_t stream, uint32_t *se
     static std::atomic<bool> attr1[kMaxDevices];
     if (int r = smem_limit_once(attr1, echo::indexer_kernel<1>, static_cast<int>(smem), "indexer smem attribute"))
       return r;
-    echo::indexer_kernel<1><<<grid, echo::kIndexerThreads, smem, stream>>>(tk, tq, tr, P);
+    echo::indexer_kernel<1><<<grid, echo::Roles<1>::kThreads, smem, stream>>>(tk, tq, tr, P);
   } else {
     static std::atomic<bool> attr2[kMaxDevices];
     if (int r = smem_limit_once(attr2, echo::indexer_kernel<2>, static_cast<int>(smem), "indexer smem attribute"))
       return r;
-    echo::indexer_kernel<2><<<grid, echo::kIndexerThreads, smem, stream>>>(tk, tq, tr, P);
+    echo::indexer_kernel<2><<<grid, echo::Roles<2>::kThreads, smem, stream>>>(tk, tq, tr, P);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "indexer launch");
