@@ -4,8 +4,9 @@
 // radix select over the score bits as the selection machinery).
 //
 // sm_103a design: one thread-block cluster of kTopkCluster CTAs per (request,
-// query) row.  Each CTA keeps its slice of the row in shared memory as
-// order-preserving uint32 keys (one global read).  The keys are reduced to
+// query) row (4 or 2 when that many rows would not fit one wave of the GPU).  Each
+// CTA keeps its slice of the row in shared memory as order-preserving uint32 keys (one
+// global read).  The keys are reduced to
 // key - min (cluster min / max), and a 12-bit digit of the reduced key (the top
 // bits in which the row's keys differ) is histogrammed per CTA.  The cluster finds
 // the digit d holding the target-th largest key in two small gathers over
@@ -587,19 +588,31 @@ __global__ void __launch_bounds__(kSelThreads, 1)
 
 namespace echo_host {
 
+int sm_count();
+
 static int launch_topk_impl(const float *scores, const int32_t *ctx_len, int B, int n_q, int L_max, int k,
                             int32_t *sel, float *kth, const echo::ClaimArgs &ca, int do_claim, cudaStream_t stream,
                             bool pdl) {
   const int rows = B * n_q;
   if (rows == 0) return ECHO_OK;
-  const int C = echo::kTopkCluster;
+  const size_t fixed = sizeof(echo::SelSmem) + sizeof(echo::TopkExtra);
+  // CTAs per row: kTopkCluster when every row's cluster fits one wave of the GPU (one
+  // CTA per SM), else fewer and larger CTAs per row (halving while the slice still fits
+  // shared memory), so that many rows take fewer waves
+  int C = echo::kTopkCluster;
+  const int sms = sm_count();
+  while (C > 2 && rows * C > sms) {
+    const int c2 = C / 2;
+    const int ch = (((L_max + c2 - 1) / c2) + 3) & ~3;
+    if (ch > echo::kMaxChunk || fixed + static_cast<size_t>(ch) * sizeof(uint32_t) > echo::kTopkSmemMax) break;
+    C = c2;
+  }
   int chunk = (L_max + C - 1) / C;
   chunk = (chunk + 3) & ~3;
   if (chunk > echo::kMaxChunk) {
     set_error("top-k: L_max %d exceeds the supported %d", L_max, C * echo::kMaxChunk);
     return ECHO_ENOTSUP;
   }
-  const size_t fixed = sizeof(echo::SelSmem) + sizeof(echo::TopkExtra);
   size_t smem = fixed + static_cast<size_t>(chunk > 0 ? chunk : 4) * sizeof(uint32_t);
   if (smem > static_cast<size_t>(echo::kTopkSmemMax)) {
     set_error("top-k: L_max %d needs more shared memory than a CTA has", L_max);
