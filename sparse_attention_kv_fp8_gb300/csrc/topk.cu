@@ -4,7 +4,7 @@
 // radix select over the score bits as the selection machinery).
 //
 // sm_103a design: one thread-block cluster of kTopkCluster CTAs per (request,
-// query) row (4 or 2 when that many rows would not fit one wave of the GPU).  Each
+// query) row (4 or 2 CTAs when the rows are many: see the launcher).  Each
 // CTA keeps its slice of the row in shared memory as order-preserving uint32 keys (one
 // global read).  The keys are reduced to
 // key - min (cluster min / max), and a 12-bit digit of the reduced key (the top
@@ -596,17 +596,18 @@ static int launch_topk_impl(const float *scores, const int32_t *ctx_len, int B, 
   const int rows = B * n_q;
   if (rows == 0) return ECHO_OK;
   const size_t fixed = sizeof(echo::SelSmem) + sizeof(echo::TopkExtra);
-  // CTAs per row: kTopkCluster when every row's cluster fits one wave of the GPU (one
-  // CTA per SM), else fewer and larger CTAs per row (halving while the slice still fits
-  // shared memory), so that many rows take fewer waves
-  int C = echo::kTopkCluster;
+  // CTAs per row (one CTA per SM): kTopkCluster while the rows' clusters take at most
+  // half the SMs; else 4 (many 8-CTA clusters wait longer for 8 free SMs of one GPC as the
+  // kernel before drains); else 2 when only that fits one wave.  A slice that would not
+  // fit shared memory keeps the larger cluster.
   const int sms = sm_count();
-  while (C > 2 && rows * C > sms) {
-    const int c2 = C / 2;
-    const int ch = (((L_max + c2 - 1) / c2) + 3) & ~3;
-    if (ch > echo::kMaxChunk || fixed + static_cast<size_t>(ch) * sizeof(uint32_t) > echo::kTopkSmemMax) break;
-    C = c2;
-  }
+  auto fits = [&](int c) {
+    const int ch = (((L_max + c - 1) / c) + 3) & ~3;
+    return ch <= echo::kMaxChunk && fixed + static_cast<size_t>(ch) * sizeof(uint32_t) <= echo::kTopkSmemMax;
+  };
+  int C = echo::kTopkCluster;
+  if (rows * C > sms / 2 && fits(4)) C = 4;
+  if (C == 4 && rows * C > sms && fits(2)) C = 2;
   int chunk = (L_max + C - 1) / C;
   chunk = (chunk + 3) & ~3;
   if (chunk > echo::kMaxChunk) {
