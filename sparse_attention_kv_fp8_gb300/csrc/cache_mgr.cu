@@ -295,6 +295,7 @@ constexpr int kSlotWarps = 8;              // P2 roles: slot scan, entries, stag
 constexpr int kEntWarps = 6;
 constexpr int kStageWarps = kCoopWarps - kSlotWarps - kEntWarps;
 constexpr int kRows = 4;                   // KV rows a warp copies at once
+constexpr uint32_t kSpreadMin = 2u * kCoopWarps * kRows;  // misses over which a CTA's copies may be spread
 constexpr int kRowVecs = (kRows * kKvChunks + 31) / 32;  // 16-byte vectors per lane
 
 // Loads of up to kRows KV rows (one warp): row u of the group comes from src[u].
@@ -326,6 +327,89 @@ __device__ __forceinline__ const int4 *row_source(const OpParams &P, int32_t f, 
   if (P.mode == kModeAppend) return reinterpret_cast<const int4 *>(P.new_kv) + static_cast<size_t>(f) * rc;
   if (st >= 0) return reinterpret_cast<const int4 *>(P.stage_rows) + static_cast<size_t>(st) * kKvChunks;
   return reinterpret_cast<const int4 *>(P.pool.host_kv) + static_cast<size_t>(h) * rc;
+}
+
+// The rows of ranks [rbase, rbase + ntk) of the list of slots to take: slot maps,
+// priority, indices-buffer entry and out_slot of each, and its KV bytes; warp w takes
+// groups of kRows ranks from w * kRows on.  The slots come from tcache[t] (this CTA's
+// own, cached at ranking) or the global alloc_slot.  use_first: each warp's first group
+// was read before the ranking (entries, host rows, sources in my_*, latent bytes in
+// buf).  Returns this lane's count of rows copied from the staging area.
+__device__ __forceinline__ unsigned long long take_rows(const OpParams &P, int rbase, int ntk, const int32_t *tcache,
+                                                        bool use_first, int my_t0, int32_t my_f, int32_t my_h,
+                                                        int32_t my_src, int4 (&buf)[kRowVecs], int32_t clock,
+                                                        bool copies, bool latent_rows) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long used = 0;
+  for (int t0 = my_t0; t0 < ntk; t0 += kCoopWarps * kRows) {
+    const int nr = min(kRows, ntk - t0);
+    const bool first = use_first && t0 == my_t0;
+    int32_t f = -1, h = -1, st = -1, s = -1;
+    if (lane < nr) {
+      const int r = rbase + t0 + lane;
+      if (first) {
+        f = my_f;
+        h = my_h;
+        st = my_src;
+      } else {
+        f = P.ws.miss_f[r];
+        h = P.ws.miss_h[r];
+        st = P.ws.miss_src[r];
+      }
+      s = tcache ? tcache[t0 + lane] : __ldcg(P.ws.alloc_slot + r);
+      P.pool.free_[s] = 0;
+      P.pool.prio[s] = clock;
+      P.pool.to_host[s] = h;
+      P.pool.h2g[h] = s;
+      P.pool.idxbuf[r] = s;
+      if (P.mode == kModeAlloc) P.out_slots[f] = s;
+      if (P.mode == kModeRecall) {
+        P.out_slot[f] = s;
+        P.ws.miss_stage[f] = -1;  // staging lookup back to its resting state
+        used += st >= 0;
+      }
+    }
+    if (copies && latent_rows) {
+      int32_t slot[kRows];
+      const int4 *src[kRows];
+#pragma unroll
+      for (int u = 0; u < kRows; ++u) {
+        slot[u] = __shfl_sync(0xffffffffu, s, u);
+        const int32_t fu = __shfl_sync(0xffffffffu, f, u), hu = __shfl_sync(0xffffffffu, h, u),
+                      su = __shfl_sync(0xffffffffu, st, u);
+        src[u] = u < nr ? row_source(P, fu, hu, su) : nullptr;
+      }
+      if (!first) rows_load(src, nr, buf);
+      rows_store(reinterpret_cast<int4 *>(P.pool.gpu_kv), slot, nr, buf);
+    }
+  }
+  // rows of other lengths (block rows): every warp of the CTA copies 4 KB segments of
+  // the rows it takes, so that a few large rows still keep all the warps'
+  // loads in flight
+  if (copies && !latent_rows && ntk > 0) {
+    const int rc = P.pool.row_chunks;
+    const int nseg = (rc + 32 * 8 - 1) / (32 * 8);
+    int4 *kv = reinterpret_cast<int4 *>(P.pool.gpu_kv);
+    for (int it = warp; it < ntk * nseg; it += kCoopWarps) {
+      const int t = it / nseg, c0 = (it % nseg) * (32 * 8);
+      const int r = rbase + t;
+      const int32_t s = tcache ? tcache[t] : __ldcg(P.ws.alloc_slot + r);
+      const int4 *src = row_source(P, P.ws.miss_f[r], P.ws.miss_h[r], P.ws.miss_src[r]);
+      int4 *dst = kv + static_cast<size_t>(s) * rc;
+      int4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = c0 + j * 32 + lane;
+        if (i < rc) v[j] = __ldcs(src + i);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = c0 + j * 32 + lane;
+        if (i < rc) dst[i] = v[j];
+      }
+    }
+  }
+  return used;
 }
 
 __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParams P) {
@@ -806,24 +890,33 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
   // that owns the slot writes everything about it: the evicted row's map, the new
   // row's maps, priority, indices-buffer entry, out_slot and KV bytes =====
   uint32_t pre_lt = 0, pre_eq = 0, pre_fr = 0, free_total = 0;
+  uint32_t r_lt = 0, r_eq = 0, r_fr = 0;  // the counts of CTA r = threadIdx.x (when G <= the CTA's threads)
+  uint32_t n_big = 0;  // CTAs whose candidate slots are more than kSpreadMin: only they can take that many
   {
-    uint32_t a3[3] = {0, 0, 0}, t1 = 0;
+    uint32_t a3[3] = {0, 0, 0}, t1 = 0, big = 0;
     for (int r = threadIdx.x; r < G; r += kCoopThreads) {
       const uint32_t lt = __ldcg(P.ws.cta + r * kCVals + kCLt), eq = __ldcg(P.ws.cta + r * kCVals + kCEq),
                      fr = __ldcg(P.ws.cta + r * kCVals + kCFree);
+      if (r == static_cast<int>(threadIdx.x)) {
+        r_lt = lt;
+        r_eq = eq;
+        r_fr = fr;
+      }
       if (r < c) {
         a3[0] += lt;
         a3[1] += eq;
         a3[2] += fr;
       }
       t1 += fr;
+      big += lt + eq + fr > kSpreadMin;
     }
-    uint32_t v4[4] = {a3[0], a3[1], a3[2], t1}, ex4[4], tot4[4];
-    coop_scan<4>(v4, ex4, tot4, S);
-    pre_lt = tot4[0];
-    pre_eq = tot4[1];
-    pre_fr = tot4[2];
-    free_total = tot4[3];
+    uint32_t v5[5] = {a3[0], a3[1], a3[2], t1, big}, ex5[5], tot5[5];
+    coop_scan<5>(v5, ex5, tot5, S);
+    pre_lt = tot5[0];
+    pre_eq = tot5[1];
+    pre_fr = tot5[2];
+    free_total = tot5[3];
+    n_big = tot5[4];
   }
   const int32_t A = (P.mode == kModeEvict) ? 0 : static_cast<int32_t>(min(M, free_total + static_cast<uint32_t>(E)));
   // the next reserve: the ranks after the misses'
@@ -832,12 +925,19 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
   const uint32_t a_lo = pre_fr + pre_lt + min(pre_eq, needT);
   const uint32_t n_mine = my_fr + my_lt + (min(pre_eq + my_eq, needT) - min(pre_eq, needT));
   const int n_take = static_cast<int>(min(a_lo + n_mine, static_cast<uint32_t>(A)) - min(a_lo, static_cast<uint32_t>(A)));
+  // Where the copies fall: when some CTA may take more than kSpreadMin misses (a pool
+  // with free slots, whose lowest free slots take the misses and sit in a few CTAs'
+  // ranges; or victims bunched in a few ranges), the copies may be spread over the
+  // grid after the ranking.  Otherwise (victims scattered over all CTAs) the slots'
+  // owners copy, and the first rows are loaded before the ranking.
+  const bool may_spread = copies && G <= kCoopThreads && A > static_cast<int32_t>(kSpreadMin) && n_big > 0;
   // each warp's first four misses: entry, host row, source, and the KV rows themselves,
-  // loaded now so that the host reads overlap the ranking below
+  // loaded now so that the host reads overlap the ranking below (not when the copies
+  // may be spread)
   int4 buf[kRowVecs];
   int32_t my_f = -1, my_h = -1, my_src = -1;  // lane u < kRows: rank a_lo + warp * kRows + u
   const int my_t0 = warp * kRows;
-  const int my_nr = n_take > my_t0 ? min(kRows, n_take - my_t0) : 0;
+  const int my_nr = (!may_spread && n_take > my_t0) ? min(kRows, n_take - my_t0) : 0;
   if (lane < my_nr) {
     const int r = static_cast<int>(a_lo) + my_t0 + lane;
     my_f = P.ws.miss_f[r];
@@ -911,75 +1011,40 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
   }
   __syncthreads();  // this CTA's slot table complete
   ECHO_TRACE_MARK(7);
-  // the misses this CTA's slots take: four per warp (the first four already loaded)
   unsigned long long used = 0;
-  for (int t0 = my_t0; t0 < n_take; t0 += kCoopWarps * kRows) {
-    const int nr = min(kRows, n_take - t0);
-    const bool first = t0 == my_t0;
-    int32_t f = -1, h = -1, st = -1, s = -1;
-    if (lane < nr) {
-      const int r = static_cast<int>(a_lo) + t0 + lane;
-      if (first) {
-        f = my_f;
-        h = my_h;
-        st = my_src;
-      } else {
-        f = P.ws.miss_f[r];
-        h = P.ws.miss_h[r];
-        st = P.ws.miss_src[r];
-      }
-      s = take_cache ? take_cache[t0 + lane] : __ldcg(P.ws.alloc_slot + r);
-      P.pool.free_[s] = 0;
-      P.pool.prio[s] = clock;
-      P.pool.to_host[s] = h;
-      P.pool.h2g[h] = s;
-      P.pool.idxbuf[r] = s;
-      if (P.mode == kModeAlloc) P.out_slots[f] = s;
-      if (P.mode == kModeRecall) {
-        P.out_slot[f] = s;
-        P.ws.miss_stage[f] = -1;  // staging lookup back to its resting state
-        used += st >= 0;
-      }
+  if (!may_spread) {
+    // the misses this CTA's slots take: four per warp (the first four already loaded)
+    used = take_rows(P, static_cast<int>(a_lo), n_take, take_cache, true, my_t0, my_f, my_h, my_src, buf, clock,
+                     copies, latent_rows);
+  } else {
+    // Every CTA computes every CTA's share (the same numbers); when the largest is over
+    // kSpreadMin and four times the mean, every CTA copies an even stripe of all ranks
+    // once every CTA has ranked its slots (one more barrier), else the owners copy.
+    uint32_t v3[3] = {r_lt, r_eq, r_fr}, ex3[3], tot3[3];
+    coop_scan<3>(v3, ex3, tot3, S);
+    uint32_t take = 0;
+    if (static_cast<int>(threadIdx.x) < G) {
+      const uint32_t alo = ex3[2] + ex3[0] + min(ex3[1], needT);
+      const uint32_t nm = r_fr + r_lt + (min(ex3[1] + r_eq, needT) - min(ex3[1], needT));
+      take = min(alo + nm, static_cast<uint32_t>(A)) - min(alo, static_cast<uint32_t>(A));
     }
-    if (copies && latent_rows) {
-      int32_t slot[kRows];
-      const int4 *src[kRows];
 #pragma unroll
-      for (int u = 0; u < kRows; ++u) {
-        slot[u] = __shfl_sync(0xffffffffu, s, u);
-        const int32_t fu = __shfl_sync(0xffffffffu, f, u), hu = __shfl_sync(0xffffffffu, h, u),
-                      su = __shfl_sync(0xffffffffu, st, u);
-        src[u] = u < nr ? row_source(P, fu, hu, su) : nullptr;
-      }
-      if (!first) rows_load(src, nr, buf);
-      rows_store(reinterpret_cast<int4 *>(P.pool.gpu_kv), slot, nr, buf);
+    for (int o = 16; o > 0; o >>= 1) take = max(take, __shfl_xor_sync(0xffffffffu, take, o));
+    if (lane == 0) S->ws[0][warp] = take;
+    __syncthreads();
+    uint32_t mx = 0;
+    for (int w = 0; w < kCoopWarps; ++w) mx = max(mx, S->ws[0][w]);
+    __syncthreads();
+    int rbase = static_cast<int>(a_lo), ntk = n_take;
+    const int32_t *tcache = take_cache;
+    if (mx > kSpreadMin && static_cast<unsigned long long>(mx) * G > 4ull * static_cast<uint32_t>(A)) {
+      if (!grid_barrier(glob, P.status, S)) return;
+      const int per = (A + G - 1) / G;
+      rbase = min(A, c * per);
+      ntk = min(A, rbase + per) - rbase;
+      tcache = nullptr;
     }
-  }
-  // rows of other lengths (block rows): every warp of the CTA copies 4 KB segments of
-  // the rows this CTA's slots take, so that a few large rows still keep all the warps'
-  // loads in flight
-  if (copies && !latent_rows && n_take > 0) {
-    const int rc = P.pool.row_chunks;
-    const int nseg = (rc + 32 * 8 - 1) / (32 * 8);
-    int4 *kv = reinterpret_cast<int4 *>(P.pool.gpu_kv);
-    for (int it = warp; it < n_take * nseg; it += kCoopWarps) {
-      const int t = it / nseg, c0 = (it % nseg) * (32 * 8);
-      const int r = static_cast<int>(a_lo) + t;
-      const int32_t s = take_cache ? take_cache[t] : __ldcg(P.ws.alloc_slot + r);
-      const int4 *src = row_source(P, P.ws.miss_f[r], P.ws.miss_h[r], P.ws.miss_src[r]);
-      int4 *dst = kv + static_cast<size_t>(s) * rc;
-      int4 v[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int i = c0 + j * 32 + lane;
-        if (i < rc) v[j] = __ldcs(src + i);
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int i = c0 + j * 32 + lane;
-        if (i < rc) dst[i] = v[j];
-      }
-    }
+    used = take_rows(P, rbase, ntk, tcache, false, my_t0, my_f, my_h, my_src, buf, clock, copies, latent_rows);
   }
   // misses beyond the pool's capacity stay out of it
   for (int r = A + gtid; r < static_cast<int>(M); r += gthreads) {

@@ -96,6 +96,27 @@ def test_prefetching_calls_need_latent_rows():
         echo.echo_prefetch_recall(c.pool, c.ws, sel, c.r2h_t, c.ctx, 1, out, stage=stage)
 
 
+def test_block_recall_into_a_mostly_free_pool_matches_oracle():
+    """40,000 slots, 500 resident: the misses (about 4,000 a step) take the lowest free
+    slots, which sit in a few CTAs' slot ranges, so the recall spreads their copies of
+    2,000-byte rows over the whole grid; results equal the oracle's step after step."""
+    rows, n_blocks, k, R = 8, 2048, 512, 1000
+    c = BlockCase(rows, n_blocks, R, n_g=40000, n_resident=500, clock=40, seed=21, k=k)
+    for t, sc in enumerate(wl.block_scores(rows, n_blocks, 21, 3, 0.7)):
+        sel, _ = oracle.select_topk(sc, c.ctx_np, k)
+        out = torch.empty(sel.shape, dtype=torch.int32, device="cuda")
+        stats, st = echo.Stats(), torch.zeros(1, dtype=torch.int32, device="cuda")
+        echo.echo_prefetch_recall(c.pool, c.ws, dev(sel), c.r2h_t, c.ctx, 40 + t, out, stats=stats, dev_status=st)
+        ost = oracle.Stats()
+        ref, rs = c.orc.prefetch_recall(sel, c.r2h, 40 + t, stats=ost)
+        torch.cuda.synchronize()
+        assert np.array_equal(out.cpu().numpy(), ref), t
+        assert int(st.item()) == rs
+        assert stats.as_dict() == ost.as_dict()
+        c.assert_equal(f"step {t}")
+    assert ost.as_dict()["evicted"] == 0
+
+
 def test_block_recall_at_the_bench_size():
     """The bench's block probe configuration: 4 requests x 8 KV heads, 1024 blocks of
     32 KB each (1 GiB host pool), 8192 slots; a cold recall of 64 blocks per selection

@@ -73,6 +73,8 @@ def recall_and_compare(c: Case, sel: np.ndarray, clock: int, stage_rows=None):
     (4, 1, 3000, 200, 1000, 1000, 2),      # full pool: eviction every step
     (3, 2, 2000, 300, 1500, 1400, 3),      # two query tokens: de-duplicated union
     (2, 1, 5000, 700, 900, 880, 4),        # misses exceed the pool: exhaustion
+    (4, 1, 8192, 1024, 40000, 2000, 5),    # mostly free, over 128 slots per CTA: the misses take
+                                           # the free slots of a few CTAs, copies spread over the grid
 ])
 def test_recall_matches_oracle(B, n_q, L, k, n_g, res, seed):
     c = Case(B, n_q, L, L, n_g, res, clock=100, seed=seed, k=k)
