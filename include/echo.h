@@ -450,7 +450,7 @@ int echo_sparse_mla_decode(const echo_mla_args *args, void *stream);
  * programmatic dependent launches; plus 2 for the append (write-through kernel,
  * cache-manager kernel).  stage_events: optional array of
  * ECHO_NUM_STAGES + 1 cudaEvent_t (timing-enabled) recorded around the stages
- * (as external event nodes under capture).
+ * (as external event nodes under stream capture, plain records otherwise).
  */
 typedef struct echo_step_args {
     const echo_pool *pool;

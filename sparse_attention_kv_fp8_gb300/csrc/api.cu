@@ -438,9 +438,19 @@ static int step_enqueue(const echo_step_args *a, cudaStream_t s) {
   void *stream = s;
   const bool prefetch = a->s_hat && a->stage;
   cudaEvent_t *ev = reinterpret_cast<cudaEvent_t *>(a->stage_events);
+  // under stream capture the records become external event nodes of the graph (so
+  // that they still time each replay); outside capture they are plain records (the
+  // external flag is refused there)
+  unsigned int ev_flags = cudaEventRecordDefault;
+  if (ev) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    const cudaError_t e = cudaStreamIsCapturing(s, &cs);
+    if (e != cudaSuccess) return cuda_fail(e, "stream capture status");
+    if (cs == cudaStreamCaptureStatusActive) ev_flags = cudaEventRecordExternal;
+  }
   auto mark = [&](int i) -> int {
     if (!ev || !ev[i]) return ECHO_OK;
-    cudaError_t e = cudaEventRecordWithFlags(ev[i], s, cudaEventRecordExternal);
+    cudaError_t e = cudaEventRecordWithFlags(ev[i], s, ev_flags);
     return e == cudaSuccess ? ECHO_OK : cuda_fail(e, "stage event");
   };
   TRY(mark(ECHO_STAGE_APPEND));

@@ -242,6 +242,52 @@ def test_graph_replay_equals_eager():
         assert torch.equal(a.s_hat, b.s_hat) and int(a.clock.item()) == int(b.clock.item()) == 301 + step
 
 
+def test_stage_events_eager_and_captured():
+    """Stage events (one record before each stage and one after the last) work on eager
+    launches and inside a captured graph: the steps' outputs, the pool and the clock
+    equal those of steps without events, and every stage's elapsed time is readable."""
+    cases = [Case(2, 1, 3000, 2990, 1000, 1000, clock=300, seed=32, k=256) for _ in range(2)]
+    plain = StepRunner(cases[0], s_hat0=float("inf"), append=False)
+    timed = StepRunner(cases[1], s_hat0=float("inf"), append=False)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(echo.NUM_STAGES + 1)]
+    for e in evs:
+        e.record()
+    c = cases[1]
+    timed.args = echo.make_step_args(c.pool, c.ws, timed.q_buf, c.w, c.k_index, c.ctx, c.r2h_t, c.k, timed.out,
+                                     stage=c.stage, s_hat=timed.s_hat, clock_dev=timed.clock, advance_clock=True,
+                                     stats=timed.stats, events=evs)
+    qf = cases[0].inp.q_float
+    g = None
+    for step in range(5):
+        qf, q, _, _ = step_inputs(cases[0], step, qf)
+        plain.set_inputs(q)
+        plain.run()
+        timed.set_inputs(q)
+        if step < 3:       # eager: plain event records
+            timed.run()
+        else:              # captured once, then replayed: external event nodes
+            if g is None:
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                s = torch.cuda.Stream()
+                s.wait_stream(torch.cuda.current_stream())
+                with torch.cuda.stream(s):
+                    with torch.cuda.graph(g, stream=s):
+                        timed.run()
+                torch.cuda.current_stream().wait_stream(s)
+            g.replay()
+        torch.cuda.synchronize()
+        times = [evs[i].elapsed_time(evs[i + 1]) for i in range(echo.NUM_STAGES)]
+        assert all(t >= 0.0 for t in times) and times[1] > 0.0, (step, times)
+        for name in ("scores", "sel", "kth", "out_slot"):
+            x, y = getattr(plain.out, name).cpu().numpy(), getattr(timed.out, name).cpu().numpy()
+            assert np.array_equal(x, y, equal_nan=(name == "scores")), (step, name)
+        ma, mb = cases[0].gpu_meta(), cases[1].gpu_meta()
+        for key in ma:
+            assert np.array_equal(ma[key], mb[key]), (step, key)
+        assert torch.equal(plain.s_hat, timed.s_hat) and int(plain.clock.item()) == int(timed.clock.item())
+
+
 def test_results_written_straight_into_pinned_host_memory():
     """out_slot and the status word may live in pinned host memory (zero-copy results):
     the same steps give the same slots, selections and pool as device-resident results."""
