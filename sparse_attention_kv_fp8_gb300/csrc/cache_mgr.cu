@@ -412,7 +412,50 @@ __device__ __forceinline__ unsigned long long take_rows(const OpParams &P, int r
   return used;
 }
 
-__global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParams P) {
+// The copies when some CTA may take many misses (a pool with free slots: the lowest
+// free slots take the misses and sit in a few CTAs' ranges).  Every CTA computes every
+// CTA's share from the per-CTA counts (thread r holds CTA r's: r_lt, r_eq, r_fr; the same
+// numbers in every CTA); when the largest is over kSpreadMin and four times the mean,
+// every CTA copies an even stripe of all ranks once every CTA has ranked its slots (one
+// more grid barrier), else the owners copy their own.  Out of line, and the kernel's
+// parameters in the constant bank (__grid_constant__, so that the reference to them
+// needs no local copy): the full-pool path keeps the code it had.  Returns the lane's
+// count of rows copied from the staging area, or ~0 when the grid barrier gave up.
+__device__ __noinline__ unsigned long long spread_takes(const OpParams &P, CoopSmem *S, uint32_t *glob, uint32_t r_lt,
+                                                       uint32_t r_eq, uint32_t r_fr, uint32_t needT, int32_t A,
+                                                       uint32_t a_lo, int n_take, const int32_t *take_cache,
+                                                       int32_t clock, bool copies, bool latent_rows) {
+  const int G = gridDim.x, c = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t v3[3] = {r_lt, r_eq, r_fr}, ex3[3], tot3[3];
+  coop_scan<3>(v3, ex3, tot3, S);
+  uint32_t take = 0;
+  if (static_cast<int>(threadIdx.x) < G) {
+    const uint32_t alo = ex3[2] + ex3[0] + min(ex3[1], needT);
+    const uint32_t nm = r_fr + r_lt + (min(ex3[1] + r_eq, needT) - min(ex3[1], needT));
+    take = min(alo + nm, static_cast<uint32_t>(A)) - min(alo, static_cast<uint32_t>(A));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) take = max(take, __shfl_xor_sync(0xffffffffu, take, o));
+  if (lane == 0) S->ws[0][warp] = take;
+  __syncthreads();
+  uint32_t mx = 0;
+  for (int w = 0; w < kCoopWarps; ++w) mx = max(mx, S->ws[0][w]);
+  __syncthreads();
+  int rbase = static_cast<int>(a_lo), ntk = n_take;
+  const int32_t *tcache = take_cache;
+  if (mx > kSpreadMin && static_cast<unsigned long long>(mx) * G > 4ull * static_cast<uint32_t>(A)) {
+    if (!grid_barrier(glob, P.status, S)) return ~0ull;
+    const int per = (A + G - 1) / G;
+    rbase = min(A, c * per);
+    ntk = min(A, rbase + per) - rbase;
+    tcache = nullptr;
+  }
+  int4 buf[kRowVecs];
+  return take_rows(P, rbase, ntk, tcache, false, warp * kRows, -1, -1, -1, buf, clock, copies, latent_rows);
+}
+
+__global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const __grid_constant__ OpParams P) {
   __shared__ CoopSmem S_;
   CoopSmem *S = &S_;
   extern __shared__ __align__(16) int32_t dyn_smem[];
@@ -1017,34 +1060,9 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const OpParam
     used = take_rows(P, static_cast<int>(a_lo), n_take, take_cache, true, my_t0, my_f, my_h, my_src, buf, clock,
                      copies, latent_rows);
   } else {
-    // Every CTA computes every CTA's share (the same numbers); when the largest is over
-    // kSpreadMin and four times the mean, every CTA copies an even stripe of all ranks
-    // once every CTA has ranked its slots (one more barrier), else the owners copy.
-    uint32_t v3[3] = {r_lt, r_eq, r_fr}, ex3[3], tot3[3];
-    coop_scan<3>(v3, ex3, tot3, S);
-    uint32_t take = 0;
-    if (static_cast<int>(threadIdx.x) < G) {
-      const uint32_t alo = ex3[2] + ex3[0] + min(ex3[1], needT);
-      const uint32_t nm = r_fr + r_lt + (min(ex3[1] + r_eq, needT) - min(ex3[1], needT));
-      take = min(alo + nm, static_cast<uint32_t>(A)) - min(alo, static_cast<uint32_t>(A));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) take = max(take, __shfl_xor_sync(0xffffffffu, take, o));
-    if (lane == 0) S->ws[0][warp] = take;
-    __syncthreads();
-    uint32_t mx = 0;
-    for (int w = 0; w < kCoopWarps; ++w) mx = max(mx, S->ws[0][w]);
-    __syncthreads();
-    int rbase = static_cast<int>(a_lo), ntk = n_take;
-    const int32_t *tcache = take_cache;
-    if (mx > kSpreadMin && static_cast<unsigned long long>(mx) * G > 4ull * static_cast<uint32_t>(A)) {
-      if (!grid_barrier(glob, P.status, S)) return;
-      const int per = (A + G - 1) / G;
-      rbase = min(A, c * per);
-      ntk = min(A, rbase + per) - rbase;
-      tcache = nullptr;
-    }
-    used = take_rows(P, rbase, ntk, tcache, false, my_t0, my_f, my_h, my_src, buf, clock, copies, latent_rows);
+    // the owners' copies, or an even stripe per CTA (spread_takes decides)
+    used = spread_takes(P, S, glob, r_lt, r_eq, r_fr, needT, A, a_lo, n_take, take_cache, clock, copies, latent_rows);
+    if (used == ~0ull) return;
   }
   // misses beyond the pool's capacity stay out of it
   for (int r = A + gtid; r < static_cast<int>(M); r += gthreads) {
