@@ -61,7 +61,7 @@ constexpr int kQueueCap = 64;      // entries per epilogue -> prefetch queue
 // kPfTailMin tiles per group queues no candidate from its last kPfTailTiles tiles
 // (their host reads would land after the CTA's scoring ends and only lengthen the
 // kernel; the recall fetches such rows if they are selected)
-constexpr int kPfTailTiles = 2;
+constexpr int kPfTailTiles = 4;
 constexpr int kPfTailMin = 8;
 // host rows of the tiles (req_to_host slices, 128 x int32) staged by TMA for the
 // epilogue: a ring the producer may refill only after the epilogue read the tile
