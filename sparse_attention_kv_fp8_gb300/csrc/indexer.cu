@@ -60,8 +60,11 @@ constexpr int kQueueCap = 64;      // entries per epilogue -> prefetch queue
 // prefetching while scoring: each epilogue warpgroup of a CTA with at least
 // kPfTailMin tiles per group queues no candidate from its last kPfTailTiles tiles
 // (their host reads would land after the CTA's scoring ends and only lengthen the
-// kernel; the recall fetches such rows if they are selected)
+// kernel; the recall fetches such rows if they are selected).  Into the staging area
+// the last four tiles are cut; direct to slot only the last two, since a row placed
+// there spares the recall a whole copy, where a staged row still needs one.
 constexpr int kPfTailTiles = 4;
+constexpr int kPfTailTilesDirect = 2;
 constexpr int kPfTailMin = 8;
 // host rows of the tiles (req_to_host slices, 128 x int32) staged by TMA for the
 // epilogue: a ring the producer may refill only after the epilogue read the tile
@@ -331,6 +334,7 @@ __global__ void __launch_bounds__(Roles<NQ>::kThreads, 1)
     int b = ctl->first_b, t = ctl->first_t, cur_b = -1;
     for (int u = 0; u < grp; ++u) next_tile(P, b, t);
     const bool pf_cut = P.pf_while_scoring && n_tiles >= kPfTailMin * kEpiGroups;
+    const int pf_tail = (P.reserve != nullptr ? kPfTailTilesDirect : kPfTailTiles) * kEpiGroups;
     float shat[NQ];
     int valid[NQ];
     uint32_t hist_on = 0;  // bit j: query j's row has a selection histogram (window in hwin[e][j])
@@ -412,7 +416,7 @@ __global__ void __launch_bounds__(Roles<NQ>::kThreads, 1)
           }
         }
 
-      if (prefetch && !(pf_cut && i + kPfTailTiles * kEpiGroups >= n_tiles)) {
+      if (prefetch && !(pf_cut && i + pf_tail >= n_tiles)) {
         // threshold test only; the residency test, ticket and copy happen in the
         // prefetch warps so that no global load sits on this path
         bool pass = false;
