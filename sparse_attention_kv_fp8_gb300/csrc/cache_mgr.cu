@@ -929,9 +929,11 @@ __global__ void __launch_bounds__(kCoopThreads, 1) cache_op_kernel(const __grid_
   ECHO_TRACE_MARK(6);
 
   // ===== P4: evictions and allocations together.  Free slots and victims, in slot
-  // order, form the list of slots to take; the r-th of them takes miss r, and the CTA
-  // that owns the slot writes everything about it: the evicted row's map, the new
-  // row's maps, priority, indices-buffer entry, out_slot and KV bytes =====
+  // order, form the list of slots to take; the r-th of them takes miss r.  The CTA
+  // that owns a slot ranks it and clears the evicted row's map; the CTA that copies
+  // rank r (the slot's owner, or, when a few CTAs hold most of the slots to take, the
+  // CTA whose even stripe of the ranks holds r) writes the rest: the new row's maps,
+  // priority, indices-buffer entry, out_slot and KV bytes =====
   uint32_t pre_lt = 0, pre_eq = 0, pre_fr = 0, free_total = 0;
   uint32_t r_lt = 0, r_eq = 0, r_fr = 0;  // the counts of CTA r = threadIdx.x (when G <= the CTA's threads)
   uint32_t n_big = 0;  // CTAs whose candidate slots are more than kSpreadMin: only they can take that many
